@@ -1,0 +1,448 @@
+"""Benchmark of the paged decode step on GB300.
+
+Default workload: bf16 MHA decode step, 32 heads x head_dim 128, block 16,
+64 sequences with context lengths uniform on [1, 2048]; one step = kv_write of
+each sequence's new token + paged decode attention over its context.  The
+metric is KV bytes the attention must read (sum_s L_s * 2 * Hkv * D * 2) per
+second, with decode steps/s beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2..5]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU with
+no collective on the data path (sequences shard across GPUs with nothing to
+exchange); the time is the max over ranks and the value the sum.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import (WORKLOADS, make_beam_case, make_decode_case, poison_unused,  # noqa: E402
+                       write_step_schedule, beam_setup_schedule, beam_step_schedule)
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak), decode steps/sec"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of the tensor-core decode kernel from one ncu capture,
+# valid only while the kernel source hashes to `source_sha`.
+TRAFFIC = {"source_sha": None, "bytes_per_launch": {}}
+
+
+def launch_partition(w, max_blocks: int) -> int:
+    """Partition size (tokens) the benchmark launches a workload with: the
+    workload's own split if it names one, else 512-token partitions for
+    contexts longer than that (balances ragged lengths across SMs)."""
+    if w.partition_size:
+        return w.partition_size
+    return 512 if max_blocks * w.block_size > 512 else 0
+
+
+def kernel_sha() -> str:
+    p = os.path.join(ROOT, "paged_kv_cache_312_gb300", "csrc", "decode_tc.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+# workload set-up (host), shared by both arms
+# ---------------------------------------------------------------------------
+
+class Step:
+    """Host tensors of one decode step of a workload, plus its byte counts."""
+
+    def __init__(self, key: int, seed: int, allocator_cls):
+        w = WORKLOADS[key]
+        self.w = w
+        self.pairs = torch.zeros((0, 2), dtype=torch.int64)
+        self.slots = None
+        self.new_key = self.new_value = None
+        if key == 5:
+            case = make_beam_case(w, seed=seed)
+            mgr = allocator_cls(case.pool_blocks, w.block_size, free_order=case.pool_order)
+            pre, suf = beam_setup_schedule(mgr, case)
+            _, self.slots, self.pairs, self.tables, self.lens = beam_step_schedule(mgr, case)
+            NB, Hkv, B, D = case.pool_blocks, w.num_kv_heads, w.block_size, w.head_dim
+            self.k_cache = torch.full((NB, Hkv, B, D), float("nan"), dtype=w.torch_dtype)
+            self.v_cache = torch.full_like(self.k_cache, float("nan"))
+            self.setup_slots = torch.cat([pre.reshape(-1)] + suf)
+            self.setup_keys = torch.cat([case.prefix_k.reshape(-1, Hkv, D)] + case.suffix_k)
+            self.setup_vals = torch.cat([case.prefix_v.reshape(-1, Hkv, D)] + case.suffix_v)
+            self.q, self.new_key, self.new_value = case.q, case.new_key, case.new_value
+            self.unique_blocks = int(mgr.stats()[2])
+        else:
+            case = make_decode_case(w, seed=seed, poison=not w.writes_new_token)
+            self.k_cache, self.v_cache, self.q = case.k_cache, case.v_cache, case.q
+            self.setup_slots = None
+            if w.writes_new_token:
+                mgr = allocator_cls(case.num_blocks, w.block_size, free_order=case.pool_order)
+                self.slots, self.pairs, self.tables, self.lens = write_step_schedule(
+                    mgr, case.lengths)
+                poison_unused(self.k_cache, self.v_cache, self.tables, case.lengths - 1)
+                self.new_key, self.new_value = case.new_key, case.new_value
+            else:
+                self.tables, self.lens = case.block_tables, case.context_lens
+            self.unique_blocks = None
+        self.P = launch_partition(w, self.tables.shape[1])
+        L = self.lens.to(torch.int64)
+        b = w.torch_dtype.itemsize
+        self.kv_bytes = int(L.sum()) * 2 * w.num_kv_heads * w.head_dim * b
+        S = L.numel()
+        io = S * w.num_heads * w.head_dim * (b + 4) + int((L + w.block_size - 1).div(
+            w.block_size, rounding_mode="floor").sum()) * 4 + S * 4
+        self.attn_bytes = self.kv_bytes + io  # KV + q + fp32 out + table entries + lens
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled while the timed region runs
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, rank, world, local_rank):
+    import paged_kv_cache_312_gb300 as pkv
+    import __graft_entry__
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    st = Step(args.workload, args.seed, pkv.BlockAllocator)
+    w = st.w
+    kc, vc = st.k_cache.to(dev), st.v_cache.to(dev)
+    if st.setup_slots is not None:  # beam history
+        pkv.kv_write(kc, vc, st.setup_keys.to(dev), st.setup_vals.to(dev), st.setup_slots.to(dev))
+    q, bt, cl = st.q.to(dev), st.tables.to(dev), st.lens.to(dev)
+    S, Hq, D = q.shape
+    out = torch.empty((S, Hq, D), dtype=torch.float32, device=dev)
+    ws = None
+    if st.P:
+        ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, bt.shape[1] * w.block_size, st.P),
+                         dtype=torch.uint8, device=dev)
+    has_write = st.slots is not None
+    if has_write:
+        nk, nv, sl = st.new_key.to(dev), st.new_value.to(dev), st.slots.to(dev)
+    pairs = st.pairs.to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if pairs.shape[0]:
+            pkv.kv_copy_blocks(kc, vc, pairs, stream=stream)
+        if has_write:
+            pkv.kv_write(kc, vc, nk, nv, sl, stream=stream)
+        if ev is not None:
+            ev.record(stream)
+        pkv.paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, w.block_size, w.num_kv_heads,
+                                   partition_size=st.P, workspace=ws, stream=stream)
+
+    launches_per_step = (1 if pairs.shape[0] else 0) + (1 if has_write else 0) + \
+        (2 if st.P and bt.shape[1] * w.block_size > st.P else 1)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert pkv.device_status() == 0
+
+    # ---- device-timed region: K steps, events per step on the launch stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(mids[i])
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop() if clocks else None
+    total_ms = t0.elapsed_time(t1)
+    attn_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    assert pkv.device_status() == 0
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_q = st.q.pin_memory()
+        h_bt, h_cl = st.tables.pin_memory(), st.lens.pin_memory()
+        h_out = torch.empty((S, Hq, D), dtype=torch.float32).pin_memory()
+        h_in = [h_q, h_bt, h_cl]
+        if has_write:
+            h_nk, h_nv, h_sl = st.new_key.pin_memory(), st.new_value.pin_memory(), \
+                st.slots.pin_memory()
+            h_in += [h_nk, h_nv, h_sl]
+        h_pairs = st.pairs.pin_memory()
+        h_in.append(h_pairs)
+        h2d = sum(t.numel() * t.element_size() for t in h_in)
+        d2h = h_out.numel() * h_out.element_size()
+        k = max(1, min(args.steps, 50))
+        torch.cuda.synchronize(dev)
+        w0 = time.perf_counter()
+        for _ in range(k):
+            q.copy_(h_q, non_blocking=True)
+            bt.copy_(h_bt, non_blocking=True)
+            cl.copy_(h_cl, non_blocking=True)
+            if has_write:
+                nk.copy_(h_nk, non_blocking=True)
+                nv.copy_(h_nv, non_blocking=True)
+                sl.copy_(h_sl, non_blocking=True)
+            if pairs.shape[0]:
+                pairs.copy_(h_pairs, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+            stream.synchronize()
+        e2e_s = (time.perf_counter() - w0) / k
+        e2e = {"value": round(st.kv_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e2e_s * 1e3, 4), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": k}
+
+    peak, peak_src = measured_peaks()
+    attn_avg = statistics.mean(attn_ms)
+    achieved = st.attn_bytes / (attn_avg * 1e-3) / 1e9
+    value = st.kv_bytes * world / (ms_per_step * 1e-3) / 1e9
+    tr = TRAFFIC["bytes_per_launch"].get(str(args.workload)) \
+        if TRAFFIC["source_sha"] == kernel_sha() else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded N(0,1) values, shuffled block pool)",
+        "config": {"workload": w.name, "num_seqs": S, "num_heads": Hq,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": D, "block_size": w.block_size,
+                   "partition_size": st.P, "kv_bytes_per_step": st.kv_bytes,
+                   "step": ("cow-copy + " if pairs.shape[0] else "") +
+                   ("kv_write + " if has_write else "") + "paged_decode_attention",
+                   "l2": "inputs larger than L2 (KV %.2f GB vs 129 MB L2), no flush" %
+                   (st.kv_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "steps_per_s": round(1e3 / ms_per_step, 2),
+        "pct_hbm_peak": round(100 * value / world / peak, 2),
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (tensor-core partition "
+                     "kernel + log-sum-exp merge)" if st.P else
+                     "paged_decode_attention (tensor-core kernel)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": tr,
+                     "algorithmic_bytes_per_launch": st.attn_bytes,
+                     "avg_launch_ms": round(attn_avg, 5),
+                     "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src
+                     if peak_src == "measured" else "fallback 6.8 TB/s"},
+    }
+    if st.unique_blocks is not None:
+        ub = st.unique_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2 * 2
+        line["config"]["unique_kv_bytes"] = ub
+        line["pct_hbm_peak_unique_bytes"] = round(100 * ub / (attn_avg * 1e-3) / 1e9 / peak, 2)
+    return line, st
+
+
+def cpu_baseline(st, budget_s=8.0):
+    """Time the oracle (as it stands) on this host's cores on a bounded sample
+    of the same step: passes over the step's sequences (write + attention)
+    until the budget is used."""
+    import oracle
+    w = st.w
+    n = os.cpu_count() or 1
+    S = st.q.shape[0]
+    done_bytes, t_used, passes = 0, 0.0, 0
+    kc, vc = st.k_cache.clone(), st.v_cache.clone()
+    if st.setup_slots is not None:
+        oracle.kv_write(kc, vc, st.setup_keys, st.setup_vals, st.setup_slots, w.block_size)
+    chunk = max(1, min(S, 4 * n))
+    L = st.lens.to(torch.int64)
+    while t_used < budget_s and passes < 100:
+        for c0 in range(0, S, chunk):
+            idx = torch.arange(c0, min(S, c0 + chunk))
+            t = time.perf_counter()
+            if c0 == 0:
+                if st.pairs.shape[0]:
+                    oracle.kv_copy_blocks(kc, vc, st.pairs)
+                if st.slots is not None:
+                    oracle.kv_write(kc, vc, st.new_key, st.new_value, st.slots, w.block_size)
+            oracle.paged_decode_attention(st.q[idx], kc, vc, st.tables[idx], st.lens[idx],
+                                          w.scale, w.block_size, w.num_kv_heads, nthreads=n)
+            t_used += time.perf_counter() - t
+            done_bytes += int(L[idx].sum()) * 2 * w.num_kv_heads * w.head_dim * \
+                w.torch_dtype.itemsize
+            if t_used >= budget_s:
+                break
+        passes += 1
+    return {"value": round(done_bytes / t_used / 1e9, 4), "unit": "GB/s", "cores": n,
+            "kind": "oracle",
+            "sample": "%.2f GB of the step's KV (%d pass(es) over chunks of %d sequences, "
+                      "fp64 C oracle, %.1f s)" % (done_bytes / 1e9, passes, chunk, t_used)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=8.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        line = run_reference(args)
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("gloo")
+    line, st = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(st, args.cpu_budget)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores over K steps of a
+    bounded sample of the workload (the sample is a fixed subset of the step's
+    sequences chosen to keep each step to a few seconds)."""
+    import oracle
+    from oracle.blockmgr import BlockManager  # the oracle's own block manager builds the tables
+
+    st = Step(args.workload, args.seed, BlockManager)
+    w = st.w
+    n = os.cpu_count() or 1
+    kc, vc = st.k_cache.clone(), st.v_cache.clone()
+    if st.setup_slots is not None:
+        oracle.kv_write(kc, vc, st.setup_keys, st.setup_vals, st.setup_slots, w.block_size)
+    S = st.q.shape[0]
+    L = st.lens.to(torch.int64)
+    # bounded sample: time one full pass, keep a prefix of sequences ~2 s/step
+    t = time.perf_counter()
+    oracle.paged_decode_attention(st.q[:min(S, n)], kc, vc, st.tables[:min(S, n)],
+                                  st.lens[:min(S, n)], w.scale, w.block_size, w.num_kv_heads,
+                                  nthreads=n)
+    per_seq = (time.perf_counter() - t) / min(S, n)
+    m = int(max(1, min(S, 2.0 / max(per_seq, 1e-6))))
+    idx = torch.arange(m)
+    sample_bytes = int(L[idx].sum()) * 2 * w.num_kv_heads * w.head_dim * w.torch_dtype.itemsize
+
+    def step():
+        if st.pairs.shape[0]:
+            oracle.kv_copy_blocks(kc, vc, st.pairs)
+        if st.slots is not None:
+            oracle.kv_write(kc, vc, st.new_key, st.new_value, st.slots, w.block_size)
+        oracle.paged_decode_attention(st.q[idx], kc, vc, st.tables[idx], st.lens[idx], w.scale,
+                                      w.block_size, w.num_kv_heads, nthreads=n)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = sample_bytes / dt / 1e9
+    sample = "%d of %d sequences of the step (%.3f GB of KV per step), fp64 C oracle" % (
+        m, S, sample_bytes / 1e9)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "num_seqs": S, "num_heads": w.num_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                       "block_size": w.block_size},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,252 @@
+/*
+ * pkv.h -- C ABI of the GB300 paged KV-cache decode library (libpkv.so).
+ *
+ * The operations follow the method of "Efficient Memory Management for Large
+ * Language Model Serving with PagedAttention" (Kwon et al., 2023) as the
+ * following web pages describe it:
+ *   [AIPP]  aiplusplus.yigather.com, "PagedAttention: bringing OS virtual
+ *           memory to LLM inference"
+ *   [AUT]   auturnal.com, "paged-attention serving guide" (v1)
+ *   [CAY]   cayang0802.github.io, "Paged Attention" paper walkthrough
+ *   [LAIN]  lain42.top reading journal on the paper
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every call returns an int status: PKV_OK (0) or a negative PKV_ERR_*.
+ *   pkv_last_error_string() describes the most recent failure of the calling
+ *   thread.  Argument errors are detected on the host before anything is
+ *   launched; nothing is then written.
+ * - Device calls take device pointers the CALLER owns (allocated by PyTorch or
+ *   cudaMalloc).  The library never allocates or frees device memory.  Host
+ *   allocator calls work on host memory only.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Device calls only enqueue work: they return once launched, and the output
+ *   is ready when the stream reaches that point.
+ * - Kernels check every block id, slot and context length they read against
+ *   the sizes passed in.  A bad value is skipped (never dereferenced) and sets
+ *   a bit in the device status word; pkv_device_status() reads it.
+ * - dtype codes: PKV_F32, PKV_F16, PKV_BF16.  q, K and V share one dtype.
+ *
+ * KV cache layout (the pages fix only that a block stores the K and V of B
+ * consecutive tokens [AIPP core idea 1]; this layout is this library's
+ * choice, made so one (block, head) tile is B*D contiguous elements):
+ *     k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
+ *     token i of a sequence lives in its logical block i / block_size, at
+ *     offset i % block_size; block_tables[s][j] is the physical block of
+ *     logical block j of sequence s [AIPP core idea 3].
+ *     Both caches must start on a 16-byte boundary (tensor-memory-access
+ *     tile loads); PKV_ERR_ALIGN otherwise.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define PKV_OK 0
+#define PKV_ERR_NULL -1        /* a required pointer is NULL                  */
+#define PKV_ERR_SHAPE -2       /* sizes out of range or inconsistent          */
+#define PKV_ERR_DTYPE -3       /* unknown dtype code                          */
+#define PKV_ERR_UNSUPPORTED -4 /* valid request this build does not implement */
+#define PKV_ERR_CUDA -5        /* a CUDA runtime/driver call failed           */
+#define PKV_ERR_BOUNDS -6      /* a kernel saw an out-of-range id (status)    */
+#define PKV_ERR_OOM -7         /* allocator: not enough free blocks           */
+#define PKV_ERR_WORKSPACE -8   /* workspace missing or too small              */
+#define PKV_ERR_STATE -9       /* allocator: unknown / duplicate sequence     */
+#define PKV_ERR_ALIGN -10      /* a pointer is not aligned as required        */
+
+/* ---- dtypes -------------------------------------------------------------- */
+#define PKV_F32 0
+#define PKV_F16 1
+#define PKV_BF16 2
+
+/* ---- device status word bits (set by kernels, read by pkv_device_status) -- */
+#define PKV_STATUS_BAD_BLOCK 1u  /* block-table entry outside [0, num_blocks)   */
+#define PKV_STATUS_BAD_LEN 2u    /* context_len < 0 or > max_blocks*block_size  */
+#define PKV_STATUS_BAD_SLOT 4u   /* slot >= num_blocks*block_size               */
+#define PKV_STATUS_BAD_PAIR 8u   /* copy pair id outside [0, num_blocks)        */
+#define PKV_STATUS_TIMEOUT 16u   /* a tile load did not arrive within ~1 s; the
+                                    kernel stopped early (output invalid)       */
+
+/* Text of the calling thread's most recent error ("" if none).  The pointer
+ * stays valid until that thread's next failing call. */
+const char* pkv_last_error_string(void);
+
+/* Library ABI version (major * 100 + minor). */
+int pkv_version(void);
+
+/*
+ * Reads (and, if reset != 0, clears) the device status word after waiting
+ * for `stream`.  *bits receives the OR of PKV_STATUS_* seen since the last
+ * reset on the current device.  Returns PKV_ERR_BOUNDS if any bit was set,
+ * else PKV_OK.  This call synchronises the stream.
+ */
+int pkv_device_status(void* stream, uint32_t* bits, int reset);
+
+/*
+ * kv_write -- store each new token's K and V in its cache slot.
+ * [CAY, KV-cache paragraph]: only the new token's key and value are computed
+ * each step, the earlier ones are kept; [AIPP core idea 4 / LAIN on-demand
+ * allocation]: the slot comes from a block allocated when the sequence grows.
+ *
+ * key, value   : [num_tokens][num_kv_heads][head_dim], dtype `dtype`.
+ * slot_mapping : int64 [num_tokens]; slot = physical_block*block_size+offset.
+ *                slot < 0 marks padding: that token is skipped.
+ *                slot >= num_blocks*block_size is skipped and sets
+ *                PKV_STATUS_BAD_SLOT.
+ * k_cache, v_cache : cache arrays as laid out above; written in place.
+ * Two tokens with the same slot race (either value may land).  Bit-exact copy.
+ */
+int pkv_kv_write(void* k_cache, void* v_cache, const void* key, const void* value,
+                 const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                 int num_kv_heads, int head_dim, int block_size, int dtype, void* stream);
+
+/*
+ * paged_decode_attention -- one query token per sequence attends to that
+ * sequence's cached tokens, which sit in fixed-size physical blocks reached
+ * through the block table.  [AIPP key techniques 1]: the kernel follows the
+ * block table to assemble scattered K/V blocks; [LAIN method]: table lookup,
+ * block fetch and attention are fused in one kernel; [AUT section 1]: paging
+ * changes storage, not what attention reads, so
+ *     out[s,h,:] = sum_i softmax_i(scale * q[s,h,:] . K_s[i,g,:]) V_s[i,g,:]
+ * over i < context_lens[s], with KV head g = h / (num_heads / num_kv_heads)
+ * (grouped-query attention, [AUT section 1]: GQA/MQA change the KV head count).
+ *
+ * out          : [num_seqs][num_heads][head_dim], dtype out_dtype (written).
+ * q            : [num_seqs][num_heads][head_dim], dtype kv_dtype.
+ * block_tables : int32 [num_seqs][max_blocks_per_seq]; only the first
+ *                ceil(context_lens[s]/block_size) entries of row s are read.
+ * context_lens : int32 [num_seqs], tokens attended (the token written this
+ *                step included).  0 gives an all-zero output row.
+ * scale        : softmax scale (usually 1/sqrt(head_dim)).
+ * partition_size : 0 = each (sequence, KV head) is handled in one pass.
+ *                > 0 = split-context decode: each sequence's tokens are cut
+ *                into partitions of this many tokens (a multiple of
+ *                block_size); each partition writes its max, sum and
+ *                unnormalised output to `workspace`, and a second kernel
+ *                merges them by log-sum-exp.  (The pages are silent on
+ *                splitting; the merge is exact in real arithmetic.)
+ * workspace    : device scratch of at least pkv_decode_workspace_bytes(...)
+ *                bytes, 256-byte aligned, when partition_size > 0 (else may be
+ *                NULL).  Contents on entry are ignored; calls that share a
+ *                workspace must not overlap on the GPU.
+ * Supported: block_size in {8,16,32}; head_dim in {64,128}; num_heads a
+ * multiple of num_kv_heads; out_dtype any of the three.  16-bit KV with
+ * num_heads/num_kv_heads <= 8 runs on the tensor-core kernel, the rest on a
+ * CUDA-core kernel; both accumulate in fp32.
+ */
+int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               const int32_t* context_lens, float scale, int block_size,
+                               int num_kv_heads, int num_seqs, int num_heads, int head_dim,
+                               int max_blocks_per_seq, int num_blocks, int kv_dtype,
+                               int out_dtype, int partition_size, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* Workspace bytes pkv_paged_decode_attention needs for these sizes, where
+ * max_context_len = max_blocks_per_seq * block_size.  0 if partition_size==0. */
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                  int max_context_len, int partition_size);
+
+/*
+ * kv_copy_blocks -- copy-on-write copy of whole physical blocks.
+ * [AUT section 3]: when a branch must modify a shared block that is not yet
+ * full, copy-on-write keeps branches from overwriting each other; [AIPP key
+ * techniques 3]: several block tables point at one physical block and a copy
+ * is made only on write.
+ *
+ * pairs : int64 [num_pairs][2] device array of (src, dst) physical block ids.
+ *         For every KV head, all block_size slots of K and V are copied.
+ *         Destinations must be distinct and must not appear as a source in
+ *         the same call (the copies run in parallel); an id outside
+ *         [0, num_blocks) skips that pair and sets PKV_STATUS_BAD_PAIR.
+ * Bit-exact copy.
+ */
+int pkv_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
+                       int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                       int dtype, void* stream);
+
+/*
+ * Kernel selection for pkv_paged_decode_attention (process-wide):
+ * PKV_KERNEL_AUTO (default) picks the tensor-core kernel where supported;
+ * PKV_KERNEL_CUDA_CORE forces the CUDA-core kernel for every shape (used to
+ * test both).  Returns PKV_ERR_SHAPE for an unknown value.
+ */
+#define PKV_KERNEL_AUTO 0
+#define PKV_KERNEL_CUDA_CORE 1
+int pkv_set_decode_kernel(int which);
+
+/* ==========================================================================
+ * Host block allocator (host memory only; not thread-safe per handle).
+ * [AIPP core idea 1-4, effects]: fixed-size blocks, a block table per
+ * sequence, blocks allocated on demand and any free block serves;
+ * [AIPP continuous batching]: a finished sequence frees its blocks at once;
+ * [AUT section 3]: shared blocks carry a reference count that must match the
+ * lifetime of the sequences using them, and a write into a shared block that
+ * is not full copies it first; [AUT section 6]: OOM must be handled.
+ *
+ * Free list: a stack.  Blocks are first handed out in `free_order`
+ * (identity if NULL); a block whose count drops to zero is pushed on top and
+ * is handed out next.  A sequence releases its blocks last to first.
+ * Any call that fails leaves the allocator unchanged.
+ * ========================================================================== */
+typedef struct pkv_allocator pkv_allocator;
+
+/* free_order: NULL or a permutation of [0, num_blocks). */
+int pkv_alloc_create(int num_blocks, int block_size, const int32_t* free_order,
+                     pkv_allocator** out);
+int pkv_alloc_destroy(pkv_allocator* a);
+
+/* New sequence holding prompt_len tokens: takes ceil(prompt_len/B) blocks.
+ * PKV_ERR_STATE if seq exists; PKV_ERR_OOM if too few free blocks. */
+int pkv_seq_add(pkv_allocator* a, int64_t seq, int prompt_len);
+
+/* Reserves the slot of the sequence's next token.  A fresh block is taken if
+ * the token starts a block; if the last block is shared (count > 1) and not
+ * full, a private copy target is taken instead: *cow_src/*cow_dst receive the
+ * pair to pass to pkv_kv_copy_blocks before the write (else both are -1). */
+int pkv_seq_append(pkv_allocator* a, int64_t seq, int64_t* slot, int64_t* cow_src,
+                   int64_t* cow_dst);
+
+/* One decode step: pkv_seq_append on each of seqs[0..n) in order, all or
+ * nothing.  slots: [n]; cow_pairs: [n][2] capacity; *num_pairs = pairs made. */
+int pkv_step_append(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots,
+                    int64_t* cow_pairs, int* num_pairs);
+
+/* child shares every block of parent (each count + 1).  PKV_ERR_STATE if the
+ * parent is unknown or the child exists. */
+int pkv_seq_fork(pkv_allocator* a, int64_t parent, int64_t child);
+
+/* Drops the sequence; blocks whose count reaches zero return to the pool. */
+int pkv_seq_free(pkv_allocator* a, int64_t seq);
+
+int pkv_seq_len(pkv_allocator* a, int64_t seq, int* len);
+
+/* Copies the sequence's table into out[0..cap); *n = its length (may be > cap,
+ * in which case only cap entries are written and PKV_ERR_SHAPE is returned). */
+int pkv_block_table(pkv_allocator* a, int64_t seq, int32_t* out, int cap, int* n);
+
+/* Dense tables for a batch: tables [n][max_blocks] (unused entries -1) and
+ * lens [n].  PKV_ERR_SHAPE if a table is longer than max_blocks. */
+int pkv_block_tables_dense(pkv_allocator* a, const int64_t* seqs, int n, int max_blocks,
+                           int32_t* tables, int32_t* lens);
+
+int pkv_refcount(pkv_allocator* a, int block, int* count);
+int pkv_num_free_blocks(pkv_allocator* a, int* n);
+
+/* Eq. (2)-(3) of [AUT]: allocated positions = sum over sequences of
+ * B * blocks held, valid positions = sum of lengths (position utilisation
+ * U = valid / allocated); blocks_in_use counts physical blocks once. */
+int pkv_stats(pkv_allocator* a, int64_t* allocated_positions, int64_t* valid_positions,
+              int64_t* blocks_in_use);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

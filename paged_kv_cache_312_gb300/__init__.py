@@ -1,0 +1,15 @@
+"""GB300-native paged KV-cache decode path (PagedAttention).
+
+The work happens in libpkv.so (CUDA kernels for sm_103a behind the C ABI of
+include/pkv.h); this package is the thin Python binding over it.
+"""
+from ._binding import (  # noqa: F401
+    KERNEL_AUTO, KERNEL_CUDA_CORE, PKV_BF16, PKV_F16, PKV_F32, STATUS_BITS, BlockAllocator,
+    OutOfBlocks, PkvError, decode_workspace_bytes, device_status, kv_copy_blocks, kv_write, lib,
+    paged_decode_attention, set_decode_kernel,
+)
+
+__all__ = [
+    "BlockAllocator", "OutOfBlocks", "PkvError", "decode_workspace_bytes", "device_status",
+    "kv_copy_blocks", "kv_write", "lib", "paged_decode_attention", "set_decode_kernel",
+]

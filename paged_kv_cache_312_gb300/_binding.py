@@ -1,0 +1,279 @@
+"""ctypes binding of libpkv.so: argument marshalling only.
+
+Every function here takes torch tensors, checks that shapes and dtypes agree,
+and passes raw pointers, sizes and the current CUDA stream to the C ABI
+declared in include/pkv.h.  All arithmetic runs in the library's kernels; there
+is no fallback: if the library is missing or a call fails, a RuntimeError is
+raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
+
+PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
+DTYPE_CODE = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+KERNEL_AUTO, KERNEL_CUDA_CORE = 0, 1
+STATUS_BITS = {1: "bad block id", 2: "bad context length", 4: "bad slot", 8: "bad copy pair",
+               16: "tile load timeout"}
+
+# name -> (restype, argtypes)
+_P, _I, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "pkv_last_error_string": (ctypes.c_char_p, []),
+    "pkv_version": (_I, []),
+    "pkv_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint32), _I]),
+    "pkv_kv_write": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pkv_paged_decode_attention": (_I, [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I,
+                                        _I, _I, _I, _P, _SZ, _P]),
+    "pkv_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_kv_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pkv_set_decode_kernel": (_I, [_I]),
+    "pkv_alloc_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
+    "pkv_alloc_destroy": (_I, [_P]),
+    "pkv_seq_add": (_I, [_P, _I64, _I]),
+    "pkv_seq_append": (_I, [_P, _I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
+                            ctypes.POINTER(_I64)]),
+    "pkv_step_append": (_I, [_P, _P, _I, _P, _P, ctypes.POINTER(_I)]),
+    "pkv_seq_fork": (_I, [_P, _I64, _I64]),
+    "pkv_seq_free": (_I, [_P, _I64]),
+    "pkv_seq_len": (_I, [_P, _I64, ctypes.POINTER(_I)]),
+    "pkv_block_table": (_I, [_P, _I64, _P, _I, ctypes.POINTER(_I)]),
+    "pkv_block_tables_dense": (_I, [_P, _P, _I, _I, _P, _P]),
+    "pkv_refcount": (_I, [_P, _I, ctypes.POINTER(_I)]),
+    "pkv_num_free_blocks": (_I, [_P, ctypes.POINTER(_I)]),
+    "pkv_stats": (_I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded libpkv.so (RuntimeError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "libpkv.so is not built (expected %s); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(handle, name)
+            f.restype, f.argtypes = res, args
+        _lib = handle
+    return _lib
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code, where):
+        msg = lib().pkv_last_error_string().decode(errors="replace")
+        super().__init__("%s failed (status %d): %s" % (where, code, msg))
+        self.code = code
+
+
+class OutOfBlocks(PkvError):
+    pass
+
+
+def _check(rc, where):
+    if rc != 0:
+        if rc == -7:
+            raise OutOfBlocks(rc, where)
+        raise PkvError(rc, where)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ---------------------------------------------------------------------------
+# device calls
+# ---------------------------------------------------------------------------
+
+def kv_write(k_cache, v_cache, key, value, slot_mapping, stream=None):
+    """Store key/value [T, Hkv, D] into the caches [NB, Hkv, B, D] at
+    slot_mapping (int64 [T], -1 = skip)."""
+    NB, Hkv, B, D = k_cache.shape
+    T = key.shape[0]
+    if v_cache.shape != k_cache.shape or key.shape != (T, Hkv, D) or value.shape != key.shape:
+        raise ValueError("kv_write: shape mismatch")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T:
+        raise ValueError("kv_write: slot_mapping must be int64 [T]")
+    if len({k_cache.dtype, v_cache.dtype, key.dtype, value.dtype}) != 1:
+        raise ValueError("kv_write: dtypes differ")
+    rc = lib().pkv_kv_write(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _dev(key, "key"),
+                            _dev(value, "value"), _dev(slot_mapping, "slot_mapping"), T, NB, Hkv,
+                            D, B, DTYPE_CODE[k_cache.dtype], _stream(stream))
+    _check(rc, "pkv_kv_write")
+
+
+def decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_size):
+    return int(lib().pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len,
+                                                partition_size))
+
+
+def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           block_size, num_kv_heads, partition_size=0, workspace=None,
+                           stream=None):
+    """out [S, Hq, D] = paged decode attention of q [S, Hq, D] over the caches."""
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = k_cache.shape
+    if (Hkv, B, Dk) != (num_kv_heads, block_size, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("paged_decode_attention: cache shape mismatch")
+    if out.shape != q.shape:
+        raise ValueError("paged_decode_attention: out must be [S, Hq, D]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks], context_lens [S]")
+    if q.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise ValueError("q, k_cache, v_cache must share a dtype")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    rc = lib().pkv_paged_decode_attention(
+        _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables"), _dev(context_lens, "context_lens"), float(scale),
+        int(block_size), int(num_kv_heads), S, Hq, D, block_tables.shape[1], NB,
+        DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], int(partition_size), ws_ptr, ws_bytes,
+        _stream(stream))
+    _check(rc, "pkv_paged_decode_attention")
+
+
+def kv_copy_blocks(k_cache, v_cache, pairs, stream=None):
+    """Copy whole physical blocks: pairs is int64 [P, 2] of (src, dst)."""
+    NB, Hkv, B, D = k_cache.shape
+    if pairs.dtype != torch.int64 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int64 [P, 2]")
+    rc = lib().pkv_kv_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                  _dev(pairs, "pairs") if pairs.numel() else ctypes.c_void_p(0),
+                                  pairs.shape[0], NB, Hkv, D, B, DTYPE_CODE[k_cache.dtype],
+                                  _stream(stream))
+    _check(rc, "pkv_kv_copy_blocks")
+
+
+def device_status(reset=True, stream=None):
+    """OR of the status bits kernels raised since the last reset (syncs)."""
+    bits = ctypes.c_uint32(0)
+    rc = lib().pkv_device_status(_stream(stream), ctypes.byref(bits), 1 if reset else 0)
+    if rc not in (0, -6):
+        _check(rc, "pkv_device_status")
+    return int(bits.value)
+
+
+def set_decode_kernel(which):
+    _check(lib().pkv_set_decode_kernel(int(which)), "pkv_set_decode_kernel")
+
+
+# ---------------------------------------------------------------------------
+# host block allocator
+# ---------------------------------------------------------------------------
+
+class BlockAllocator:
+    """Host-side block manager (refcounts, copy-on-write, slot mapping)."""
+
+    def __init__(self, num_blocks, block_size, free_order=None):
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        self._order = None
+        ptr = ctypes.c_void_p(0)
+        if free_order is not None:
+            self._order = torch.as_tensor(free_order, dtype=torch.int32).contiguous()
+            if self._order.numel() != self.num_blocks:
+                raise ValueError("free_order must hold num_blocks ids")
+            ptr = ctypes.c_void_p(self._order.data_ptr())
+        h = ctypes.c_void_p(0)
+        _check(lib().pkv_alloc_create(self.num_blocks, self.block_size, ptr, ctypes.byref(h)),
+               "pkv_alloc_create")
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.pkv_alloc_destroy(h)
+            self._h = None
+
+    def add(self, seq, prompt_len):
+        _check(lib().pkv_seq_add(self._h, int(seq), int(prompt_len)), "pkv_seq_add")
+
+    def append(self, seq):
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().pkv_seq_append(self._h, int(seq), ctypes.byref(slot), ctypes.byref(src),
+                                    ctypes.byref(dst)), "pkv_seq_append")
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def step_append(self, seqs):
+        """Returns (slots int64 [n], cow_pairs int64 [P, 2]) as host tensors."""
+        s = torch.as_tensor(list(seqs), dtype=torch.int64).contiguous()
+        n = s.numel()
+        slots = torch.empty(n, dtype=torch.int64)
+        pairs = torch.empty((max(n, 1), 2), dtype=torch.int64)
+        npairs = ctypes.c_int(0)
+        _check(lib().pkv_step_append(self._h, ctypes.c_void_p(s.data_ptr()), n,
+                                     ctypes.c_void_p(slots.data_ptr()),
+                                     ctypes.c_void_p(pairs.data_ptr()), ctypes.byref(npairs)),
+               "pkv_step_append")
+        return slots, pairs[:npairs.value].clone()
+
+    def fork(self, parent, child):
+        _check(lib().pkv_seq_fork(self._h, int(parent), int(child)), "pkv_seq_fork")
+
+    def free(self, seq):
+        _check(lib().pkv_seq_free(self._h, int(seq)), "pkv_seq_free")
+
+    free_seq = free
+
+    def length(self, seq):
+        n = ctypes.c_int()
+        _check(lib().pkv_seq_len(self._h, int(seq), ctypes.byref(n)), "pkv_seq_len")
+        return n.value
+
+    def table(self, seq):
+        n = ctypes.c_int()
+        rc = lib().pkv_block_table(self._h, int(seq), ctypes.c_void_p(0), 0, ctypes.byref(n))
+        if rc not in (0, -2):
+            _check(rc, "pkv_block_table")
+        buf = torch.empty(max(n.value, 1), dtype=torch.int32)
+        _check(lib().pkv_block_table(self._h, int(seq), ctypes.c_void_p(buf.data_ptr()), n.value,
+                                     ctypes.byref(n)), "pkv_block_table")
+        return buf[:n.value].tolist()
+
+    def dense_tables(self, seqs, max_blocks):
+        s = torch.as_tensor(list(seqs), dtype=torch.int64).contiguous()
+        tables = torch.empty((s.numel(), max_blocks), dtype=torch.int32)
+        lens = torch.empty(s.numel(), dtype=torch.int32)
+        _check(lib().pkv_block_tables_dense(self._h, ctypes.c_void_p(s.data_ptr()), s.numel(),
+                                            int(max_blocks), ctypes.c_void_p(tables.data_ptr()),
+                                            ctypes.c_void_p(lens.data_ptr())),
+               "pkv_block_tables_dense")
+        return tables, lens
+
+    def refcount(self, block):
+        c = ctypes.c_int()
+        _check(lib().pkv_refcount(self._h, int(block), ctypes.byref(c)), "pkv_refcount")
+        return c.value
+
+    def num_free(self):
+        c = ctypes.c_int()
+        _check(lib().pkv_num_free_blocks(self._h, ctypes.byref(c)), "pkv_num_free_blocks")
+        return c.value
+
+    def stats(self):
+        a, v, u = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().pkv_stats(self._h, ctypes.byref(a), ctypes.byref(v), ctypes.byref(u)),
+               "pkv_stats")
+        return a.value, v.value, u.value

@@ -1,0 +1,299 @@
+// Host block allocator for the paged KV cache (C ABI in include/pkv.h).
+//
+// What it keeps, following the PagedAttention pages:
+//  - a pool of fixed-size physical blocks and, per sequence, a block table
+//    mapping logical block i to a physical block (aiplusplus page, "core
+//    idea" 1-3);
+//  - on-demand allocation: blocks for the prompt on arrival, one more when a
+//    new token starts a block; any free block serves (same page, "core idea"
+//    4 and "effects"); a finished sequence returns its blocks at once
+//    ("continuous batching");
+//  - reference counts for blocks shared between tables (prefix sharing, beam
+//    search) and a copy-on-write decision when a sequence writes into a
+//    shared block that is not full (auturnal guide, section 3; cayang0802
+//    walkthrough, beam search of width 4).
+// Every operation either completes or leaves the state untouched (OOM and
+// bad arguments included), as the auturnal guide's section 6 asks of OOM.
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+struct pkv_allocator {
+    int num_blocks = 0;
+    int block_size = 0;
+    std::vector<int32_t> free_stack;  // back() is handed out next
+    std::vector<int32_t> ref;         // reference count per physical block
+    struct Seq {
+        std::vector<int32_t> table;
+        int64_t len = 0;
+    };
+    std::unordered_map<int64_t, Seq> seqs;
+
+    int32_t pop()
+    {
+        int32_t b = free_stack.back();
+        free_stack.pop_back();
+        ref[b] = 1;
+        return b;
+    }
+    void release(int32_t b)
+    {
+        if (--ref[b] == 0) free_stack.push_back(b);
+    }
+    void append_one(Seq& s, int64_t* slot, int64_t* src, int64_t* dst)
+    {
+        *src = *dst = -1;
+        int64_t p = s.len;
+        if (p % block_size == 0) {
+            s.table.push_back(pop());
+        } else {
+            int32_t last = s.table.back();
+            if (ref[last] > 1) {
+                int32_t fresh = pop();
+                release(last);
+                s.table.back() = fresh;
+                *src = last;
+                *dst = fresh;
+            }
+        }
+        *slot = (int64_t)s.table[p / block_size] * block_size + p % block_size;
+        s.len = p + 1;
+    }
+};
+
+extern "C" {
+
+int pkv_alloc_create(int num_blocks, int block_size, const int32_t* free_order,
+                     pkv_allocator** out)
+{
+    if (!out) return pkv_fail(PKV_ERR_NULL, "pkv_alloc_create: out is NULL");
+    *out = nullptr;
+    if (num_blocks < 0 || block_size <= 0)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_alloc_create: num_blocks=%d block_size=%d",
+                        num_blocks, block_size);
+    pkv_allocator* a = new (std::nothrow) pkv_allocator();
+    if (!a) return pkv_fail(PKV_ERR_OOM, "pkv_alloc_create: host allocation failed");
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    a->ref.assign(num_blocks, 0);
+    a->free_stack.resize(num_blocks);
+    std::vector<char> seen(num_blocks, 0);
+    for (int i = 0; i < num_blocks; ++i) {
+        int32_t b = free_order ? free_order[i] : i;
+        if (b < 0 || b >= num_blocks || seen[b]) {
+            delete a;
+            return pkv_fail(PKV_ERR_SHAPE, "pkv_alloc_create: free_order is not a permutation");
+        }
+        seen[b] = 1;
+        a->free_stack[num_blocks - 1 - i] = b;  // first of free_order on top
+    }
+    *out = a;
+    return PKV_OK;
+}
+
+int pkv_alloc_destroy(pkv_allocator* a)
+{
+    delete a;
+    return PKV_OK;
+}
+
+int pkv_seq_add(pkv_allocator* a, int64_t seq, int prompt_len)
+{
+    if (!a) return pkv_fail(PKV_ERR_NULL, "pkv_seq_add: allocator is NULL");
+    if (prompt_len < 0) return pkv_fail(PKV_ERR_SHAPE, "pkv_seq_add: negative prompt_len");
+    if (a->seqs.count(seq)) return pkv_fail(PKV_ERR_STATE, "pkv_seq_add: sequence exists");
+    int64_t n = (prompt_len + (int64_t)a->block_size - 1) / a->block_size;
+    if (n > (int64_t)a->free_stack.size())
+        return pkv_fail(PKV_ERR_OOM, "pkv_seq_add: %lld blocks needed, %zu free",
+                        (long long)n, a->free_stack.size());
+    pkv_allocator::Seq s;
+    s.table.reserve(n);
+    for (int64_t i = 0; i < n; ++i) s.table.push_back(a->pop());
+    s.len = prompt_len;
+    a->seqs.emplace(seq, std::move(s));
+    return PKV_OK;
+}
+
+int pkv_seq_append(pkv_allocator* a, int64_t seq, int64_t* slot, int64_t* cow_src,
+                   int64_t* cow_dst)
+{
+    if (!a || !slot || !cow_src || !cow_dst)
+        return pkv_fail(PKV_ERR_NULL, "pkv_seq_append: NULL argument");
+    auto it = a->seqs.find(seq);
+    if (it == a->seqs.end()) return pkv_fail(PKV_ERR_STATE, "pkv_seq_append: unknown sequence");
+    const pkv_allocator::Seq& s = it->second;
+    bool need = s.len % a->block_size == 0 || a->ref[s.table.back()] > 1;
+    if (need && a->free_stack.empty())
+        return pkv_fail(PKV_ERR_OOM, "pkv_seq_append: no free block");
+    a->append_one(it->second, slot, cow_src, cow_dst);
+    return PKV_OK;
+}
+
+int pkv_step_append(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots,
+                    int64_t* cow_pairs, int* num_pairs)
+{
+    if (!a || (n > 0 && (!seqs || !slots || !cow_pairs)) || !num_pairs)
+        return pkv_fail(PKV_ERR_NULL, "pkv_step_append: NULL argument");
+    if (n < 0) return pkv_fail(PKV_ERR_SHAPE, "pkv_step_append: n < 0");
+    // Plan first (all or nothing): walk the batch tracking the count changes
+    // earlier appends would make, so that a block shared by two sequences of
+    // the same step is copied once and the last holder writes in place.
+    std::vector<pkv_allocator::Seq*> ptr(n);
+    std::unordered_map<int32_t, int> dref;
+    int64_t need = 0;
+    for (int i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seqs[i]);
+        if (it == a->seqs.end())
+            return pkv_fail(PKV_ERR_STATE, "pkv_step_append: unknown sequence %lld",
+                            (long long)seqs[i]);
+        ptr[i] = &it->second;
+    }
+    {
+        // Simulate on copies of the touched tables.  A table entry of -1
+        // stands for a block taken in this step (private to its sequence).
+        std::unordered_map<int64_t, pkv_allocator::Seq> sim;
+        for (int i = 0; i < n; ++i) {
+            auto f = sim.find(seqs[i]);
+            if (f == sim.end()) f = sim.emplace(seqs[i], *ptr[i]).first;
+            pkv_allocator::Seq& s = f->second;
+            if (s.len % a->block_size == 0) {
+                s.table.push_back(-1);
+                need += 1;
+            } else {
+                int32_t last = s.table.back();
+                if (last >= 0 && a->ref[last] + dref[last] > 1) {
+                    dref[last] -= 1;
+                    s.table.back() = -1;
+                    need += 1;
+                }
+            }
+            s.len += 1;
+        }
+    }
+    if (need > (int64_t)a->free_stack.size())
+        return pkv_fail(PKV_ERR_OOM, "pkv_step_append: %lld blocks needed, %zu free",
+                        (long long)need, a->free_stack.size());
+    int np = 0;
+    for (int i = 0; i < n; ++i) {
+        int64_t src, dst;
+        a->append_one(*ptr[i], &slots[i], &src, &dst);
+        if (src >= 0) {
+            cow_pairs[2 * np] = src;
+            cow_pairs[2 * np + 1] = dst;
+            ++np;
+        }
+    }
+    *num_pairs = np;
+    return PKV_OK;
+}
+
+int pkv_seq_fork(pkv_allocator* a, int64_t parent, int64_t child)
+{
+    if (!a) return pkv_fail(PKV_ERR_NULL, "pkv_seq_fork: allocator is NULL");
+    auto it = a->seqs.find(parent);
+    if (it == a->seqs.end()) return pkv_fail(PKV_ERR_STATE, "pkv_seq_fork: unknown parent");
+    if (a->seqs.count(child)) return pkv_fail(PKV_ERR_STATE, "pkv_seq_fork: child exists");
+    pkv_allocator::Seq s = it->second;
+    for (int32_t b : s.table) a->ref[b] += 1;
+    a->seqs.emplace(child, std::move(s));
+    return PKV_OK;
+}
+
+int pkv_seq_free(pkv_allocator* a, int64_t seq)
+{
+    if (!a) return pkv_fail(PKV_ERR_NULL, "pkv_seq_free: allocator is NULL");
+    auto it = a->seqs.find(seq);
+    if (it == a->seqs.end()) return pkv_fail(PKV_ERR_STATE, "pkv_seq_free: unknown sequence");
+    const std::vector<int32_t>& t = it->second.table;
+    for (size_t i = t.size(); i-- > 0;) a->release(t[i]);
+    a->seqs.erase(it);
+    return PKV_OK;
+}
+
+int pkv_seq_len(pkv_allocator* a, int64_t seq, int* len)
+{
+    if (!a || !len) return pkv_fail(PKV_ERR_NULL, "pkv_seq_len: NULL argument");
+    auto it = a->seqs.find(seq);
+    if (it == a->seqs.end()) return pkv_fail(PKV_ERR_STATE, "pkv_seq_len: unknown sequence");
+    *len = (int)it->second.len;
+    return PKV_OK;
+}
+
+int pkv_block_table(pkv_allocator* a, int64_t seq, int32_t* out, int cap, int* n)
+{
+    if (!a || !n || (cap > 0 && !out)) return pkv_fail(PKV_ERR_NULL, "pkv_block_table: NULL");
+    auto it = a->seqs.find(seq);
+    if (it == a->seqs.end()) return pkv_fail(PKV_ERR_STATE, "pkv_block_table: unknown sequence");
+    const std::vector<int32_t>& t = it->second.table;
+    *n = (int)t.size();
+    int m = cap < (int)t.size() ? cap : (int)t.size();
+    if (m > 0) std::memcpy(out, t.data(), sizeof(int32_t) * m);
+    if ((int)t.size() > cap)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_block_table: table has %zu entries, cap %d",
+                        t.size(), cap);
+    return PKV_OK;
+}
+
+int pkv_block_tables_dense(pkv_allocator* a, const int64_t* seqs, int n, int max_blocks,
+                           int32_t* tables, int32_t* lens)
+{
+    if (!a || (n > 0 && (!seqs || !tables || !lens)))
+        return pkv_fail(PKV_ERR_NULL, "pkv_block_tables_dense: NULL argument");
+    if (n < 0 || max_blocks < 0) return pkv_fail(PKV_ERR_SHAPE, "pkv_block_tables_dense: sizes");
+    for (int i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seqs[i]);
+        if (it == a->seqs.end())
+            return pkv_fail(PKV_ERR_STATE, "pkv_block_tables_dense: unknown sequence");
+        if ((int64_t)it->second.table.size() > max_blocks)
+            return pkv_fail(PKV_ERR_SHAPE, "pkv_block_tables_dense: table longer than %d",
+                            max_blocks);
+    }
+    for (int i = 0; i < n; ++i) {
+        const pkv_allocator::Seq& s = a->seqs.find(seqs[i])->second;
+        int32_t* row = tables + (size_t)i * max_blocks;
+        size_t k = s.table.size();
+        if (k) std::memcpy(row, s.table.data(), sizeof(int32_t) * k);
+        for (size_t j = k; j < (size_t)max_blocks; ++j) row[j] = -1;
+        lens[i] = (int32_t)s.len;
+    }
+    return PKV_OK;
+}
+
+int pkv_refcount(pkv_allocator* a, int block, int* count)
+{
+    if (!a || !count) return pkv_fail(PKV_ERR_NULL, "pkv_refcount: NULL argument");
+    if (block < 0 || block >= a->num_blocks)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_refcount: block %d out of range", block);
+    *count = a->ref[block];
+    return PKV_OK;
+}
+
+int pkv_num_free_blocks(pkv_allocator* a, int* n)
+{
+    if (!a || !n) return pkv_fail(PKV_ERR_NULL, "pkv_num_free_blocks: NULL argument");
+    *n = (int)a->free_stack.size();
+    return PKV_OK;
+}
+
+int pkv_stats(pkv_allocator* a, int64_t* allocated_positions, int64_t* valid_positions,
+              int64_t* blocks_in_use)
+{
+    if (!a || !allocated_positions || !valid_positions || !blocks_in_use)
+        return pkv_fail(PKV_ERR_NULL, "pkv_stats: NULL argument");
+    int64_t alloc = 0, valid = 0;
+    for (const auto& kv : a->seqs) {
+        alloc += (int64_t)kv.second.table.size() * a->block_size;
+        valid += kv.second.len;
+    }
+    *allocated_positions = alloc;
+    *valid_positions = valid;
+    *blocks_in_use = (int64_t)a->num_blocks - (int64_t)a->free_stack.size();
+    return PKV_OK;
+}
+
+}  // extern "C"

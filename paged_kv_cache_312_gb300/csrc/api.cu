@@ -1,0 +1,311 @@
+// C-ABI entry points of libpkv (declared in include/pkv.h): argument checks,
+// workspace carving, TMA tensor maps and kernel selection.  All arithmetic of
+// the path runs in the kernels (kernels_basic.cu, decode_tc.cu).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+#include "pkv_kernels.h"
+
+// ---------------------------------------------------------------------------
+// errors
+// ---------------------------------------------------------------------------
+namespace {
+thread_local char g_err[512] = "";
+int g_decode_kernel = PKV_KERNEL_AUTO;
+}  // namespace
+
+int pkv_fail(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+static int cuda_fail(cudaError_t e, const char* where)
+{
+    return pkv_fail(PKV_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------------------
+// TMA tensor maps: a cache viewed as [NB*Hkv*B rows][D columns] of 16-bit
+// elements, loaded in boxes of 64 columns x B rows with the 128-byte swizzle.
+// Encoded maps are cached by (address, rows, D, B, dtype).
+// ---------------------------------------------------------------------------
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct MapEntry {
+    const void* ptr = nullptr;
+    uint64_t rows = 0;
+    int D = 0, B = 0, dtype = -1;
+    CUtensorMap map;
+};
+
+std::mutex g_map_mu;
+MapEntry g_maps[16];
+int g_map_next = 0;
+EncodeTiledFn g_encode = nullptr;
+
+int get_encoder()
+{
+    if (g_encode) return PKV_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return pkv_fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return PKV_OK;
+}
+
+int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtensorMap* out)
+{
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (const MapEntry& m : g_maps) {
+        if (m.ptr == cache && m.rows == rows && m.D == D && m.B == B && m.dtype == dtype) {
+            *out = m.map;
+            return PKV_OK;
+        }
+    }
+    int rc = get_encoder();
+    if (rc != PKV_OK) return rc;
+    MapEntry& m = g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % 16;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)B};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(&m.map,
+                          dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          2, const_cast<void*>(cache), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        m.ptr = nullptr;
+        return pkv_fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
+    m.ptr = cache;
+    m.rows = rows;
+    m.D = D;
+    m.B = B;
+    m.dtype = dtype;
+    *out = m.map;
+    return PKV_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Split workspace: (max, sum) pairs first, unnormalised outputs after.
+void carve_workspace(void* ws, size_t S, size_t H, size_t P, size_t D, float2** ml, float** o)
+{
+    *ml = static_cast<float2*>(ws);
+    *o = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(S * H * P * sizeof(float2)));
+    (void)D;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_last_error_string(void) { return g_err; }
+
+int pkv_version(void) { return 100; }
+
+int pkv_set_decode_kernel(int which)
+{
+    if (which != PKV_KERNEL_AUTO && which != PKV_KERNEL_CUDA_CORE)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_set_decode_kernel: unknown value %d", which);
+    g_decode_kernel = which;
+    return PKV_OK;
+}
+
+int pkv_device_status(void* stream, uint32_t* bits, int reset)
+{
+    if (!bits) return pkv_fail(PKV_ERR_NULL, "pkv_device_status: bits is NULL");
+    unsigned int* word = pkv_status_word_ptr();
+    if (!word) return pkv_fail(PKV_ERR_CUDA, "pkv_device_status: no device status word");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int host = 0;
+    cudaError_t e = cudaMemcpyAsync(&host, word, sizeof host, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && reset) e = cudaMemsetAsync(word, 0, sizeof(unsigned int), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_device_status");
+    *bits = host;
+    if (host) return pkv_fail(PKV_ERR_BOUNDS, "device status bits 0x%x", host);
+    return PKV_OK;
+}
+
+int pkv_kv_write(void* k_cache, void* v_cache, const void* key, const void* value,
+                 const int64_t* slot_mapping, int num_tokens, int num_blocks, int num_kv_heads,
+                 int head_dim, int block_size, int dtype, void* stream)
+{
+    const int eb = pkv_dtype_bytes(dtype);
+    if (!eb) return pkv_fail(PKV_ERR_DTYPE, "pkv_kv_write: dtype %d", dtype);
+    if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_kv_write: bad sizes");
+    if ((head_dim * eb) % 16 != 0)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_kv_write: head_dim*elem_bytes must be a multiple of 16");
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !key || !value || !slot_mapping)
+        return pkv_fail(PKV_ERR_NULL, "pkv_kv_write: NULL pointer");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(key, 16) || !aligned(value, 16))
+        return pkv_fail(PKV_ERR_ALIGN, "pkv_kv_write: caches, key and value need 16-byte alignment");
+    unsigned int* status = pkv_status_word_ptr();
+    if (!status) return pkv_fail(PKV_ERR_CUDA, "pkv_kv_write: no device status word");
+    cudaError_t e = launch_kv_write(k_cache, v_cache, key, value, slot_mapping, num_tokens,
+                                    num_blocks, num_kv_heads, head_dim, block_size, eb, status,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "pkv_kv_write launch");
+}
+
+int pkv_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
+                       int num_blocks, int num_kv_heads, int head_dim, int block_size, int dtype,
+                       void* stream)
+{
+    const int eb = pkv_dtype_bytes(dtype);
+    if (!eb) return pkv_fail(PKV_ERR_DTYPE, "pkv_kv_copy_blocks: dtype %d", dtype);
+    if (num_pairs < 0 || num_blocks < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_kv_copy_blocks: bad sizes");
+    const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * eb;
+    if (block_bytes % 16 != 0)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_kv_copy_blocks: block bytes must be a multiple of 16");
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !pairs) return pkv_fail(PKV_ERR_NULL, "pkv_kv_copy_blocks: NULL");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(pairs, 8))
+        return pkv_fail(PKV_ERR_ALIGN, "pkv_kv_copy_blocks: misaligned pointer");
+    unsigned int* status = pkv_status_word_ptr();
+    if (!status) return pkv_fail(PKV_ERR_CUDA, "pkv_kv_copy_blocks: no device status word");
+    cudaError_t e = launch_kv_copy_blocks(k_cache, v_cache, pairs, num_pairs, num_blocks,
+                                          block_bytes, status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "pkv_kv_copy_blocks launch");
+}
+
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                  int partition_size)
+{
+    if (partition_size <= 0 || num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 ||
+        max_context_len <= 0)
+        return 0;
+    const size_t P = ((size_t)max_context_len + partition_size - 1) / partition_size;
+    const size_t n = (size_t)num_seqs * num_heads * P;
+    return align256(n * sizeof(float2)) + n * head_dim * sizeof(float);
+}
+
+int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               float scale, int block_size, int num_kv_heads, int num_seqs,
+                               int num_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
+                               int kv_dtype, int out_dtype, int partition_size, void* workspace,
+                               size_t workspace_bytes, void* stream)
+{
+    static const char* fn = "pkv_paged_decode_attention";
+    if (!pkv_dtype_bytes(kv_dtype) || !pkv_dtype_bytes(out_dtype))
+        return pkv_fail(PKV_ERR_DTYPE, "%s: dtype kv=%d out=%d", fn, kv_dtype, out_dtype);
+    if (num_seqs < 0 || num_seqs > 65535)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: num_seqs %d outside [0, 65535]", fn, num_seqs);
+    if (head_dim != 64 && head_dim != 128)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: head_dim %d not in {64,128}", fn, head_dim);
+    if (block_size != 8 && block_size != 16 && block_size != 32)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: block_size %d not in {8,16,32}", fn, block_size);
+    if (num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads != 0 ||
+        num_heads > 65535)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: num_heads %d / num_kv_heads %d", fn, num_heads,
+                        num_kv_heads);
+    if (max_blocks_per_seq <= 0 || num_blocks <= 0)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: max_blocks_per_seq %d, num_blocks %d", fn,
+                        max_blocks_per_seq, num_blocks);
+    if ((int64_t)max_blocks_per_seq * block_size > (1ll << 30))
+        return pkv_fail(PKV_ERR_SHAPE, "%s: max context too long", fn);
+    if ((int64_t)num_blocks * num_kv_heads * block_size >= (1ll << 31))
+        return pkv_fail(PKV_ERR_SHAPE, "%s: cache has >= 2^31 rows", fn);
+    if (partition_size < 0 || (partition_size > 0 && partition_size % block_size != 0))
+        return pkv_fail(PKV_ERR_SHAPE, "%s: partition_size %d must be 0 or a multiple of %d", fn,
+                        partition_size, block_size);
+    if (!std::isfinite(scale)) return pkv_fail(PKV_ERR_SHAPE, "%s: scale is not finite", fn);
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return pkv_fail(PKV_ERR_NULL, "%s: NULL pointer", fn);
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) ||
+        !aligned(out, pkv_dtype_bytes(out_dtype)))
+        return pkv_fail(PKV_ERR_ALIGN, "%s: caches need 16-byte, q 4-byte alignment", fn);
+
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    p.block_size = block_size;
+    p.num_kv_heads = num_kv_heads;
+    p.num_heads = num_heads;
+    p.head_dim = head_dim;
+    p.num_seqs = num_seqs;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.out_dtype = out_dtype;
+    p.ws_ml = nullptr;
+    p.ws_o = nullptr;
+    const int max_ctx = max_blocks_per_seq * block_size;
+    if (partition_size == 0) {
+        p.partition_tokens = max_ctx;
+        p.max_partitions = 1;
+    } else {
+        p.partition_tokens = partition_size;
+        p.max_partitions = (max_ctx + partition_size - 1) / partition_size;
+        const size_t need =
+            pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_ctx, partition_size);
+        if (!workspace || workspace_bytes < need)
+            return pkv_fail(PKV_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn,
+                            need, workspace ? workspace_bytes : (size_t)0);
+        if (!aligned(workspace, 256))
+            return pkv_fail(PKV_ERR_ALIGN, "%s: workspace needs 256-byte alignment", fn);
+        carve_workspace(workspace, num_seqs, num_heads, p.max_partitions, head_dim, &p.ws_ml,
+                        &p.ws_o);
+    }
+    p.status = pkv_status_word_ptr();
+    if (!p.status) return pkv_fail(PKV_ERR_CUDA, "%s: no device status word", fn);
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int G = num_heads / num_kv_heads;
+    const bool tensor_core =
+        g_decode_kernel == PKV_KERNEL_AUTO && kv_dtype != PKV_F32 && G <= 8;
+    cudaError_t e;
+    if (tensor_core) {
+        CUtensorMap kmap, vmap;
+        const uint64_t rows = (uint64_t)num_blocks * num_kv_heads * block_size;
+        int rc = tensor_map(k_cache, rows, head_dim, block_size, kv_dtype, &kmap);
+        if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap);
+        if (rc != PKV_OK) return rc;
+        e = launch_decode_tensor_core(p, kv_dtype, &kmap, &vmap, st);
+    } else {
+        e = launch_decode_cuda_core(p, kv_dtype, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_paged_decode_attention launch");
+    if (p.max_partitions > 1) {
+        e = launch_lse_reduce(p, st);
+        if (e != cudaSuccess) return cuda_fail(e, "pkv_paged_decode_attention reduce launch");
+    }
+    return PKV_OK;
+}
+
+}  // extern "C"

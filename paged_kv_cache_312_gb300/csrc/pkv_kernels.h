@@ -1,0 +1,51 @@
+// Launch interfaces between the C-ABI layer (api.cu) and the kernel files.
+// Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+// Everything one decode launch needs; passed by value as a kernel parameter.
+struct DecodeParams {
+    void* out;                   // [S][Hq][D], out_dtype
+    const void* q;               // [S][Hq][D], kv dtype
+    const void* k_cache;         // [NB][Hkv][B][D]
+    const void* v_cache;
+    const int32_t* block_tables; // [S][max_blocks]
+    const int32_t* context_lens; // [S]
+    float scale_log2;            // softmax scale * log2(e): scores live in base 2
+    int block_size, num_kv_heads, num_heads, head_dim;
+    int num_seqs, max_blocks, num_blocks;
+    int partition_tokens;        // tokens per partition (>= max context if unsplit)
+    int max_partitions;          // ceil(max_blocks * block_size / partition_tokens)
+    int out_dtype;
+    float2* ws_ml;               // [S][Hq][max_partitions] (max, sum) in base 2
+    float* ws_o;                 // [S][Hq][max_partitions][D] unnormalised output
+    unsigned int* status;        // device status word (PKV_STATUS_* bits)
+};
+
+// Device status word of the current device (address of a __device__ symbol).
+unsigned int* pkv_status_word_ptr();
+
+cudaError_t launch_kv_write(void* k_cache, void* v_cache, const void* key, const void* value,
+                            const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                            int num_kv_heads, int head_dim, int block_size, int elem_bytes,
+                            unsigned int* status, cudaStream_t stream);
+
+cudaError_t launch_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs,
+                                  int num_pairs, int num_blocks, size_t block_bytes,
+                                  unsigned int* status, cudaStream_t stream);
+
+// CUDA-core decode (any dtype, any group size).  Grid: partitions x heads x seqs.
+cudaError_t launch_decode_cuda_core(const DecodeParams& p, int kv_dtype, cudaStream_t stream);
+
+// Tensor-core decode (16-bit KV, group size <= 8).  The tensor maps describe
+// k_cache / v_cache as 2-D [NB*Hkv*B rows][D columns] for tile loads.
+cudaError_t launch_decode_tensor_core(const DecodeParams& p, int kv_dtype,
+                                      const void* k_map, const void* v_map,
+                                      cudaStream_t stream);
+
+// Log-sum-exp merge of split partitions (only sequences with > 1 partition).
+cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);

@@ -1,0 +1,214 @@
+"""Host-side checks of libpkv (no GPU): the C ABI loads and exports every
+declared symbol, arguments are rejected on the host before any launch, and the
+C++ block allocator makes exactly the decisions of the oracle's reference
+block manager."""
+import ctypes
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_312_gb300 as pkv
+from oracle.blockmgr import BlockManager, OutOfBlocks
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_312_gb300 import build
+    build.build()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(pkv_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 20
+    handle = ctypes.CDLL(pkv._binding.LIB_PATH)
+    for n in names:
+        assert hasattr(handle, n), n
+    # and the binding knows each one's signature
+    assert set(names) <= set(pkv._binding._SIGS)
+
+
+def test_version_and_error_string():
+    L = pkv.lib()
+    assert L.pkv_version() == 100
+    rc = L.pkv_set_decode_kernel(7)
+    assert rc == -2
+    assert b"unknown value" in L.pkv_last_error_string()
+
+
+def _attn(L, **kw):
+    a = dict(out=256, q=256, k=256, v=256, bt=256, cl=256, scale=0.1, B=16, Hkv=4, S=2, Hq=8, D=128,
+             maxb=4, NB=10, kvdt=2, odt=0, P=0, ws=0, wsb=0)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return L.pkv_paged_decode_attention(P(a["out"]), P(a["q"]), P(a["k"]), P(a["v"]), P(a["bt"]),
+                                        P(a["cl"]), a["scale"], a["B"], a["Hkv"], a["S"], a["Hq"],
+                                        a["D"], a["maxb"], a["NB"], a["kvdt"], a["odt"], a["P"],
+                                        P(a["ws"]), a["wsb"], P(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), -2), (dict(B=12), -2), (dict(Hq=6), -2), (dict(kvdt=5), -3),
+    (dict(odt=9), -3), (dict(P=20), -2), (dict(P=32, ws=0), -8), (dict(maxb=0), -2),
+    (dict(S=70000), -2), (dict(q=0), -1), (dict(k=8), -10), (dict(scale=float("nan")), -2),
+])
+def test_decode_rejects_bad_arguments_on_host(kw, code):
+    assert _attn(pkv.lib(), **kw) == code
+
+
+def test_decode_with_no_sequences_is_a_no_op():
+    assert _attn(pkv.lib(), S=0, out=0, q=0) == 0
+
+
+def test_workspace_size_formula():
+    L = pkv.lib()
+    assert L.pkv_decode_workspace_bytes(8, 32, 128, 32768, 0) == 0
+    n = 8 * 32 * 64
+    expect = ((n * 8 + 255) // 256) * 256 + n * 128 * 4
+    assert L.pkv_decode_workspace_bytes(8, 32, 128, 32768, 512) == expect
+
+
+def test_write_and_copy_reject_bad_arguments_on_host():
+    L = pkv.lib()
+    P = ctypes.c_void_p
+    assert L.pkv_kv_write(P(16), P(16), P(16), P(16), P(8), 3, 4, 2, 12, 16, 2, P(0)) == -2
+    assert L.pkv_kv_write(P(16), P(16), P(16), P(16), P(8), 3, 4, 2, 64, 16, 7, P(0)) == -3
+    assert L.pkv_kv_write(P(16), P(16), P(0), P(16), P(8), 3, 4, 2, 64, 16, 2, P(0)) == -1
+    assert L.pkv_kv_write(P(16), P(16), P(24), P(16), P(8), 3, 4, 2, 64, 16, 2, P(0)) == -10
+    assert L.pkv_kv_write(P(0), P(0), P(0), P(0), P(0), 0, 4, 2, 64, 16, 2, P(0)) == 0
+    assert L.pkv_kv_copy_blocks(P(16), P(16), P(0), 2, 4, 2, 64, 16, 2, P(0)) == -1
+    assert L.pkv_kv_copy_blocks(P(0), P(0), P(0), 0, 4, 2, 64, 16, 2, P(0)) == 0
+
+
+# --------------------------------------------------------------------------
+# C++ allocator against the reference block manager
+# --------------------------------------------------------------------------
+
+def _same(cpp, ref, seqs):
+    for s in seqs:
+        assert cpp.table(s) == ref.table(s)
+        assert cpp.length(s) == ref.length(s)
+    for b in range(ref.num_blocks):
+        assert cpp.refcount(b) == ref.refcount(b)
+    assert cpp.num_free() == ref.num_free()
+    assert cpp.stats() == ref.stats()
+
+
+def test_allocator_worked_example():
+    lengths = [37, 91, 128, 201, 511]
+    for B, expect in ((16, 992), (32, 1024)):
+        a = pkv.BlockAllocator(100, B)
+        for s, n in enumerate(lengths):
+            a.add(s, n)
+        alloc, valid, used = a.stats()
+        assert (alloc, valid, used * B) == (expect, 968, expect)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_allocator_matches_reference_on_random_operations(seed):
+    rnd = random.Random(seed)
+    NB, B = 48, 4
+    order = list(np.random.default_rng(seed).permutation(NB))
+    cpp, ref = pkv.BlockAllocator(NB, B, free_order=order), BlockManager(NB, B, free_order=order)
+    live, nid = [], 0
+    for _ in range(1500):
+        op = rnd.random()
+        if op < 0.15 or not live:
+            n = rnd.randint(0, 10)
+            try:
+                ref.add(nid, n)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    cpp.add(nid, n)
+            else:
+                cpp.add(nid, n)
+                live.append(nid)
+            nid += 1
+        elif op < 0.5:
+            s = rnd.choice(live)
+            try:
+                r = ref.append(s)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    cpp.append(s)
+            else:
+                assert cpp.append(s) == r
+        elif op < 0.65:
+            s = rnd.choice(live)
+            ref.fork(s, nid)
+            cpp.fork(s, nid)
+            live.append(nid)
+            nid += 1
+        elif op < 0.85:
+            seqs = [rnd.choice(live) for _ in range(rnd.randint(1, 6))]
+            try:
+                slots, pairs = ref.step_append(seqs)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    cpp.step_append(seqs)
+            else:
+                cs, cp = cpp.step_append(seqs)
+                assert cs.tolist() == slots
+                assert [tuple(p) for p in cp.tolist()] == pairs
+        else:
+            s = live.pop(rnd.randrange(len(live)))
+            ref.free_seq(s)
+            cpp.free(s)
+        _same(cpp, ref, live)
+
+
+def test_allocator_errors_leave_state_unchanged():
+    a = pkv.BlockAllocator(3, 4)
+    a.add(0, 8)
+    snap = (a.table(0), a.num_free(), a.stats())
+    with pytest.raises(pkv.OutOfBlocks):
+        a.add(1, 9)
+    with pytest.raises(pkv.PkvError):
+        a.add(0, 1)  # exists
+    with pytest.raises(pkv.PkvError):
+        a.fork(5, 6)  # unknown parent
+    with pytest.raises(pkv.PkvError):
+        a.free(9)
+    assert (a.table(0), a.num_free(), a.stats()) == snap
+    with pytest.raises(pkv.PkvError):
+        pkv.BlockAllocator(3, 4, free_order=[0, 0, 1])
+
+
+def test_allocator_dense_tables():
+    a = pkv.BlockAllocator(10, 4, free_order=[9, 8, 7, 6, 5, 4, 3, 2, 1, 0])
+    a.add(1, 5)
+    a.add(2, 0)
+    t, l = a.dense_tables([1, 2], 3)
+    assert t.tolist() == [[9, 8, -1], [-1, -1, -1]] and l.tolist() == [5, 0]
+    with pytest.raises(pkv.PkvError):
+        a.dense_tables([1], 1)
+
+
+def test_beam_fork_cow_pairs():
+    # A width-4 beam over one partial block: three children copy, the last
+    # holder writes in place.
+    a = pkv.BlockAllocator(16, 4)
+    a.add(0, 6)
+    for c in (1, 2, 3):
+        a.fork(0, c)
+    last = a.table(0)[-1]
+    assert a.refcount(last) == 4
+    slots, pairs = a.step_append([0, 1, 2, 3])
+    assert [p[0] for p in pairs.tolist()] == [last, last, last]
+    assert a.refcount(last) == 1 and a.table(3)[-1] == last
+    assert len(set(slots.tolist())) == 4

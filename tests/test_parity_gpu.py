@@ -1,0 +1,341 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle.
+
+Cache writes and block copies must match bit for bit; attention outputs must
+be within max-abs 2e-3 of the oracle for 16-bit KV and 1e-5 for fp32 KV (fp32
+output).  Cases span several 16-token tiles, ragged tails, empty sequences,
+bad ids, every block size / head_dim / group size the kernels support, both
+decode kernels, the split-context path, and the full-size workloads (checked
+on sampled sequences)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_312_gb300 as pkv
+from oracle.blockmgr import BlockManager
+from workloads import (WORKLOADS, Workload, beam_setup_schedule, beam_step_schedule,
+                       make_beam_case, make_decode_case, poison_unused, write_step_schedule)
+
+pytestmark = pytest.mark.gpu
+
+TOL16, TOL32 = 2e-3, 1e-5
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    pkv.device_status(reset=True)
+    yield
+    pkv.set_decode_kernel(pkv.KERNEL_AUTO)
+
+
+@pytest.fixture(autouse=True)
+def clean_status():
+    pkv.device_status(reset=True)
+    yield
+
+
+def tol(dtype):
+    return TOL32 if dtype == torch.float32 else TOL16
+
+
+def bits(t):
+    t = t.cpu().contiguous()
+    return t.view(torch.int32) if t.element_size() == 4 else t.view(torch.int16)
+
+
+def gpu_decode(q, kc, vc, bt, cl, scale, B, Hkv, P=0, out_dtype=torch.float32, kernel=None):
+    if kernel is not None:
+        pkv.set_decode_kernel(kernel)
+    try:
+        S, Hq, D = q.shape
+        out = torch.full((S, Hq, D), float("nan"), dtype=out_dtype, device=DEV)
+        ws = None
+        if P:
+            n = pkv.decode_workspace_bytes(S, Hq, D, bt.shape[1] * B, P)
+            ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+        pkv.paged_decode_attention(out, q.to(DEV), kc, vc, bt.to(DEV), cl.to(DEV), scale, B, Hkv,
+                                   partition_size=P, workspace=ws)
+        torch.cuda.synchronize()
+        return out
+    finally:
+        pkv.set_decode_kernel(pkv.KERNEL_AUTO)
+
+
+def max_err(out, ref):
+    return float(np.abs(out.cpu().double().numpy() - ref).max())
+
+
+# --------------------------------------------------------------------------
+# kv_write / kv_copy_blocks: bit-exact
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("B,D,Hkv", [(8, 64, 3), (16, 128, 8), (32, 128, 2)])
+def test_kv_write_bit_exact(dtype, B, D, Hkv):
+    NB, T = 23, 150
+    g = torch.Generator().manual_seed(B + D)
+    kc = torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    vc = torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    key = torch.randn(T, Hkv, D, generator=g).to(dtype)
+    val = torch.randn(T, Hkv, D, generator=g).to(dtype)
+    slots = torch.randperm(NB * B, generator=g)[:T].to(torch.int64)
+    slots[::7] = -1  # padding tokens
+    dk, dv = kc.to(DEV), vc.to(DEV)
+    pkv.kv_write(dk, dv, key.to(DEV), val.to(DEV), slots.to(DEV))
+    oracle.kv_write(kc, vc, key, val, slots, B)
+    torch.cuda.synchronize()
+    assert torch.equal(bits(dk), bits(kc)) and torch.equal(bits(dv), bits(vc))
+    assert pkv.device_status() == 0
+
+
+def test_kv_write_out_of_range_slot_is_flagged_and_skipped():
+    NB, Hkv, B, D = 4, 2, 16, 64
+    kc = torch.zeros(NB, Hkv, B, D, dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    key = torch.ones(2, Hkv, D, dtype=torch.bfloat16, device=DEV)
+    slots = torch.tensor([NB * B, 5], dtype=torch.int64, device=DEV)
+    pkv.kv_write(kc, vc, key, key, slots)
+    assert pkv.device_status() & 4
+    assert float(kc.float().sum()) == Hkv * D  # only slot 5 was written
+    assert float(kc[0, :, 5].float().sum()) == Hkv * D
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_copy_blocks_bit_exact(dtype):
+    NB, Hkv, B, D = 40, 4, 16, 128
+    g = torch.Generator().manual_seed(3)
+    kc = torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    vc = torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    perm = torch.randperm(NB, generator=g)
+    pairs = torch.stack([perm[:12], perm[12:24]], dim=1).to(torch.int64)
+    dk, dv = kc.to(DEV), vc.to(DEV)
+    pkv.kv_copy_blocks(dk, dv, pairs.to(DEV))
+    oracle.kv_copy_blocks(kc, vc, pairs)
+    torch.cuda.synchronize()
+    assert torch.equal(bits(dk), bits(kc)) and torch.equal(bits(dv), bits(vc))
+    bad = torch.tensor([[0, NB]], dtype=torch.int64, device=DEV)
+    pkv.kv_copy_blocks(dk, dv, bad)
+    assert pkv.device_status() & 8
+    assert torch.equal(bits(dk), bits(kc))
+
+
+# --------------------------------------------------------------------------
+# decode attention on small cases (several tiles, ragged tails, empty rows)
+# --------------------------------------------------------------------------
+
+RAGGED = [0, 1, 7, 15, 16, 17, 33, 100, 129, 300, 513]
+
+SMALL = [  # dtype, Hq, Hkv, D, B
+    ("bf16", 8, 1, 128, 16), ("bf16", 32, 4, 128, 16), ("bf16", 16, 16, 128, 16),
+    ("f16", 8, 4, 128, 8), ("bf16", 4, 2, 64, 32), ("f16", 16, 4, 64, 16),
+    ("bf16", 6, 2, 128, 32), ("f16", 12, 12, 64, 8), ("bf16", 16, 2, 64, 8),
+    ("f32", 8, 2, 128, 16), ("f32", 4, 4, 64, 32), ("bf16", 32, 2, 128, 16),
+]
+
+
+@pytest.mark.parametrize("kernel", [pkv.KERNEL_AUTO, pkv.KERNEL_CUDA_CORE])
+@pytest.mark.parametrize("P", [0, 64])
+@pytest.mark.parametrize("dt,Hq,Hkv,D,B", SMALL)
+def test_decode_small(dt, Hq, Hkv, D, B, P, kernel):
+    w = Workload(0, "small", dt, Hq, Hkv, D, B, len(RAGGED), "fixed")
+    case = make_decode_case(w, seed=Hq * 7 + B + D, lengths=RAGGED)
+    if P and P % B:
+        pytest.skip("partition must be a multiple of the block size")
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    out = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, B, Hkv, P=P,
+                     kernel=kernel)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, B, Hkv)
+    assert pkv.device_status() == 0
+    assert max_err(out, ref) <= tol(w.torch_dtype)
+    assert torch.equal(out[0].cpu(), torch.zeros_like(out[0].cpu()))  # length-0 row
+
+
+def test_workload1_fp32():
+    w = WORKLOADS[1]
+    for seed in (0, 1, 2):
+        case = make_decode_case(w, seed=seed)
+        kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+        out = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale,
+                         w.block_size, w.num_kv_heads)
+        ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                            case.context_lens, w.scale, w.block_size,
+                                            w.num_kv_heads)
+        assert max_err(out, ref) <= TOL32
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
+def test_16bit_outputs(out_dtype):
+    # The output is rounded once to its dtype: allow the attention tolerance
+    # plus one unit of rounding at the reference's magnitude.
+    w = Workload(0, "o", "bf16", 16, 4, 128, 16, 6, "fixed")
+    case = make_decode_case(w, seed=5, lengths=[1, 5, 40, 77, 200, 333])
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    for P in (0, 32):
+        out = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, 16, 4,
+                         P=P, out_dtype=out_dtype)
+        ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache,
+                                            case.block_tables, case.context_lens, w.scale, 16, 4)
+        rel = 2.0 ** -8 if out_dtype == torch.bfloat16 else 2.0 ** -11
+        diff = np.abs(out.cpu().double().numpy() - ref)
+        assert (diff <= TOL16 + rel * np.abs(ref)).all()
+
+
+def test_bad_block_id_and_length_are_flagged():
+    w = Workload(0, "bad", "bf16", 8, 2, 128, 16, 3, "fixed")
+    case = make_decode_case(w, seed=9, lengths=[40, 40, 40])
+    bt = case.block_tables.clone()
+    bt[1, 1] = case.num_blocks + 5
+    cl = case.context_lens.clone()
+    cl[2] = bt.shape[1] * 16 + 1
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    for kernel in (pkv.KERNEL_AUTO, pkv.KERNEL_CUDA_CORE):
+        out = gpu_decode(case.q, kc, vc, bt, cl, w.scale, 16, 2, kernel=kernel)
+        st = pkv.device_status()
+        assert st & 1 and st & 2
+        ref = oracle.paged_decode_attention(case.q[:1], case.k_cache, case.v_cache, bt[:1],
+                                            cl[:1], w.scale, 16, 2)
+        assert max_err(out[:1], ref) <= TOL16  # the healthy sequence is unaffected
+        assert torch.isfinite(out[1]).all()
+
+
+def test_split_matches_one_pass_and_kernels_agree():
+    w = Workload(0, "split", "bf16", 32, 8, 128, 16, 5, "fixed")
+    case = make_decode_case(w, seed=11, lengths=[1000, 1, 513, 512, 2049])
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, 16, 8)
+    for P in (0, 16, 256, 512, 4096):
+        for kernel in (pkv.KERNEL_AUTO, pkv.KERNEL_CUDA_CORE):
+            out = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, 16, 8,
+                             P=P, kernel=kernel)
+            assert max_err(out, ref) <= TOL16, (P, kernel)
+
+
+def test_nan_poison_and_physical_permutation():
+    # Same logical data paged twice with different physical ids: same output.
+    w = Workload(0, "perm", "f16", 16, 4, 128, 16, 4, "fixed")
+    a = make_decode_case(w, seed=21, lengths=[50, 129, 7, 260])
+    perm = torch.randperm(a.num_blocks, generator=torch.Generator().manual_seed(1))
+    kc2 = torch.empty_like(a.k_cache)
+    vc2 = torch.empty_like(a.v_cache)
+    kc2[perm] = a.k_cache
+    vc2[perm] = a.v_cache
+    bt2 = torch.where(a.block_tables >= 0, perm[a.block_tables.clamp(min=0).long()].int(),
+                      a.block_tables)
+    o1 = gpu_decode(a.q, a.k_cache.to(DEV), a.v_cache.to(DEV), a.block_tables, a.context_lens,
+                    w.scale, 16, 4)
+    o2 = gpu_decode(a.q, kc2.to(DEV), vc2.to(DEV), bt2, a.context_lens, w.scale, 16, 4)
+    assert torch.isfinite(o1).all()
+    assert torch.equal(o1, o2)
+
+
+# --------------------------------------------------------------------------
+# full-size workloads, in the launch configuration the benchmark times
+# --------------------------------------------------------------------------
+
+def sampled_oracle(case_q, kc_host, vc_host, bt, cl, w, idx):
+    idx = torch.as_tensor(idx)
+    return oracle.paged_decode_attention(case_q[idx], kc_host, vc_host, bt[idx], cl[idx], w.scale,
+                                         w.block_size, w.num_kv_heads,
+                                         nthreads=oracle.default_threads())
+
+
+def pick(lens, k=6):
+    order = np.argsort(np.asarray(lens))
+    return sorted(set([int(order[0]), int(order[-1]), int(order[len(order) // 2])] +
+                      list(np.random.default_rng(0).choice(len(lens), k, replace=False))))
+
+
+def test_workload2_write_then_attend_full_size():
+    import bench
+    w = WORKLOADS[2]
+    case = make_decode_case(w, seed=0, poison=False)
+    ref_mgr = BlockManager(case.num_blocks, w.block_size, free_order=case.pool_order)
+    gpu_mgr = pkv.BlockAllocator(case.num_blocks, w.block_size, free_order=case.pool_order)
+    slots_r, pairs_r, bt_r, cl_r = write_step_schedule(ref_mgr, case.lengths)
+    slots, pairs, bt, cl = write_step_schedule(gpu_mgr, case.lengths)
+    assert torch.equal(slots, slots_r) and torch.equal(bt, bt_r) and pairs.numel() == 0
+    poison_unused(case.k_cache, case.v_cache, bt, case.lengths - 1)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    P = bench.launch_partition(w, bt.shape[1])
+    pkv.kv_write(kc, vc, case.new_key.to(DEV), case.new_value.to(DEV), slots.to(DEV))
+    out = gpu_decode(case.q, kc, vc, bt, cl, w.scale, w.block_size, w.num_kv_heads, P=P)
+    assert pkv.device_status() == 0
+    oracle.kv_write(case.k_cache, case.v_cache, case.new_key, case.new_value, slots_r,
+                    w.block_size)
+    assert torch.equal(bits(kc), bits(case.k_cache)) and torch.equal(bits(vc), bits(case.v_cache))
+    idx = pick(cl.tolist())
+    ref = sampled_oracle(case.q, case.k_cache, case.v_cache, bt_r, cl_r, w, idx)
+    assert max_err(out[idx], ref) <= TOL16
+
+
+@pytest.mark.parametrize("key", [3, 4])
+def test_gqa_and_long_context_full_size(key):
+    import bench
+    w = WORKLOADS[key]
+    case = make_decode_case(w, seed=0)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    P = bench.launch_partition(w, case.block_tables.shape[1])
+    out = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, w.block_size,
+                     w.num_kv_heads, P=P)
+    assert pkv.device_status() == 0
+    idx = pick(case.context_lens.tolist(), k=4 if key == 3 else 1)
+    ref = sampled_oracle(case.q, case.k_cache, case.v_cache, case.block_tables,
+                         case.context_lens, w, idx)
+    assert max_err(out[idx], ref) <= TOL16
+    assert torch.isfinite(out).all()
+
+
+def test_workload5_beam_step_full_size():
+    import bench
+    w = WORKLOADS[5]
+    case = make_beam_case(w, seed=0)
+    ref_mgr = BlockManager(case.pool_blocks, w.block_size, free_order=case.pool_order)
+    gpu_mgr = pkv.BlockAllocator(case.pool_blocks, w.block_size, free_order=case.pool_order)
+    host = {}
+    for name, mgr in (("ref", ref_mgr), ("gpu", gpu_mgr)):
+        pre, suf = beam_setup_schedule(mgr, case)
+        host[name] = (pre, suf) + beam_step_schedule(mgr, case)
+    pre, suf, ids, slots, pairs, bt, cl = host["gpu"]
+    pre_r, suf_r, ids_r, slots_r, pairs_r, bt_r, cl_r = host["ref"]
+    assert torch.equal(pre, pre_r) and all(torch.equal(a, b) for a, b in zip(suf, suf_r))
+    assert torch.equal(slots, slots_r) and torch.equal(pairs, pairs_r) and torch.equal(bt, bt_r)
+    assert pairs.shape[0] > 0  # re-selection shares partial blocks: copies happen
+
+    NB, Hkv, B, D = case.pool_blocks, w.num_kv_heads, w.block_size, w.head_dim
+    G, W = case.parents.shape
+    kh = torch.full((NB, Hkv, B, D), float("nan"), dtype=torch.float16)
+    vh = torch.full_like(kh, float("nan"))
+    keys = torch.cat([case.prefix_k.reshape(-1, Hkv, D)] + case.suffix_k)
+    vals = torch.cat([case.prefix_v.reshape(-1, Hkv, D)] + case.suffix_v)
+    all_slots = torch.cat([pre.reshape(-1)] + suf)
+    kc, vc = kh.to(DEV), vh.to(DEV)
+    # history (setup), then the timed step: CoW copy, write, attend
+    pkv.kv_write(kc, vc, keys.to(DEV), vals.to(DEV), all_slots.to(DEV))
+    pkv.kv_copy_blocks(kc, vc, pairs.to(DEV))
+    pkv.kv_write(kc, vc, case.new_key.to(DEV), case.new_value.to(DEV), slots.to(DEV))
+    P = bench.launch_partition(w, bt.shape[1])
+    out = gpu_decode(case.q, kc, vc, bt, cl, w.scale, B, Hkv, P=P)
+    assert pkv.device_status() == 0
+    oracle.kv_write(kh, vh, keys, vals, torch.cat([pre_r.reshape(-1)] + suf_r), B)
+    oracle.kv_copy_blocks(kh, vh, pairs_r)
+    oracle.kv_write(kh, vh, case.new_key, case.new_value, slots_r, B)
+    assert torch.equal(bits(kc), bits(kh)) and torch.equal(bits(vc), bits(vh))
+    idx = pick(cl.tolist())
+    ref = sampled_oracle(case.q, kh, vh, bt_r, cl_r, w, idx)
+    assert max_err(out[idx], ref) <= TOL16
+    # isolation: each beam sees its parent's history plus its own new token
+    g0 = 0
+    for b in range(W):
+        par = g0 * W + int(case.parents[g0, b])
+        n = int(case.suffix[par])
+        K = oracle.gather_sequence(kh, bt_r[b].tolist(), int(cl_r[b]))
+        expect = torch.cat([case.prefix_k[g0], case.suffix_k[par], case.new_key[b:b + 1]])
+        assert int(cl_r[b]) == w.prefix_len + n + 1
+        assert np.array_equal(K, expect.double().numpy())

@@ -110,28 +110,29 @@ def blocks_for(length: int, block_size: int) -> int:
 class DecodeCase:
     """Inputs of one decode step, all on the host."""
     workload: Workload
+    lengths: np.ndarray          # context length per sequence (new token included)
     q: torch.Tensor              # [S, Hq, D]
     k_cache: torch.Tensor        # [NB, Hkv, B, D]
     v_cache: torch.Tensor
-    block_tables: torch.Tensor   # int32 [S, max_blocks], unused entries -1
+    block_tables: torch.Tensor   # int32 [S, max_blocks]: sequential pagination, -1 unused
     context_lens: torch.Tensor   # int32 [S]
+    pool_order: np.ndarray       # physical ids in hand-out order
     new_key: torch.Tensor | None = None    # [S, Hkv, D] token written this step
     new_value: torch.Tensor | None = None
-    pool_order: np.ndarray | None = None   # physical ids in hand-out order
 
     @property
     def num_blocks(self) -> int:
         return self.k_cache.shape[0]
 
 
-def make_decode_case(w: Workload, seed: int = 0, lengths=None, max_blocks=None,
-                     poison: bool = True, num_seqs=None) -> DecodeCase:
+def make_decode_case(w: Workload, seed: int = 0, lengths=None, num_seqs=None,
+                     poison: bool = True, pool_blocks=None) -> DecodeCase:
     """Random paged cache for workload w.
 
-    Sequences receive physical blocks from a seeded shuffle of the pool, in
-    sequence order.  When the workload writes a new token each step, the
-    token at position context_len - 1 is drawn as new_key/new_value and its
-    cache slot is left poisoned: the step's write must fill it.
+    block_tables hands out the shuffled pool in sequence order (sequence s
+    takes the next blocks_for(L_s) ids).  Workloads that write a new token
+    each step draw it as new_key/new_value; callers that build their tables
+    through a block allocator instead should poison with `poison_unused`.
     """
     rng = np.random.default_rng(seed)
     if lengths is None:
@@ -143,10 +144,10 @@ def make_decode_case(w: Workload, seed: int = 0, lengths=None, max_blocks=None,
     B, Hkv, D, Hq = w.block_size, w.num_kv_heads, w.head_dim, w.num_heads
     need = [blocks_for(n, B) for n in lengths]
     total = int(sum(need))
-    NB = w.pool_blocks if w.pool_blocks else max(1, math.ceil(1.25 * total))
+    NB = pool_blocks or w.pool_blocks or max(1, math.ceil(1.25 * total))
     if NB < total:
         raise ValueError("pool too small")
-    maxb = max_blocks if max_blocks is not None else max(1, max(need, default=1))
+    maxb = max(1, max(need, default=1))
     order = rng.permutation(NB)
     tables = np.full((S, maxb), -1, dtype=np.int32)
     cur = 0
@@ -162,21 +163,148 @@ def make_decode_case(w: Workload, seed: int = 0, lengths=None, max_blocks=None,
     if w.writes_new_token:
         new_key = normal_values(rng, (S, Hkv, D), dt)
         new_value = normal_values(rng, (S, Hkv, D), dt)
+    tables_t = torch.from_numpy(tables)
     if poison:
-        valid = np.zeros((NB, B), dtype=bool)
-        for s in range(S):
-            n = int(lengths[s]) - (1 if w.writes_new_token else 0)
-            for i in range(need[s]):
-                valid[tables[s, i], :max(0, min(B, n - i * B))] = True
-        bad = torch.from_numpy(~valid)[:, None, :, None].expand(NB, Hkv, B, D)
-        k_cache[bad] = float("nan")
-        v_cache[bad] = float("nan")
-    return DecodeCase(w, q, k_cache, v_cache, torch.from_numpy(tables),
-                      torch.from_numpy(lengths.astype(np.int32)), new_key, new_value,
-                      order)
+        filled = lengths - (1 if w.writes_new_token else 0)
+        poison_unused(k_cache, v_cache, tables_t, filled)
+    return DecodeCase(w, lengths, q, k_cache, v_cache, tables_t,
+                      torch.from_numpy(lengths.astype(np.int32)), order, new_key, new_value)
+
+
+def poison_unused(k_cache: torch.Tensor, v_cache: torch.Tensor, tables, filled) -> None:
+    """NaN into every cache slot that does not hold one of the first filled[s]
+    tokens of some sequence s (tables: [S, max_blocks], -1 = unused)."""
+    NB, _, B, _ = k_cache.shape
+    valid = np.zeros((NB, B), dtype=bool)
+    tables = np.asarray(tables)
+    for s in range(tables.shape[0]):
+        n = int(filled[s])
+        for i in range(blocks_for(n, B)):
+            valid[tables[s, i], :min(B, n - i * B)] = True
+    bad = torch.from_numpy(~valid)[:, None, :, None]
+    k_cache.masked_fill_(bad, float("nan"))
+    v_cache.masked_fill_(bad, float("nan"))
+
+
+def dense_tables(manager, seqs, max_blocks=None):
+    """int32 [n, max_blocks] tables (-1 unused) and int32 lengths read from a
+    block manager exposing table(seq) and length(seq)."""
+    rows = [manager.table(s) for s in seqs]
+    mb = max_blocks or max(1, max(len(r) for r in rows))
+    t = torch.full((len(rows), mb), -1, dtype=torch.int32)
+    for i, r in enumerate(rows):
+        if r:
+            t[i, :len(r)] = torch.tensor(r, dtype=torch.int32)
+    lens = torch.tensor([manager.length(s) for s in seqs], dtype=torch.int32)
+    return t, lens
+
+
+def write_step_schedule(manager, lengths):
+    """Drive a block manager to the state of a decode step in which sequence
+    s already holds lengths[s] - 1 tokens and one more is appended for each
+    sequence.  Returns (slots int64 [S], cow pairs, tables, lens)."""
+    S = len(lengths)
+    for s in range(S):
+        manager.add(s, int(lengths[s]) - 1)
+    slots, pairs = manager.step_append(list(range(S)))
+    tables, lens = dense_tables(manager, range(S))
+    return (torch.as_tensor(slots, dtype=torch.int64).reshape(-1),
+            torch.as_tensor(pairs, dtype=torch.int64).reshape(-1, 2), tables, lens)
 
 
 def beam_parents(rng: np.random.Generator, groups: int, width: int) -> np.ndarray:
     """Seeded beam re-selection: each beam of each group picks a parent beam of
     the same group uniformly at random.  Returns [groups, width]."""
     return rng.integers(0, width, size=(groups, width), dtype=np.int64)
+
+
+@dataclass
+class BeamCase:
+    """Beam-search workload: per group a shared prompt, per beam a private
+    suffix, then one decode step after a seeded re-selection of parents."""
+    workload: Workload
+    suffix: np.ndarray           # [groups * width] suffix lengths
+    parents: np.ndarray          # [groups, width] parent beam of each new beam
+    prefix_k: torch.Tensor       # [groups, prefix, Hkv, D]
+    prefix_v: torch.Tensor
+    suffix_k: list               # per beam [suffix, Hkv, D]
+    suffix_v: list
+    q: torch.Tensor              # [groups * width, Hq, D]
+    new_key: torch.Tensor        # [groups * width, Hkv, D]
+    new_value: torch.Tensor
+    pool_blocks: int
+    pool_order: np.ndarray
+
+
+def make_beam_case(w: Workload, seed: int = 0, groups=None, prefix_len=None) -> BeamCase:
+    rng = np.random.default_rng(seed)
+    G = groups or w.beam_groups
+    W = w.beam_width
+    P = w.prefix_len if prefix_len is None else prefix_len
+    B, Hkv, D, Hq = w.block_size, w.num_kv_heads, w.head_dim, w.num_heads
+    suffix = rng.integers(0, 257, size=G * W, dtype=np.int64)
+    parents = beam_parents(rng, G, W)
+    need = G * blocks_for(P, B) + sum(blocks_for(P + n + 1, B) - blocks_for(P, B) + 1
+                                      for n in suffix)
+    NB = max(1, math.ceil(1.25 * need))
+    order = rng.permutation(NB)
+    dt = w.torch_dtype
+    prefix_k = normal_values(rng, (G, P, Hkv, D), dt)
+    prefix_v = normal_values(rng, (G, P, Hkv, D), dt)
+    suffix_k = [normal_values(rng, (int(n), Hkv, D), dt) for n in suffix]
+    suffix_v = [normal_values(rng, (int(n), Hkv, D), dt) for n in suffix]
+    q = normal_values(rng, (G * W, Hq, D), dt)
+    new_key = normal_values(rng, (G * W, Hkv, D), dt)
+    new_value = normal_values(rng, (G * W, Hkv, D), dt)
+    return BeamCase(w, suffix, parents, prefix_k, prefix_v, suffix_k, suffix_v, q, new_key,
+                    new_value, NB, order)
+
+
+def beam_setup_schedule(manager, case: BeamCase):
+    """Drive a block manager through the beam workload's history: each group's
+    prompt is appended token by token to a root sequence, the root is forked
+    into `width` beams (prompt blocks shared, count = width) and freed, and
+    each beam appends its private suffix.  Returns the slots of the prompt
+    tokens [groups, prefix] and of each beam's suffix tokens (list)."""
+    G, W = case.parents.shape
+    P = case.prefix_k.shape[1]
+    roots = [10_000 + g for g in range(G)]
+    for r in roots:
+        manager.add(r, 0)
+    prefix_slots = torch.empty((G, P), dtype=torch.int64)
+    for p in range(P):
+        slots, pairs = manager.step_append(roots)
+        assert len(pairs) == 0
+        prefix_slots[:, p] = torch.as_tensor(slots, dtype=torch.int64).reshape(-1)
+    for g in range(G):
+        for b in range(W):
+            manager.fork(roots[g], g * W + b)
+        manager.free_seq(roots[g])
+    suffix_slots = [[] for _ in range(G * W)]
+    remaining = [int(n) for n in case.suffix]
+    while any(remaining):
+        active = [i for i in range(G * W) if remaining[i] > 0]
+        slots, pairs = manager.step_append(active)
+        assert len(pairs) == 0
+        for i, sl in zip(active, torch.as_tensor(slots).reshape(-1).tolist()):
+            suffix_slots[i].append(sl)
+            remaining[i] -= 1
+    return prefix_slots, [torch.tensor(x, dtype=torch.int64) for x in suffix_slots]
+
+
+def beam_step_schedule(manager, case: BeamCase):
+    """Beam re-selection and one decode step: new beam b of group g is forked
+    from old beam parents[g, b], the old beams are freed, and every new beam
+    appends one token (a beam appending into a still-shared partial block
+    gets a copy first).  Returns (new beam ids, slots, cow pairs, tables, lens)."""
+    G, W = case.parents.shape
+    new_ids = [20_000 + i for i in range(G * W)]
+    for g in range(G):
+        for b in range(W):
+            manager.fork(g * W + int(case.parents[g, b]), new_ids[g * W + b])
+    for i in range(G * W):
+        manager.free_seq(i)
+    slots, pairs = manager.step_append(new_ids)
+    tables, lens = dense_tables(manager, new_ids)
+    return (new_ids, torch.as_tensor(slots, dtype=torch.int64).reshape(-1),
+            torch.as_tensor(pairs, dtype=torch.int64).reshape(-1, 2), tables, lens)
