@@ -153,6 +153,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over the ranks of the default process group (the
+    job's time is that of its slowest GPU)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -174,7 +184,7 @@ def run_gpu(args, rank, world, local_rank):
     __graft_entry__.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    st = Step(args.workload, args.seed, pkv.BlockAllocator)
+    st = Step(args.workload, args.seed + rank, pkv.BlockAllocator)  # independent problems
     w = st.w
     kc, vc = st.k_cache.to(dev), st.v_cache.to(dev)
     if st.setup_slots is not None:  # beam history
@@ -230,10 +240,7 @@ def run_gpu(args, rank, world, local_rank):
     clk = clocks.stop() if clocks else None
     total_ms = t0.elapsed_time(t1)
     attn_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
     assert pkv.device_status() == 0
 
