@@ -154,6 +154,39 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                   int max_context_len, int partition_size);
 
 /*
+ * paged_decode_attention_noalloc -- the split-context decode above
+ * (partition_size > 0 required) without a caller workspace.  The pages have
+ * no counterpart to this call; it exists for callers that cannot allocate
+ * device memory at all -- e.g. a plugin invoked from a host framework's
+ * execute step that forbids allocation there, a serving loop whose memory is
+ * carved up once at start-up by another allocator, or latency-critical code
+ * that cannot pay for cudaMalloc's possible device-wide synchronisation.
+ *
+ * The partition scratch lives in a fixed array inside libpkv's own device
+ * memory, PKV_NOALLOC_SCRATCH_BYTES (16 MiB) per GPU, held by every GPU that
+ * loads the library until the process exits.  Sizes whose scratch need
+ * (pkv_decode_workspace_bytes) exceeds it are rejected with
+ * PKV_ERR_WORKSPACE and a message giving both figures; nothing is launched.
+ * The call allocates nothing: no cudaMalloc / cudaFree, no allocating
+ * library routine.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls on a device share the one
+ * array, and it keeps the last call's contents (no clearing is needed: each
+ * call writes every scratch slot it reads before reading it), so calls that
+ * overlap on the GPU -- on different streams, or different threads -- race
+ * and give wrong results.  Arguments and results are otherwise those of
+ * pkv_paged_decode_attention.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+int pkv_paged_decode_attention_noalloc(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, float scale, int block_size,
+                                       int num_kv_heads, int num_seqs, int num_heads,
+                                       int head_dim, int max_blocks_per_seq, int num_blocks,
+                                       int kv_dtype, int out_dtype, int partition_size,
+                                       void* stream);
+
+/*
  * kv_copy_blocks -- copy-on-write copy of whole physical blocks.
  * [AUT section 3]: when a branch must modify a shared block that is not yet
  * full, copy-on-write keeps branches from overwriting each other; [AIPP key

@@ -32,6 +32,8 @@ _SIGS = {
     "pkv_paged_decode_attention": (_I, [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I,
                                         _I, _I, _I, _P, _SZ, _P]),
     "pkv_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_paged_decode_attention_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I,
+                                                _I, _I, _I, _I, _I, _P]),
     "pkv_kv_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pkv_set_decode_kernel": (_I, [_I]),
     "pkv_alloc_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
@@ -153,6 +155,28 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
         DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], int(partition_size), ws_ptr, ws_bytes,
         _stream(stream))
     _check(rc, "pkv_paged_decode_attention")
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                   block_size, num_kv_heads, partition_size, stream=None):
+    """Split-context decode whose scratch is the library's fixed device array
+    (for callers that cannot allocate device memory); see include/pkv.h."""
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = k_cache.shape
+    if (Hkv, B, Dk) != (num_kv_heads, block_size, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("paged_decode_attention_noalloc: cache shape mismatch")
+    if out.shape != q.shape or block_tables.dtype != torch.int32 or \
+            context_lens.dtype != torch.int32 or block_tables.shape[0] != S:
+        raise ValueError("paged_decode_attention_noalloc: bad out/table/length tensors")
+    rc = lib().pkv_paged_decode_attention_noalloc(
+        _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables"), _dev(context_lens, "context_lens"), float(scale),
+        int(block_size), int(num_kv_heads), S, Hq, D, block_tables.shape[1], NB,
+        DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], int(partition_size), _stream(stream))
+    _check(rc, "pkv_paged_decode_attention_noalloc")
 
 
 def kv_copy_blocks(k_cache, v_cache, pairs, stream=None):
