@@ -110,7 +110,7 @@ class Step:
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -124,7 +124,9 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def stop(self, t_begin=None, t_end=None):
+        """Stops sampling; summarises the samples taken between host wall
+        times t_begin and t_end (all samples if no window holds any)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -133,24 +135,28 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 8:
+            if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-            except ValueError:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                rows.append((ts, float(f[1]), float(f[2]),
+                             {n for n, v in zip(names, f[5:9]) if v.lower() == "active"}))
+            except (ValueError, IndexError):
                 continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        inside = [r for r in rows if t_begin is None or t_begin - 0.05 <= r[0] <= t_end + 0.05]
+        window = "timed region" if inside else "around the timed region"
+        use = inside or rows
+        if not use:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = set().union(*[r[3] for r in use])
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use), "reasons": sorted(reasons),
+                "samples": len(use), "window": window}
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -228,6 +234,7 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
+    wall0 = time.time()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -237,7 +244,8 @@ def run_gpu(args, rank, world, local_rank):
         ends[i].record(stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
-    clk = clocks.stop() if clocks else None
+    wall1 = time.time()
+    clk = clocks.stop(wall0, wall1) if clocks else None
     total_ms = t0.elapsed_time(t1)
     attn_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
     total_ms = max_over_ranks(total_ms, world)
@@ -361,8 +369,8 @@ def cpu_baseline(st, budget_s=8.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
