@@ -44,11 +44,12 @@ TRAFFIC = {"source_sha": None, "bytes_per_launch": {}}
 
 def launch_partition(w, max_blocks: int) -> int:
     """Partition size (tokens) the benchmark launches a workload with: the
-    workload's own split if it names one, else 512-token partitions for
-    contexts longer than that (balances ragged lengths across SMs)."""
+    workload's own split if it names one; else one pass per (sequence, KV
+    head) while every context fits in 2048 tokens, and 1024-token partitions
+    beyond (so that a few long contexts do not finish last)."""
     if w.partition_size:
         return w.partition_size
-    return 512 if max_blocks * w.block_size > 512 else 0
+    return 0 if max_blocks * w.block_size <= 2048 else 1024
 
 
 def kernel_sha() -> str:
@@ -63,7 +64,7 @@ def kernel_sha() -> str:
 class Step:
     """Host tensors of one decode step of a workload, plus its byte counts."""
 
-    def __init__(self, key: int, seed: int, allocator_cls):
+    def __init__(self, key: int, seed: int, allocator_cls, partition=None):
         w = WORKLOADS[key]
         self.w = w
         self.pairs = torch.zeros((0, 2), dtype=torch.int64)
@@ -95,7 +96,7 @@ class Step:
             else:
                 self.tables, self.lens = case.block_tables, case.context_lens
             self.unique_blocks = None
-        self.P = launch_partition(w, self.tables.shape[1])
+        self.P = launch_partition(w, self.tables.shape[1]) if partition is None else partition
         L = self.lens.to(torch.int64)
         b = w.torch_dtype.itemsize
         self.kv_bytes = int(L.sum()) * 2 * w.num_kv_heads * w.head_dim * b
@@ -190,7 +191,8 @@ def run_gpu(args, rank, world, local_rank):
     __graft_entry__.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    st = Step(args.workload, args.seed + rank, pkv.BlockAllocator)  # independent problems
+    st = Step(args.workload, args.seed + rank, pkv.BlockAllocator,  # independent problems
+              partition=args.partition)
     w = st.w
     kc, vc = st.k_cache.to(dev), st.v_cache.to(dev)
     if st.setup_slots is not None:  # beam history
@@ -218,8 +220,9 @@ def run_gpu(args, rank, world, local_rank):
         pkv.paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, w.block_size, w.num_kv_heads,
                                    partition_size=st.P, workspace=ws, stream=stream)
 
-    launches_per_step = (1 if pairs.shape[0] else 0) + (1 if has_write else 0) + \
-        (2 if st.P and bt.shape[1] * w.block_size > st.P else 1)
+    # one decode kernel per call (split mode also merges inside it, after a
+    # driver memset of its completion counters)
+    launches_per_step = (1 if pairs.shape[0] else 0) + (1 if has_write else 0) + 1
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -312,9 +315,9 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (tensor-core partition "
-                     "kernel + log-sum-exp merge)" if st.P else
-                     "paged_decode_attention (tensor-core kernel)",
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention call: tensor-core "
+                     "decode kernel with in-kernel log-sum-exp merge (+ counter memset)"
+                     if st.P else "paged_decode_attention (tensor-core kernel)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": tr,
                      "algorithmic_bytes_per_launch": st.attn_bytes,
@@ -373,6 +376,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--partition", type=int, default=None,
+                    help="partition size in tokens (default: the workload's launch setting)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

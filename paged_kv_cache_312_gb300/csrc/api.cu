@@ -40,7 +40,8 @@ static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 // ---------------------------------------------------------------------------
 // TMA tensor maps: a cache viewed as [NB*Hkv*B rows][D columns] of 16-bit
-// elements, loaded in boxes of 64 columns x B rows with the 128-byte swizzle.
+// elements, loaded in boxes of 64 columns x min(B, 16) rows with the 128-byte
+// swizzle.
 // Encoded maps are cached by (address, rows, D, B, dtype).
 // ---------------------------------------------------------------------------
 namespace {
@@ -90,7 +91,7 @@ int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtens
     g_map_next = (g_map_next + 1) % 16;
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)B};
+    cuuint32_t box[2] = {64, (cuuint32_t)(B < 16 ? B : 16)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(&m.map,
                           dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -113,12 +114,22 @@ int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtens
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Split workspace: (max, sum) pairs first, unnormalised outputs after.
-void carve_workspace(void* ws, size_t S, size_t H, size_t P, size_t D, float2** ml, float** o)
+// Split workspace, in order (each part 256-byte aligned):
+//   done : u32 [S][H]           partitions finished per (sequence, KV head)
+//   ml   : float2 [S][H][P]     per-partition (max, sum), base 2
+//   o    : float [S][H][P][D]   per-partition unnormalised output
+// with H the number of query heads (an upper bound for the KV heads).
+struct WorkspaceLayout {
+    size_t ml, o, total;
+};
+
+WorkspaceLayout workspace_layout(size_t S, size_t H, size_t P, size_t D)
 {
-    *ml = static_cast<float2*>(ws);
-    *o = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(S * H * P * sizeof(float2)));
-    (void)D;
+    WorkspaceLayout w;
+    w.ml = align256(S * H * sizeof(unsigned));
+    w.o = w.ml + align256(S * H * P * sizeof(float2));
+    w.total = w.o + S * H * P * D * sizeof(float);
+    return w;
 }
 
 }  // namespace
@@ -205,8 +216,7 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int
         max_context_len <= 0)
         return 0;
     const size_t P = ((size_t)max_context_len + partition_size - 1) / partition_size;
-    const size_t n = (size_t)num_seqs * num_heads * P;
-    return align256(n * sizeof(float2)) + n * head_dim * sizeof(float);
+    return workspace_layout(num_seqs, num_heads, P, head_dim).total;
 }
 
 int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -265,6 +275,7 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, co
     p.out_dtype = out_dtype;
     p.ws_ml = nullptr;
     p.ws_o = nullptr;
+    p.done = nullptr;
     const int max_ctx = max_blocks_per_seq * block_size;
     if (partition_size == 0) {
         p.partition_tokens = max_ctx;
@@ -279,8 +290,13 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, co
                             need, workspace ? workspace_bytes : (size_t)0);
         if (!aligned(workspace, 256))
             return pkv_fail(PKV_ERR_ALIGN, "%s: workspace needs 256-byte alignment", fn);
-        carve_workspace(workspace, num_seqs, num_heads, p.max_partitions, head_dim, &p.ws_ml,
-                        &p.ws_o);
+        if ((int64_t)p.max_partitions * num_heads >= (1ll << 31))
+            return pkv_fail(PKV_ERR_SHAPE, "%s: too many partitions", fn);
+        const WorkspaceLayout L = workspace_layout(num_seqs, num_heads, p.max_partitions, head_dim);
+        char* base = static_cast<char*>(workspace);
+        p.done = reinterpret_cast<unsigned*>(base);
+        p.ws_ml = reinterpret_cast<float2*>(base + L.ml);
+        p.ws_o = reinterpret_cast<float*>(base + L.o);
     }
     p.status = pkv_status_word_ptr();
     if (!p.status) return pkv_fail(PKV_ERR_CUDA, "%s: no device status word", fn);
@@ -296,10 +312,21 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, co
         int rc = tensor_map(k_cache, rows, head_dim, block_size, kv_dtype, &kmap);
         if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap);
         if (rc != PKV_OK) return rc;
-        e = launch_decode_tensor_core(p, kv_dtype, &kmap, &vmap, st);
-    } else {
-        e = launch_decode_cuda_core(p, kv_dtype, st);
+        // grid: every (sequence, KV head, partition) slot, partitions of one
+        // (sequence, KV head) adjacent; slots past a sequence's end exit at once
+        const long long grid = (long long)num_seqs * num_kv_heads * p.max_partitions;
+        if (grid >= (1ll << 31))
+            return pkv_fail(PKV_ERR_SHAPE, "%s: more than 2^31 work items", fn);
+        if (p.max_partitions > 1) {
+            // completion counters for the in-kernel merge start at zero
+            e = cudaMemsetAsync(p.done, 0, sizeof(unsigned) * (size_t)num_seqs * num_kv_heads, st);
+            if (e != cudaSuccess) return cuda_fail(e, "pkv_paged_decode_attention counter reset");
+        }
+        e = launch_decode_tensor_core(p, kv_dtype, &kmap, &vmap, grid, st);
+        if (e != cudaSuccess) return cuda_fail(e, "pkv_paged_decode_attention launch");
+        return PKV_OK;
     }
+    e = launch_decode_cuda_core(p, kv_dtype, st);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_paged_decode_attention launch");
     if (p.max_partitions > 1) {
         e = launch_lse_reduce(p, st);

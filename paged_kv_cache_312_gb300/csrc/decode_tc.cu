@@ -7,26 +7,33 @@
 // with k_i, v_i found through the block table.
 //
 // How (GB300 design):
-//  * One CTA = one (partition, KV head, sequence).  All G <= 8 query heads of
-//    the group ride along, so every K/V tile is read from HBM once per group
-//    (auturnal guide section 1: GQA/MQA shrink the KV head count).
-//  * Each (physical block, KV head) tile is B*D contiguous elements.  A 2-D
-//    TMA tensor map views a cache as [NB*Hkv*B rows][D cols]; one
-//    cp.async.bulk.tensor per 64-column half lands a tile in shared memory
-//    with the 128-byte swizzle, completing on an mbarrier.
-//  * Each warp owns a ring of NS stages and streams every NW-th stage of the
-//    partition; its lane 0 issues the loads NS stages ahead.
-//  * Q K^T runs on mma.sync m16n8k16 with tokens on M (16 per tile), the
-//    query heads of the group on N (8) and head_dim on K; the score fragment
-//    is turned into the P^T operand of the P V product by movmatrix (an 8x8
-//    transpose in registers), and P V accumulates O^T (head_dim x heads) in
-//    fp32.  P is split into a 16-bit high part and a 16-bit remainder so the
-//    product keeps ~16 significant bits.
-//  * Online softmax in base 2 with fp32 running max / sum per head; warps
-//    merge their states through shared memory at the end.
+//  * One CTA per (sequence, KV head, partition of <= P tokens); the slots of
+//    one (sequence, KV head) are adjacent in the grid and slots past a
+//    sequence's end exit at once.  All G <= 8 query heads of the KV group
+//    ride along, so every K/V tile is read from HBM once per group (auturnal
+//    guide section 1: GQA/MQA shrink the KV head count).
+//  * A stage is 16 tokens of K and V.  A 2-D TMA tensor map views a cache as
+//    [NB*Hkv*B rows][D cols]; one cp.async.bulk.tensor per 64-column half
+//    (and per block for B = 8) lands a stage in shared memory with the
+//    128-byte swizzle and completes on an mbarrier.  Each of the 4 warps
+//    streams every 4th stage through its own ring of NS stages; its lane 0
+//    issues loads NS stages ahead.  Block ids are fetched 32 stages at a time
+//    (one per lane) and broadcast by shuffle.  Three CTAs share an SM, so one
+//    CTA's start-up latency hides behind the others' streaming.
+//  * Q K^T runs on mma.sync m16n8k16 with tokens on M, the group's query heads
+//    on N (8) and head_dim on K; movmatrix turns the score fragment into the
+//    P^T operand of P V, which accumulates O^T in fp32.  P is split into a
+//    16-bit high part and a 16-bit remainder (~16 significant bits).
+//  * Online softmax in base 2 (fp32); the warps merge through shared memory
+//    (reusing the rings) at the end.  An unsplit item writes the output; a
+//    partition writes (max, sum, unnormalised output) to the workspace and
+//    bumps its (sequence, KV head) counter, and the CTA that finishes the
+//    last partition merges them all by log-sum-exp.
 //  * Masked tokens (past context_len, or in a block whose id is out of range)
 //    get score -inf and a zeroed V fragment, so NaN or stale data in unused
 //    slots never reaches the output.
+//  * Every wait is bounded (~1 s); a wait that gives up sets the TIMEOUT
+//    status bit, which makes every other wait give up at once.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -36,8 +43,6 @@
 #include "pkv_kernels.h"
 
 namespace {
-
-constexpr int kWarps = 4;
 
 // ---- PTX wrappers -----------------------------------------------------------
 
@@ -196,62 +201,58 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t x, bool keep_lo, bool kee
 
 // ---- compile-time geometry -----------------------------------------------------
 
-template <int D, int B>
+template <int D, int B, int NW, int NS>
 struct Geometry {
-    static constexpr int SB = B >= 16 ? 1 : 16 / B;      // physical blocks per stage
-    static constexpr int ST = SB * B;                    // tokens per stage
-    static constexpr int TILES = ST / 16;                // 16-token mma tiles per stage
-    static constexpr int NH = D / 64;                    // 128-byte column halves
-    static constexpr int HALF_BYTES = B * 128;           // one block, one half
-    static constexpr int BLOCK_BYTES = NH * HALF_BYTES;  // one block of K (or V)
-    static constexpr int KV_BYTES = SB * BLOCK_BYTES;    // K (or V) part of a stage
+    static constexpr int ROWS = B < 16 ? B : 16;     // rows per TMA box
+    static constexpr int IDS = 16 / ROWS;            // physical blocks per 16-token stage
+    static constexpr int NH = D / 64;                // 128-byte column halves
+    static constexpr int SUB_BYTES = ROWS * 128;     // one box
+    static constexpr int KV_BYTES = 16 * D * 2;      // K (or V) of a 16-token stage
     static constexpr int STAGE_BYTES = 2 * KV_BYTES;
-    // ring depth: ~24-32 KB of loads in flight per warp
-    static constexpr int NS = STAGE_BYTES >= 16384 ? 2 : 3;
     static constexpr int RING_BYTES = NS * STAGE_BYTES;
-    static constexpr int MERGE_BYTES = kWarps * 8 * (D + 2) * 4;
+    static constexpr int MERGE_BYTES = NW * 8 * (D + 2) * 4;
     static constexpr int DATA_BYTES =
-        (kWarps * RING_BYTES > MERGE_BYTES ? kWarps * RING_BYTES : MERGE_BYTES);
-    static constexpr int SMEM_BYTES =
-        1024 /*align slack*/ + DATA_BYTES + kWarps * NS * 8 /*barriers*/ + kWarps * NS * SB * 4;
-    static_assert(HALF_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
+        NW * RING_BYTES > MERGE_BYTES ? NW * RING_BYTES : MERGE_BYTES;  // merge reuses rings
+    static constexpr int BAR_OFF = DATA_BYTES;
+    static constexpr int SID_OFF = BAR_OFF + NW * NS * 8;
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + SID_OFF + NW * NS * 2 * 4;
+    // partition weights cached for the in-kernel merge (after the warp merge)
+    static constexpr int WCACHE = ((DATA_BYTES - MERGE_BYTES) / 4 - 16 - NW * 32 * 4 - 4) & ~3;
+    static_assert(WCACHE > 0, "room for merge weights");
+    static_assert(SUB_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
+    static_assert(STAGE_BYTES % 1024 == 0 && RING_BYTES % 1024 == 0, "stage alignment");
 };
 
-// Shared-memory byte offset of (token row r of the 16-token tile, 16-byte
-// chunk c of the head_dim row) inside a K or V stage buffer, honouring the
-// 128-byte swizzle the TMA applied (chunk index XOR row % 8).
-template <int D, int B>
-__device__ __forceinline__ uint32_t tile_offset(int tile, int r, int c)
+// Shared-memory offset of (token row r of the stage, 16-byte chunk c of the
+// head_dim row) in a K or V stage buffer laid out [block][half][row][128 B],
+// honouring the 128-byte swizzle (chunk XOR row % 8).
+template <int D, int B, int NW, int NS>
+__device__ __forceinline__ uint32_t stage_offset(int r, int c)
 {
-    using Gm = Geometry<D, B>;
-    const int tok = tile * 16 + r;       // token within the stage
-    const int u = tok / B;               // physical block within the stage
-    const int row = tok % B;             // row within the block
+    using Gm = Geometry<D, B, NW, NS>;
+    const int u = r / Gm::ROWS, row = r % Gm::ROWS;
     const int half = c >> 3, cc = c & 7;
-    return u * Gm::BLOCK_BYTES + half * Gm::HALF_BYTES + row * 128 + ((cc ^ (row & 7)) << 4);
+    return (u * Gm::NH + half) * Gm::SUB_BYTES + row * 128 + ((cc ^ (row & 7)) << 4);
 }
 
-template <typename T, int D, int B>
-__global__ void __launch_bounds__(kWarps * 32)
+// One CTA = one work item (a partition of one (sequence, KV head)); NW warps
+// each stream every NW-th 16-token stage of it through their own ring of NS
+// stages, and merge their softmax states at the end.
+template <typename T, int D, int B, int NW, int NS>
+__global__ void __launch_bounds__(NW * 32)
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap)
 {
-    using Gm = Geometry<D, B>;
-    constexpr int NS = Gm::NS;
-    constexpr int KSTEPS = D / 16;  // QK^T k-steps
-    constexpr int MTILES = D / 16;  // PV m-tiles (head_dim rows)
+    using Gm = Geometry<D, B, NW, NS>;
+    constexpr int KSTEPS = D / 16;  // Q K^T k-steps
+    constexpr int MTILES = D / 16;  // P V m-tiles (head_dim rows)
+    constexpr int IDS = Gm::IDS;    // physical blocks per stage (2 when B = 8)
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::DATA_BYTES);
-    int* sid = reinterpret_cast<int*>(bars + kWarps * NS);  // block ids per [warp][slot][unit]
-
-    const int part = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gq = lane >> 2, tq = lane & 3;  // mma fragment row group / column pair
-
-    // ---- extent of this CTA's work
+    // ---- which item: slot b = ((s * Hkv) + g) * max_partitions + part
+    const int part = blockIdx.x % p.max_partitions;
+    const int sg = blockIdx.x / p.max_partitions;
+    const int s = sg / p.num_kv_heads;
+    const int g = sg - s * p.num_kv_heads;
     int L = p.context_lens[s];
     if (L < 0 || (int64_t)L > (int64_t)p.max_blocks * B) {
         if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
@@ -261,13 +262,20 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     if (part >= (nparts > 0 ? nparts : 1)) return;
     const int begin = part * p.partition_tokens;
     const int end = min(L, begin + p.partition_tokens);
-    const int nblk = end > begin ? (end - begin + B - 1) / B : 0;
-    const int nst = (nblk + Gm::SB - 1) / Gm::SB;
-    const int first_blk = begin / B;
+    const int nst = end > begin ? (end - begin + 15) / 16 : 0;
     const int G = p.num_heads / p.num_kv_heads;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::BAR_OFF);
+    int* sid = reinterpret_cast<int*>(smem + Gm::SID_OFF);  // [warp][slot][2] block ids
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tq = lane & 3;  // mma fragment row group / column pair
+    uint8_t* ring = smem + warp * Gm::RING_BYTES;
     const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
 
-    // ---- barriers
     if (lane == 0) {
         for (int i = 0; i < NS; ++i) mbar_init(smem_u32(&bars[warp * NS + i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -275,22 +283,20 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     }
     __syncwarp();
 
-    // ---- this warp's stages: gs = warp + j * kWarps, j < cnt
-    const int cnt = nst > warp ? (nst - warp + kWarps - 1) / kWarps : 0;
-    uint8_t* ring = smem + warp * Gm::RING_BYTES;
-
-    // Block ids of this warp's next 32 stages, one (or SB) per lane.
+    // ---- this warp's stages: q = warp + j * NW, j < cnt
+    const int cnt = nst > warp ? (nst - warp + NW - 1) / NW : 0;
     int win_base = 0;
-    int win_ids[Gm::SB];
+    int win_ids[IDS];
+    // Block ids of this warp's stages jbase .. jbase+31, one per lane.
     auto load_window = [&](int jbase) {
         win_base = jbase;
+        const int j = jbase + lane;
 #pragma unroll
-        for (int u = 0; u < Gm::SB; ++u) {
-            const int j = jbase + lane;
-            const int b = (warp + j * kWarps) * Gm::SB + u;  // block within partition
+        for (int u = 0; u < IDS; ++u) {
             int id = -1;
-            if (j < cnt && b < nblk) {
-                id = table[first_blk + b];
+            const int tok = begin + (warp + j * NW) * 16 + u * B;  // first token of the box
+            if (j < cnt && tok < end) {
+                id = table[tok / B];
                 if (id < 0 || id >= p.num_blocks) {
                     atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
                     id = -1;
@@ -299,43 +305,44 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             win_ids[u] = id;
         }
     };
-    // Block id of stage j, unit u (all lanes call; win_base <= j < win_base + 32).
-    auto stage_id = [&](int j, int u) { return __shfl_sync(0xffffffffu, win_ids[u], j - win_base); };
-
-    // Starts the loads of stage j into slot j % NS and records its block ids
-    // for the consumer.  Called by the whole warp.
+    // Starts the loads of stage j into slot j % NS (whole warp calls).
     auto issue = [&](int j) {
-        int ids[Gm::SB];
+        int ids[IDS];
 #pragma unroll
-        for (int u = 0; u < Gm::SB; ++u) ids[u] = stage_id(j, u);
+        for (int u = 0; u < IDS; ++u) ids[u] = __shfl_sync(0xffffffffu, win_ids[u], j - win_base);
         if (lane == 0) {
             const int slot = j % NS;
-#pragma unroll
-            for (int u = 0; u < Gm::SB; ++u) sid[(warp * NS + slot) * Gm::SB + u] = ids[u];
+            sid[(warp * NS + slot) * 2 + 0] = ids[0];
+            sid[(warp * NS + slot) * 2 + 1] = ids[IDS - 1];
             const uint32_t bar = smem_u32(&bars[warp * NS + slot]);
             const uint32_t kdst = smem_u32(ring + slot * Gm::STAGE_BYTES);
             const uint32_t vdst = kdst + Gm::KV_BYTES;
+            const int tok0 = begin + (warp + j * NW) * 16;
             uint32_t bytes = 0;
 #pragma unroll
-            for (int u = 0; u < Gm::SB; ++u)
-                if (ids[u] >= 0) bytes += 2 * Gm::BLOCK_BYTES;
+            for (int u = 0; u < IDS; ++u)
+                if (ids[u] >= 0) bytes += 2 * Gm::NH * Gm::SUB_BYTES;
             fence_proxy_async();
             mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
-            for (int u = 0; u < Gm::SB; ++u) {
+            for (int u = 0; u < IDS; ++u) {
                 if (ids[u] < 0) continue;
-                const int row = (ids[u] * p.num_kv_heads + g) * B;
+                // B >= 16: one 16-row box at the stage's offset in its block;
+                // B == 8: one 8-row box per block.
+                const int row = (ids[u] * p.num_kv_heads + g) * B + (IDS > 1 ? 0 : tok0 % B);
 #pragma unroll
                 for (int hf = 0; hf < Gm::NH; ++hf) {
-                    const uint32_t off = u * Gm::BLOCK_BYTES + hf * Gm::HALF_BYTES;
+                    const uint32_t off = (u * Gm::NH + hf) * Gm::SUB_BYTES;
                     tma_load_2d(kdst + off, &kmap, hf * 64, row, bar);
                     tma_load_2d(vdst + off, &vmap, hf * 64, row, bar);
                 }
             }
         }
+        __syncwarp();
     };
 
     if (cnt > 0) load_window(0);
+    for (int j = 0; j < NS && j < cnt; ++j) issue(j);
 
     // ---- Q^T as the B operand of Q K^T: column n = query head g*G + n.
     uint32_t qb[KSTEPS][2];
@@ -353,18 +360,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         }
     }
 
-    // prologue
-    for (int j = 0; j < NS && j < cnt; ++j) issue(j);
-    __syncwarp();
-
-    // running state for heads 2*tq and 2*tq+1
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2tq, 2tq+1
     float acc[MTILES][4];
 #pragma unroll
     for (int i = 0; i < MTILES; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     const float sl = p.scale_log2;
-
-    // per-lane ldmatrix row/chunk assignments
     const int lj = lane >> 3, lr = lane & 7;
     const int k_row = (lj & 1) * 8 + lr, k_chunk_add = lj >> 1;  // K: non-transposed A
     const int v_row = (lj >> 1) * 8 + lr, v_chunk_add = lj & 1;  // V: transposed A
@@ -373,98 +373,87 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         const int slot = j % NS;
         const uint32_t bar = smem_u32(&bars[warp * NS + slot]);
         if (!mbar_wait_bounded(bar, (j / NS) & 1, p.status)) {
-            // The copies of this stage never landed: flag, stop issuing, and
-            // give the ones still outstanding a bounded wait before leaving.
+            // The copies of this stage never landed: flag, stop, and give the
+            // ones still outstanding a bounded wait before leaving.
             if (lane == 0) atomicOr(p.status, PKV_STATUS_TIMEOUT);
             for (int jj = j + 1; jj < j + NS && jj < cnt; ++jj)
                 mbar_wait_bounded(smem_u32(&bars[warp * NS + jj % NS]), (jj / NS) & 1, p.status);
             break;
         }
-        const int gs = warp + j * kWarps;
-        int ids[Gm::SB];
-#pragma unroll
-        for (int u = 0; u < Gm::SB; ++u) ids[u] = sid[(warp * NS + slot) * Gm::SB + u];
+        const int id0 = sid[(warp * NS + slot) * 2 + 0];
+        const int id1 = sid[(warp * NS + slot) * 2 + 1];
         const uint32_t kbase = smem_u32(ring + slot * Gm::STAGE_BYTES);
         const uint32_t vbase = kbase + Gm::KV_BYTES;
-        const int stage_tok0 = begin + gs * Gm::ST;
+        const int tok0 = begin + (warp + j * NW) * 16;
+        auto valid = [&](int r) {
+            return tok0 + r < end && ((IDS > 1 && r >= B) ? id1 : id0) >= 0;
+        };
+        const bool all_valid = tok0 + 16 <= end && id0 >= 0 && id1 >= 0;
 
+        // ---- S^T = K Q^T  (16 tokens x 8 heads)
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int tile = 0; tile < Gm::TILES; ++tile) {
-            const int tok0 = stage_tok0 + tile * 16;
-            // validity of this lane's score rows (tokens gq and gq + 8)
-            auto valid = [&](int r) {
-                const int u = (tile * 16 + r) / B;
-                return tok0 + r < end && ids[u] >= 0;
-            };
-            const bool all_valid = tok0 + 16 <= end && (Gm::SB == 1 ? ids[0] >= 0 : (ids[0] >= 0 && ids[Gm::SB - 1] >= 0));
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(kbase + stage_offset<D, B, NW, NS>(k_row, 2 * kk + k_chunk_add), a);
+            Mma<T>::run(sc, a, qb[kk][0], qb[kk][1]);
+        }
+        float x0 = sc[0] * sl, x1 = sc[1] * sl, x2 = sc[2] * sl, x3 = sc[3] * sl;
+        if (!all_valid) {
+            if (!valid(gq)) x0 = x1 = -INFINITY;
+            if (!valid(gq + 8)) x2 = x3 = -INFINITY;
+        }
+        // ---- online softmax (per head: reduce over the 8 row groups)
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);  // 0 while m is -inf
+        m0 = mn0;
+        m1 = mn1;
+        const float p0 = ex2(x0 - ms0), p1 = ex2(x1 - ms1);
+        const float p2 = ex2(x2 - ms0), p3 = ex2(x3 - ms1);
+        l0 = l0 * al0 + p0 + p2;
+        l1 = l1 * al1 + p1 + p3;
+#pragma unroll
+        for (int i = 0; i < MTILES; ++i) {
+            acc[i][0] *= al0;
+            acc[i][1] *= al1;
+            acc[i][2] *= al0;
+            acc[i][3] *= al1;
+        }
+        // ---- P^T operand (tokens 2tq.. x head gq) via an in-register transpose
+        uint32_t h01, l01, h23, l23;
+        Mma<T>::split(p0, p1, h01, l01);
+        Mma<T>::split(p2, p3, h23, l23);
+        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
 
-            // ---- S^T = K Q^T  (16 tokens x 8 heads)
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        bool v0 = true, v1 = true, v8 = true, v9 = true;
+        if (!all_valid) {
+            v0 = valid(2 * tq);
+            v1 = valid(2 * tq + 1);
+            v8 = valid(2 * tq + 8);
+            v9 = valid(2 * tq + 9);
+        }
+        // ---- O^T += V^T P^T
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                uint32_t a[4];
-                ldsm_x4(kbase + tile_offset<D, B>(tile, k_row, 2 * kk + k_chunk_add), a);
-                Mma<T>::run(sc, a, qb[kk][0], qb[kk][1]);
-            }
-            float x0 = sc[0] * sl, x1 = sc[1] * sl, x2 = sc[2] * sl, x3 = sc[3] * sl;
+        for (int i = 0; i < MTILES; ++i) {
+            uint32_t a[4];
+            ldsm_x4_trans(vbase + stage_offset<D, B, NW, NS>(v_row, 2 * i + v_chunk_add), a);
             if (!all_valid) {
-                if (!valid(gq)) x0 = x1 = -INFINITY;
-                if (!valid(gq + 8)) x2 = x3 = -INFINITY;
+                a[0] = mask_pair(a[0], v0, v1);
+                a[1] = mask_pair(a[1], v0, v1);
+                a[2] = mask_pair(a[2], v8, v9);
+                a[3] = mask_pair(a[3], v8, v9);
             }
-            // ---- online softmax (per head: reduce over the 8 row groups)
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);  // 0 while m is -inf
-            m0 = mn0;
-            m1 = mn1;
-            const float p0 = ex2(x0 - ms0), p1 = ex2(x1 - ms1);
-            const float p2 = ex2(x2 - ms0), p3 = ex2(x3 - ms1);
-            l0 = l0 * al0 + p0 + p2;
-            l1 = l1 * al1 + p1 + p3;
-#pragma unroll
-            for (int i = 0; i < MTILES; ++i) {
-                acc[i][0] *= al0;
-                acc[i][1] *= al1;
-                acc[i][2] *= al0;
-                acc[i][3] *= al1;
-            }
-            // ---- P^T operand: rows gq / gq+8 (tokens) x cols 2tq.. (heads),
-            // transposed in registers to (tokens 2tq.. x head gq)
-            uint32_t h01, l01, h23, l23;
-            Mma<T>::split(p0, p1, h01, l01);
-            Mma<T>::split(p2, p3, h23, l23);
-            const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-            const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-
-            // V fragment tokens held by this lane: 2tq, 2tq+1 (regs 0,1), +8 (regs 2,3)
-            bool v0 = true, v1 = true, v8 = true, v9 = true;
-            if (!all_valid) {
-                v0 = valid(2 * tq);
-                v1 = valid(2 * tq + 1);
-                v8 = valid(2 * tq + 8);
-                v9 = valid(2 * tq + 9);
-            }
-            // ---- O^T += V^T P^T
-#pragma unroll
-            for (int i = 0; i < MTILES; ++i) {
-                uint32_t a[4];
-                ldsm_x4_trans(vbase + tile_offset<D, B>(tile, v_row, 2 * i + v_chunk_add), a);
-                if (!all_valid) {
-                    a[0] = mask_pair(a[0], v0, v1);
-                    a[1] = mask_pair(a[1], v0, v1);
-                    a[2] = mask_pair(a[2], v8, v9);
-                    a[3] = mask_pair(a[3], v8, v9);
-                }
-                Mma<T>::run(acc[i], a, bh0, bh1);
-                Mma<T>::run(acc[i], a, bl0, bl1);
-            }
+            Mma<T>::run(acc[i], a, bh0, bh1);
+            Mma<T>::run(acc[i], a, bl0, bl1);
         }
         __syncwarp();
         if (j + NS < cnt) {
@@ -482,84 +471,177 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
 
     // ---- merge the warps (shared memory reused once every ring is drained)
     __syncthreads();
-    float* sm_m = reinterpret_cast<float*>(smem);            // [kWarps][8]
-    float* sm_l = sm_m + kWarps * 8;                         // [kWarps][8]
-    float* sm_o = sm_l + kWarps * 8;                         // [kWarps][8][D]
+    float* wm = reinterpret_cast<float*>(smem) + warp * 8 * (D + 2);  // [8][D], m[8], l[8]
     if (gq == 0) {
-        sm_m[warp * 8 + 2 * tq] = m0;
-        sm_m[warp * 8 + 2 * tq + 1] = m1;
-        sm_l[warp * 8 + 2 * tq] = l0;
-        sm_l[warp * 8 + 2 * tq + 1] = l1;
+        wm[8 * D + 2 * tq] = m0;
+        wm[8 * D + 2 * tq + 1] = m1;
+        wm[8 * D + 8 + 2 * tq] = l0;
+        wm[8 * D + 8 + 2 * tq + 1] = l1;
     }
 #pragma unroll
     for (int i = 0; i < MTILES; ++i) {
-        float* o = sm_o + (size_t)warp * 8 * D;
-        o[(2 * tq) * D + 16 * i + gq] = acc[i][0];
-        o[(2 * tq + 1) * D + 16 * i + gq] = acc[i][1];
-        o[(2 * tq) * D + 16 * i + gq + 8] = acc[i][2];
-        o[(2 * tq + 1) * D + 16 * i + gq + 8] = acc[i][3];
+        wm[(2 * tq) * D + 16 * i + gq] = acc[i][0];
+        wm[(2 * tq + 1) * D + 16 * i + gq] = acc[i][1];
+        wm[(2 * tq) * D + 16 * i + gq + 8] = acc[i][2];
+        wm[(2 * tq + 1) * D + 16 * i + gq + 8] = acc[i][3];
     }
     __syncthreads();
-
+    const float* sm = reinterpret_cast<const float*>(smem);
+    const size_t hbase = (size_t)s * p.num_heads + (size_t)g * G;
     for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int n = idx / D, d = idx % D;
+        const int n = idx / D, d = idx - n * D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 8 + n]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * 8 * (D + 2) + 8 * D + n]);
         float den = 0.f, num = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float wt = (sm_m[w * 8 + n] == -INFINITY) ? 0.f : ex2(sm_m[w * 8 + n] - M);
-            den += wt * sm_l[w * 8 + n];
-            num += wt * sm_o[((size_t)w * 8 + n) * D + d];
+        for (int w = 0; w < NW; ++w) {
+            const float* ww = sm + w * 8 * (D + 2);
+            const float mw = ww[8 * D + n];
+            const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
+            den += wt * ww[8 * D + 8 + n];
+            num += wt * ww[n * D + d];
         }
-        const int h = g * G + n;
         if (nparts <= 1) {
-            store_out(p.out, ((size_t)s * p.num_heads + h) * D + d, den > 0.f ? num / den : 0.f,
-                      p.out_dtype);
+            store_out(p.out, (hbase + n) * D + d, den > 0.f ? num / den : 0.f, p.out_dtype);
         } else {
-            const size_t slot = ((size_t)s * p.num_heads + h) * p.max_partitions + part;
+            const size_t slot = (hbase + n) * p.max_partitions + part;
             p.ws_o[slot * D + d] = num;
             if (d == 0) p.ws_ml[slot] = make_float2(M, den);
+        }
+    }
+    if (nparts <= 1) return;
+
+    // ---- split: the CTA that finishes the last partition of (s, g) merges
+    // them by log-sum-exp: M = max_i m_i, w_i = 2^(m_i - M),
+    // out = sum_i w_i O_i / sum_i w_i l_i.
+    __shared__ int is_last;
+    __syncthreads();  // this CTA's partition results are written ...
+    if (threadIdx.x == 0) {
+        __threadfence();  // ... and published before the count goes up
+        is_last = atomicAdd(&p.done[sg], 1u) == (unsigned)nparts - 1;
+        if (is_last) __threadfence();  // see every other partition's results
+    }
+    __syncthreads();
+    if (!is_last) return;
+    constexpr int NT = NW * 32;
+    float* wts = reinterpret_cast<float*>(smem) + NW * 8 * (D + 2);  // [G][nparts] weights
+    float* hinv = wts + Gm::WCACHE;                                    // [8]
+    float* hmax = hinv + 8;                                            // [8]
+    float4* red = reinterpret_cast<float4*>(hmax + 8);                 // [NT] partial sums
+    const bool cached = G * nparts <= Gm::WCACHE;
+    for (int n = warp; n < G; n += NW) {
+        const size_t base = (hbase + n) * p.max_partitions;
+        float M = -INFINITY;
+        for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(&p.ws_ml[base + i]).x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float den = 0.f;
+        for (int i = lane; i < nparts; i += 32) {
+            const float2 ml = __ldcg(&p.ws_ml[base + i]);
+            const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+            if (cached) wts[n * nparts + i] = w;
+            den += w * ml.y;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (lane == 0) {
+            hmax[n] = M;
+            hinv[n] = den > 0.f ? 1.f / den : 0.f;
+        }
+    }
+    __syncthreads();
+    // Outputs in float4 units; when the group has fewer of them than
+    // threads, K threads share one output, each summing every K-th partition.
+    const int O4 = G * D / 4;
+    const int K = O4 >= NT ? 1 : NT / O4;
+    for (int o0 = 0; o0 < O4; o0 += NT) {
+        const int t = threadIdx.x;
+        const int o = o0 + (K == 1 ? t : t % O4), k = K == 1 ? 0 : t / O4;
+        float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        const bool active = o < O4 && k < K;
+        if (active) {
+            const int n = o / (D / 4), d4 = o - n * (D / 4);
+            const size_t base = (hbase + n) * p.max_partitions;
+            const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * D) + d4;
+#pragma unroll 8
+            for (int i = k; i < nparts; i += K) {
+                float w;
+                if (cached) {
+                    w = wts[n * nparts + i];
+                } else {
+                    const float mi = __ldcg(&p.ws_ml[base + i]).x;
+                    w = mi == -INFINITY ? 0.f : ex2(mi - hmax[n]);
+                }
+                const float4 v = __ldcg(src + (size_t)i * (D / 4));
+                acc4.x += w * v.x;
+                acc4.y += w * v.y;
+                acc4.z += w * v.z;
+                acc4.w += w * v.w;
+            }
+        }
+        if (K > 1) {
+            red[t] = acc4;
+            __syncthreads();
+            if (k == 0 && active) {
+                for (int kk = 1; kk < K; ++kk) {
+                    const float4 r = red[t + kk * O4];
+                    acc4.x += r.x;
+                    acc4.y += r.y;
+                    acc4.z += r.z;
+                    acc4.w += r.w;
+                }
+            }
+        }
+        if (k == 0 && active) {
+            const int n = o / (D / 4), d = (o - n * (D / 4)) * 4;
+            const float inv = hinv[n];
+            const size_t at = (hbase + n) * D + d;
+            store_out(p.out, at + 0, acc4.x * inv, p.out_dtype);
+            store_out(p.out, at + 1, acc4.y * inv, p.out_dtype);
+            store_out(p.out, at + 2, acc4.z * inv, p.out_dtype);
+            store_out(p.out, at + 3, acc4.w * inv, p.out_dtype);
         }
     }
 }
 
 template <typename T, int D, int B>
-cudaError_t launch_tc(const DecodeParams& p, const void* kmap, const void* vmap,
+cudaError_t launch_tc(const DecodeParams& p, const void* kmap, const void* vmap, long long grid,
                       cudaStream_t stream)
 {
-    using Gm = Geometry<D, B>;
-    auto kern = decode_tc_kernel<T, D, B>;
+    // 4 warps x 2-stage rings: 64 KB (D = 128) per CTA, three CTAs per SM,
+    // up to 192 KB of tile loads in flight per SM
+    constexpr int NW = 4, NS = 2;
+    using Gm = Geometry<D, B, NW, NS>;
+    auto kern = decode_tc_kernel<T, D, B, NW, NS>;
     // set on every launch: the attribute belongs to the current device's copy
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.max_partitions, p.num_kv_heads, p.num_seqs);
-    kern<<<grid, kWarps * 32, Gm::SMEM_BYTES, stream>>>(
+    kern<<<(unsigned)grid, NW * 32, Gm::SMEM_BYTES, stream>>>(
         p, *static_cast<const CUtensorMap*>(kmap), *static_cast<const CUtensorMap*>(vmap));
     return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_tc_dtype(const DecodeParams& p, const void* kmap, const void* vmap,
-                            cudaStream_t stream)
+                            long long grid, cudaStream_t stream)
 {
     if (p.head_dim == 128) {
-        if (p.block_size == 16) return launch_tc<T, 128, 16>(p, kmap, vmap, stream);
-        if (p.block_size == 32) return launch_tc<T, 128, 32>(p, kmap, vmap, stream);
-        return launch_tc<T, 128, 8>(p, kmap, vmap, stream);
+        if (p.block_size == 16) return launch_tc<T, 128, 16>(p, kmap, vmap, grid, stream);
+        if (p.block_size == 32) return launch_tc<T, 128, 32>(p, kmap, vmap, grid, stream);
+        return launch_tc<T, 128, 8>(p, kmap, vmap, grid, stream);
     }
-    if (p.block_size == 16) return launch_tc<T, 64, 16>(p, kmap, vmap, stream);
-    if (p.block_size == 32) return launch_tc<T, 64, 32>(p, kmap, vmap, stream);
-    return launch_tc<T, 64, 8>(p, kmap, vmap, stream);
+    if (p.block_size == 16) return launch_tc<T, 64, 16>(p, kmap, vmap, grid, stream);
+    if (p.block_size == 32) return launch_tc<T, 64, 32>(p, kmap, vmap, grid, stream);
+    return launch_tc<T, 64, 8>(p, kmap, vmap, grid, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_tensor_core(const DecodeParams& p, int kv_dtype, const void* k_map,
-                                      const void* v_map, cudaStream_t stream)
+                                      const void* v_map, long long grid, cudaStream_t stream)
 {
-    if (kv_dtype == PKV_BF16) return launch_tc_dtype<__nv_bfloat16>(p, k_map, v_map, stream);
-    return launch_tc_dtype<__half>(p, k_map, v_map, stream);
+    if (kv_dtype == PKV_BF16) return launch_tc_dtype<__nv_bfloat16>(p, k_map, v_map, grid, stream);
+    return launch_tc_dtype<__half>(p, k_map, v_map, grid, stream);
 }

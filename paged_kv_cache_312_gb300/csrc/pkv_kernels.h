@@ -23,6 +23,7 @@ struct DecodeParams {
     int out_dtype;
     float2* ws_ml;               // [S][Hq][max_partitions] (max, sum) in base 2
     float* ws_o;                 // [S][Hq][max_partitions][D] unnormalised output
+    unsigned int* done;          // [S][Hkv] partitions finished (tensor-core split mode)
     unsigned int* status;        // device status word (PKV_STATUS_* bits)
 };
 
@@ -41,11 +42,14 @@ cudaError_t launch_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* p
 // CUDA-core decode (any dtype, any group size).  Grid: partitions x heads x seqs.
 cudaError_t launch_decode_cuda_core(const DecodeParams& p, int kv_dtype, cudaStream_t stream);
 
-// Tensor-core decode (16-bit KV, group size <= 8).  The tensor maps describe
-// k_cache / v_cache as 2-D [NB*Hkv*B rows][D columns] for tile loads.
-cudaError_t launch_decode_tensor_core(const DecodeParams& p, int kv_dtype,
-                                      const void* k_map, const void* v_map,
-                                      cudaStream_t stream);
+// Tensor-core decode (16-bit KV, group size <= 8), one CTA per (sequence,
+// KV head, partition), partitions of one (sequence, KV head) adjacent in the
+// grid.  The tensor maps describe k_cache / v_cache as 2-D [NB*Hkv*B rows]
+// [D columns] loaded in boxes of 64 columns x min(B, 16) rows.  In split mode
+// p.done must be zero; the CTA that finishes the last partition of a
+// (sequence, KV head) merges its partitions.
+cudaError_t launch_decode_tensor_core(const DecodeParams& p, int kv_dtype, const void* k_map,
+                                      const void* v_map, long long grid, cudaStream_t stream);
 
 // Log-sum-exp merge of split partitions (only sequences with > 1 partition).
 cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);

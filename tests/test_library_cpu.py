@@ -78,9 +78,10 @@ def test_decode_with_no_sequences_is_a_no_op():
 def test_workspace_size_formula():
     L = pkv.lib()
     assert L.pkv_decode_workspace_bytes(8, 32, 128, 32768, 0) == 0
-    n = 8 * 32 * 64
-    expect = ((n * 8 + 255) // 256) * 256 + n * 128 * 4
-    assert L.pkv_decode_workspace_bytes(8, 32, 128, 32768, 512) == expect
+    S, H, P, D = 8, 32, 64, 128
+    a = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    expect = a(S * H * 4) + a(S * H * P * 8) + S * H * P * D * 4
+    assert L.pkv_decode_workspace_bytes(S, H, D, 32768, 512) == expect
 
 
 def test_write_and_copy_reject_bad_arguments_on_host():

@@ -217,6 +217,21 @@ def test_split_matches_one_pass_and_kernels_agree():
             assert max_err(out, ref) <= TOL16, (P, kernel)
 
 
+def test_split_with_thousands_of_partitions():
+    # 1500 and 1875 partitions of 16 tokens: more merge weights than the
+    # decode kernel keeps in shared memory, so the merge recomputes them.
+    w = Workload(0, "many", "bf16", 16, 2, 128, 16, 3, "fixed")
+    case = make_decode_case(w, seed=13, lengths=[24000, 30000, 17])
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, 16, 2)
+    for P in (16, 32, 4096):
+        out = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, 16, 2,
+                         P=P)
+        assert pkv.device_status() == 0
+        assert max_err(out, ref) <= TOL16, P
+
+
 def test_nan_poison_and_physical_permutation():
     # Same logical data paged twice with different physical ids: same output.
     w = Workload(0, "perm", "f16", 16, 4, 128, 16, 4, "fixed")
