@@ -37,9 +37,11 @@ from workloads import (WORKLOADS, make_beam_case, make_decode_case, poison_unuse
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak), decode steps/sec"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per launch of the tensor-core decode kernel from one ncu capture,
+# DRAM bytes (read + write) per launch of the tensor-core decode kernel from
+# one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
 # valid only while the kernel source hashes to `source_sha`.
-TRAFFIC = {"source_sha": None, "bytes_per_launch": {}}
+TRAFFIC = {"source_sha": "2237fc80701c2477",
+           "bytes_per_launch": {"2": 1108844736, "3": 807163648, "4": 1091818800}}
 
 
 def launch_partition(w, max_blocks: int) -> int:
