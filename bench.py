@@ -31,8 +31,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import (WORKLOADS, make_beam_case, make_decode_case, poison_unused,  # noqa: E402
-                       write_step_schedule, beam_setup_schedule, beam_step_schedule)
+from workloads import (WORKLOADS, Workload, make_beam_case, make_decode_case,  # noqa: E402
+                       poison_unused, write_step_schedule, beam_setup_schedule,
+                       beam_step_schedule)
 
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak), decode steps/sec"
 FALLBACK_HBM_GBS = 6800.0
@@ -371,6 +372,139 @@ def cpu_baseline(st, budget_s=8.0):
                       "fp64 C oracle, %.1f s)" % (done_bytes / 1e9, passes, chunk, t_used)}
 
 
+SWEEP_BLOCKS = (8, 16, 32)
+SWEEP_GROUPS = (1, 4, 8)
+SWEEP_DIMS = (64, 128)
+
+
+def sweep_workload(B: int, G: int, D: int) -> Workload:
+    """The block-size / GQA / head-dim sweep: bf16, 8 KV heads, 64 sequences
+    with contexts uniform on [1024, 4096] (0.34-0.67 GB of KV, beyond L2)."""
+    return Workload(0, "sweep-b%d-g%d-d%d" % (B, G, D), "bf16", 8 * G, 8, D, B, 64,
+                    "uniform:1024:4096")
+
+
+def run_sweep(args):
+    """Attention GB/s over B x G x D, one JSON line per point, plus the
+    allocation side of the same trade-off for the drawn lengths: table entries
+    (indirection) and position utilisation (tail waste), Eq. (2)-(3)."""
+    import paged_kv_cache_312_gb300 as pkv
+    import __graft_entry__
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    peak, _ = measured_peaks()
+    stream = torch.cuda.current_stream(dev)
+    for B in SWEEP_BLOCKS:
+        for D in SWEEP_DIMS:
+            base = sweep_workload(B, max(SWEEP_GROUPS), D)
+            case = make_decode_case(base, seed=args.seed)
+            kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
+            bt, cl = case.block_tables.to(dev), case.context_lens.to(dev)
+            L = case.context_lens.to(torch.int64)
+            for G in SWEEP_GROUPS:
+                w = sweep_workload(B, G, D)
+                q = case.q[:, :w.num_heads].contiguous().to(dev)
+                S = q.shape[0]
+                P = launch_partition(w, bt.shape[1]) if args.partition is None else args.partition
+                out = torch.empty((S, w.num_heads, D), dtype=torch.float32, device=dev)
+                ws = None
+                if P:
+                    ws = torch.empty(pkv.decode_workspace_bytes(S, w.num_heads, D,
+                                                                bt.shape[1] * B, P),
+                                     dtype=torch.uint8, device=dev)
+
+                def call():
+                    pkv.paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, B, 8,
+                                               partition_size=P, workspace=ws, stream=stream)
+                for _ in range(args.warmup):
+                    call()
+                torch.cuda.synchronize(dev)
+                t0 = torch.cuda.Event(enable_timing=True)
+                t1 = torch.cuda.Event(enable_timing=True)
+                t0.record(stream)
+                for _ in range(args.steps):
+                    call()
+                t1.record(stream)
+                torch.cuda.synchronize(dev)
+                assert pkv.device_status() == 0
+                ms = t0.elapsed_time(t1) / args.steps
+                kv = int(L.sum()) * 2 * 8 * D * 2
+                entries = int(((L + B - 1) // B).sum())
+                alloc = entries * B
+                line = {"sweep": {"block_size": B, "group": G, "head_dim": D,
+                                  "num_heads": w.num_heads, "num_kv_heads": 8,
+                                  "partition_size": P},
+                        "attn_ms": round(ms, 5), "kv_bytes": kv,
+                        "attn_gbs": round(kv / (ms * 1e-3) / 1e9, 1),
+                        "frac_of_measured_peak": round(kv / (ms * 1e-3) / 1e9 / peak, 4),
+                        "table_entries": entries,
+                        "position_utilisation": round(int(L.sum()) / alloc, 5),
+                        "tail_waste_positions": alloc - int(L.sum())}
+                print(json.dumps(line), flush=True)
+
+
+def run_swap(args):
+    """Preemption by swapping: move every block of 64 sequences x 2048 tokens
+    (bf16, 8 KV heads x 128) from the device cache to a pinned host pool and
+    back with kv_swap_blocks, block pairs shuffled on both sides, for block
+    sizes 8 / 16 / 32.  Reference: a plain copy of the same bytes between one
+    contiguous device buffer and one pinned host buffer (torch copy_, the copy
+    engines over NVLink-C2C)."""
+    import paged_kv_cache_312_gb300 as pkv
+    import __graft_entry__
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    S, L, Hkv, D = 64, 2048, 8, 128
+    total = S * L * Hkv * D * 2 * 2  # K and V, bf16
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    flat_d = torch.empty(total, dtype=torch.uint8, device=dev)
+    flat_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    ref = {"out": total / (timed(lambda: flat_h.copy_(flat_d, non_blocking=True), 10) * 1e-3)
+           / 1e9,
+           "in": total / (timed(lambda: flat_d.copy_(flat_h, non_blocking=True), 10) * 1e-3)
+           / 1e9}
+    del flat_d, flat_h
+    rng = np.random.default_rng(args.seed)
+    for B in (8, 16, 32):
+        nb = S * L // B
+        kd = torch.randn(nb, Hkv, B, D, device=dev).to(torch.bfloat16)
+        vd = torch.randn(nb, Hkv, B, D, device=dev).to(torch.bfloat16)
+        kh = torch.empty(nb, Hkv, B, D, dtype=torch.bfloat16).pin_memory()
+        vh = torch.empty(nb, Hkv, B, D, dtype=torch.bfloat16).pin_memory()
+        pairs = torch.from_numpy(np.stack([rng.permutation(nb), rng.permutation(nb)], 1))
+        out_pairs = pairs.to(dev)
+        in_pairs = pairs[:, [1, 0]].contiguous().to(dev)
+        ms_out = timed(lambda: pkv.kv_swap_blocks(kh, vh, kd, vd, out_pairs, stream=stream), 10)
+        ms_in = timed(lambda: pkv.kv_swap_blocks(kd, vd, kh, vh, in_pairs, stream=stream), 10)
+        assert pkv.device_status() == 0
+        for direction, ms in (("out (device -> pinned host)", ms_out),
+                              ("in (pinned host -> device)", ms_in)):
+            gbs = total / (ms * 1e-3) / 1e9
+            key = "out" if direction.startswith("out") else "in"
+            print(json.dumps({"swap": {"block_size": B, "direction": direction,
+                                       "blocks": nb, "block_bytes": Hkv * B * D * 2 * 2},
+                              "bytes": total, "ms": round(ms, 4), "gbs": round(gbs, 1),
+                              "reference_copy_gbs": round(ref[key], 1),
+                              "frac_of_reference": round(gbs / ref[key], 3)}), flush=True)
+        del kd, vd, kh, vh
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -384,6 +518,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=8.0)
+    ap.add_argument("--swap", action="store_true",
+                    help="device <-> pinned host block swap throughput (one JSON line per "
+                         "block size and direction; not the benchmark line)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="block size x GQA group x head_dim sweep of the attention call "
+                         "(one JSON line per point; not the benchmark line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -392,6 +532,12 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.sweep:
+        run_sweep(args)
+        return
+    if args.swap:
+        run_swap(args)
+        return
     if args.impl == "reference":
         if rank != 0:
             return

@@ -205,6 +205,28 @@ int pkv_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int n
                        int dtype, void* stream);
 
 /*
+ * kv_swap_blocks -- move whole blocks between two KV pools, for preemption by
+ * swapping.  [AIPP section 4] / [CAY preemption]: when GPU memory runs out, a
+ * sequence's KV blocks can be moved to CPU memory and brought back later
+ * (small blocks make that transfer less efficient).  On GB300 a pinned host
+ * pool (cudaHostAlloc, or memory the CPU allocated on a coherent Grace
+ * system) is reached by the kernel directly over NVLink-C2C, so one launch
+ * gathers or scatters any set of scattered blocks.
+ *
+ * dst_* / src_* : pools laid out like the cache ([blocks][num_kv_heads]
+ *                 [block_size][head_dim]); each pointer may be device memory or
+ *                 host memory the GPU can address; 16-byte aligned.
+ * pairs : int64 [num_pairs][2] (src block, dst block), in memory the GPU can
+ *         read.  Destinations must be distinct; an id out of range skips the
+ *         pair and sets PKV_STATUS_BAD_PAIR.  For every KV head, all
+ *         block_size slots of K and V are copied, bit-exact.
+ */
+int pkv_kv_swap_blocks(void* dst_k_cache, void* dst_v_cache, const void* src_k_cache,
+                       const void* src_v_cache, const int64_t* pairs, int num_pairs,
+                       int num_src_blocks, int num_dst_blocks, int num_kv_heads, int head_dim,
+                       int block_size, int dtype, void* stream);
+
+/*
  * Kernel selection for pkv_paged_decode_attention (process-wide):
  * PKV_KERNEL_AUTO (default) picks the tensor-core kernel where supported;
  * PKV_KERNEL_CUDA_CORE forces the CUDA-core kernel for every shape (used to
@@ -257,6 +279,18 @@ int pkv_seq_fork(pkv_allocator* a, int64_t parent, int64_t child);
 
 /* Drops the sequence; blocks whose count reaches zero return to the pool. */
 int pkv_seq_free(pkv_allocator* a, int64_t seq);
+
+/* Moves a sequence from allocator `from` to allocator `to` (same block size),
+ * e.g. from the device pool to a host swap pool and back ([AIPP section 4],
+ * [CAY preemption]): takes one fresh block of `to` per block of the sequence,
+ * writes the (from block, to block) pairs in table order to pairs[0..2*n) for
+ * pkv_kv_swap_blocks, then releases the sequence in `from` (blocks it shared
+ * stay with their other users; the moved copy is private).  cap = pairs
+ * capacity in pairs.  All or nothing: PKV_ERR_OOM if `to` lacks blocks,
+ * PKV_ERR_SHAPE if cap is too small, PKV_ERR_STATE if seq is unknown in
+ * `from` or already in `to`. */
+int pkv_seq_swap(pkv_allocator* from, pkv_allocator* to, int64_t seq, int64_t* pairs, int cap,
+                 int* num_pairs);
 
 int pkv_seq_len(pkv_allocator* a, int64_t seq, int* len);
 

@@ -19,6 +19,8 @@ Language Model Serving with PagedAttention", Kwon et al. 2023):
 * ``kv_copy_blocks`` -- auturnal guide section 3 and aiplusplus "key
   techniques" 3: a branch that must modify a shared, not-full block first
   gets a private copy (copy-on-write).
+* ``kv_swap_blocks`` -- aiplusplus section 4 and the cayang0802 walkthrough
+  (preemption by swapping): blocks move between the GPU pool and a CPU pool.
 * ``kv_bytes`` / ``allocated_positions`` / ``tail_waste`` /
   ``position_utilisation`` -- auturnal guide Eq. (1), (2), (3).
 * ``decode_partitions`` / ``lse_combine`` -- the split-context form: softmax
@@ -43,7 +45,7 @@ from . import build as _build
 
 __all__ = [
     "DTYPE_CODE", "paged_decode_attention", "kv_write", "kv_copy_blocks",
-    "slot_for_position", "kv_bytes", "allocated_positions", "tail_waste",
+    "kv_swap_blocks", "slot_for_position", "kv_bytes", "allocated_positions", "tail_waste",
     "position_utilisation", "fixed_reservation_positions", "gather_sequence",
     "decode_partitions", "lse_combine", "widen",
 ]
@@ -62,10 +64,11 @@ def _load():
         lib.orc_widen.argtypes = [P, I, I64, P]
         lib.orc_kv_write.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
         lib.orc_kv_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I]
+        lib.orc_kv_swap_blocks.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I]
         lib.orc_paged_decode_attention.argtypes = [
             P, P, P, P, I, P, P, D, I, I, I, I, I, I, I, I]
         for f in (lib.orc_widen, lib.orc_kv_write, lib.orc_kv_copy_blocks,
-                  lib.orc_paged_decode_attention):
+                  lib.orc_kv_swap_blocks, lib.orc_paged_decode_attention):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -139,6 +142,22 @@ def kv_copy_blocks(k_cache, v_cache, pairs):
                                     pr.shape[0], NB, Hkv, D, B, DTYPE_CODE[k_cache.dtype])
     if rc != 0:
         raise ValueError("orc_kv_copy_blocks failed: %d" % rc)
+
+
+def kv_swap_blocks(dst_k, dst_v, src_k, src_v, pairs):
+    """In place: for each (src, dst) row of pairs, block dst of the
+    destination pools becomes a copy of block src of the source pools."""
+    for t in (dst_k, dst_v):
+        if not t.is_contiguous():
+            raise ValueError("pools must be contiguous")
+    src_k, src_v = _cpu(src_k), _cpu(src_v)
+    pr = _cpu(pairs).to(torch.int64).reshape(-1, 2).contiguous()
+    NS_, Hkv, B, D = src_k.shape
+    rc = _load().orc_kv_swap_blocks(dst_k.data_ptr(), dst_v.data_ptr(), src_k.data_ptr(),
+                                    src_v.data_ptr(), pr.data_ptr(), pr.shape[0], NS_,
+                                    dst_k.shape[0], Hkv, D, B, DTYPE_CODE[src_k.dtype])
+    if rc != 0:
+        raise ValueError("orc_kv_swap_blocks failed: %d" % rc)
 
 
 def slot_for_position(table_row, position: int, block_size: int) -> int:

@@ -144,6 +144,27 @@ class BlockManager:
             self._release(b)
         del self.lens[seq]
 
+    def swap_to(self, other: "BlockManager", seq: int):
+        """Preemption by swapping (aiplusplus section 4; cayang0802
+        walkthrough): move `seq` into the pool managed by `other`.  Takes one
+        fresh block of `other` per block of the sequence, in table order, then
+        releases the sequence here.  Returns the (this block, other block)
+        pairs.  All or nothing."""
+        if seq not in self.tables:
+            raise KeyError("no such sequence")
+        if seq in other.tables or other is self:
+            raise KeyError("sequence exists in the target")
+        if other.B != self.B:
+            raise ValueError("block sizes differ")
+        table = self.tables[seq]
+        if len(table) > len(other.free):
+            raise OutOfBlocks()
+        moved = [other._pop() for _ in table]
+        other.tables[seq] = moved
+        other.lens[seq] = self.lens[seq]
+        self.free_seq(seq)
+        return list(zip(table, moved))
+
     # -- queries ------------------------------------------------------------
     def table(self, seq: int):
         return list(self.tables[seq])

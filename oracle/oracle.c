@@ -143,6 +143,26 @@ int orc_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int n
     return ORC_OK;
 }
 
+/* ---- swap: whole blocks from one pool to another (preemption by swapping:
+ *      a preempted sequence's blocks move to CPU memory and back) --------- */
+int orc_kv_swap_blocks(void* dst_k, void* dst_v, const void* src_k, const void* src_v,
+                       const int64_t* pairs, int num_pairs, int num_src_blocks,
+                       int num_dst_blocks, int num_kv_heads, int head_dim, int block_size,
+                       int dtype)
+{
+    int eb = elem_bytes(dtype);
+    if (!eb || num_pairs < 0) return ORC_BAD_ARG;
+    size_t blk_bytes = (size_t)num_kv_heads * block_size * head_dim * eb;
+    for (int i = 0; i < num_pairs; ++i) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_src_blocks || dst < 0 || dst >= num_dst_blocks)
+            return ORC_BAD_BLOCK;
+        memcpy((char*)dst_k + dst * blk_bytes, (const char*)src_k + src * blk_bytes, blk_bytes);
+        memcpy((char*)dst_v + dst * blk_bytes, (const char*)src_v + src * blk_bytes, blk_bytes);
+    }
+    return ORC_OK;
+}
+
 /* ---- decode attention: gather through the block table, then softmax ---- */
 
 typedef struct {

@@ -6,12 +6,12 @@ include/pkv.h); this package is the thin Python binding over it.
 from ._binding import (  # noqa: F401
     KERNEL_AUTO, KERNEL_CUDA_CORE, PKV_BF16, PKV_F16, PKV_F32, STATUS_BITS, BlockAllocator,
     NOALLOC_SCRATCH_BYTES, OutOfBlocks, PkvError, decode_workspace_bytes, device_status,
-    kv_copy_blocks, kv_write, lib, paged_decode_attention, paged_decode_attention_noalloc,
-    set_decode_kernel,
+    kv_copy_blocks, kv_swap_blocks, kv_write, lib, paged_decode_attention,
+    paged_decode_attention_noalloc, set_decode_kernel,
 )
 
 __all__ = [
     "BlockAllocator", "OutOfBlocks", "PkvError", "decode_workspace_bytes", "device_status",
-    "kv_copy_blocks", "kv_write", "lib", "paged_decode_attention",
+    "kv_copy_blocks", "kv_swap_blocks", "kv_write", "lib", "paged_decode_attention",
     "paged_decode_attention_noalloc", "set_decode_kernel",
 ]

@@ -35,6 +35,8 @@ _SIGS = {
     "pkv_paged_decode_attention_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I,
                                                 _I, _I, _I, _I, _I, _P]),
     "pkv_kv_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pkv_kv_swap_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "pkv_seq_swap": (_I, [_P, _P, _I64, _P, _I, ctypes.POINTER(_I)]),
     "pkv_set_decode_kernel": (_I, [_I]),
     "pkv_alloc_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_alloc_destroy": (_I, [_P]),
@@ -179,6 +181,37 @@ def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, conte
     _check(rc, "pkv_paged_decode_attention_noalloc")
 
 
+def _reachable(t: torch.Tensor, name: str):
+    """Address of a CUDA tensor or of a pinned host tensor (which the GPU
+    addresses directly)."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("%s must be a CUDA tensor or pinned host memory" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def kv_swap_blocks(dst_k, dst_v, src_k, src_v, pairs, stream=None):
+    """Copy whole blocks from pool src to pool dst (pairs int64 [P, 2] of
+    (src block, dst block)); each pool may live on the GPU or in pinned host
+    memory."""
+    NS_, Hkv, B, D = src_k.shape
+    ND = dst_k.shape[0]
+    if dst_k.shape[1:] != src_k.shape[1:] or dst_v.shape != dst_k.shape or \
+            src_v.shape != src_k.shape:
+        raise ValueError("kv_swap_blocks: pool shapes differ")
+    if len({dst_k.dtype, dst_v.dtype, src_k.dtype, src_v.dtype}) != 1:
+        raise ValueError("kv_swap_blocks: dtypes differ")
+    if pairs.dtype != torch.int64 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int64 [P, 2]")
+    rc = lib().pkv_kv_swap_blocks(
+        _reachable(dst_k, "dst_k"), _reachable(dst_v, "dst_v"), _reachable(src_k, "src_k"),
+        _reachable(src_v, "src_v"),
+        _reachable(pairs, "pairs") if pairs.numel() else ctypes.c_void_p(0), pairs.shape[0],
+        NS_, ND, Hkv, D, B, DTYPE_CODE[src_k.dtype], _stream(stream))
+    _check(rc, "pkv_kv_swap_blocks")
+
+
 def kv_copy_blocks(k_cache, v_cache, pairs, stream=None):
     """Copy whole physical blocks: pairs is int64 [P, 2] of (src, dst)."""
     NB, Hkv, B, D = k_cache.shape
@@ -260,6 +293,16 @@ class BlockAllocator:
         _check(lib().pkv_seq_free(self._h, int(seq)), "pkv_seq_free")
 
     free_seq = free
+
+    def swap_to(self, other, seq):
+        """Move `seq` into allocator `other`; returns the (this block, other
+        block) pairs, int64 [n, 2], for kv_swap_blocks."""
+        n = max(1, len(self.table(seq)))
+        pairs = torch.empty((n, 2), dtype=torch.int64)
+        got = ctypes.c_int(0)
+        _check(lib().pkv_seq_swap(self._h, other._h, int(seq), ctypes.c_void_p(pairs.data_ptr()),
+                                  n, ctypes.byref(got)), "pkv_seq_swap")
+        return pairs[:got.value].clone()
 
     def length(self, seq):
         n = ctypes.c_int()

@@ -215,6 +215,39 @@ int pkv_seq_free(pkv_allocator* a, int64_t seq)
     return PKV_OK;
 }
 
+int pkv_seq_swap(pkv_allocator* from, pkv_allocator* to, int64_t seq, int64_t* pairs, int cap,
+                 int* num_pairs)
+{
+    if (!from || !to || !num_pairs) return pkv_fail(PKV_ERR_NULL, "pkv_seq_swap: NULL argument");
+    if (from == to) return pkv_fail(PKV_ERR_STATE, "pkv_seq_swap: same allocator");
+    if (from->block_size != to->block_size)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_seq_swap: block sizes differ");
+    auto it = from->seqs.find(seq);
+    if (it == from->seqs.end()) return pkv_fail(PKV_ERR_STATE, "pkv_seq_swap: unknown sequence");
+    if (to->seqs.count(seq)) return pkv_fail(PKV_ERR_STATE, "pkv_seq_swap: sequence exists");
+    const std::vector<int32_t>& t = it->second.table;
+    const int n = (int)t.size();
+    if (n > 0 && !pairs) return pkv_fail(PKV_ERR_NULL, "pkv_seq_swap: pairs is NULL");
+    if (n > cap) return pkv_fail(PKV_ERR_SHAPE, "pkv_seq_swap: %d pairs, cap %d", n, cap);
+    if (n > (int)to->free_stack.size())
+        return pkv_fail(PKV_ERR_OOM, "pkv_seq_swap: %d blocks needed, %zu free", n,
+                        to->free_stack.size());
+    pkv_allocator::Seq moved;
+    moved.len = it->second.len;
+    moved.table.reserve(n);
+    for (int i = 0; i < n; ++i) {
+        const int32_t b = to->pop();
+        moved.table.push_back(b);
+        pairs[2 * i] = t[i];
+        pairs[2 * i + 1] = b;
+    }
+    for (int i = n; i-- > 0;) from->release(t[i]);
+    from->seqs.erase(it);
+    to->seqs.emplace(seq, std::move(moved));
+    *num_pairs = n;
+    return PKV_OK;
+}
+
 int pkv_seq_len(pkv_allocator* a, int64_t seq, int* len)
 {
     if (!a || !len) return pkv_fail(PKV_ERR_NULL, "pkv_seq_len: NULL argument");

@@ -209,6 +209,33 @@ int pkv_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int n
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "pkv_kv_copy_blocks launch");
 }
 
+int pkv_kv_swap_blocks(void* dst_k_cache, void* dst_v_cache, const void* src_k_cache,
+                       const void* src_v_cache, const int64_t* pairs, int num_pairs,
+                       int num_src_blocks, int num_dst_blocks, int num_kv_heads, int head_dim,
+                       int block_size, int dtype, void* stream)
+{
+    const int eb = pkv_dtype_bytes(dtype);
+    if (!eb) return pkv_fail(PKV_ERR_DTYPE, "pkv_kv_swap_blocks: dtype %d", dtype);
+    if (num_pairs < 0 || num_src_blocks < 0 || num_dst_blocks < 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || block_size <= 0)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_kv_swap_blocks: bad sizes");
+    const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * eb;
+    if (block_bytes % 16 != 0)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_kv_swap_blocks: block bytes must be a multiple of 16");
+    if (num_pairs == 0) return PKV_OK;
+    if (!dst_k_cache || !dst_v_cache || !src_k_cache || !src_v_cache || !pairs)
+        return pkv_fail(PKV_ERR_NULL, "pkv_kv_swap_blocks: NULL pointer");
+    if (!aligned(dst_k_cache, 16) || !aligned(dst_v_cache, 16) || !aligned(src_k_cache, 16) ||
+        !aligned(src_v_cache, 16) || !aligned(pairs, 8))
+        return pkv_fail(PKV_ERR_ALIGN, "pkv_kv_swap_blocks: misaligned pointer");
+    unsigned int* status = pkv_status_word_ptr();
+    if (!status) return pkv_fail(PKV_ERR_CUDA, "pkv_kv_swap_blocks: no device status word");
+    cudaError_t e = launch_kv_swap_blocks(dst_k_cache, dst_v_cache, src_k_cache, src_v_cache,
+                                          pairs, num_pairs, num_src_blocks, num_dst_blocks,
+                                          block_bytes, status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "pkv_kv_swap_blocks launch");
+}
+
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
                                   int partition_size)
 {

@@ -81,6 +81,54 @@ __global__ void copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restric
 }
 
 // ---------------------------------------------------------------------------
+// kv_swap_blocks: whole blocks from one pool to another, e.g. the device cache
+// and a pinned host swap pool that the GPU reaches directly over NVLink-C2C
+// (aiplusplus page, section 4, and the cayang0802 walkthrough: a preempted
+// sequence's KV blocks are swapped out to CPU memory and back).  Each thread
+// keeps four 16-byte loads of K and four of V in flight before storing.
+// ---------------------------------------------------------------------------
+constexpr int kSwapThreads = 256;
+constexpr int kSwapUnroll = 4;
+
+__global__ void __launch_bounds__(kSwapThreads)
+swap_blocks_kernel(uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
+                   const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
+                   const int64_t* __restrict__ pairs, int num_src_blocks, int num_dst_blocks,
+                   size_t vec_per_block, unsigned int* status)
+{
+    const int64_t src = pairs[2 * blockIdx.x], dst = pairs[2 * blockIdx.x + 1];
+    if (src < 0 || src >= num_src_blocks || dst < 0 || dst >= num_dst_blocks) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) flag(status, PKV_STATUS_BAD_PAIR);
+        return;
+    }
+    const uint4* ks = src_k + (size_t)src * vec_per_block;
+    const uint4* vs = src_v + (size_t)src * vec_per_block;
+    uint4* kd = dst_k + (size_t)dst * vec_per_block;
+    uint4* vd = dst_v + (size_t)dst * vec_per_block;
+    const size_t step = (size_t)gridDim.y * kSwapThreads * kSwapUnroll;
+    for (size_t i0 = ((size_t)blockIdx.y * kSwapUnroll) * kSwapThreads + threadIdx.x;
+         i0 < vec_per_block; i0 += step) {
+        uint4 a[kSwapUnroll], b[kSwapUnroll];
+#pragma unroll
+        for (int u = 0; u < kSwapUnroll; ++u) {
+            const size_t i = i0 + (size_t)u * kSwapThreads;
+            if (i < vec_per_block) {
+                a[u] = ks[i];
+                b[u] = vs[i];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kSwapUnroll; ++u) {
+            const size_t i = i0 + (size_t)u * kSwapThreads;
+            if (i < vec_per_block) {
+                kd[i] = a[u];
+                vd[i] = b[u];
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // CUDA-core paged decode.  One CTA = one (partition, query head, sequence);
 // its 4 warps take tokens round-robin, each lane holding D/32 elements of q,
 // of the running output and of each K/V row it reads.  Scores are kept in
@@ -287,6 +335,22 @@ cudaError_t launch_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* p
     copy_blocks_kernel<<<grid, threads, 0, stream>>>(static_cast<uint4*>(k_cache),
                                                      static_cast<uint4*>(v_cache), pairs,
                                                      num_blocks, vec, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kv_swap_blocks(void* dst_k, void* dst_v, const void* src_k, const void* src_v,
+                                  const int64_t* pairs, int num_pairs, int num_src_blocks,
+                                  int num_dst_blocks, size_t block_bytes, unsigned int* status,
+                                  cudaStream_t stream)
+{
+    const size_t vec = block_bytes / 16;
+    size_t chunks = (vec + kSwapThreads * kSwapUnroll - 1) / (kSwapThreads * kSwapUnroll);
+    if (chunks < 1) chunks = 1;
+    if (chunks > 65535) chunks = 65535;
+    dim3 grid(num_pairs, (unsigned)chunks);
+    swap_blocks_kernel<<<grid, kSwapThreads, 0, stream>>>(
+        static_cast<uint4*>(dst_k), static_cast<uint4*>(dst_v), static_cast<const uint4*>(src_k),
+        static_cast<const uint4*>(src_v), pairs, num_src_blocks, num_dst_blocks, vec, status);
     return cudaGetLastError();
 }
 

@@ -39,6 +39,13 @@ cudaError_t launch_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* p
                                   int num_pairs, int num_blocks, size_t block_bytes,
                                   unsigned int* status, cudaStream_t stream);
 
+// Whole blocks (all heads, K and V) from pool `src` to pool `dst`; either pool
+// may be device memory or pinned host memory mapped into the address space.
+cudaError_t launch_kv_swap_blocks(void* dst_k, void* dst_v, const void* src_k, const void* src_v,
+                                  const int64_t* pairs, int num_pairs, int num_src_blocks,
+                                  int num_dst_blocks, size_t block_bytes, unsigned int* status,
+                                  cudaStream_t stream);
+
 // CUDA-core decode (any dtype, any group size).  Grid: partitions x heads x seqs.
 cudaError_t launch_decode_cuda_core(const DecodeParams& p, int kv_dtype, cudaStream_t stream);
 

@@ -173,6 +173,67 @@ def test_allocator_matches_reference_on_random_operations(seed):
         _same(cpp, ref, live)
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_swap_matches_reference_between_two_pools(seed):
+    rnd = random.Random(100 + seed)
+    B = 4
+    cg, rg = pkv.BlockAllocator(24, B), BlockManager(24, B)
+    cc, rc = pkv.BlockAllocator(10, B), BlockManager(10, B)
+    where = {}  # seq -> "gpu" | "cpu"
+    nid = 0
+    for _ in range(800):
+        op = rnd.random()
+        on_gpu = [s for s, w in where.items() if w == "gpu"]
+        on_cpu = [s for s, w in where.items() if w == "cpu"]
+        if op < 0.2 or not where:
+            n = rnd.randint(0, 9)
+            try:
+                rg.add(nid, n)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    cg.add(nid, n)
+            else:
+                cg.add(nid, n)
+                where[nid] = "gpu"
+            nid += 1
+        elif op < 0.45 and on_gpu:
+            s = rnd.choice(on_gpu)
+            try:
+                r = rg.append(s)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    cg.append(s)
+            else:
+                assert cg.append(s) == r
+        elif op < 0.55 and on_gpu:
+            s = rnd.choice(on_gpu)
+            rg.fork(s, nid)
+            cg.fork(s, nid)
+            where[nid] = "gpu"
+            nid += 1
+        elif op < 0.75 and (on_gpu or on_cpu):
+            s = rnd.choice(on_gpu + on_cpu)
+            src_r, dst_r, src_c, dst_c = (rg, rc, cg, cc) if where[s] == "gpu" else (rc, rg, cc, cg)
+            try:
+                pairs = src_r.swap_to(dst_r, s)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    src_c.swap_to(dst_c, s)
+            else:
+                got = src_c.swap_to(dst_c, s)
+                assert [tuple(p) for p in got.tolist()] == pairs
+                where[s] = "cpu" if where[s] == "gpu" else "gpu"
+        else:
+            s = rnd.choice(list(where))
+            (rg if where[s] == "gpu" else rc).free_seq(s)
+            (cg if where[s] == "gpu" else cc).free(s)
+            del where[s]
+        _same(cg, rg, [s for s, w in where.items() if w == "gpu"])
+        _same(cc, rc, [s for s, w in where.items() if w == "cpu"])
+    with pytest.raises(pkv.PkvError):
+        cg.swap_to(cg, next(iter(where)) if where else 0)
+
+
 def test_allocator_errors_leave_state_unchanged():
     a = pkv.BlockAllocator(3, 4)
     a.add(0, 8)

@@ -437,6 +437,52 @@ def test_cow_isolation_between_beams():
     bm.check_invariants()
 
 
+def test_swap_out_and_back_preserves_every_sequence():
+    # Preemption by swapping: a sequence's blocks move to a CPU pool and back
+    # into other GPU blocks; its logical K/V and its attention are unchanged,
+    # and the sequences that shared its prefix keep theirs.
+    B, Hkv, D, Hq = 4, 2, 8, 4
+    gpu, cpu = BlockManager(20, B, free_order=list(range(19, -1, -1))), BlockManager(12, B)
+    g = torch.Generator().manual_seed(21)
+    kc = torch.full((20, Hkv, B, D), float("nan"))
+    vc = torch.full_like(kc, float("nan"))
+    hk = torch.full((12, Hkv, B, D), float("nan"))
+    hv = torch.full_like(hk, float("nan"))
+    K = torch.randn(11, Hkv, D, generator=g)
+    V = torch.randn(11, Hkv, D, generator=g)
+    gpu.add(0, 0)
+    oracle.kv_write(kc, vc, K[:9], V[:9], torch.tensor([gpu.append(0)[0] for _ in range(9)]), B)
+    gpu.fork(0, 1)  # 1 shares 0's blocks
+    slot, cow = gpu.append(1)
+    oracle.kv_copy_blocks(kc, vc, torch.tensor([cow]))
+    oracle.kv_write(kc, vc, K[9:10], V[9:10], torch.tensor([slot]), B)
+    q = torch.randn(1, Hq, D, generator=g)
+
+    def attend(mgr, kcache, vcache, seq):
+        bt = torch.tensor([mgr.table(seq)], dtype=torch.int32)
+        cl = torch.tensor([mgr.length(seq)], dtype=torch.int32)
+        return oracle.paged_decode_attention(q, kcache, vcache, bt, cl, 0.3, B, Hkv)
+
+    before0, before1 = attend(gpu, kc, vc, 0), attend(gpu, kc, vc, 1)
+    pairs = gpu.swap_to(cpu, 1)
+    assert [p[0] for p in pairs] == gpu.table(0)[:2] + [cow[1]]
+    oracle.kv_swap_blocks(hk, hv, kc, vc, torch.tensor(pairs))
+    gpu.check_invariants()
+    cpu.check_invariants()
+    assert np.array_equal(attend(cpu, hk, hv, 1), before1)   # readable from the CPU pool
+    assert np.array_equal(attend(gpu, kc, vc, 0), before0)   # sharer untouched
+    back = cpu.swap_to(gpu, 1)
+    oracle.kv_swap_blocks(kc, vc, hk, hv, torch.tensor(back))
+    assert np.array_equal(attend(gpu, kc, vc, 1), before1)
+    expect = torch.cat([K[:9], K[9:10]]).double().numpy()
+    assert np.array_equal(oracle.gather_sequence(kc, gpu.table(1), 10), expect)
+    assert cpu.num_free() == 12
+    gpu.check_invariants()
+    with pytest.raises(OutOfBlocks):
+        gpu.swap_to(BlockManager(1, B), 0)  # needs 3 blocks
+    assert gpu.length(0) == 9
+
+
 # --------------------------------------------------------------------------
 # Block manager: random model check of its invariants, OOM atomicity.
 # --------------------------------------------------------------------------

@@ -156,6 +156,24 @@ def test_decode_small(dt, Hq, Hkv, D, B, P, kernel):
     assert torch.equal(out[0].cpu(), torch.zeros_like(out[0].cpu()))  # length-0 row
 
 
+@pytest.mark.parametrize("B", [8, 16, 32])
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_sweep_points(B, G, D):
+    # every point of the block-size / GQA / head-dim sweep, at a small size
+    # and in its bench launch configuration (1024-token partitions)
+    import bench
+    w = bench.sweep_workload(B, G, D)
+    case = make_decode_case(w, seed=B * 100 + G * 10 + D, lengths=[1, 700, 1500, 2100])
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    P = bench.launch_partition(w, case.block_tables.shape[1])
+    out = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, B, 8, P=P)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, B, 8)
+    assert pkv.device_status() == 0
+    assert max_err(out, ref) <= TOL16
+
+
 def test_workload1_fp32():
     w = WORKLOADS[1]
     for seed in (0, 1, 2):
@@ -230,6 +248,63 @@ def test_split_with_thousands_of_partitions():
                          P=P)
         assert pkv.device_status() == 0
         assert max_err(out, ref) <= TOL16, P
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("pairs_on_host", [False, True])
+def test_swap_blocks_to_pinned_host_and_back(dtype, pairs_on_host):
+    # Device pool -> pinned host pool -> other device blocks, bit-exact, with
+    # the pair list either on the GPU or in pinned host memory.
+    NB, NH, Hkv, B, D = 30, 12, 4, 16, 128
+    g = torch.Generator().manual_seed(7)
+    kc = torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    vc = torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    hk = torch.zeros(NH, Hkv, B, D, dtype=dtype).pin_memory()
+    hv = torch.zeros(NH, Hkv, B, D, dtype=dtype).pin_memory()
+    out_pairs = torch.tensor([[3, 0], [17, 5], [29, 11], [0, 2]], dtype=torch.int64)
+    in_pairs = torch.tensor([[0, 20], [5, 21], [11, 1], [2, 4]], dtype=torch.int64)
+    place = (lambda t: t.pin_memory()) if pairs_on_host else (lambda t: t.to(DEV))
+    dk, dv = kc.to(DEV), vc.to(DEV)
+    pkv.kv_swap_blocks(hk, hv, dk, dv, place(out_pairs))
+    torch.cuda.synchronize()
+    rk, rv = torch.zeros_like(hk), torch.zeros_like(hv)
+    oracle.kv_swap_blocks(rk, rv, kc, vc, out_pairs)
+    assert torch.equal(bits(hk), bits(rk)) and torch.equal(bits(hv), bits(rv))
+    pkv.kv_swap_blocks(dk, dv, hk, hv, place(in_pairs))
+    torch.cuda.synchronize()
+    oracle.kv_swap_blocks(kc, vc, rk, rv, in_pairs)
+    assert torch.equal(bits(dk), bits(kc)) and torch.equal(bits(dv), bits(vc))
+    assert pkv.device_status() == 0
+    pkv.kv_swap_blocks(hk, hv, dk, dv, place(torch.tensor([[NB, 0]], dtype=torch.int64)))
+    assert pkv.device_status() & 8
+    assert torch.equal(bits(hk), bits(rk))
+
+
+def test_swap_round_trip_keeps_attention():
+    # A sequence swapped out to a host pool by the allocator and the swap
+    # kernel, then back into other device blocks, attends exactly as before.
+    w = Workload(0, "swap", "bf16", 16, 4, 128, 16, 5, "fixed")
+    case = make_decode_case(w, seed=3, lengths=[100, 300, 17, 512, 64])
+    NB = case.num_blocks
+    gpu = pkv.BlockAllocator(NB + 40, 16, free_order=list(case.pool_order) + list(range(NB, NB + 40)))
+    for s, n in enumerate(case.lengths):
+        gpu.add(s, int(n))
+    bt0, cl = gpu.dense_tables(range(5), case.block_tables.shape[1])
+    assert torch.equal(bt0, case.block_tables)
+    kc = torch.cat([case.k_cache, torch.zeros(40, 4, 16, 128, dtype=torch.bfloat16)]).to(DEV)
+    vc = torch.cat([case.v_cache, torch.zeros(40, 4, 16, 128, dtype=torch.bfloat16)]).to(DEV)
+    before = gpu_decode(case.q, kc, vc, bt0, cl, w.scale, 16, 4)
+    host = pkv.BlockAllocator(64, 16)
+    hk = torch.zeros(64, 4, 16, 128, dtype=torch.bfloat16).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory()
+    pkv.kv_swap_blocks(hk, hv, kc, vc, gpu.swap_to(host, 3).to(DEV))
+    gpu.add(99, 64)  # another sequence takes some of the freed blocks meanwhile
+    pkv.kv_swap_blocks(kc, vc, hk, hv, host.swap_to(gpu, 3).to(DEV))
+    bt1, cl1 = gpu.dense_tables(range(5), case.block_tables.shape[1])
+    assert not torch.equal(bt1[3], bt0[3])
+    after = gpu_decode(case.q, kc, vc, bt1, cl1, w.scale, 16, 4)
+    assert pkv.device_status() == 0
+    assert torch.equal(before, after)
 
 
 def test_nan_poison_and_physical_permutation():
