@@ -303,6 +303,37 @@ int pkv_block_table(pkv_allocator* a, int64_t seq, int32_t* out, int cap, int* n
 int pkv_block_tables_dense(pkv_allocator* a, const int64_t* seqs, int n, int max_blocks,
                            int32_t* tables, int32_t* lens);
 
+/* ---- automatic prefix caching ([CAY] prefix caching: each full block is
+ * keyed by a hash of its own tokens and all preceding tokens; blocks with the
+ * same key hold the same KV and are reused instead of recomputed).
+ * Key of full block i: FNV-1a 64-bit over the key of block i-1 (0 for i = 0)
+ * as 8 little-endian bytes, then the block's block_size token ids as 4
+ * little-endian bytes each.  A hit is confirmed against the stored parent key
+ * and token ids, so a hash collision cannot alias two different blocks.
+ * A registered block whose count drops to zero stays findable in a
+ * least-recently-freed list; it is handed out again (and unregistered) only
+ * once the plain free list is empty.  Free-block counts include it. */
+
+/* New sequence for the prompt tokens[0..n): reuses the cached blocks of the
+ * longest prefix of full blocks found in the index, takes fresh blocks for
+ * the rest.  *reused_tokens = tokens covered by reused blocks (a multiple of
+ * block_size): their K/V is already in the cache; the caller writes the
+ * remaining ones.  Errors as pkv_seq_add. */
+int pkv_seq_add_cached(pkv_allocator* a, int64_t seq, const int32_t* tokens, int n,
+                       int* reused_tokens);
+
+/* Registers the full blocks covering tokens[0..n) of a sequence (n <= its
+ * length; call once their K/V has been written).  Blocks already registered,
+ * or whose key is already in the index, are skipped; *registered = blocks
+ * added. */
+int pkv_seq_register_blocks(pkv_allocator* a, int64_t seq, const int32_t* tokens, int n,
+                            int* registered);
+
+/* Blocks reused by pkv_seq_add_cached so far, blocks in the index, and
+ * registered blocks currently unused (count 0). */
+int pkv_prefix_cache_stats(pkv_allocator* a, int64_t* hit_blocks, int64_t* cached_blocks,
+                           int64_t* cached_free_blocks);
+
 int pkv_refcount(pkv_allocator* a, int block, int* count);
 int pkv_num_free_blocks(pkv_allocator* a, int* n);
 

@@ -37,6 +37,10 @@ _SIGS = {
     "pkv_kv_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pkv_kv_swap_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "pkv_seq_swap": (_I, [_P, _P, _I64, _P, _I, ctypes.POINTER(_I)]),
+    "pkv_seq_add_cached": (_I, [_P, _I64, _P, _I, ctypes.POINTER(_I)]),
+    "pkv_seq_register_blocks": (_I, [_P, _I64, _P, _I, ctypes.POINTER(_I)]),
+    "pkv_prefix_cache_stats": (_I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
+                                    ctypes.POINTER(_I64)]),
     "pkv_set_decode_kernel": (_I, [_I]),
     "pkv_alloc_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_alloc_destroy": (_I, [_P]),
@@ -293,6 +297,30 @@ class BlockAllocator:
         _check(lib().pkv_seq_free(self._h, int(seq)), "pkv_seq_free")
 
     free_seq = free
+
+    def add_cached(self, seq, tokens):
+        """New sequence for prompt `tokens`, reusing cached full blocks of its
+        longest matching prefix; returns the number of reused tokens."""
+        t = torch.as_tensor(list(tokens), dtype=torch.int32).contiguous()
+        got = ctypes.c_int(0)
+        _check(lib().pkv_seq_add_cached(self._h, int(seq), ctypes.c_void_p(t.data_ptr()),
+                                        t.numel(), ctypes.byref(got)), "pkv_seq_add_cached")
+        return got.value
+
+    def register_blocks(self, seq, tokens):
+        """Index the full blocks covering `tokens` (a prefix of the sequence)."""
+        t = torch.as_tensor(list(tokens), dtype=torch.int32).contiguous()
+        got = ctypes.c_int(0)
+        _check(lib().pkv_seq_register_blocks(self._h, int(seq), ctypes.c_void_p(t.data_ptr()),
+                                             t.numel(), ctypes.byref(got)),
+               "pkv_seq_register_blocks")
+        return got.value
+
+    def prefix_cache_stats(self):
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().pkv_prefix_cache_stats(self._h, ctypes.byref(a), ctypes.byref(b),
+                                            ctypes.byref(c)), "pkv_prefix_cache_stats")
+        return a.value, b.value, c.value
 
     def swap_to(self, other, seq):
         """Move `seq` into allocator `other`; returns the (this block, other

@@ -12,16 +12,59 @@
 //    search) and a copy-on-write decision when a sequence writes into a
 //    shared block that is not full (auturnal guide, section 3; cayang0802
 //    walkthrough, beam search of width 4).
+//  - an index of full blocks by content for automatic prefix caching
+//    (cayang0802 walkthrough, prefix caching): a full block's key is a hash
+//    of its own tokens and of every token before it, so equal keys mean equal
+//    KV; a new sequence reuses the cached blocks of its longest matching
+//    prefix.  A registered block whose count drops to zero is kept, still
+//    findable, in a least-recently-freed list, and is only evicted (and
+//    unregistered) when the plain free list is empty.
 // Every operation either completes or leaves the state untouched (OOM and
 // bad arguments included), as the auturnal guide's section 6 asks of OOM.
 #include <cstdint>
 #include <cstring>
+#include <list>
 #include <new>
 #include <unordered_map>
 #include <vector>
 
 #include "pkv.h"
 #include "pkv_internal.h"
+
+namespace {
+
+// FNV-1a, 64-bit (Fowler, Noll, Vo): offset basis 14695981039346656037,
+// prime 1099511628211, over bytes.
+struct Fnv1a {
+    uint64_t h = 14695981039346656037ull;
+    void byte(uint8_t b)
+    {
+        h ^= b;
+        h *= 1099511628211ull;
+    }
+    void u64(uint64_t v)
+    {
+        for (int i = 0; i < 8; ++i) byte((uint8_t)(v >> (8 * i)));
+    }
+    void i32(int32_t v)
+    {
+        const uint32_t u = (uint32_t)v;
+        for (int i = 0; i < 4; ++i) byte((uint8_t)(u >> (8 * i)));
+    }
+};
+
+// Key of a full block: FNV-1a over the parent block's key (0 for the first
+// block, 8 bytes little-endian) followed by the block's B token ids (4 bytes
+// little-endian each).
+uint64_t block_key(uint64_t parent, const int32_t* tokens, int block_size)
+{
+    Fnv1a f;
+    f.u64(parent);
+    for (int i = 0; i < block_size; ++i) f.i32(tokens[i]);
+    return f.h;
+}
+
+}  // namespace
 
 struct pkv_allocator {
     int num_blocks = 0;
@@ -34,16 +77,63 @@ struct pkv_allocator {
     };
     std::unordered_map<int64_t, Seq> seqs;
 
+    // ---- prefix cache: registered full blocks
+    std::unordered_map<uint64_t, int32_t> index;  // key -> block
+    std::vector<char> registered;                 // per block
+    std::vector<uint64_t> key, parent_key;        // per registered block
+    std::vector<int32_t> tokens;                  // [num_blocks][block_size]
+    std::list<int32_t> cached_free;               // count 0, still findable; front = oldest
+    std::vector<std::list<int32_t>::iterator> cached_pos;
+    int64_t prefix_hits = 0;
+
+    size_t available() const { return free_stack.size() + cached_free.size(); }
+
+    void unregister(int32_t b)
+    {
+        auto it = index.find(key[b]);
+        if (it != index.end() && it->second == b) index.erase(it);
+        registered[b] = 0;
+    }
     int32_t pop()
     {
-        int32_t b = free_stack.back();
-        free_stack.pop_back();
+        int32_t b;
+        if (!free_stack.empty()) {
+            b = free_stack.back();
+            free_stack.pop_back();
+        } else {  // evict the least recently freed cached block
+            b = cached_free.front();
+            cached_free.pop_front();
+            unregister(b);
+        }
         ref[b] = 1;
         return b;
     }
     void release(int32_t b)
     {
-        if (--ref[b] == 0) free_stack.push_back(b);
+        if (--ref[b] == 0) {
+            if (registered[b]) {
+                cached_free.push_back(b);
+                cached_pos[b] = std::prev(cached_free.end());
+            } else {
+                free_stack.push_back(b);
+            }
+        }
+    }
+    void take(int32_t b)  // one more user of a registered block
+    {
+        if (ref[b] == 0) cached_free.erase(cached_pos[b]);
+        ref[b] += 1;
+    }
+    // Block cached for (parent key, tokens), or -1.
+    int32_t lookup(uint64_t k, uint64_t parent, const int32_t* toks) const
+    {
+        auto it = index.find(k);
+        if (it == index.end()) return -1;
+        const int32_t b = it->second;
+        if (parent_key[b] != parent ||
+            std::memcmp(&tokens[(size_t)b * block_size], toks, sizeof(int32_t) * block_size))
+            return -1;  // a key collision: contents differ
+        return b;
     }
     void append_one(Seq& s, int64_t* slot, int64_t* src, int64_t* dst)
     {
@@ -81,6 +171,11 @@ int pkv_alloc_create(int num_blocks, int block_size, const int32_t* free_order,
     a->num_blocks = num_blocks;
     a->block_size = block_size;
     a->ref.assign(num_blocks, 0);
+    a->registered.assign(num_blocks, 0);
+    a->key.assign(num_blocks, 0);
+    a->parent_key.assign(num_blocks, 0);
+    a->tokens.assign((size_t)num_blocks * block_size, 0);
+    a->cached_pos.resize(num_blocks);
     a->free_stack.resize(num_blocks);
     std::vector<char> seen(num_blocks, 0);
     for (int i = 0; i < num_blocks; ++i) {
@@ -108,9 +203,9 @@ int pkv_seq_add(pkv_allocator* a, int64_t seq, int prompt_len)
     if (prompt_len < 0) return pkv_fail(PKV_ERR_SHAPE, "pkv_seq_add: negative prompt_len");
     if (a->seqs.count(seq)) return pkv_fail(PKV_ERR_STATE, "pkv_seq_add: sequence exists");
     int64_t n = (prompt_len + (int64_t)a->block_size - 1) / a->block_size;
-    if (n > (int64_t)a->free_stack.size())
+    if (n > (int64_t)a->available())
         return pkv_fail(PKV_ERR_OOM, "pkv_seq_add: %lld blocks needed, %zu free",
-                        (long long)n, a->free_stack.size());
+                        (long long)n, a->available());
     pkv_allocator::Seq s;
     s.table.reserve(n);
     for (int64_t i = 0; i < n; ++i) s.table.push_back(a->pop());
@@ -128,7 +223,7 @@ int pkv_seq_append(pkv_allocator* a, int64_t seq, int64_t* slot, int64_t* cow_sr
     if (it == a->seqs.end()) return pkv_fail(PKV_ERR_STATE, "pkv_seq_append: unknown sequence");
     const pkv_allocator::Seq& s = it->second;
     bool need = s.len % a->block_size == 0 || a->ref[s.table.back()] > 1;
-    if (need && a->free_stack.empty())
+    if (need && a->available() == 0)
         return pkv_fail(PKV_ERR_OOM, "pkv_seq_append: no free block");
     a->append_one(it->second, slot, cow_src, cow_dst);
     return PKV_OK;
@@ -175,9 +270,9 @@ int pkv_step_append(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots
             s.len += 1;
         }
     }
-    if (need > (int64_t)a->free_stack.size())
+    if (need > (int64_t)a->available())
         return pkv_fail(PKV_ERR_OOM, "pkv_step_append: %lld blocks needed, %zu free",
-                        (long long)need, a->free_stack.size());
+                        (long long)need, a->available());
     int np = 0;
     for (int i = 0; i < n; ++i) {
         int64_t src, dst;
@@ -229,9 +324,9 @@ int pkv_seq_swap(pkv_allocator* from, pkv_allocator* to, int64_t seq, int64_t* p
     const int n = (int)t.size();
     if (n > 0 && !pairs) return pkv_fail(PKV_ERR_NULL, "pkv_seq_swap: pairs is NULL");
     if (n > cap) return pkv_fail(PKV_ERR_SHAPE, "pkv_seq_swap: %d pairs, cap %d", n, cap);
-    if (n > (int)to->free_stack.size())
+    if (n > (int)to->available())
         return pkv_fail(PKV_ERR_OOM, "pkv_seq_swap: %d blocks needed, %zu free", n,
-                        to->free_stack.size());
+                        to->available());
     pkv_allocator::Seq moved;
     moved.len = it->second.len;
     moved.table.reserve(n);
@@ -245,6 +340,88 @@ int pkv_seq_swap(pkv_allocator* from, pkv_allocator* to, int64_t seq, int64_t* p
     from->seqs.erase(it);
     to->seqs.emplace(seq, std::move(moved));
     *num_pairs = n;
+    return PKV_OK;
+}
+
+int pkv_seq_add_cached(pkv_allocator* a, int64_t seq, const int32_t* tokens, int n,
+                       int* reused_tokens)
+{
+    if (!a || !reused_tokens || (n > 0 && !tokens))
+        return pkv_fail(PKV_ERR_NULL, "pkv_seq_add_cached: NULL argument");
+    if (n < 0) return pkv_fail(PKV_ERR_SHAPE, "pkv_seq_add_cached: negative length");
+    if (a->seqs.count(seq)) return pkv_fail(PKV_ERR_STATE, "pkv_seq_add_cached: sequence exists");
+    const int B = a->block_size;
+    const int64_t nblocks = (n + (int64_t)B - 1) / B;
+    // the longest chain of cached full blocks matching the prompt
+    std::vector<int32_t> hits;
+    uint64_t parent = 0;
+    int64_t revive = 0;
+    for (int64_t i = 0; i < n / B; ++i) {
+        const uint64_t k = block_key(parent, tokens + i * B, B);
+        const int32_t b = a->lookup(k, parent, tokens + i * B);
+        if (b < 0) break;
+        hits.push_back(b);
+        if (a->ref[b] == 0) ++revive;
+        parent = k;
+    }
+    const int64_t fresh = nblocks - (int64_t)hits.size();
+    if (fresh > (int64_t)a->available() - revive)
+        return pkv_fail(PKV_ERR_OOM, "pkv_seq_add_cached: %lld blocks needed, %zu free",
+                        (long long)fresh, a->available() - (size_t)revive);
+    pkv_allocator::Seq s;
+    s.table.reserve(nblocks);
+    for (int32_t b : hits) {
+        a->take(b);
+        s.table.push_back(b);
+    }
+    for (int64_t i = 0; i < fresh; ++i) s.table.push_back(a->pop());
+    s.len = n;
+    a->seqs.emplace(seq, std::move(s));
+    a->prefix_hits += (int64_t)hits.size();
+    *reused_tokens = (int)hits.size() * B;
+    return PKV_OK;
+}
+
+int pkv_seq_register_blocks(pkv_allocator* a, int64_t seq, const int32_t* tokens, int n,
+                            int* registered)
+{
+    if (!a || !registered || (n > 0 && !tokens))
+        return pkv_fail(PKV_ERR_NULL, "pkv_seq_register_blocks: NULL argument");
+    auto it = a->seqs.find(seq);
+    if (it == a->seqs.end())
+        return pkv_fail(PKV_ERR_STATE, "pkv_seq_register_blocks: unknown sequence");
+    if (n < 0 || n > it->second.len)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_seq_register_blocks: %d tokens, sequence holds %lld",
+                        n, (long long)it->second.len);
+    const int B = a->block_size;
+    const std::vector<int32_t>& t = it->second.table;
+    uint64_t parent = 0;
+    int added = 0;
+    for (int i = 0; i < n / B; ++i) {
+        const uint64_t k = block_key(parent, tokens + (size_t)i * B, B);
+        const int32_t b = t[i];
+        if (!a->registered[b] && a->index.find(k) == a->index.end()) {
+            a->index.emplace(k, b);
+            a->registered[b] = 1;
+            a->key[b] = k;
+            a->parent_key[b] = parent;
+            std::memcpy(&a->tokens[(size_t)b * B], tokens + (size_t)i * B, sizeof(int32_t) * B);
+            ++added;
+        }
+        parent = k;
+    }
+    *registered = added;
+    return PKV_OK;
+}
+
+int pkv_prefix_cache_stats(pkv_allocator* a, int64_t* hit_blocks, int64_t* cached_blocks,
+                           int64_t* cached_free_blocks)
+{
+    if (!a || !hit_blocks || !cached_blocks || !cached_free_blocks)
+        return pkv_fail(PKV_ERR_NULL, "pkv_prefix_cache_stats: NULL argument");
+    *hit_blocks = a->prefix_hits;
+    *cached_blocks = (int64_t)a->index.size();
+    *cached_free_blocks = (int64_t)a->cached_free.size();
     return PKV_OK;
 }
 
@@ -309,7 +486,7 @@ int pkv_refcount(pkv_allocator* a, int block, int* count)
 int pkv_num_free_blocks(pkv_allocator* a, int* n)
 {
     if (!a || !n) return pkv_fail(PKV_ERR_NULL, "pkv_num_free_blocks: NULL argument");
-    *n = (int)a->free_stack.size();
+    *n = (int)a->available();
     return PKV_OK;
 }
 
@@ -325,7 +502,7 @@ int pkv_stats(pkv_allocator* a, int64_t* allocated_positions, int64_t* valid_pos
     }
     *allocated_positions = alloc;
     *valid_positions = valid;
-    *blocks_in_use = (int64_t)a->num_blocks - (int64_t)a->free_stack.size();
+    *blocks_in_use = (int64_t)a->num_blocks - (int64_t)a->available();
     return PKV_OK;
 }
 

@@ -234,6 +234,60 @@ def test_swap_matches_reference_between_two_pools(seed):
         cg.swap_to(cg, next(iter(where)) if where else 0)
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_prefix_cache_matches_reference(seed):
+    rnd = random.Random(200 + seed)
+    B = 4
+    order = list(np.random.default_rng(seed).permutation(40))
+    cpp, ref = pkv.BlockAllocator(40, B, free_order=order), BlockManager(40, B, free_order=order)
+    templates = [[rnd.randrange(50) for _ in range(rnd.randint(4, 17))] for _ in range(3)]
+    toks = {}
+    nid = 0
+    for _ in range(1200):
+        op = rnd.random()
+        live = list(toks)
+        if op < 0.3 or not live:
+            prompt = rnd.choice(templates)[:rnd.randint(0, 17)] + \
+                [rnd.randrange(50) for _ in range(rnd.randint(0, 5))]
+            try:
+                r = ref.add_cached(nid, prompt)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    cpp.add_cached(nid, prompt)
+            else:
+                assert cpp.add_cached(nid, prompt) == r
+                toks[nid] = list(prompt)
+            nid += 1
+        elif op < 0.5:
+            s = rnd.choice(live)
+            n = rnd.randint(0, len(toks[s]))
+            assert cpp.register_blocks(s, toks[s][:n]) == ref.register_blocks(s, toks[s][:n])
+        elif op < 0.7:
+            s = rnd.choice(live)
+            try:
+                r = ref.append(s)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    cpp.append(s)
+            else:
+                assert cpp.append(s) == r
+                toks[s].append(rnd.randrange(50))
+        elif op < 0.78:
+            s = rnd.choice(live)
+            ref.fork(s, nid)
+            cpp.fork(s, nid)
+            toks[nid] = list(toks[s])
+            nid += 1
+        else:
+            s = live[rnd.randrange(len(live))]
+            ref.free_seq(s)
+            cpp.free(s)
+            del toks[s]
+        _same(cpp, ref, list(toks))
+        assert cpp.prefix_cache_stats() == ref.prefix_cache_stats()
+        ref.check_invariants()
+
+
 def test_allocator_errors_leave_state_unchanged():
     a = pkv.BlockAllocator(3, 4)
     a.add(0, 8)

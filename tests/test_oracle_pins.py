@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from oracle.blockmgr import BlockManager, OutOfBlocks
+from oracle.blockmgr import BlockManager, OutOfBlocks, block_key, fnv1a64
 from workloads import WORKLOADS, make_decode_case, normal_values
 
 pytestmark = pytest.mark.filterwarnings("ignore")
@@ -481,6 +481,87 @@ def test_swap_out_and_back_preserves_every_sequence():
     with pytest.raises(OutOfBlocks):
         gpu.swap_to(BlockManager(1, B), 0)  # needs 3 blocks
     assert gpu.length(0) == 9
+
+
+# --------------------------------------------------------------------------
+# Automatic prefix caching (hash of a block and everything before it).
+# --------------------------------------------------------------------------
+
+def test_fnv1a64_published_vectors():
+    # Test vectors of the FNV-1a 64-bit hash (Fowler/Noll/Vo reference list).
+    assert fnv1a64(b"") == 0xcbf29ce484222325
+    assert fnv1a64(b"a") == 0xaf63dc4c8601ec8c
+    assert fnv1a64(b"foobar") == 0x85944171f73967e8
+
+
+def test_block_key_depends_on_every_preceding_token():
+    a = block_key(0, [1, 2, 3, 4])
+    assert a != block_key(0, [1, 2, 3, 5])
+    assert block_key(a, [9, 9, 9, 9]) != block_key(block_key(0, [1, 2, 3, 5]), [9, 9, 9, 9])
+    assert block_key(0, [-1, 0, 0, 0]) == fnv1a64(bytes(8) + b"\xff\xff\xff\xff" + bytes(12))
+
+
+def test_prefix_cache_reuses_blocks_and_keeps_outputs():
+    # Sequence 1 shares 2 full blocks of prompt with sequence 0 and differs in
+    # the third: it reuses exactly those 2 blocks, only its own tokens are
+    # written, and its attention equals attention over a fresh full copy.
+    B, Hkv, D, Hq = 4, 2, 8, 2
+    mgr = BlockManager(16, B)
+    g = torch.Generator().manual_seed(33)
+    tok0 = [5, 6, 7, 8, 9, 10, 11, 12, 13, 14]
+    tok1 = tok0[:8] + [99, 98, 97]
+    K = {t: torch.randn(Hkv, D, generator=g) for t in set(tok0 + tok1)}  # KV of a token
+    kc = torch.full((16, Hkv, B, D), float("nan"))
+    vc = torch.full_like(kc, float("nan"))
+
+    def write(seq, tokens, start):
+        table = mgr.table(seq)
+        slots = torch.tensor([oracle.slot_for_position(table, p, B)
+                              for p in range(start, len(tokens))])
+        ks = torch.stack([K[t] for t in tokens[start:]])
+        oracle.kv_write(kc, vc, ks, -ks, slots, B)
+
+    assert mgr.add_cached(0, tok0) == 0
+    write(0, tok0, 0)
+    assert mgr.register_blocks(0, tok0) == 2
+    reused = mgr.add_cached(1, tok1)
+    assert reused == 8 and mgr.table(1)[:2] == mgr.table(0)[:2]
+    assert mgr.table(1)[2] != mgr.table(0)[2]
+    write(1, tok1, reused)
+    q = torch.randn(1, Hq, D, generator=g)
+    bt = torch.tensor([mgr.table(1)], dtype=torch.int32)
+    out = oracle.paged_decode_attention(q, kc, vc, bt, torch.tensor([11], dtype=torch.int32),
+                                        0.5, B, Hkv)
+    ks = torch.stack([K[t] for t in tok1])  # [11, Hkv, D]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q.double()[:, :, None, :].transpose(0, 1), ks.double().transpose(0, 1)[:, None],
+        -ks.double().transpose(0, 1)[:, None], scale=0.5)
+    np.testing.assert_allclose(out[0], ref[:, 0, 0, :].numpy(), rtol=1e-12, atol=1e-12)
+    assert mgr.prefix_cache_stats() == (2, 2, 0)
+    mgr.check_invariants()
+
+
+def test_prefix_cache_keeps_freed_blocks_until_the_pool_runs_dry():
+    B = 2
+    mgr = BlockManager(6, B)
+    t = [1, 2, 3, 4, 5]
+    mgr.add_cached(0, t)
+    mgr.register_blocks(0, t)
+    kept = mgr.table(0)[:2]
+    mgr.free_seq(0)
+    assert mgr.num_free() == 6 and mgr.prefix_cache_stats()[2] == 2
+    assert mgr.add_cached(1, t) == 4 and mgr.table(1)[:2] == kept  # revived
+    mgr.free_seq(1)
+    # released last to first: the cached list holds block 1 (oldest), block 0
+    mgr.add(2, 10)  # 5 blocks: the 4 plain free ones, then block 1 is evicted
+    assert mgr.prefix_cache_stats()[1:] == (1, 1)
+    assert kept[1] in mgr.table(2) and kept[0] not in mgr.table(2)
+    mgr.free_seq(2)
+    assert mgr.add_cached(3, t) == 2 and mgr.table(3)[0] == kept[0]  # block 0 survived
+    mgr.check_invariants()
+    with pytest.raises(OutOfBlocks):
+        mgr.add_cached(4, [7] * 12)
+    assert mgr.table(3)[0] == kept[0]
 
 
 # --------------------------------------------------------------------------

@@ -307,6 +307,52 @@ def test_swap_round_trip_keeps_attention():
     assert torch.equal(before, after)
 
 
+def test_prefix_cached_sequence_attends_like_a_fresh_one():
+    # Sequence 1 reuses sequence 0's cached prompt blocks; only its own tokens
+    # are written on the GPU.  Its attention must equal the oracle's over a
+    # cache where every token of sequence 1 was written afresh.
+    B, Hkv, D, Hq = 16, 4, 128, 16
+    g = torch.Generator().manual_seed(9)
+    vocab = 64
+    KV = torch.randn(vocab, 2, Hkv, D, generator=g).to(torch.bfloat16)  # K/V of a token id
+    tok0 = torch.randint(0, vocab, (300,), generator=g).tolist()
+    tok1 = tok0[:256] + torch.randint(0, vocab, (37,), generator=g).tolist()
+    mgr = pkv.BlockAllocator(64, B)
+    kc = torch.full((64, Hkv, B, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    vc = torch.full_like(kc, float("nan"))
+
+    def write(seq, tokens, start):
+        table = mgr.table(seq)
+        slots = torch.tensor([oracle.slot_for_position(table, p, B)
+                              for p in range(start, len(tokens))], dtype=torch.int64)
+        kv = KV[torch.tensor(tokens[start:])]
+        pkv.kv_write(kc, vc, kv[:, 0].contiguous().to(DEV), kv[:, 1].contiguous().to(DEV),
+                     slots.to(DEV))
+
+    assert mgr.add_cached(0, tok0) == 0
+    write(0, tok0, 0)
+    assert mgr.register_blocks(0, tok0) == 300 // B
+    reused = mgr.add_cached(1, tok1)
+    assert reused == 256
+    write(1, tok1, reused)
+    q = torch.randn(1, Hq, D, generator=g).to(torch.bfloat16)
+    bt = torch.tensor([mgr.table(1)], dtype=torch.int32)
+    cl = torch.tensor([len(tok1)], dtype=torch.int32)
+    out = gpu_decode(q, kc, vc, bt, cl, D ** -0.5, B, Hkv)
+    # fresh: every token of sequence 1 written into its own blocks on the host
+    fk = torch.full((64, Hkv, B, D), float("nan"), dtype=torch.bfloat16)
+    fv = torch.full_like(fk, float("nan"))
+    fresh_table = list(range(-(-len(tok1) // B)))
+    kv = KV[torch.tensor(tok1)]
+    oracle.kv_write(fk, fv, kv[:, 0].contiguous(), kv[:, 1].contiguous(),
+                    torch.tensor([oracle.slot_for_position(fresh_table, p, B)
+                                  for p in range(len(tok1))]), B)
+    ref = oracle.paged_decode_attention(q, fk, fv, torch.tensor([fresh_table], dtype=torch.int32),
+                                        cl, D ** -0.5, B, Hkv)
+    assert pkv.device_status() == 0
+    assert max_err(out, ref) <= TOL16
+
+
 def test_nan_poison_and_physical_permutation():
     # Same logical data paged twice with different physical ids: same output.
     w = Workload(0, "perm", "f16", 16, 4, 128, 16, 4, "fixed")
