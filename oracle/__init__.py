@@ -14,6 +14,10 @@ Language Model Serving with PagedAttention", Kwon et al. 2023):
   "key techniques" 1 (block table lookup assembles scattered K/V blocks);
   auturnal guide section 1 (paging changes storage, not what attention reads)
   and its verification protocol (compare with a contiguous-KV baseline).
+* ``paged_prefill_attention`` -- the same attention for several new query
+  tokens per sequence, each causal over the sequence's tokens up to its own
+  position (cayang0802 walkthrough, recomputation: a whole prompt's KV is
+  produced in one parallel pass).
 * ``kv_write`` -- cayang0802 page, KV-cache paragraph: only the new token's
   K and V are computed and stored; slot = block * B + offset (core idea 3).
 * ``kv_copy_blocks`` -- auturnal guide section 3 and aiplusplus "key
@@ -44,7 +48,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "DTYPE_CODE", "paged_decode_attention", "kv_write", "kv_copy_blocks",
+    "DTYPE_CODE", "paged_decode_attention", "paged_prefill_attention", "kv_write", "kv_copy_blocks",
     "kv_swap_blocks", "slot_for_position", "kv_bytes", "allocated_positions", "tail_waste",
     "position_utilisation", "fixed_reservation_positions", "gather_sequence",
     "decode_partitions", "lse_combine", "widen",
@@ -65,10 +69,13 @@ def _load():
         lib.orc_kv_write.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
         lib.orc_kv_copy_blocks.argtypes = [P, P, P, I, I, I, I, I, I]
         lib.orc_kv_swap_blocks.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I]
+        lib.orc_paged_prefill_attention.argtypes = [
+            P, P, P, P, I, P, P, P, D, I, I, I, I, I, I, I, I]
         lib.orc_paged_decode_attention.argtypes = [
             P, P, P, P, I, P, P, D, I, I, I, I, I, I, I, I]
         for f in (lib.orc_widen, lib.orc_kv_write, lib.orc_kv_copy_blocks,
-                  lib.orc_kv_swap_blocks, lib.orc_paged_decode_attention):
+                  lib.orc_kv_swap_blocks, lib.orc_paged_decode_attention,
+                  lib.orc_paged_prefill_attention):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -114,6 +121,32 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
         int(block_size), int(num_kv_heads), S, Hq, D, bt.shape[1], NB, int(nthreads))
     if rc != 0:
         raise ValueError("orc_paged_decode_attention failed: %d" % rc)
+    return out
+
+
+def paged_prefill_attention(q, k_cache, v_cache, block_tables, context_lens, query_start,
+                            scale, block_size, num_kv_heads, nthreads=1) -> np.ndarray:
+    """Multi-token (prefill) attention over paged KV: rows query_start[s] ..
+    query_start[s+1]-1 of q ([rows, Hq, D]) are the last qn_s tokens of
+    sequence s; row t of s sits at position L_s - qn_s + t and attends to the
+    sequence's tokens 0 .. L_s - qn_s + t (causal).  Returns float64
+    [rows, Hq, D].  (cayang0802 walkthrough: the KV of a whole prompt can be
+    computed in one parallel pass -- the prefill that recomputation relies
+    on.)"""
+    q, k_cache, v_cache = _cpu(q), _cpu(k_cache), _cpu(v_cache)
+    bt = _cpu(block_tables).to(torch.int32)
+    cl = _cpu(context_lens).to(torch.int32)
+    qs = _cpu(query_start).to(torch.int32)
+    R, Hq, D = q.shape
+    S = cl.numel()
+    out = np.full((R, Hq, D), np.nan, dtype=np.float64)
+    rc = _load().orc_paged_prefill_attention(
+        out.ctypes.data, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        DTYPE_CODE[q.dtype], bt.data_ptr(), cl.data_ptr(), qs.data_ptr(), float(scale),
+        int(block_size), int(num_kv_heads), S, Hq, D, bt.shape[1], k_cache.shape[0],
+        int(nthreads))
+    if rc != 0:
+        raise ValueError("orc_paged_prefill_attention failed: %d" % rc)
     return out
 
 

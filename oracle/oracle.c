@@ -245,6 +245,87 @@ static int attend_one_sequence(const attn_job* j, int s)
     return ORC_OK;
 }
 
+/* Multi-token (prefill) form: the query rows query_start[s] ..
+ * query_start[s+1]-1 are the last qn tokens of sequence s; row t sits at
+ * position L - qn + t and attends causally to tokens 0 .. L - qn + t. */
+typedef struct {
+    attn_job base;
+    const int32_t* query_start;
+} prefill_job;
+
+static int prefill_one_sequence(const prefill_job* pj, int s)
+{
+    const attn_job* j = &pj->base;
+    const int B = j->B, Hkv = j->Hkv, Hq = j->Hq, D = j->D;
+    const int G = Hq / Hkv;
+    const int L = j->context_lens[s];
+    const int r0 = pj->query_start[s], qn = pj->query_start[s + 1] - r0;
+    if (L < 0 || (int64_t)L > (int64_t)j->max_blocks * B || qn < 0 || qn > L) return ORC_BAD_LEN;
+    if (qn == 0) return ORC_OK;
+    double* K = malloc(sizeof(double) * (size_t)L * Hkv * D);
+    double* V = malloc(sizeof(double) * (size_t)L * Hkv * D);
+    double* z = malloc(sizeof(double) * (size_t)L);
+    double* qd = malloc(sizeof(double) * (size_t)D);
+    if (!K || !V || !z || !qd) {
+        free(K); free(V); free(z); free(qd);
+        return ORC_NO_MEM;
+    }
+    const int32_t* table = j->block_tables + (size_t)s * j->max_blocks;
+    for (int i = 0; i < L; ++i) {
+        int32_t phys = table[i / B];
+        if (phys < 0 || phys >= j->NB) {
+            free(K); free(V); free(z); free(qd);
+            return ORC_BAD_BLOCK;
+        }
+        for (int g = 0; g < Hkv; ++g)
+            for (int d = 0; d < D; ++d) {
+                size_t src = (((size_t)phys * Hkv + g) * B + i % B) * D + d;
+                K[((size_t)i * Hkv + g) * D + d] = load_elem(j->k_cache, j->dtype, src);
+                V[((size_t)i * Hkv + g) * D + d] = load_elem(j->v_cache, j->dtype, src);
+            }
+    }
+    for (int t = 0; t < qn; ++t) {
+        const int last = L - qn + t;  /* newest key this row may see */
+        for (int h = 0; h < Hq; ++h) {
+            const int g = h / G;
+            const size_t row = ((size_t)(r0 + t) * Hq + h) * D;
+            for (int d = 0; d < D; ++d) qd[d] = load_elem(j->q, j->dtype, row + d);
+            double m = -INFINITY;
+            for (int i = 0; i <= last; ++i) {
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += qd[d] * K[((size_t)i * Hkv + g) * D + d];
+                z[i] = j->scale * dot;
+                if (z[i] > m) m = z[i];
+            }
+            double den = 0.0;
+            for (int i = 0; i <= last; ++i) {
+                z[i] = exp(z[i] - m);
+                den += z[i];
+            }
+            for (int d = 0; d < D; ++d) {
+                double num = 0.0;
+                for (int i = 0; i <= last; ++i) num += z[i] * V[((size_t)i * Hkv + g) * D + d];
+                j->out[row + d] = num / den;
+            }
+        }
+    }
+    free(K); free(V); free(z); free(qd);
+    return ORC_OK;
+}
+
+static void* prefill_worker(void* arg)
+{
+    prefill_job* pj = (prefill_job*)arg;
+    for (int s = pj->base.tid; s < pj->base.S; s += pj->base.nthreads) {
+        int rc = prefill_one_sequence(pj, s);
+        if (rc != ORC_OK) {
+            pj->base.status = rc;
+            break;
+        }
+    }
+    return NULL;
+}
+
 static void* attn_worker(void* arg)
 {
     attn_job* j = (attn_job*)arg;
@@ -300,6 +381,47 @@ int orc_paged_decode_attention(double* out, const void* q, const void* k_cache,
     }
     for (int t = 0; t < nthreads; ++t)
         if (jobs[t].status != ORC_OK) rc = jobs[t].status;
+    free(jobs);
+    free(th);
+    return rc;
+}
+
+/* out: [total rows][num_heads][head_dim] doubles, rows as query_start says. */
+int orc_paged_prefill_attention(double* out, const void* q, const void* k_cache,
+                                const void* v_cache, int dtype, const int32_t* block_tables,
+                                const int32_t* context_lens, const int32_t* query_start,
+                                double scale, int block_size, int num_kv_heads, int num_seqs,
+                                int num_heads, int head_dim, int max_blocks_per_seq,
+                                int num_blocks, int nthreads)
+{
+    if (!elem_bytes(dtype) || block_size <= 0 || num_kv_heads <= 0 || num_heads <= 0 ||
+        head_dim <= 0 || num_seqs < 0 || num_heads % num_kv_heads != 0)
+        return ORC_BAD_ARG;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > num_seqs) nthreads = num_seqs > 0 ? num_seqs : 1;
+    prefill_job* jobs = calloc((size_t)nthreads, sizeof(prefill_job));
+    pthread_t* th = calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs); free(th);
+        return ORC_NO_MEM;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        attn_job j = {out, q, k_cache, v_cache, dtype, block_tables, context_lens, scale,
+                      block_size, num_kv_heads, num_seqs, num_heads, head_dim,
+                      max_blocks_per_seq, num_blocks, nthreads, t, ORC_OK};
+        jobs[t].base = j;
+        jobs[t].query_start = query_start;
+    }
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, prefill_worker, &jobs[t]) != 0) break;
+        ++started;
+    }
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+    for (int t = started; t < nthreads; ++t) prefill_worker(&jobs[t]);
+    int rc = ORC_OK;
+    for (int t = 0; t < nthreads; ++t)
+        if (jobs[t].base.status != ORC_OK) rc = jobs[t].base.status;
     free(jobs);
     free(th);
     return rc;

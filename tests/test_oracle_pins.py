@@ -314,6 +314,51 @@ def test_threads_do_not_change_bits():
 
 
 # --------------------------------------------------------------------------
+# Prefill (several query tokens per sequence, causal).
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_prefill_matches_sdpa_with_causal_mask(dtype):
+    S, Hq, Hkv, D, B = 3, 6, 2, 16, 8
+    Kl, Vl = _random_logical(61, S, 60, Hkv, D, dtype, Lmin=10)
+    lens = [k.shape[0] for k in Kl]
+    qn = [lens[0], 3, 1]  # a whole prompt, a 3-token chunk, one token
+    starts = torch.tensor([0, qn[0], qn[0] + qn[1], sum(qn)], dtype=torch.int32)
+    g = torch.Generator().manual_seed(4)
+    q = torch.randn(sum(qn), Hq, D, generator=g).to(dtype)
+    kc, vc, bt, cl = _scatter_case(Kl, Vl, B, 40, dtype, seed=8, Hq=Hq)
+    out = oracle.paged_prefill_attention(q, kc, vc, bt, cl, starts, 0.3, B, Hkv)
+    for s in range(S):
+        L, n = lens[s], qn[s]
+        rows = q[starts[s]:starts[s + 1]].to(torch.float64).transpose(0, 1)[None]  # [1,Hq,n,D]
+        mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]     # [n, L]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            rows, Kl[s].double().transpose(0, 1)[None], Vl[s].double().transpose(0, 1)[None],
+            attn_mask=mask, scale=0.3, enable_gqa=True)[0].transpose(0, 1).numpy()
+        np.testing.assert_allclose(out[starts[s]:starts[s + 1]], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_last_row_is_decode_and_first_row_is_v0():
+    w = WORKLOADS[1]
+    case = make_decode_case(w, seed=3, lengths=[40, 17])
+    L = case.context_lens.tolist()
+    g = torch.Generator().manual_seed(2)
+    q = torch.randn(sum(L), 4, 64, generator=g)
+    starts = torch.tensor([0, L[0], L[0] + L[1]], dtype=torch.int32)
+    out = oracle.paged_prefill_attention(q, case.k_cache, case.v_cache, case.block_tables,
+                                         case.context_lens, starts, w.scale, 16, 4)
+    last = torch.stack([q[L[0] - 1], q[L[0] + L[1] - 1]])
+    dec = oracle.paged_decode_attention(last, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, 16, 4)
+    assert np.array_equal(out[[L[0] - 1, L[0] + L[1] - 1]], dec)
+    v0 = case.v_cache[int(case.block_tables[0, 0]), :, 0, :].double().numpy()
+    assert np.array_equal(out[0], v0)
+    with pytest.raises(ValueError):  # more query rows than context
+        oracle.paged_prefill_attention(q[:50], case.k_cache, case.v_cache, case.block_tables,
+                                       case.context_lens, torch.tensor([0, 41, 50]), 0.1, 16, 4)
+
+
+# --------------------------------------------------------------------------
 # Split-context form: log-sum-exp combination equals the one-pass result.
 # --------------------------------------------------------------------------
 
