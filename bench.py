@@ -444,6 +444,63 @@ def run_sweep(args):
                 print(json.dumps(line), flush=True)
 
 
+def measured_bf16_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured burst cuBLAS bf16"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback 1.9 PFLOP/s"
+
+
+def run_prefill(args):
+    """Paged prefill: 16 sequences whose whole 2048-token prompts attend
+    causally over the paged cache (bf16, 32 query / 8 KV heads x 128, block
+    16).  Reports attention TFLOP/s (4 * D per query head per attended key)
+    against the measured dense bf16 tensor peak."""
+    import paged_kv_cache_312_gb300 as pkv
+    import __graft_entry__
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    S, L, Hq, Hkv, D, B = 16, 2048, 32, 8, 128, 16
+    w = Workload(0, "prefill-bf16-32x8-d128-b16-16x2048", "bf16", Hq, Hkv, D, B, S, "fixed",
+                 fixed_lengths=(L,) * S)
+    case = make_decode_case(w, seed=args.seed)
+    kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
+    bt, cl = case.block_tables.to(dev), case.context_lens.to(dev)
+    qs = torch.arange(0, (S + 1) * L, L, dtype=torch.int32, device=dev)
+    q = torch.randn(S * L, Hq, D, device=dev).to(torch.bfloat16)
+    out = torch.empty(S * L, Hq, D, dtype=torch.bfloat16, device=dev)
+
+    def call():
+        pkv.paged_prefill_attention(out, q, kc, vc, bt, cl, qs, w.scale, B, Hkv,
+                                    max_query_len=L, stream=stream)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    steps = max(1, min(args.steps, 50))
+    a.record(stream)
+    for _ in range(steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    assert pkv.device_status() == 0
+    ms = a.elapsed_time(b) / steps
+    keys = S * L * (L + 1) // 2  # attended (query, key) pairs per head
+    flops = 4 * D * Hq * keys
+    peak, src = measured_bf16_tflops()
+    tf = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({"prefill": {"workload": w.name, "query_tokens": S * L, "causal": True},
+                      "ms": round(ms, 4), "tflops": round(tf, 1),
+                      "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                                   "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                                   "peak_source": src},
+                      "kv_bytes": int(case.context_lens.sum()) * 2 * Hkv * D * 2}), flush=True)
+
+
 def run_swap(args):
     """Preemption by swapping: move every block of 64 sequences x 2048 tokens
     (bf16, 8 KV heads x 128) from the device cache to a pinned host pool and
@@ -518,6 +575,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=8.0)
+    ap.add_argument("--prefill", action="store_true",
+                    help="paged prefill throughput (one JSON line; not the benchmark line)")
     ap.add_argument("--swap", action="store_true",
                     help="device <-> pinned host block swap throughput (one JSON line per "
                          "block size and direction; not the benchmark line)")
@@ -537,6 +596,9 @@ def main():
         return
     if args.swap:
         run_swap(args)
+        return
+    if args.prefill:
+        run_prefill(args)
         return
     if args.impl == "reference":
         if rank != 0:

@@ -148,6 +148,33 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
                                int out_dtype, int partition_size, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/*
+ * paged_prefill_attention -- several new query tokens per sequence (a prompt,
+ * or a chunk of one), each attending causally over the sequence's cached
+ * tokens up to its own position.  [CAY recomputation]: a whole sequence's KV
+ * can be produced in one parallel pass, the prefill that recomputing a
+ * preempted sequence relies on; the attention itself is the one above
+ * ([AIPP key techniques 1], [AUT section 1]) with a causal limit:
+ *     out[r,h,:] = sum_{i <= L_s - qn_s + t} softmax_i(scale q[r,h,:] . K_s[i,g,:]) V_s[i,g,:]
+ * for row r = query_start[s] + t, t < qn_s = query_start[s+1] - query_start[s].
+ * The new tokens' K/V must already be in the cache (pkv_kv_write).
+ *
+ * q, out      : [rows][num_heads][head_dim], rows = query_start[num_seqs];
+ *               q 16-byte aligned.
+ * query_start : int32 [num_seqs + 1], non-decreasing, device memory.
+ * max_query_len : >= every qn_s (sizes the grid).  A sequence with qn_s >
+ *               max_query_len or qn_s > context_lens[s] is skipped and sets
+ *               PKV_STATUS_BAD_LEN.
+ * 16-bit KV only (PKV_ERR_UNSUPPORTED for fp32); head_dim in {64,128};
+ * block_size in {8,16,32}; no workspace.
+ */
+int pkv_paged_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                const int32_t* query_start, float scale, int block_size,
+                                int num_kv_heads, int num_seqs, int num_heads, int head_dim,
+                                int max_blocks_per_seq, int num_blocks, int max_query_len,
+                                int kv_dtype, int out_dtype, void* stream);
+
 /* Workspace bytes pkv_paged_decode_attention needs for these sizes, where
  * max_context_len = max_blocks_per_seq * block_size.  0 if partition_size==0. */
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,

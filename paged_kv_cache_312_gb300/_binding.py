@@ -32,6 +32,8 @@ _SIGS = {
     "pkv_paged_decode_attention": (_I, [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I,
                                         _I, _I, _I, _P, _SZ, _P]),
     "pkv_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_paged_prefill_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I,
+                                         _I, _I, _I, _I, _I, _P]),
     "pkv_paged_decode_attention_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I,
                                                 _I, _I, _I, _I, _I, _P]),
     "pkv_kv_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
@@ -161,6 +163,30 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
         DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], int(partition_size), ws_ptr, ws_bytes,
         _stream(stream))
     _check(rc, "pkv_paged_decode_attention")
+
+
+def paged_prefill_attention(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                            scale, block_size, num_kv_heads, max_query_len=None, stream=None):
+    """Causal multi-token attention over the paged cache: rows
+    query_start[s]..query_start[s+1]-1 of q ([rows, Hq, D]) are the last
+    tokens of sequence s."""
+    R, Hq, D = q.shape
+    NB, Hkv, B, Dk = k_cache.shape
+    S = context_lens.shape[0]
+    if (Hkv, B, Dk) != (num_kv_heads, block_size, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("paged_prefill_attention: cache shape mismatch")
+    if out.shape != q.shape or query_start.dtype != torch.int32 or \
+            query_start.shape != (S + 1,) or block_tables.shape[0] != S:
+        raise ValueError("paged_prefill_attention: bad out/query_start/table tensors")
+    if max_query_len is None:
+        raise ValueError("paged_prefill_attention: pass max_query_len (a host integer)")
+    rc = lib().pkv_paged_prefill_attention(
+        _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables"), _dev(context_lens, "context_lens"),
+        _dev(query_start, "query_start"), float(scale), int(block_size), int(num_kv_heads), S,
+        Hq, D, block_tables.shape[1], NB, int(max_query_len), DTYPE_CODE[q.dtype],
+        DTYPE_CODE[out.dtype], _stream(stream))
+    _check(rc, "pkv_paged_prefill_attention")
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

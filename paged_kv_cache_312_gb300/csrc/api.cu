@@ -236,6 +236,71 @@ int pkv_kv_swap_blocks(void* dst_k_cache, void* dst_v_cache, const void* src_k_c
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "pkv_kv_swap_blocks launch");
 }
 
+int pkv_paged_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                const int32_t* query_start, float scale, int block_size,
+                                int num_kv_heads, int num_seqs, int num_heads, int head_dim,
+                                int max_blocks_per_seq, int num_blocks, int max_query_len,
+                                int kv_dtype, int out_dtype, void* stream)
+{
+    static const char* fn = "pkv_paged_prefill_attention";
+    if (!pkv_dtype_bytes(kv_dtype) || !pkv_dtype_bytes(out_dtype))
+        return pkv_fail(PKV_ERR_DTYPE, "%s: dtype kv=%d out=%d", fn, kv_dtype, out_dtype);
+    if (kv_dtype == PKV_F32)
+        return pkv_fail(PKV_ERR_UNSUPPORTED, "%s: fp32 KV is not supported (16-bit only)", fn);
+    if (num_seqs < 0 || num_seqs > 65535)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: num_seqs %d outside [0, 65535]", fn, num_seqs);
+    if (head_dim != 64 && head_dim != 128)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: head_dim %d not in {64,128}", fn, head_dim);
+    if (block_size != 8 && block_size != 16 && block_size != 32)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: block_size %d not in {8,16,32}", fn, block_size);
+    if (num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads != 0 ||
+        num_heads > 65535)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: num_heads %d / num_kv_heads %d", fn, num_heads,
+                        num_kv_heads);
+    if (max_blocks_per_seq <= 0 || num_blocks <= 0 || max_query_len < 0)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: bad sizes", fn);
+    if ((int64_t)max_blocks_per_seq * block_size > (1ll << 30))
+        return pkv_fail(PKV_ERR_SHAPE, "%s: max context too long", fn);
+    if ((int64_t)num_blocks * num_kv_heads * block_size >= (1ll << 31))
+        return pkv_fail(PKV_ERR_SHAPE, "%s: cache has >= 2^31 rows", fn);
+    if (!std::isfinite(scale)) return pkv_fail(PKV_ERR_SHAPE, "%s: scale is not finite", fn);
+    if (num_seqs == 0 || max_query_len == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+        return pkv_fail(PKV_ERR_NULL, "%s: NULL pointer", fn);
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) ||
+        !aligned(out, pkv_dtype_bytes(out_dtype)))
+        return pkv_fail(PKV_ERR_ALIGN, "%s: caches and q need 16-byte alignment", fn);
+    PrefillParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.query_start = query_start;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.block_size = block_size;
+    p.num_kv_heads = num_kv_heads;
+    p.num_heads = num_heads;
+    p.head_dim = head_dim;
+    p.num_seqs = num_seqs;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.max_query_len = max_query_len;
+    p.out_dtype = out_dtype;
+    p.status = pkv_status_word_ptr();
+    if (!p.status) return pkv_fail(PKV_ERR_CUDA, "%s: no device status word", fn);
+    CUtensorMap kmap, vmap;
+    const uint64_t rows = (uint64_t)num_blocks * num_kv_heads * block_size;
+    int rc = tensor_map(k_cache, rows, head_dim, block_size, kv_dtype, &kmap);
+    if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap);
+    if (rc != PKV_OK) return rc;
+    cudaError_t e =
+        launch_prefill_tensor_core(p, kv_dtype, &kmap, &vmap, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "pkv_paged_prefill_attention launch");
+}
+
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
                                   int partition_size)
 {

@@ -27,6 +27,27 @@ struct DecodeParams {
     unsigned int* status;        // device status word (PKV_STATUS_* bits)
 };
 
+// Everything one prefill launch needs (passed by value).
+struct PrefillParams {
+    void* out;                   // [rows][Hq][D], out_dtype
+    const void* q;               // [rows][Hq][D], kv dtype
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables; // [S][max_blocks]
+    const int32_t* context_lens; // [S]
+    const int32_t* query_start;  // [S + 1] first query row of each sequence
+    float scale_log2;
+    int block_size, num_kv_heads, num_heads, head_dim;
+    int num_seqs, max_blocks, num_blocks, max_query_len;
+    int out_dtype;
+    unsigned int* status;
+};
+
+// Tensor-core paged prefill (16-bit KV): one CTA per (64 query rows, query
+// head, sequence); tensor maps as for the decode kernel.
+cudaError_t launch_prefill_tensor_core(const PrefillParams& p, int kv_dtype, const void* k_map,
+                                       const void* v_map, cudaStream_t stream);
+
 // Device status word of the current device (address of a __device__ symbol).
 unsigned int* pkv_status_word_ptr();
 

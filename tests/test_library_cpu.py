@@ -71,6 +71,25 @@ def test_decode_rejects_bad_arguments_on_host(kw, code):
     assert _attn(pkv.lib(), **kw) == code
 
 
+def test_prefill_rejects_bad_arguments_on_host():
+    L = pkv.lib()
+    P = ctypes.c_void_p
+
+    def call(**kw):
+        a = dict(kvdt=2, D=128, B=16, Hq=8, Hkv=2, S=2, maxq=5, q=256)
+        a.update(kw)
+        return L.pkv_paged_prefill_attention(P(256), P(a["q"]), P(256), P(256), P(256), P(256),
+                                             P(256), 0.1, a["B"], a["Hkv"], a["S"], a["Hq"],
+                                             a["D"], 4, 10, a["maxq"], a["kvdt"], 0, P(0))
+    assert call(kvdt=0) == -4      # fp32 KV not supported
+    assert call(D=96) == -2
+    assert call(B=4) == -2
+    assert call(Hq=7) == -2
+    assert call(maxq=-1) == -2
+    assert call(q=264) == -10
+    assert call(S=0) == 0 and call(maxq=0) == 0
+
+
 def test_decode_with_no_sequences_is_a_no_op():
     assert _attn(pkv.lib(), S=0, out=0, q=0) == 0
 

@@ -353,6 +353,86 @@ def test_prefix_cached_sequence_attends_like_a_fresh_one():
     assert max_err(out, ref) <= TOL16
 
 
+# --------------------------------------------------------------------------
+# paged prefill (causal multi-token queries)
+# --------------------------------------------------------------------------
+
+def gpu_prefill(q, kc, vc, bt, cl, qs, scale, B, Hkv, out_dtype=torch.float32):
+    out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=DEV)
+    qn = (qs[1:] - qs[:-1]).tolist()
+    pkv.paged_prefill_attention(out, q.to(DEV), kc, vc, bt.to(DEV), cl.to(DEV), qs.to(DEV),
+                                scale, B, Hkv, max_query_len=max(qn + [0]))
+    torch.cuda.synchronize()
+    return out
+
+
+PREFILL = [  # dtype, Hq, Hkv, D, B
+    ("bf16", 8, 2, 128, 16), ("f16", 4, 4, 128, 32), ("bf16", 16, 2, 64, 8),
+    ("f16", 6, 3, 64, 16), ("bf16", 32, 8, 128, 32), ("bf16", 8, 1, 128, 8),
+]
+
+
+@pytest.mark.parametrize("dt,Hq,Hkv,D,B", PREFILL)
+def test_prefill_small(dt, Hq, Hkv, D, B):
+    # whole prompts, chunks of longer contexts, single tokens, an empty query
+    # set; lengths off every tile boundary
+    lengths = [1, 17, 64, 65, 200, 300, 129, 40]
+    qn = [1, 17, 64, 65, 77, 1, 128, 0]
+    w = Workload(0, "prefill", dt, Hq, Hkv, D, B, len(lengths), "fixed")
+    case = make_decode_case(w, seed=Hq + D + B, lengths=lengths)
+    qs = torch.tensor([0] + list(np.cumsum(qn)), dtype=torch.int32)
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(int(qs[-1]), Hq, D, generator=g).to(w.torch_dtype)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, B, Hkv)
+    ref = oracle.paged_prefill_attention(q, case.k_cache, case.v_cache, case.block_tables,
+                                         case.context_lens, qs, w.scale, B, Hkv)
+    assert pkv.device_status() == 0
+    assert max_err(out, ref) <= TOL16
+
+
+def test_prefill_long_prompts_and_16bit_out():
+    w = Workload(0, "prefill-long", "bf16", 16, 4, 128, 16, 3, "fixed")
+    lengths = [1500, 777, 2048]
+    qn = [1500, 300, 1024]
+    case = make_decode_case(w, seed=77, lengths=lengths)
+    qs = torch.tensor([0] + list(np.cumsum(qn)), dtype=torch.int32)
+    q = torch.randn(int(qs[-1]), 16, 128, generator=torch.Generator().manual_seed(6)).to(
+        torch.bfloat16)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_prefill_attention(q, case.k_cache, case.v_cache, case.block_tables,
+                                         case.context_lens, qs, w.scale, 16, 4,
+                                         nthreads=oracle.default_threads())
+    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, 16, 4)
+    assert max_err(out, ref) <= TOL16
+    out16 = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, 16, 4,
+                        out_dtype=torch.bfloat16)
+    diff = np.abs(out16.cpu().double().numpy() - ref)
+    assert (diff <= TOL16 + 2.0 ** -8 * np.abs(ref)).all()
+    assert pkv.device_status() == 0
+
+
+def test_prefill_last_row_equals_decode_and_bad_lengths_flag():
+    w = Workload(0, "pd", "f16", 8, 2, 128, 16, 2, "fixed")
+    case = make_decode_case(w, seed=8, lengths=[333, 90])
+    qn = [40, 90]
+    qs = torch.tensor([0, 40, 130], dtype=torch.int32)
+    q = torch.randn(130, 8, 128, generator=torch.Generator().manual_seed(1)).to(torch.float16)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, 16, 2)
+    dec = gpu_decode(torch.stack([q[39], q[129]]), kc, vc, case.block_tables, case.context_lens,
+                     w.scale, 16, 2)
+    assert float((out[[39, 129]] - dec).abs().max()) <= 2 * TOL16
+    bad = torch.tensor([0, 40, 130 + 300], dtype=torch.int32)  # 390 rows for a 90-token context
+    q2 = torch.zeros(430, 8, 128, dtype=torch.float16)
+    out2 = torch.zeros(430, 8, 128, dtype=torch.float32, device=DEV)
+    pkv.paged_prefill_attention(out2, q2.to(DEV), kc, vc, case.block_tables.to(DEV),
+                                case.context_lens.to(DEV), bad.to(DEV), w.scale, 16, 2,
+                                max_query_len=390)
+    assert pkv.device_status() & 2
+    assert not out2[40:].any()
+
+
 def test_nan_poison_and_physical_permutation():
     # Same logical data paged twice with different physical ids: same output.
     w = Workload(0, "perm", "f16", 16, 4, 128, 16, 4, "fixed")
