@@ -56,8 +56,12 @@ def launch_partition(w, max_blocks: int) -> int:
 
 
 def kernel_sha() -> str:
-    p = os.path.join(ROOT, "paged_kv_cache_312_gb300", "csrc", "decode_tc.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    """Hash of the decode kernel's sources (the traffic figures above hold
+    only for the kernel they were captured from)."""
+    h = hashlib.sha256()
+    for name in ("decode_tc.cu", "tc_common.cuh"):
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_312_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
 
 
 # ---------------------------------------------------------------------------
@@ -476,29 +480,34 @@ def run_prefill(args):
     def call():
         pkv.paged_prefill_attention(out, q, kc, vc, bt, cl, qs, w.scale, B, Hkv,
                                     max_query_len=L, stream=stream)
-    for _ in range(args.warmup):
-        call()
-    torch.cuda.synchronize(dev)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    steps = max(1, min(args.steps, 50))
-    a.record(stream)
-    for _ in range(steps):
-        call()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    assert pkv.device_status() == 0
-    ms = a.elapsed_time(b) / steps
     keys = S * L * (L + 1) // 2  # attended (query, key) pairs per head
     flops = 4 * D * Hq * keys
     peak, src = measured_bf16_tflops()
-    tf = flops / (ms * 1e-3) / 1e12
-    print(json.dumps({"prefill": {"workload": w.name, "query_tokens": S * L, "causal": True},
-                      "ms": round(ms, 4), "tflops": round(tf, 1),
-                      "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
-                                   "unit": "TFLOP/s", "frac": round(tf / peak, 4),
-                                   "peak_source": src},
-                      "kv_bytes": int(case.context_lens.sum()) * 2 * Hkv * D * 2}), flush=True)
+    steps = max(1, min(args.steps, 50))
+    for name, kernel in (("tcgen05", pkv.PREFILL_TCGEN05), ("warp_mma", pkv.PREFILL_WARP_MMA)):
+        pkv.set_prefill_kernel(kernel)
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        assert pkv.device_status() == 0
+        ms = a.elapsed_time(b) / steps
+        tf = flops / (ms * 1e-3) / 1e12
+        print(json.dumps({"prefill": {"workload": w.name, "query_tokens": S * L, "causal": True,
+                                      "kernel": name},
+                          "ms": round(ms, 4), "tflops": round(tf, 1),
+                          "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                                       "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                                       "peak_source": src},
+                          "kv_bytes": int(case.context_lens.sum()) * 2 * Hkv * D * 2}),
+              flush=True)
+    pkv.set_prefill_kernel(pkv.PREFILL_WARP_MMA)
 
 
 def run_swap(args):

@@ -263,6 +263,18 @@ int pkv_kv_swap_blocks(void* dst_k_cache, void* dst_v_cache, const void* src_k_c
 #define PKV_KERNEL_CUDA_CORE 1
 int pkv_set_decode_kernel(int which);
 
+/*
+ * Kernel selection for pkv_paged_prefill_attention (process-wide):
+ * PKV_PREFILL_WARP_MMA (default) runs the warp-level mma.sync kernel (64
+ * query rows per CTA); PKV_PREFILL_TCGEN05 runs the 5th-generation
+ * tensor-core kernel (tcgen05 MMAs, accumulators in tensor memory, 128 rows
+ * per CTA).  Both compute the same result up to fp32 accumulation order.
+ * Returns PKV_ERR_SHAPE for an unknown value.
+ */
+#define PKV_PREFILL_TCGEN05 0
+#define PKV_PREFILL_WARP_MMA 1
+int pkv_set_prefill_kernel(int which);
+
 /* ==========================================================================
  * Host block allocator (host memory only; not thread-safe per handle).
  * [AIPP core idea 1-4, effects]: fixed-size blocks, a block table per

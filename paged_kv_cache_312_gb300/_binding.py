@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
 PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
 DTYPE_CODE = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
 KERNEL_AUTO, KERNEL_CUDA_CORE = 0, 1
+PREFILL_TCGEN05, PREFILL_WARP_MMA = 0, 1
 STATUS_BITS = {1: "bad block id", 2: "bad context length", 4: "bad slot", 8: "bad copy pair",
                16: "tile load timeout"}
 
@@ -44,6 +45,7 @@ _SIGS = {
     "pkv_prefix_cache_stats": (_I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                                     ctypes.POINTER(_I64)]),
     "pkv_set_decode_kernel": (_I, [_I]),
+    "pkv_set_prefill_kernel": (_I, [_I]),
     "pkv_alloc_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_alloc_destroy": (_I, [_P]),
     "pkv_seq_add": (_I, [_P, _I64, _I]),
@@ -265,6 +267,10 @@ def device_status(reset=True, stream=None):
 
 def set_decode_kernel(which):
     _check(lib().pkv_set_decode_kernel(int(which)), "pkv_set_decode_kernel")
+
+
+def set_prefill_kernel(which):
+    _check(lib().pkv_set_prefill_kernel(int(which)), "pkv_set_prefill_kernel")
 
 
 # ---------------------------------------------------------------------------

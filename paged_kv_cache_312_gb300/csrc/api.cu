@@ -20,6 +20,7 @@
 namespace {
 thread_local char g_err[512] = "";
 int g_decode_kernel = PKV_KERNEL_AUTO;
+int g_prefill_kernel = PKV_PREFILL_WARP_MMA;
 }  // namespace
 
 int pkv_fail(int code, const char* fmt, ...)
@@ -145,6 +146,14 @@ int pkv_set_decode_kernel(int which)
     if (which != PKV_KERNEL_AUTO && which != PKV_KERNEL_CUDA_CORE)
         return pkv_fail(PKV_ERR_SHAPE, "pkv_set_decode_kernel: unknown value %d", which);
     g_decode_kernel = which;
+    return PKV_OK;
+}
+
+int pkv_set_prefill_kernel(int which)
+{
+    if (which != PKV_PREFILL_TCGEN05 && which != PKV_PREFILL_WARP_MMA)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_set_prefill_kernel: unknown value %d", which);
+    g_prefill_kernel = which;
     return PKV_OK;
 }
 
@@ -297,7 +306,10 @@ int pkv_paged_prefill_attention(void* out, const void* q, const void* k_cache, c
     if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap);
     if (rc != PKV_OK) return rc;
     cudaError_t e =
-        launch_prefill_tensor_core(p, kv_dtype, &kmap, &vmap, static_cast<cudaStream_t>(stream));
+        g_prefill_kernel == PKV_PREFILL_WARP_MMA
+            ? launch_prefill_tensor_core(p, kv_dtype, &kmap, &vmap,
+                                         static_cast<cudaStream_t>(stream))
+            : launch_prefill_tcgen05(p, kv_dtype, &kmap, &vmap, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "pkv_paged_prefill_attention launch");
 }
 

@@ -48,6 +48,11 @@ struct PrefillParams {
 cudaError_t launch_prefill_tensor_core(const PrefillParams& p, int kv_dtype, const void* k_map,
                                        const void* v_map, cudaStream_t stream);
 
+// The same on the 5th-generation tensor cores (tcgen05, accumulators in
+// tensor memory): one CTA per (128 query rows, query head, sequence).
+cudaError_t launch_prefill_tcgen05(const PrefillParams& p, int kv_dtype, const void* k_map,
+                                   const void* v_map, cudaStream_t stream);
+
 // Device status word of the current device (address of a __device__ symbol).
 unsigned int* pkv_status_word_ptr();
 

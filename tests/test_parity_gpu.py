@@ -357,13 +357,22 @@ def test_prefix_cached_sequence_attends_like_a_fresh_one():
 # paged prefill (causal multi-token queries)
 # --------------------------------------------------------------------------
 
-def gpu_prefill(q, kc, vc, bt, cl, qs, scale, B, Hkv, out_dtype=torch.float32):
-    out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=DEV)
-    qn = (qs[1:] - qs[:-1]).tolist()
-    pkv.paged_prefill_attention(out, q.to(DEV), kc, vc, bt.to(DEV), cl.to(DEV), qs.to(DEV),
-                                scale, B, Hkv, max_query_len=max(qn + [0]))
-    torch.cuda.synchronize()
-    return out
+PREFILL_KERNELS = [pytest.param(pkv.PREFILL_TCGEN05, id="tcgen05"),
+                   pytest.param(pkv.PREFILL_WARP_MMA, id="warp_mma")]
+
+
+def gpu_prefill(q, kc, vc, bt, cl, qs, scale, B, Hkv, out_dtype=torch.float32,
+                kernel=pkv.PREFILL_WARP_MMA):
+    pkv.set_prefill_kernel(kernel)
+    try:
+        out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=DEV)
+        qn = (qs[1:] - qs[:-1]).tolist()
+        pkv.paged_prefill_attention(out, q.to(DEV), kc, vc, bt.to(DEV), cl.to(DEV), qs.to(DEV),
+                                    scale, B, Hkv, max_query_len=max(qn + [0]))
+        torch.cuda.synchronize()
+        return out
+    finally:
+        pkv.set_prefill_kernel(pkv.PREFILL_WARP_MMA)
 
 
 PREFILL = [  # dtype, Hq, Hkv, D, B
@@ -372,8 +381,9 @@ PREFILL = [  # dtype, Hq, Hkv, D, B
 ]
 
 
+@pytest.mark.parametrize("kernel", PREFILL_KERNELS)
 @pytest.mark.parametrize("dt,Hq,Hkv,D,B", PREFILL)
-def test_prefill_small(dt, Hq, Hkv, D, B):
+def test_prefill_small(dt, Hq, Hkv, D, B, kernel):
     # whole prompts, chunks of longer contexts, single tokens, an empty query
     # set; lengths off every tile boundary
     lengths = [1, 17, 64, 65, 200, 300, 129, 40]
@@ -384,14 +394,16 @@ def test_prefill_small(dt, Hq, Hkv, D, B):
     g = torch.Generator().manual_seed(5)
     q = torch.randn(int(qs[-1]), Hq, D, generator=g).to(w.torch_dtype)
     kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
-    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, B, Hkv)
+    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, B, Hkv,
+                      kernel=kernel)
     ref = oracle.paged_prefill_attention(q, case.k_cache, case.v_cache, case.block_tables,
                                          case.context_lens, qs, w.scale, B, Hkv)
     assert pkv.device_status() == 0
     assert max_err(out, ref) <= TOL16
 
 
-def test_prefill_long_prompts_and_16bit_out():
+@pytest.mark.parametrize("kernel", PREFILL_KERNELS)
+def test_prefill_long_prompts_and_16bit_out(kernel):
     w = Workload(0, "prefill-long", "bf16", 16, 4, 128, 16, 3, "fixed")
     lengths = [1500, 777, 2048]
     qn = [1500, 300, 1024]
@@ -403,34 +415,66 @@ def test_prefill_long_prompts_and_16bit_out():
     ref = oracle.paged_prefill_attention(q, case.k_cache, case.v_cache, case.block_tables,
                                          case.context_lens, qs, w.scale, 16, 4,
                                          nthreads=oracle.default_threads())
-    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, 16, 4)
+    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, 16, 4,
+                      kernel=kernel)
     assert max_err(out, ref) <= TOL16
     out16 = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, 16, 4,
-                        out_dtype=torch.bfloat16)
+                        out_dtype=torch.bfloat16, kernel=kernel)
     diff = np.abs(out16.cpu().double().numpy() - ref)
     assert (diff <= TOL16 + 2.0 ** -8 * np.abs(ref)).all()
     assert pkv.device_status() == 0
 
 
-def test_prefill_last_row_equals_decode_and_bad_lengths_flag():
+@pytest.mark.parametrize("kernel", PREFILL_KERNELS)
+def test_prefill_last_row_equals_decode_and_bad_lengths_flag(kernel):
     w = Workload(0, "pd", "f16", 8, 2, 128, 16, 2, "fixed")
     case = make_decode_case(w, seed=8, lengths=[333, 90])
     qn = [40, 90]
     qs = torch.tensor([0, 40, 130], dtype=torch.int32)
     q = torch.randn(130, 8, 128, generator=torch.Generator().manual_seed(1)).to(torch.float16)
     kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
-    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, 16, 2)
+    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, 16, 2,
+                      kernel=kernel)
     dec = gpu_decode(torch.stack([q[39], q[129]]), kc, vc, case.block_tables, case.context_lens,
                      w.scale, 16, 2)
     assert float((out[[39, 129]] - dec).abs().max()) <= 2 * TOL16
     bad = torch.tensor([0, 40, 130 + 300], dtype=torch.int32)  # 390 rows for a 90-token context
     q2 = torch.zeros(430, 8, 128, dtype=torch.float16)
     out2 = torch.zeros(430, 8, 128, dtype=torch.float32, device=DEV)
-    pkv.paged_prefill_attention(out2, q2.to(DEV), kc, vc, case.block_tables.to(DEV),
-                                case.context_lens.to(DEV), bad.to(DEV), w.scale, 16, 2,
-                                max_query_len=390)
+    pkv.set_prefill_kernel(kernel)
+    try:
+        pkv.paged_prefill_attention(out2, q2.to(DEV), kc, vc, case.block_tables.to(DEV),
+                                    case.context_lens.to(DEV), bad.to(DEV), w.scale, 16, 2,
+                                    max_query_len=390)
+    finally:
+        pkv.set_prefill_kernel(pkv.PREFILL_WARP_MMA)
     assert pkv.device_status() & 2
     assert not out2[40:].any()
+
+
+@pytest.mark.parametrize("kernel", PREFILL_KERNELS)
+def test_prefill_nan_poison_and_bad_block(kernel):
+    # Unused cache slots hold NaN: outputs stay finite and match the oracle.
+    # A table entry out of range is skipped (its keys masked) and flagged.
+    w = Workload(0, "pp", "bf16", 8, 2, 128, 16, 2, "fixed")
+    case = make_decode_case(w, seed=31, lengths=[70, 200])
+    poison_unused(case.k_cache, case.v_cache, case.block_tables, case.context_lens)
+    qs = torch.tensor([0, 70, 70 + 150], dtype=torch.int32)
+    q = torch.randn(220, 8, 128, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, 16, 2,
+                      kernel=kernel)
+    ref = oracle.paged_prefill_attention(q, case.k_cache, case.v_cache, case.block_tables,
+                                         case.context_lens, qs, w.scale, 16, 2)
+    assert torch.isfinite(out).all()
+    assert max_err(out, ref) <= TOL16
+    assert pkv.device_status() == 0
+    bt = case.block_tables.clone()
+    bt[1, 2] = case.num_blocks + 5  # tokens 32..47 of sequence 1
+    out_bad = gpu_prefill(q, kc, vc, bt, case.context_lens, qs, w.scale, 16, 2, kernel=kernel)
+    assert pkv.device_status() & 1
+    assert torch.isfinite(out_bad).all()
+    assert max_err(out_bad[:70], ref[:70]) <= TOL16  # the healthy sequence is unaffected
 
 
 def test_nan_poison_and_physical_permutation():
