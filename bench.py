@@ -507,7 +507,7 @@ def run_prefill(args):
                                        "peak_source": src},
                           "kv_bytes": int(case.context_lens.sum()) * 2 * Hkv * D * 2}),
               flush=True)
-    pkv.set_prefill_kernel(pkv.PREFILL_WARP_MMA)
+    pkv.set_prefill_kernel(pkv.PREFILL_TCGEN05)
 
 
 def run_swap(args):

@@ -265,11 +265,11 @@ int pkv_set_decode_kernel(int which);
 
 /*
  * Kernel selection for pkv_paged_prefill_attention (process-wide):
- * PKV_PREFILL_WARP_MMA (default) runs the warp-level mma.sync kernel (64
- * query rows per CTA); PKV_PREFILL_TCGEN05 runs the 5th-generation
- * tensor-core kernel (tcgen05 MMAs, accumulators in tensor memory, 128 rows
- * per CTA).  Both compute the same result up to fp32 accumulation order.
- * Returns PKV_ERR_SHAPE for an unknown value.
+ * PKV_PREFILL_TCGEN05 (default) runs the 5th-generation tensor-core kernel
+ * (tcgen05 MMAs with S, P and O in tensor memory, 256 query rows per CTA,
+ * warp-specialised); PKV_PREFILL_WARP_MMA runs the warp-level mma.sync
+ * kernel (64 rows per CTA).  Both compute the same result up to fp32
+ * accumulation order.  Returns PKV_ERR_SHAPE for an unknown value.
  */
 #define PKV_PREFILL_TCGEN05 0
 #define PKV_PREFILL_WARP_MMA 1

@@ -20,7 +20,7 @@
 namespace {
 thread_local char g_err[512] = "";
 int g_decode_kernel = PKV_KERNEL_AUTO;
-int g_prefill_kernel = PKV_PREFILL_WARP_MMA;
+int g_prefill_kernel = PKV_PREFILL_TCGEN05;
 }  // namespace
 
 int pkv_fail(int code, const char* fmt, ...)

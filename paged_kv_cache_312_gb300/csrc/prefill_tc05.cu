@@ -7,26 +7,31 @@
 // (cayang0802 walkthrough, recomputation; aiplusplus PagedAttention page,
 // "key techniques" 1 for the block-table walk).
 //
-// How (GB300 design):
-//  * One CTA of 4 warps per (128 query rows, query head, sequence), latest
-//    (heaviest) query tiles first.  Thread r owns query row r: it reads that
-//    row of S from tensor memory, so the row max and row sum need no shuffles.
-//  * Key/value tiles of 64 tokens arrive by TMA (16-row boxes of the paged
-//    cache, 128-byte swizzle, laid out [column half][key][128 B]) through a
-//    3-stage mbarrier ring.
-//  * S_j = Q K_j^T is one chain of tcgen05.mma (M=128, N=64, K=head_dim, both
-//    operands K-major in shared memory) into one of two S buffers in tensor
-//    memory, so S_{j+1} runs on the tensor cores while the threads do the
-//    softmax of tile j.
-//  * O += P_j V_j accumulates in tensor memory (M=128, N=head_dim, K=64; V is
-//    the MN-major operand).  P goes to shared memory as a 16-bit high part and
-//    remainder and both are multiplied, keeping ~16 bits of P.  A row whose
-//    running max grew has its O row rescaled in place (tcgen05.ld / st).
-//  * Thread 0 issues every TMA copy and MMA; tcgen05.commit arrives on the
-//    mbarriers the threads wait on.  Every wait is bounded; a wait that gives
-//    up sets the TIMEOUT status bit (which ends the waits of every other CTA
-//    too), and the CTA drains its own copies and MMAs before it frees its
-//    tensor memory.
+// How (GB300 design): one CTA of 10 warps per (256 query rows, query head,
+// sequence), latest (heaviest) rows first; the rows form two 128-row tiles
+// A and B whose softmax work alternates with each other's tensor-core work.
+//  * warp 9 (loads): K and V tiles of 64 tokens by TMA (16-row boxes of the
+//    paged cache, 128-byte swizzle, [column half][key][128 B]) into an
+//    8-slot ring, K(0) V(0) K(1) V(1) ...; its lanes read the tile's block
+//    table entries in parallel and record bad entries for the softmax.
+//  * warp 8 (MMA issue, one lane): S_X(j) = Q_X K(j)^T into tensor memory
+//    (M=128, N=64, K=head_dim; Q and K K-major in shared memory), then
+//    O_X += P_X(j) V(j) with P read from tensor memory (M=128, N=head_dim,
+//    K=64; V the MN-major operand).  S_X(j+1) is issued as soon as the
+//    softmax of X has posted P_X(j).
+//  * warps 0-3 (tile A) and 4-7 (tile B): thread r owns row r of its tile:
+//    it reads the row of S from tensor memory, masks (diagonal, tail and bad
+//    blocks only), keeps a running max and sum in base 2, and writes P back
+//    to tensor memory as a 16-bit high part and remainder (both are
+//    multiplied, keeping ~16 bits of P).  The running max used for P moves
+//    only when the row max exceeds it by more than 8 (a factor 2^8), and only
+//    then is the O row rescaled; O and the sum always share the same max, so
+//    the result is unchanged.
+//  * Tensor memory (512 columns): tile A S [0,64) P [64,128) O [128,256),
+//    tile B the same at +256.
+// Every wait is bounded; a wait that gives up sets the TIMEOUT status bit
+// (which ends the waits of every other CTA too), and before the CTA frees
+// its tensor memory it waits (bounded) for its own copies and MMAs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,30 +46,36 @@ namespace {
 
 using namespace pkv_tc;
 
-constexpr int kRows = 128;   // query rows per CTA (MMA M)
-constexpr int kKeys = 64;    // keys per tile (N of S, K of P V)
-constexpr int kStages = 3;
-constexpr int kThreads = 128;
-constexpr uint32_t kTmemCols = 256;  // S0 [0,64), S1 [64,128), O [128, 128 + D)
-constexpr int kBars = kStages + 4;   // kv_full[kStages], s_done[2], o_done, drain
+constexpr int kTileRows = 128;  // query rows per tile (MMA M)
+constexpr int kQTiles = 2;      // query tiles per CTA
+constexpr int kKeys = 64;       // keys per K/V tile
+constexpr int kSlots = 8;       // K/V ring slots (one K or one V tile each)
+constexpr int kRing = 16;       // bad-block masks kept per tile index
+constexpr int kMmaWarp = 8, kLoadWarp = 9;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTileCols = 256;  // tensor-memory columns per query tile
+constexpr uint32_t kColP = 64, kColO = 128;
+// barriers: full[kSlots], empty[kSlots], s_full[2], p_full[2], o_full[2], drain
+constexpr int kBars = 2 * kSlots + 7;
 
 template <int D, int B>
 struct G5 {
     static constexpr int NH = D / 64;
     static constexpr int ROWS = B < 16 ? B : 16;  // rows per TMA box
-    static constexpr int IDS = 16 / ROWS;         // blocks per 16-token group
-    static constexpr int HALF_Q = kRows * 128;    // one 64-column half of Q
-    static constexpr int HALF_KV = kKeys * 128;   // one 64-column half of a K or V tile
-    static constexpr int Q_OFF = 0;
-    static constexpr int STAGE_OFF = Q_OFF + NH * HALF_Q;
-    static constexpr int STAGE_BYTES = 2 * NH * HALF_KV;  // K halves, then V halves
-    static constexpr int P_OFF = STAGE_OFF + kStages * STAGE_BYTES;
-    static constexpr int P_BYTES = kRows * 128;           // 64 keys x 2 bytes per row
-    static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;   // P high part, remainder
+    static constexpr int IDS = 16 / ROWS;         // boxes per 16-token group
+    static constexpr int SUBS = 4 * IDS;          // boxes per 64-token tile and half
+    static constexpr int HALF_Q = kTileRows * 128;
+    static constexpr int HALF_KV = kKeys * 128;
+    static constexpr int Q_BYTES = NH * HALF_Q;
+    static constexpr int SLOT_BYTES = NH * HALF_KV;
+    static constexpr int SLOT_OFF = kQTiles * Q_BYTES;
+    static constexpr int BAR_OFF = SLOT_OFF + kSlots * SLOT_BYTES;
     static constexpr int TSLOT_OFF = BAR_OFF + kBars * 8;
-    static constexpr int KID_OFF = TSLOT_OFF + 16;        // [stage][4 groups][2] ids
-    static constexpr int SMEM_BYTES = 1024 + KID_OFF + kStages * 8 * 4;
+    static constexpr int KBAD_OFF = TSLOT_OFF + 16;
+    static constexpr int SMEM_BYTES = 1024 + KBAD_OFF + kRing * 4;
     static_assert(HALF_KV % 1024 == 0 && HALF_Q % 1024 == 0, "swizzle atoms");
+    static_assert(SUBS <= 32, "one lane per box");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -166,6 +177,63 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
         if (clock64() - t0 > (1ll << 31)) return;
 }
 
+// tcgen05.mma with the A operand in tensor memory (K-major, two 16-bit
+// elements per 32-bit column, the lower key in the low half).
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                        uint32_t idesc, int accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive output values of one row: 16-byte stores when `vec`.
+__device__ __forceinline__ void store_row32(void* out, size_t at, const float (&v)[32],
+                                            int out_dtype, bool vec)
+{
+    if (!vec) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) store_out(out, at + i, v[i], out_dtype);
+        return;
+    }
+    if (out_dtype == PKV_F32) {
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + at);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else if (out_dtype == PKV_F16) {
+        uint4* o = reinterpret_cast<uint4*>(static_cast<__half*>(out) + at);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __half2 x = __floats2half2_rn(v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
+                w[e] = *reinterpret_cast<uint32_t*>(&x);
+            }
+            o[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + at);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 x = __floats2bfloat162_rn(v[8 * i + 2 * e], v[8 * i + 2 * e + 1]);
+                w[e] = *reinterpret_cast<uint32_t*>(&x);
+            }
+            o[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
 template <typename T, int D, int B>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
@@ -173,37 +241,47 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
 {
     using Gm = G5<D, B>;
     constexpr int IDS = Gm::IDS;
-    const int qtile = gridDim.x - 1 - blockIdx.x;  // latest (heaviest) tiles first
+    const int ctile = gridDim.x - 1 - blockIdx.x;  // latest (heaviest) rows first
     const int h = blockIdx.y, s = blockIdx.z;
     const int r0 = p.query_start[s];
     const int qn = p.query_start[s + 1] - r0;
     const int L = p.context_lens[s];
     if (L < 0 || (int64_t)L > (int64_t)p.max_blocks * B || qn < 0 || qn > L ||
         qn > p.max_query_len) {
-        if (qtile == 0 && h == 0 && threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
+        if (ctile == 0 && h == 0 && threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
         return;
     }
-    const int q0 = qtile * kRows;
+    const int q0 = ctile * kQTiles * kTileRows;
     if (q0 >= qn) return;
     const int g = h / (p.num_heads / p.num_kv_heads);
     const int base_pos = L - qn;
-    const int last_pos = base_pos + min(qn, q0 + kRows) - 1;
-    const int nkt = last_pos / kKeys + 1;
+    // key tiles each query tile needs (0 for a tile past the last row)
+    auto tiles_for = [&](int x) {
+        const int rows = min(qn - (q0 + x * kTileRows), kTileRows);
+        return rows > 0 ? (base_pos + q0 + x * kTileRows + rows - 1) / kKeys + 1 : 0;
+    };
+    const int nkt_a = tiles_for(0), nkt_b = tiles_for(1);
+    auto nkt_of = [&](int x) { return x ? nkt_b : nkt_a; };
+    const int nkt = max(nkt_a, nkt_b);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + Gm::BAR_OFF);
-    uint64_t* s_done = kv_full + kStages;  // [2]
-    uint64_t* o_done = s_done + 2;
-    uint64_t* drain = o_done + 1;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::BAR_OFF);
+    uint64_t* empty = full + kSlots;
+    uint64_t* s_full = empty + kSlots;  // [2]
+    uint64_t* p_full = s_full + 2;      // [2], one arrival per softmax warp
+    uint64_t* o_full = p_full + 2;      // [2]
+    uint64_t* drain = o_full + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Gm::TSLOT_OFF);
-    int* kid = reinterpret_cast<int*>(smem + Gm::KID_OFF);
-    const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    uint32_t* kbad = reinterpret_cast<uint32_t*>(smem + Gm::KBAD_OFF);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int i = 0; i < kBars; ++i) mbar_init(smem_u32(&kv_full[i]), 1);
+        for (int i = 0; i < kBars; ++i) {
+            uint64_t* b = &full[i];
+            mbar_init(smem_u32(b), (b == &p_full[0] || b == &p_full[1]) ? 4 : 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -213,17 +291,16 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // ---- this thread's query row into shared memory (zero past qn)
-    {
-        const bool live = q0 + tid < qn;
-        const T* src =
-            static_cast<const T*>(p.q) + ((size_t)(r0 + q0 + tid) * p.num_heads + h) * D;
+    if (warp < 8) {  // this thread's query row into shared memory (zero past qn)
+        const int x = warp >> 2, r = tid & (kTileRows - 1);
+        const int row = q0 + x * kTileRows + r;
+        const T* src = static_cast<const T*>(p.q) + ((size_t)(r0 + row) * p.num_heads + h) * D;
+        uint8_t* qx = smem + x * Gm::Q_BYTES;
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (live) v = *reinterpret_cast<const uint4*>(src + c * 8);
-            *reinterpret_cast<uint4*>(smem + Gm::Q_OFF + (c >> 3) * Gm::HALF_Q + swz(tid, c & 7)) =
-                v;
+            if (row < qn) v = *reinterpret_cast<const uint4*>(src + c * 8);
+            *reinterpret_cast<uint4*>(qx + (c >> 3) * Gm::HALF_Q + swz(r, c & 7)) = v;
         }
     }
     fence_proxy_async();
@@ -242,219 +319,260 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             atomicOr(p.status, PKV_STATUS_TIMEOUT);
         }
     };
+    // ring position of K(j) (t = 2j) and V(j) (t = 2j + 1)
+    auto slot_of = [](int t) { return t % kSlots; };
+    auto phase_of = [](int t) { return (t / kSlots) & 1; };
 
-    // thread 0: TMA loads of key tile kt into stage kt % kStages
-    int issued = 0, landed = 0;
-    auto issue_tile = [&](int kt) {
-        const int st = kt % kStages;
-        const uint32_t bar = smem_u32(&kv_full[st]);
-        const uint32_t kdst = smem_u32(smem + Gm::STAGE_OFF + st * Gm::STAGE_BYTES);
-        const uint32_t vdst = kdst + Gm::NH * Gm::HALF_KV;
-        int ids[4][IDS];
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int grp = 0; grp < 4; ++grp)
-#pragma unroll
-            for (int u = 0; u < IDS; ++u) {
-                const int tok = kt * kKeys + grp * 16 + u * Gm::ROWS;
-                int id = -1;
-                if (tok < L) {
-                    id = table[tok / B];
-                    if (id < 0 || id >= p.num_blocks) {
-                        atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
-                        id = -1;
-                    }
-                }
-                ids[grp][u] = id;
-                kid[(st * 4 + grp) * 2 + u] = id;
-                if (IDS == 1) kid[(st * 4 + grp) * 2 + 1] = id;
-                if (id >= 0) bytes += 2 * Gm::NH * Gm::ROWS * 128;
-            }
-        mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-        for (int grp = 0; grp < 4; ++grp)
-#pragma unroll
-            for (int u = 0; u < IDS; ++u) {
-                if (ids[grp][u] < 0) continue;
-                const int tok = kt * kKeys + grp * 16 + u * Gm::ROWS;
-                const int row = (ids[grp][u] * p.num_kv_heads + g) * B + (IDS > 1 ? 0 : tok % B);
-                const uint32_t off = (grp * 16 + u * Gm::ROWS) * 128;
-#pragma unroll
-                for (int hf = 0; hf < Gm::NH; ++hf) {
-                    tma_load_2d(kdst + hf * Gm::HALF_KV + off, &kmap, hf * 64, row, bar);
-                    tma_load_2d(vdst + hf * Gm::HALF_KV + off, &vmap, hf * 64, row, bar);
+    if (warp == kLoadWarp) {
+        // ------------------------------------------------------------ loads
+        int issued = 0;
+        for (int t = 0; t < 2 * nkt; ++t) {
+            const int j = t >> 1, sl = slot_of(t);
+            const bool is_v = t & 1;
+            if (t >= kSlots && lane == 0) wait(&empty[sl], ((t / kSlots) - 1) & 1);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const int grp = lane / IDS, u = lane % IDS;
+            const int tok = j * kKeys + grp * 16 + u * Gm::ROWS;
+            int id = -1;
+            bool bad = false;
+            if (lane < Gm::SUBS && tok < L) {
+                id = p.block_tables[(size_t)s * p.max_blocks + tok / B];
+                if (id < 0 || id >= p.num_blocks) {
+                    bad = true;
+                    id = -1;
                 }
             }
-        issued = kt + 1;
-    };
-    const uint32_t id_s = instr_desc<T>(kRows, kKeys, 0);
-    const uint32_t id_o = instr_desc<T>(kRows, D, 1);
-    // thread 0: S_kt = Q K_kt^T into S buffer kt % 2
-    auto issue_s = [&](int kt) {
-        const uint32_t q = smem_u32(smem + Gm::Q_OFF);
-        const uint32_t kb = smem_u32(smem + Gm::STAGE_OFF + (kt % kStages) * Gm::STAGE_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk & 3) * 32;
-            umma(tbase + (kt & 1) * kKeys, smem_desc(q + (kk >> 2) * Gm::HALF_Q + off, 16, 1024),
-                 smem_desc(kb + (kk >> 2) * Gm::HALF_KV + off, 16, 1024), id_s, kk > 0);
-        }
-        umma_commit(smem_u32(&s_done[kt & 1]));
-    };
-
-    if (tid == 0) {
-        for (int kt = 0; kt < kStages && kt < nkt; ++kt) issue_tile(kt);
-        wait(&kv_full[0], 0);
-        if (ok) {
-            landed = 1;
-            issue_s(0);
-        }
-    }
-    __syncwarp();
-
-    const int row_t = q0 + tid;                          // query row within the sequence
-    const int pos = row_t < qn ? base_pos + row_t : -1;  // its position (-1: padding row)
-    const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
-    const uint32_t o_tmem = tbase + 2 * kKeys;           // O columns (lane 0)
-    const float sl = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
-    uint8_t* phi = smem + Gm::P_OFF;
-    uint8_t* plo = phi + Gm::P_BYTES;
-
-    for (int j = 0; j < nkt; ++j) {
-        const int st = j % kStages;
-        // thread 0: S_{j+1} as soon as its K tile has landed, so the tensor
-        // cores work while the threads run this tile's softmax
-        if (tid == 0 && j + 1 < nkt) {
-            wait(&kv_full[(j + 1) % kStages], ((j + 1) / kStages) & 1);
-            if (ok) {
-                landed = j + 2;
-                issue_s(j + 1);
+            const unsigned have = __ballot_sync(0xffffffffu, id >= 0);
+            const unsigned bads = __ballot_sync(0xffffffffu, bad);
+            const uint32_t bar = smem_u32(&full[sl]);
+            if (lane == 0) {
+                if (!is_v) {
+                    kbad[j % kRing] = bads;
+                    if (bads) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
+                }
+                mbar_arrive_expect_tx(bar, __popc(have) * Gm::NH * Gm::ROWS * 128);
             }
+            __syncwarp();
+            if (id >= 0) {
+                const int row = (id * p.num_kv_heads + g) * B + (IDS > 1 ? 0 : tok % B);
+                const uint32_t dst = smem_u32(smem + Gm::SLOT_OFF + sl * Gm::SLOT_BYTES) +
+                                     (grp * 16 + u * Gm::ROWS) * 128;
+#pragma unroll
+                for (int hf = 0; hf < Gm::NH; ++hf)
+                    tma_load_2d(dst + hf * Gm::HALF_KV, is_v ? &vmap : &kmap, hf * 64, row, bar);
+            }
+            issued = t + 1;
         }
+        // the ring's last fills must have landed before the CTA exits
+        if (lane == 0)
+            for (int t = max(0, issued - kSlots); t < issued; ++t)
+                drain_wait(smem_u32(&full[slot_of(t)]), phase_of(t));
         __syncwarp();
-        wait(&s_done[j & 1], (j >> 1) & 1);
-        wait(&kv_full[st], (j / kStages) & 1);
-        tmem_fence_after();
-        const int key0 = j * kKeys;
-        const int* kid_t = kid + st * 8;
-        // ---- this row of S_j: scale, causal and validity mask, max
-        float sv[kKeys];
-        {
-            float a[32];
-            tmem_ld32(lane_base + (j & 1) * kKeys, a);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------- MMA issue
+        const uint32_t id_s = instr_desc<T>(kTileRows, kKeys, 0);
+        const uint32_t id_o = instr_desc<T>(kTileRows, D, 1);
+        const uint32_t q_base = smem_u32(smem);
+        const uint32_t slot_base = smem_u32(smem + Gm::SLOT_OFF);
+        auto issue_s = [&](int x, int j) {
+            const uint32_t kb = slot_base + slot_of(2 * j) * Gm::SLOT_BYTES;
+            const uint32_t qb = q_base + x * Gm::Q_BYTES;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sv[i] = a[i];
-            tmem_ld32(lane_base + (j & 1) * kKeys + 32, a);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sv[32 + i] = a[i];
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < kKeys; ++k) {
-            const bool valid = key0 + k <= pos && kid_t[(k >> 4) * 2 + (k & 15) / Gm::ROWS] >= 0;
-            sv[k] = valid ? sv[k] * sl : -INFINITY;
-            mx = fmaxf(mx, sv[k]);
-        }
-        const float mn = fmaxf(m, mx);
-        const float ms = mn == -INFINITY ? 0.f : mn;
-        const float alpha = ex2(m - ms);  // 0 while m is -inf
-        // O holds something to rescale only once m is finite
-        const bool grew = m != -INFINITY && alpha != 1.f;
-        m = mn;
-        float rs = 0.f;
-#pragma unroll
-        for (int k = 0; k < kKeys; ++k) {
-            sv[k] = ex2(sv[k] - ms);
-            rs += sv[k];
-        }
-        l = l * alpha + rs;
-        // ---- V rows of keys that were not loaded (past the context, bad
-        // block) are zeroed: their P is 0, and 0 * NaN must not reach O
-        {
-            bool all_loaded = key0 + kKeys <= L;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) all_loaded = all_loaded && kid_t[i] >= 0;
-            if (!all_loaded) {
-                uint8_t* vt = smem + Gm::STAGE_OFF + st * Gm::STAGE_BYTES + Gm::NH * Gm::HALF_KV;
-                for (int i = tid; i < Gm::NH * kKeys * 8; i += kThreads) {
-                    const int hf = i / (kKeys * 8), k = (i >> 3) % kKeys, c = i & 7;
-                    if (key0 + k >= L || kid_t[(k >> 4) * 2 + (k & 15) / Gm::ROWS] < 0)
-                        *reinterpret_cast<uint4*>(vt + hf * Gm::HALF_KV + k * 128 + c * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                }
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * Gm::HALF_Q + (kk & 3) * 32;
+                const uint32_t koff = (kk >> 2) * Gm::HALF_KV + (kk & 3) * 32;
+                umma(tbase + x * kTileCols, smem_desc(qb + off, 16, 1024),
+                     smem_desc(kb + koff, 16, 1024), id_s, kk > 0);
             }
-        }
-        // ---- P V_{j-1} must be done before O is rescaled and P rewritten
-        if (j > 0) {
-            wait(o_done, (j - 1) & 1);
-            tmem_fence_after();
-            if (__any_sync(0xffffffffu, grew)) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(lane_base + 2 * kKeys + c * 32, o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tmem_st32(lane_base + 2 * kKeys + c * 32, o);
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            }
-        }
-        // ---- P (high part and remainder), row-major by key, swizzled
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                Mma<T>::split(sv[c * 8 + 2 * e], sv[c * 8 + 2 * e + 1], hw[e], lw[e]);
-            *reinterpret_cast<uint4*>(phi + swz(tid, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(plo + swz(tid, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-        fence_proxy_async();
-        tmem_fence_before();
-        __syncthreads();
-        tmem_fence_after();
-        if (tid == 0 && ok) {
-            // stage (j-1) % kStages is free (S_{j-1} and P V_{j-1} are done):
-            // refill it with tile j + 2
-            if (j > 0 && j + 2 < nkt) issue_tile(j + 2);
-            const uint32_t vb =
-                smem_u32(smem + Gm::STAGE_OFF + st * Gm::STAGE_BYTES + Gm::NH * Gm::HALF_KV);
-            const uint32_t ph = smem_u32(phi), pl = smem_u32(plo);
+            umma_commit(smem_u32(&s_full[x]));
+        };
+        auto issue_pv = [&](int x, int j) {
+            const uint32_t vb = slot_base + slot_of(2 * j + 1) * Gm::SLOT_BYTES;
+            const uint32_t pc = tbase + x * kTileCols + kColP;
 #pragma unroll
             for (int kk = 0; kk < kKeys / 16; ++kk) {
                 const uint64_t vd = smem_desc(vb + kk * 2048, Gm::HALF_KV, 1024);
-                umma(o_tmem, smem_desc(ph + kk * 32, 16, 1024), vd, id_o, j > 0 || kk > 0);
-                umma(o_tmem, smem_desc(pl + kk * 32, 16, 1024), vd, id_o, 1);
+                umma_ts(tbase + x * kTileCols + kColO, pc + kk * 8, vd, id_o, j > 0 || kk > 0);
+                umma_ts(tbase + x * kTileCols + kColO, pc + 32 + kk * 8, vd, id_o, 1);
             }
-            umma_commit(smem_u32(o_done));
+            umma_commit(smem_u32(&o_full[x]));
+        };
+        // V(j) landed; rows of keys past the context or in a bad block are
+        // zeroed (their P is 0, and 0 * NaN must not reach O)
+        auto v_ready = [&](int j) {
+            const int t = 2 * j + 1;
+            if (lane == 0) wait(&full[slot_of(t)], phase_of(t));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();  // the other lanes read kbad after lane 0's acquire
+            const int key0 = j * kKeys;
+            const uint32_t bm = kbad[j % kRing];
+            if (ok && (key0 + kKeys > L || bm)) {
+                uint8_t* vt = smem + Gm::SLOT_OFF + slot_of(t) * Gm::SLOT_BYTES;
+                for (int i = lane; i < Gm::NH * kKeys * 8; i += 32) {
+                    const int hf = i / (kKeys * 8), k = (i >> 3) % kKeys, c = i & 7;
+                    const int box = (k >> 4) * IDS + (k & 15) / Gm::ROWS;
+                    if (key0 + k >= L || ((bm >> box) & 1u))
+                        *reinterpret_cast<uint4*>(vt + hf * Gm::HALF_KV + k * 128 + c * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async();
+            }
+            __syncwarp();
+        };
+        auto k_ready = [&](int j) {
+            if (lane == 0) wait(&full[slot_of(2 * j)], phase_of(2 * j));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+        };
+
+        k_ready(0);
+        if (lane == 0 && ok) {
+            tmem_fence_after();
+            for (int x = 0; x < kQTiles; ++x)
+                if (nkt_of(x) > 0) issue_s(x, 0);
+            umma_commit(smem_u32(&empty[slot_of(0)]));
         }
         __syncwarp();
-    }
-    // ---- epilogue: O / l for this thread's row
-    wait(o_done, (nkt - 1) & 1);
-    tmem_fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+        for (int j = 0; j < nkt && ok; ++j) {
+            bool v_in = false;
+            for (int x = 0; x < kQTiles && ok; ++x) {
+                if (j >= nkt_of(x)) continue;
+                if (lane == 0) wait(&p_full[x], j & 1);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (j + 1 < nkt_of(x)) {
+                    k_ready(j + 1);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        tmem_fence_after();
+                        issue_s(x, j + 1);
+                    }
+                    __syncwarp();
+                }
+                if (!v_in) {
+                    v_ready(j);
+                    v_in = true;
+                    if (!ok) break;
+                }
+                if (lane == 0) {
+                    tmem_fence_after();
+                    issue_pv(x, j);
+                }
+                __syncwarp();
+            }
+            if (lane == 0 && ok) {
+                if (j + 1 < nkt) umma_commit(smem_u32(&empty[slot_of(2 * j + 2)]));
+                umma_commit(smem_u32(&empty[slot_of(2 * j + 1)]));
+            }
+            __syncwarp();
+        }
+        // every MMA this thread issued has finished before the CTA exits
+        if (lane == 0) {
+            umma_commit(smem_u32(drain));
+            drain_wait(smem_u32(drain), 0);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------------- softmax
+        const int x = warp >> 2;
+        const int row = q0 + x * kTileRows + (tid & (kTileRows - 1));
+        const int pos = row < qn ? base_pos + row : -1;  // -1: padding row
+        const int my_nkt = nkt_of(x);
+        const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16) + x * kTileCols;
+        const float sl = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < my_nkt; ++j) {
+            wait(&s_full[x], j & 1);
+            wait(&full[slot_of(2 * j)], phase_of(2 * j));  // orders the read of kbad
+            tmem_fence_after();
+            float sv[kKeys];
+            {
+                float a[32];
+                tmem_ld32(tl, a);
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32(lane_base + 2 * kKeys + c * 32, o);
-        if (pos >= 0 && ok) {
-            const size_t at = ((size_t)(r0 + row_t) * p.num_heads + h) * D + c * 32;
+                for (int i = 0; i < 32; ++i) sv[i] = a[i];
+                tmem_ld32(tl + 32, a);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) store_out(p.out, at + i, o[i] * inv, p.out_dtype);
+                for (int i = 0; i < 32; ++i) sv[32 + i] = a[i];
+            }
+            const int key0 = j * kKeys;
+            const uint32_t bm = kbad[j % kRing];
+            if (key0 + kKeys - 1 <= pos && bm == 0) {
+#pragma unroll
+                for (int k = 0; k < kKeys; ++k) sv[k] *= sl;
+            } else {
+#pragma unroll
+                for (int k = 0; k < kKeys; ++k) {
+                    const int box = (k >> 4) * IDS + (k & 15) / Gm::ROWS;
+                    const bool valid = key0 + k <= pos && !((bm >> box) & 1u);
+                    sv[k] = valid ? sv[k] * sl : -INFINITY;
+                }
+            }
+            float mx = sv[0];
+#pragma unroll
+            for (int k = 1; k < kKeys; ++k) mx = fmaxf(mx, sv[k]);
+            float alpha = 1.f;
+            bool rescale = false;
+            if (mx > m + 8.f) {  // also the first finite max (m = -inf)
+                rescale = m != -INFINITY;
+                alpha = ex2(m - mx);
+                m = mx;
+            }
+            const float ms = m == -INFINITY ? 0.f : m;
+            float rs = 0.f;
+#pragma unroll
+            for (int k = 0; k < kKeys; ++k) {
+                sv[k] = ex2(sv[k] - ms);
+                rs += sv[k];
+            }
+            l = l * alpha + rs;
+            uint32_t hw[32], lw[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) Mma<T>::split(sv[2 * i], sv[2 * i + 1], hw[i], lw[i]);
+            // P V_{j-1} has read P and written O before either is touched
+            if (j > 0) wait(&o_full[x], (j - 1) & 1);
+            tmem_fence_after();
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tl + kColO + c * 32, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    tmem_st32(tl + kColO + c * 32, o);
+                }
+            }
+            float hf[32], lf[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                hf[i] = __uint_as_float(hw[i]);
+                lf[i] = __uint_as_float(lw[i]);
+            }
+            tmem_st32(tl + kColP, hf);
+            tmem_st32(tl + kColP + 32, lf);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tmem_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&p_full[x]));
+        }
+        // ---- epilogue: O / l for this thread's row
+        if (my_nkt > 0) {
+            wait(&o_full[x], (my_nkt - 1) & 1);
+            tmem_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const bool vec = (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                tmem_ld32(tl + kColO + c * 32, o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] *= inv;
+                if (pos >= 0 && ok)
+                    store_row32(p.out, ((size_t)(r0 + row) * p.num_heads + h) * D + c * 32, o,
+                                p.out_dtype, vec);
+            }
         }
     }
-    if (tid == 0 && !ok) {
-        // a wait gave up: let this CTA's copies and MMAs finish before its
-        // shared and tensor memory go away
-        for (int t = landed; t < issued; ++t)
-            drain_wait(smem_u32(&kv_full[t % kStages]), (t / kStages) & 1);
-        umma_commit(smem_u32(drain));
-        drain_wait(smem_u32(drain), 0);
-    }
-    __syncwarp();
     tmem_fence_before();
     __syncthreads();
     tmem_fence_after();
@@ -473,7 +591,8 @@ cudaError_t launch5(const PrefillParams& p, const void* kmap, const void* vmap,
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.max_query_len + kRows - 1) / kRows, p.num_heads, p.num_seqs);
+    const int rows = kQTiles * kTileRows;
+    dim3 grid((p.max_query_len + rows - 1) / rows, p.num_heads, p.num_seqs);
     kern<<<grid, kThreads, Gm::SMEM_BYTES, stream>>>(p, *static_cast<const CUtensorMap*>(kmap),
                                                      *static_cast<const CUtensorMap*>(vmap));
     return cudaGetLastError();

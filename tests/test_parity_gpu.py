@@ -362,7 +362,7 @@ PREFILL_KERNELS = [pytest.param(pkv.PREFILL_TCGEN05, id="tcgen05"),
 
 
 def gpu_prefill(q, kc, vc, bt, cl, qs, scale, B, Hkv, out_dtype=torch.float32,
-                kernel=pkv.PREFILL_WARP_MMA):
+                kernel=pkv.PREFILL_TCGEN05):
     pkv.set_prefill_kernel(kernel)
     try:
         out = torch.full(q.shape, float("nan"), dtype=out_dtype, device=DEV)
@@ -372,7 +372,7 @@ def gpu_prefill(q, kc, vc, bt, cl, qs, scale, B, Hkv, out_dtype=torch.float32,
         torch.cuda.synchronize()
         return out
     finally:
-        pkv.set_prefill_kernel(pkv.PREFILL_WARP_MMA)
+        pkv.set_prefill_kernel(pkv.PREFILL_TCGEN05)
 
 
 PREFILL = [  # dtype, Hq, Hkv, D, B
@@ -447,7 +447,7 @@ def test_prefill_last_row_equals_decode_and_bad_lengths_flag(kernel):
                                     case.context_lens.to(DEV), bad.to(DEV), w.scale, 16, 2,
                                     max_query_len=390)
     finally:
-        pkv.set_prefill_kernel(pkv.PREFILL_WARP_MMA)
+        pkv.set_prefill_kernel(pkv.PREFILL_TCGEN05)
     assert pkv.device_status() & 2
     assert not out2[40:].any()
 
