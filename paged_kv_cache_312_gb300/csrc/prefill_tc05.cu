@@ -55,9 +55,10 @@ constexpr int kMmaWarp = 8, kLoadWarp = 9;
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTileCols = 256;  // tensor-memory columns per query tile
-constexpr uint32_t kColP = 64, kColO = 128;
-// barriers: full[kSlots], empty[kSlots], s_full[2], p_full[2], o_full[2], drain
-constexpr int kBars = 2 * kSlots + 7;
+constexpr uint32_t kColO = 128;     // S buffers at columns 0 and 64, O at 128
+// barriers: full[kSlots], empty[kSlots], s_full[tile][buffer],
+// p_full[tile][buffer], o_full[tile], drain
+constexpr int kBars = 2 * kSlots + 11;
 
 template <int D, int B>
 struct G5 {
@@ -97,6 +98,17 @@ __device__ __forceinline__ uint32_t instr_desc(int M, int N, int b_mn_major)
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// MMAs are issued by one lane that elect.sync picks from a converged warp
+// (always the same lane, so its commits track all of them); the operands
+// are computed by the whole warp, so they are warp-uniform.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(e));
+    return e != 0;
+}
+
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                      int accumulate)
 {
@@ -112,6 +124,15 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
         : "memory");
+}
+
+// A shared-memory descriptor moved by `bytes` (the start-address field is
+// the low 14 bits of the low word; addresses stay below 256 KB, so the add
+// never carries out of it).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes)
+{
+    const uint32_t lo = (uint32_t)d + (bytes >> 4);
+    return ((d >> 32) << 32) | lo;
 }
 
 __device__ __forceinline__ void tmem_fence_before()
@@ -269,9 +290,9 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::BAR_OFF);
     uint64_t* empty = full + kSlots;
-    uint64_t* s_full = empty + kSlots;  // [2]
-    uint64_t* p_full = s_full + 2;      // [2], one arrival per softmax warp
-    uint64_t* o_full = p_full + 2;      // [2]
+    uint64_t* s_full = empty + kSlots;  // [tile * 2 + buffer]
+    uint64_t* p_full = s_full + 4;      // [tile * 2 + buffer], one arrival per softmax warp
+    uint64_t* o_full = p_full + 4;      // [tile]
     uint64_t* drain = o_full + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Gm::TSLOT_OFF);
     uint32_t* kbad = reinterpret_cast<uint32_t*>(smem + Gm::KBAD_OFF);
@@ -280,7 +301,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
     if (tid == 0) {
         for (int i = 0; i < kBars; ++i) {
             uint64_t* b = &full[i];
-            mbar_init(smem_u32(b), (b == &p_full[0] || b == &p_full[1]) ? 4 : 1);
+            mbar_init(smem_u32(b), (b >= p_full && b < p_full + 4) ? 4 : 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -326,23 +347,30 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
     if (warp == kLoadWarp) {
         // ------------------------------------------------------------ loads
         int issued = 0;
+        const int grp = lane / IDS, u = lane % IDS;
+        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
+        // block-table entry of this lane's box in key tile j (-1: past the
+        // context); read one tile ahead so the load latency is hidden
+        auto entry = [&](int j) {
+            const int tok = j * kKeys + grp * 16 + u * Gm::ROWS;
+            return (lane < Gm::SUBS && j < nkt && tok < L) ? table[tok / B] : -1;
+        };
+        int id_next = entry(0);
+        int id = -1;
+        bool bad = false;
         for (int t = 0; t < 2 * nkt; ++t) {
             const int j = t >> 1, sl = slot_of(t);
             const bool is_v = t & 1;
+            if (!is_v) {  // new key tile: validate its entries, fetch the next tile's
+                const int tok = j * kKeys + grp * 16 + u * Gm::ROWS;
+                id = id_next;
+                bad = lane < Gm::SUBS && tok < L && (id < 0 || id >= p.num_blocks);
+                if (bad) id = -1;
+                id_next = entry(j + 1);
+            }
             if (t >= kSlots && lane == 0) wait(&empty[sl], ((t / kSlots) - 1) & 1);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            const int grp = lane / IDS, u = lane % IDS;
-            const int tok = j * kKeys + grp * 16 + u * Gm::ROWS;
-            int id = -1;
-            bool bad = false;
-            if (lane < Gm::SUBS && tok < L) {
-                id = p.block_tables[(size_t)s * p.max_blocks + tok / B];
-                if (id < 0 || id >= p.num_blocks) {
-                    bad = true;
-                    id = -1;
-                }
-            }
             const unsigned have = __ballot_sync(0xffffffffu, id >= 0);
             const unsigned bads = __ballot_sync(0xffffffffu, bad);
             const uint32_t bar = smem_u32(&full[sl]);
@@ -355,6 +383,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             }
             __syncwarp();
             if (id >= 0) {
+                const int tok = j * kKeys + grp * 16 + u * Gm::ROWS;
                 const int row = (id * p.num_kv_heads + g) * B + (IDS > 1 ? 0 : tok % B);
                 const uint32_t dst = smem_u32(smem + Gm::SLOT_OFF + sl * Gm::SLOT_BYTES) +
                                      (grp * 16 + u * Gm::ROWS) * 128;
@@ -373,30 +402,48 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         // ------------------------------------------------------- MMA issue
         const uint32_t id_s = instr_desc<T>(kTileRows, kKeys, 0);
         const uint32_t id_o = instr_desc<T>(kTileRows, D, 1);
+        const uint32_t tm = __shfl_sync(0xffffffffu, tbase, 0);  // warp-uniform
         const uint32_t q_base = smem_u32(smem);
         const uint32_t slot_base = smem_u32(smem + Gm::SLOT_OFF);
+        // descriptors of Q and of ring slot 0; every operand is one of these
+        // moved by a constant or per-slot offset
+        const uint64_t q_desc = smem_desc(q_base, 16, 1024);
+        const uint64_t k_desc = smem_desc(slot_base, 16, 1024);          // K-major
+        const uint64_t v_desc = smem_desc(slot_base, Gm::HALF_KV, 1024);  // MN-major
+        // S_x(j) into S buffer j % 2 of tile x
         auto issue_s = [&](int x, int j) {
-            const uint32_t kb = slot_base + slot_of(2 * j) * Gm::SLOT_BYTES;
-            const uint32_t qb = q_base + x * Gm::Q_BYTES;
+            const uint64_t qd = desc_add(q_desc, x * Gm::Q_BYTES);
+            const uint64_t kd = desc_add(k_desc, slot_of(2 * j) * Gm::SLOT_BYTES);
+            const uint32_t d = tm + x * kTileCols + (j & 1) * kKeys;
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * Gm::HALF_Q + (kk & 3) * 32;
-                const uint32_t koff = (kk >> 2) * Gm::HALF_KV + (kk & 3) * 32;
-                umma(tbase + x * kTileCols, smem_desc(qb + off, 16, 1024),
-                     smem_desc(kb + koff, 16, 1024), id_s, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma(d, desc_add(qd, (kk >> 2) * Gm::HALF_Q + (kk & 3) * 32),
+                         desc_add(kd, (kk >> 2) * Gm::HALF_KV + (kk & 3) * 32), id_s, kk > 0);
+                umma_commit(smem_u32(&s_full[x * 2 + (j & 1)]));
             }
-            umma_commit(smem_u32(&s_full[x]));
+            __syncwarp();
         };
+        // O_x += P_x(j) V(j), P_x(j) in S buffer j % 2 (high part, remainder)
         auto issue_pv = [&](int x, int j) {
-            const uint32_t vb = slot_base + slot_of(2 * j + 1) * Gm::SLOT_BYTES;
-            const uint32_t pc = tbase + x * kTileCols + kColP;
+            const uint64_t vd = desc_add(v_desc, slot_of(2 * j + 1) * Gm::SLOT_BYTES);
+            const uint32_t pc = tm + x * kTileCols + (j & 1) * kKeys;
+            const uint32_t oc = tm + x * kTileCols + kColO;
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kKeys / 16; ++kk) {
-                const uint64_t vd = smem_desc(vb + kk * 2048, Gm::HALF_KV, 1024);
-                umma_ts(tbase + x * kTileCols + kColO, pc + kk * 8, vd, id_o, j > 0 || kk > 0);
-                umma_ts(tbase + x * kTileCols + kColO, pc + 32 + kk * 8, vd, id_o, 1);
+                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                    const uint64_t b = desc_add(vd, kk * 2048);
+                    umma_ts(oc, pc + kk * 8, b, id_o, j > 0 || kk > 0);
+                    umma_ts(oc, pc + 32 + kk * 8, b, id_o, 1);
+                }
+                umma_commit(smem_u32(&o_full[x]));
             }
-            umma_commit(smem_u32(&o_full[x]));
+            __syncwarp();
+        };
+        // commit from the issuing lane (tracks every MMA it issued so far)
+        auto commit = [&](uint64_t* bar) {
+            if (elect_one()) umma_commit(smem_u32(bar));
+            __syncwarp();
         };
         // V(j) landed; rows of keys past the context or in a bad block are
         // zeroed (their P is 0, and 0 * NaN must not reach O)
@@ -425,52 +472,52 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             ok = __shfl_sync(0xffffffffu, ok, 0);
         };
 
-        k_ready(0);
-        if (lane == 0 && ok) {
-            tmem_fence_after();
-            for (int x = 0; x < kQTiles; ++x)
-                if (nkt_of(x) > 0) issue_s(x, 0);
-            umma_commit(smem_u32(&empty[slot_of(0)]));
+        // S for the first two key tiles (both S buffers), then per key tile
+        // j: P_x(j) V(j) for each tile, and S_x(j + 2) into the buffer that
+        // P_x(j) V(j) has finished reading
+        for (int j = 0; j < 2 && j < nkt && ok; ++j) {
+            k_ready(j);
+            if (ok) {
+                tmem_fence_after();
+                for (int x = 0; x < kQTiles; ++x)
+                    if (j < nkt_of(x)) issue_s(x, j);
+                commit(&empty[slot_of(2 * j)]);
+            }
+            __syncwarp();
         }
-        __syncwarp();
         for (int j = 0; j < nkt && ok; ++j) {
-            bool v_in = false;
+            v_ready(j);
             for (int x = 0; x < kQTiles && ok; ++x) {
                 if (j >= nkt_of(x)) continue;
-                if (lane == 0) wait(&p_full[x], j & 1);
+                if (lane == 0) wait(&p_full[x * 2 + (j & 1)], (j >> 1) & 1);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                if (j + 1 < nkt_of(x)) {
-                    k_ready(j + 1);
-                    if (!ok) break;
-                    if (lane == 0) {
-                        tmem_fence_after();
-                        issue_s(x, j + 1);
-                    }
-                    __syncwarp();
-                }
-                if (!v_in) {
-                    v_ready(j);
-                    v_in = true;
-                    if (!ok) break;
-                }
-                if (lane == 0) {
+                if (ok) {
                     tmem_fence_after();
                     issue_pv(x, j);
                 }
                 __syncwarp();
             }
-            if (lane == 0 && ok) {
-                if (j + 1 < nkt) umma_commit(smem_u32(&empty[slot_of(2 * j + 2)]));
-                umma_commit(smem_u32(&empty[slot_of(2 * j + 1)]));
+            if (ok) commit(&empty[slot_of(2 * j + 1)]);
+            __syncwarp();
+            if (j + 2 >= nkt || !ok) continue;
+            k_ready(j + 2);
+            for (int x = 0; x < kQTiles && ok; ++x) {
+                if (j + 2 >= nkt_of(x)) continue;
+                if (lane == 0) wait(&o_full[x], j & 1);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (ok) {
+                    tmem_fence_after();
+                    issue_s(x, j + 2);
+                }
+                __syncwarp();
             }
+            if (ok) commit(&empty[slot_of(2 * j + 4)]);
             __syncwarp();
         }
-        // every MMA this thread issued has finished before the CTA exits
-        if (lane == 0) {
-            umma_commit(smem_u32(drain));
-            drain_wait(smem_u32(drain), 0);
-        }
+        // every MMA this warp issued has finished before the CTA exits
+        __syncwarp();
+        commit(drain);
+        if (lane == 0) drain_wait(smem_u32(drain), 0);
         __syncwarp();
     } else {
         // --------------------------------------------------------- softmax
@@ -482,25 +529,26 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         const float sl = p.scale_log2;
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < my_nkt; ++j) {
-            wait(&s_full[x], j & 1);
-            wait(&full[slot_of(2 * j)], phase_of(2 * j));  // orders the read of kbad
+            // S_x(j) done; K(j) had landed (and its kbad entry was written
+            // before the load warp's release-arrive) before S_x(j) was issued
+            wait(&s_full[x * 2 + (j & 1)], (j >> 1) & 1);
             tmem_fence_after();
             float sv[kKeys];
             {
                 float a[32];
-                tmem_ld32(tl, a);
+                tmem_ld32(tl + (j & 1) * kKeys, a);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) sv[i] = a[i];
-                tmem_ld32(tl + 32, a);
+                tmem_ld32(tl + (j & 1) * kKeys + 32, a);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) sv[32 + i] = a[i];
             }
             const int key0 = j * kKeys;
             const uint32_t bm = kbad[j % kRing];
-            if (key0 + kKeys - 1 <= pos && bm == 0) {
-#pragma unroll
-                for (int k = 0; k < kKeys; ++k) sv[k] *= sl;
-            } else {
+            // unmasked tile (every key visible and loaded, positive scale):
+            // scores stay raw and the scale is folded into the exponent's FMA
+            const bool plain = key0 + kKeys - 1 <= pos && bm == 0 && sl > 0.f;
+            if (!plain) {
 #pragma unroll
                 for (int k = 0; k < kKeys; ++k) {
                     const int box = (k >> 4) * IDS + (k & 15) / Gm::ROWS;
@@ -508,9 +556,17 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                     sv[k] = valid ? sv[k] * sl : -INFINITY;
                 }
             }
-            float mx = sv[0];
+            const float mul = plain ? sl : 1.f;
+            float mp[8];  // independent partial maxima (short dependency chains)
 #pragma unroll
-            for (int k = 1; k < kKeys; ++k) mx = fmaxf(mx, sv[k]);
+            for (int i = 0; i < 8; ++i) mp[i] = sv[i];
+#pragma unroll
+            for (int k = 8; k < kKeys; ++k) mp[k & 7] = fmaxf(mp[k & 7], sv[k]);
+#pragma unroll
+            for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) mp[i] = fmaxf(mp[i], mp[i + w]);
+            const float mx = mp[0] * mul;
             float alpha = 1.f;
             bool rescale = false;
             if (mx > m + 8.f) {  // also the first finite max (m = -inf)
@@ -519,19 +575,37 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                 m = mx;
             }
             const float ms = m == -INFINITY ? 0.f : m;
-            float rs = 0.f;
+            float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < kKeys; ++k) {
-                sv[k] = ex2(sv[k] - ms);
-                rs += sv[k];
+                sv[k] = ex2(fmaf(sv[k], mul, -ms));
+                sp[k & 7] += sv[k];
             }
+#pragma unroll
+            for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) sp[i] += sp[i + w];
+            const float rs = sp[0];
             l = l * alpha + rs;
             uint32_t hw[32], lw[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) Mma<T>::split(sv[2 * i], sv[2 * i + 1], hw[i], lw[i]);
-            // P V_{j-1} has read P and written O before either is touched
-            if (j > 0) wait(&o_full[x], (j - 1) & 1);
-            tmem_fence_after();
+            float hf[32], lf[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                hf[i] = __uint_as_float(hw[i]);
+                lf[i] = __uint_as_float(lw[i]);
+            }
+            // P_x(j) over S_x(j) (already read); P V_x(j-2), the last reader
+            // of this buffer, finished before S_x(j) was written
+            tmem_st32(tl + (j & 1) * kKeys, hf);
+            tmem_st32(tl + (j & 1) * kKeys + 32, lf);
+            // every phase of o_full is waited in turn (a parity wait must not
+            // fall two phases behind); O is rescaled after P V_x(j-1) wrote it
+            if (j > 0) {
+                wait(&o_full[x], (j - 1) & 1);
+                tmem_fence_after();
+            }
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -542,18 +616,10 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                     tmem_st32(tl + kColO + c * 32, o);
                 }
             }
-            float hf[32], lf[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                hf[i] = __uint_as_float(hw[i]);
-                lf[i] = __uint_as_float(lw[i]);
-            }
-            tmem_st32(tl + kColP, hf);
-            tmem_st32(tl + kColP + 32, lf);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tmem_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&p_full[x]));
+            if (lane == 0) mbar_arrive(smem_u32(&p_full[x * 2 + (j & 1)]));
         }
         // ---- epilogue: O / l for this thread's row
         if (my_nkt > 0) {
