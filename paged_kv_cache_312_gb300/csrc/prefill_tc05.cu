@@ -10,25 +10,26 @@
 // How (GB300 design): one CTA of 10 warps per (256 query rows, query head,
 // sequence), latest (heaviest) rows first; the rows form two 128-row tiles
 // A and B whose softmax work alternates with each other's tensor-core work.
-//  * warp 9 (loads): K and V tiles of 64 tokens by TMA (16-row boxes of the
-//    paged cache, 128-byte swizzle, [column half][key][128 B]) into an
-//    8-slot ring, K(0) V(0) K(1) V(1) ...; its lanes read the tile's block
-//    table entries in parallel and record bad entries for the softmax.
-//  * warp 8 (MMA issue, one lane): S_X(j) = Q_X K(j)^T into tensor memory
-//    (M=128, N=64, K=head_dim; Q and K K-major in shared memory), then
+//  * warp 9 (loads): K and V tiles of 128 tokens by TMA (16-row boxes of the
+//    paged cache, 128-byte swizzle, [column half][key][128 B]) into a ring of
+//    slots, K(0) V(0) K(1) V(1) ...; its lanes read the tile's block-table
+//    entries in parallel (one tile ahead) and record bad entries.
+//  * warp 8 (MMA issue): S_X(j) = Q_X K(j)^T into tensor memory (M=128,
+//    N=128, K=head_dim; Q and K K-major in shared memory), then
 //    O_X += P_X(j) V(j) with P read from tensor memory (M=128, N=head_dim,
-//    K=64; V the MN-major operand).  S_X(j+1) is issued as soon as the
-//    softmax of X has posted P_X(j).
-//  * warps 0-3 (tile A) and 4-7 (tile B): thread r owns row r of its tile:
-//    it reads the row of S from tensor memory, masks (diagonal, tail and bad
-//    blocks only), keeps a running max and sum in base 2, and writes P back
-//    to tensor memory as a 16-bit high part and remainder (both are
-//    multiplied, keeping ~16 bits of P).  The running max used for P moves
-//    only when the row max exceeds it by more than 8 (a factor 2^8), and only
-//    then is the O row rescaled; O and the sum always share the same max, so
-//    the result is unchanged.
-//  * Tensor memory (512 columns): tile A S [0,64) P [64,128) O [128,256),
-//    tile B the same at +256.
+//    K=128; V the MN-major operand).  The whole warp computes the operands
+//    and one elected lane issues.
+//  * warps 0-3 (tile A) and 4-7 (tile B): thread r owns row r of its tile.
+//    It reads its row of S from tensor memory in four 32-key chunks, masks
+//    (diagonal, tail and bad blocks only), keeps a running max and sum in
+//    base 2 and writes P back over the chunk of S it came from, as a 16-bit
+//    high part and remainder for each 16-key step (both are multiplied,
+//    keeping ~16 bits of P).  The running max used for P moves only when the
+//    row max exceeds it by more than 8 (a factor 2^8), and only then is the O
+//    row rescaled; O and the sum always share the same max, so the result is
+//    unchanged.
+//  * Tensor memory (512 columns): tile A S/P [0,128) O [128,256), tile B the
+//    same at +256.  S_X(j+1) is issued once P_X(j) V(j) has read P_X(j).
 // Every wait is bounded; a wait that gives up sets the TIMEOUT status bit
 // (which ends the waits of every other CTA too), and before the CTA frees
 // its tensor memory it waits (bounded) for its own copies and MMAs.
@@ -48,31 +49,29 @@ using namespace pkv_tc;
 
 constexpr int kTileRows = 128;  // query rows per tile (MMA M)
 constexpr int kQTiles = 2;      // query tiles per CTA
-constexpr int kKeys = 64;       // keys per K/V tile
-constexpr int kSlots = 8;       // K/V ring slots (one K or one V tile each)
+constexpr int kKeys = 128;      // keys per K/V tile
 constexpr int kRing = 16;       // bad-block masks kept per tile index
 constexpr int kMmaWarp = 8, kLoadWarp = 9;
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTileCols = 256;  // tensor-memory columns per query tile
-constexpr uint32_t kColO = 128;     // S buffers at columns 0 and 64, O at 128
-// barriers: full[kSlots], empty[kSlots], s_full[tile][buffer],
-// p_full[tile][buffer], o_full[tile], drain
-constexpr int kBars = 2 * kSlots + 11;
+constexpr uint32_t kColO = 128;      // S/P at columns [0,128), O at [128,256)
 
 template <int D, int B>
 struct G5 {
     static constexpr int NH = D / 64;
     static constexpr int ROWS = B < 16 ? B : 16;  // rows per TMA box
     static constexpr int IDS = 16 / ROWS;         // boxes per 16-token group
-    static constexpr int SUBS = 4 * IDS;          // boxes per 64-token tile and half
+    static constexpr int SUBS = (kKeys / 16) * IDS;  // boxes per key tile and half
     static constexpr int HALF_Q = kTileRows * 128;
     static constexpr int HALF_KV = kKeys * 128;
     static constexpr int Q_BYTES = NH * HALF_Q;
     static constexpr int SLOT_BYTES = NH * HALF_KV;
+    static constexpr int SLOTS = D == 128 ? 4 : 8;  // K/V ring (one K or V tile each)
+    static constexpr int BARS = 2 * SLOTS + 7;  // full, empty, s_full[2], p_full[2], o_full[2], drain
     static constexpr int SLOT_OFF = kQTiles * Q_BYTES;
-    static constexpr int BAR_OFF = SLOT_OFF + kSlots * SLOT_BYTES;
-    static constexpr int TSLOT_OFF = BAR_OFF + kBars * 8;
+    static constexpr int BAR_OFF = SLOT_OFF + SLOTS * SLOT_BYTES;
+    static constexpr int TSLOT_OFF = BAR_OFF + BARS * 8;
     static constexpr int KBAD_OFF = TSLOT_OFF + 16;
     static constexpr int SMEM_BYTES = 1024 + KBAD_OFF + kRing * 4;
     static_assert(HALF_KV % 1024 == 0 && HALF_Q % 1024 == 0, "swizzle atoms");
@@ -255,6 +254,59 @@ __device__ __forceinline__ void store_row32(void* out, size_t at, const float (&
     }
 }
 
+// Packed fp32 pair arithmetic (one instruction for two lanes of work).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// p0, p1 -> (16-bit high parts, 16-bit remainders), each packed lower key in
+// the low half.  The high part is p rounded to T; the remainder p - high is
+// exact in fp32 and then rounded to T.
+template <typename T>
+__device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uint32_t& lo)
+{
+    uint32_t h;
+    if (std::is_same<T, __nv_bfloat16>::value) {
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(p1), "f"(p0));
+        const float2 hf = make_float2(__uint_as_float(h << 16), __uint_as_float(h & 0xFFFF0000u));
+        const float2 r = fsub2(make_float2(p0, p1), hf);
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(r.y), "f"(r.x));
+    } else {
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(p1), "f"(p0));
+        const __half2 hh = *reinterpret_cast<const __half2*>(&h);
+        const float2 hf = __half22float2(hh);
+        const float2 r = fsub2(make_float2(p0, p1), hf);
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(r.y), "f"(r.x));
+    }
+    hi = h;
+}
+
 template <typename T, int D, int B>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
@@ -262,6 +314,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
 {
     using Gm = G5<D, B>;
     constexpr int IDS = Gm::IDS;
+    constexpr int SLOTS = Gm::SLOTS;
     const int ctile = gridDim.x - 1 - blockIdx.x;  // latest (heaviest) rows first
     const int h = blockIdx.y, s = blockIdx.z;
     const int r0 = p.query_start[s];
@@ -289,19 +342,19 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::BAR_OFF);
-    uint64_t* empty = full + kSlots;
-    uint64_t* s_full = empty + kSlots;  // [tile * 2 + buffer]
-    uint64_t* p_full = s_full + 4;      // [tile * 2 + buffer], one arrival per softmax warp
-    uint64_t* o_full = p_full + 4;      // [tile]
+    uint64_t* empty = full + SLOTS;
+    uint64_t* s_full = empty + SLOTS;  // [tile]
+    uint64_t* p_full = s_full + 2;     // [tile], one arrival per softmax warp
+    uint64_t* o_full = p_full + 2;     // [tile]
     uint64_t* drain = o_full + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Gm::TSLOT_OFF);
     uint32_t* kbad = reinterpret_cast<uint32_t*>(smem + Gm::KBAD_OFF);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int i = 0; i < kBars; ++i) {
+        for (int i = 0; i < Gm::BARS; ++i) {
             uint64_t* b = &full[i];
-            mbar_init(smem_u32(b), (b >= p_full && b < p_full + 4) ? 4 : 1);
+            mbar_init(smem_u32(b), (b == &p_full[0] || b == &p_full[1]) ? 4 : 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -341,8 +394,8 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         }
     };
     // ring position of K(j) (t = 2j) and V(j) (t = 2j + 1)
-    auto slot_of = [](int t) { return t % kSlots; };
-    auto phase_of = [](int t) { return (t / kSlots) & 1; };
+    auto slot_of = [](int t) { return t % SLOTS; };
+    auto phase_of = [](int t) { return (t / SLOTS) & 1; };
 
     if (warp == kLoadWarp) {
         // ------------------------------------------------------------ loads
@@ -368,7 +421,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                 if (bad) id = -1;
                 id_next = entry(j + 1);
             }
-            if (t >= kSlots && lane == 0) wait(&empty[sl], ((t / kSlots) - 1) & 1);
+            if (t >= SLOTS && lane == 0) wait(&empty[sl], ((t / SLOTS) - 1) & 1);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const unsigned have = __ballot_sync(0xffffffffu, id >= 0);
@@ -395,7 +448,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         }
         // the ring's last fills must have landed before the CTA exits
         if (lane == 0)
-            for (int t = max(0, issued - kSlots); t < issued; ++t)
+            for (int t = max(0, issued - SLOTS); t < issued; ++t)
                 drain_wait(smem_u32(&full[slot_of(t)]), phase_of(t));
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -410,31 +463,32 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         const uint64_t q_desc = smem_desc(q_base, 16, 1024);
         const uint64_t k_desc = smem_desc(slot_base, 16, 1024);          // K-major
         const uint64_t v_desc = smem_desc(slot_base, Gm::HALF_KV, 1024);  // MN-major
-        // S_x(j) into S buffer j % 2 of tile x
+        // S_x(j) into tile x's S/P columns
         auto issue_s = [&](int x, int j) {
             const uint64_t qd = desc_add(q_desc, x * Gm::Q_BYTES);
             const uint64_t kd = desc_add(k_desc, slot_of(2 * j) * Gm::SLOT_BYTES);
-            const uint32_t d = tm + x * kTileCols + (j & 1) * kKeys;
+            const uint32_t d = tm + x * kTileCols;
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     umma(d, desc_add(qd, (kk >> 2) * Gm::HALF_Q + (kk & 3) * 32),
                          desc_add(kd, (kk >> 2) * Gm::HALF_KV + (kk & 3) * 32), id_s, kk > 0);
-                umma_commit(smem_u32(&s_full[x * 2 + (j & 1)]));
+                umma_commit(smem_u32(&s_full[x]));
             }
             __syncwarp();
         };
-        // O_x += P_x(j) V(j), P_x(j) in S buffer j % 2 (high part, remainder)
+        // O_x += P_x(j) V(j); P of 16-key step kk at columns 16 kk (high
+        // parts) and 16 kk + 8 (remainders)
         auto issue_pv = [&](int x, int j) {
             const uint64_t vd = desc_add(v_desc, slot_of(2 * j + 1) * Gm::SLOT_BYTES);
-            const uint32_t pc = tm + x * kTileCols + (j & 1) * kKeys;
+            const uint32_t pc = tm + x * kTileCols;
             const uint32_t oc = tm + x * kTileCols + kColO;
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
                     const uint64_t b = desc_add(vd, kk * 2048);
-                    umma_ts(oc, pc + kk * 8, b, id_o, j > 0 || kk > 0);
-                    umma_ts(oc, pc + 32 + kk * 8, b, id_o, 1);
+                    umma_ts(oc, pc + kk * 16, b, id_o, j > 0 || kk > 0);
+                    umma_ts(oc, pc + kk * 16 + 8, b, id_o, 1);
                 }
                 umma_commit(smem_u32(&o_full[x]));
             }
@@ -472,47 +526,36 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             ok = __shfl_sync(0xffffffffu, ok, 0);
         };
 
-        // S for the first two key tiles (both S buffers), then per key tile
-        // j: P_x(j) V(j) for each tile, and S_x(j + 2) into the buffer that
-        // P_x(j) V(j) has finished reading
-        for (int j = 0; j < 2 && j < nkt && ok; ++j) {
-            k_ready(j);
-            if (ok) {
-                tmem_fence_after();
-                for (int x = 0; x < kQTiles; ++x)
-                    if (j < nkt_of(x)) issue_s(x, j);
-                commit(&empty[slot_of(2 * j)]);
-            }
-            __syncwarp();
+        // S for the first key tile; then per key tile j: P_x(j) V(j) for
+        // each tile, and S_x(j + 1) once P_x(j) V(j) has read P_x(j)
+        k_ready(0);
+        if (ok) {
+            tmem_fence_after();
+            for (int x = 0; x < kQTiles; ++x)
+                if (nkt_of(x) > 0) issue_s(x, 0);
+            commit(&empty[slot_of(0)]);
         }
         for (int j = 0; j < nkt && ok; ++j) {
             v_ready(j);
             for (int x = 0; x < kQTiles && ok; ++x) {
                 if (j >= nkt_of(x)) continue;
-                if (lane == 0) wait(&p_full[x * 2 + (j & 1)], (j >> 1) & 1);
+                if (lane == 0) wait(&p_full[x], j & 1);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (ok) {
                     tmem_fence_after();
                     issue_pv(x, j);
                 }
-                __syncwarp();
             }
             if (ok) commit(&empty[slot_of(2 * j + 1)]);
-            __syncwarp();
-            if (j + 2 >= nkt || !ok) continue;
-            k_ready(j + 2);
+            if (j + 1 >= nkt || !ok) continue;
+            k_ready(j + 1);
             for (int x = 0; x < kQTiles && ok; ++x) {
-                if (j + 2 >= nkt_of(x)) continue;
+                if (j + 1 >= nkt_of(x)) continue;
                 if (lane == 0) wait(&o_full[x], j & 1);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (ok) {
-                    tmem_fence_after();
-                    issue_s(x, j + 2);
-                }
-                __syncwarp();
+                if (ok) issue_s(x, j + 1);
             }
-            if (ok) commit(&empty[slot_of(2 * j + 4)]);
-            __syncwarp();
+            if (ok) commit(&empty[slot_of(2 * j + 2)]);
         }
         // every MMA this warp issued has finished before the CTA exits
         __syncwarp();
@@ -530,38 +573,42 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < my_nkt; ++j) {
             // S_x(j) done; K(j) had landed (and its kbad entry was written
-            // before the load warp's release-arrive) before S_x(j) was issued
-            wait(&s_full[x * 2 + (j & 1)], (j >> 1) & 1);
+            // before the load warp's release-arrive) before S_x(j) was issued.
+            // P V_x(j-1) finished before S_x(j) was issued; waiting for it here
+            // keeps every o_full phase waited in turn (a parity wait must not
+            // fall two phases behind)
+            wait(&s_full[x], j & 1);
+            if (j > 0) wait(&o_full[x], (j - 1) & 1);
             tmem_fence_after();
-            float sv[kKeys];
-            {
-                float a[32];
-                tmem_ld32(tl + (j & 1) * kKeys, a);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sv[i] = a[i];
-                tmem_ld32(tl + (j & 1) * kKeys + 32, a);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sv[32 + i] = a[i];
-            }
             const int key0 = j * kKeys;
             const uint32_t bm = kbad[j % kRing];
             // unmasked tile (every key visible and loaded, positive scale):
             // scores stay raw and the scale is folded into the exponent's FMA
             const bool plain = key0 + kKeys - 1 <= pos && bm == 0 && sl > 0.f;
-            if (!plain) {
-#pragma unroll
-                for (int k = 0; k < kKeys; ++k) {
-                    const int box = (k >> 4) * IDS + (k & 15) / Gm::ROWS;
-                    const bool valid = key0 + k <= pos && !((bm >> box) & 1u);
-                    sv[k] = valid ? sv[k] * sl : -INFINITY;
-                }
-            }
             const float mul = plain ? sl : 1.f;
-            float mp[8];  // independent partial maxima (short dependency chains)
+            auto load_chunk = [&](int c, float (&v)[32]) {
+                tmem_ld32(tl + c * 32, v);
+                if (!plain) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mp[i] = sv[i];
+                    for (int i = 0; i < 32; ++i) {
+                        const int k = c * 32 + i;
+                        const int box = (k >> 4) * IDS + (k & 15) / Gm::ROWS;
+                        const bool valid = key0 + k <= pos && !((bm >> box) & 1u);
+                        v[i] = valid ? v[i] * sl : -INFINITY;
+                    }
+                }
+            };
+            // pass 1: row max (eight independent partial maxima)
+            float mp[8];
 #pragma unroll
-            for (int k = 8; k < kKeys; ++k) mp[k & 7] = fmaxf(mp[k & 7], sv[k]);
+            for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kKeys / 32; ++c) {
+                float v[32];
+                load_chunk(c, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mp[i & 7] = fmaxf(mp[i & 7], v[i]);
+            }
 #pragma unroll
             for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
@@ -575,37 +622,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                 m = mx;
             }
             const float ms = m == -INFINITY ? 0.f : m;
-            float sp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int k = 0; k < kKeys; ++k) {
-                sv[k] = ex2(fmaf(sv[k], mul, -ms));
-                sp[k & 7] += sv[k];
-            }
-#pragma unroll
-            for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-                for (int i = 0; i < w; ++i) sp[i] += sp[i + w];
-            const float rs = sp[0];
-            l = l * alpha + rs;
-            uint32_t hw[32], lw[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) Mma<T>::split(sv[2 * i], sv[2 * i + 1], hw[i], lw[i]);
-            float hf[32], lf[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                hf[i] = __uint_as_float(hw[i]);
-                lf[i] = __uint_as_float(lw[i]);
-            }
-            // P_x(j) over S_x(j) (already read); P V_x(j-2), the last reader
-            // of this buffer, finished before S_x(j) was written
-            tmem_st32(tl + (j & 1) * kKeys, hf);
-            tmem_st32(tl + (j & 1) * kKeys + 32, lf);
-            // every phase of o_full is waited in turn (a parity wait must not
-            // fall two phases behind); O is rescaled after P V_x(j-1) wrote it
-            if (j > 0) {
-                wait(&o_full[x], (j - 1) & 1);
-                tmem_fence_after();
-            }
+            // O is rescaled before P V_x(j) is issued (it waits for p_full)
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -616,10 +633,37 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                     tmem_st32(tl + kColO + c * 32, o);
                 }
             }
+            // pass 2: P = 2^(s - m) per chunk, written over that chunk of S as
+            // [16-key step][high parts 8 columns][remainders 8 columns]
+            float2 sum2 = make_float2(0.f, 0.f);
+            const float2 mul2 = make_float2(mul, mul), nms2 = make_float2(-ms, -ms);
+#pragma unroll
+            for (int c = 0; c < kKeys / 32; ++c) {
+                float v[32];
+                load_chunk(c, v);
+                float pw[32];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int k = half * 16 + 2 * i;
+                        float2 e = ffma2(make_float2(v[k], v[k + 1]), mul2, nms2);
+                        e.x = ex2(e.x);
+                        e.y = ex2(e.y);
+                        sum2 = fadd2(sum2, e);
+                        uint32_t hw, lw;
+                        split_pair<T>(e.x, e.y, hw, lw);
+                        pw[half * 16 + i] = __uint_as_float(hw);
+                        pw[half * 16 + 8 + i] = __uint_as_float(lw);
+                    }
+                }
+                tmem_st32(tl + c * 32, pw);
+            }
+            l = l * alpha + (sum2.x + sum2.y);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tmem_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&p_full[x * 2 + (j & 1)]));
+            if (lane == 0) mbar_arrive(smem_u32(&p_full[x]));
         }
         // ---- epilogue: O / l for this thread's row
         if (my_nkt > 0) {
