@@ -29,7 +29,8 @@
 //    row rescaled; O and the sum always share the same max, so the result is
 //    unchanged.
 //  * Tensor memory (512 columns): tile A S/P [0,128) O [128,256), tile B the
-//    same at +256.  S_X(j+1) is issued once P_X(j) V(j) has read P_X(j).
+//    same at +256.  S_X(j+1) is issued once P_X(j) V(j) has read P_X(j),
+//    before the other tile's P V.
 // Every wait is bounded; a wait that gives up sets the TIMEOUT status bit
 // (which ends the waits of every other CTA too), and before the CTA frees
 // its tensor memory it waits (bounded) for its own copies and MMAs.
@@ -526,8 +527,10 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             ok = __shfl_sync(0xffffffffu, ok, 0);
         };
 
-        // S for the first key tile; then per key tile j: P_x(j) V(j) for
-        // each tile, and S_x(j + 1) once P_x(j) V(j) has read P_x(j)
+        // S for the first key tile; then per key tile j and query tile x:
+        // P_x(j) V(j), and S_x(j + 1) as soon as P_x(j) V(j) has read P_x(j)
+        // (it shares S_x's columns), ahead of the other tile's P V so the
+        // softmax of x waits for its next S as little as possible
         k_ready(0);
         if (ok) {
             tmem_fence_after();
@@ -541,21 +544,18 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                 if (j >= nkt_of(x)) continue;
                 if (lane == 0) wait(&p_full[x], j & 1);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (ok) {
-                    tmem_fence_after();
-                    issue_pv(x, j);
-                }
-            }
-            if (ok) commit(&empty[slot_of(2 * j + 1)]);
-            if (j + 1 >= nkt || !ok) continue;
-            k_ready(j + 1);
-            for (int x = 0; x < kQTiles && ok; ++x) {
+                if (!ok) break;
+                tmem_fence_after();
+                issue_pv(x, j);
                 if (j + 1 >= nkt_of(x)) continue;
+                k_ready(j + 1);
                 if (lane == 0) wait(&o_full[x], j & 1);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (ok) issue_s(x, j + 1);
             }
-            if (ok) commit(&empty[slot_of(2 * j + 2)]);
+            if (!ok) break;
+            commit(&empty[slot_of(2 * j + 1)]);
+            if (j + 1 < nkt) commit(&empty[slot_of(2 * j + 2)]);
         }
         // every MMA this warp issued has finished before the CTA exits
         __syncwarp();
