@@ -359,30 +359,37 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tslot)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    if (warp < 8) {  // this thread's query row into shared memory (zero past qn)
-        const int x = warp >> 2, r = tid & (kTileRows - 1);
-        const int row = q0 + x * kTileRows + r;
-        const T* src = static_cast<const T*>(p.q) + ((size_t)(r0 + row) * p.num_heads + h) * D;
-        uint8_t* qx = smem + x * Gm::Q_BYTES;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (row < qn) v = *reinterpret_cast<const uint4*>(src + c * 8);
-            *reinterpret_cast<uint4*>(qx + (c >> 3) * Gm::HALF_Q + swz(r, c & 7)) = v;
+    __syncthreads();  // barriers initialised; the load warp starts its copies now
+    uint32_t tbase = 0;
+    if (warp != kLoadWarp) {
+        if (warp == 0) {
+            asm volatile(
+                "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                    smem_u32(tslot)),
+                "r"(kTmemCols)
+                : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         }
+        if (warp < 8) {  // this thread's query row into shared memory (zero past qn)
+            const int x = warp >> 2, r = tid & (kTileRows - 1);
+            const int row = q0 + x * kTileRows + r;
+            const T* src =
+                static_cast<const T*>(p.q) + ((size_t)(r0 + row) * p.num_heads + h) * D;
+            uint8_t* qx = smem + x * Gm::Q_BYTES;
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (row < qn) v = *reinterpret_cast<const uint4*>(src + c * 8);
+                *reinterpret_cast<uint4*>(qx + (c >> 3) * Gm::HALF_Q + swz(r, c & 7)) = v;
+            }
+        }
+        fence_proxy_async();
+        tmem_fence_before();
+        // softmax and MMA warps only (named barrier 1, 9 warps)
+        asm volatile("bar.sync 1, %0;" ::"n"(kThreads - 32) : "memory");
+        tmem_fence_after();
+        tbase = *tslot;
     }
-    fence_proxy_async();
-    tmem_fence_before();
-    __syncthreads();
-    tmem_fence_after();
-    const uint32_t tbase = *tslot;
 
     bool ok = true;
     // Waits for a phase unless this thread already gave up; a wait that gives
