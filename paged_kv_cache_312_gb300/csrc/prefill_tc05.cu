@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
+#include <algorithm>
 #include <type_traits>
 
 #include "pkv.h"
@@ -69,7 +70,7 @@ struct G5 {
     static constexpr int Q_BYTES = NH * HALF_Q;
     static constexpr int SLOT_BYTES = NH * HALF_KV;
     static constexpr int SLOTS = D == 128 ? 4 : 8;  // K/V ring (one K or V tile each)
-    static constexpr int BARS = 2 * SLOTS + 7;  // full, empty, s_full[2], p_full[2], o_full[2], drain
+    static constexpr int BARS = 2 * SLOTS + 9;  // full, empty, s/p/o/q_full[2], drain
     static constexpr int SLOT_OFF = kQTiles * Q_BYTES;
     static constexpr int BAR_OFF = SLOT_OFF + SLOTS * SLOT_BYTES;
     static constexpr int TSLOT_OFF = BAR_OFF + BARS * 8;
@@ -308,36 +309,65 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uin
     hi = h;
 }
 
+// One work item: 256 query rows (tiles A and B) of one query head of one
+// sequence.  Items are numbered with the latest (heaviest) rows first and the
+// head fastest, so consecutive items (taken by neighbouring CTAs) have equal
+// cost and share their sequence's K/V in L2.
+struct Item {
+    int h, s, r0, qn, L, q0, g, base_pos, nkt_a, nkt_b, nkt;
+};
+
+template <int B>
+__device__ __forceinline__ bool decode_item(const PrefillParams& p, int items_x, int v, Item& it)
+{
+    const int hs = p.num_heads * p.num_seqs;
+    const int ct = items_x - 1 - v / hs;
+    const int rem = v % hs;
+    it.h = rem % p.num_heads;
+    it.s = rem / p.num_heads;
+    it.r0 = p.query_start[it.s];
+    it.qn = p.query_start[it.s + 1] - it.r0;
+    it.L = p.context_lens[it.s];
+    if (it.L < 0 || (int64_t)it.L > (int64_t)p.max_blocks * B || it.qn < 0 || it.qn > it.L ||
+        it.qn > p.max_query_len)
+        return false;  // flagged once per sequence by the load warp
+    it.q0 = ct * kQTiles * kTileRows;
+    if (it.q0 >= it.qn) return false;
+    it.g = it.h / (p.num_heads / p.num_kv_heads);
+    it.base_pos = it.L - it.qn;
+    auto tiles_for = [&](int x) {
+        const int rows = min(it.qn - (it.q0 + x * kTileRows), kTileRows);
+        return rows > 0 ? (it.base_pos + it.q0 + x * kTileRows + rows - 1) / kKeys + 1 : 0;
+    };
+    it.nkt_a = tiles_for(0);
+    it.nkt_b = tiles_for(1);
+    it.nkt = max(it.nkt_a, it.nkt_b);
+    return true;
+}
+
+template <int B>
+__device__ __forceinline__ bool item_bad_lengths(const PrefillParams& p, int items_x, int v)
+{
+    const int hs = p.num_heads * p.num_seqs;
+    const int ct = items_x - 1 - v / hs;
+    const int rem = v % hs;
+    if (ct != items_x - 1 || rem % p.num_heads != 0) return false;  // once per sequence
+    const int s = rem / p.num_heads;
+    const int qn = p.query_start[s + 1] - p.query_start[s];
+    const int L = p.context_lens[s];
+    return L < 0 || (int64_t)L > (int64_t)p.max_blocks * B || qn < 0 || qn > L ||
+           qn > p.max_query_len;
+}
+
 template <typename T, int D, int B>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
-                    const __grid_constant__ CUtensorMap vmap)
+                    const __grid_constant__ CUtensorMap vmap, int items_x)
 {
     using Gm = G5<D, B>;
     constexpr int IDS = Gm::IDS;
     constexpr int SLOTS = Gm::SLOTS;
-    const int ctile = gridDim.x - 1 - blockIdx.x;  // latest (heaviest) rows first
-    const int h = blockIdx.y, s = blockIdx.z;
-    const int r0 = p.query_start[s];
-    const int qn = p.query_start[s + 1] - r0;
-    const int L = p.context_lens[s];
-    if (L < 0 || (int64_t)L > (int64_t)p.max_blocks * B || qn < 0 || qn > L ||
-        qn > p.max_query_len) {
-        if (ctile == 0 && h == 0 && threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
-        return;
-    }
-    const int q0 = ctile * kQTiles * kTileRows;
-    if (q0 >= qn) return;
-    const int g = h / (p.num_heads / p.num_kv_heads);
-    const int base_pos = L - qn;
-    // key tiles each query tile needs (0 for a tile past the last row)
-    auto tiles_for = [&](int x) {
-        const int rows = min(qn - (q0 + x * kTileRows), kTileRows);
-        return rows > 0 ? (base_pos + q0 + x * kTileRows + rows - 1) / kKeys + 1 : 0;
-    };
-    const int nkt_a = tiles_for(0), nkt_b = tiles_for(1);
-    auto nkt_of = [&](int x) { return x ? nkt_b : nkt_a; };
-    const int nkt = max(nkt_a, nkt_b);
+    const int total_items = items_x * p.num_heads * p.num_seqs;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -347,7 +377,8 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
     uint64_t* s_full = empty + SLOTS;  // [tile]
     uint64_t* p_full = s_full + 2;     // [tile], one arrival per softmax warp
     uint64_t* o_full = p_full + 2;     // [tile]
-    uint64_t* drain = o_full + 2;
+    uint64_t* q_full = o_full + 2;     // [tile], one arrival per softmax warp
+    uint64_t* drain = q_full + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Gm::TSLOT_OFF);
     uint32_t* kbad = reinterpret_cast<uint32_t*>(smem + Gm::KBAD_OFF);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -355,41 +386,23 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
     if (tid == 0) {
         for (int i = 0; i < Gm::BARS; ++i) {
             uint64_t* b = &full[i];
-            mbar_init(smem_u32(b), (b == &p_full[0] || b == &p_full[1]) ? 4 : 1);
+            const bool per_warp = b == &p_full[0] || b == &p_full[1] || b == &q_full[0] ||
+                                  b == &q_full[1];
+            mbar_init(smem_u32(b), per_warp ? 4 : 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __syncthreads();  // barriers initialised; the load warp starts its copies now
-    uint32_t tbase = 0;
-    if (warp != kLoadWarp) {
-        if (warp == 0) {
-            asm volatile(
-                "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                    smem_u32(tslot)),
-                "r"(kTmemCols)
-                : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-        }
-        if (warp < 8) {  // this thread's query row into shared memory (zero past qn)
-            const int x = warp >> 2, r = tid & (kTileRows - 1);
-            const int row = q0 + x * kTileRows + r;
-            const T* src =
-                static_cast<const T*>(p.q) + ((size_t)(r0 + row) * p.num_heads + h) * D;
-            uint8_t* qx = smem + x * Gm::Q_BYTES;
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (row < qn) v = *reinterpret_cast<const uint4*>(src + c * 8);
-                *reinterpret_cast<uint4*>(qx + (c >> 3) * Gm::HALF_Q + swz(r, c & 7)) = v;
-            }
-        }
-        fence_proxy_async();
-        tmem_fence_before();
-        // softmax and MMA warps only (named barrier 1, 9 warps)
-        asm volatile("bar.sync 1, %0;" ::"n"(kThreads - 32) : "memory");
-        tmem_fence_after();
-        tbase = *tslot;
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tslot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    const uint32_t tbase = *tslot;
 
     bool ok = true;
     // Waits for a phase unless this thread already gave up; a wait that gives
@@ -401,63 +414,70 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             atomicOr(p.status, PKV_STATUS_TIMEOUT);
         }
     };
-    // ring position of K(j) (t = 2j) and V(j) (t = 2j + 1)
+    // ring position of K(kt) (t = 2 kt) and V(kt) (t = 2 kt + 1), kt counted
+    // over all of this CTA's key tiles
     auto slot_of = [](int t) { return t % SLOTS; };
     auto phase_of = [](int t) { return (t / SLOTS) & 1; };
 
     if (warp == kLoadWarp) {
         // ------------------------------------------------------------ loads
-        int issued = 0;
+        int t = 0, kt0 = 0;
         const int grp = lane / IDS, u = lane % IDS;
-        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
-        // block-table entry of this lane's box in key tile j (-1: past the
-        // context); read one tile ahead so the load latency is hidden
-        auto entry = [&](int j) {
-            const int tok = j * kKeys + grp * 16 + u * Gm::ROWS;
-            return (lane < Gm::SUBS && j < nkt && tok < L) ? table[tok / B] : -1;
-        };
-        int id_next = entry(0);
-        int id = -1;
-        bool bad = false;
-        for (int t = 0; t < 2 * nkt; ++t) {
-            const int j = t >> 1, sl = slot_of(t);
-            const bool is_v = t & 1;
-            if (!is_v) {  // new key tile: validate its entries, fetch the next tile's
+        for (int v = blockIdx.x; v < total_items && ok; v += gridDim.x) {
+            if (lane == 0 && item_bad_lengths<B>(p, items_x, v))
+                atomicOr(p.status, PKV_STATUS_BAD_LEN);
+            Item it;
+            if (!decode_item<B>(p, items_x, v, it)) continue;
+            const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks;
+            // block-table entry of this lane's box in key tile j (-1: past the
+            // context); read one tile ahead so the load latency is hidden
+            auto entry = [&](int j) {
                 const int tok = j * kKeys + grp * 16 + u * Gm::ROWS;
-                id = id_next;
-                bad = lane < Gm::SUBS && tok < L && (id < 0 || id >= p.num_blocks);
+                return (lane < Gm::SUBS && j < it.nkt && tok < it.L) ? table[tok / B] : -1;
+            };
+            int id_next = entry(0);
+            for (int j = 0; j < it.nkt; ++j) {
+                const int tok = j * kKeys + grp * 16 + u * Gm::ROWS;
+                int id = id_next;
+                const bool bad = lane < Gm::SUBS && tok < it.L && (id < 0 || id >= p.num_blocks);
                 if (bad) id = -1;
                 id_next = entry(j + 1);
-            }
-            if (t >= SLOTS && lane == 0) wait(&empty[sl], ((t / SLOTS) - 1) & 1);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            const unsigned have = __ballot_sync(0xffffffffu, id >= 0);
-            const unsigned bads = __ballot_sync(0xffffffffu, bad);
-            const uint32_t bar = smem_u32(&full[sl]);
-            if (lane == 0) {
-                if (!is_v) {
-                    kbad[j % kRing] = bads;
-                    if (bads) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
-                }
-                mbar_arrive_expect_tx(bar, __popc(have) * Gm::NH * Gm::ROWS * 128);
-            }
-            __syncwarp();
-            if (id >= 0) {
-                const int tok = j * kKeys + grp * 16 + u * Gm::ROWS;
-                const int row = (id * p.num_kv_heads + g) * B + (IDS > 1 ? 0 : tok % B);
-                const uint32_t dst = smem_u32(smem + Gm::SLOT_OFF + sl * Gm::SLOT_BYTES) +
-                                     (grp * 16 + u * Gm::ROWS) * 128;
+                const unsigned have = __ballot_sync(0xffffffffu, id >= 0);
+                const unsigned bads = __ballot_sync(0xffffffffu, bad);
+                for (int kv = 0; kv < 2; ++kv, ++t) {
+                    const int sl = slot_of(t);
+                    if (t >= SLOTS && lane == 0) wait(&empty[sl], ((t / SLOTS) - 1) & 1);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    const uint32_t bar = smem_u32(&full[sl]);
+                    if (lane == 0) {
+                        if (kv == 0) {
+                            kbad[(kt0 + j) % kRing] = bads;
+                            if (bads) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
+                        }
+                        mbar_arrive_expect_tx(bar, __popc(have) * Gm::NH * Gm::ROWS * 128);
+                    }
+                    __syncwarp();
+                    if (id >= 0) {
+                        const int row =
+                            (id * p.num_kv_heads + it.g) * B + (IDS > 1 ? 0 : tok % B);
+                        const uint32_t dst =
+                            smem_u32(smem + Gm::SLOT_OFF + sl * Gm::SLOT_BYTES) +
+                            (grp * 16 + u * Gm::ROWS) * 128;
 #pragma unroll
-                for (int hf = 0; hf < Gm::NH; ++hf)
-                    tma_load_2d(dst + hf * Gm::HALF_KV, is_v ? &vmap : &kmap, hf * 64, row, bar);
+                        for (int hf = 0; hf < Gm::NH; ++hf)
+                            tma_load_2d(dst + hf * Gm::HALF_KV, kv ? &vmap : &kmap, hf * 64, row,
+                                        bar);
+                    }
+                }
+                if (!ok) break;
             }
-            issued = t + 1;
+            kt0 += it.nkt;
         }
         // the ring's last fills must have landed before the CTA exits
         if (lane == 0)
-            for (int t = max(0, issued - SLOTS); t < issued; ++t)
-                drain_wait(smem_u32(&full[slot_of(t)]), phase_of(t));
+            for (int f = max(0, t - SLOTS); f < t; ++f)
+                drain_wait(smem_u32(&full[slot_of(f)]), phase_of(f));
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issue
@@ -471,10 +491,10 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         const uint64_t q_desc = smem_desc(q_base, 16, 1024);
         const uint64_t k_desc = smem_desc(slot_base, 16, 1024);          // K-major
         const uint64_t v_desc = smem_desc(slot_base, Gm::HALF_KV, 1024);  // MN-major
-        // S_x(j) into tile x's S/P columns
-        auto issue_s = [&](int x, int j) {
+        // S_x = Q_x K(kt)^T into tile x's S/P columns
+        auto issue_s = [&](int x, int kt) {
             const uint64_t qd = desc_add(q_desc, x * Gm::Q_BYTES);
-            const uint64_t kd = desc_add(k_desc, slot_of(2 * j) * Gm::SLOT_BYTES);
+            const uint64_t kd = desc_add(k_desc, slot_of(2 * kt) * Gm::SLOT_BYTES);
             const uint32_t d = tm + x * kTileCols;
             if (elect_one()) {
 #pragma unroll
@@ -485,17 +505,17 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             }
             __syncwarp();
         };
-        // O_x += P_x(j) V(j); P of 16-key step kk at columns 16 kk (high
+        // O_x (+)= P_x V(kt); P of 16-key step kk at columns 16 kk (high
         // parts) and 16 kk + 8 (remainders)
-        auto issue_pv = [&](int x, int j) {
-            const uint64_t vd = desc_add(v_desc, slot_of(2 * j + 1) * Gm::SLOT_BYTES);
+        auto issue_pv = [&](int x, int kt, bool first) {
+            const uint64_t vd = desc_add(v_desc, slot_of(2 * kt + 1) * Gm::SLOT_BYTES);
             const uint32_t pc = tm + x * kTileCols;
             const uint32_t oc = tm + x * kTileCols + kColO;
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
                     const uint64_t b = desc_add(vd, kk * 2048);
-                    umma_ts(oc, pc + kk * 16, b, id_o, j > 0 || kk > 0);
+                    umma_ts(oc, pc + kk * 16, b, id_o, !first || kk > 0);
                     umma_ts(oc, pc + kk * 16 + 8, b, id_o, 1);
                 }
                 umma_commit(smem_u32(&o_full[x]));
@@ -507,15 +527,18 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             if (elect_one()) umma_commit(smem_u32(bar));
             __syncwarp();
         };
-        // V(j) landed; rows of keys past the context or in a bad block are
+        auto k_ready = [&](int kt) {
+            if (lane == 0) wait(&full[slot_of(2 * kt)], phase_of(2 * kt));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+        };
+        // V(kt) landed; rows of keys past the context or in a bad block are
         // zeroed (their P is 0, and 0 * NaN must not reach O)
-        auto v_ready = [&](int j) {
-            const int t = 2 * j + 1;
+        auto v_ready = [&](int kt, int key0, int L) {
+            const int t = 2 * kt + 1;
             if (lane == 0) wait(&full[slot_of(t)], phase_of(t));
             ok = __shfl_sync(0xffffffffu, ok, 0);
             __syncwarp();  // the other lanes read kbad after lane 0's acquire
-            const int key0 = j * kKeys;
-            const uint32_t bm = kbad[j % kRing];
+            const uint32_t bm = kbad[kt % kRing];
             if (ok && (key0 + kKeys > L || bm)) {
                 uint8_t* vt = smem + Gm::SLOT_OFF + slot_of(t) * Gm::SLOT_BYTES;
                 for (int i = lane; i < Gm::NH * kKeys * 8; i += 32) {
@@ -529,40 +552,58 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             }
             __syncwarp();
         };
-        auto k_ready = [&](int j) {
-            if (lane == 0) wait(&full[slot_of(2 * j)], phase_of(2 * j));
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-        };
 
-        // S for the first key tile; then per key tile j and query tile x:
-        // P_x(j) V(j), and S_x(j + 1) as soon as P_x(j) V(j) has read P_x(j)
-        // (it shares S_x's columns), ahead of the other tile's P V so the
-        // softmax of x waits for its next S as little as possible
-        k_ready(0);
-        if (ok) {
-            tmem_fence_after();
-            for (int x = 0; x < kQTiles; ++x)
-                if (nkt_of(x) > 0) issue_s(x, 0);
-            commit(&empty[slot_of(0)]);
-        }
-        for (int j = 0; j < nkt && ok; ++j) {
-            v_ready(j);
+        // per tile x: S/P/O phases count this CTA's key tiles of x so far
+        // (n[x]); q_full phases count the items in which x has rows (nq[x])
+        int n[kQTiles] = {0, 0}, nq[kQTiles] = {0, 0};
+        int kt0 = 0;
+        for (int v = blockIdx.x; v < total_items && ok; v += gridDim.x) {
+            Item it;
+            if (!decode_item<B>(p, items_x, v, it)) continue;
+            auto nkt_of = [&](int x) { return x ? it.nkt_b : it.nkt_a; };
+            // S_x of the first key tile: after the softmax of x has loaded the
+            // new Q and read out the previous O, and the previous P V_x (which
+            // read P in the S columns) has finished
+            k_ready(kt0);
             for (int x = 0; x < kQTiles && ok; ++x) {
-                if (j >= nkt_of(x)) continue;
-                if (lane == 0) wait(&p_full[x], j & 1);
+                if (nkt_of(x) == 0) continue;
+                if (lane == 0) {
+                    wait(&q_full[x], nq[x] & 1);
+                    if (n[x] > 0) wait(&o_full[x], (n[x] - 1) & 1);
+                }
+                ++nq[x];
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 tmem_fence_after();
-                issue_pv(x, j);
-                if (j + 1 >= nkt_of(x)) continue;
-                k_ready(j + 1);
-                if (lane == 0) wait(&o_full[x], j & 1);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (ok) issue_s(x, j + 1);
+                issue_s(x, kt0);
             }
             if (!ok) break;
-            commit(&empty[slot_of(2 * j + 1)]);
-            if (j + 1 < nkt) commit(&empty[slot_of(2 * j + 2)]);
+            commit(&empty[slot_of(2 * kt0)]);
+            // per key tile j and query tile x: P_x(j) V(j), then S_x(j + 1) as
+            // soon as that P V has read P_x(j) (it shares S_x's columns), ahead
+            // of the other tile's P V
+            for (int j = 0; j < it.nkt && ok; ++j) {
+                const int kt = kt0 + j;
+                v_ready(kt, j * kKeys, it.L);
+                for (int x = 0; x < kQTiles && ok; ++x) {
+                    if (j >= nkt_of(x)) continue;
+                    if (lane == 0) wait(&p_full[x], n[x] & 1);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    tmem_fence_after();
+                    issue_pv(x, kt, j == 0);
+                    ++n[x];
+                    if (j + 1 >= nkt_of(x)) continue;
+                    k_ready(kt + 1);
+                    if (lane == 0) wait(&o_full[x], (n[x] - 1) & 1);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (ok) issue_s(x, kt + 1);
+                }
+                if (!ok) break;
+                commit(&empty[slot_of(2 * kt + 1)]);
+                if (j + 1 < it.nkt) commit(&empty[slot_of(2 * kt + 2)]);
+            }
+            kt0 += it.nkt;
         }
         // every MMA this warp issued has finished before the CTA exits
         __syncwarp();
@@ -571,123 +612,164 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         __syncwarp();
     } else {
         // --------------------------------------------------------- softmax
-        const int x = warp >> 2;
-        const int row = q0 + x * kTileRows + (tid & (kTileRows - 1));
-        const int pos = row < qn ? base_pos + row : -1;  // -1: padding row
-        const int my_nkt = nkt_of(x);
+        const int x = warp >> 2, r = tid & (kTileRows - 1);
         const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16) + x * kTileCols;
         const float sl = p.scale_log2;
-        float m = -INFINITY, l = 0.f;
-        for (int j = 0; j < my_nkt; ++j) {
-            // S_x(j) done; K(j) had landed (and its kbad entry was written
-            // before the load warp's release-arrive) before S_x(j) was issued.
-            // P V_x(j-1) finished before S_x(j) was issued; waiting for it here
-            // keeps every o_full phase waited in turn (a parity wait must not
-            // fall two phases behind)
-            wait(&s_full[x], j & 1);
-            if (j > 0) wait(&o_full[x], (j - 1) & 1);
-            tmem_fence_after();
-            const int key0 = j * kKeys;
-            const uint32_t bm = kbad[j % kRing];
-            // unmasked tile (every key visible and loaded, positive scale):
-            // scores stay raw and the scale is folded into the exponent's FMA
-            const bool plain = key0 + kKeys - 1 <= pos && bm == 0 && sl > 0.f;
-            const float mul = plain ? sl : 1.f;
-            auto load_chunk = [&](int c, float (&v)[32]) {
-                tmem_ld32(tl + c * 32, v);
-                if (!plain) {
+        const bool vec = (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+        uint8_t* qx = smem + x * Gm::Q_BYTES;
+        int n = 0, kt0 = 0;
+        for (int v = blockIdx.x; v < total_items && ok; v += gridDim.x) {
+            Item it;
+            if (!decode_item<B>(p, items_x, v, it)) continue;
+            const int my_nkt = x ? it.nkt_b : it.nkt_a;
+            const int row = it.q0 + x * kTileRows + r;
+            const int pos = row < it.qn ? it.base_pos + row : -1;  // -1: padding row
+            if (my_nkt > 0) {
+                // this row of Q into shared memory (zero past qn); the S MMAs of
+                // this tile's previous item finished before its last softmax
+                const T* src = static_cast<const T*>(p.q) +
+                               ((size_t)(it.r0 + row) * p.num_heads + it.h) * D;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int k = c * 32 + i;
-                        const int box = (k >> 4) * IDS + (k & 15) / Gm::ROWS;
-                        const bool valid = key0 + k <= pos && !((bm >> box) & 1u);
-                        v[i] = valid ? v[i] * sl : -INFINITY;
+                for (int c = 0; c < D / 8; ++c) {
+                    uint4 q4 = make_uint4(0u, 0u, 0u, 0u);
+                    if (row < it.qn) q4 = *reinterpret_cast<const uint4*>(src + c * 8);
+                    *reinterpret_cast<uint4*>(qx + (c >> 3) * Gm::HALF_Q + swz(r, c & 7)) = q4;
+                }
+                fence_proxy_async();
+                tmem_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&q_full[x]));
+                // the next item's Q row of this thread into L2 meanwhile
+                {
+                    Item nx;
+                    const int vn = v + gridDim.x;
+                    if (vn < total_items && decode_item<B>(p, items_x, vn, nx)) {
+                        const int rn = nx.q0 + x * kTileRows + r;
+                        if (rn < nx.qn) {
+                            const T* qn_src = static_cast<const T*>(p.q) +
+                                              ((size_t)(nx.r0 + rn) * p.num_heads + nx.h) * D;
+#pragma unroll
+                            for (int c = 0; c < D * (int)sizeof(T); c += 128)
+                                asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                                    reinterpret_cast<const uint8_t*>(qn_src) + c));
+                        }
                     }
                 }
-            };
-            // pass 1: row max (eight independent partial maxima)
-            float mp[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kKeys / 32; ++c) {
-                float v[32];
-                load_chunk(c, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mp[i & 7] = fmaxf(mp[i & 7], v[i]);
             }
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < my_nkt; ++j, ++n) {
+                // S_x(j) done; K(j) had landed (and its kbad entry was written
+                // before the load warp's release-arrive) before S_x(j) was
+                // issued.  P V_x(j-1) finished before S_x(j) was issued; waiting
+                // for it here keeps every o_full phase waited in turn (a parity
+                // wait must not fall two phases behind)
+                wait(&s_full[x], n & 1);
+                if (j > 0) wait(&o_full[x], (n - 1) & 1);
+                tmem_fence_after();
+                const int key0 = j * kKeys;
+                const uint32_t bm = kbad[(kt0 + j) % kRing];
+                // unmasked tile (every key visible and loaded, positive scale):
+                // scores stay raw and the scale is folded into the exponent's FMA
+                const bool plain = key0 + kKeys - 1 <= pos && bm == 0 && sl > 0.f;
+                const float mul = plain ? sl : 1.f;
+                auto load_chunk = [&](int c, float (&vv)[32]) {
+                    tmem_ld32(tl + c * 32, vv);
+                    if (!plain) {
 #pragma unroll
-            for (int w = 4; w >= 1; w >>= 1)
+                        for (int i = 0; i < 32; ++i) {
+                            const int k = c * 32 + i;
+                            const int box = (k >> 4) * IDS + (k & 15) / Gm::ROWS;
+                            const bool valid = key0 + k <= pos && !((bm >> box) & 1u);
+                            vv[i] = valid ? vv[i] * sl : -INFINITY;
+                        }
+                    }
+                };
+                // pass 1: row max (eight independent partial maxima)
+                float mp[8];
 #pragma unroll
-                for (int i = 0; i < w; ++i) mp[i] = fmaxf(mp[i], mp[i + w]);
-            const float mx = mp[0] * mul;
-            float alpha = 1.f;
-            bool rescale = false;
-            if (mx > m + 8.f) {  // also the first finite max (m = -inf)
-                rescale = m != -INFINITY;
-                alpha = ex2(m - mx);
-                m = mx;
+                for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kKeys / 32; ++c) {
+                    float vv[32];
+                    load_chunk(c, vv);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mp[i & 7] = fmaxf(mp[i & 7], vv[i]);
+                }
+#pragma unroll
+                for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int i = 0; i < w; ++i) mp[i] = fmaxf(mp[i], mp[i + w]);
+                const float mx = mp[0] * mul;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (mx > m + 8.f) {  // also the first finite max (m = -inf)
+                    rescale = m != -INFINITY;
+                    alpha = ex2(m - mx);
+                    m = mx;
+                }
+                const float ms = m == -INFINITY ? 0.f : m;
+                // O is rescaled before P V_x(j) is issued (it waits for p_full)
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(tl + kColO + c * 32, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(tl + kColO + c * 32, o);
+                    }
+                }
+                // pass 2: P = 2^(s - m) per chunk, written over that chunk of S
+                // as [16-key step][high parts 8 columns][remainders 8 columns]
+                float2 sum2 = make_float2(0.f, 0.f);
+                const float2 mul2 = make_float2(mul, mul), nms2 = make_float2(-ms, -ms);
+#pragma unroll
+                for (int c = 0; c < kKeys / 32; ++c) {
+                    float vv[32];
+                    load_chunk(c, vv);
+                    float pw[32];
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int k = half * 16 + 2 * i;
+                            float2 e = ffma2(make_float2(vv[k], vv[k + 1]), mul2, nms2);
+                            e.x = ex2(e.x);
+                            e.y = ex2(e.y);
+                            sum2 = fadd2(sum2, e);
+                            uint32_t hw, lw;
+                            split_pair<T>(e.x, e.y, hw, lw);
+                            pw[half * 16 + i] = __uint_as_float(hw);
+                            pw[half * 16 + 8 + i] = __uint_as_float(lw);
+                        }
+                    }
+                    tmem_st32(tl + c * 32, pw);
+                }
+                l = l * alpha + (sum2.x + sum2.y);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tmem_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&p_full[x]));
             }
-            const float ms = m == -INFINITY ? 0.f : m;
-            // O is rescaled before P V_x(j) is issued (it waits for p_full)
-            if (__any_sync(0xffffffffu, rescale)) {
+            // ---- epilogue: O / l for this thread's row
+            if (my_nkt > 0) {
+                wait(&o_full[x], (n - 1) & 1);
+                tmem_fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     float o[32];
                     tmem_ld32(tl + kColO + c * 32, o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tmem_st32(tl + kColO + c * 32, o);
+                    for (int i = 0; i < 32; ++i) o[i] *= inv;
+                    if (pos >= 0 && ok)
+                        store_row32(p.out,
+                                    ((size_t)(it.r0 + row) * p.num_heads + it.h) * D + c * 32,
+                                    o, p.out_dtype, vec);
                 }
+                tmem_fence_before();
             }
-            // pass 2: P = 2^(s - m) per chunk, written over that chunk of S as
-            // [16-key step][high parts 8 columns][remainders 8 columns]
-            float2 sum2 = make_float2(0.f, 0.f);
-            const float2 mul2 = make_float2(mul, mul), nms2 = make_float2(-ms, -ms);
-#pragma unroll
-            for (int c = 0; c < kKeys / 32; ++c) {
-                float v[32];
-                load_chunk(c, v);
-                float pw[32];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int k = half * 16 + 2 * i;
-                        float2 e = ffma2(make_float2(v[k], v[k + 1]), mul2, nms2);
-                        e.x = ex2(e.x);
-                        e.y = ex2(e.y);
-                        sum2 = fadd2(sum2, e);
-                        uint32_t hw, lw;
-                        split_pair<T>(e.x, e.y, hw, lw);
-                        pw[half * 16 + i] = __uint_as_float(hw);
-                        pw[half * 16 + 8 + i] = __uint_as_float(lw);
-                    }
-                }
-                tmem_st32(tl + c * 32, pw);
-            }
-            l = l * alpha + (sum2.x + sum2.y);
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            tmem_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&p_full[x]));
-        }
-        // ---- epilogue: O / l for this thread's row
-        if (my_nkt > 0) {
-            wait(&o_full[x], (my_nkt - 1) & 1);
-            tmem_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const bool vec = (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                tmem_ld32(tl + kColO + c * 32, o);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] *= inv;
-                if (pos >= 0 && ok)
-                    store_row32(p.out, ((size_t)(r0 + row) * p.num_heads + h) * D + c * 32, o,
-                                p.out_dtype, vec);
-            }
+            kt0 += it.nkt;
         }
     }
     tmem_fence_before();
@@ -697,6 +779,20 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
                      "r"(kTmemCols)
                      : "memory");
+}
+
+int sm_count()
+{
+    static int count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (count[dev] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
+            c = 148;
+        count[dev] = c;
+    }
+    return count[dev];
 }
 
 template <typename T, int D, int B>
@@ -709,9 +805,15 @@ cudaError_t launch5(const PrefillParams& p, const void* kmap, const void* vmap,
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int rows = kQTiles * kTileRows;
-    dim3 grid((p.max_query_len + rows - 1) / rows, p.num_heads, p.num_seqs);
+    const int items_x = (p.max_query_len + rows - 1) / rows;
+    const long long items = (long long)items_x * p.num_heads * p.num_seqs;
+    if (items <= 0) return cudaSuccess;
+    if (items > (1ll << 31) - 1) return cudaErrorInvalidValue;
+    // persistent: one CTA per SM (shared memory and tensor memory allow one)
+    const int grid = (int)std::min<long long>(items, sm_count());
     kern<<<grid, kThreads, Gm::SMEM_BYTES, stream>>>(p, *static_cast<const CUtensorMap*>(kmap),
-                                                     *static_cast<const CUtensorMap*>(vmap));
+                                                     *static_cast<const CUtensorMap*>(vmap),
+                                                     items_x);
     return cudaGetLastError();
 }
 
