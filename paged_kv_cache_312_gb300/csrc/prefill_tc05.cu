@@ -70,7 +70,9 @@ struct G5 {
     static constexpr int Q_BYTES = NH * HALF_Q;
     static constexpr int SLOT_BYTES = NH * HALF_KV;
     static constexpr int SLOTS = D == 128 ? 4 : 8;  // K/V ring (one K or V tile each)
-    static constexpr int BARS = 2 * SLOTS + 9;  // full, empty, s/p/o/q_full[2], drain
+    // full, empty per slot; s_full, o_full, q_full per tile; p_half per tile
+    // and half; drain
+    static constexpr int BARS = 2 * SLOTS + 11;
     static constexpr int SLOT_OFF = kQTiles * Q_BYTES;
     static constexpr int BAR_OFF = SLOT_OFF + SLOTS * SLOT_BYTES;
     static constexpr int TSLOT_OFF = BAR_OFF + BARS * 8;
@@ -256,6 +258,14 @@ __device__ __forceinline__ void store_row32(void* out, size_t at, const float (&
     }
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Packed fp32 pair arithmetic (one instruction for two lanes of work).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
 {
@@ -375,8 +385,8 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::BAR_OFF);
     uint64_t* empty = full + SLOTS;
     uint64_t* s_full = empty + SLOTS;  // [tile]
-    uint64_t* p_full = s_full + 2;     // [tile], one arrival per softmax warp
-    uint64_t* o_full = p_full + 2;     // [tile]
+    uint64_t* p_half = s_full + 2;     // [tile * 2 + half], one arrival per softmax warp
+    uint64_t* o_full = p_half + 4;     // [tile]
     uint64_t* q_full = o_full + 2;     // [tile], one arrival per softmax warp
     uint64_t* drain = q_full + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Gm::TSLOT_OFF);
@@ -386,7 +396,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
     if (tid == 0) {
         for (int i = 0; i < Gm::BARS; ++i) {
             uint64_t* b = &full[i];
-            const bool per_warp = b == &p_full[0] || b == &p_full[1] || b == &q_full[0] ||
+            const bool per_warp = (b >= p_half && b < p_half + 4) || b == &q_full[0] ||
                                   b == &q_full[1];
             mbar_init(smem_u32(b), per_warp ? 4 : 1);
         }
@@ -505,20 +515,21 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             }
             __syncwarp();
         };
-        // O_x (+)= P_x V(kt); P of 16-key step kk at columns 16 kk (high
-        // parts) and 16 kk + 8 (remainders)
-        auto issue_pv = [&](int x, int kt, bool first) {
+        // O_x (+)= P_x V(kt) for keys [64 hh, 64 hh + 64); P of 16-key step
+        // kk at columns 16 kk (high parts) and 16 kk + 8 (remainders)
+        auto issue_pv_half = [&](int x, int kt, int hh, bool first) {
             const uint64_t vd = desc_add(v_desc, slot_of(2 * kt + 1) * Gm::SLOT_BYTES);
             const uint32_t pc = tm + x * kTileCols;
             const uint32_t oc = tm + x * kTileCols + kColO;
             if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                for (int k4 = 0; k4 < kKeys / 32; ++k4) {
+                    const int kk = hh * (kKeys / 32) + k4;
                     const uint64_t b = desc_add(vd, kk * 2048);
                     umma_ts(oc, pc + kk * 16, b, id_o, !first || kk > 0);
                     umma_ts(oc, pc + kk * 16 + 8, b, id_o, 1);
                 }
-                umma_commit(smem_u32(&o_full[x]));
+                if (hh == 1) umma_commit(smem_u32(&o_full[x]));
             }
             __syncwarp();
         };
@@ -587,11 +598,16 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                 v_ready(kt, j * kKeys, it.L);
                 for (int x = 0; x < kQTiles && ok; ++x) {
                     if (j >= nkt_of(x)) continue;
-                    if (lane == 0) wait(&p_full[x], n[x] & 1);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    // the first half of P_x(j) goes to the tensor cores while the
+                    // softmax computes the second
+                    for (int hh = 0; hh < 2 && ok; ++hh) {
+                        if (lane == 0) wait(&p_half[x * 2 + hh], n[x] & 1);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) break;
+                        tmem_fence_after();
+                        issue_pv_half(x, kt, hh, j == 0);
+                    }
                     if (!ok) break;
-                    tmem_fence_after();
-                    issue_pv(x, kt, j == 0);
                     ++n[x];
                     if (j + 1 >= nkt_of(x)) continue;
                     k_ready(kt + 1);
@@ -693,7 +709,9 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                     float vv[32];
                     load_chunk(c, vv);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mp[i & 7] = fmaxf(mp[i & 7], vv[i]);
+                    for (int i = 0; i < 32; i += 16)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) mp[e] = fmax3(mp[e], vv[i + e], vv[i + 8 + e]);
                 }
 #pragma unroll
                 for (int w = 4; w >= 1; w >>= 1)
@@ -708,7 +726,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                     m = mx;
                 }
                 const float ms = m == -INFINITY ? 0.f : m;
-                // O is rescaled before P V_x(j) is issued (it waits for p_full)
+                // O is rescaled before P V_x(j) is issued (it waits for p_half)
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -744,12 +762,16 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                         }
                     }
                     tmem_st32(tl + c * 32, pw);
+                    if (c == kKeys / 64 - 1 || c == kKeys / 32 - 1) {
+                        // a half of P_x(j) is in place: its P V may start
+                        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                        tmem_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(smem_u32(&p_half[x * 2 + (c == kKeys / 32 - 1)]));
+                    }
                 }
                 l = l * alpha + (sum2.x + sum2.y);
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                tmem_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&p_full[x]));
             }
             // ---- epilogue: O / l for this thread's row
             if (my_nkt > 0) {
