@@ -1,8 +1,10 @@
 """Benchmark of the paged decode step on GB300.
 
 Default workload: bf16 MHA decode step, 32 heads x head_dim 128, block 16,
-64 sequences with context lengths uniform on [1, 2048]; one step = kv_write of
-each sequence's new token + paged decode attention over its context.  The
+64 sequences with context lengths uniform on [1, 2048]; one step = each
+sequence's new token appended to the cache and paged decode attention over
+its context, in one decode-step call (the append runs inside the attention
+launch).  The
 metric is KV bytes the attention must read (sum_s L_s * 2 * Hkv * D * 2) per
 second, with decode steps/s beside it.
 
@@ -104,6 +106,12 @@ class Step:
                 self.tables, self.lens = case.block_tables, case.context_lens
             self.unique_blocks = None
         self.P = launch_partition(w, self.tables.shape[1]) if partition is None else partition
+        if self.slots is not None:
+            # the step's new tokens sit at position L-1 of each sequence (what
+            # the decode-step call writes, through the table)
+            for s_, (row, n) in enumerate(zip(self.tables.tolist(), self.lens.tolist())):
+                want = row[(n - 1) // w.block_size] * w.block_size + (n - 1) % w.block_size
+                assert int(self.slots[s_]) == want, "step slot is not position L-1"
         L = self.lens.to(torch.int64)
         b = w.torch_dtype.itemsize
         self.kv_bytes = int(L.sum()) * 2 * w.num_kv_heads * w.head_dim * b
@@ -111,6 +119,8 @@ class Step:
         io = S * w.num_heads * w.head_dim * (b + 4) + int((L + w.block_size - 1).div(
             w.block_size, rounding_mode="floor").sum()) * 4 + S * 4
         self.attn_bytes = self.kv_bytes + io  # KV + q + fp32 out + table entries + lens
+        if self.slots is not None:  # the decode step also reads and stores the new K/V
+            self.attn_bytes += 2 * 2 * S * w.num_kv_heads * w.head_dim * b
 
 
 # ---------------------------------------------------------------------------
@@ -213,23 +223,26 @@ def run_gpu(args, rank, world, local_rank):
                          dtype=torch.uint8, device=dev)
     has_write = st.slots is not None
     if has_write:
-        nk, nv, sl = st.new_key.to(dev), st.new_value.to(dev), st.slots.to(dev)
+        nk, nv = st.new_key.to(dev), st.new_value.to(dev)
     pairs = st.pairs.to(dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
         if pairs.shape[0]:
             pkv.kv_copy_blocks(kc, vc, pairs, stream=stream)
-        if has_write:
-            pkv.kv_write(kc, vc, nk, nv, sl, stream=stream)
         if ev is not None:
             ev.record(stream)
-        pkv.paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, w.block_size, w.num_kv_heads,
-                                   partition_size=st.P, workspace=ws, stream=stream)
+        if has_write:  # append the new tokens and attend, one call
+            pkv.decode_step(out, q, nk, nv, kc, vc, bt, cl, w.scale, w.block_size,
+                            w.num_kv_heads, partition_size=st.P, workspace=ws, stream=stream)
+        else:
+            pkv.paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, w.block_size,
+                                       w.num_kv_heads, partition_size=st.P, workspace=ws,
+                                       stream=stream)
 
-    # one decode kernel per call (split mode also merges inside it, after a
-    # driver memset of its completion counters)
-    launches_per_step = (1 if pairs.shape[0] else 0) + (1 if has_write else 0) + 1
+    # one decode kernel per call, the append fused in (split mode also merges
+    # inside it, after a driver memset of its completion counters)
+    launches_per_step = (1 if pairs.shape[0] else 0) + 1
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -270,9 +283,8 @@ def run_gpu(args, rank, world, local_rank):
         h_out = torch.empty((S, Hq, D), dtype=torch.float32).pin_memory()
         h_in = [h_q, h_bt, h_cl]
         if has_write:
-            h_nk, h_nv, h_sl = st.new_key.pin_memory(), st.new_value.pin_memory(), \
-                st.slots.pin_memory()
-            h_in += [h_nk, h_nv, h_sl]
+            h_nk, h_nv = st.new_key.pin_memory(), st.new_value.pin_memory()
+            h_in += [h_nk, h_nv]
         h_pairs = st.pairs.pin_memory()
         h_in.append(h_pairs)
         h2d = sum(t.numel() * t.element_size() for t in h_in)
@@ -287,7 +299,6 @@ def run_gpu(args, rank, world, local_rank):
             if has_write:
                 nk.copy_(h_nk, non_blocking=True)
                 nv.copy_(h_nv, non_blocking=True)
-                sl.copy_(h_sl, non_blocking=True)
             if pairs.shape[0]:
                 pairs.copy_(h_pairs, non_blocking=True)
             step()
@@ -313,7 +324,8 @@ def run_gpu(args, rank, world, local_rank):
                    "num_kv_heads": w.num_kv_heads, "head_dim": D, "block_size": w.block_size,
                    "partition_size": st.P, "kv_bytes_per_step": st.kv_bytes,
                    "step": ("cow-copy + " if pairs.shape[0] else "") +
-                   ("kv_write + " if has_write else "") + "paged_decode_attention",
+                   ("decode_step (new tokens appended inside the attention launch)"
+                    if has_write else "paged_decode_attention"),
                    "l2": "inputs larger than L2 (KV %.2f GB vs 129 MB L2), no flush" %
                    (st.kv_bytes / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -322,9 +334,10 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention call: tensor-core "
-                     "decode kernel with in-kernel log-sum-exp merge (+ counter memset)"
-                     if st.P else "paged_decode_attention (tensor-core kernel)",
+        "roofline": {"bound": "hbm", "kernel": ("decode_step" if has_write else
+                                                "paged_decode_attention") +
+                     (" call: tensor-core decode kernel with in-kernel log-sum-exp merge "
+                      "(+ counter memset)" if st.P else " (tensor-core kernel)"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": tr,
                      "algorithmic_bytes_per_launch": st.attn_bytes,

@@ -149,6 +149,36 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
                                size_t workspace_bytes, void* stream);
 
 /*
+ * decode_step -- one decode step of every sequence in one call: each
+ * sequence's new token is appended to the cache and then attended to along
+ * with everything before it.  Equivalent to pkv_kv_write of the new tokens
+ * followed by pkv_paged_decode_attention ([CAY] KV-cache paragraph: each
+ * step's K/V is stored, then every step attends over all cached tokens;
+ * [AIPP core idea 3-4]: the token at position p of sequence s sits at slot
+ * table[s][p / block_size] * block_size + p % block_size).
+ *
+ * new_k, new_v : [num_seqs][num_kv_heads][head_dim], dtype kv_dtype, 16-byte
+ *                aligned: the new token of sequence s, written at position
+ *                context_lens[s] - 1 (context_lens counts the new token; its
+ *                block must already be in the table, e.g. from
+ *                pkv_step_append).
+ * k_cache, v_cache : written at those positions, read as in
+ *                pkv_paged_decode_attention.
+ * All other arguments, the workspace and the error behaviour are those of
+ * pkv_paged_decode_attention.  A sequence whose table entry for the new
+ * position is out of range gets no write and sets PKV_STATUS_BAD_BLOCK.
+ * On the tensor-core kernel the write happens inside the attention launch
+ * (by the CTA that reads that position); on the CUDA-core kernel a separate
+ * append launch precedes the attention.
+ */
+int pkv_decode_step(void* out, const void* q, const void* new_k, const void* new_v,
+                    void* k_cache, void* v_cache, const int32_t* block_tables,
+                    const int32_t* context_lens, float scale, int block_size, int num_kv_heads,
+                    int num_seqs, int num_heads, int head_dim, int max_blocks_per_seq,
+                    int num_blocks, int kv_dtype, int out_dtype, int partition_size,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * paged_prefill_attention -- several new query tokens per sequence (a prompt,
  * or a chunk of one), each attending causally over the sequence's cached
  * tokens up to its own position.  [CAY recomputation]: a whole sequence's KV

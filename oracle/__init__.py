@@ -166,6 +166,29 @@ def kv_write(k_cache, v_cache, key, value, slot_mapping, block_size):
         raise ValueError("orc_kv_write failed: %d" % rc)
 
 
+def decode_step(q, new_k, new_v, k_cache, v_cache, block_tables, context_lens, scale,
+                block_size, num_kv_heads, nthreads=1):
+    """One decode step ([CAY] KV-cache paragraph): in place, the new token of
+    sequence s (new_k/new_v[s]) is stored at position context_lens[s] - 1,
+    i.e. at slot_for_position(table row, L - 1) ([AIPP] core idea 3-4); then
+    the step's query attends over the updated cache.  Returns that output.
+    A sequence with no tokens, or whose table entry for the new position is
+    not a block of the cache, gets no write."""
+    NB = k_cache.shape[0]
+    lens = _cpu(context_lens).tolist()
+    tables = _cpu(block_tables)
+    slots = []
+    for s, L in enumerate(lens):
+        ok = L > 0 and (L - 1) // block_size < tables.shape[1]
+        if ok:
+            blk = int(tables[s, (L - 1) // block_size])
+            ok = 0 <= blk < NB
+        slots.append(slot_for_position(tables[s].tolist(), L - 1, block_size) if ok else -1)
+    kv_write(k_cache, v_cache, new_k, new_v, torch.tensor(slots, dtype=torch.int64), block_size)
+    return paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                  block_size, num_kv_heads, nthreads=nthreads)
+
+
 def kv_copy_blocks(k_cache, v_cache, pairs):
     """In place: for each (src, dst) row of pairs, in order, the whole physical
     block dst of K and V becomes a copy of block src."""

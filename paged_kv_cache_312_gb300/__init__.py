@@ -5,14 +5,16 @@ include/pkv.h); this package is the thin Python binding over it.
 """
 from ._binding import (  # noqa: F401
     KERNEL_AUTO, KERNEL_CUDA_CORE, PKV_BF16, PKV_F16, PKV_F32, PREFILL_TCGEN05, PREFILL_WARP_MMA,
-    STATUS_BITS, BlockAllocator, NOALLOC_SCRATCH_BYTES, OutOfBlocks, PkvError, decode_workspace_bytes, device_status,
+    STATUS_BITS, BlockAllocator, NOALLOC_SCRATCH_BYTES, OutOfBlocks, PkvError, decode_step,
+    decode_workspace_bytes, device_status,
     kv_copy_blocks, kv_swap_blocks, kv_write, lib, paged_decode_attention,
     paged_decode_attention_noalloc, paged_prefill_attention, set_decode_kernel,
     set_prefill_kernel,
 )
 
 __all__ = [
-    "BlockAllocator", "OutOfBlocks", "PkvError", "decode_workspace_bytes", "device_status",
+    "BlockAllocator", "OutOfBlocks", "PkvError", "decode_step", "decode_workspace_bytes",
+    "device_status",
     "kv_copy_blocks", "kv_swap_blocks", "kv_write", "lib", "paged_decode_attention",
     "paged_decode_attention_noalloc", "paged_prefill_attention", "set_decode_kernel",
     "set_prefill_kernel",

@@ -33,6 +33,8 @@ _SIGS = {
     "pkv_paged_decode_attention": (_I, [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I,
                                         _I, _I, _I, _P, _SZ, _P]),
     "pkv_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I,
+                             _I, _I, _I, _P, _SZ, _P]),
     "pkv_paged_prefill_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I,
                                          _I, _I, _I, _I, _I, _P]),
     "pkv_paged_decode_attention_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I,
@@ -165,6 +167,35 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
         DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], int(partition_size), ws_ptr, ws_bytes,
         _stream(stream))
     _check(rc, "pkv_paged_decode_attention")
+
+
+def decode_step(out, q, new_k, new_v, k_cache, v_cache, block_tables, context_lens, scale,
+                block_size, num_kv_heads, partition_size=0, workspace=None, stream=None):
+    """One decode step: new_k/new_v [S, Hkv, D] are written at position
+    context_lens[s]-1 of each sequence, then out [S, Hq, D] = paged decode
+    attention of q over the updated caches."""
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = k_cache.shape
+    if (Hkv, B, Dk) != (num_kv_heads, block_size, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("decode_step: cache shape mismatch")
+    if out.shape != q.shape or new_k.shape != (S, Hkv, D) or new_v.shape != new_k.shape:
+        raise ValueError("decode_step: out must be [S, Hq, D], new_k/new_v [S, Hkv, D]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks], context_lens [S]")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype == new_k.dtype == new_v.dtype):
+        raise ValueError("q, new_k, new_v, k_cache, v_cache must share a dtype")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    rc = lib().pkv_decode_step(
+        _dev(out, "out"), _dev(q, "q"), _dev(new_k, "new_k"), _dev(new_v, "new_v"),
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"),
+        _dev(context_lens, "context_lens"), float(scale), int(block_size), int(num_kv_heads), S,
+        Hq, D, block_tables.shape[1], NB, DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype],
+        int(partition_size), ws_ptr, ws_bytes, _stream(stream))
+    _check(rc, "pkv_decode_step")
 
 
 def paged_prefill_attention(out, q, k_cache, v_cache, block_tables, context_lens, query_start,

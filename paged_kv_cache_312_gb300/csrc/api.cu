@@ -323,14 +323,20 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int
     return workspace_layout(num_seqs, num_heads, P, head_dim).total;
 }
 
-int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
-                               const int32_t* block_tables, const int32_t* context_lens,
-                               float scale, int block_size, int num_kv_heads, int num_seqs,
-                               int num_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
-                               int kv_dtype, int out_dtype, int partition_size, void* workspace,
-                               size_t workspace_bytes, void* stream)
+}  // extern "C"
+
+namespace {
+
+// Decode attention, optionally with the step's append fused in (new_k and
+// new_v non-NULL: each sequence's new token goes to position
+// context_lens[s]-1 first).
+int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
+                const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                float scale, int block_size, int num_kv_heads, int num_seqs, int num_heads,
+                int head_dim, int max_blocks_per_seq, int num_blocks, int kv_dtype, int out_dtype,
+                int partition_size, void* workspace, size_t workspace_bytes, void* stream,
+                const void* new_k, const void* new_v)
 {
-    static const char* fn = "pkv_paged_decode_attention";
     if (!pkv_dtype_bytes(kv_dtype) || !pkv_dtype_bytes(out_dtype))
         return pkv_fail(PKV_ERR_DTYPE, "%s: dtype kv=%d out=%d", fn, kv_dtype, out_dtype);
     if (num_seqs < 0 || num_seqs > 65535)
@@ -360,6 +366,10 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, co
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) ||
         !aligned(out, pkv_dtype_bytes(out_dtype)))
         return pkv_fail(PKV_ERR_ALIGN, "%s: caches need 16-byte, q 4-byte alignment", fn);
+    const bool append = new_k != nullptr;
+    if (append && (!new_v || !aligned(new_k, 16) || !aligned(new_v, 16)))
+        return pkv_fail(new_v ? PKV_ERR_ALIGN : PKV_ERR_NULL,
+                        "%s: new_k and new_v need 16-byte alignment", fn);
 
     DecodeParams p;
     p.out = out;
@@ -380,6 +390,8 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, co
     p.ws_ml = nullptr;
     p.ws_o = nullptr;
     p.done = nullptr;
+    p.new_k = nullptr;
+    p.new_v = nullptr;
     const int max_ctx = max_blocks_per_seq * block_size;
     if (partition_size == 0) {
         p.partition_tokens = max_ctx;
@@ -424,19 +436,61 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, co
         if (p.max_partitions > 1) {
             // completion counters for the in-kernel merge start at zero
             e = cudaMemsetAsync(p.done, 0, sizeof(unsigned) * (size_t)num_seqs * num_kv_heads, st);
-            if (e != cudaSuccess) return cuda_fail(e, "pkv_paged_decode_attention counter reset");
+            if (e != cudaSuccess) return cuda_fail(e, fn);
         }
+        // the tensor-core kernel writes the new tokens itself
+        p.new_k = new_k;
+        p.new_v = new_v;
         e = launch_decode_tensor_core(p, kv_dtype, &kmap, &vmap, grid, st);
-        if (e != cudaSuccess) return cuda_fail(e, "pkv_paged_decode_attention launch");
+        if (e != cudaSuccess) return cuda_fail(e, fn);
         return PKV_OK;
     }
+    if (append) {
+        e = launch_kv_append(const_cast<void*>(k_cache), const_cast<void*>(v_cache), new_k, new_v,
+                             block_tables, context_lens, num_seqs, max_blocks_per_seq, num_blocks,
+                             num_kv_heads, head_dim, block_size, pkv_dtype_bytes(kv_dtype),
+                             p.status, st);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+    }
     e = launch_decode_cuda_core(p, kv_dtype, st);
-    if (e != cudaSuccess) return cuda_fail(e, "pkv_paged_decode_attention launch");
+    if (e != cudaSuccess) return cuda_fail(e, fn);
     if (p.max_partitions > 1) {
         e = launch_lse_reduce(p, st);
-        if (e != cudaSuccess) return cuda_fail(e, "pkv_paged_decode_attention reduce launch");
+        if (e != cudaSuccess) return cuda_fail(e, fn);
     }
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               float scale, int block_size, int num_kv_heads, int num_seqs,
+                               int num_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
+                               int kv_dtype, int out_dtype, int partition_size, void* workspace,
+                               size_t workspace_bytes, void* stream)
+{
+    return decode_impl("pkv_paged_decode_attention", out, q, k_cache, v_cache, block_tables,
+                       context_lens, scale, block_size, num_kv_heads, num_seqs, num_heads, head_dim,
+                       max_blocks_per_seq, num_blocks, kv_dtype, out_dtype, partition_size,
+                       workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+int pkv_decode_step(void* out, const void* q, const void* new_k, const void* new_v,
+                    void* k_cache, void* v_cache, const int32_t* block_tables,
+                    const int32_t* context_lens, float scale, int block_size, int num_kv_heads,
+                    int num_seqs, int num_heads, int head_dim, int max_blocks_per_seq,
+                    int num_blocks, int kv_dtype, int out_dtype, int partition_size,
+                    void* workspace, size_t workspace_bytes, void* stream)
+{
+    static const char* fn = "pkv_decode_step";
+    if (num_seqs > 0 && (!new_k || !new_v)) return pkv_fail(PKV_ERR_NULL, "%s: NULL new_k/new_v", fn);
+    return decode_impl(fn, out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                       block_size, num_kv_heads, num_seqs, num_heads, head_dim, max_blocks_per_seq,
+                       num_blocks, kv_dtype, out_dtype, partition_size, workspace, workspace_bytes,
+                       stream, new_k, new_v);
 }
 
 }  // extern "C"

@@ -189,6 +189,31 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         __syncwarp();
     };
 
+    // ---- decode step with append: the warp that streams the stage holding
+    // position L-1 first writes this KV head's slice of the new token there
+    // (16 bytes per lane), then orders the write before its own TMA reads
+    if (p.new_k != nullptr && L > 0 && begin <= L - 1 && L - 1 < end &&
+        ((L - 1 - begin) / 16) % NW == warp) {
+        const int id = table[(L - 1) / B];
+        if (id < 0 || id >= p.num_blocks) {
+            if (lane == 0) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
+        } else {
+            constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte chunks per row
+            const int c = lane % CH;
+            const bool is_v = lane >= CH;
+            if (lane < 2 * CH) {
+                const size_t src = ((size_t)s * p.num_kv_heads + g) * D;
+                const size_t dst = (((size_t)id * p.num_kv_heads + g) * B + (L - 1) % B) * D;
+                const uint4 v = reinterpret_cast<const uint4*>(
+                    static_cast<const T*>(is_v ? p.new_v : p.new_k) + src)[c];
+                reinterpret_cast<uint4*>(
+                    const_cast<T*>(static_cast<const T*>(is_v ? p.v_cache : p.k_cache)) + dst)[c] = v;
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        __syncwarp();
+    }
+
     if (cnt > 0) load_window(0);
     for (int j = 0; j < NS && j < cnt; ++j) issue(j);
 

@@ -54,6 +54,43 @@ __global__ void kv_write_kernel(uint4* __restrict__ k_cache, uint4* __restrict__
 }
 
 // ---------------------------------------------------------------------------
+// kv_append: the decode step's new token of sequence s (new_k/new_v
+// [S][Hkv][D]) goes to position context_lens[s]-1, i.e. slot
+// table[s][(L-1)/B] * B + (L-1) % B -- the slot mapping of the aiplusplus
+// PagedAttention page (core idea 3-4) for the token just appended.  Used by
+// the decode step when it runs on the CUDA-core kernel; the tensor-core
+// kernel performs the same write itself.
+// ---------------------------------------------------------------------------
+__global__ void kv_append_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                 const uint4* __restrict__ new_k, const uint4* __restrict__ new_v,
+                                 const int32_t* __restrict__ block_tables,
+                                 const int32_t* __restrict__ context_lens, int max_blocks,
+                                 int num_blocks, int num_kv_heads, int vec_per_head,
+                                 int block_size, unsigned int* status)
+{
+    const int s = blockIdx.x;
+    const int i = blockIdx.y * blockDim.x + threadIdx.x;  // (head, 16-byte chunk)
+    if (i >= num_kv_heads * vec_per_head) return;
+    const int L = context_lens[s];
+    if (L <= 0) return;
+    if ((int64_t)L > (int64_t)max_blocks * block_size) {
+        if (i == 0) flag(status, PKV_STATUS_BAD_LEN);
+        return;
+    }
+    const int id = block_tables[(size_t)s * max_blocks + (L - 1) / block_size];
+    if (id < 0 || id >= num_blocks) {
+        if (i == 0) flag(status, PKV_STATUS_BAD_BLOCK);
+        return;
+    }
+    const int h = i / vec_per_head, c = i - h * vec_per_head;
+    const size_t dst =
+        (((size_t)id * num_kv_heads + h) * block_size + (L - 1) % block_size) * vec_per_head + c;
+    const size_t src = (size_t)s * num_kv_heads * vec_per_head + i;
+    k_cache[dst] = new_k[src];
+    v_cache[dst] = new_v[src];
+}
+
+// ---------------------------------------------------------------------------
 // kv_copy_blocks: physical block src -> dst for K and V; a block of all heads
 // is one contiguous run of block_bytes in this layout.
 // (auturnal guide, section 3: copy-on-write of a shared block that is not
@@ -319,6 +356,23 @@ cudaError_t launch_kv_write(void* k_cache, void* v_cache, const void* key, const
         static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
         static_cast<const uint4*>(key), static_cast<const uint4*>(value), slot_mapping,
         num_blocks, num_kv_heads, vec_per_head, block_size, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* new_k, const void* new_v,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             int num_seqs, int max_blocks, int num_blocks, int num_kv_heads,
+                             int head_dim, int block_size, int elem_bytes, unsigned int* status,
+                             cudaStream_t stream)
+{
+    const int vec_per_head = head_dim * elem_bytes / 16;
+    const int per_seq = num_kv_heads * vec_per_head;
+    const int threads = per_seq < 256 ? ((per_seq + 31) / 32) * 32 : 256;
+    dim3 grid(num_seqs, (per_seq + threads - 1) / threads);
+    kv_append_kernel<<<grid, threads, 0, stream>>>(
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+        static_cast<const uint4*>(new_k), static_cast<const uint4*>(new_v), block_tables,
+        context_lens, max_blocks, num_blocks, num_kv_heads, vec_per_head, block_size, status);
     return cudaGetLastError();
 }
 

@@ -25,6 +25,11 @@ struct DecodeParams {
     float* ws_o;                 // [S][Hq][max_partitions][D] unnormalised output
     unsigned int* done;          // [S][Hkv] partitions finished (tensor-core split mode)
     unsigned int* status;        // device status word (PKV_STATUS_* bits)
+    // Decode step with append (tensor-core kernel only; NULL otherwise): the
+    // K/V of each sequence's new token, [S][Hkv][D] in the cache dtype, is
+    // written at position context_lens[s]-1 before it is attended.
+    const void* new_k;
+    const void* new_v;
 };
 
 // Everything one prefill launch needs (passed by value).
@@ -60,6 +65,14 @@ cudaError_t launch_kv_write(void* k_cache, void* v_cache, const void* key, const
                             const int64_t* slot_mapping, int num_tokens, int num_blocks,
                             int num_kv_heads, int head_dim, int block_size, int elem_bytes,
                             unsigned int* status, cudaStream_t stream);
+
+// Appends one token per sequence: new_k/new_v [S][Hkv][D] go to position
+// context_lens[s]-1 through the block table (one CTA per sequence and KV head).
+cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* new_k, const void* new_v,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             int num_seqs, int max_blocks, int num_blocks, int num_kv_heads,
+                             int head_dim, int block_size, int elem_bytes, unsigned int* status,
+                             cudaStream_t stream);
 
 cudaError_t launch_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs,
                                   int num_pairs, int num_blocks, size_t block_bytes,

@@ -90,6 +90,24 @@ def test_prefill_rejects_bad_arguments_on_host():
     assert call(S=0) == 0 and call(maxq=0) == 0
 
 
+def test_decode_step_rejects_bad_arguments_on_host():
+    L = pkv.lib()
+    P = ctypes.c_void_p
+
+    def call(**kw):
+        a = dict(nk=256, nv=256, D=128, S=2, P=0)
+        a.update(kw)
+        return L.pkv_decode_step(P(256), P(256), P(a["nk"]), P(a["nv"]), P(256), P(256), P(256),
+                                 P(256), 0.1, 16, 4, a["S"], 8, a["D"], 4, 10, 2, 0, a["P"],
+                                 P(0), 0, P(0))
+    assert call(nk=0) == -1        # new token K missing
+    assert call(nv=0) == -1
+    assert call(nk=264) == -10     # new_k not 16-byte aligned
+    assert call(D=96) == -2        # the attention's own checks still apply
+    assert call(P=32) == -8        # split mode without a workspace
+    assert call(S=0, nk=0, nv=0) == 0
+
+
 def test_decode_with_no_sequences_is_a_no_op():
     assert _attn(pkv.lib(), S=0, out=0, q=0) == 0
 

@@ -420,6 +420,29 @@ def test_kv_write_skips_negative_slots_and_rejects_out_of_range():
         oracle.kv_write(kc, vc, key[:1], key[:1], torch.tensor([NB * B]), B)
 
 
+def test_decode_step_appends_at_position_then_attends():
+    # The decode step stores each new token at position L-1 through the table
+    # and attends over the sequence with it: against plain softmax attention
+    # over the gathered sequence with the new row put in by hand.
+    from workloads import Workload
+    w = Workload(0, "step", "f32", 4, 2, 64, 16, 4, "fixed", writes_new_token=True)
+    case = make_decode_case(w, seed=12, lengths=[1, 16, 17, 40])
+    k, v = case.k_cache.clone(), case.v_cache.clone()
+    out = oracle.decode_step(case.q, case.new_key, case.new_value, k, v, case.block_tables,
+                             case.context_lens, w.scale, 16, 2)
+    for s, L in enumerate(case.lengths):
+        K = oracle.gather_sequence(k, case.block_tables[s].tolist(), int(L))
+        V = oracle.gather_sequence(v, case.block_tables[s].tolist(), int(L))
+        assert np.array_equal(K[L - 1], case.new_key[s].double().numpy())
+        assert np.array_equal(V[L - 1], case.new_value[s].double().numpy())
+        for hq in range(4):
+            g = hq // 2
+            sc = K[:, g, :] @ case.q[s, hq].double().numpy() * w.scale
+            p_ = np.exp(sc - sc.max())
+            ref = (p_[:, None] * V[:, g, :]).sum(0) / p_.sum()
+            assert np.abs(out[s, hq] - ref).max() < 1e-12
+
+
 def test_slot_for_position_agrees_with_block_manager():
     bm = BlockManager(50, 16, free_order=np.random.default_rng(1).permutation(50))
     bm.add(0, 0)

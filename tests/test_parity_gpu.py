@@ -354,6 +354,76 @@ def test_prefix_cached_sequence_attends_like_a_fresh_one():
 
 
 # --------------------------------------------------------------------------
+# decode step: append the new token, then attend (one call)
+# --------------------------------------------------------------------------
+
+STEP_CASES = [  # dtype, Hq, Hkv, D, B, partition
+    ("bf16", 32, 32, 128, 16, 0), ("bf16", 32, 8, 128, 16, 64), ("f16", 16, 2, 64, 8, 0),
+    ("bf16", 8, 1, 128, 32, 32), ("f16", 8, 8, 128, 16, 512),
+    ("f32", 4, 4, 64, 16, 0), ("bf16", 32, 2, 128, 16, 0),  # CUDA-core kernel paths
+]
+
+
+@pytest.mark.parametrize("dt,Hq,Hkv,D,B,P", STEP_CASES)
+def test_decode_step_matches_oracle(dt, Hq, Hkv, D, B, P):
+    # the new position's slot holds NaN until the step writes it; lengths put
+    # the new token first in a block, last in a block, mid-block, alone
+    w = Workload(0, "step", dt, Hq, Hkv, D, B, 6, "fixed", writes_new_token=True)
+    lengths = [1, B, B + 1, 3 * B - 5, 700, 2049]
+    case = make_decode_case(w, seed=Hq + B + P, lengths=lengths)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    out = torch.full(case.q.shape, float("nan"), dtype=torch.float32, device=DEV)
+    ws = None
+    if P:
+        n = pkv.decode_workspace_bytes(6, Hq, D, case.block_tables.shape[1] * B, P)
+        ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    pkv.decode_step(out, case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV), kc, vc,
+                    case.block_tables.to(DEV), case.context_lens.to(DEV), w.scale, B, Hkv,
+                    partition_size=P, workspace=ws)
+    torch.cuda.synchronize()
+    k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+    ref = oracle.decode_step(case.q, case.new_key, case.new_value, k_ref, v_ref,
+                             case.block_tables, case.context_lens, w.scale, B, Hkv)
+    assert pkv.device_status() == 0
+    # the cache is bit-exact (NaN slots elsewhere compared as bits)
+    assert torch.equal(bits(kc), bits(k_ref)) and torch.equal(bits(vc), bits(v_ref))
+    assert max_err(out, ref) <= tol(w.torch_dtype)
+
+
+def test_decode_step_equals_write_then_attend_and_flags_bad_block():
+    w = Workload(0, "step2", "bf16", 16, 4, 128, 16, 3, "fixed", writes_new_token=True)
+    case = make_decode_case(w, seed=5, lengths=[33, 64, 200])
+    bt = case.block_tables.clone()
+    kc1, vc1 = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    kc2, vc2 = kc1.clone(), vc1.clone()
+    out1 = torch.empty(case.q.shape, dtype=torch.float32, device=DEV)
+    out2 = torch.empty_like(out1)
+    q, nk, nv = case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV)
+    pkv.decode_step(out1, q, nk, nv, kc1, vc1, bt.to(DEV), case.context_lens.to(DEV),
+                    w.scale, 16, 4)
+    slots = torch.tensor([oracle.slot_for_position(bt[s].tolist(), int(L) - 1, 16)
+                          for s, L in enumerate(case.lengths)], dtype=torch.int64)
+    pkv.kv_write(kc2, vc2, nk, nv, slots.to(DEV))
+    pkv.paged_decode_attention(out2, q, kc2, vc2, bt.to(DEV), case.context_lens.to(DEV),
+                               w.scale, 16, 4)
+    torch.cuda.synchronize()
+    assert torch.equal(bits(kc1), bits(kc2)) and torch.equal(bits(vc1), bits(vc2))
+    assert torch.equal(out1, out2)  # same kernel, same inputs: same bits
+    assert pkv.device_status() == 0
+    # a table entry out of range at the new position: no write, flagged
+    bt[1, (64 - 1) // 16] = case.num_blocks + 3
+    kc3, vc3 = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    pkv.decode_step(out1, q, nk, nv, kc3, vc3, bt.to(DEV), case.context_lens.to(DEV),
+                    w.scale, 16, 4)
+    torch.cuda.synchronize()
+    assert pkv.device_status() & 1
+    ref0 = oracle.decode_step(case.q[:1], case.new_key[:1], case.new_value[:1],
+                              case.k_cache.clone(), case.v_cache.clone(), bt[:1],
+                              case.context_lens[:1], w.scale, 16, 4)
+    assert max_err(out1[:1], ref0) <= TOL16  # the healthy sequence is unaffected
+
+
+# --------------------------------------------------------------------------
 # paged prefill (causal multi-token queries)
 # --------------------------------------------------------------------------
 
