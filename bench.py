@@ -43,8 +43,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
 # valid only while the kernel source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "ac8d7038dc08777c",
-           "bytes_per_launch": {"2": 1107315200, "3": 806457344, "4": 1091047424}}
+TRAFFIC = {"source_sha": "6ca73094d0266bd0",
+           "bytes_per_launch": {"2": 1109220352, "3": 806757888, "4": 1091534080}}
 
 
 def launch_partition(w, max_blocks: int) -> int:
