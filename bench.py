@@ -248,10 +248,8 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     assert pkv.device_status() == 0
 
-    # ---- device-timed region: K steps, events per step on the launch stream
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # ---- device-timed region: K steps back to back, one event on each side
+    # (the per-step events of the roofline pass below would add gaps)
     clocks = ClockSampler(local_rank) if rank == 0 else None
     time.sleep(0.3 if clocks else 0)
     if world > 1:
@@ -262,17 +260,28 @@ def run_gpu(args, rank, world, local_rank):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(args.steps):
-        starts[i].record(stream)
-        step(mids[i])
-        ends[i].record(stream)
+        step()
     t1.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
     clk = clocks.stop(wall0, wall1) if clocks else None
     total_ms = t0.elapsed_time(t1)
-    attn_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
     total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
+    assert pkv.device_status() == 0
+
+    # ---- roofline pass: the same K steps with events around each decode
+    # call, for that kernel's own average duration
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        step(mids[i])
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    attn_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
     assert pkv.device_status() == 0
 
     # ---- end to end through the public API with pinned host buffers
