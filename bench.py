@@ -354,11 +354,37 @@ def run_gpu(args, rank, world, local_rank):
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
     }
+    if st.slots is not None and rank == 0:
+        line["host_allocator"] = host_allocator_timing(st, pkv)
     if st.unique_blocks is not None:
         ub = st.unique_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2 * 2
         line["config"]["unique_kv_bytes"] = ub
         line["pct_hbm_peak_unique_bytes"] = round(100 * ub / (attn_avg * 1e-3) / 1e9 / peak, 2)
     return line, st
+
+
+def host_allocator_timing(st, pkv, steps=256):
+    """Host side of a decode step (a1/a2): pkv_step_append for every sequence
+    (slot mapping, new blocks, copy-on-write decisions) plus the read-back of
+    the dense block tables the device calls take.  Timed over `steps`
+    consecutive steps from the workload's lengths, in a pool with room for
+    them; mean microseconds per step."""
+    w = st.w
+    lens = st.lens.tolist()
+    S, B = len(lens), w.block_size
+    need = sum((n + steps + B - 1) // B for n in lens)
+    a = pkv.BlockAllocator(need + S, B)
+    for i, n in enumerate(lens):
+        a.add(i, max(0, n - 1))
+    seqs = list(range(S))
+    maxb = max((n + steps + B - 1) // B for n in lens)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        a.step_append(seqs)
+        a.dense_tables(seqs, maxb)
+    us = (time.perf_counter() - t0) / steps * 1e6
+    return {"us_per_step": round(us, 2), "steps": steps, "sequences": S,
+            "what": "pkv_step_append for every sequence + dense block-table read-back"}
 
 
 def cpu_baseline(st, budget_s=8.0):
