@@ -284,6 +284,19 @@ int pkv_kv_swap_blocks(void* dst_k_cache, void* dst_v_cache, const void* src_k_c
                        int block_size, int dtype, void* stream);
 
 /*
+ * selftest_bounded_wait -- exercises the bounded waits the kernels use.
+ * Launches num_ctas CTAs (1..65535); each waits on an mbarrier that nothing
+ * arrives on.  The first wait to reach its bound (about 2^31 cycles, about a
+ * second) sets PKV_STATUS_TIMEOUT; the other CTAs see the bit and give up at
+ * once.  Each CTA then completes its barrier itself and increments *drained
+ * (a device uint32 the caller zeroes) if the drain wait -- the one a kernel
+ * uses for its own copies after a timeout -- returns in bound.  Expect the
+ * TIMEOUT bit set (reset it with pkv_device_status) and *drained == num_ctas;
+ * the context stays usable.  Nothing faults or stays in flight.
+ */
+int pkv_selftest_bounded_wait(int num_ctas, unsigned int* drained, void* stream);
+
+/*
  * Kernel selection for pkv_paged_decode_attention (process-wide):
  * PKV_KERNEL_AUTO (default) picks the tensor-core kernel where supported;
  * PKV_KERNEL_CUDA_CORE forces the CUDA-core kernel for every shape (used to

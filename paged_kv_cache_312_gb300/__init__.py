@@ -8,14 +8,14 @@ from ._binding import (  # noqa: F401
     STATUS_BITS, BlockAllocator, NOALLOC_SCRATCH_BYTES, OutOfBlocks, PkvError, decode_step,
     decode_workspace_bytes, device_status,
     kv_copy_blocks, kv_swap_blocks, kv_write, lib, paged_decode_attention,
-    paged_decode_attention_noalloc, paged_prefill_attention, set_decode_kernel,
-    set_prefill_kernel,
+    paged_decode_attention_noalloc, paged_prefill_attention, selftest_bounded_wait,
+    set_decode_kernel, set_prefill_kernel,
 )
 
 __all__ = [
     "BlockAllocator", "OutOfBlocks", "PkvError", "decode_step", "decode_workspace_bytes",
     "device_status",
     "kv_copy_blocks", "kv_swap_blocks", "kv_write", "lib", "paged_decode_attention",
-    "paged_decode_attention_noalloc", "paged_prefill_attention", "set_decode_kernel",
-    "set_prefill_kernel",
+    "paged_decode_attention_noalloc", "paged_prefill_attention", "selftest_bounded_wait",
+    "set_decode_kernel", "set_prefill_kernel",
 ]

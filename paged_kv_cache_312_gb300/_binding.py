@@ -21,7 +21,7 @@ DTYPE_CODE = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PK
 KERNEL_AUTO, KERNEL_CUDA_CORE = 0, 1
 PREFILL_TCGEN05, PREFILL_WARP_MMA = 0, 1
 STATUS_BITS = {1: "bad block id", 2: "bad context length", 4: "bad slot", 8: "bad copy pair",
-               16: "tile load timeout"}
+               16: "wait timeout"}
 
 # name -> (restype, argtypes)
 _P, _I, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
@@ -47,6 +47,7 @@ _SIGS = {
     "pkv_prefix_cache_stats": (_I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                                     ctypes.POINTER(_I64)]),
     "pkv_set_decode_kernel": (_I, [_I]),
+    "pkv_selftest_bounded_wait": (_I, [_I, _P, _P]),
     "pkv_set_prefill_kernel": (_I, [_I]),
     "pkv_alloc_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_alloc_destroy": (_I, [_P]),
@@ -294,6 +295,13 @@ def device_status(reset=True, stream=None):
     if rc not in (0, -6):
         _check(rc, "pkv_device_status")
     return int(bits.value)
+
+
+def selftest_bounded_wait(num_ctas, drained, stream=None):
+    """Launch the bounded-wait self-test (see include/pkv.h); `drained` is a
+    zeroed int32/uint32 CUDA tensor of one element."""
+    _check(lib().pkv_selftest_bounded_wait(int(num_ctas), _dev(drained, "drained"),
+                                           _stream(stream)), "pkv_selftest_bounded_wait")
 
 
 def set_decode_kernel(which):

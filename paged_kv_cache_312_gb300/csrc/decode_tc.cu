@@ -246,11 +246,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         const int slot = j % NS;
         const uint32_t bar = smem_u32(&bars[warp * NS + slot]);
         if (!mbar_wait_bounded(bar, (j / NS) & 1, p.status)) {
-            // The copies of this stage never landed: flag, stop, and give the
-            // ones still outstanding a bounded wait before leaving.
+            // The copies of this stage never landed: flag, stop, and give this
+            // stage and the ones still outstanding a bounded wait (one that
+            // does not stop at the TIMEOUT bit just set) before leaving.
             if (lane == 0) atomicOr(p.status, PKV_STATUS_TIMEOUT);
-            for (int jj = j + 1; jj < j + NS && jj < cnt; ++jj)
-                mbar_wait_bounded(smem_u32(&bars[warp * NS + jj % NS]), (jj / NS) & 1, p.status);
+            for (int jj = j; jj < j + NS && jj < cnt; ++jj)
+                mbar_drain_wait(smem_u32(&bars[warp * NS + jj % NS]), (jj / NS) & 1);
             break;
         }
         const int id0 = sid[(warp * NS + slot) * 2 + 0];

@@ -125,7 +125,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
     __syncthreads();
 
     // Thread 0: start the loads of key tile kt into stage kt % kStages.
+    int issued = 0, landed = 0;  // thread 0: tiles whose copies it started / saw land
     auto issue = [&](int kt) {
+        issued = kt + 1;
         const int st = kt % kStages;
         const uint32_t bar = smem_u32(&bars[st]);
         const uint32_t kdst = smem_u32(smem + st * Pg::STAGE_BYTES);
@@ -210,10 +212,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
 
     for (int kt = 0; kt < nkt; ++kt) {
         const int st = kt % kStages;
-        if (!mbar_wait_bounded(smem_u32(&bars[st]), (kt / kStages) & 1, p.status)) {
+        if (!aborted && !mbar_wait_bounded(smem_u32(&bars[st]), (kt / kStages) & 1, p.status)) {
             if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_TIMEOUT);
             aborted = true;
         }
+        if (!aborted) landed = kt + 1;
         const int key0 = kt * kKT;
         if (!aborted && key0 <= warp_last_pos) {
             const uint32_t kbase = smem_u32(smem + st * Pg::STAGE_BYTES);
@@ -330,7 +333,14 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kma
         __syncthreads();  // every warp is done with stage st
         if (threadIdx.x == 0 && !aborted && kt + kStages < nkt) issue(kt + kStages);
     }
-    if (aborted) return;
+    if (__syncthreads_or(aborted)) {
+        // a wait gave up: the copies thread 0 started and did not see land get
+        // a bounded wait before the CTA's shared memory goes away
+        if (threadIdx.x == 0)
+            for (int kt = landed; kt < issued; ++kt)
+                mbar_drain_wait(smem_u32(&bars[kt % kStages]), (kt / kStages) & 1);
+        return;
+    }
 
     // ---- normalise and store this thread's two rows
 #pragma unroll

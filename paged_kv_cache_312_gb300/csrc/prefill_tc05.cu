@@ -192,15 +192,6 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk)
     return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-// Plain bounded wait (no early exit on the status bit): drains this CTA's
-// own asynchronous work after one of its waits has given up.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
-{
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > (1ll << 31)) return;
-}
-
 // tcgen05.mma with the A operand in tensor memory (K-major, two 16-bit
 // elements per 32-bit column, the lower key in the low half).
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
@@ -487,7 +478,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         // the ring's last fills must have landed before the CTA exits
         if (lane == 0)
             for (int f = max(0, t - SLOTS); f < t; ++f)
-                drain_wait(smem_u32(&full[slot_of(f)]), phase_of(f));
+                mbar_drain_wait(smem_u32(&full[slot_of(f)]), phase_of(f));
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issue
@@ -624,7 +615,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         // every MMA this warp issued has finished before the CTA exits
         __syncwarp();
         commit(drain);
-        if (lane == 0) drain_wait(smem_u32(drain), 0);
+        if (lane == 0) mbar_drain_wait(smem_u32(drain), 0);
         __syncwarp();
     } else {
         // --------------------------------------------------------- softmax

@@ -61,6 +61,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return true;
 }
 
+// Bounded wait (~2^31 cycles) that ignores the status word: after a wait has
+// given up (and set TIMEOUT), a CTA uses it to let its own copies still in
+// flight land before it exits.  Returns false if the bound ran out.
+__device__ __forceinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity)
+{
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > (1ll << 31)) return false;
+    return true;
+}
+
 __device__ __forceinline__ void fence_proxy_async()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -108,6 +108,14 @@ def test_decode_step_rejects_bad_arguments_on_host():
     assert call(S=0, nk=0, nv=0) == 0
 
 
+def test_selftest_rejects_bad_arguments_on_host():
+    L = pkv.lib()
+    P = ctypes.c_void_p
+    assert L.pkv_selftest_bounded_wait(0, P(256), P(0)) == -2
+    assert L.pkv_selftest_bounded_wait(70000, P(256), P(0)) == -2
+    assert L.pkv_selftest_bounded_wait(4, P(0), P(0)) == -1
+
+
 def test_decode_with_no_sequences_is_a_no_op():
     assert _attn(pkv.lib(), S=0, out=0, q=0) == 0
 

@@ -354,6 +354,34 @@ def test_prefix_cached_sequence_attends_like_a_fresh_one():
 
 
 # --------------------------------------------------------------------------
+# bounded waits: a wait that nothing completes gives up, flags, and the
+# context stays usable (no fault, nothing left in flight)
+# --------------------------------------------------------------------------
+
+def test_bounded_waits_give_up_flag_and_leave_the_context_usable():
+    import time
+    n = 600  # more CTAs than one wait: they must stop on the first one's flag
+    drained = torch.zeros(1, dtype=torch.int32, device=DEV)
+    t0 = time.time()
+    pkv.selftest_bounded_wait(n, drained)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    st = pkv.device_status(reset=True)
+    assert st & 16  # PKV_STATUS_TIMEOUT
+    assert int(drained.item()) == n
+    assert elapsed < 10.0, elapsed
+    # the same context still computes correct attention
+    w = Workload(0, "after", "bf16", 8, 2, 128, 16, 3, "fixed")
+    case = make_decode_case(w, seed=3, lengths=[5, 100, 300])
+    out = gpu_decode(case.q, case.k_cache.to(DEV), case.v_cache.to(DEV), case.block_tables,
+                     case.context_lens, w.scale, 16, 2)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, 16, 2)
+    assert pkv.device_status() == 0
+    assert max_err(out, ref) <= TOL16
+
+
+# --------------------------------------------------------------------------
 # decode step: append the new token, then attend (one call)
 # --------------------------------------------------------------------------
 
