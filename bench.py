@@ -43,8 +43,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
 # valid only while the kernel source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "6ca73094d0266bd0",
-           "bytes_per_launch": {"2": 1109220352, "3": 806757888, "4": 1091534080}}
+TRAFFIC = {"source_sha": "f17e1031c51a1eee",
+           "bytes_per_launch": {"2": 1109504000, "3": 806807296, "4": 1091304192}}
 
 
 def launch_partition(w, max_blocks: int) -> int:
@@ -214,17 +214,23 @@ def run_gpu(args, rank, world, local_rank):
     kc, vc = st.k_cache.to(dev), st.v_cache.to(dev)
     if st.setup_slots is not None:  # beam history
         pkv.kv_write(kc, vc, st.setup_keys.to(dev), st.setup_vals.to(dev), st.setup_slots.to(dev))
-    q, bt, cl = st.q.to(dev), st.tables.to(dev), st.lens.to(dev)
+    # the step's inputs live in one pinned host buffer and one device buffer
+    # (views per tensor), so a step's host->device traffic is a single copy
+    has_write = st.slots is not None
+    inputs = [st.q, st.tables, st.lens, st.pairs]
+    if has_write:
+        inputs += [st.new_key, st.new_value]
+    h_pack, views = pack_inputs(inputs, dev)
+    q, bt, cl, pairs = views[:4]
+    if has_write:
+        nk, nv = views[4:6]
     S, Hq, D = q.shape
     out = torch.empty((S, Hq, D), dtype=torch.float32, device=dev)
     ws = None
     if st.P:
         ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, bt.shape[1] * w.block_size, st.P),
                          dtype=torch.uint8, device=dev)
-    has_write = st.slots is not None
-    if has_write:
-        nk, nv = st.new_key.to(dev), st.new_value.to(dev)
-    pairs = st.pairs.to(dev)
+    d_pack = views[-1]
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
@@ -284,39 +290,27 @@ def run_gpu(args, rank, world, local_rank):
     attn_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
     assert pkv.device_status() == 0
 
-    # ---- end to end through the public API with pinned host buffers
+    # ---- end to end through the public API with pinned host buffers: every
+    # step copies its inputs to the device (one packed copy), runs the calls,
+    # reads the output back and synchronises
     e2e = None
     if not args.no_e2e:
-        h_q = st.q.pin_memory()
-        h_bt, h_cl = st.tables.pin_memory(), st.lens.pin_memory()
         h_out = torch.empty((S, Hq, D), dtype=torch.float32).pin_memory()
-        h_in = [h_q, h_bt, h_cl]
-        if has_write:
-            h_nk, h_nv = st.new_key.pin_memory(), st.new_value.pin_memory()
-            h_in += [h_nk, h_nv]
-        h_pairs = st.pairs.pin_memory()
-        h_in.append(h_pairs)
-        h2d = sum(t.numel() * t.element_size() for t in h_in)
+        h2d = h_pack.numel()
         d2h = h_out.numel() * h_out.element_size()
         k = max(1, min(args.steps, 50))
         torch.cuda.synchronize(dev)
         w0 = time.perf_counter()
         for _ in range(k):
-            q.copy_(h_q, non_blocking=True)
-            bt.copy_(h_bt, non_blocking=True)
-            cl.copy_(h_cl, non_blocking=True)
-            if has_write:
-                nk.copy_(h_nk, non_blocking=True)
-                nv.copy_(h_nv, non_blocking=True)
-            if pairs.shape[0]:
-                pairs.copy_(h_pairs, non_blocking=True)
+            d_pack.copy_(h_pack, non_blocking=True)
             step()
             h_out.copy_(out, non_blocking=True)
             stream.synchronize()
         e2e_s = (time.perf_counter() - w0) / k
         e2e = {"value": round(st.kv_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(e2e_s * 1e3, 4), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": k}
+               "d2h_bytes_per_step": int(d2h), "steps": k,
+               "inputs": "q, block tables, lengths, CoW pairs, new K/V in one pinned buffer"}
 
     peak, peak_src = measured_peaks()
     attn_avg = statistics.mean(attn_ms)
@@ -361,6 +355,27 @@ def run_gpu(args, rank, world, local_rank):
         line["config"]["unique_kv_bytes"] = ub
         line["pct_hbm_peak_unique_bytes"] = round(100 * ub / (attn_avg * 1e-3) / 1e9 / peak, 2)
     return line, st
+
+
+def pack_inputs(tensors, dev):
+    """One pinned host buffer holding every tensor (256-byte aligned), and the
+    device copy of it: returns (host buffer, [device view per tensor...,
+    device buffer])."""
+    offs, total = [], 0
+    for t in tensors:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host = torch.zeros(max(total, 256), dtype=torch.uint8).pin_memory()
+    for t, o in zip(tensors, offs):
+        n = t.numel() * t.element_size()
+        if n:
+            host[o:o + n].copy_(t.contiguous().reshape(-1).view(torch.uint8))
+    buf = host.to(dev)
+    views = []
+    for t, o in zip(tensors, offs):
+        n = t.numel() * t.element_size()
+        views.append(buf[o:o + n].view(t.dtype).view(t.shape))
+    return host, views + [buf]
 
 
 def host_allocator_timing(st, pkv, steps=256):
