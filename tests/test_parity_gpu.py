@@ -354,6 +354,40 @@ def test_prefix_cached_sequence_attends_like_a_fresh_one():
 
 
 # --------------------------------------------------------------------------
+# maximum sizes: the most sequences a call takes (65535), tiny contexts
+# --------------------------------------------------------------------------
+
+def test_decode_and_decode_step_at_the_sequence_limit():
+    S, B = 65535, 8
+    w = Workload(0, "max-seqs", "bf16", 2, 1, 64, B, S, "fixed", writes_new_token=True)
+    rng = np.random.default_rng(33)
+    lengths = rng.integers(1, 3 * B + 1, size=S)
+    case = make_decode_case(w, seed=34, lengths=lengths.tolist())
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    out = torch.empty(case.q.shape, dtype=torch.float32, device=DEV)
+    pkv.decode_step(out, case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV), kc, vc,
+                    case.block_tables.to(DEV), case.context_lens.to(DEV), w.scale, B, 1)
+    torch.cuda.synchronize()
+    k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+    ref = oracle.decode_step(case.q, case.new_key, case.new_value, k_ref, v_ref,
+                             case.block_tables, case.context_lens, w.scale, B, 1,
+                             nthreads=oracle.default_threads())
+    assert pkv.device_status() == 0
+    assert torch.equal(bits(kc), bits(k_ref)) and torch.equal(bits(vc), bits(v_ref))
+    assert max_err(out, ref) <= TOL16
+    # plain attention over the updated cache, split into one-block partitions
+    n = pkv.decode_workspace_bytes(S, 2, 64, case.block_tables.shape[1] * B, B)
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    out2 = torch.empty_like(out)
+    pkv.paged_decode_attention(out2, case.q.to(DEV), kc, vc, case.block_tables.to(DEV),
+                               case.context_lens.to(DEV), w.scale, B, 1, partition_size=B,
+                               workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    assert max_err(out2, ref) <= TOL16
+
+
+# --------------------------------------------------------------------------
 # bounded waits: a wait that nothing completes gives up, flags, and the
 # context stays usable (no fault, nothing left in flight)
 # --------------------------------------------------------------------------
@@ -496,6 +530,29 @@ def test_prefill_small(dt, Hq, Hkv, D, B, kernel):
                       kernel=kernel)
     ref = oracle.paged_prefill_attention(q, case.k_cache, case.v_cache, case.block_tables,
                                          case.context_lens, qs, w.scale, B, Hkv)
+    assert pkv.device_status() == 0
+    assert max_err(out, ref) <= TOL16
+
+
+def test_prefill_many_items_per_persistent_cta():
+    # 64 sequences x 32 heads of short prompts: about 14 work items per CTA of
+    # the persistent kernel, so every query tile crosses many item boundaries;
+    # items with an empty second tile, one-row prompts and no-query sequences
+    # are mixed in
+    rng = np.random.default_rng(17)
+    S = 64
+    lengths = rng.integers(1, 400, size=S)
+    qn = np.minimum(lengths, rng.choice([0, 1, 7, 128, 129, 255, 256, 300], size=S))
+    w = Workload(0, "prefill-many", "bf16", 32, 8, 128, 8, S, "fixed")
+    case = make_decode_case(w, seed=18, lengths=lengths.tolist())
+    qs = torch.tensor([0] + list(np.cumsum(qn)), dtype=torch.int32)
+    q = torch.randn(int(qs[-1]), 32, 128, generator=torch.Generator().manual_seed(9)).to(
+        torch.bfloat16)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    out = gpu_prefill(q, kc, vc, case.block_tables, case.context_lens, qs, w.scale, 8, 8)
+    ref = oracle.paged_prefill_attention(q, case.k_cache, case.v_cache, case.block_tables,
+                                         case.context_lens, qs, w.scale, 8, 8,
+                                         nthreads=oracle.default_threads())
     assert pkv.device_status() == 0
     assert max_err(out, ref) <= TOL16
 
