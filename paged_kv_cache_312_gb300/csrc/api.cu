@@ -393,6 +393,7 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
     p.new_k = nullptr;
     p.new_v = nullptr;
     const int max_ctx = max_blocks_per_seq * block_size;
+    p.cta_parts = 1;
     if (partition_size == 0) {
         p.partition_tokens = max_ctx;
         p.max_partitions = 1;
@@ -428,9 +429,15 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
         int rc = tensor_map(k_cache, rows, head_dim, block_size, kv_dtype, &kmap);
         if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap);
         if (rc != PKV_OK) return rc;
-        // grid: every (sequence, KV head, partition) slot, partitions of one
-        // (sequence, KV head) adjacent; slots past a sequence's end exit at once
-        const long long grid = (long long)num_seqs * num_kv_heads * p.max_partitions;
+        // grid: every (sequence, KV head, partition group) slot, the groups of
+        // one (sequence, KV head) adjacent; slots past a sequence's end exit at
+        // once.  Short partitions of long contexts go one per warp, four to a
+        // CTA (with few partitions per sequence, a CTA would leave warps idle).
+        if (p.partition_tokens <= kWarpPartitionMaxTokens &&
+            p.max_partitions >= kWarpPartitionMinCount)
+            p.cta_parts = kDecodeTcWarps;
+        const long long groups = (p.max_partitions + p.cta_parts - 1) / p.cta_parts;
+        const long long grid = (long long)num_seqs * num_kv_heads * groups;
         if (grid >= (1ll << 31))
             return pkv_fail(PKV_ERR_SHAPE, "%s: more than 2^31 work items", fn);
         if (p.max_partitions > 1) {

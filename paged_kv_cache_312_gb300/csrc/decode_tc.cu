@@ -7,16 +7,19 @@
 // with k_i, v_i found through the block table.
 //
 // How (GB300 design):
-//  * One CTA per (sequence, KV head, partition of <= P tokens); the slots of
-//    one (sequence, KV head) are adjacent in the grid and slots past a
-//    sequence's end exit at once.  All G <= 8 query heads of the KV group
+//  * One CTA per (sequence, KV head, partition of <= P tokens), or per four
+//    consecutive partitions when they are short (<= 512 tokens, one per
+//    warp, so that a CTA's start-up and end are spread over more bytes); the
+//    slots of one (sequence, KV head) are adjacent in the grid and slots past
+//    a sequence's end exit at once.  All G <= 8 query heads of the KV group
 //    ride along, so every K/V tile is read from HBM once per group (auturnal
 //    guide section 1: GQA/MQA shrink the KV head count).
 //  * A stage is 16 tokens of K and V.  A 2-D TMA tensor map views a cache as
 //    [NB*Hkv*B rows][D cols]; one cp.async.bulk.tensor per 64-column half
 //    (and per block for B = 8) lands a stage in shared memory with the
 //    128-byte swizzle and completes on an mbarrier.  Each of the 4 warps
-//    streams every 4th stage through its own ring of NS stages; its lane 0
+//    streams every 4th stage of its CTA's partition (or every stage of its
+//    own partition) through its own ring of NS stages; its lane 0
 //    issues loads NS stages ahead.  Block ids are fetched 32 stages at a time
 //    (one per lane) and broadcast by shuffle.  Three CTAs share an SM, so one
 //    CTA's start-up latency hides behind the others' streaming.
@@ -24,11 +27,12 @@
 //    on N (8) and head_dim on K; movmatrix turns the score fragment into the
 //    P^T operand of P V, which accumulates O^T in fp32.  P is split into a
 //    16-bit high part and a 16-bit remainder (~16 significant bits).
-//  * Online softmax in base 2 (fp32); the warps merge through shared memory
-//    (reusing the rings) at the end.  An unsplit item writes the output; a
-//    partition writes (max, sum, unnormalised output) to the workspace and
-//    bumps its (sequence, KV head) counter, and the CTA that finishes the
-//    last partition merges them all by log-sum-exp.
+//  * Online softmax in base 2 (fp32); the warps of a partition merge through
+//    shared memory (reusing the rings) at the end.  An unsplit item writes
+//    the output; a partition writes (max, sum, unnormalised output) to the
+//    workspace, the CTA bumps its (sequence, KV head) counter by its number
+//    of partitions, and the CTA that completes the count merges all
+//    partitions by log-sum-exp.
 //  * Masked tokens (past context_len, or in a block whose id is out of range)
 //    get score -inf and a zeroed V fragment, so NaN or stale data in unused
 //    slots never reaches the output.
@@ -83,9 +87,11 @@ __device__ __forceinline__ uint32_t stage_offset(int r, int c)
     return (u * Gm::NH + half) * Gm::SUB_BYTES + row * 128 + ((cc ^ (row & 7)) << 4);
 }
 
-// One CTA = one work item (a partition of one (sequence, KV head)); NW warps
-// each stream every NW-th 16-token stage of it through their own ring of NS
-// stages, and merge their softmax states at the end.
+// One CTA = one work item: one partition of one (sequence, KV head), whose
+// 16-token stages the NW warps stream in turn (warp w takes stages w, w + NW,
+// ...) through rings of NS stages each, merging their softmax states at the
+// end; or, for short split partitions, up to NW consecutive partitions, one
+// per warp, each warp's state being its partition's result.
 template <typename T, int D, int B, int NW, int NS>
 __global__ void __launch_bounds__(NW * 32)
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
@@ -96,9 +102,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     constexpr int MTILES = D / 16;  // P V m-tiles (head_dim rows)
     constexpr int IDS = Gm::IDS;    // physical blocks per stage (2 when B = 8)
 
-    // ---- which item: slot b = ((s * Hkv) + g) * max_partitions + part
-    const int part = blockIdx.x % p.max_partitions;
-    const int sg = blockIdx.x / p.max_partitions;
+    // ---- which item: slot b = ((s * Hkv) + g) * max_groups + grp; group grp
+    // holds partitions grp * cta_parts .. + cta_parts - 1 of (s, g)
+    const int max_groups = (p.max_partitions + p.cta_parts - 1) / p.cta_parts;
+    const int grp = blockIdx.x % max_groups;
+    const int sg = blockIdx.x / max_groups;
     const int s = sg / p.num_kv_heads;
     const int g = sg - s * p.num_kv_heads;
     int L = p.context_lens[s];
@@ -107,7 +115,17 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         L = 0;
     }
     const int nparts = (L + p.partition_tokens - 1) / p.partition_tokens;
-    if (part >= (nparts > 0 ? nparts : 1)) return;
+    const int p0 = grp * p.cta_parts;
+    if (p0 >= (nparts > 0 ? nparts : 1)) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // np_cta partitions here: a single one is spread over all NW warps
+    // (warp w streams its stages w, w + NW, ...); several get a warp each,
+    // and warps past np_cta have nothing to stream.
+    const int np_cta = min(p.cta_parts, (nparts > 0 ? nparts : 1) - p0);
+    const bool solo = np_cta == 1;
+    const int wpp = solo ? NW : 1;       // warps per partition
+    const int wsub = solo ? warp : 0;    // this warp's rank within it
+    const int part = solo ? p0 : p0 + warp;
     const int begin = part * p.partition_tokens;
     const int end = min(L, begin + p.partition_tokens);
     const int nst = end > begin ? (end - begin + 15) / 16 : 0;
@@ -119,7 +137,6 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::BAR_OFF);
     int* sid = reinterpret_cast<int*>(smem + Gm::SID_OFF);  // [warp][slot][2] block ids
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gq = lane >> 2, tq = lane & 3;  // mma fragment row group / column pair
     uint8_t* ring = smem + warp * Gm::RING_BYTES;
     const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
@@ -131,8 +148,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     }
     __syncwarp();
 
-    // ---- this warp's stages: q = warp + j * NW, j < cnt
-    const int cnt = nst > warp ? (nst - warp + NW - 1) / NW : 0;
+    // ---- this warp's stages of its partition: q = wsub + j * wpp, j < cnt
+    const int cnt = nst > wsub ? (nst - wsub + wpp - 1) / wpp : 0;
     int win_base = 0;
     int win_ids[IDS];
     // Block ids of this warp's stages jbase .. jbase+31, one per lane.
@@ -142,7 +159,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
         for (int u = 0; u < IDS; ++u) {
             int id = -1;
-            const int tok = begin + (warp + j * NW) * 16 + u * B;  // first token of the box
+            const int tok = begin + (wsub + j * wpp) * 16 + u * B;  // first token of the box
             if (j < cnt && tok < end) {
                 id = table[tok / B];
                 if (id < 0 || id >= p.num_blocks) {
@@ -165,7 +182,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             const uint32_t bar = smem_u32(&bars[warp * NS + slot]);
             const uint32_t kdst = smem_u32(ring + slot * Gm::STAGE_BYTES);
             const uint32_t vdst = kdst + Gm::KV_BYTES;
-            const int tok0 = begin + (warp + j * NW) * 16;
+            const int tok0 = begin + (wsub + j * wpp) * 16;
             uint32_t bytes = 0;
 #pragma unroll
             for (int u = 0; u < IDS; ++u)
@@ -193,7 +210,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     // position L-1 first writes this KV head's slice of the new token there
     // (16 bytes per lane), then orders the write before its own TMA reads
     if (p.new_k != nullptr && L > 0 && begin <= L - 1 && L - 1 < end &&
-        ((L - 1 - begin) / 16) % NW == warp) {
+        ((L - 1 - begin) / 16) % wpp == wsub) {
         const int id = table[(L - 1) / B];
         if (id < 0 || id >= p.num_blocks) {
             if (lane == 0) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
@@ -258,7 +275,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         const int id1 = sid[(warp * NS + slot) * 2 + 1];
         const uint32_t kbase = smem_u32(ring + slot * Gm::STAGE_BYTES);
         const uint32_t vbase = kbase + Gm::KV_BYTES;
-        const int tok0 = begin + (warp + j * NW) * 16;
+        const int tok0 = begin + (wsub + j * wpp) * 16;
         auto valid = [&](int r) {
             return tok0 + r < end && ((IDS > 1 && r >= B) ? id1 : id0) >= 0;
         };
@@ -343,48 +360,68 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
 
-    // ---- merge the warps (shared memory reused once every ring is drained)
-    __syncthreads();
-    float* wm = reinterpret_cast<float*>(smem) + warp * 8 * (D + 2);  // [8][D], m[8], l[8]
-    if (gq == 0) {
-        wm[8 * D + 2 * tq] = m0;
-        wm[8 * D + 2 * tq + 1] = m1;
-        wm[8 * D + 8 + 2 * tq] = l0;
-        wm[8 * D + 8 + 2 * tq + 1] = l1;
-    }
-#pragma unroll
-    for (int i = 0; i < MTILES; ++i) {
-        wm[(2 * tq) * D + 16 * i + gq] = acc[i][0];
-        wm[(2 * tq + 1) * D + 16 * i + gq] = acc[i][1];
-        wm[(2 * tq) * D + 16 * i + gq + 8] = acc[i][2];
-        wm[(2 * tq + 1) * D + 16 * i + gq + 8] = acc[i][3];
-    }
-    __syncthreads();
-    const float* sm = reinterpret_cast<const float*>(smem);
     const size_t hbase = (size_t)s * p.num_heads + (size_t)g * G;
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int n = idx / D, d = idx - n * D;
-        float M = -INFINITY;
+    if (!solo) {
+        // ---- a warp's own partition: its softmax state is the partition's
+        // result, written straight to the workspace (heads 2tq and 2tq + 1)
+        if (warp < np_cta) {
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * 8 * (D + 2) + 8 * D + n]);
-        float den = 0.f, num = 0.f;
+            for (int h = 0; h < 2; ++h) {
+                const int n = 2 * tq + h;
+                if (n >= G) break;
+                const size_t slot = (hbase + n) * p.max_partitions + part;
+                if (gq == 0) p.ws_ml[slot] = make_float2(h ? m1 : m0, h ? l1 : l0);
+                float* o = p.ws_o + slot * D;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const float* ww = sm + w * 8 * (D + 2);
-            const float mw = ww[8 * D + n];
-            const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
-            den += wt * ww[8 * D + 8 + n];
-            num += wt * ww[n * D + d];
+                for (int i = 0; i < MTILES; ++i) {
+                    o[16 * i + gq] = acc[i][h];
+                    o[16 * i + gq + 8] = acc[i][2 + h];
+                }
+            }
         }
-        if (nparts <= 1) {
-            store_out(p.out, (hbase + n) * D + d, den > 0.f ? num / den : 0.f, p.out_dtype);
-        } else {
-            const size_t slot = (hbase + n) * p.max_partitions + part;
-            p.ws_o[slot * D + d] = num;
-            if (d == 0) p.ws_ml[slot] = make_float2(M, den);
+    } else {
+        // ---- merge the warps (shared memory reused once every ring is drained)
+        __syncthreads();
+        float* wm = reinterpret_cast<float*>(smem) + warp * 8 * (D + 2);  // [8][D], m[8], l[8]
+        if (gq == 0) {
+            wm[8 * D + 2 * tq] = m0;
+            wm[8 * D + 2 * tq + 1] = m1;
+            wm[8 * D + 8 + 2 * tq] = l0;
+            wm[8 * D + 8 + 2 * tq + 1] = l1;
         }
+#pragma unroll
+        for (int i = 0; i < MTILES; ++i) {
+            wm[(2 * tq) * D + 16 * i + gq] = acc[i][0];
+            wm[(2 * tq + 1) * D + 16 * i + gq] = acc[i][1];
+            wm[(2 * tq) * D + 16 * i + gq + 8] = acc[i][2];
+            wm[(2 * tq + 1) * D + 16 * i + gq + 8] = acc[i][3];
+        }
+        __syncthreads();
+        const float* sm = reinterpret_cast<const float*>(smem);
+        for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+            const int n = idx / D, d = idx - n * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * 8 * (D + 2) + 8 * D + n]);
+            float den = 0.f, num = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float* ww = sm + w * 8 * (D + 2);
+                const float mw = ww[8 * D + n];
+                const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
+                den += wt * ww[8 * D + 8 + n];
+                num += wt * ww[n * D + d];
+            }
+            if (nparts <= 1) {
+                store_out(p.out, (hbase + n) * D + d, den > 0.f ? num / den : 0.f, p.out_dtype);
+            } else {
+                const size_t slot = (hbase + n) * p.max_partitions + part;
+                p.ws_o[slot * D + d] = num;
+                if (d == 0) p.ws_ml[slot] = make_float2(M, den);
+            }
+        }
+        if (nparts <= 1) return;
     }
-    if (nparts <= 1) return;
 
     // ---- split: the CTA that finishes the last partition of (s, g) merges
     // them by log-sum-exp: M = max_i m_i, w_i = 2^(m_i - M),
@@ -393,7 +430,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     __syncthreads();  // this CTA's partition results are written ...
     if (threadIdx.x == 0) {
         __threadfence();  // ... and published before the count goes up
-        is_last = atomicAdd(&p.done[sg], 1u) == (unsigned)nparts - 1;
+        is_last = atomicAdd(&p.done[sg], (unsigned)np_cta) == (unsigned)(nparts - np_cta);
         if (is_last) __threadfence();  // see every other partition's results
     }
     __syncthreads();
@@ -406,16 +443,34 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     const bool cached = G * nparts <= Gm::WCACHE;
     for (int n = warp; n < G; n += NW) {
         const size_t base = (hbase + n) * p.max_partitions;
+        // the (max, sum) pairs of the first 64 partitions are read once and
+        // kept in registers for both passes; any further ones are re-read
+        float2 ml[2];
         float M = -INFINITY;
-        for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldcg(&p.ws_ml[base + i]).x);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = lane + 32 * r;
+            ml[r] = i < nparts ? __ldcg(&p.ws_ml[base + i]) : make_float2(-INFINITY, 0.f);
+            M = fmaxf(M, ml[r].x);
+        }
+        for (int i = lane + 64; i < nparts; i += 32) M = fmaxf(M, __ldcg(&p.ws_ml[base + i]).x);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float den = 0.f;
-        for (int i = lane; i < nparts; i += 32) {
-            const float2 ml = __ldcg(&p.ws_ml[base + i]);
-            const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = lane + 32 * r;
+            if (i < nparts) {
+                const float w = ml[r].x == -INFINITY ? 0.f : ex2(ml[r].x - M);
+                if (cached) wts[n * nparts + i] = w;
+                den += w * ml[r].y;
+            }
+        }
+        for (int i = lane + 64; i < nparts; i += 32) {
+            const float2 mli = __ldcg(&p.ws_ml[base + i]);
+            const float w = mli.x == -INFINITY ? 0.f : ex2(mli.x - M);
             if (cached) wts[n * nparts + i] = w;
-            den += w * ml.y;
+            den += w * mli.y;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
@@ -438,7 +493,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             const int n = o / (D / 4), d4 = o - n * (D / 4);
             const size_t base = (hbase + n) * p.max_partitions;
             const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * D) + d4;
-#pragma unroll 8
+#pragma unroll 16
             for (int i = k; i < nparts; i += K) {
                 float w;
                 if (cached) {
@@ -485,7 +540,7 @@ cudaError_t launch_tc(const DecodeParams& p, const void* kmap, const void* vmap,
 {
     // 4 warps x 2-stage rings: 64 KB (D = 128) per CTA, three CTAs per SM,
     // up to 192 KB of tile loads in flight per SM
-    constexpr int NW = 4, NS = 2;
+    constexpr int NW = kDecodeTcWarps, NS = 2;
     using Gm = Geometry<D, B, NW, NS>;
     auto kern = decode_tc_kernel<T, D, B, NW, NS>;
     // set on every launch: the attribute belongs to the current device's copy

@@ -20,6 +20,8 @@ struct DecodeParams {
     int num_seqs, max_blocks, num_blocks;
     int partition_tokens;        // tokens per partition (>= max context if unsplit)
     int max_partitions;          // ceil(max_blocks * block_size / partition_tokens)
+    int cta_parts;               // tensor-core kernel: consecutive partitions per CTA
+                                 // (1, or kDecodeTcWarps: one partition per warp)
     int out_dtype;
     float2* ws_ml;               // [S][Hq][max_partitions] (max, sum) in base 2
     float* ws_o;                 // [S][Hq][max_partitions][D] unnormalised output
@@ -89,11 +91,20 @@ cudaError_t launch_kv_swap_blocks(void* dst_k, void* dst_v, const void* src_k, c
 cudaError_t launch_decode_cuda_core(const DecodeParams& p, int kv_dtype, cudaStream_t stream);
 
 // Tensor-core decode (16-bit KV, group size <= 8), one CTA per (sequence,
-// KV head, partition), partitions of one (sequence, KV head) adjacent in the
-// grid.  The tensor maps describe k_cache / v_cache as 2-D [NB*Hkv*B rows]
-// [D columns] loaded in boxes of 64 columns x min(B, 16) rows.  In split mode
-// p.done must be zero; the CTA that finishes the last partition of a
-// (sequence, KV head) merges its partitions.
+// KV head, group of p.cta_parts consecutive partitions), the groups of one
+// (sequence, KV head) adjacent in the grid; the grid is
+// S * Hkv * ceil(max_partitions / cta_parts).  A CTA that holds one partition
+// spreads it over all its warps; one that holds several gives each warp a
+// partition of its own.  The tensor maps describe k_cache / v_cache as 2-D
+// [NB*Hkv*B rows][D columns] loaded in boxes of 64 columns x min(B, 16) rows.
+// In split mode p.done must be zero; the CTA that finishes the last partition
+// of a (sequence, KV head) merges its partitions.
+constexpr int kDecodeTcWarps = 4;
+// Split partitions of at most this many tokens get one warp each (four per
+// CTA), so that a CTA's start-up and end are spread over more KV bytes, when
+// the longest context spans at least kWarpPartitionMinCount of them.
+constexpr int kWarpPartitionMaxTokens = 512;
+constexpr int kWarpPartitionMinCount = 16;
 cudaError_t launch_decode_tensor_core(const DecodeParams& p, int kv_dtype, const void* k_map,
                                       const void* v_map, long long grid, cudaStream_t stream);
 

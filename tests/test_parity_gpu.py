@@ -139,9 +139,12 @@ SMALL = [  # dtype, Hq, Hkv, D, B
 
 
 @pytest.mark.parametrize("kernel", [pkv.KERNEL_AUTO, pkv.KERNEL_CUDA_CORE])
-@pytest.mark.parametrize("P", [0, 64])
+@pytest.mark.parametrize("P", [0, 16, 64])
 @pytest.mark.parametrize("dt,Hq,Hkv,D,B", SMALL)
 def test_decode_small(dt, Hq, Hkv, D, B, P, kernel):
+    # P = 16 splits the 513-token context into 33 partitions: the tensor-core
+    # kernel then gives each warp a partition of its own (groups of four, the
+    # last one partial); P = 64 (9 partitions) spreads each over all warps
     w = Workload(0, "small", dt, Hq, Hkv, D, B, len(RAGGED), "fixed")
     case = make_decode_case(w, seed=Hq * 7 + B + D, lengths=RAGGED)
     if P and P % B:
