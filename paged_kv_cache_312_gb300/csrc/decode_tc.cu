@@ -398,25 +398,36 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         }
         __syncthreads();
         const float* sm = reinterpret_cast<const float*>(smem);
-        for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-            const int n = idx / D, d = idx - n * D;
+        // four consecutive outputs of one head per thread
+        const bool vec_out = (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+        for (int idx = threadIdx.x; idx < G * D / 4; idx += blockDim.x) {
+            const int n = idx / (D / 4), d = (idx - n * (D / 4)) * 4;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * 8 * (D + 2) + 8 * D + n]);
-            float den = 0.f, num = 0.f;
+            float den = 0.f;
+            float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
                 const float* ww = sm + w * 8 * (D + 2);
                 const float mw = ww[8 * D + n];
                 const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
                 den += wt * ww[8 * D + 8 + n];
-                num += wt * ww[n * D + d];
+                const float4 o = *reinterpret_cast<const float4*>(ww + n * D + d);
+                num.x += wt * o.x;
+                num.y += wt * o.y;
+                num.z += wt * o.z;
+                num.w += wt * o.w;
             }
             if (nparts <= 1) {
-                store_out(p.out, (hbase + n) * D + d, den > 0.f ? num / den : 0.f, p.out_dtype);
+                const bool pos = den > 0.f;
+                store_out4(p.out, (hbase + n) * D + d,
+                           make_float4(pos ? num.x / den : 0.f, pos ? num.y / den : 0.f,
+                                       pos ? num.z / den : 0.f, pos ? num.w / den : 0.f),
+                           p.out_dtype, vec_out);
             } else {
                 const size_t slot = (hbase + n) * p.max_partitions + part;
-                p.ws_o[slot * D + d] = num;
+                *reinterpret_cast<float4*>(p.ws_o + slot * D + d) = num;
                 if (d == 0) p.ws_ml[slot] = make_float2(M, den);
             }
         }

@@ -172,6 +172,32 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, int ou
         static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
 }
 
+// Four consecutive outputs (idx a multiple of 4): one 16-byte (fp32) or
+// 8-byte (16-bit) store when `vec` says the output base is 16-byte aligned.
+__device__ __forceinline__ void store_out4(void* out, size_t idx, float4 v, int out_dtype, bool vec)
+{
+    if (!vec) {
+        store_out(out, idx + 0, v.x, out_dtype);
+        store_out(out, idx + 1, v.y, out_dtype);
+        store_out(out, idx + 2, v.z, out_dtype);
+        store_out(out, idx + 3, v.w, out_dtype);
+    } else if (out_dtype == PKV_F32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = v;
+    } else if (out_dtype == PKV_F16) {
+        const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&a);
+        u.y = *reinterpret_cast<const uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(static_cast<__half*>(out) + idx) = u;
+    } else {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&a);
+        u.y = *reinterpret_cast<const uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + idx) = u;
+    }
+}
+
 // Zeroes the 16-bit halves of a packed pair whose token is masked.
 __device__ __forceinline__ uint32_t mask_pair(uint32_t x, bool keep_lo, bool keep_hi)
 {

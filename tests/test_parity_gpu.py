@@ -207,6 +207,35 @@ def test_16bit_outputs(out_dtype):
         assert (diff <= TOL16 + rel * np.abs(ref)).all()
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_output_base_not_16_byte_aligned(out_dtype):
+    # the decode kernel stores four outputs at a time only from a 16-byte
+    # aligned base; one element past an aligned base takes the scalar stores
+    w = Workload(0, "ua", "bf16", 16, 2, 128, 16, 4, "fixed")
+    case = make_decode_case(w, seed=21, lengths=[1, 50, 300, 1000])
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, 16, 2)
+    n = case.q.numel()
+    for P in (0, 64):
+        big = torch.full((n + 1,), float("nan"), dtype=out_dtype, device=DEV)
+        out = big[1:].view(case.q.shape)
+        assert out.data_ptr() % 16 != 0
+        ws = None
+        if P:
+            nb = pkv.decode_workspace_bytes(4, 16, 128, case.block_tables.shape[1] * 16, P)
+            ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+        pkv.paged_decode_attention(out, case.q.to(DEV), kc, vc, case.block_tables.to(DEV),
+                                   case.context_lens.to(DEV), w.scale, 16, 2,
+                                   partition_size=P, workspace=ws)
+        torch.cuda.synchronize()
+        assert pkv.device_status() == 0
+        assert torch.isnan(big[:1].float()).all()  # nothing written before the view
+        rel = 0.0 if out_dtype == torch.float32 else 2.0 ** -8
+        diff = np.abs(out.float().cpu().double().numpy() - ref)
+        assert (diff <= TOL16 + rel * np.abs(ref)).all(), P
+
+
 def test_bad_block_id_and_length_are_flagged():
     w = Workload(0, "bad", "bf16", 8, 2, 128, 16, 3, "fixed")
     case = make_decode_case(w, seed=9, lengths=[40, 40, 40])
