@@ -281,43 +281,57 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         };
         const bool all_valid = tok0 + 16 <= end && id0 >= 0 && id1 >= 0;
 
-        // ---- S^T = K Q^T  (16 tokens x 8 heads)
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- S^T = K Q^T  (16 tokens x 8 heads), as two independent
+        // accumulation chains (even and odd k-steps)
+        float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < KSTEPS; ++kk) {
             uint32_t a[4];
             ldsm_x4(kbase + stage_offset<D, B, NW, NS>(k_row, 2 * kk + k_chunk_add), a);
-            Mma<T>::run(sc, a, qb[kk][0], qb[kk][1]);
+            if (kk & 1)
+                Mma<T>::run(sd, a, qb[kk][0], qb[kk][1]);
+            else
+                Mma<T>::run(sc, a, qb[kk][0], qb[kk][1]);
         }
-        float x0 = sc[0] * sl, x1 = sc[1] * sl, x2 = sc[2] * sl, x3 = sc[3] * sl;
+        float x0 = (sc[0] + sd[0]) * sl, x1 = (sc[1] + sd[1]) * sl;
+        float x2 = (sc[2] + sd[2]) * sl, x3 = (sc[3] + sd[3]) * sl;
         if (!all_valid) {
             if (!valid(gq)) x0 = x1 = -INFINITY;
             if (!valid(gq + 8)) x2 = x3 = -INFINITY;
         }
-        // ---- online softmax (per head: reduce over the 8 row groups)
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+        // ---- online softmax in base 2 against a reference max per head that
+        // moves only when a score passes it by more than 8 (so p <= 2^8): most
+        // stages need neither the max over the 8 row groups nor a rescale of O
+        const bool up = fmaxf(x0, x2) > m0 + 8.f || fmaxf(x1, x3) > m1 + 8.f;
+        if (__any_sync(0xffffffffu, up)) {
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            // 0 while m is -inf (nothing accumulated yet), 1 if m stays
+            const float al0 = mn0 == -INFINITY ? 1.f : ex2(m0 - mn0);
+            const float al1 = mn1 == -INFINITY ? 1.f : ex2(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int i = 0; i < MTILES; ++i) {
+                acc[i][0] *= al0;
+                acc[i][1] *= al1;
+                acc[i][2] *= al0;
+                acc[i][3] *= al1;
+            }
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = ex2(m0 - ms0), al1 = ex2(m1 - ms1);  // 0 while m is -inf
-        m0 = mn0;
-        m1 = mn1;
+        const float ms0 = m0 == -INFINITY ? 0.f : m0;
+        const float ms1 = m1 == -INFINITY ? 0.f : m1;
         const float p0 = ex2(x0 - ms0), p1 = ex2(x1 - ms1);
         const float p2 = ex2(x2 - ms0), p3 = ex2(x3 - ms1);
-        l0 = l0 * al0 + p0 + p2;
-        l1 = l1 * al1 + p1 + p3;
-#pragma unroll
-        for (int i = 0; i < MTILES; ++i) {
-            acc[i][0] *= al0;
-            acc[i][1] *= al1;
-            acc[i][2] *= al0;
-            acc[i][3] *= al1;
-        }
+        l0 += p0 + p2;
+        l1 += p1 + p3;
         // ---- P^T operand (tokens 2tq.. x head gq) via an in-register transpose
         uint32_t h01, l01, h23, l23;
         Mma<T>::split(p0, p1, h01, l01);
