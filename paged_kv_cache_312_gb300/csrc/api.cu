@@ -55,7 +55,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 struct MapEntry {
     const void* ptr = nullptr;
     uint64_t rows = 0;
-    int D = 0, B = 0, dtype = -1;
+    int D = 0, B = 0, dtype = -1, halves = 0;
     CUtensorMap map;
 };
 
@@ -77,11 +77,18 @@ int get_encoder()
     return PKV_OK;
 }
 
-int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtensorMap* out)
+// A cache viewed as [rows][D] bf16/fp16, loaded in boxes of 64 columns x
+// min(B, 16) rows with the 128-byte swizzle.  halves = 0: a 2-D map, one box
+// per 64-column half.  halves = 1: a 3-D map whose outermost dimension steps
+// over the 64-column halves (stride 128 bytes), so that one box brings every
+// half of min(B, 16) rows, laid out half after half in shared memory.
+int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtensorMap* out,
+               int halves = 0)
 {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (const MapEntry& m : g_maps) {
-        if (m.ptr == cache && m.rows == rows && m.D == D && m.B == B && m.dtype == dtype) {
+        if (m.ptr == cache && m.rows == rows && m.D == D && m.B == B && m.dtype == dtype &&
+            m.halves == halves) {
             *out = m.map;
             return PKV_OK;
         }
@@ -90,14 +97,15 @@ int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtens
     if (rc != PKV_OK) return rc;
     MapEntry& m = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % 16;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)(B < 16 ? B : 16)};
-    cuuint32_t estr[2] = {1, 1};
+    const cuuint32_t box_rows = (cuuint32_t)(B < 16 ? B : 16);
+    cuuint64_t dims[3] = {(cuuint64_t)(halves ? 64 : D), (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, (cuuint32_t)(D / 64)};
+    cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(&m.map,
                           dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                          2, const_cast<void*>(cache), dims, strides, box, estr,
+                          halves ? 3 : 2, const_cast<void*>(cache), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -109,6 +117,7 @@ int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtens
     m.D = D;
     m.B = B;
     m.dtype = dtype;
+    m.halves = halves;
     *out = m.map;
     return PKV_OK;
 }
@@ -426,8 +435,8 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
     if (tensor_core) {
         CUtensorMap kmap, vmap;
         const uint64_t rows = (uint64_t)num_blocks * num_kv_heads * block_size;
-        int rc = tensor_map(k_cache, rows, head_dim, block_size, kv_dtype, &kmap);
-        if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap);
+        int rc = tensor_map(k_cache, rows, head_dim, block_size, kv_dtype, &kmap, 1);
+        if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap, 1);
         if (rc != PKV_OK) return rc;
         // grid: every (sequence, KV head, partition group) slot, the groups of
         // one (sequence, KV head) adjacent; slots past a sequence's end exit at

@@ -195,12 +195,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                 // B >= 16: one 16-row box at the stage's offset in its block;
                 // B == 8: one 8-row box per block.
                 const int row = (ids[u] * p.num_kv_heads + g) * B + (IDS > 1 ? 0 : tok0 % B);
-#pragma unroll
-                for (int hf = 0; hf < Gm::NH; ++hf) {
-                    const uint32_t off = (u * Gm::NH + hf) * Gm::SUB_BYTES;
-                    tma_load_2d(kdst + off, &kmap, hf * 64, row, bar);
-                    tma_load_2d(vdst + off, &vmap, hf * 64, row, bar);
-                }
+                // one box brings both 64-column halves (the tensor map's
+                // outer dimension steps over them)
+                const uint32_t off = u * Gm::NH * Gm::SUB_BYTES;
+                tma_load_3d(kdst + off, &kmap, 0, row, 0, bar);
+                tma_load_3d(vdst + off, &vmap, 0, row, 0, bar);
             }
         }
         __syncwarp();
