@@ -61,7 +61,7 @@ def kernel_sha() -> str:
     """Hash of the decode kernel's sources (the traffic figures above hold
     only for the kernel they were captured from)."""
     h = hashlib.sha256()
-    for name in ("decode_tc.cu", "tc_common.cuh"):
+    for name in ("decode_tc.cu", "decode_tc.cuh", "tc_common.cuh"):
         h.update(open(os.path.join(ROOT, "paged_kv_cache_312_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:16]
 
@@ -217,13 +217,23 @@ def run_gpu(args, rank, world, local_rank):
     # the step's inputs live in one pinned host buffer and one device buffer
     # (views per tensor), so a step's host->device traffic is a single copy
     has_write = st.slots is not None
+    # beam groups: the beams of a group (consecutive sequences) attend their
+    # shared prompt blocks in one CTA per (group, KV head)
+    grouped = st.unique_blocks is not None and not args.ungrouped
     inputs = [st.q, st.tables, st.lens, st.pairs]
     if has_write:
         inputs += [st.new_key, st.new_value]
+    if grouped:
+        S_ = st.q.shape[0]
+        gstart = torch.arange(0, S_ + 1, w.beam_width, dtype=torch.int32)
+        shared = pkv.group_shared_tokens(st.tables, st.lens, gstart, w.block_size)
+        inputs += [gstart, shared]
     h_pack, views = pack_inputs(inputs, dev)
     q, bt, cl, pairs = views[:4]
     if has_write:
         nk, nv = views[4:6]
+    if grouped:
+        gs_d, sh_d = views[-3:-1]
     S, Hq, D = q.shape
     out = torch.empty((S, Hq, D), dtype=torch.float32, device=dev)
     ws = None
@@ -238,7 +248,11 @@ def run_gpu(args, rank, world, local_rank):
             pkv.kv_copy_blocks(kc, vc, pairs, stream=stream)
         if ev is not None:
             ev.record(stream)
-        if has_write:  # append the new tokens and attend, one call
+        if grouped:  # append the new tokens and attend, one CTA per (group, KV head)
+            pkv.paged_decode_grouped(out, q, kc, vc, bt, cl, gs_d, sh_d, w.scale, w.block_size,
+                                     w.num_kv_heads, new_k=nk if has_write else None,
+                                     new_v=nv if has_write else None, stream=stream)
+        elif has_write:  # append the new tokens and attend, one call
             pkv.decode_step(out, q, nk, nv, kc, vc, bt, cl, w.scale, w.block_size,
                             w.num_kv_heads, partition_size=st.P, workspace=ws, stream=stream)
         else:
@@ -327,7 +341,10 @@ def run_gpu(args, rank, world, local_rank):
                    "num_kv_heads": w.num_kv_heads, "head_dim": D, "block_size": w.block_size,
                    "partition_size": st.P, "kv_bytes_per_step": st.kv_bytes,
                    "step": ("cow-copy + " if pairs.shape[0] else "") +
-                   ("decode_step (new tokens appended inside the attention launch)"
+                   ("paged_decode_grouped (beam groups of %d: shared prompt blocks read once "
+                    "per group; new tokens appended inside the attention launch)" % w.beam_width
+                    if grouped else
+                    "decode_step (new tokens appended inside the attention launch)"
                     if has_write else "paged_decode_attention"),
                    "l2": "inputs larger than L2 (KV %.2f GB vs 129 MB L2), no flush" %
                    (st.kv_bytes / 1e9),
@@ -337,7 +354,8 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "hbm", "kernel": ("decode_step" if has_write else
+        "roofline": {"bound": "hbm", "kernel": ("paged_decode_grouped" if grouped else
+                                                "decode_step" if has_write else
                                                 "paged_decode_attention") +
                      (" call: tensor-core decode kernel with in-kernel log-sum-exp merge "
                       "(+ counter memset)" if st.P else " (tensor-core kernel)"),
@@ -349,7 +367,7 @@ def run_gpu(args, rank, world, local_rank):
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
     }
     if st.slots is not None and rank == 0:
-        line["host_allocator"] = host_allocator_timing(st, pkv)
+        line["host_allocator"] = host_allocator_timing(st, pkv, grouped)
     if st.unique_blocks is not None:
         ub = st.unique_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2 * 2
         line["config"]["unique_kv_bytes"] = ub
@@ -378,10 +396,11 @@ def pack_inputs(tensors, dev):
     return host, views + [buf]
 
 
-def host_allocator_timing(st, pkv, steps=256):
+def host_allocator_timing(st, pkv, grouped=False, steps=256):
     """Host side of a decode step (a1/a2): pkv_step_append for every sequence
     (slot mapping, new blocks, copy-on-write decisions) plus the read-back of
-    the dense block tables the device calls take.  Timed over `steps`
+    the dense block tables the device calls take (and, for beam groups, the
+    shared prefix of each group found from those tables).  Timed over `steps`
     consecutive steps from the workload's lengths, in a pool with room for
     them; mean microseconds per step."""
     w = st.w
@@ -393,13 +412,17 @@ def host_allocator_timing(st, pkv, steps=256):
         a.add(i, max(0, n - 1))
     seqs = list(range(S))
     maxb = max((n + steps + B - 1) // B for n in lens)
+    gstart = torch.arange(0, S + 1, max(1, w.beam_width), dtype=torch.int32)
     t0 = time.perf_counter()
     for _ in range(steps):
         a.step_append(seqs)
-        a.dense_tables(seqs, maxb)
+        tables, tl = a.dense_tables(seqs, maxb)
+        if grouped:
+            pkv.group_shared_tokens(tables, tl, gstart, B)
     us = (time.perf_counter() - t0) / steps * 1e6
     return {"us_per_step": round(us, 2), "steps": steps, "sequences": S,
-            "what": "pkv_step_append for every sequence + dense block-table read-back"}
+            "what": "pkv_step_append for every sequence + dense block-table read-back" +
+            (" + shared prefix per beam group" if grouped else "")}
 
 
 def cpu_baseline(st, budget_s=8.0):
@@ -645,6 +668,9 @@ def main():
                     help="partition size in tokens (default: the workload's launch setting)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ungrouped", action="store_true",
+                    help="beam workload: attend every beam on its own (decode_step) instead of "
+                         "one CTA per beam group")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=8.0)
     ap.add_argument("--prefill", action="store_true",

@@ -181,6 +181,51 @@ int pkv_decode_step(void* out, const void* q, const void* new_k, const void* new
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * paged_decode_grouped -- decode attention (optionally a decode step, with
+ * new_k/new_v) for groups of sequences that share a prefix of physical
+ * blocks, as the beams of a beam search or the samples of one prompt do
+ * ([CAY beam search]: the common logical blocks of the beams map to one
+ * physical copy).  The result is exactly that of pkv_decode_step /
+ * pkv_paged_decode_attention for every sequence; the shared blocks are only
+ * read once per group instead of once per member.
+ *
+ * group_start   : int32 [num_groups + 1], device memory, non-decreasing:
+ *                 group i is sequences group_start[i] .. group_start[i+1]-1
+ *                 (consecutive), with 1 <= members and members * G <= 8
+ *                 (G = num_heads / num_kv_heads).  A group outside these
+ *                 bounds is skipped and sets PKV_STATUS_BAD_LEN.
+ * shared_tokens : int32 [num_groups], device memory: the first
+ *                 shared_tokens[i] positions of every member of group i lie
+ *                 in the same physical blocks (same table entries), e.g. from
+ *                 pkv_group_shared_tokens.  The kernel uses it rounded down
+ *                 to a multiple of 16, at most every member's context (and,
+ *                 in a decode step, short of every member's new token).
+ * new_k, new_v  : NULL for attention only; else as in pkv_decode_step, each
+ *                 new token in a block private to its sequence.
+ * Other arguments as in pkv_decode_step; not split (no partition_size or
+ * workspace).  Needs the tensor-core kernel: 16-bit KV, G <= 8, kernel
+ * choice PKV_KERNEL_AUTO (else PKV_ERR_UNSUPPORTED).
+ */
+int pkv_paged_decode_grouped(void* out, const void* q, const void* new_k, const void* new_v,
+                             void* k_cache, void* v_cache, const int32_t* block_tables,
+                             const int32_t* context_lens, const int32_t* group_start,
+                             const int32_t* shared_tokens, int num_groups, float scale,
+                             int block_size, int num_kv_heads, int num_seqs, int num_heads,
+                             int head_dim, int max_blocks_per_seq, int num_blocks, int kv_dtype,
+                             int out_dtype, void* stream);
+
+/*
+ * group_shared_tokens -- host helper for pkv_paged_decode_grouped: for each
+ * group, the number of leading positions whose table entries every member
+ * holds in common (whole blocks), capped at the shortest member's context.
+ * All pointers are host memory; block_tables is [num_seqs][max_blocks_per_seq].
+ * A group outside [0, num_seqs) or empty gives PKV_ERR_SHAPE.
+ */
+int pkv_group_shared_tokens(const int32_t* block_tables, const int32_t* context_lens,
+                            const int32_t* group_start, int num_groups, int num_seqs,
+                            int max_blocks_per_seq, int block_size, int32_t* shared_tokens);
+
+/*
  * paged_prefill_attention -- several new query tokens per sequence (a prompt,
  * or a chunk of one), each attending causally over the sequence's cached
  * tokens up to its own position.  [CAY recomputation]: a whole sequence's KV

@@ -35,6 +35,9 @@ _SIGS = {
     "pkv_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "pkv_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I,
                              _I, _I, _I, _P, _SZ, _P]),
+    "pkv_paged_decode_grouped": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _F, _I, _I, _I,
+                                      _I, _I, _I, _I, _I, _I, _P]),
+    "pkv_group_shared_tokens": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "pkv_paged_prefill_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I,
                                          _I, _I, _I, _I, _I, _P]),
     "pkv_paged_decode_attention_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I,
@@ -197,6 +200,66 @@ def decode_step(out, q, new_k, new_v, k_cache, v_cache, block_tables, context_le
         Hq, D, block_tables.shape[1], NB, DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype],
         int(partition_size), ws_ptr, ws_bytes, _stream(stream))
     _check(rc, "pkv_decode_step")
+
+
+def paged_decode_grouped(out, q, k_cache, v_cache, block_tables, context_lens, group_start,
+                         shared_tokens, scale, block_size, num_kv_heads, new_k=None, new_v=None,
+                         stream=None):
+    """Decode attention (a decode step when new_k/new_v [S, Hkv, D] are
+    given) for groups of consecutive sequences sharing a prefix of physical
+    blocks: group i is sequences group_start[i]..group_start[i+1]-1, whose
+    first shared_tokens[i] positions use the same table entries.  Same
+    result as decode_step / paged_decode_attention for every sequence."""
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = k_cache.shape
+    if (Hkv, B, Dk) != (num_kv_heads, block_size, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("paged_decode_grouped: cache shape mismatch")
+    if out.shape != q.shape:
+        raise ValueError("paged_decode_grouped: out must be [S, Hq, D]")
+    if (new_k is None) != (new_v is None):
+        raise ValueError("paged_decode_grouped: pass both new_k and new_v, or neither")
+    if new_k is not None and (new_k.shape != (S, Hkv, D) or new_v.shape != new_k.shape or
+                              new_k.dtype != q.dtype or new_v.dtype != q.dtype):
+        raise ValueError("paged_decode_grouped: new_k/new_v must be [S, Hkv, D] in q's dtype")
+    for t, name in ((block_tables, "block_tables"), (context_lens, "context_lens"),
+                    (group_start, "group_start"), (shared_tokens, "shared_tokens")):
+        if t.dtype != torch.int32:
+            raise ValueError("%s must be int32" % name)
+    G = group_start.shape[0] - 1
+    if group_start.dim() != 1 or G < 1 or shared_tokens.shape != (G,):
+        raise ValueError("group_start must be [num_groups + 1], shared_tokens [num_groups]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks], context_lens [S]")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise ValueError("q, k_cache, v_cache must share a dtype")
+    nk = _dev(new_k, "new_k") if new_k is not None else ctypes.c_void_p(0)
+    nv = _dev(new_v, "new_v") if new_v is not None else ctypes.c_void_p(0)
+    rc = lib().pkv_paged_decode_grouped(
+        _dev(out, "out"), _dev(q, "q"), nk, nv, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables"), _dev(context_lens, "context_lens"),
+        _dev(group_start, "group_start"), _dev(shared_tokens, "shared_tokens"), G, float(scale),
+        int(block_size), int(num_kv_heads), S, Hq, D, block_tables.shape[1], NB,
+        DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], _stream(stream))
+    _check(rc, "pkv_paged_decode_grouped")
+
+
+def group_shared_tokens(block_tables, context_lens, group_start, block_size):
+    """Host helper: for each group, the leading positions whose table
+    entries all members hold in common (whole blocks), at most the shortest
+    member's context.  CPU int32 tensors in, CPU int32 [num_groups] out."""
+    bt = block_tables.to(torch.int32).contiguous()
+    cl = context_lens.to(torch.int32).contiguous()
+    gs = group_start.to(torch.int32).contiguous()
+    if bt.is_cuda or cl.is_cuda or gs.is_cuda:
+        raise ValueError("group_shared_tokens takes host tensors")
+    G = gs.shape[0] - 1
+    out = torch.zeros(max(G, 0), dtype=torch.int32)
+    rc = lib().pkv_group_shared_tokens(
+        ctypes.c_void_p(bt.data_ptr()), ctypes.c_void_p(cl.data_ptr()),
+        ctypes.c_void_p(gs.data_ptr()), G, bt.shape[0], bt.shape[1], int(block_size),
+        ctypes.c_void_p(out.data_ptr()))
+    _check(rc, "pkv_group_shared_tokens")
+    return out
 
 
 def paged_prefill_attention(out, q, k_cache, v_cache, block_tables, context_lens, query_start,

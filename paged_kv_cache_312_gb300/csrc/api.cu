@@ -4,7 +4,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -344,7 +346,8 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
                 float scale, int block_size, int num_kv_heads, int num_seqs, int num_heads,
                 int head_dim, int max_blocks_per_seq, int num_blocks, int kv_dtype, int out_dtype,
                 int partition_size, void* workspace, size_t workspace_bytes, void* stream,
-                const void* new_k, const void* new_v)
+                const void* new_k, const void* new_v, const int32_t* group_start = nullptr,
+                const int32_t* shared_tokens = nullptr, int num_groups = 0)
 {
     if (!pkv_dtype_bytes(kv_dtype) || !pkv_dtype_bytes(out_dtype))
         return pkv_fail(PKV_ERR_DTYPE, "%s: dtype kv=%d out=%d", fn, kv_dtype, out_dtype);
@@ -379,6 +382,19 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
     if (append && (!new_v || !aligned(new_k, 16) || !aligned(new_v, 16)))
         return pkv_fail(new_v ? PKV_ERR_ALIGN : PKV_ERR_NULL,
                         "%s: new_k and new_v need 16-byte alignment", fn);
+    const bool grouped = group_start != nullptr;
+    if (grouped) {
+        if (!shared_tokens) return pkv_fail(PKV_ERR_NULL, "%s: NULL shared_tokens", fn);
+        if (num_groups < 1 || num_groups > num_seqs)
+            return pkv_fail(PKV_ERR_SHAPE, "%s: num_groups %d outside [1, %d]", fn, num_groups,
+                            num_seqs);
+        if (partition_size != 0)
+            return pkv_fail(PKV_ERR_UNSUPPORTED, "%s: beam groups are not split", fn);
+        if (kv_dtype == PKV_F32 || num_heads / num_kv_heads > 8 ||
+            g_decode_kernel != PKV_KERNEL_AUTO)
+            return pkv_fail(PKV_ERR_UNSUPPORTED,
+                            "%s: beam groups need the tensor-core kernel (16-bit KV, G <= 8)", fn);
+    }
 
     DecodeParams p;
     p.out = out;
@@ -401,6 +417,9 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
     p.done = nullptr;
     p.new_k = nullptr;
     p.new_v = nullptr;
+    p.group_start = nullptr;
+    p.shared_tokens = nullptr;
+    p.num_groups = 0;
     const int max_ctx = max_blocks_per_seq * block_size;
     p.cta_parts = 1;
     if (partition_size == 0) {
@@ -438,6 +457,18 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
         int rc = tensor_map(k_cache, rows, head_dim, block_size, kv_dtype, &kmap, 1);
         if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap, 1);
         if (rc != PKV_OK) return rc;
+        if (grouped) {
+            // one CTA per (beam group, KV head); each writes its new tokens
+            p.group_start = group_start;
+            p.shared_tokens = shared_tokens;
+            p.num_groups = num_groups;
+            p.new_k = new_k;
+            p.new_v = new_v;
+            e = launch_decode_grouped(p, kv_dtype, &kmap, &vmap,
+                                      (long long)num_groups * num_kv_heads, st);
+            if (e != cudaSuccess) return cuda_fail(e, fn);
+            return PKV_OK;
+        }
         // grid: every (sequence, KV head, partition group) slot, the groups of
         // one (sequence, KV head) adjacent; slots past a sequence's end exit at
         // once.  Short partitions of long contexts go one per warp, four to a
@@ -492,6 +523,57 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, co
                        context_lens, scale, block_size, num_kv_heads, num_seqs, num_heads, head_dim,
                        max_blocks_per_seq, num_blocks, kv_dtype, out_dtype, partition_size,
                        workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+int pkv_paged_decode_grouped(void* out, const void* q, const void* new_k, const void* new_v,
+                             void* k_cache, void* v_cache, const int32_t* block_tables,
+                             const int32_t* context_lens, const int32_t* group_start,
+                             const int32_t* shared_tokens, int num_groups, float scale,
+                             int block_size, int num_kv_heads, int num_seqs, int num_heads,
+                             int head_dim, int max_blocks_per_seq, int num_blocks, int kv_dtype,
+                             int out_dtype, void* stream)
+{
+    static const char* fn = "pkv_paged_decode_grouped";
+    if (num_seqs > 0 && !group_start) return pkv_fail(PKV_ERR_NULL, "%s: NULL group_start", fn);
+    if (num_seqs > 0 && (new_k == nullptr) != (new_v == nullptr))
+        return pkv_fail(PKV_ERR_NULL, "%s: new_k and new_v must both be set or both NULL", fn);
+    return decode_impl(fn, out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                       block_size, num_kv_heads, num_seqs, num_heads, head_dim, max_blocks_per_seq,
+                       num_blocks, kv_dtype, out_dtype, 0, nullptr, 0, stream, new_k, new_v,
+                       group_start, shared_tokens, num_groups);
+}
+
+int pkv_group_shared_tokens(const int32_t* block_tables, const int32_t* context_lens,
+                            const int32_t* group_start, int num_groups, int num_seqs,
+                            int max_blocks_per_seq, int block_size, int32_t* shared_tokens)
+{
+    static const char* fn = "pkv_group_shared_tokens";
+    if (num_groups < 0 || num_seqs < 0 || max_blocks_per_seq <= 0 || block_size <= 0)
+        return pkv_fail(PKV_ERR_SHAPE, "%s: bad sizes", fn);
+    if (num_groups == 0) return PKV_OK;
+    if (!block_tables || !context_lens || !group_start || !shared_tokens)
+        return pkv_fail(PKV_ERR_NULL, "%s: NULL pointer", fn);
+    for (int i = 0; i < num_groups; ++i) {
+        const int a = group_start[i], b = group_start[i + 1];
+        if (a < 0 || b <= a || b > num_seqs)
+            return pkv_fail(PKV_ERR_SHAPE, "%s: group %d spans [%d, %d)", fn, i, a, b);
+        // leading table entries that every member holds in common, within
+        // every member's context
+        int64_t shared = INT64_MAX;
+        for (int s = a; s < b; ++s) shared = std::min<int64_t>(shared, context_lens[s]);
+        const int32_t* t0 = block_tables + (size_t)a * max_blocks_per_seq;
+        int blocks = 0;
+        while (blocks < max_blocks_per_seq && (int64_t)blocks * block_size < shared) {
+            bool same = t0[blocks] >= 0;
+            for (int s = a + 1; s < b && same; ++s)
+                same = block_tables[(size_t)s * max_blocks_per_seq + blocks] == t0[blocks];
+            if (!same) break;
+            ++blocks;
+        }
+        shared = std::min<int64_t>(shared, (int64_t)blocks * block_size);
+        shared_tokens[i] = (int32_t)std::max<int64_t>(shared, 0);
+    }
+    return PKV_OK;
 }
 
 int pkv_decode_step(void* out, const void* q, const void* new_k, const void* new_v,

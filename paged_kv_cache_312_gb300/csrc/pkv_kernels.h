@@ -32,6 +32,12 @@ struct DecodeParams {
     // written at position context_lens[s]-1 before it is attended.
     const void* new_k;
     const void* new_v;
+    // Beam groups (tensor-core kernel only; NULL otherwise): group i holds
+    // sequences group_start[i] .. group_start[i+1]-1, whose first
+    // shared_tokens[i] tokens use the same physical blocks.
+    const int32_t* group_start;
+    const int32_t* shared_tokens;
+    int num_groups;
 };
 
 // Everything one prefill launch needs (passed by value).
@@ -107,6 +113,12 @@ constexpr int kWarpPartitionMaxTokens = 512;
 constexpr int kWarpPartitionMinCount = 16;
 cudaError_t launch_decode_tensor_core(const DecodeParams& p, int kv_dtype, const void* k_map,
                                       const void* v_map, long long grid, cudaStream_t stream);
+
+// Tensor-core decode over beam groups: one CTA per (group, KV head), grid
+// num_groups * num_kv_heads, unsplit.  Each shared-prefix K/V tile is read
+// once for all members of the group; p.group_start / p.shared_tokens set.
+cudaError_t launch_decode_grouped(const DecodeParams& p, int kv_dtype, const void* k_map,
+                                  const void* v_map, long long grid, cudaStream_t stream);
 
 // Log-sum-exp merge of split partitions (only sequences with > 1 partition).
 cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);

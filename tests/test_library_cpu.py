@@ -8,6 +8,7 @@ import random
 import re
 
 import numpy as np
+import torch
 import pytest
 
 import paged_kv_cache_312_gb300 as pkv
@@ -373,3 +374,59 @@ def test_beam_fork_cow_pairs():
     assert [p[0] for p in pairs.tolist()] == [last, last, last]
     assert a.refcount(last) == 1 and a.table(3)[-1] == last
     assert len(set(slots.tolist())) == 4
+
+
+def test_grouped_decode_rejects_bad_arguments_on_host():
+    L = pkv.lib()
+    P = ctypes.c_void_p
+
+    def call(**kw):
+        a = dict(nk=256, nv=256, gs=256, G=1, kv=2, Hq=8, P=0)
+        a.update(kw)
+        return L.pkv_paged_decode_grouped(P(256), P(256), P(a["nk"]), P(a["nv"]), P(256), P(256),
+                                          P(256), P(256), P(a["gs"]), P(256), a["G"], 0.1, 16, 4,
+                                          2, a["Hq"], 128, 4, 10, a["kv"], 0, P(0))
+    assert call(gs=0) == -1          # no group table
+    assert call(nv=0) == -1          # new_k without new_v
+    assert call(G=0) == -2           # fewer than one group
+    assert call(G=3) == -2           # more groups than sequences
+    assert call(kv=0) == -4          # fp32 KV has no tensor-core path
+    assert call(Hq=40) == -4         # 10 query heads per KV head
+    assert call(nk=0, nv=0, G=0) == -2  # attention only: same group checks
+
+
+def _shared_reference(bt, cl, gs, B):
+    out = []
+    for i in range(len(gs) - 1):
+        mem = list(range(gs[i], gs[i + 1]))
+        lim = min(cl[s] for s in mem)
+        n = 0
+        while n < bt.shape[1] and n * B < lim and bt[mem[0], n] >= 0 and \
+                all(bt[s, n] == bt[mem[0], n] for s in mem):
+            n += 1
+        out.append(max(0, min(lim, n * B)))
+    return out
+
+
+def test_group_shared_tokens_against_a_reference():
+    rng = np.random.default_rng(5)
+    for trial in range(200):
+        B = int(rng.choice([8, 16, 32]))
+        S = int(rng.integers(1, 12))
+        mb = int(rng.integers(1, 10))
+        bt = rng.integers(-1, 6, size=(S, mb)).astype(np.int32)
+        # groups: consecutive runs; copy a random prefix of the first member's row
+        cuts = sorted(set(rng.integers(1, S + 1, size=int(rng.integers(0, 4))).tolist()) | {S})
+        gs = [0] + cuts
+        for i in range(len(gs) - 1):
+            k = int(rng.integers(0, mb + 1))
+            for s in range(gs[i] + 1, gs[i + 1]):
+                bt[s, :k] = bt[gs[i], :k]
+        cl = rng.integers(0, mb * B + 1, size=S).astype(np.int32)
+        got = pkv.group_shared_tokens(torch.from_numpy(bt), torch.from_numpy(cl),
+                                      torch.tensor(gs, dtype=torch.int32), B)
+        assert got.tolist() == _shared_reference(bt, cl, gs, B), (bt, cl, gs, B)
+    with pytest.raises(pkv.PkvError):  # a group past the last sequence
+        pkv.group_shared_tokens(torch.zeros(2, 3, dtype=torch.int32),
+                                torch.ones(2, dtype=torch.int32),
+                                torch.tensor([0, 3], dtype=torch.int32), 16)

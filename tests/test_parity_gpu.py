@@ -786,3 +786,124 @@ def test_workload5_beam_step_full_size():
         expect = torch.cat([case.prefix_k[g0], case.suffix_k[par], case.new_key[b:b + 1]])
         assert int(cl_r[b]) == w.prefix_len + n + 1
         assert np.array_equal(K, expect.double().numpy())
+
+
+# --------------------------------------------------------------------------
+# Beam groups: sequences sharing a prefix of physical blocks, attended by one
+# CTA per (group, KV head) that reads each shared tile once
+# --------------------------------------------------------------------------
+
+def make_group_case(dt, Hq, Hkv, D, B, groups, seed, step):
+    """groups: list of (shared blocks, [tail tokens per member]).  Members of
+    a group hold the same first `shared blocks` ids, then blocks of their own
+    for the tail; unused slots are NaN.  With step, each member's last token
+    is the new one (its slot NaN until the step writes it)."""
+    g = torch.Generator().manual_seed(seed)
+    dtype = {"bf16": torch.bfloat16, "f16": torch.float16}[dt]
+    rows, lens = [], []
+    nxt = 0
+    for nsh, tails in groups:
+        shared_ids = list(range(nxt, nxt + nsh))
+        nxt += nsh
+        for t in tails:
+            own = -(-t // B)
+            rows.append(shared_ids + list(range(nxt, nxt + own)))
+            nxt += own
+            lens.append(nsh * B + t)
+    NB = nxt + 3
+    perm = torch.randperm(NB, generator=g).tolist()  # physical ids in shuffled order
+    S = len(rows)
+    mb = max(len(r) for r in rows)
+    bt = torch.full((S, mb), -1, dtype=torch.int32)
+    for s, r in enumerate(rows):
+        bt[s, :len(r)] = torch.tensor([perm[i] for i in r], dtype=torch.int32)
+    cl = torch.tensor(lens, dtype=torch.int32)
+    kc = torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    vc = torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    # NaN in every slot no sequence attends (and in the new tokens' slots)
+    used = torch.zeros(NB, B, dtype=torch.bool)
+    for s in range(S):
+        n = int(cl[s]) - (1 if step else 0)
+        for i in range(n):
+            used[int(bt[s, i // B]), i % B] = True
+    unused = (~used)[:, None, :, None].expand_as(kc)
+    kc[unused] = float("nan")
+    vc[unused] = float("nan")
+    q = torch.randn(S, Hq, D, generator=g).to(dtype)
+    nk = torch.randn(S, Hkv, D, generator=g).to(dtype)
+    nv = torch.randn(S, Hkv, D, generator=g).to(dtype)
+    gs = [0]
+    for _, tails in groups:
+        gs.append(gs[-1] + len(tails))
+    return q, kc, vc, bt, cl, torch.tensor(gs, dtype=torch.int32), nk, nv
+
+
+GROUP_CASES = [  # dtype, Hq, Hkv, D, B, groups (shared blocks, member tails)
+    ("f16", 8, 8, 128, 16, [(64, [1, 40, 256, 0]), (3, [17, 1]), (0, [5, 9, 100]), (10, [33])]),
+    ("bf16", 4, 4, 64, 8, [(5, [1, 2, 3, 4, 5, 6, 7, 8]), (12, [60, 0])]),
+    ("bf16", 16, 8, 128, 32, [(4, [16, 33, 1, 64]), (2, [31])]),
+    ("f16", 8, 2, 128, 16, [(9, [7, 70]), (1, [1, 2])]),
+    ("bf16", 16, 2, 64, 16, [(3, [50])]),  # G = 8: one member per group
+]
+
+
+@pytest.mark.parametrize("step", [False, True])
+@pytest.mark.parametrize("dt,Hq,Hkv,D,B,groups", GROUP_CASES)
+def test_beam_groups_match_oracle(dt, Hq, Hkv, D, B, groups, step):
+    if step:  # a decode step needs a new token in each member's own tail
+        groups = [(nsh, [max(t, 1) for t in tails]) for nsh, tails in groups]
+    q, kc, vc, bt, cl, gs, nk, nv = make_group_case(dt, Hq, Hkv, D, B, groups, seed=Hq + B + D,
+                                                    step=step)
+    scale = D ** -0.5
+    sh = pkv.group_shared_tokens(bt, cl, gs, B)
+    for i, (nsh, tails) in enumerate(groups):  # the helper finds the shared blocks
+        expect = min(nsh * B, min(nsh * B + t for t in tails)) if len(tails) > 1 else \
+            nsh * B + tails[0]
+        assert int(sh[i]) == expect
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=DEV)
+    pkv.paged_decode_grouped(out, q.to(DEV), kd, vd, bt.to(DEV), cl.to(DEV), gs.to(DEV),
+                             sh.to(DEV), scale, B, Hkv,
+                             new_k=nk.to(DEV) if step else None,
+                             new_v=nv.to(DEV) if step else None)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    if step:
+        k_ref, v_ref = kc.clone(), vc.clone()
+        ref = oracle.decode_step(q, nk, nv, k_ref, v_ref, bt, cl, scale, B, Hkv)
+        assert torch.equal(bits(kd), bits(k_ref)) and torch.equal(bits(vd), bits(v_ref))
+    else:
+        ref = oracle.paged_decode_attention(q, kc, vc, bt, cl, scale, B, Hkv)
+    assert max_err(out, ref) <= TOL16
+
+
+def test_beam_groups_equal_ungrouped_step_and_flag_oversized_groups():
+    groups = [(20, [3, 90, 1, 17]), (6, [40, 41])]
+    q, kc, vc, bt, cl, gs, nk, nv = make_group_case("f16", 8, 8, 128, 16, groups, seed=3,
+                                                    step=True)
+    sh = pkv.group_shared_tokens(bt, cl, gs, 16)
+    k1, v1 = kc.to(DEV), vc.to(DEV)
+    k2, v2 = k1.clone(), v1.clone()
+    o1 = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+    o2 = torch.empty_like(o1)
+    pkv.paged_decode_grouped(o1, q.to(DEV), k1, v1, bt.to(DEV), cl.to(DEV), gs.to(DEV),
+                             sh.to(DEV), 128 ** -0.5, 16, 8, new_k=nk.to(DEV), new_v=nv.to(DEV))
+    pkv.decode_step(o2, q.to(DEV), nk.to(DEV), nv.to(DEV), k2, v2, bt.to(DEV), cl.to(DEV),
+                    128 ** -0.5, 16, 8)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    assert torch.equal(bits(k1), bits(k2)) and torch.equal(bits(v1), bits(v2))
+    assert float((o1 - o2).abs().max()) <= TOL16
+    # six members with two query heads each (G = 2) need 12 > 8 columns: the
+    # group is skipped and flagged
+    q6, kc6, vc6, bt6, cl6, gs6, _, _ = make_group_case(
+        "f16", 16, 8, 128, 16, [(4, [1, 2, 3, 4, 5, 6])], seed=4, step=False)
+    out = torch.full(q6.shape, 7.0, dtype=torch.float32, device=DEV)
+    pkv.paged_decode_grouped(out, q6.to(DEV), kc6.to(DEV), vc6.to(DEV), bt6.to(DEV),
+                             cl6.to(DEV), gs6.to(DEV),
+                             pkv.group_shared_tokens(bt6, cl6, gs6, 16).to(DEV),
+                             128 ** -0.5, 16, 8)
+    torch.cuda.synchronize()
+    assert pkv.device_status() & 2  # bad context length / group
+    assert bool((out == 7.0).all())  # nothing written for the skipped group
+    pkv.device_status(reset=True)
