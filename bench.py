@@ -43,8 +43,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
 # valid only while the kernel source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "c9d2461bec1c6577",
-           "bytes_per_launch": {"2": 1109470976, "3": 806885376, "4": 1089196800}}
+TRAFFIC = {"source_sha": "a401f23a0d238703",
+           "bytes_per_launch": {"2": 1109416448, "3": 806718976, "4": 1089934592}}
 
 
 def launch_partition(w, max_blocks: int) -> int:
