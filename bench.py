@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -43,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
 # valid only while the kernel source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "a401f23a0d238703",
+TRAFFIC = {"source_sha": "3fabd6e647d79553",
            "bytes_per_launch": {"2": 1109416448, "3": 806718976, "4": 1089934592}}
 
 
@@ -58,11 +59,15 @@ def launch_partition(w, max_blocks: int) -> int:
 
 
 def kernel_sha() -> str:
-    """Hash of the decode kernel's sources (the traffic figures above hold
-    only for the kernel they were captured from)."""
+    """Hash of the decode kernel's sources, comments and blank space left out
+    (the traffic figures above hold only for the code they were captured
+    from)."""
     h = hashlib.sha256()
     for name in ("decode_tc.cu", "decode_tc.cuh", "tc_common.cuh"):
-        h.update(open(os.path.join(ROOT, "paged_kv_cache_312_gb300", "csrc", name), "rb").read())
+        text = open(os.path.join(ROOT, "paged_kv_cache_312_gb300", "csrc", name)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -14,25 +14,35 @@
 //    a sequence's end exit at once.  All G <= 8 query heads of the KV group
 //    ride along, so every K/V tile is read from HBM once per group (auturnal
 //    guide section 1: GQA/MQA shrink the KV head count).
-//  * A stage is 16 tokens of K and V.  A 2-D TMA tensor map views a cache as
-//    [NB*Hkv*B rows][D cols]; one cp.async.bulk.tensor per 64-column half
-//    (and per block for B = 8) lands a stage in shared memory with the
-//    128-byte swizzle and completes on an mbarrier.  Each of the 4 warps
+//  * A stage is 16 tokens of K and V.  A 3-D TMA tensor map views a cache as
+//    [D/64 column halves][NB*Hkv*B rows][64 cols] (the halves' stride, 128
+//    bytes, is below the rows'); one cp.async.bulk.tensor per block of the
+//    stage lands it in shared memory, half after half, with the 128-byte
+//    swizzle, and completes on an mbarrier.  Each of the 4 warps
 //    streams every 4th stage of its CTA's partition (or every stage of its
 //    own partition) through its own ring of NS stages; its lane 0
 //    issues loads NS stages ahead.  Block ids are fetched 32 stages at a time
 //    (one per lane) and broadcast by shuffle.  Three CTAs share an SM, so one
 //    CTA's start-up latency hides behind the others' streaming.
 //  * Q K^T runs on mma.sync m16n8k16 with tokens on M, the group's query heads
-//    on N (8) and head_dim on K; movmatrix turns the score fragment into the
-//    P^T operand of P V, which accumulates O^T in fp32.  P is split into a
-//    16-bit high part and a 16-bit remainder (~16 significant bits).
-//  * Online softmax in base 2 (fp32); the warps of a partition merge through
+//    on N (8) and head_dim on K (two independent accumulation chains);
+//    movmatrix turns the score fragment into the P^T operand of P V, which
+//    accumulates O^T in fp32.  P is split into a 16-bit high part and a
+//    16-bit remainder (~16 significant bits).
+//  * Online softmax in base 2 (fp32) against a per-head reference max that
+//    moves only when a score passes it by more than 8, so most stages need
+//    neither a cross-lane max nor a rescale of O; the warps of a partition merge through
 //    shared memory (reusing the rings) at the end.  An unsplit item writes
 //    the output; a partition writes (max, sum, unnormalised output) to the
 //    workspace, the CTA bumps its (sequence, KV head) counter by its number
 //    of partitions, and the CTA that completes the count merges all
 //    partitions by log-sum-exp.
+//  * Beam groups (GR): one CTA per (group, KV head) attends every member of a
+//    group of sequences that share a prefix of physical blocks: the shared
+//    prefix once with all members' query heads as the N columns, then each
+//    member's own tail with the other columns masked (cayang0802 "Paged
+//    Attention" page, beam-search paragraph: the beams keep one physical
+//    copy of their common blocks).
 //  * Masked tokens (past context_len, or in a block whose id is out of range)
 //    get score -inf and a zeroed V fragment, so NaN or stale data in unused
 //    slots never reaches the output.
