@@ -907,3 +907,38 @@ def test_beam_groups_equal_ungrouped_step_and_flag_oversized_groups():
     assert pkv.device_status() & 2  # bad context length / group
     assert bool((out == 7.0).all())  # nothing written for the skipped group
     pkv.device_status(reset=True)
+
+
+def test_workload5_grouped_step_full_size():
+    # the benchmark's beam step through the beam-group call: CoW copy, then
+    # one launch that appends every beam's new token and attends the group
+    w = WORKLOADS[5]
+    case = make_beam_case(w, seed=1)
+    mgr = pkv.BlockAllocator(case.pool_blocks, w.block_size, free_order=case.pool_order)
+    pre, suf = beam_setup_schedule(mgr, case)
+    ids, slots, pairs, bt, cl = beam_step_schedule(mgr, case)
+    NB, Hkv, B, D = case.pool_blocks, w.num_kv_heads, w.block_size, w.head_dim
+    G, W = case.parents.shape
+    kh = torch.full((NB, Hkv, B, D), float("nan"), dtype=torch.float16)
+    vh = torch.full_like(kh, float("nan"))
+    keys = torch.cat([case.prefix_k.reshape(-1, Hkv, D)] + case.suffix_k)
+    vals = torch.cat([case.prefix_v.reshape(-1, Hkv, D)] + case.suffix_v)
+    all_slots = torch.cat([pre.reshape(-1)] + suf)
+    oracle.kv_write(kh, vh, keys, vals, all_slots, B)
+    oracle.kv_copy_blocks(kh, vh, pairs)
+    kc, vc = kh.to(DEV), vh.to(DEV)  # history and copies in place; new tokens not yet
+    gs = torch.arange(0, G * W + 1, W, dtype=torch.int32)
+    sh = pkv.group_shared_tokens(bt, cl, gs, B)
+    assert int(sh.min()) >= w.prefix_len  # every group shares at least its prompt
+    out = torch.full(case.q.shape, float("nan"), dtype=torch.float32, device=DEV)
+    pkv.paged_decode_grouped(out, case.q.to(DEV), kc, vc, bt.to(DEV), cl.to(DEV), gs.to(DEV),
+                             sh.to(DEV), w.scale, B, Hkv, new_k=case.new_key.to(DEV),
+                             new_v=case.new_value.to(DEV))
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    oracle.kv_write(kh, vh, case.new_key, case.new_value, slots, B)
+    assert torch.equal(bits(kc), bits(kh)) and torch.equal(bits(vc), bits(vh))
+    idx = pick(cl.tolist())
+    ref = sampled_oracle(case.q, kh, vh, bt, cl, w, idx)
+    assert max_err(out[idx], ref) <= TOL16
+    assert bool(torch.isfinite(out).all())
