@@ -193,7 +193,9 @@ int pkv_decode_step(void* out, const void* q, const void* new_k, const void* new
  *                 group i is sequences group_start[i] .. group_start[i+1]-1
  *                 (consecutive), with 1 <= members and members * G <= 8
  *                 (G = num_heads / num_kv_heads).  A group outside these
- *                 bounds is skipped and sets PKV_STATUS_BAD_LEN.
+ *                 bounds is skipped and sets PKV_STATUS_BAD_LEN.  Sequences
+ *                 in no group are not attended: their output rows (and, in a
+ *                 decode step, their caches) are left as they were.
  * shared_tokens : int32 [num_groups], device memory: the first
  *                 shared_tokens[i] positions of every member of group i lie
  *                 in the same physical blocks (same table entries), e.g. from

@@ -942,3 +942,26 @@ def test_workload5_grouped_step_full_size():
     ref = sampled_oracle(case.q, kh, vh, bt, cl, w, idx)
     assert max_err(out[idx], ref) <= TOL16
     assert bool(torch.isfinite(out).all())
+
+
+def test_beam_groups_empty_members_and_uncovered_sequences():
+    # a member with no tokens gets a zero row; sequences outside every group
+    # are not touched
+    groups = [(2, [0, 30, 5]), (0, [0]), (3, [7, 9])]
+    q, kc, vc, bt, cl, gs, _, _ = make_group_case("bf16", 8, 8, 128, 16, groups, seed=8,
+                                                  step=False)
+    cl = cl.clone()
+    cl[0] = 0  # first member of group 0: empty
+    gs_part = gs[:3].clone()  # groups 0 and 1 only; group 2's sequences uncovered
+    sh = pkv.group_shared_tokens(bt, cl, gs_part, 16)
+    assert int(sh[0]) == 0  # the empty member shares nothing
+    out = torch.full(q.shape, 5.0, dtype=torch.float32, device=DEV)
+    pkv.paged_decode_grouped(out, q.to(DEV), kc.to(DEV), vc.to(DEV), bt.to(DEV), cl.to(DEV),
+                             gs_part.to(DEV), sh.to(DEV), 128 ** -0.5, 16, 8)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    ref = oracle.paged_decode_attention(q, kc, vc, bt, cl, 128 ** -0.5, 16, 8)
+    covered = int(gs_part[-1])
+    assert max_err(out[:covered], ref[:covered]) <= TOL16
+    assert bool((out[0] == 0).all())
+    assert bool((out[covered:] == 5.0).all())
