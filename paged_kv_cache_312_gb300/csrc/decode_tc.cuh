@@ -604,9 +604,15 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     __shared__ int is_last;
     __syncthreads();  // this CTA's partition results are written ...
     if (threadIdx.x == 0) {
-        __threadfence();  // ... and published before the count goes up
-        is_last = atomicAdd(&p.done[sg], (unsigned)np_cta) == (unsigned)(nparts - np_cta);
-        if (is_last) __threadfence();  // see every other partition's results
+        // release: this CTA's partition results (ordered before this thread by
+        // the barrier) are visible before the count goes up; acquire for the
+        // CTA that completes the count: it sees every other partition's results
+        unsigned prev;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+                     : "=r"(prev)
+                     : "l"(&p.done[sg]), "r"((unsigned)np_cta)
+                     : "memory");
+        is_last = prev == (unsigned)(nparts - np_cta);
     }
     __syncthreads();
     if (!is_last) return;
