@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
 # valid only while the kernel source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "3fabd6e647d79553",
-           "bytes_per_launch": {"2": 1109416448, "3": 806718976, "4": 1089934592}}
+TRAFFIC = {"source_sha": "a9bc91e1ce02f08f",
+           "bytes_per_launch": {"2": 1109129216, "3": 806961408, "4": 1089678592}}
 
 
 def launch_partition(w, max_blocks: int) -> int:
