@@ -205,7 +205,9 @@ int pkv_decode_step(void* out, const void* q, const void* new_k, const void* new
  * new_k, new_v  : NULL for attention only; else as in pkv_decode_step, each
  *                 new token in a block private to its sequence.
  * Other arguments as in pkv_decode_step; not split (no partition_size or
- * workspace).  Needs the tensor-core kernel: 16-bit KV, G <= 8, kernel
+ * workspace): one CTA streams a whole group for one KV head, so with few
+ * groups and long contexts the split, ungrouped pkv_decode_step keeps more of
+ * the GPU busy.  Needs the tensor-core kernel: 16-bit KV, G <= 8, kernel
  * choice PKV_KERNEL_AUTO (else PKV_ERR_UNSUPPORTED).
  */
 int pkv_paged_decode_grouped(void* out, const void* q, const void* new_k, const void* new_v,
