@@ -737,13 +737,16 @@ def run_reference(args):
         oracle.kv_write(kc, vc, st.setup_keys, st.setup_vals, st.setup_slots, w.block_size)
     S = st.q.shape[0]
     L = st.lens.to(torch.int64)
-    # bounded sample: time one full pass, keep a prefix of sequences ~2 s/step
+    # bounded sample: time one pass over a few sequences, then keep a prefix of
+    # the step's sequences sized so that the whole run (warm-up and timed
+    # steps) takes about two minutes, and no step more than 2 s
     t = time.perf_counter()
     oracle.paged_decode_attention(st.q[:min(S, n)], kc, vc, st.tables[:min(S, n)],
                                   st.lens[:min(S, n)], w.scale, w.block_size, w.num_kv_heads,
                                   nthreads=n)
     per_seq = (time.perf_counter() - t) / min(S, n)
-    m = int(max(1, min(S, 2.0 / max(per_seq, 1e-6))))
+    step_budget = min(2.0, 120.0 / max(1, args.steps + args.warmup))
+    m = int(max(1, min(S, step_budget / max(per_seq, 1e-6))))
     idx = torch.arange(m)
     sample_bytes = int(L[idx].sum()) * 2 * w.num_kv_heads * w.head_dim * w.torch_dtype.itemsize
 
