@@ -468,7 +468,7 @@ def cpu_baseline(st, budget_s=8.0):
 
 
 SWEEP_BLOCKS = (8, 16, 32)
-SWEEP_GROUPS = (1, 4, 8)
+SWEEP_GROUPS = (1, 4, 8, 16, 32, 64)
 SWEEP_DIMS = (64, 128)
 
 

@@ -139,8 +139,10 @@ int pkv_kv_write(void* k_cache, void* v_cache, const void* key, const void* valu
  *                workspace must not overlap on the GPU.
  * Supported: block_size in {8,16,32}; head_dim in {64,128}; num_heads a
  * multiple of num_kv_heads; out_dtype any of the three.  16-bit KV with
- * num_heads/num_kv_heads <= 8 runs on the tensor-core kernel, the rest on a
- * CUDA-core kernel; both accumulate in fp32.
+ * G = num_heads/num_kv_heads <= 256 runs on the tensor-core kernel (one CTA
+ * carries up to 16 query heads of a KV group; a wider group is cut into
+ * ceil(G/16) head slices, each reading the group's K/V), the rest (fp32 KV)
+ * on a CUDA-core kernel; both accumulate in fp32.
  */
 int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
                                const void* v_cache, const int32_t* block_tables,

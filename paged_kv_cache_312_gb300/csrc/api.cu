@@ -422,6 +422,7 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
     p.num_groups = 0;
     const int max_ctx = max_blocks_per_seq * block_size;
     p.cta_parts = 1;
+    p.head_slices = 1;
     if (partition_size == 0) {
         p.partition_tokens = max_ctx;
         p.max_partitions = 1;
@@ -448,8 +449,10 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int G = num_heads / num_kv_heads;
+    // wider KV groups are cut into head slices of <= 16 columns (each slice
+    // reads the group's K/V; adjacent in the grid, the repeats meet in L2)
     const bool tensor_core =
-        g_decode_kernel == PKV_KERNEL_AUTO && kv_dtype != PKV_F32 && G <= 8;
+        g_decode_kernel == PKV_KERNEL_AUTO && kv_dtype != PKV_F32 && G <= 256;
     cudaError_t e;
     if (tensor_core) {
         CUtensorMap kmap, vmap;
@@ -476,19 +479,24 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
         if (p.partition_tokens <= kWarpPartitionMaxTokens &&
             p.max_partitions >= kWarpPartitionMinCount)
             p.cta_parts = kDecodeTcWarps;
+        p.head_slices = (G + kDecodeTcMaxColumns - 1) / kDecodeTcMaxColumns;
+        const int columns = (G + p.head_slices - 1) / p.head_slices;
         const long long groups = (p.max_partitions + p.cta_parts - 1) / p.cta_parts;
-        const long long grid = (long long)num_seqs * num_kv_heads * groups;
+        const long long grid = (long long)num_seqs * num_kv_heads * p.head_slices * groups;
         if (grid >= (1ll << 31))
             return pkv_fail(PKV_ERR_SHAPE, "%s: more than 2^31 work items", fn);
         if (p.max_partitions > 1) {
             // completion counters for the in-kernel merge start at zero
-            e = cudaMemsetAsync(p.done, 0, sizeof(unsigned) * (size_t)num_seqs * num_kv_heads, st);
+            e = cudaMemsetAsync(p.done, 0,
+                                sizeof(unsigned) * (size_t)num_seqs * num_kv_heads * p.head_slices,
+                                st);
             if (e != cudaSuccess) return cuda_fail(e, fn);
         }
         // the tensor-core kernel writes the new tokens itself
         p.new_k = new_k;
         p.new_v = new_v;
-        e = launch_decode_tensor_core(p, kv_dtype, &kmap, &vmap, grid, st);
+        e = columns > 8 ? launch_decode_tensor_core_wide(p, kv_dtype, &kmap, &vmap, grid, st)
+                        : launch_decode_tensor_core(p, kv_dtype, &kmap, &vmap, grid, st);
         if (e != cudaSuccess) return cuda_fail(e, fn);
         return PKV_OK;
     }

@@ -11,9 +11,12 @@
 //    consecutive partitions when they are short (<= 512 tokens, one per
 //    warp, so that a CTA's start-up and end are spread over more bytes); the
 //    slots of one (sequence, KV head) are adjacent in the grid and slots past
-//    a sequence's end exit at once.  All G <= 8 query heads of the KV group
-//    ride along, so every K/V tile is read from HBM once per group (auturnal
-//    guide section 1: GQA/MQA shrink the KV head count).
+//    a sequence's end exit at once.  The query heads of the KV group ride
+//    along as the mma's N columns, so every K/V tile is read from HBM once
+//    per group (auturnal guide section 1: GQA/MQA shrink the KV head count):
+//    one n8 tile for G <= 8, two for G <= 16 (NT = 2); a wider group is cut
+//    into head slices of at most 16 columns, one CTA each, adjacent in the
+//    grid so that the slices' repeated reads of a tile meet in L2.
 //  * A stage is 16 tokens of K and V.  A 3-D TMA tensor map views a cache as
 //    [D/64 column halves][NB*Hkv*B rows][64 cols] (the halves' stride, 128
 //    bytes, is below the rows'); one cp.async.bulk.tensor per block of the
@@ -25,7 +28,7 @@
 //    (one per lane) and broadcast by shuffle.  Three CTAs share an SM, so one
 //    CTA's start-up latency hides behind the others' streaming.
 //  * Q K^T runs on mma.sync m16n8k16 with tokens on M, the group's query heads
-//    on N (8) and head_dim on K (two independent accumulation chains);
+//    on N (8 per tile) and head_dim on K (independent accumulation chains);
 //    movmatrix turns the score fragment into the P^T operand of P V, which
 //    accumulates O^T in fp32.  P is split into a 16-bit high part and a
 //    16-bit remainder (~16 significant bits).
@@ -65,8 +68,9 @@ using namespace pkv_tc;
 
 // ---- compile-time geometry -----------------------------------------------------
 
-template <int D, int B, int NW, int NS>
+template <int D, int B, int NW, int NS, int NT = 1>
 struct Geometry {
+    static constexpr int NC = 8 * NT;                // query-head columns (n8 tiles x 8)
     static constexpr int ROWS = B < 16 ? B : 16;     // rows per TMA box
     static constexpr int IDS = 16 / ROWS;            // physical blocks per 16-token stage
     static constexpr int NH = D / 64;                // 128-byte column halves
@@ -74,7 +78,7 @@ struct Geometry {
     static constexpr int KV_BYTES = 16 * D * 2;      // K (or V) of a 16-token stage
     static constexpr int STAGE_BYTES = 2 * KV_BYTES;
     static constexpr int RING_BYTES = NS * STAGE_BYTES;
-    static constexpr int MERGE_BYTES = NW * 8 * (D + 2) * 4;
+    static constexpr int MERGE_BYTES = NW * NC * (D + 2) * 4;
     static constexpr int DATA_BYTES =
         NW * RING_BYTES > MERGE_BYTES ? NW * RING_BYTES : MERGE_BYTES;  // merge reuses rings
     static constexpr int BAR_OFF = DATA_BYTES;
@@ -84,8 +88,14 @@ struct Geometry {
     static constexpr int SID_INTS = 8;
     static constexpr int SMEM_BYTES = 1024 /*align slack*/ + SID_OFF + NW * NS * SID_INTS * 4;
     // partition weights cached for the in-kernel merge (after the warp merge)
-    static constexpr int WCACHE = ((DATA_BYTES - MERGE_BYTES) / 4 - 16 - NW * 32 * 4 - 4) & ~3;
+    static constexpr int WCACHE = ((DATA_BYTES - MERGE_BYTES) / 4 - 2 * NC - NW * 32 * 4 - 4) & ~3;
     static_assert(WCACHE > 0, "room for merge weights");
+    // CTAs per SM the register allocation is held to (0: the compiler's
+    // choice).  The shared memory admits 3 CTAs at D = 128 (~66 KB each),
+    // which the compiler's choice already fits; at D = 64 it admits 6 (~34
+    // KB), and there the compiler's choice would spill, so the bound is 6
+    // CTAs, or 5 for two column tiles (96 registers a thread)
+    static constexpr int MIN_CTAS = D == 128 ? 0 : (NT == 1 ? 6 : 5);
     static_assert(SUB_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
     static_assert(STAGE_BYTES % 1024 == 0 && RING_BYTES % 1024 == 0, "stage alignment");
 };
@@ -107,12 +117,13 @@ __device__ __forceinline__ uint32_t stage_offset(int r, int c)
 // ...) through rings of NS stages each, merging their softmax states at the
 // end; or, for short split partitions, up to NW consecutive partitions, one
 // per warp, each warp's state being its partition's result.
-template <typename T, int D, int B, int NW, int NS, bool GR>
-__global__ void __launch_bounds__(NW * 32)
+template <typename T, int D, int B, int NW, int NS, bool GR, int NT>
+__global__ void __launch_bounds__(NW * 32, (Geometry<D, B, NW, NS, NT>::MIN_CTAS))
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap)
 {
-    using Gm = Geometry<D, B, NW, NS>;
+    using Gm = Geometry<D, B, NW, NS, NT>;
+    constexpr int NC = Gm::NC;      // query-head columns of the mma's N (8 per tile)
     constexpr int KSTEPS = D / 16;  // Q K^T k-steps
     constexpr int MTILES = D / 16;  // P V m-tiles (head_dim rows)
     constexpr int IDS = Gm::IDS;    // physical blocks per stage (2 when B = 8)
@@ -120,6 +131,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.num_heads / p.num_kv_heads;
     int s, g, sg, L, nparts, p0, np_cta, wpp, wsub, part, begin, end, nst;
+    // this CTA's query heads: g*G + hb .. + ncol - 1 (all of the KV group,
+    // or one slice of at most NC of them when the group is wider)
+    int hb = 0, ncol;
     bool solo;
     // Beam groups (GR): one CTA per (group, KV head).  The group's members
     // are sequences s0 .. s0 + nm - 1 whose first `shared` tokens sit in the
@@ -133,7 +147,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         g = blockIdx.x - gi * p.num_kv_heads;
         s0 = p.group_start[gi];
         nm = p.group_start[gi + 1] - s0;
-        if (nm < 1 || nm * G > 8 || s0 < 0 || s0 + nm > p.num_seqs) {
+        if (nm < 1 || nm * G > NC || s0 < 0 || s0 + nm > p.num_seqs) {
             if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
             return;
         }
@@ -159,6 +173,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             if (m < nm) nst += (Lm[m] - shared + 15) / 16;
         s = s0;
         sg = 0;
+        ncol = nm * G;
         L = Lm[0];
         nparts = 1;
         p0 = 0;
@@ -170,13 +185,19 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         begin = 0;
         end = 0;
     } else {
-        // ---- which item: slot b = ((s * Hkv) + g) * max_groups + grp; group
-        // grp holds partitions grp * cta_parts .. + cta_parts - 1 of (s, g)
+        // ---- which item: slot b = (((s * Hkv) + g) * HS + hs) * max_groups +
+        // grp; group grp holds partitions grp * cta_parts .. + cta_parts - 1
+        // of (s, g), for head slice hs of the KV group's query heads
         const int max_groups = (p.max_partitions + p.cta_parts - 1) / p.cta_parts;
         const int grp = blockIdx.x % max_groups;
         sg = blockIdx.x / max_groups;
-        s = sg / p.num_kv_heads;
-        g = sg - s * p.num_kv_heads;
+        const int HS = p.head_slices;
+        const int sgk = sg / HS, hs = sg - sgk * HS;
+        s = sgk / p.num_kv_heads;
+        g = sgk - s * p.num_kv_heads;
+        const int GC = (G + HS - 1) / HS;
+        hb = hs * GC;
+        ncol = min(GC, G - hb);
         L = p.context_lens[s];
         if (L < 0 || (int64_t)L > (int64_t)p.max_blocks * B) {
             if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
@@ -367,30 +388,39 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     if (cnt > 0) load_window(0);
     for (int j = 0; j < NS && j < cnt; ++j) issue(j);
 
-    // ---- Q^T as the B operand of Q K^T: column n = query head g*G + n (GR:
-    // member n / G, query head g*G + n % G).
-    uint32_t qb[KSTEPS][2];
-    {
-        const int n = gq;
-        const int mn = GR ? n / G : 0, hn = GR ? n - mn * G : n;
-        const bool col = GR ? mn < nm : n < G;
+    // ---- Q^T as the B operand of Q K^T: column n (tile n / 8) = query head
+    // g*G + hb + n (GR: member n / G, query head g*G + n % G); columns past
+    // ncol are zero.
+    uint32_t qb[NT][KSTEPS][2];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const int n = 8 * t + gq;
+        const int mn = GR ? n / G : 0, hn = GR ? n - mn * G : hb + n;
+        const bool col = n < ncol;
         const T* qrow = static_cast<const T*>(p.q) +
-                        ((size_t)(GR ? s0 + min(mn, nm - 1) : s) * p.num_heads + g * G + hn) * D;
+                        ((size_t)(GR ? s0 + min(mn, nm - 1) : s) * p.num_heads + g * G +
+                         (col ? hn : 0)) * D;
 #pragma unroll
         for (int kk = 0; kk < KSTEPS; ++kk) {
             if (col) {
-                qb[kk][0] = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * tq);
-                qb[kk][1] = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * tq);
+                qb[t][kk][0] = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * tq);
+                qb[t][kk][1] = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * tq);
             } else {
-                qb[kk][0] = qb[kk][1] = 0u;
+                qb[t][kk][0] = qb[t][kk][1] = 0u;
             }
         }
     }
 
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2tq, 2tq+1
-    float acc[MTILES][4];
+    // softmax state of columns 8t + 2tq (index 0) and 8t + 2tq + 1 (index 1)
+    float mr[NT][2], lr_[NT][2];
+    float acc[NT][MTILES][4];
 #pragma unroll
-    for (int i = 0; i < MTILES; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int t = 0; t < NT; ++t) {
+        mr[t][0] = mr[t][1] = -INFINITY;
+        lr_[t][0] = lr_[t][1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < MTILES; ++i) acc[t][i][0] = acc[t][i][1] = acc[t][i][2] = acc[t][i][3] = 0.f;
+    }
     const float sl = p.scale_log2;
     const int lj = lane >> 3, lr = lane & 7;
     const int k_row = (lj & 1) * 8 + lr, k_chunk_add = lj >> 1;  // K: non-transposed A
@@ -420,71 +450,95 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         };
         const bool all_valid = tok0 + 16 <= endr && id0 >= 0 && id1 >= 0;
 
-        // ---- S^T = K Q^T  (16 tokens x 8 heads), as two independent
-        // accumulation chains (even and odd k-steps)
-        float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- S^T = K Q^T  (16 tokens x 8 heads per tile); with one tile, as
+        // two independent accumulation chains (even and odd k-steps)
+        float sc[NT][4], sd[NT][4];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = sd[t][0] = sd[t][1] = sd[t][2] =
+                sd[t][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < KSTEPS; ++kk) {
             uint32_t a[4];
             ldsm_x4(kbase + stage_offset<D, B, NW, NS>(k_row, 2 * kk + k_chunk_add), a);
-            if (kk & 1)
-                Mma<T>::run(sd, a, qb[kk][0], qb[kk][1]);
-            else
-                Mma<T>::run(sc, a, qb[kk][0], qb[kk][1]);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                if (NT == 1 && (kk & 1))
+                    Mma<T>::run(sd[t], a, qb[t][kk][0], qb[t][kk][1]);
+                else
+                    Mma<T>::run(sc[t], a, qb[t][kk][0], qb[t][kk][1]);
+            }
         }
-        float x0 = (sc[0] + sd[0]) * sl, x1 = (sc[1] + sd[1]) * sl;
-        float x2 = (sc[2] + sd[2]) * sl, x3 = (sc[3] + sd[3]) * sl;
-        if (!all_valid) {
-            if (!valid(gq)) x0 = x1 = -INFINITY;
-            if (!valid(gq + 8)) x2 = x3 = -INFINITY;
-        }
-        if constexpr (GR) {
-            // a member's own tail: the other members' columns see nothing
-            const int mem = sinfo[4];
-            if (mem >= 0) {
-                if ((2 * tq) / G != mem) x0 = x2 = -INFINITY;
-                if ((2 * tq + 1) / G != mem) x1 = x3 = -INFINITY;
+        // x[t][0..3]: (token gq, column 8t+2tq), (gq, +1), (gq+8, 8t+2tq), (gq+8, +1)
+        float x[NT][4];
+        const bool vg = all_valid || valid(gq), vg8 = all_valid || valid(gq + 8);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[t][e] = (sc[t][e] + sd[t][e]) * sl;
+            if (!vg) x[t][0] = x[t][1] = -INFINITY;
+            if (!vg8) x[t][2] = x[t][3] = -INFINITY;
+            if constexpr (GR) {
+                // a member's own tail: the other members' columns see nothing
+                const int mem = sinfo[4];
+                if (mem >= 0) {
+                    if ((8 * t + 2 * tq) / G != mem) x[t][0] = x[t][2] = -INFINITY;
+                    if ((8 * t + 2 * tq + 1) / G != mem) x[t][1] = x[t][3] = -INFINITY;
+                }
             }
         }
         // ---- online softmax in base 2 against a reference max per head that
         // moves only when a score passes it by more than 8 (so p <= 2^8): most
         // stages need neither the max over the 8 row groups nor a rescale of O
-        const bool up = fmaxf(x0, x2) > m0 + 8.f || fmaxf(x1, x3) > m1 + 8.f;
+        bool up = false;
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            up = up || fmaxf(x[t][0], x[t][2]) > mr[t][0] + 8.f ||
+                 fmaxf(x[t][1], x[t][3]) > mr[t][1] + 8.f;
         if (__any_sync(0xffffffffu, up)) {
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            // 0 while m is -inf (nothing accumulated yet), 1 if m stays
-            const float al0 = mn0 == -INFINITY ? 1.f : ex2(m0 - mn0);
-            const float al1 = mn1 == -INFINITY ? 1.f : ex2(m1 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            l0 *= al0;
-            l1 *= al1;
+            for (int t = 0; t < NT; ++t) {
+                float mx0 = fmaxf(x[t][0], x[t][2]), mx1 = fmaxf(x[t][1], x[t][3]);
 #pragma unroll
-            for (int i = 0; i < MTILES; ++i) {
-                acc[i][0] *= al0;
-                acc[i][1] *= al1;
-                acc[i][2] *= al0;
-                acc[i][3] *= al1;
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                const float mn0 = fmaxf(mr[t][0], mx0), mn1 = fmaxf(mr[t][1], mx1);
+                // 0 while m is -inf (nothing accumulated yet), 1 if m stays
+                const float al0 = mn0 == -INFINITY ? 1.f : ex2(mr[t][0] - mn0);
+                const float al1 = mn1 == -INFINITY ? 1.f : ex2(mr[t][1] - mn1);
+                mr[t][0] = mn0;
+                mr[t][1] = mn1;
+                lr_[t][0] *= al0;
+                lr_[t][1] *= al1;
+#pragma unroll
+                for (int i = 0; i < MTILES; ++i) {
+                    acc[t][i][0] *= al0;
+                    acc[t][i][1] *= al1;
+                    acc[t][i][2] *= al0;
+                    acc[t][i][3] *= al1;
+                }
             }
         }
-        const float ms0 = m0 == -INFINITY ? 0.f : m0;
-        const float ms1 = m1 == -INFINITY ? 0.f : m1;
-        const float p0 = ex2(x0 - ms0), p1 = ex2(x1 - ms1);
-        const float p2 = ex2(x2 - ms0), p3 = ex2(x3 - ms1);
-        l0 += p0 + p2;
-        l1 += p1 + p3;
         // ---- P^T operand (tokens 2tq.. x head gq) via an in-register transpose
-        uint32_t h01, l01, h23, l23;
-        Mma<T>::split(p0, p1, h01, l01);
-        Mma<T>::split(p2, p3, h23, l23);
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+        uint32_t bh0[NT], bh1[NT], bl0[NT], bl1[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const float ms0 = mr[t][0] == -INFINITY ? 0.f : mr[t][0];
+            const float ms1 = mr[t][1] == -INFINITY ? 0.f : mr[t][1];
+            const float p0 = ex2(x[t][0] - ms0), p1 = ex2(x[t][1] - ms1);
+            const float p2 = ex2(x[t][2] - ms0), p3 = ex2(x[t][3] - ms1);
+            lr_[t][0] += p0 + p2;
+            lr_[t][1] += p1 + p3;
+            uint32_t h01, l01, h23, l23;
+            Mma<T>::split(p0, p1, h01, l01);
+            Mma<T>::split(p2, p3, h23, l23);
+            bh0[t] = movmatrix_trans(h01);
+            bh1[t] = movmatrix_trans(h23);
+            bl0[t] = movmatrix_trans(l01);
+            bl1[t] = movmatrix_trans(l23);
+        }
 
         bool v0 = true, v1 = true, v8 = true, v9 = true;
         if (!all_valid) {
@@ -504,8 +558,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                 a[2] = mask_pair(a[2], v8, v9);
                 a[3] = mask_pair(a[3], v8, v9);
             }
-            Mma<T>::run(acc[i], a, bh0, bh1);
-            Mma<T>::run(acc[i], a, bl0, bl1);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                Mma<T>::run(acc[t][i], a, bh0[t], bh1[t]);
+                Mma<T>::run(acc[t][i], a, bl0[t], bl1[t]);
+            }
         }
         __syncwarp();
         if (j + NS < cnt) {
@@ -516,65 +573,75 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
 
     // ---- per-warp sums over the 8 row groups
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            lr_[t][0] += __shfl_xor_sync(0xffffffffu, lr_[t][0], o);
+            lr_[t][1] += __shfl_xor_sync(0xffffffffu, lr_[t][1], o);
+        }
     }
 
-    const size_t hbase = (size_t)s * p.num_heads + (size_t)g * G;
+    const size_t hbase = (size_t)s * p.num_heads + (size_t)g * G + hb;
     if (!solo) {
         // ---- a warp's own partition: its softmax state is the partition's
-        // result, written straight to the workspace (heads 2tq and 2tq + 1)
+        // result, written straight to the workspace (columns 8t+2tq, +1)
         if (warp < np_cta) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int n = 2 * tq + h;
-                if (n >= G) break;
-                const size_t slot = (hbase + n) * p.max_partitions + part;
-                if (gq == 0) p.ws_ml[slot] = make_float2(h ? m1 : m0, h ? l1 : l0);
-                float* o = p.ws_o + slot * D;
+            for (int t = 0; t < NT; ++t) {
 #pragma unroll
-                for (int i = 0; i < MTILES; ++i) {
-                    o[16 * i + gq] = acc[i][h];
-                    o[16 * i + gq + 8] = acc[i][2 + h];
+                for (int h = 0; h < 2; ++h) {
+                    const int n = 8 * t + 2 * tq + h;
+                    if (n < ncol) {
+                        const size_t slot = (hbase + n) * p.max_partitions + part;
+                        if (gq == 0) p.ws_ml[slot] = make_float2(mr[t][h], lr_[t][h]);
+                        float* o = p.ws_o + slot * D;
+#pragma unroll
+                        for (int i = 0; i < MTILES; ++i) {
+                            o[16 * i + gq] = acc[t][i][h];
+                            o[16 * i + gq + 8] = acc[t][i][2 + h];
+                        }
+                    }
                 }
             }
         }
     } else {
         // ---- merge the warps (shared memory reused once every ring is drained)
         __syncthreads();
-        float* wm = reinterpret_cast<float*>(smem) + warp * 8 * (D + 2);  // [8][D], m[8], l[8]
-        if (gq == 0) {
-            wm[8 * D + 2 * tq] = m0;
-            wm[8 * D + 2 * tq + 1] = m1;
-            wm[8 * D + 8 + 2 * tq] = l0;
-            wm[8 * D + 8 + 2 * tq + 1] = l1;
-        }
+        float* wm = reinterpret_cast<float*>(smem) + warp * NC * (D + 2);  // [NC][D], m[NC], l[NC]
 #pragma unroll
-        for (int i = 0; i < MTILES; ++i) {
-            wm[(2 * tq) * D + 16 * i + gq] = acc[i][0];
-            wm[(2 * tq + 1) * D + 16 * i + gq] = acc[i][1];
-            wm[(2 * tq) * D + 16 * i + gq + 8] = acc[i][2];
-            wm[(2 * tq + 1) * D + 16 * i + gq + 8] = acc[i][3];
+        for (int t = 0; t < NT; ++t) {
+            const int n = 8 * t + 2 * tq;
+            if (gq == 0) {
+                wm[NC * D + n] = mr[t][0];
+                wm[NC * D + n + 1] = mr[t][1];
+                wm[NC * D + NC + n] = lr_[t][0];
+                wm[NC * D + NC + n + 1] = lr_[t][1];
+            }
+#pragma unroll
+            for (int i = 0; i < MTILES; ++i) {
+                wm[n * D + 16 * i + gq] = acc[t][i][0];
+                wm[(n + 1) * D + 16 * i + gq] = acc[t][i][1];
+                wm[n * D + 16 * i + gq + 8] = acc[t][i][2];
+                wm[(n + 1) * D + 16 * i + gq + 8] = acc[t][i][3];
+            }
         }
         __syncthreads();
         const float* sm = reinterpret_cast<const float*>(smem);
         // four consecutive outputs of one head per thread
         const bool vec_out = (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
-        const int ncol = GR ? nm * G : G;
         for (int idx = threadIdx.x; idx < ncol * D / 4; idx += blockDim.x) {
             const int n = idx / (D / 4), d = (idx - n * (D / 4)) * 4;
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * 8 * (D + 2) + 8 * D + n]);
+            for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * NC * (D + 2) + NC * D + n]);
             float den = 0.f;
             float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                const float* ww = sm + w * 8 * (D + 2);
-                const float mw = ww[8 * D + n];
+                const float* ww = sm + w * NC * (D + 2);
+                const float mw = ww[NC * D + n];
                 const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
-                den += wt * ww[8 * D + 8 + n];
+                den += wt * ww[NC * D + NC + n];
                 const float4 o = *reinterpret_cast<const float4*>(ww + n * D + d);
                 num.x += wt * o.x;
                 num.y += wt * o.y;
@@ -598,8 +665,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         if (nparts <= 1) return;
     }
 
-    // ---- split: the CTA that finishes the last partition of (s, g) merges
-    // them by log-sum-exp: M = max_i m_i, w_i = 2^(m_i - M),
+    // ---- split: the CTA that finishes the last partition of (s, g, head
+    // slice) merges them by log-sum-exp: M = max_i m_i, w_i = 2^(m_i - M),
     // out = sum_i w_i O_i / sum_i w_i l_i.
     __shared__ int is_last;
     __syncthreads();  // this CTA's partition results are written ...
@@ -616,13 +683,13 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     }
     __syncthreads();
     if (!is_last) return;
-    constexpr int NT = NW * 32;
-    float* wts = reinterpret_cast<float*>(smem) + NW * 8 * (D + 2);  // [G][nparts] weights
-    float* hinv = wts + Gm::WCACHE;                                    // [8]
-    float* hmax = hinv + 8;                                            // [8]
-    float4* red = reinterpret_cast<float4*>(hmax + 8);                 // [NT] partial sums
-    const bool cached = G * nparts <= Gm::WCACHE;
-    for (int n = warp; n < G; n += NW) {
+    constexpr int NTH = NW * 32;
+    float* wts = reinterpret_cast<float*>(smem) + NW * NC * (D + 2);  // [ncol][nparts] weights
+    float* hinv = wts + Gm::WCACHE;                                    // [NC]
+    float* hmax = hinv + NC;                                           // [NC]
+    float4* red = reinterpret_cast<float4*>(hmax + NC);                // [NTH] partial sums
+    const bool cached = ncol * nparts <= Gm::WCACHE;
+    for (int n = warp; n < ncol; n += NW) {
         const size_t base = (hbase + n) * p.max_partitions;
         // the (max, sum) pairs of the first 64 partitions are read once and
         // kept in registers for both passes; any further ones are re-read
@@ -661,11 +728,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         }
     }
     __syncthreads();
-    // Outputs in float4 units; when the group has fewer of them than
+    // Outputs in float4 units; when the slice has fewer of them than
     // threads, K threads share one output, each summing every K-th partition.
-    const int O4 = G * D / 4;
-    const int K = O4 >= NT ? 1 : NT / O4;
-    for (int o0 = 0; o0 < O4; o0 += NT) {
+    const int O4 = ncol * D / 4;
+    const int K = O4 >= NTH ? 1 : NTH / O4;
+    for (int o0 = 0; o0 < O4; o0 += NTH) {
         const int t = threadIdx.x;
         const int o = o0 + (K == 1 ? t : t % O4), k = K == 1 ? 0 : t / O4;
         float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -715,15 +782,15 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     }
 }
 
-template <typename T, int D, int B, bool GR>
+template <typename T, int D, int B, bool GR, int NT>
 cudaError_t launch_tc(const DecodeParams& p, const void* kmap, const void* vmap, long long grid,
                       cudaStream_t stream)
 {
     // 4 warps x 2-stage rings: 64 KB (D = 128) per CTA, three CTAs per SM,
     // up to 192 KB of tile loads in flight per SM
     constexpr int NW = kDecodeTcWarps, NS = 2;
-    using Gm = Geometry<D, B, NW, NS>;
-    auto kern = decode_tc_kernel<T, D, B, NW, NS, GR>;
+    using Gm = Geometry<D, B, NW, NS, NT>;
+    auto kern = decode_tc_kernel<T, D, B, NW, NS, GR, NT>;
     // set on every launch: the attribute belongs to the current device's copy
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES);
@@ -733,18 +800,19 @@ cudaError_t launch_tc(const DecodeParams& p, const void* kmap, const void* vmap,
     return cudaGetLastError();
 }
 
-template <typename T, bool GR>
+// NT: n8 column tiles of query heads per CTA (1: up to 8 columns, 2: up to 16)
+template <typename T, bool GR, int NT>
 cudaError_t launch_tc_dtype(const DecodeParams& p, const void* kmap, const void* vmap,
                             long long grid, cudaStream_t stream)
 {
     if (p.head_dim == 128) {
-        if (p.block_size == 16) return launch_tc<T, 128, 16, GR>(p, kmap, vmap, grid, stream);
-        if (p.block_size == 32) return launch_tc<T, 128, 32, GR>(p, kmap, vmap, grid, stream);
-        return launch_tc<T, 128, 8, GR>(p, kmap, vmap, grid, stream);
+        if (p.block_size == 16) return launch_tc<T, 128, 16, GR, NT>(p, kmap, vmap, grid, stream);
+        if (p.block_size == 32) return launch_tc<T, 128, 32, GR, NT>(p, kmap, vmap, grid, stream);
+        return launch_tc<T, 128, 8, GR, NT>(p, kmap, vmap, grid, stream);
     }
-    if (p.block_size == 16) return launch_tc<T, 64, 16, GR>(p, kmap, vmap, grid, stream);
-    if (p.block_size == 32) return launch_tc<T, 64, 32, GR>(p, kmap, vmap, grid, stream);
-    return launch_tc<T, 64, 8, GR>(p, kmap, vmap, grid, stream);
+    if (p.block_size == 16) return launch_tc<T, 64, 16, GR, NT>(p, kmap, vmap, grid, stream);
+    if (p.block_size == 32) return launch_tc<T, 64, 32, GR, NT>(p, kmap, vmap, grid, stream);
+    return launch_tc<T, 64, 8, GR, NT>(p, kmap, vmap, grid, stream);
 }
 
 }  // namespace

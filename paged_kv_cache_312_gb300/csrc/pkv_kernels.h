@@ -22,10 +22,12 @@ struct DecodeParams {
     int max_partitions;          // ceil(max_blocks * block_size / partition_tokens)
     int cta_parts;               // tensor-core kernel: consecutive partitions per CTA
                                  // (1, or kDecodeTcWarps: one partition per warp)
+    int head_slices;             // tensor-core kernel: CTAs that split one KV group's
+                                 // G query heads, ceil(G / HS) columns each (<= 16)
     int out_dtype;
     float2* ws_ml;               // [S][Hq][max_partitions] (max, sum) in base 2
     float* ws_o;                 // [S][Hq][max_partitions][D] unnormalised output
-    unsigned int* done;          // [S][Hkv] partitions finished (tensor-core split mode)
+    unsigned int* done;          // [S][Hkv][HS] partitions finished (tensor-core split mode)
     unsigned int* status;        // device status word (PKV_STATUS_* bits)
     // Decode step with append (tensor-core kernel only; NULL otherwise): the
     // K/V of each sequence's new token, [S][Hkv][D] in the cache dtype, is
@@ -96,10 +98,12 @@ cudaError_t launch_kv_swap_blocks(void* dst_k, void* dst_v, const void* src_k, c
 // CUDA-core decode (any dtype, any group size).  Grid: partitions x heads x seqs.
 cudaError_t launch_decode_cuda_core(const DecodeParams& p, int kv_dtype, cudaStream_t stream);
 
-// Tensor-core decode (16-bit KV, group size <= 8), one CTA per (sequence,
-// KV head, group of p.cta_parts consecutive partitions), the groups of one
-// (sequence, KV head) adjacent in the grid; the grid is
-// S * Hkv * ceil(max_partitions / cta_parts).  A CTA that holds one partition
+// Tensor-core decode (16-bit KV), one CTA per (sequence, KV head, head
+// slice, group of p.cta_parts consecutive partitions), the groups of one
+// (sequence, KV head, head slice) adjacent in the grid; the grid is
+// S * Hkv * HS * ceil(max_partitions / cta_parts).  A CTA takes ceil(G / HS)
+// query heads as the mma's N columns: launch_decode_tensor_core up to 8
+// (one n8 tile), launch_decode_tensor_core_wide up to 16 (two tiles).  A CTA that holds one partition
 // spreads it over all its warps; one that holds several gives each warp a
 // partition of its own.  The tensor maps describe k_cache / v_cache as 2-D
 // [NB*Hkv*B rows][D columns] loaded in boxes of 64 columns x min(B, 16) rows.
@@ -111,8 +115,11 @@ constexpr int kDecodeTcWarps = 4;
 // the longest context spans at least kWarpPartitionMinCount of them.
 constexpr int kWarpPartitionMaxTokens = 512;
 constexpr int kWarpPartitionMinCount = 16;
+constexpr int kDecodeTcMaxColumns = 16;
 cudaError_t launch_decode_tensor_core(const DecodeParams& p, int kv_dtype, const void* k_map,
                                       const void* v_map, long long grid, cudaStream_t stream);
+cudaError_t launch_decode_tensor_core_wide(const DecodeParams& p, int kv_dtype, const void* k_map,
+                                           const void* v_map, long long grid, cudaStream_t stream);
 
 // Tensor-core decode over beam groups: one CTA per (group, KV head), grid
 // num_groups * num_kv_heads, unsplit.  Each shared-prefix K/V tile is read

@@ -135,6 +135,10 @@ SMALL = [  # dtype, Hq, Hkv, D, B
     ("f16", 8, 4, 128, 8), ("bf16", 4, 2, 64, 32), ("f16", 16, 4, 64, 16),
     ("bf16", 6, 2, 128, 32), ("f16", 12, 12, 64, 8), ("bf16", 16, 2, 64, 8),
     ("f32", 8, 2, 128, 16), ("f32", 4, 4, 64, 32), ("bf16", 32, 2, 128, 16),
+    # wide groups: two n8 column tiles (G = 10, 12), head slices (G = 32: 2 x
+    # 16; G = 40: 14 + 14 + 12 columns)
+    ("f16", 20, 2, 128, 32), ("bf16", 12, 1, 64, 16), ("bf16", 32, 1, 64, 16),
+    ("f16", 40, 1, 128, 8),
 ]
 
 
@@ -160,7 +164,7 @@ def test_decode_small(dt, Hq, Hkv, D, B, P, kernel):
 
 
 @pytest.mark.parametrize("B", [8, 16, 32])
-@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("G", [1, 4, 8, 16, 64])
 @pytest.mark.parametrize("D", [64, 128])
 def test_sweep_points(B, G, D):
     # every point of the block-size / GQA / head-dim sweep, at a small size
@@ -267,10 +271,12 @@ def test_split_matches_one_pass_and_kernels_agree():
             assert max_err(out, ref) <= TOL16, (P, kernel)
 
 
-def test_split_with_thousands_of_partitions():
+@pytest.mark.parametrize("Hq", [16, 32, 64])
+def test_split_with_thousands_of_partitions(Hq):
     # 1500 and 1875 partitions of 16 tokens: more merge weights than the
-    # decode kernel keeps in shared memory, so the merge recomputes them.
-    w = Workload(0, "many", "bf16", 16, 2, 128, 16, 3, "fixed")
+    # decode kernel keeps in shared memory, so the merge recomputes them;
+    # G = 8, 16 (two column tiles) and 32 (two head slices)
+    w = Workload(0, "many", "bf16", Hq, 2, 128, 16, 3, "fixed")
     case = make_decode_case(w, seed=13, lengths=[24000, 30000, 17])
     kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
     ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
@@ -454,7 +460,8 @@ def test_bounded_waits_give_up_flag_and_leave_the_context_usable():
 STEP_CASES = [  # dtype, Hq, Hkv, D, B, partition
     ("bf16", 32, 32, 128, 16, 0), ("bf16", 32, 8, 128, 16, 64), ("f16", 16, 2, 64, 8, 0),
     ("bf16", 8, 1, 128, 32, 32), ("f16", 8, 8, 128, 16, 512),
-    ("f32", 4, 4, 64, 16, 0), ("bf16", 32, 2, 128, 16, 0),  # CUDA-core kernel paths
+    ("bf16", 32, 2, 128, 16, 0), ("f16", 48, 2, 64, 8, 32),  # G = 16, G = 24 (2 slices)
+    ("f32", 4, 4, 64, 16, 0),  # CUDA-core kernel path
 ]
 
 
