@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
 # valid only while the kernel source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "a9bc91e1ce02f08f",
-           "bytes_per_launch": {"2": 1109129216, "3": 806961408, "4": 1089678592}}
+TRAFFIC = {"source_sha": "96126fa153e23e9f",
+           "bytes_per_launch": {"2": 1109458944, "3": 806618624, "4": 1089745408}}
 
 
 def launch_partition(w, max_blocks: int) -> int:
@@ -490,14 +490,18 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     peak, _ = measured_peaks()
     stream = torch.cuda.current_stream(dev)
-    for B in SWEEP_BLOCKS:
-        for D in SWEEP_DIMS:
-            base = sweep_workload(B, max(SWEEP_GROUPS), D)
+    blocks, groups, dims = SWEEP_BLOCKS, SWEEP_GROUPS, SWEEP_DIMS
+    if args.sweep_point:
+        pb, pg, pd = (int(x) for x in args.sweep_point.split(","))
+        blocks, groups, dims = (pb,), (pg,), (pd,)
+    for B in blocks:
+        for D in dims:
+            base = sweep_workload(B, max(groups), D)
             case = make_decode_case(base, seed=args.seed)
             kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
             bt, cl = case.block_tables.to(dev), case.context_lens.to(dev)
             L = case.context_lens.to(torch.int64)
-            for G in SWEEP_GROUPS:
+            for G in groups:
                 w = sweep_workload(B, G, D)
                 q = case.q[:, :w.num_heads].contiguous().to(dev)
                 S = q.shape[0]
@@ -686,6 +690,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="block size x GQA group x head_dim sweep of the attention call "
                          "(one JSON line per point; not the benchmark line)")
+    ap.add_argument("--sweep-point", default=None, metavar="B,G,D",
+                    help="with --sweep: time only this block size, group and head_dim")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
