@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
 # valid only while the kernel source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "96126fa153e23e9f",
-           "bytes_per_launch": {"2": 1109458944, "3": 806618624, "4": 1089745408}}
+TRAFFIC = {"source_sha": "4a7ce33260d38795",
+           "bytes_per_launch": {"2": 1109543936, "3": 806343168, "4": 1089596160}}
 
 
 def launch_partition(w, max_blocks: int) -> int:
@@ -242,9 +242,13 @@ def run_gpu(args, rank, world, local_rank):
     S, Hq, D = q.shape
     out = torch.empty((S, Hq, D), dtype=torch.float32, device=dev)
     ws = None
+    gparts = args.group_parts if grouped else 1
     if st.P:
         ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, bt.shape[1] * w.block_size, st.P),
                          dtype=torch.uint8, device=dev)
+    elif gparts > 1:
+        ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, gparts, 1), dtype=torch.uint8,
+                         device=dev)
     d_pack = views[-1]
     stream = torch.cuda.current_stream(dev)
 
@@ -256,7 +260,8 @@ def run_gpu(args, rank, world, local_rank):
         if grouped:  # append the new tokens and attend, one CTA per (group, KV head)
             pkv.paged_decode_grouped(out, q, kc, vc, bt, cl, gs_d, sh_d, w.scale, w.block_size,
                                      w.num_kv_heads, new_k=nk if has_write else None,
-                                     new_v=nv if has_write else None, stream=stream)
+                                     new_v=nv if has_write else None, parts=gparts,
+                                     workspace=ws, max_members=w.beam_width, stream=stream)
         elif has_write:  # append the new tokens and attend, one call
             pkv.decode_step(out, q, nk, nv, kc, vc, bt, cl, w.scale, w.block_size,
                             w.num_kv_heads, partition_size=st.P, workspace=ws, stream=stream)
@@ -345,9 +350,12 @@ def run_gpu(args, rank, world, local_rank):
         "config": {"workload": w.name, "num_seqs": S, "num_heads": Hq,
                    "num_kv_heads": w.num_kv_heads, "head_dim": D, "block_size": w.block_size,
                    "partition_size": st.P, "kv_bytes_per_step": st.kv_bytes,
+                   "group_parts": gparts if grouped else None,
                    "step": ("cow-copy + " if pairs.shape[0] else "") +
                    ("paged_decode_grouped (beam groups of %d: shared prompt blocks read once "
-                    "per group; new tokens appended inside the attention launch)" % w.beam_width
+                    "per group; each group's stages over %d CTA(s) a KV head, merged in the "
+                    "launch; new tokens appended inside the attention launch)"
+                    % (w.beam_width, gparts)
                     if grouped else
                     "decode_step (new tokens appended inside the attention launch)"
                     if has_write else "paged_decode_attention"),
@@ -363,7 +371,7 @@ def run_gpu(args, rank, world, local_rank):
                                                 "decode_step" if has_write else
                                                 "paged_decode_attention") +
                      (" call: tensor-core decode kernel with in-kernel log-sum-exp merge "
-                      "(+ counter memset)" if st.P else " (tensor-core kernel)"),
+                      "(+ counter memset)" if st.P or gparts > 1 else " (tensor-core kernel)"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": tr,
                      "algorithmic_bytes_per_launch": st.attn_bytes,
@@ -605,6 +613,87 @@ def run_prefill(args):
     pkv.set_prefill_kernel(pkv.PREFILL_TCGEN05)
 
 
+def run_sampling(args):
+    """Parallel sampling of one long prompt: n = 4 samples share every block
+    of an L-token prompt (L = 8192 and 32768; bf16, 32 query / 8 KV heads x
+    128, block 16) and each holds one private block of 1-16 tokens.  Times
+    the ungrouped split decode (1024-token partitions) against the beam-group
+    call with each group's stages over 1, 8, 32 and 64 CTAs a KV head, each
+    call on its own after an L2 flush.  GB/s count the unique KV bytes (the
+    prompt once)."""
+    import paged_kv_cache_312_gb300 as pkv
+    import __graft_entry__
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peak, _ = measured_peaks()
+    n, Hq, Hkv, D, B = 4, 32, 8, 128, 16
+    gen = torch.Generator(device=dev)
+    rng = np.random.default_rng(args.seed)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for Lp in (8192, 32768):
+        gen.manual_seed(args.seed + Lp)
+        nbp = Lp // B
+        NB = nbp + n
+        perm = torch.from_numpy(rng.permutation(NB).astype(np.int32))
+        tails = rng.integers(1, B + 1, size=n)
+        bt = torch.empty((n, nbp + 1), dtype=torch.int32)
+        for s_ in range(n):
+            bt[s_, :nbp] = perm[:nbp]
+            bt[s_, nbp] = perm[nbp + s_]
+        cl = torch.tensor([Lp + int(t) for t in tails], dtype=torch.int32)
+        kc = torch.randn((NB, Hkv, B, D), generator=gen, device=dev).to(torch.bfloat16)
+        vc = torch.randn((NB, Hkv, B, D), generator=gen, device=dev).to(torch.bfloat16)
+        q = torch.randn((n, Hq, D), generator=gen, device=dev).to(torch.bfloat16)
+        gs = torch.tensor([0, n], dtype=torch.int32)
+        sh = pkv.group_shared_tokens(bt, cl, gs, B)
+        btd, cld, gsd, shd = bt.to(dev), cl.to(dev), gs.to(dev), sh.to(dev)
+        unique = (Lp + int(tails.sum())) * 2 * Hkv * D * 2
+        P = 1024
+        ws_u = torch.empty(pkv.decode_workspace_bytes(n, Hq, D, (nbp + 1) * B, P),
+                           dtype=torch.uint8, device=dev)
+        ref = torch.empty((n, Hq, D), dtype=torch.float32, device=dev)
+        calls = [("ungrouped, %d-token partitions" % P, 0,
+                  lambda o: pkv.paged_decode_attention(o, q, kc, vc, btd, cld, D ** -0.5, B, Hkv,
+                                                       partition_size=P, workspace=ws_u,
+                                                       stream=stream))]
+        for parts in (1, 8, 32, 64):
+            ws_g = torch.empty(pkv.decode_workspace_bytes(n, Hq, D, parts, 1),
+                               dtype=torch.uint8, device=dev) if parts > 1 else None
+            calls.append(("grouped, %d part(s)" % parts, parts,
+                          lambda o, parts=parts, ws_g=ws_g: pkv.paged_decode_grouped(
+                              o, q, kc, vc, btd, cld, gsd, shd, D ** -0.5, B, Hkv, parts=parts,
+                              workspace=ws_g, max_members=n, stream=stream)))
+        calls[0][2](ref)
+        for name, parts, fn in calls:
+            out = torch.empty_like(ref)
+            for _ in range(args.warmup):
+                fn(out)
+            torch.cuda.synchronize(dev)
+            # each call timed on its own, after a 256 MB write that flushes L2
+            k = min(args.steps, 200)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(k)]
+            for a_, b_ in evs:
+                flush.zero_()
+                a_.record(stream)
+                fn(out)
+                b_.record(stream)
+            torch.cuda.synchronize(dev)
+            assert pkv.device_status() == 0
+            ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
+            print(json.dumps({"sampling": {"samples": n, "prompt_tokens": Lp, "call": name,
+                                           "parts": parts, "num_heads": Hq, "num_kv_heads": Hkv,
+                                           "head_dim": D, "block_size": B},
+                              "ms": round(ms, 5), "unique_kv_bytes": unique,
+                              "unique_gbs": round(unique / (ms * 1e-3) / 1e9, 1),
+                              "frac_of_measured_peak": round(unique / (ms * 1e-3) / 1e9 / peak, 4),
+                              "max_abs_diff_vs_ungrouped": float((out - ref).abs().max())}),
+                  flush=True)
+        del kc, vc
+
+
 def run_swap(args):
     """Preemption by swapping: move every block of 64 sequences x 2048 tokens
     (bf16, 8 KV heads x 128) from the device cache to a pinned host pool and
@@ -680,6 +769,8 @@ def main():
     ap.add_argument("--ungrouped", action="store_true",
                     help="beam workload: attend every beam on its own (decode_step) instead of "
                          "one CTA per beam group")
+    ap.add_argument("--group-parts", type=int, default=1,
+                    help="beam workload: CTAs that share one beam group's stages for a KV head")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=8.0)
     ap.add_argument("--prefill", action="store_true",
@@ -687,6 +778,10 @@ def main():
     ap.add_argument("--swap", action="store_true",
                     help="device <-> pinned host block swap throughput (one JSON line per "
                          "block size and direction; not the benchmark line)")
+    ap.add_argument("--sampling", action="store_true",
+                    help="parallel sampling of one long prompt: ungrouped split decode against "
+                         "the beam-group call over several part counts (one JSON line per call; "
+                         "not the benchmark line)")
     ap.add_argument("--sweep", action="store_true",
                     help="block size x GQA group x head_dim sweep of the attention call "
                          "(one JSON line per point; not the benchmark line)")
@@ -702,6 +797,9 @@ def main():
 
     if args.sweep:
         run_sweep(args)
+        return
+    if args.sampling:
+        run_sampling(args)
         return
     if args.swap:
         run_swap(args)

@@ -193,11 +193,17 @@ int pkv_decode_step(void* out, const void* q, const void* new_k, const void* new
  *
  * group_start   : int32 [num_groups + 1], device memory, non-decreasing:
  *                 group i is sequences group_start[i] .. group_start[i+1]-1
- *                 (consecutive), with 1 <= members and members * G <= 8
+ *                 (consecutive), with 1 <= members and members * G <= 16
  *                 (G = num_heads / num_kv_heads).  A group outside these
- *                 bounds is skipped and sets PKV_STATUS_BAD_LEN.  Sequences
- *                 in no group are not attended: their output rows (and, in a
- *                 decode step, their caches) are left as they were.
+ *                 bounds (or above 8 columns when the one-tile kernel was
+ *                 chosen, see max_members) is skipped and sets
+ *                 PKV_STATUS_BAD_LEN.  Sequences in no group are not
+ *                 attended: their output rows (and, in a decode step, their
+ *                 caches) are left as they were.
+ * max_members   : an upper bound on any group's members, or 0 for
+ *                 num_seqs - num_groups + 1.  When max_members * G <= 8 the
+ *                 kernel carries the group's query heads as one n8 column
+ *                 tile, else as two (twice the mma work per K/V byte).
  * shared_tokens : int32 [num_groups], device memory: the first
  *                 shared_tokens[i] positions of every member of group i lie
  *                 in the same physical blocks (same table entries), e.g. from
@@ -206,19 +212,34 @@ int pkv_decode_step(void* out, const void* q, const void* new_k, const void* new
  *                 in a decode step, short of every member's new token).
  * new_k, new_v  : NULL for attention only; else as in pkv_decode_step, each
  *                 new token in a block private to its sequence.
- * Other arguments as in pkv_decode_step; not split (no partition_size or
- * workspace): one CTA streams a whole group for one KV head, so with few
- * groups and long contexts the split, ungrouped pkv_decode_step keeps more of
- * the GPU busy.  Needs the tensor-core kernel: 16-bit KV, G <= 8, kernel
- * choice PKV_KERNEL_AUTO (else PKV_ERR_UNSUPPORTED).
+ * parts         : 0 or 1: one CTA streams a whole group for one KV head.
+ *                 2 .. 64: a group's list of 16-token stages (its shared
+ *                 prefix, then each member's own tail) is cut into `parts`
+ *                 runs of equal length, one CTA each; each run writes (max,
+ *                 sum, unnormalised output) per member query head to the
+ *                 workspace and the last run to finish merges them by
+ *                 log-sum-exp inside the same launch (the pages are silent on
+ *                 splitting; the merge is exact in real arithmetic).  More
+ *                 parts even out the waves when num_groups * num_kv_heads is
+ *                 not a large multiple of the CTAs the GPU holds at once.
+ * workspace     : device scratch when parts > 1 (else may be NULL): at least
+ *                 pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim,
+ *                 parts, 1) bytes, 256-byte aligned; contents on entry are
+ *                 ignored; calls that share it must not overlap on the GPU.
+ * Other arguments as in pkv_decode_step (no partition_size).  Needs the
+ * tensor-core kernel: 16-bit KV, G <= 16, kernel choice PKV_KERNEL_AUTO (else
+ * PKV_ERR_UNSUPPORTED).  A group is read by at most `parts` CTAs a KV head,
+ * so with few groups and long contexts the split, ungrouped pkv_decode_step
+ * can keep more of the GPU busy.
  */
 int pkv_paged_decode_grouped(void* out, const void* q, const void* new_k, const void* new_v,
                              void* k_cache, void* v_cache, const int32_t* block_tables,
                              const int32_t* context_lens, const int32_t* group_start,
-                             const int32_t* shared_tokens, int num_groups, float scale,
-                             int block_size, int num_kv_heads, int num_seqs, int num_heads,
-                             int head_dim, int max_blocks_per_seq, int num_blocks, int kv_dtype,
-                             int out_dtype, void* stream);
+                             const int32_t* shared_tokens, int num_groups, int max_members,
+                             float scale, int block_size, int num_kv_heads, int num_seqs,
+                             int num_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
+                             int kv_dtype, int out_dtype, int parts, void* workspace,
+                             size_t workspace_bytes, void* stream);
 
 /*
  * group_shared_tokens -- host helper for pkv_paged_decode_grouped: for each

@@ -35,8 +35,8 @@ _SIGS = {
     "pkv_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "pkv_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I,
                              _I, _I, _I, _P, _SZ, _P]),
-    "pkv_paged_decode_grouped": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _F, _I, _I, _I,
-                                      _I, _I, _I, _I, _I, _I, _P]),
+    "pkv_paged_decode_grouped": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _F, _I, _I,
+                                      _I, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
     "pkv_group_shared_tokens": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "pkv_paged_prefill_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I,
                                          _I, _I, _I, _I, _I, _P]),
@@ -204,12 +204,18 @@ def decode_step(out, q, new_k, new_v, k_cache, v_cache, block_tables, context_le
 
 def paged_decode_grouped(out, q, k_cache, v_cache, block_tables, context_lens, group_start,
                          shared_tokens, scale, block_size, num_kv_heads, new_k=None, new_v=None,
-                         stream=None):
+                         parts=1, workspace=None, max_members=None, stream=None):
     """Decode attention (a decode step when new_k/new_v [S, Hkv, D] are
     given) for groups of consecutive sequences sharing a prefix of physical
     blocks: group i is sequences group_start[i]..group_start[i+1]-1, whose
     first shared_tokens[i] positions use the same table entries.  Same
-    result as decode_step / paged_decode_attention for every sequence."""
+    result as decode_step / paged_decode_attention for every sequence.
+    parts > 1 cuts each group's stage list over that many CTAs (merged in
+    the launch); it needs a workspace of
+    decode_workspace_bytes(S, Hq, D, parts, 1) bytes.  max_members bounds the
+    members of any group (it picks the kernel width: one n8 column tile when
+    max_members * G <= 8); None leaves the bound to the library (the
+    sequences the other groups leave)."""
     S, Hq, D = q.shape
     NB, Hkv, B, Dk = k_cache.shape
     if (Hkv, B, Dk) != (num_kv_heads, block_size, D) or v_cache.shape != k_cache.shape:
@@ -234,12 +240,17 @@ def paged_decode_grouped(out, q, k_cache, v_cache, block_tables, context_lens, g
         raise ValueError("q, k_cache, v_cache must share a dtype")
     nk = _dev(new_k, "new_k") if new_k is not None else ctypes.c_void_p(0)
     nv = _dev(new_v, "new_v") if new_v is not None else ctypes.c_void_p(0)
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
     rc = lib().pkv_paged_decode_grouped(
         _dev(out, "out"), _dev(q, "q"), nk, nv, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables"), _dev(context_lens, "context_lens"),
-        _dev(group_start, "group_start"), _dev(shared_tokens, "shared_tokens"), G, float(scale),
+        _dev(group_start, "group_start"), _dev(shared_tokens, "shared_tokens"), G,
+        int(max_members or 0), float(scale),
         int(block_size), int(num_kv_heads), S, Hq, D, block_tables.shape[1], NB,
-        DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], _stream(stream))
+        DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], int(parts), ws_ptr, ws_bytes,
+        _stream(stream))
     _check(rc, "pkv_paged_decode_grouped")
 
 

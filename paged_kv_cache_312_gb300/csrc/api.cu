@@ -347,7 +347,8 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
                 int head_dim, int max_blocks_per_seq, int num_blocks, int kv_dtype, int out_dtype,
                 int partition_size, void* workspace, size_t workspace_bytes, void* stream,
                 const void* new_k, const void* new_v, const int32_t* group_start = nullptr,
-                const int32_t* shared_tokens = nullptr, int num_groups = 0)
+                const int32_t* shared_tokens = nullptr, int num_groups = 0, int group_parts = 1,
+                int max_members = 0)
 {
     if (!pkv_dtype_bytes(kv_dtype) || !pkv_dtype_bytes(out_dtype))
         return pkv_fail(PKV_ERR_DTYPE, "%s: dtype kv=%d out=%d", fn, kv_dtype, out_dtype);
@@ -389,11 +390,17 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
             return pkv_fail(PKV_ERR_SHAPE, "%s: num_groups %d outside [1, %d]", fn, num_groups,
                             num_seqs);
         if (partition_size != 0)
-            return pkv_fail(PKV_ERR_UNSUPPORTED, "%s: beam groups are not split", fn);
-        if (kv_dtype == PKV_F32 || num_heads / num_kv_heads > 8 ||
+            return pkv_fail(PKV_ERR_UNSUPPORTED, "%s: beam groups split by parts, not tokens", fn);
+        if (group_parts < 1 || group_parts > kMaxGroupParts)
+            return pkv_fail(PKV_ERR_SHAPE, "%s: parts %d outside [1, %d]", fn, group_parts,
+                            kMaxGroupParts);
+        if (kv_dtype == PKV_F32 || num_heads / num_kv_heads > kDecodeTcMaxColumns ||
             g_decode_kernel != PKV_KERNEL_AUTO)
             return pkv_fail(PKV_ERR_UNSUPPORTED,
-                            "%s: beam groups need the tensor-core kernel (16-bit KV, G <= 8)", fn);
+                            "%s: beam groups need the tensor-core kernel (16-bit KV, G <= 16)",
+                            fn);
+        if (max_members < 0)
+            return pkv_fail(PKV_ERR_SHAPE, "%s: max_members %d < 0", fn, max_members);
     }
 
     DecodeParams p;
@@ -423,14 +430,18 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
     const int max_ctx = max_blocks_per_seq * block_size;
     p.cta_parts = 1;
     p.head_slices = 1;
-    if (partition_size == 0) {
+    if (partition_size == 0 && (!grouped || group_parts == 1)) {
         p.partition_tokens = max_ctx;
         p.max_partitions = 1;
     } else {
-        p.partition_tokens = partition_size;
-        p.max_partitions = (max_ctx + partition_size - 1) / partition_size;
+        // token partitions, or (beam groups) parts of each group's stage list
+        p.partition_tokens = grouped ? max_ctx : partition_size;
+        p.max_partitions =
+            grouped ? group_parts : (max_ctx + partition_size - 1) / partition_size;
         const size_t need =
-            pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_ctx, partition_size);
+            grouped ? pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, group_parts, 1)
+                    : pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_ctx,
+                                                 partition_size);
         if (!workspace || workspace_bytes < need)
             return pkv_fail(PKV_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn,
                             need, workspace ? workspace_bytes : (size_t)0);
@@ -461,14 +472,26 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
         if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap, 1);
         if (rc != PKV_OK) return rc;
         if (grouped) {
-            // one CTA per (beam group, KV head); each writes its new tokens
+            // one CTA per (beam group, KV head, part); each writes the new
+            // tokens of its run
             p.group_start = group_start;
             p.shared_tokens = shared_tokens;
             p.num_groups = num_groups;
             p.new_k = new_k;
             p.new_v = new_v;
+            if (p.max_partitions > 1) {
+                e = cudaMemsetAsync(p.done, 0, sizeof(unsigned) * (size_t)num_groups * num_kv_heads,
+                                    st);
+                if (e != cudaSuccess) return cuda_fail(e, fn);
+            }
+            // one n8 column tile when every group's members * G fits 8
+            // (max_members 0: bounded by the sequences the other groups leave)
+            const long long members =
+                max_members > 0 ? max_members : (long long)num_seqs - num_groups + 1;
+            const bool wide = members * G > 8;
             e = launch_decode_grouped(p, kv_dtype, &kmap, &vmap,
-                                      (long long)num_groups * num_kv_heads, st);
+                                      (long long)num_groups * num_kv_heads * p.max_partitions, wide,
+                                      st);
             if (e != cudaSuccess) return cuda_fail(e, fn);
             return PKV_OK;
         }
@@ -536,10 +559,11 @@ int pkv_paged_decode_attention(void* out, const void* q, const void* k_cache, co
 int pkv_paged_decode_grouped(void* out, const void* q, const void* new_k, const void* new_v,
                              void* k_cache, void* v_cache, const int32_t* block_tables,
                              const int32_t* context_lens, const int32_t* group_start,
-                             const int32_t* shared_tokens, int num_groups, float scale,
-                             int block_size, int num_kv_heads, int num_seqs, int num_heads,
-                             int head_dim, int max_blocks_per_seq, int num_blocks, int kv_dtype,
-                             int out_dtype, void* stream)
+                             const int32_t* shared_tokens, int num_groups, int max_members,
+                             float scale, int block_size, int num_kv_heads, int num_seqs,
+                             int num_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
+                             int kv_dtype, int out_dtype, int parts, void* workspace,
+                             size_t workspace_bytes, void* stream)
 {
     static const char* fn = "pkv_paged_decode_grouped";
     if (num_seqs > 0 && !group_start) return pkv_fail(PKV_ERR_NULL, "%s: NULL group_start", fn);
@@ -547,8 +571,9 @@ int pkv_paged_decode_grouped(void* out, const void* q, const void* new_k, const 
         return pkv_fail(PKV_ERR_NULL, "%s: new_k and new_v must both be set or both NULL", fn);
     return decode_impl(fn, out, q, k_cache, v_cache, block_tables, context_lens, scale,
                        block_size, num_kv_heads, num_seqs, num_heads, head_dim, max_blocks_per_seq,
-                       num_blocks, kv_dtype, out_dtype, 0, nullptr, 0, stream, new_k, new_v,
-                       group_start, shared_tokens, num_groups);
+                       num_blocks, kv_dtype, out_dtype, 0, workspace, workspace_bytes, stream, new_k,
+                       new_v, group_start, shared_tokens, num_groups, parts < 1 ? 1 : parts,
+                       max_members);
 }
 
 int pkv_group_shared_tokens(const int32_t* block_tables, const int32_t* context_lens,

@@ -8,8 +8,15 @@
 #include "decode_tc.cuh"
 
 cudaError_t launch_decode_grouped(const DecodeParams& p, int kv_dtype, const void* k_map,
-                                  const void* v_map, long long grid, cudaStream_t stream)
+                                  const void* v_map, long long grid, bool wide,
+                                  cudaStream_t stream)
 {
-    if (kv_dtype == PKV_BF16) return launch_tc_dtype<__nv_bfloat16, true, 1>(p, k_map, v_map, grid, stream);
+    if (wide) {
+        if (kv_dtype == PKV_BF16)
+            return launch_tc_dtype<__nv_bfloat16, true, 2>(p, k_map, v_map, grid, stream);
+        return launch_tc_dtype<__half, true, 2>(p, k_map, v_map, grid, stream);
+    }
+    if (kv_dtype == PKV_BF16)
+        return launch_tc_dtype<__nv_bfloat16, true, 1>(p, k_map, v_map, grid, stream);
     return launch_tc_dtype<__half, true, 1>(p, k_map, v_map, grid, stream);
 }

@@ -86,7 +86,8 @@ struct Geometry {
     // per ring slot: block ids of the stage (2), and for beam groups its first
     // token, region end and member (3)
     static constexpr int SID_INTS = 8;
-    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + SID_OFF + NW * NS * SID_INTS * 4;
+    static constexpr int GM_OFF = SID_OFF + NW * NS * SID_INTS * 4;  // beam groups: [NC] lengths
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + GM_OFF + NC * 4;
     // partition weights cached for the in-kernel merge (after the warp merge)
     static constexpr int WCACHE = ((DATA_BYTES - MERGE_BYTES) / 4 - 2 * NC - NW * 32 * 4 - 4) & ~3;
     static_assert(WCACHE > 0, "room for merge weights");
@@ -135,53 +136,57 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     // or one slice of at most NC of them when the group is wider)
     int hb = 0, ncol;
     bool solo;
-    // Beam groups (GR): one CTA per (group, KV head).  The group's members
+    // Beam groups (GR): one CTA per (group, KV head, part).  The group's members
     // are sequences s0 .. s0 + nm - 1 whose first `shared` tokens sit in the
     // same physical blocks; the CTA streams that shared prefix once for all
-    // members (their query heads are the mma's N columns, nm * G <= 8), then
+    // members (their query heads are the mma's N columns, nm * G <= NC), then
     // each member's own tail with the other members' columns masked.
-    int s0 = 0, nm = 1, shared = 0, nsh = 0;
-    int Lm[8];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int* glen = reinterpret_cast<int*>(smem + Gm::GM_OFF);  // GR: members' context lengths
+    int s0 = 0, nm = 1, shared = 0, nsh = 0, qbase = 0;
     if constexpr (GR) {
-        const int gi = blockIdx.x / p.num_kv_heads;
-        g = blockIdx.x - gi * p.num_kv_heads;
+        // slot b = (gi * Hkv + g) * parts + part: part `part` of the group's
+        // stage list (shared prefix, then each member's tail) for KV head g
+        const int gparts = p.max_partitions;
+        sg = blockIdx.x / gparts;
+        part = blockIdx.x - sg * gparts;
+        const int gi = sg / p.num_kv_heads;
+        g = sg - gi * p.num_kv_heads;
         s0 = p.group_start[gi];
         nm = p.group_start[gi + 1] - s0;
         if (nm < 1 || nm * G > NC || s0 < 0 || s0 + nm > p.num_seqs) {
             if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
             return;
         }
-        int min_len = INT_MAX;  // (the new token of a decode step stays private)
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            int l = 0;
-            if (m < nm) {
-                l = p.context_lens[s0 + m];
-                if (l < 0 || (int64_t)l > (int64_t)p.max_blocks * B) {
-                    if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
-                    l = 0;
-                }
-                min_len = min(min_len, p.new_k != nullptr ? l - 1 : l);
+        if (threadIdx.x < nm) {
+            int l = p.context_lens[s0 + threadIdx.x];
+            if (l < 0 || (int64_t)l > (int64_t)p.max_blocks * B) {
+                atomicOr(p.status, PKV_STATUS_BAD_LEN);
+                l = 0;
             }
-            Lm[m] = l;
+            glen[threadIdx.x] = l;
         }
+        __syncthreads();
+        int min_len = INT_MAX;  // (the new token of a decode step stays private)
+        for (int m = 0; m < nm; ++m) min_len = min(min_len, p.new_k != nullptr ? glen[m] - 1 : glen[m]);
         shared = max(0, min(p.shared_tokens[gi], min_len)) & ~15;
         nsh = shared / 16;
-        nst = nsh;
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-            if (m < nm) nst += (Lm[m] - shared + 15) / 16;
+        int total = nsh;
+        for (int m = 0; m < nm; ++m) total += (glen[m] - shared + 15) / 16;
+        // this CTA's run of the list: stages qbase .. qbase + nst - 1
+        qbase = (int)((int64_t)part * total / gparts);
+        nst = (int)((int64_t)(part + 1) * total / gparts) - qbase;
         s = s0;
-        sg = 0;
         ncol = nm * G;
-        L = Lm[0];
-        nparts = 1;
+        L = glen[0];
+        nparts = gparts;
         p0 = 0;
         np_cta = 1;
         solo = true;
         wpp = NW;
         wsub = warp;
-        part = 0;
         begin = 0;
         end = 0;
     } else {
@@ -230,27 +235,21 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         mem = -1;
         tok0 = 0;
         endr = 0;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int st = m < nm ? (Lm[m] - shared + 15) / 16 : 0;
-            if (mem < 0) {
-                if (r < st) {
-                    mem = m;
-                    tok0 = shared + r * 16;
-                    endr = Lm[m];
-                } else {
-                    r -= st;
-                }
+        for (int m = 0; m < nm; ++m) {
+            const int lm = glen[m], st = (lm - shared + 15) / 16;
+            if (r < st) {
+                mem = m;
+                tok0 = shared + r * 16;
+                endr = lm;
+                break;
             }
+            r -= st;
         }
     };
     auto table_of = [&](int mem) {
         return p.block_tables + (size_t)(GR ? s0 + max(mem, 0) : s) * p.max_blocks;
     };
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::BAR_OFF);
     int* sid = reinterpret_cast<int*>(smem + Gm::SID_OFF);  // [warp][slot][2] block ids
 
@@ -276,7 +275,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         const int j = jbase + lane;
         int tk0 = begin + (wsub + j * wpp) * 16, endr = end, mem = -1;
         if constexpr (GR) {
-            if (j < cnt) stage_at(warp + j * NW, tk0, endr, mem);
+            if (j < cnt) stage_at(qbase + warp + j * NW, tk0, endr, mem);
             win_tok = tk0;
             win_end = endr;
             win_mem = mem;
@@ -370,15 +369,14 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     if (p.new_k != nullptr) {
         if constexpr (GR) {
             // member m's new token (always past the shared prefix) lies in
-            // CTA stage nsh + (stages of members before m) + (L_m-1-shared)/16
+            // list stage nsh + (stages of members before m) + (L_m-1-shared)/16;
+            // the warp of the CTA whose run holds that stage writes it
             int qb0 = nsh;
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                if (m < nm) {
-                    if (Lm[m] > shared && (qb0 + (Lm[m] - 1 - shared) / 16) % NW == warp)
-                        append(s0 + m, Lm[m], table_of(m));
-                    qb0 += (Lm[m] - shared + 15) / 16;
-                }
+            for (int m = 0; m < nm; ++m) {
+                const int lm = glen[m], qm = qb0 + (lm - 1 - shared) / 16;
+                if (lm > shared && qm >= qbase && qm < qbase + nst && (qm - qbase) % NW == warp)
+                    append(s0 + m, lm, table_of(m));
+                qb0 += (lm - shared + 15) / 16;
             }
         } else if (L > 0 && begin <= L - 1 && L - 1 < end && ((L - 1 - begin) / 16) % wpp == wsub) {
             append(s, L, table);
@@ -582,6 +580,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     }
 
     const size_t hbase = (size_t)s * p.num_heads + (size_t)g * G + hb;
+    // output / workspace row of column n: query head g*G + hb + n of sequence
+    // s, or (GR) query head g*G + n % G of member n / G
+    auto row_of = [&](int n) -> size_t {
+        return GR ? (size_t)(s0 + n / G) * p.num_heads + g * G + n % G : hbase + n;
+    };
     if (!solo) {
         // ---- a warp's own partition: its softmax state is the partition's
         // result, written straight to the workspace (columns 8t+2tq, +1)
@@ -592,7 +595,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                 for (int h = 0; h < 2; ++h) {
                     const int n = 8 * t + 2 * tq + h;
                     if (n < ncol) {
-                        const size_t slot = (hbase + n) * p.max_partitions + part;
+                        const size_t slot = row_of(n) * p.max_partitions + part;
                         if (gq == 0) p.ws_ml[slot] = make_float2(mr[t][h], lr_[t][h]);
                         float* o = p.ws_o + slot * D;
 #pragma unroll
@@ -650,14 +653,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             }
             if (nparts <= 1) {
                 const bool pos = den > 0.f;
-                const size_t orow =
-                    GR ? ((size_t)(s0 + n / G) * p.num_heads + g * G + n % G) : hbase + n;
-                store_out4(p.out, orow * D + d,
+                store_out4(p.out, row_of(n) * D + d,
                            make_float4(pos ? num.x / den : 0.f, pos ? num.y / den : 0.f,
                                        pos ? num.z / den : 0.f, pos ? num.w / den : 0.f),
                            p.out_dtype, vec_out);
             } else {
-                const size_t slot = (hbase + n) * p.max_partitions + part;
+                const size_t slot = row_of(n) * p.max_partitions + part;
                 *reinterpret_cast<float4*>(p.ws_o + slot * D + d) = num;
                 if (d == 0) p.ws_ml[slot] = make_float2(M, den);
             }
@@ -666,7 +667,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     }
 
     // ---- split: the CTA that finishes the last partition of (s, g, head
-    // slice) merges them by log-sum-exp: M = max_i m_i, w_i = 2^(m_i - M),
+    // slice), or (GR) the last part of (group, g), merges them by
+    // log-sum-exp: M = max_i m_i, w_i = 2^(m_i - M),
     // out = sum_i w_i O_i / sum_i w_i l_i.
     __shared__ int is_last;
     __syncthreads();  // this CTA's partition results are written ...
@@ -690,7 +692,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     float4* red = reinterpret_cast<float4*>(hmax + NC);                // [NTH] partial sums
     const bool cached = ncol * nparts <= Gm::WCACHE;
     for (int n = warp; n < ncol; n += NW) {
-        const size_t base = (hbase + n) * p.max_partitions;
+        const size_t base = row_of(n) * p.max_partitions;
         // the (max, sum) pairs of the first 64 partitions are read once and
         // kept in registers for both passes; any further ones are re-read
         float2 ml[2];
@@ -739,7 +741,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         const bool active = o < O4 && k < K;
         if (active) {
             const int n = o / (D / 4), d4 = o - n * (D / 4);
-            const size_t base = (hbase + n) * p.max_partitions;
+            const size_t base = row_of(n) * p.max_partitions;
             const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * D) + d4;
 #pragma unroll 16
             for (int i = k; i < nparts; i += K) {
@@ -773,7 +775,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         if (k == 0 && active) {
             const int n = o / (D / 4), d = (o - n * (D / 4)) * 4;
             const float inv = hinv[n];
-            const size_t at = (hbase + n) * D + d;
+            const size_t at = row_of(n) * D + d;
             store_out(p.out, at + 0, acc4.x * inv, p.out_dtype);
             store_out(p.out, at + 1, acc4.y * inv, p.out_dtype);
             store_out(p.out, at + 2, acc4.z * inv, p.out_dtype);

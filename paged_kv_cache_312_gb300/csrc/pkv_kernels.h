@@ -121,11 +121,17 @@ cudaError_t launch_decode_tensor_core(const DecodeParams& p, int kv_dtype, const
 cudaError_t launch_decode_tensor_core_wide(const DecodeParams& p, int kv_dtype, const void* k_map,
                                            const void* v_map, long long grid, cudaStream_t stream);
 
-// Tensor-core decode over beam groups: one CTA per (group, KV head), grid
-// num_groups * num_kv_heads, unsplit.  Each shared-prefix K/V tile is read
-// once for all members of the group; p.group_start / p.shared_tokens set.
+// Tensor-core decode over beam groups: one CTA per (group, KV head, part),
+// grid num_groups * num_kv_heads * p.max_partitions, the parts of one (group,
+// KV head) adjacent.  Each shared-prefix K/V tile is read once for all members
+// of the group; p.group_start / p.shared_tokens set.  With several parts, each
+// takes an equal run of the group's 16-token stage list (shared prefix, then
+// each member's tail) and the last to finish merges them (p.done zeroed).
+constexpr int kMaxGroupParts = 64;
+// wide: two n8 column tiles, members * G <= 16 (else one tile, <= 8).
 cudaError_t launch_decode_grouped(const DecodeParams& p, int kv_dtype, const void* k_map,
-                                  const void* v_map, long long grid, cudaStream_t stream);
+                                  const void* v_map, long long grid, bool wide,
+                                  cudaStream_t stream);
 
 // Log-sum-exp merge of split partitions (only sequences with > 1 partition).
 cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream);

@@ -851,12 +851,29 @@ GROUP_CASES = [  # dtype, Hq, Hkv, D, B, groups (shared blocks, member tails)
     ("bf16", 16, 8, 128, 32, [(4, [16, 33, 1, 64]), (2, [31])]),
     ("f16", 8, 2, 128, 16, [(9, [7, 70]), (1, [1, 2])]),
     ("bf16", 16, 2, 64, 16, [(3, [50])]),  # G = 8: one member per group
+    # two n8 column tiles: 12 columns (G = 2 x 6), 16 (G = 4 x 4), 16 (G = 1 x
+    # 16 members), and G = 16 alone
+    ("bf16", 8, 4, 64, 16, [(6, [3, 9, 17, 40, 1, 2]), (1, [5, 5])]),
+    ("f16", 16, 4, 128, 16, [(12, [5, 30, 1, 64]), (2, [7])]),
+    ("bf16", 4, 4, 128, 32, [(3, list(range(1, 17)))]),
+    ("f16", 32, 2, 64, 8, [(20, [9]), (0, [3])]),
 ]
 
 
+def group_ws(q, parts):
+    S, Hq, D = q.shape
+    if parts <= 1:
+        return None
+    return torch.empty(pkv.decode_workspace_bytes(S, Hq, D, parts, 1), dtype=torch.uint8,
+                       device=DEV)
+
+
+@pytest.mark.parametrize("parts", [1, 2, 5])
 @pytest.mark.parametrize("step", [False, True])
 @pytest.mark.parametrize("dt,Hq,Hkv,D,B,groups", GROUP_CASES)
-def test_beam_groups_match_oracle(dt, Hq, Hkv, D, B, groups, step):
+def test_beam_groups_match_oracle(dt, Hq, Hkv, D, B, groups, step, parts):
+    # parts > 1 cuts each group's stage list over that many CTAs (some runs
+    # empty when a group has fewer stages), merged inside the launch
     if step:  # a decode step needs a new token in each member's own tail
         groups = [(nsh, [max(t, 1) for t in tails]) for nsh, tails in groups]
     q, kc, vc, bt, cl, gs, nk, nv = make_group_case(dt, Hq, Hkv, D, B, groups, seed=Hq + B + D,
@@ -872,7 +889,8 @@ def test_beam_groups_match_oracle(dt, Hq, Hkv, D, B, groups, step):
     pkv.paged_decode_grouped(out, q.to(DEV), kd, vd, bt.to(DEV), cl.to(DEV), gs.to(DEV),
                              sh.to(DEV), scale, B, Hkv,
                              new_k=nk.to(DEV) if step else None,
-                             new_v=nv.to(DEV) if step else None)
+                             new_v=nv.to(DEV) if step else None,
+                             parts=parts, workspace=group_ws(q, parts))
     torch.cuda.synchronize()
     assert pkv.device_status() == 0
     if step:
@@ -901,24 +919,40 @@ def test_beam_groups_equal_ungrouped_step_and_flag_oversized_groups():
     assert pkv.device_status() == 0
     assert torch.equal(bits(k1), bits(k2)) and torch.equal(bits(v1), bits(v2))
     assert float((o1 - o2).abs().max()) <= TOL16
-    # six members with two query heads each (G = 2) need 12 > 8 columns: the
-    # group is skipped and flagged
-    q6, kc6, vc6, bt6, cl6, gs6, _, _ = make_group_case(
-        "f16", 16, 8, 128, 16, [(4, [1, 2, 3, 4, 5, 6])], seed=4, step=False)
-    out = torch.full(q6.shape, 7.0, dtype=torch.float32, device=DEV)
+    # nine members with two query heads each (G = 2) need 18 > 16 columns; six
+    # need 12, more than one tile holds when max_members = 4 picks the
+    # one-tile kernel: either way the group is skipped and flagged
+    for members, max_members in ((9, None), (6, 4)):
+        q6, kc6, vc6, bt6, cl6, gs6, _, _ = make_group_case(
+            "f16", 16, 8, 128, 16, [(4, list(range(1, members + 1)))], seed=4, step=False)
+        out = torch.full(q6.shape, 7.0, dtype=torch.float32, device=DEV)
+        pkv.paged_decode_grouped(out, q6.to(DEV), kc6.to(DEV), vc6.to(DEV), bt6.to(DEV),
+                                 cl6.to(DEV), gs6.to(DEV),
+                                 pkv.group_shared_tokens(bt6, cl6, gs6, 16).to(DEV),
+                                 128 ** -0.5, 16, 8, max_members=max_members)
+        torch.cuda.synchronize()
+        assert pkv.device_status() & 2  # bad context length / group
+        assert bool((out == 7.0).all())  # nothing written for the skipped group
+        pkv.device_status(reset=True)
+    # the same six with the default bound take the two-tile kernel
+    out = torch.full(q6.shape, float("nan"), dtype=torch.float32, device=DEV)
     pkv.paged_decode_grouped(out, q6.to(DEV), kc6.to(DEV), vc6.to(DEV), bt6.to(DEV),
                              cl6.to(DEV), gs6.to(DEV),
                              pkv.group_shared_tokens(bt6, cl6, gs6, 16).to(DEV),
                              128 ** -0.5, 16, 8)
     torch.cuda.synchronize()
-    assert pkv.device_status() & 2  # bad context length / group
-    assert bool((out == 7.0).all())  # nothing written for the skipped group
-    pkv.device_status(reset=True)
+    assert pkv.device_status() == 0
+    ref = oracle.paged_decode_attention(q6, kc6, vc6, bt6, cl6, 128 ** -0.5, 16, 8)
+    assert max_err(out, ref) <= TOL16
 
 
-def test_workload5_grouped_step_full_size():
+@pytest.mark.parametrize("parts,hint", [(1, True), (2, False)])
+def test_workload5_grouped_step_full_size(parts, hint):
     # the benchmark's beam step through the beam-group call: CoW copy, then
     # one launch that appends every beam's new token and attends the group
+    # (the bench's launch: one CTA a group and KV head, the one-tile kernel
+    # picked by the beam width as member bound; and each group's stages over
+    # two CTAs on the two-tile kernel the default bound picks)
     w = WORKLOADS[5]
     case = make_beam_case(w, seed=1)
     mgr = pkv.BlockAllocator(case.pool_blocks, w.block_size, free_order=case.pool_order)
@@ -940,7 +974,8 @@ def test_workload5_grouped_step_full_size():
     out = torch.full(case.q.shape, float("nan"), dtype=torch.float32, device=DEV)
     pkv.paged_decode_grouped(out, case.q.to(DEV), kc, vc, bt.to(DEV), cl.to(DEV), gs.to(DEV),
                              sh.to(DEV), w.scale, B, Hkv, new_k=case.new_key.to(DEV),
-                             new_v=case.new_value.to(DEV))
+                             new_v=case.new_value.to(DEV), parts=parts,
+                             workspace=group_ws(case.q, parts), max_members=W if hint else None)
     torch.cuda.synchronize()
     assert pkv.device_status() == 0
     oracle.kv_write(kh, vh, case.new_key, case.new_value, slots, B)
@@ -951,7 +986,27 @@ def test_workload5_grouped_step_full_size():
     assert bool(torch.isfinite(out).all())
 
 
-def test_beam_groups_empty_members_and_uncovered_sequences():
+@pytest.mark.parametrize("parts", [16, 64])
+def test_parallel_sampling_of_one_long_prompt_over_many_parts(parts):
+    # one group: four samples share a 4096-token prompt (256 blocks) and hold
+    # tails of their own; 16 or 64 CTAs a KV head split the 260-odd stages
+    groups = [(256, [1, 16, 7, 12])]
+    q, kc, vc, bt, cl, gs, _, _ = make_group_case("bf16", 32, 8, 128, 16, groups, seed=21,
+                                                  step=False)
+    sh = pkv.group_shared_tokens(bt, cl, gs, 16)
+    assert int(sh[0]) == 4096  # the prompt's blocks
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=DEV)
+    pkv.paged_decode_grouped(out, q.to(DEV), kc.to(DEV), vc.to(DEV), bt.to(DEV), cl.to(DEV),
+                             gs.to(DEV), sh.to(DEV), 128 ** -0.5, 16, 8, parts=parts,
+                             workspace=group_ws(q, parts))
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    ref = oracle.paged_decode_attention(q, kc, vc, bt, cl, 128 ** -0.5, 16, 8)
+    assert max_err(out, ref) <= TOL16
+
+
+@pytest.mark.parametrize("parts", [1, 4])
+def test_beam_groups_empty_members_and_uncovered_sequences(parts):
     # a member with no tokens gets a zero row; sequences outside every group
     # are not touched
     groups = [(2, [0, 30, 5]), (0, [0]), (3, [7, 9])]
@@ -964,7 +1019,8 @@ def test_beam_groups_empty_members_and_uncovered_sequences():
     assert int(sh[0]) == 0  # the empty member shares nothing
     out = torch.full(q.shape, 5.0, dtype=torch.float32, device=DEV)
     pkv.paged_decode_grouped(out, q.to(DEV), kc.to(DEV), vc.to(DEV), bt.to(DEV), cl.to(DEV),
-                             gs_part.to(DEV), sh.to(DEV), 128 ** -0.5, 16, 8)
+                             gs_part.to(DEV), sh.to(DEV), 128 ** -0.5, 16, 8, parts=parts,
+                             workspace=group_ws(q, parts))
     torch.cuda.synchronize()
     assert pkv.device_status() == 0
     ref = oracle.paged_decode_attention(q, kc, vc, bt, cl, 128 ** -0.5, 16, 8)
