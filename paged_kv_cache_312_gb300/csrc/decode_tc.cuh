@@ -34,18 +34,19 @@
 //    16-bit remainder (~16 significant bits).
 //  * Online softmax in base 2 (fp32) against a per-head reference max that
 //    moves only when a score passes it by more than 8, so most stages need
-//    neither a cross-lane max nor a rescale of O; the warps of a partition merge through
-//    shared memory (reusing the rings) at the end.  An unsplit item writes
+//    neither a cross-lane max nor a rescale of O; the warps of a partition
+//    merge through shared memory (reusing the rings) at the end.  An unsplit item writes
 //    the output; a partition writes (max, sum, unnormalised output) to the
 //    workspace, the CTA bumps its (sequence, KV head) counter by its number
 //    of partitions, and the CTA that completes the count merges all
 //    partitions by log-sum-exp.
 //  * Beam groups (GR): one CTA per (group, KV head) attends every member of a
 //    group of sequences that share a prefix of physical blocks: the shared
-//    prefix once with all members' query heads as the N columns, then each
-//    member's own tail with the other columns masked (cayang0802 "Paged
-//    Attention" page, beam-search paragraph: the beams keep one physical
-//    copy of their common blocks).
+//    prefix once with all members' query heads as the N columns (up to 8 or
+//    16), then each member's own tail with the other columns masked
+//    (cayang0802 "Paged Attention" page, beam-search paragraph: the beams
+//    keep one physical copy of their common blocks).  A group may be cut into
+//    equal runs of its stage list, one CTA each, merged like partitions.
 //  * Masked tokens (past context_len, or in a block whose id is out of range)
 //    get score -inf and a zeroed V fragment, so NaN or stale data in unused
 //    slots never reaches the output.
@@ -113,11 +114,13 @@ __device__ __forceinline__ uint32_t stage_offset(int r, int c)
     return (u * Gm::NH + half) * Gm::SUB_BYTES + row * 128 + ((cc ^ (row & 7)) << 4);
 }
 
-// One CTA = one work item: one partition of one (sequence, KV head), whose
-// 16-token stages the NW warps stream in turn (warp w takes stages w, w + NW,
-// ...) through rings of NS stages each, merging their softmax states at the
-// end; or, for short split partitions, up to NW consecutive partitions, one
-// per warp, each warp's state being its partition's result.
+// One CTA = one work item: one partition of one (sequence, KV head, head
+// slice), or one run of a beam group's stage list, whose 16-token stages the
+// NW warps stream in turn (warp w takes stages w, w + NW, ...) through rings
+// of NS stages each, merging their softmax states at the end; or, for short
+// split partitions, up to NW consecutive partitions, one per warp, each
+// warp's state being its partition's result.  NT n8 tiles carry up to 8 * NT
+// query-head columns.
 template <typename T, int D, int B, int NW, int NS, bool GR, int NT>
 __global__ void __launch_bounds__(NW * 32, (Geometry<D, B, NW, NS, NT>::MIN_CTAS))
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
@@ -251,7 +254,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     };
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::BAR_OFF);
-    int* sid = reinterpret_cast<int*>(smem + Gm::SID_OFF);  // [warp][slot][2] block ids
+    int* sid = reinterpret_cast<int*>(smem + Gm::SID_OFF);  // [warp][slot][SID_INTS] records
 
     const int gq = lane >> 2, tq = lane & 3;  // mma fragment row group / column pair
     uint8_t* ring = smem + warp * Gm::RING_BYTES;

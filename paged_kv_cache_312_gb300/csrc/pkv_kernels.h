@@ -103,12 +103,13 @@ cudaError_t launch_decode_cuda_core(const DecodeParams& p, int kv_dtype, cudaStr
 // (sequence, KV head, head slice) adjacent in the grid; the grid is
 // S * Hkv * HS * ceil(max_partitions / cta_parts).  A CTA takes ceil(G / HS)
 // query heads as the mma's N columns: launch_decode_tensor_core up to 8
-// (one n8 tile), launch_decode_tensor_core_wide up to 16 (two tiles).  A CTA that holds one partition
-// spreads it over all its warps; one that holds several gives each warp a
-// partition of its own.  The tensor maps describe k_cache / v_cache as 2-D
-// [NB*Hkv*B rows][D columns] loaded in boxes of 64 columns x min(B, 16) rows.
-// In split mode p.done must be zero; the CTA that finishes the last partition
-// of a (sequence, KV head) merges its partitions.
+// (one n8 tile), launch_decode_tensor_core_wide up to 16 (two tiles).  A CTA
+// that holds one partition spreads it over all its warps; one that holds
+// several gives each warp a partition of its own.  The tensor maps describe
+// k_cache / v_cache as 3-D [D/64 halves][NB*Hkv*B rows][64 columns], loaded
+// in boxes of both halves x min(B, 16) rows.  In split mode p.done must be
+// zero; the CTA that finishes the last partition of a (sequence, KV head,
+// head slice) merges its partitions.
 constexpr int kDecodeTcWarps = 4;
 // Split partitions of at most this many tokens get one warp each (four per
 // CTA), so that a CTA's start-up and end are spread over more KV bytes, when
