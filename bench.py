@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
 # valid only while the kernel source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "4a7ce33260d38795",
-           "bytes_per_launch": {"2": 1109543936, "3": 806343168, "4": 1089596160}}
+TRAFFIC = {"source_sha": "7c998a361ef7f58c",
+           "bytes_per_launch": {"2": 1109143040, "3": 806664448, "4": 1079614208}}
 
 
 def launch_partition(w, max_blocks: int) -> int:

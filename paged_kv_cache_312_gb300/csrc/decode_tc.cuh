@@ -588,91 +588,73 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     auto row_of = [&](int n) -> size_t {
         return GR ? (size_t)(s0 + n / G) * p.num_heads + g * G + n % G : hbase + n;
     };
-    if (!solo) {
-        // ---- a warp's own partition: its softmax state is the partition's
-        // result, written straight to the workspace (columns 8t+2tq, +1)
-        if (warp < np_cta) {
+    // this CTA's partial: index pidx of ncp per (sequence, KV head, head
+    // slice) -- one per CTA, its warps' partitions (or its share of one
+    // partition) merged first -- or (GR) of the group's runs
+    const int ncp = GR ? nparts : (nparts + p.cta_parts - 1) / p.cta_parts;
+    const int pidx = GR ? part : p0 / p.cta_parts;
+    // ---- merge the warps (shared memory reused once every ring is drained):
+    // their states cover one partition (each a share of its stages) or, with
+    // one partition per warp, consecutive partitions of the same sequence
+    __syncthreads();
+    float* wm = reinterpret_cast<float*>(smem) + warp * NC * (D + 2);  // [NC][D], m[NC], l[NC]
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int n = 8 * t + 2 * tq + h;
-                    if (n < ncol) {
-                        const size_t slot = row_of(n) * p.max_partitions + part;
-                        if (gq == 0) p.ws_ml[slot] = make_float2(mr[t][h], lr_[t][h]);
-                        float* o = p.ws_o + slot * D;
-#pragma unroll
-                        for (int i = 0; i < MTILES; ++i) {
-                            o[16 * i + gq] = acc[t][i][h];
-                            o[16 * i + gq + 8] = acc[t][i][2 + h];
-                        }
-                    }
-                }
-            }
+    for (int t = 0; t < NT; ++t) {
+        const int n = 8 * t + 2 * tq;
+        if (gq == 0) {
+            wm[NC * D + n] = mr[t][0];
+            wm[NC * D + n + 1] = mr[t][1];
+            wm[NC * D + NC + n] = lr_[t][0];
+            wm[NC * D + NC + n + 1] = lr_[t][1];
         }
-    } else {
-        // ---- merge the warps (shared memory reused once every ring is drained)
-        __syncthreads();
-        float* wm = reinterpret_cast<float*>(smem) + warp * NC * (D + 2);  // [NC][D], m[NC], l[NC]
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const int n = 8 * t + 2 * tq;
-            if (gq == 0) {
-                wm[NC * D + n] = mr[t][0];
-                wm[NC * D + n + 1] = mr[t][1];
-                wm[NC * D + NC + n] = lr_[t][0];
-                wm[NC * D + NC + n + 1] = lr_[t][1];
-            }
-#pragma unroll
-            for (int i = 0; i < MTILES; ++i) {
-                wm[n * D + 16 * i + gq] = acc[t][i][0];
-                wm[(n + 1) * D + 16 * i + gq] = acc[t][i][1];
-                wm[n * D + 16 * i + gq + 8] = acc[t][i][2];
-                wm[(n + 1) * D + 16 * i + gq + 8] = acc[t][i][3];
-            }
+        for (int i = 0; i < MTILES; ++i) {
+            wm[n * D + 16 * i + gq] = acc[t][i][0];
+            wm[(n + 1) * D + 16 * i + gq] = acc[t][i][1];
+            wm[n * D + 16 * i + gq + 8] = acc[t][i][2];
+            wm[(n + 1) * D + 16 * i + gq + 8] = acc[t][i][3];
         }
-        __syncthreads();
-        const float* sm = reinterpret_cast<const float*>(smem);
-        // four consecutive outputs of one head per thread
-        const bool vec_out = (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
-        for (int idx = threadIdx.x; idx < ncol * D / 4; idx += blockDim.x) {
-            const int n = idx / (D / 4), d = (idx - n * (D / 4)) * 4;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * NC * (D + 2) + NC * D + n]);
-            float den = 0.f;
-            float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float* ww = sm + w * NC * (D + 2);
-                const float mw = ww[NC * D + n];
-                const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
-                den += wt * ww[NC * D + NC + n];
-                const float4 o = *reinterpret_cast<const float4*>(ww + n * D + d);
-                num.x += wt * o.x;
-                num.y += wt * o.y;
-                num.z += wt * o.z;
-                num.w += wt * o.w;
-            }
-            if (nparts <= 1) {
-                const bool pos = den > 0.f;
-                store_out4(p.out, row_of(n) * D + d,
-                           make_float4(pos ? num.x / den : 0.f, pos ? num.y / den : 0.f,
-                                       pos ? num.z / den : 0.f, pos ? num.w / den : 0.f),
-                           p.out_dtype, vec_out);
-            } else {
-                const size_t slot = row_of(n) * p.max_partitions + part;
-                *reinterpret_cast<float4*>(p.ws_o + slot * D + d) = num;
-                if (d == 0) p.ws_ml[slot] = make_float2(M, den);
-            }
-        }
-        if (nparts <= 1) return;
     }
+    __syncthreads();
+    const float* sm = reinterpret_cast<const float*>(smem);
+    // four consecutive outputs of one head per thread
+    const bool vec_out = (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+    for (int idx = threadIdx.x; idx < ncol * D / 4; idx += blockDim.x) {
+        const int n = idx / (D / 4), d = (idx - n * (D / 4)) * 4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm[w * NC * (D + 2) + NC * D + n]);
+        float den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float* ww = sm + w * NC * (D + 2);
+            const float mw = ww[NC * D + n];
+            const float wt = mw == -INFINITY ? 0.f : ex2(mw - M);
+            den += wt * ww[NC * D + NC + n];
+            const float4 o = *reinterpret_cast<const float4*>(ww + n * D + d);
+            num.x += wt * o.x;
+            num.y += wt * o.y;
+            num.z += wt * o.z;
+            num.w += wt * o.w;
+        }
+        if (ncp <= 1) {
+            const bool pos = den > 0.f;
+            store_out4(p.out, row_of(n) * D + d,
+                       make_float4(pos ? num.x / den : 0.f, pos ? num.y / den : 0.f,
+                                   pos ? num.z / den : 0.f, pos ? num.w / den : 0.f),
+                       p.out_dtype, vec_out);
+        } else {
+            const size_t slot = row_of(n) * p.max_partitions + pidx;
+            *reinterpret_cast<float4*>(p.ws_o + slot * D + d) = num;
+            if (d == 0) p.ws_ml[slot] = make_float2(M, den);
+        }
+    }
+    if (ncp <= 1) return;
 
-    // ---- split: the CTA that finishes the last partition of (s, g, head
-    // slice), or (GR) the last part of (group, g), merges them by
-    // log-sum-exp: M = max_i m_i, w_i = 2^(m_i - M),
-    // out = sum_i w_i O_i / sum_i w_i l_i.
+    // ---- split: the CTA that writes the last of the ncp partials of (s, g,
+    // head slice), or (GR) of (group, g), merges them by log-sum-exp:
+    // M = max_i m_i, w_i = 2^(m_i - M), out = sum_i w_i O_i / sum_i w_i l_i.
     __shared__ int is_last;
     __syncthreads();  // this CTA's partition results are written ...
     if (threadIdx.x == 0) {
@@ -682,18 +664,18 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         unsigned prev;
         asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
                      : "=r"(prev)
-                     : "l"(&p.done[sg]), "r"((unsigned)np_cta)
+                     : "l"(&p.done[sg]), "r"(1u)
                      : "memory");
-        is_last = prev == (unsigned)(nparts - np_cta);
+        is_last = prev == (unsigned)(ncp - 1);
     }
     __syncthreads();
     if (!is_last) return;
     constexpr int NTH = NW * 32;
-    float* wts = reinterpret_cast<float*>(smem) + NW * NC * (D + 2);  // [ncol][nparts] weights
+    float* wts = reinterpret_cast<float*>(smem) + NW * NC * (D + 2);  // [ncol][ncp] weights
     float* hinv = wts + Gm::WCACHE;                                    // [NC]
     float* hmax = hinv + NC;                                           // [NC]
     float4* red = reinterpret_cast<float4*>(hmax + NC);                // [NTH] partial sums
-    const bool cached = ncol * nparts <= Gm::WCACHE;
+    const bool cached = ncol * ncp <= Gm::WCACHE;
     for (int n = warp; n < ncol; n += NW) {
         const size_t base = row_of(n) * p.max_partitions;
         // the (max, sum) pairs of the first 64 partitions are read once and
@@ -703,26 +685,26 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int i = lane + 32 * r;
-            ml[r] = i < nparts ? __ldcg(&p.ws_ml[base + i]) : make_float2(-INFINITY, 0.f);
+            ml[r] = i < ncp ? __ldcg(&p.ws_ml[base + i]) : make_float2(-INFINITY, 0.f);
             M = fmaxf(M, ml[r].x);
         }
-        for (int i = lane + 64; i < nparts; i += 32) M = fmaxf(M, __ldcg(&p.ws_ml[base + i]).x);
+        for (int i = lane + 64; i < ncp; i += 32) M = fmaxf(M, __ldcg(&p.ws_ml[base + i]).x);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float den = 0.f;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int i = lane + 32 * r;
-            if (i < nparts) {
+            if (i < ncp) {
                 const float w = ml[r].x == -INFINITY ? 0.f : ex2(ml[r].x - M);
-                if (cached) wts[n * nparts + i] = w;
+                if (cached) wts[n * ncp + i] = w;
                 den += w * ml[r].y;
             }
         }
-        for (int i = lane + 64; i < nparts; i += 32) {
+        for (int i = lane + 64; i < ncp; i += 32) {
             const float2 mli = __ldcg(&p.ws_ml[base + i]);
             const float w = mli.x == -INFINITY ? 0.f : ex2(mli.x - M);
-            if (cached) wts[n * nparts + i] = w;
+            if (cached) wts[n * ncp + i] = w;
             den += w * mli.y;
         }
 #pragma unroll
@@ -747,10 +729,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             const size_t base = row_of(n) * p.max_partitions;
             const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * D) + d4;
 #pragma unroll 16
-            for (int i = k; i < nparts; i += K) {
+            for (int i = k; i < ncp; i += K) {
                 float w;
                 if (cached) {
-                    w = wts[n * nparts + i];
+                    w = wts[n * ncp + i];
                 } else {
                     const float mi = __ldcg(&p.ws_ml[base + i]).x;
                     w = mi == -INFINITY ? 0.f : ex2(mi - hmax[n]);
