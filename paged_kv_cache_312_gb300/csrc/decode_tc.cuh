@@ -92,12 +92,13 @@ struct Geometry {
     // partition weights cached for the in-kernel merge (after the warp merge)
     static constexpr int WCACHE = ((DATA_BYTES - MERGE_BYTES) / 4 - 2 * NC - NW * 32 * 4 - 4) & ~3;
     static_assert(WCACHE > 0, "room for merge weights");
-    // CTAs per SM the register allocation is held to (0: the compiler's
-    // choice).  The shared memory admits 3 CTAs at D = 128 (~66 KB each),
-    // which the compiler's choice already fits; at D = 64 it admits 6 (~34
-    // KB), and there the compiler's choice would spill, so the bound is 6
-    // CTAs, or 5 for two column tiles (96 registers a thread)
-    static constexpr int MIN_CTAS = D == 128 ? 0 : (NT == 1 ? 6 : 5);
+    // CTAs per SM the register allocation is held to: as many as the shared
+    // memory admits (D = 128: 3 of ~66 KB, up to 168 registers a thread;
+    // D = 64: 6 of ~34 KB, 80 registers), or 5 for two column tiles at D = 64
+    // (96).  Left to itself the compiler took 96 registers at D = 128, and the
+    // freedom to use more is worth 1-4 % of HBM bandwidth there; at D = 64 it
+    // spilled.
+    static constexpr int MIN_CTAS = D == 128 ? 3 : (NT == 1 ? 6 : 5);
     static_assert(SUB_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
     static_assert(STAGE_BYTES % 1024 == 0 && RING_BYTES % 1024 == 0, "stage alignment");
 };
@@ -149,6 +150,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int* glen = reinterpret_cast<int*>(smem + Gm::GM_OFF);  // GR: members' context lengths
     int s0 = 0, nm = 1, shared = 0, nsh = 0, qbase = 0;
+    // non-GR: block ids of this warp's first 32 stages, read before the
+    // context length arrives (see below)
+    int spec_ids[IDS];
+    bool spec_solo = true;
     if constexpr (GR) {
         // slot b = (gi * Hkv + g) * parts + part: part `part` of the group's
         // stage list (shared prefix, then each member's tail) for KV head g
@@ -206,6 +211,23 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         const int GC = (G + HS - 1) / HS;
         hb = hs * GC;
         ncol = min(GC, G - hb);
+        // The first window of block ids depends on the context length only
+        // through the partition-to-warp mapping, which is known in advance
+        // unless a CTA of several partitions ends up with one: so it is read
+        // now, overlapping the length's round trip, and used below when the
+        // guess holds (entries past the context are then ignored).
+        {
+            spec_solo = p.cta_parts == 1;
+            const int gpart = grp * p.cta_parts + (spec_solo ? 0 : warp);
+            const int64_t gtok = (int64_t)gpart * p.partition_tokens +
+                                 (spec_solo ? warp + lane * NW : lane) * 16;
+            const int32_t* row = p.block_tables + (size_t)s * p.max_blocks;
+#pragma unroll
+            for (int u = 0; u < IDS; ++u) {
+                const int64_t tok = gtok + u * B;
+                spec_ids[u] = tok < (int64_t)p.max_blocks * B ? row[tok / B] : -1;
+            }
+        }
         L = p.context_lens[s];
         if (L < 0 || (int64_t)L > (int64_t)p.max_blocks * B) {
             if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
@@ -289,7 +311,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             int id = -1;
             const int tok = tk0 + u * B;  // first token of the box
             if (j < cnt && tok < endr) {
-                id = tab[tok / B];
+                id = !GR && jbase == 0 && solo == spec_solo ? spec_ids[u] : tab[tok / B];
                 if (id < 0 || id >= p.num_blocks) {
                     atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
                     id = -1;
