@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
 # valid only while the kernel source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "7c998a361ef7f58c",
-           "bytes_per_launch": {"2": 1109143040, "3": 806664448, "4": 1079614208}}
+TRAFFIC = {"source_sha": "45581cb2ce32168a",
+           "bytes_per_launch": {"2": 1109425664, "3": 806522368, "4": 1079490304}}
 
 
 def launch_partition(w, max_blocks: int) -> int:
