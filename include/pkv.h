@@ -127,11 +127,13 @@ int pkv_kv_write(void* k_cache, void* v_cache, const void* key, const void* valu
  * partition_size : 0 = each (sequence, KV head) is handled in one pass.
  *                > 0 = split-context decode: each sequence's tokens are cut
  *                into partitions of this many tokens (a multiple of
- *                block_size); each partition writes its max, sum and
- *                unnormalised output to `workspace`, and the partitions
- *                are merged by log-sum-exp: inside the same launch on the
- *                tensor-core kernel, by a second kernel otherwise.  (The
- *                pages are silent on splitting; the merge is exact in real
+ *                block_size), each attended with its own softmax state (max,
+ *                sum, unnormalised output), and the partitions are merged by
+ *                log-sum-exp through `workspace`: inside the same launch on
+ *                the tensor-core kernel (which first merges the up to four
+ *                partitions one CTA holds, one per warp, and writes one
+ *                partial per CTA), by a second kernel otherwise.  (The pages
+ *                are silent on splitting; the merge is exact in real
  *                arithmetic.)
  * workspace    : device scratch of at least pkv_decode_workspace_bytes(...)
  *                bytes, 256-byte aligned, when partition_size > 0 (else may be
