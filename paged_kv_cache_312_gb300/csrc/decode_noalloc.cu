@@ -84,9 +84,9 @@ extern "C" int pkv_paged_decode_attention_noalloc(
     void* scratch = nullptr;
     int rc = scratch_address(&scratch);
     if (rc != PKV_OK) return rc;
-    // Nothing in the scratch needs clearing: for every sequence with more
-    // than one partition, the partition kernel of this call writes each
-    // (max, sum, output) slot the merge kernel then reads, in stream order.
+    // The scratch needs no clearing here: the call below zeroes the
+    // completion counters the tensor-core kernel uses, and every (max, sum,
+    // output) slot a merge reads is written earlier in the same call.
     return pkv_paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                                       block_size, num_kv_heads, num_seqs, num_heads, head_dim,
                                       max_blocks_per_seq, num_blocks, kv_dtype, out_dtype,
