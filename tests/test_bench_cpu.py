@@ -1,0 +1,65 @@
+"""bench.py on the host: the reference arm's JSON line (the oracle timed on
+the host cores) and the launch rules the GPU arm uses, without a GPU."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+import bench
+from workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"]["workload"] == WORKLOADS[2].name
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_warmup_below_three_is_refused():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--warmup", "2"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0 and "--warmup" in r.stderr
+
+
+@pytest.mark.parametrize("key", [2, 3, 4, 5])
+def test_launch_partition_rule(key):
+    # a workload's own split if it names one; else one pass while every
+    # context fits in 2048 tokens, 1024-token partitions beyond
+    w = WORKLOADS[key]
+    for max_blocks in (1, 2048 // w.block_size, 2048 // w.block_size + 1, 32768 // w.block_size):
+        P = bench.launch_partition(w, max_blocks)
+        if w.partition_size:
+            assert P == w.partition_size
+        elif max_blocks * w.block_size <= 2048:
+            assert P == 0
+        else:
+            assert P == 1024
+
+
+def test_sweep_workloads_cover_the_sweep_grid():
+    seen = set()
+    for B in bench.SWEEP_BLOCKS:
+        for G in bench.SWEEP_GROUPS:
+            for D in bench.SWEEP_DIMS:
+                w = bench.sweep_workload(B, G, D)
+                assert (w.block_size, w.num_heads // w.num_kv_heads, w.head_dim) == (B, G, D)
+                assert w.num_kv_heads == 8 and w.dtype == "bf16"
+                seen.add(w.name)
+    assert len(seen) == len(bench.SWEEP_BLOCKS) * len(bench.SWEEP_GROUPS) * len(bench.SWEEP_DIMS)
