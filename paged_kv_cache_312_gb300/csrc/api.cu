@@ -401,6 +401,8 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
                             fn);
         if (max_members < 0)
             return pkv_fail(PKV_ERR_SHAPE, "%s: max_members %d < 0", fn, max_members);
+        if ((int64_t)num_groups * num_kv_heads * group_parts >= (1ll << 31))
+            return pkv_fail(PKV_ERR_SHAPE, "%s: more than 2^31 work items", fn);
     }
 
     DecodeParams p;

@@ -381,12 +381,12 @@ def test_grouped_decode_rejects_bad_arguments_on_host():
     P = ctypes.c_void_p
 
     def call(**kw):
-        a = dict(nk=256, nv=256, gs=256, G=1, kv=2, Hq=8, parts=1, ws=0, wsb=0, mm=0)
+        a = dict(nk=256, nv=256, gs=256, G=1, kv=2, Hq=8, Hkv=4, S=2, parts=1, ws=0, wsb=0, mm=0)
         a.update(kw)
         return L.pkv_paged_decode_grouped(P(256), P(256), P(a["nk"]), P(a["nv"]), P(256), P(256),
                                           P(256), P(256), P(a["gs"]), P(256), a["G"], a["mm"],
-                                          0.1, 16, 4, 2, a["Hq"], 128, 4, 10, a["kv"], 0,
-                                          a["parts"], P(a["ws"]), a["wsb"], P(0))
+                                          0.1, 16, a["Hkv"], a["S"], a["Hq"], 128, 4, 10, a["kv"],
+                                          0, a["parts"], P(a["ws"]), a["wsb"], P(0))
     need = L.pkv_decode_workspace_bytes(2, 8, 128, 4, 1)
     assert call(gs=0) == -1          # no group table
     assert call(nv=0) == -1          # new_k without new_v
@@ -397,6 +397,7 @@ def test_grouped_decode_rejects_bad_arguments_on_host():
     assert call(mm=-1) == -2         # a negative member bound
     assert call(nk=0, nv=0, G=0) == -2  # attention only: same group checks
     assert call(parts=65) == -2      # more parts than the kernel takes
+    assert call(G=65535, S=65535, Hq=65535, Hkv=65535) == -2  # 2^32 work items
     assert call(parts=4) == -8       # parts need a workspace ...
     assert call(parts=4, ws=256, wsb=need - 1) == -8  # ... of the stated size
     assert call(parts=4, ws=512 + 16, wsb=need) == -10  # ... 256-byte aligned
