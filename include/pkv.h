@@ -52,7 +52,7 @@ extern "C" {
 #define PKV_ERR_NULL -1        /* a required pointer is NULL                  */
 #define PKV_ERR_SHAPE -2       /* sizes out of range or inconsistent          */
 #define PKV_ERR_DTYPE -3       /* unknown dtype code                          */
-#define PKV_ERR_UNSUPPORTED -4 /* valid request this build does not implement */
+#define PKV_ERR_UNSUPPORTED -4 /* valid request the library does not implement */
 #define PKV_ERR_CUDA -5        /* a CUDA runtime/driver call failed           */
 #define PKV_ERR_BOUNDS -6      /* a kernel saw an out-of-range id (status)    */
 #define PKV_ERR_OOM -7         /* allocator: not enough free blocks           */

@@ -2,7 +2,7 @@
 
 Each translation unit is compiled by nvcc in parallel, then linked into
 paged_kv_cache_312_gb300/_build/libpkv.so.  The CUDA runtime is linked
-statically; the driver entry point for tensor-map encoding is looked up at run
+statically; the CUDA driver entry point for tensor-map encoding is looked up at run
 time, so the library needs no libcuda at link time.
 """
 from __future__ import annotations
