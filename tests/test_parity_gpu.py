@@ -461,6 +461,7 @@ STEP_CASES = [  # dtype, Hq, Hkv, D, B, partition
     ("bf16", 32, 32, 128, 16, 0), ("bf16", 32, 8, 128, 16, 64), ("f16", 16, 2, 64, 8, 0),
     ("bf16", 8, 1, 128, 32, 32), ("f16", 8, 8, 128, 16, 512),
     ("bf16", 32, 2, 128, 16, 0), ("f16", 48, 2, 64, 8, 32),  # G = 16, G = 24 (2 slices)
+    ("bf16", 16, 4, 128, 16, 16),  # 16-token partitions: one per warp, four to a CTA
     ("f32", 4, 4, 64, 16, 0),  # CUDA-core kernel path
 ]
 
