@@ -382,6 +382,41 @@ def test_lse_combine_equals_one_pass(P):
                                        atol=1e-13)
 
 
+def _merged_state(parts):
+    # one (max, sum, unnormalised output) for a run of partitions: the state
+    # a single partition over their union would have
+    M = max(m for m, _, _ in parts)
+    w = [np.exp(m - M) for m, _, _ in parts]
+    return (M, sum(wi * l for wi, (_, l, _) in zip(w, parts)),
+            sum(wi * O for wi, (_, _, O) in zip(w, parts)))
+
+
+@pytest.mark.parametrize("P,fan", [(16, 4), (7, 4), (32, 3), (1, 2)])
+def test_two_level_lse_merge_equals_the_flat_one(P, fan):
+    # merging runs of `fan` consecutive partitions first, then the runs'
+    # states (the tensor-core kernel's order with one partition per warp,
+    # four to a CTA), is the same log-sum-exp identity regrouped: it equals
+    # the flat merge and the one-pass softmax to rounding; with an empty run
+    # (max -inf) it still does
+    S, Hq, Hkv, D, B = 2, 4, 2, 16, 16
+    Kl, Vl = _random_logical(53, S, 300, Hkv, D, torch.bfloat16, Lmin=100)
+    q = torch.randn(S, Hq, D).to(torch.bfloat16)
+    kc, vc, bt, cl = _scatter_case(Kl, Vl, B, 60, torch.bfloat16, seed=7, Hq=Hq)
+    full = oracle.paged_decode_attention(q, kc, vc, bt, cl, 0.2, B, Hkv)
+    G = Hq // Hkv
+    for s in range(S):
+        K = oracle.gather_sequence(kc, bt[s], int(cl[s]))
+        V = oracle.gather_sequence(vc, bt[s], int(cl[s]))
+        for h in range(Hq):
+            parts = oracle.decode_partitions(q[s, h].double().numpy(), K[:, h // G], V[:, h // G],
+                                             0.2, P)
+            runs = [_merged_state(parts[i:i + fan]) for i in range(0, len(parts), fan)]
+            runs.append((-np.inf, 0.0, np.zeros(D)))  # a run with no tokens
+            two = oracle.lse_combine(runs)
+            np.testing.assert_allclose(two, oracle.lse_combine(parts), rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(two, full[s, h], rtol=1e-12, atol=1e-13)
+
+
 # --------------------------------------------------------------------------
 # Cache write and copy-on-write copy.
 # --------------------------------------------------------------------------
