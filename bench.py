@@ -42,20 +42,39 @@ METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak), decode steps/sec
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
-# one ncu capture of each workload's launch (profiles/ncu_decode_tc_*.md),
-# valid only while the kernel source hashes to `source_sha`.
+# one ncu capture of each workload's launch, valid only while the kernel
+# source hashes to `source_sha`.
 TRAFFIC = {"source_sha": "45581cb2ce32168a",
            "bytes_per_launch": {"2": 1109425664, "3": 806522368, "4": 1079490304}}
 
 
-def launch_partition(w, max_blocks: int) -> int:
+def launch_partition(w, max_blocks: int, lens=None) -> int:
     """Partition size (tokens) the benchmark launches a workload with: the
-    workload's own split if it names one; else one pass per (sequence, KV
-    head) while every context fits in 2048 tokens, and 1024-token partitions
-    beyond (so that a few long contexts do not finish last)."""
+    workload's own split if it names one; one pass per (sequence, KV head)
+    for a ragged batch (see `work_plan`: longest first, a long context
+    starts at once and needs no split) or while every context fits in 2048
+    tokens; 1024-token partitions beyond (so that a few long contexts do not
+    finish last)."""
     if w.partition_size:
         return w.partition_size
+    if lens is not None and ragged(lens):
+        return 0
     return 0 if max_blocks * w.block_size <= 2048 else 1024
+
+
+def ragged(lens) -> bool:
+    """A batch whose longest context is more than three times the mean."""
+    L = [int(x) for x in lens]
+    return len(L) > 0 and max(L) > 3 * (sum(L) / len(L))
+
+
+def work_plan(w, lens, P: int) -> bool:
+    """Whether the benchmark gives a launch the library's work plan (a
+    workspace): always for split launches (the library plans every split
+    launch of up to 4096 sequences), and for unsplit ones when the batch is
+    ragged, so that its long sequences start first.  A host scheduler knows
+    its lengths and can make the same choice."""
+    return P > 0 or ragged(lens)
 
 
 def kernel_sha() -> str:
@@ -63,7 +82,8 @@ def kernel_sha() -> str:
     (the traffic figures above hold only for the code they were captured
     from)."""
     h = hashlib.sha256()
-    for name in ("decode_tc.cu", "decode_tc.cuh", "tc_common.cuh"):
+    for name in ("decode_tc.cu", "decode_wide.cu", "decode_group.cu", "decode_tc.cuh",
+                 "tc_common.cuh"):
         text = open(os.path.join(ROOT, "paged_kv_cache_312_gb300", "csrc", name)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
@@ -97,9 +117,11 @@ class Step:
             self.setup_vals = torch.cat([case.prefix_v.reshape(-1, Hkv, D)] + case.suffix_v)
             self.q, self.new_key, self.new_value = case.q, case.new_key, case.new_value
             self.unique_blocks = int(mgr.stats()[2])
+            self.pool_order = case.pool_order
         else:
             case = make_decode_case(w, seed=seed, poison=not w.writes_new_token)
             self.k_cache, self.v_cache, self.q = case.k_cache, case.v_cache, case.q
+            self.pool_order = case.pool_order
             self.setup_slots = None
             if w.writes_new_token:
                 mgr = allocator_cls(case.num_blocks, w.block_size, free_order=case.pool_order)
@@ -110,7 +132,10 @@ class Step:
             else:
                 self.tables, self.lens = case.block_tables, case.context_lens
             self.unique_blocks = None
-        self.P = launch_partition(w, self.tables.shape[1]) if partition is None else partition
+        self.P = launch_partition(w, self.tables.shape[1], self.lens) if partition is None \
+            else partition
+        # the beam workload runs through the beam-group call, which has no plan
+        self.plan = self.unique_blocks is None and work_plan(w, self.lens.tolist(), self.P)
         if self.slots is not None:
             # the step's new tokens sit at position L-1 of each sequence (what
             # the decode-step call writes, through the table)
@@ -120,12 +145,90 @@ class Step:
         L = self.lens.to(torch.int64)
         b = w.torch_dtype.itemsize
         self.kv_bytes = int(L.sum()) * 2 * w.num_kv_heads * w.head_dim * b
+        # beam workload: K and V of every physical block in use, counted once
+        self.unique_bytes = None if self.unique_blocks is None else \
+            self.unique_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2 * b
         S = L.numel()
         io = S * w.num_heads * w.head_dim * (b + 4) + int((L + w.block_size - 1).div(
             w.block_size, rounding_mode="floor").sum()) * 4 + S * 4
         self.attn_bytes = self.kv_bytes + io  # KV + q + fp32 out + table entries + lens
         if self.slots is not None:  # the decode step also reads and stores the new K/V
             self.attn_bytes += 2 * 2 * S * w.num_kv_heads * w.head_dim * b
+
+
+class GpuStep:
+    """Device side of one decode step of a workload, as the benchmark times
+    it: the cache on the device (the beam history written into it), the
+    step's inputs packed in one pinned host buffer and one device buffer
+    (views per tensor), the fp32 output, the workspace, and run(), the calls
+    of one step: the copy-on-write copies (if any), then one decode call that
+    appends each sequence's new token and attends (beam groups: one CTA per
+    group and KV head)."""
+
+    def __init__(self, pkv, st: Step, dev, grouped: bool, gparts: int = 1):
+        w = st.w
+        self.pkv, self.st, self.w, self.dev = pkv, st, w, dev
+        self.grouped, self.gparts = grouped, gparts
+        self.kc, self.vc = st.k_cache.to(dev), st.v_cache.to(dev)
+        if st.setup_slots is not None:  # beam history
+            pkv.kv_write(self.kc, self.vc, st.setup_keys.to(dev), st.setup_vals.to(dev),
+                         st.setup_slots.to(dev))
+        self.has_write = st.slots is not None
+        inputs = [st.q, st.tables, st.lens, st.pairs]
+        if self.has_write:
+            inputs += [st.new_key, st.new_value]
+        if grouped:
+            S_ = st.q.shape[0]
+            gstart = torch.arange(0, S_ + 1, w.beam_width, dtype=torch.int32)
+            shared = pkv.group_shared_tokens(st.tables, st.lens, gstart, w.block_size)
+            inputs += [gstart, shared]
+        self.h_pack, views = pack_inputs(inputs, dev)
+        self.q, self.bt, self.cl, self.pairs = views[:4]
+        self.nk = self.nv = None
+        if self.has_write:
+            self.nk, self.nv = views[4:6]
+        if grouped:
+            self.gs, self.sh = views[-3:-1]
+        self.d_pack = views[-1]
+        S, Hq, D = self.q.shape
+        self.out = torch.empty((S, Hq, D), dtype=torch.float32, device=dev)
+        self.ws = None
+        if st.P or (st.plan and not grouped):
+            # split scratch, or (unsplit) the optional work plan
+            self.ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D,
+                                                             self.bt.shape[1] * w.block_size,
+                                                             st.P),
+                                  dtype=torch.uint8, device=dev)
+        elif gparts > 1:
+            self.ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, gparts, 1),
+                                  dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        # one decode kernel per call, the append fused in (split mode also
+        # merges inside it, after a driver memset of its completion counters)
+        self.launches_per_step = (1 if self.pairs.shape[0] else 0) + 1
+
+    def run(self, ev=None, stream=None):
+        """One step on `stream` (default self.stream); `ev`, if given, is
+        recorded between the copy-on-write copies and the decode call."""
+        pkv, w, st = self.pkv, self.w, self.st
+        sm = self.stream if stream is None else stream
+        if self.pairs.shape[0]:
+            pkv.kv_copy_blocks(self.kc, self.vc, self.pairs, stream=sm)
+        if ev is not None:
+            ev.record(sm)
+        if self.grouped:  # append the new tokens and attend, one CTA per (group, KV head)
+            pkv.paged_decode_grouped(self.out, self.q, self.kc, self.vc, self.bt, self.cl,
+                                     self.gs, self.sh, w.scale, w.block_size, w.num_kv_heads,
+                                     new_k=self.nk, new_v=self.nv, parts=self.gparts,
+                                     workspace=self.ws, max_members=w.beam_width, stream=sm)
+        elif self.has_write:  # append the new tokens and attend, one call
+            pkv.decode_step(self.out, self.q, self.nk, self.nv, self.kc, self.vc, self.bt,
+                            self.cl, w.scale, w.block_size, w.num_kv_heads, partition_size=st.P,
+                            workspace=self.ws, stream=sm)
+        else:
+            pkv.paged_decode_attention(self.out, self.q, self.kc, self.vc, self.bt, self.cl,
+                                       w.scale, w.block_size, w.num_kv_heads,
+                                       partition_size=st.P, workspace=self.ws, stream=sm)
 
 
 # ---------------------------------------------------------------------------
@@ -206,74 +309,49 @@ def measured_peaks():
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def run_gpu(args, rank, world, local_rank):
-    import paged_kv_cache_312_gb300 as pkv
-    import __graft_entry__
+EXTRA_WORKLOADS = (3, 4, 5)
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth (context beside the measured peak)
 
-    __graft_entry__.build()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    st = Step(args.workload, args.seed + rank, pkv.BlockAllocator,  # independent problems
-              partition=args.partition)
+
+def step_kind(st, grouped: bool, gparts: int) -> str:
     w = st.w
-    kc, vc = st.k_cache.to(dev), st.v_cache.to(dev)
-    if st.setup_slots is not None:  # beam history
-        pkv.kv_write(kc, vc, st.setup_keys.to(dev), st.setup_vals.to(dev), st.setup_slots.to(dev))
-    # the step's inputs live in one pinned host buffer and one device buffer
-    # (views per tensor), so a step's host->device traffic is a single copy
-    has_write = st.slots is not None
-    # beam groups: the beams of a group (consecutive sequences) attend their
-    # shared prompt blocks in one CTA per (group, KV head)
-    grouped = st.unique_blocks is not None and not args.ungrouped
-    inputs = [st.q, st.tables, st.lens, st.pairs]
-    if has_write:
-        inputs += [st.new_key, st.new_value]
-    if grouped:
-        S_ = st.q.shape[0]
-        gstart = torch.arange(0, S_ + 1, w.beam_width, dtype=torch.int32)
-        shared = pkv.group_shared_tokens(st.tables, st.lens, gstart, w.block_size)
-        inputs += [gstart, shared]
-    h_pack, views = pack_inputs(inputs, dev)
-    q, bt, cl, pairs = views[:4]
-    if has_write:
-        nk, nv = views[4:6]
-    if grouped:
-        gs_d, sh_d = views[-3:-1]
-    S, Hq, D = q.shape
-    out = torch.empty((S, Hq, D), dtype=torch.float32, device=dev)
-    ws = None
-    gparts = args.group_parts if grouped else 1
-    if st.P:
-        ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, bt.shape[1] * w.block_size, st.P),
-                         dtype=torch.uint8, device=dev)
-    elif gparts > 1:
-        ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, gparts, 1), dtype=torch.uint8,
-                         device=dev)
-    d_pack = views[-1]
-    stream = torch.cuda.current_stream(dev)
+    return (("cow-copy + " if st.pairs.shape[0] else "") +
+            ("paged_decode_grouped (beam groups of %d: shared prompt blocks read once per "
+             "group; each group's stages over %d CTA(s) a KV head, merged in the launch; new "
+             "tokens appended inside the attention launch)" % (w.beam_width, gparts)
+             if grouped else
+             "decode_step (new tokens appended inside the attention launch)"
+             if st.slots is not None else "paged_decode_attention"))
 
-    def step(ev=None):
-        if pairs.shape[0]:
-            pkv.kv_copy_blocks(kc, vc, pairs, stream=stream)
-        if ev is not None:
-            ev.record(stream)
-        if grouped:  # append the new tokens and attend, one CTA per (group, KV head)
-            pkv.paged_decode_grouped(out, q, kc, vc, bt, cl, gs_d, sh_d, w.scale, w.block_size,
-                                     w.num_kv_heads, new_k=nk if has_write else None,
-                                     new_v=nv if has_write else None, parts=gparts,
-                                     workspace=ws, max_members=w.beam_width, stream=stream)
-        elif has_write:  # append the new tokens and attend, one call
-            pkv.decode_step(out, q, nk, nv, kc, vc, bt, cl, w.scale, w.block_size,
-                            w.num_kv_heads, partition_size=st.P, workspace=ws, stream=stream)
-        else:
-            pkv.paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, w.block_size,
-                                       w.num_kv_heads, partition_size=st.P, workspace=ws,
-                                       stream=stream)
 
-    # one decode kernel per call, the append fused in (split mode also merges
-    # inside it, after a driver memset of its completion counters)
-    launches_per_step = (1 if pairs.shape[0] else 0) + 1
-    for _ in range(args.warmup):
+def config_of(st, grouped: bool, gparts: int, world: int) -> dict:
+    """The `config` object of a workload's line (the same on both arms)."""
+    w = st.w
+    cfg = {"workload": w.name, "num_seqs": int(st.q.shape[0]), "num_heads": w.num_heads,
+           "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+           "partition_size": st.P, "work_plan": bool(st.plan and not grouped),
+           "kv_bytes_per_step": st.kv_bytes,
+           "group_parts": gparts if grouped else None,
+           "step": step_kind(st, grouped, gparts),
+           "l2": "inputs larger than L2 (KV %.2f GB vs 129 MB L2), no flush" % (st.kv_bytes / 1e9),
+           "parallelism": "replicas" if world > 1 else "single GPU"}
+    if st.unique_blocks is not None:
+        cfg["unique_kv_bytes"] = st.unique_bytes
+    return cfg
+
+
+def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gparts,
+            e2e_alloc=False):
+    """Times one workload's step on this rank's GPU: K steps back to back
+    between two events (the value), then K more with events around each
+    decode call (the roofline), then end to end through the public API from
+    pinned host buffers.  Returns the workload's line (without cpu_baseline)."""
+    w = st.w
+    dev = torch.device("cuda", local_rank)
+    g = GpuStep(pkv, st, dev, grouped, gparts)
+    step, stream, out = g.run, g.stream, g.out
+    S, Hq, D = out.shape
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize(dev)
     assert pkv.device_status() == 0
@@ -289,7 +367,7 @@ def run_gpu(args, rank, world, local_rank):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         step()
     t1.record(stream)
     torch.cuda.synchronize(dev)
@@ -299,19 +377,19 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     total_ms = max_over_ranks(total_ms, world)
-    ms_per_step = total_ms / args.steps
+    ms_per_step = total_ms / steps
     assert pkv.device_status() == 0
 
     # ---- roofline pass: the same K steps with events around each decode
     # call, for that kernel's own average duration
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     torch.cuda.synchronize(dev)
-    for i in range(args.steps):
+    for i in range(steps):
         step(mids[i])
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
-    attn_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    attn_ms = [mids[i].elapsed_time(ends[i]) for i in range(steps)]
     assert pkv.device_status() == 0
 
     # ---- end to end through the public API with pinned host buffers: every
@@ -319,73 +397,271 @@ def run_gpu(args, rank, world, local_rank):
     # reads the output back and synchronises
     e2e = None
     if not args.no_e2e:
-        h_out = torch.empty((S, Hq, D), dtype=torch.float32).pin_memory()
-        h2d = h_pack.numel()
-        d2h = h_out.numel() * h_out.element_size()
-        k = max(1, min(args.steps, 50))
-        torch.cuda.synchronize(dev)
-        w0 = time.perf_counter()
-        for _ in range(k):
-            d_pack.copy_(h_pack, non_blocking=True)
-            step()
-            h_out.copy_(out, non_blocking=True)
-            stream.synchronize()
-        e2e_s = (time.perf_counter() - w0) / k
-        e2e = {"value": round(st.kv_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
-               "ms_per_step": round(e2e_s * 1e3, 4), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": k,
-               "inputs": "q, block tables, lengths, CoW pairs, new K/V in one pinned buffer"}
+        e2e = end_to_end(g, st, dev, max(1, min(steps, 50)), graphs=not args.no_graph)
+    launches = g.launches_per_step
+    del g
+    torch.cuda.empty_cache()
 
     peak, peak_src = measured_peaks()
     attn_avg = statistics.mean(attn_ms)
-    achieved = st.attn_bytes / (attn_avg * 1e-3) / 1e9
+    # beam groups: the bytes the launch must read are the physical blocks in
+    # use, each once (shared prompt blocks included once), not the logical
+    # KV of every beam
+    alg_bytes = st.attn_bytes if st.unique_bytes is None else \
+        st.attn_bytes - st.kv_bytes + st.unique_bytes
+    achieved = alg_bytes / (attn_avg * 1e-3) / 1e9
     value = st.kv_bytes * world / (ms_per_step * 1e-3) / 1e9
-    tr = TRAFFIC["bytes_per_launch"].get(str(args.workload)) \
-        if TRAFFIC["source_sha"] == kernel_sha() else None
+    sha = kernel_sha()
+    tr = TRAFFIC["bytes_per_launch"].get(str(w.key)) if TRAFFIC["source_sha"] == sha else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded N(0,1) values, shuffled block pool)",
-        "config": {"workload": w.name, "num_seqs": S, "num_heads": Hq,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": D, "block_size": w.block_size,
-                   "partition_size": st.P, "kv_bytes_per_step": st.kv_bytes,
-                   "group_parts": gparts if grouped else None,
-                   "step": ("cow-copy + " if pairs.shape[0] else "") +
-                   ("paged_decode_grouped (beam groups of %d: shared prompt blocks read once "
-                    "per group; each group's stages over %d CTA(s) a KV head, merged in the "
-                    "launch; new tokens appended inside the attention launch)"
-                    % (w.beam_width, gparts)
-                    if grouped else
-                    "decode_step (new tokens appended inside the attention launch)"
-                    if has_write else "paged_decode_attention"),
-                   "l2": "inputs larger than L2 (KV %.2f GB vs 129 MB L2), no flush" %
-                   (st.kv_bytes / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": config_of(st, grouped, gparts, world),
         "steps_per_s": round(1e3 / ms_per_step, 2),
         "pct_hbm_peak": round(100 * value / world / peak, 2),
+        "pct_nominal_hbm_peak": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches * steps,
         "roofline": {"bound": "hbm", "kernel": ("paged_decode_grouped" if grouped else
-                                                "decode_step" if has_write else
+                                                "decode_step" if st.slots is not None else
                                                 "paged_decode_attention") +
                      (" call: tensor-core decode kernel with in-kernel log-sum-exp merge "
                       "(+ counter memset)" if st.P or gparts > 1 else " (tensor-core kernel)"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": tr,
-                     "algorithmic_bytes_per_launch": st.attn_bytes,
+                     "frac": round(achieved / peak, 4),
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "traffic": tr, "traffic_source_sha": sha if tr is not None else None,
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "algorithmic_bytes": "unique KV (every physical block in use once) + q + "
+                                          "fp32 out + table entries + new K/V"
+                     if st.unique_bytes is not None else
+                     "KV of every attended token + q + fp32 out + table entries" +
+                     (" + new K/V" if st.slots is not None else ""),
                      "avg_launch_ms": round(attn_avg, 5),
-                     "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src
+                     "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs); nominal %.0f GB/s" %
+                     (peak_src, NOMINAL_HBM_GBS)
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
     }
+    if st.unique_blocks is not None:
+        line["pct_hbm_peak_unique_bytes"] = round(
+            100 * st.unique_bytes / (attn_avg * 1e-3) / 1e9 / peak, 2)
     if st.slots is not None and rank == 0:
         line["host_allocator"] = host_allocator_timing(st, pkv, grouped)
-    if st.unique_blocks is not None:
-        ub = st.unique_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2 * 2
-        line["config"]["unique_kv_bytes"] = ub
-        line["pct_hbm_peak_unique_bytes"] = round(100 * ub / (attn_avg * 1e-3) / 1e9 / peak, 2)
-    return line, st
+        if e2e_alloc and not args.no_e2e and not grouped:
+            line["e2e_with_allocator"] = e2e_with_allocator(pkv, st, dev, max(1, min(steps, 50)),
+                                                            graphs=not args.no_graph)
+    return line
+
+
+def run_gpu(args, rank, world, local_rank):
+    import paged_kv_cache_312_gb300 as pkv
+    import __graft_entry__
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    st = Step(args.workload, args.seed + rank, pkv.BlockAllocator,  # independent problems
+              partition=args.partition)
+    # beam groups: the beams of a group (consecutive sequences) attend their
+    # shared prompt blocks in one CTA per (group, KV head)
+    grouped = st.unique_blocks is not None and not args.ungrouped
+    gparts = args.group_parts if grouped else 1
+    line = measure(pkv, st, args, rank, world, local_rank, args.steps, args.warmup, grouped,
+                   gparts, e2e_alloc=True)
+    if cpu:
+        line["cpu_baseline"] = cpu_baseline(st, args.cpu_budget)
+    del st
+    extra = [] if args.extra in ("", "none") else [int(x) for x in args.extra.split(",")]
+    if extra:
+        line["workloads"] = {}
+    for key in extra:
+        if key == args.workload:
+            continue
+        # the other workloads, each in its own launch configuration (the
+        # beam workload through the beam-group call), K steps after W warm-up
+        sx = Step(key, args.seed + rank, pkv.BlockAllocator)
+        gx = sx.unique_blocks is not None
+        lx = measure(pkv, sx, args, rank, world, local_rank, args.steps, args.warmup, gx, 1)
+        for k_ in ("metric", "higher_is_better", "scaling", "vs_baseline", "n_gpus", "data"):
+            lx.pop(k_, None)
+        if cpu:
+            lx["cpu_baseline"] = cpu_baseline(sx, args.cpu_budget_extra)
+        line["workloads"][str(key)] = lx
+        del sx
+    return line
+
+
+def end_to_end(g, st, dev, k, graphs=True):
+    """End to end through the public API from pinned host buffers: every
+    step copies its inputs to the device (one packed copy), runs the step's
+    library calls, copies the fp32 output back and synchronises.  With
+    `graphs`, the copy, the calls and the read-back are captured once from
+    those public calls as a CUDA graph, and each step is one graph launch
+    (the copies still move every step's bytes); the plain form, one API call
+    after the other, is timed beside it."""
+    S, Hq, D = g.out.shape
+    h_out = torch.empty((S, Hq, D), dtype=torch.float32).pin_memory()
+    res = {"h2d_bytes_per_step": int(g.h_pack.numel()),
+           "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size()), "steps": k,
+           "inputs": "q, block tables, lengths, CoW pairs, new K/V in one pinned buffer"}
+
+    def body(sm):
+        g.d_pack.copy_(g.h_pack, non_blocking=True)
+        g.run(stream=sm)
+        h_out.copy_(g.out, non_blocking=True)
+
+    def timed(fn, sm):
+        torch.cuda.synchronize(dev)
+        w0 = time.perf_counter()
+        for _ in range(k):
+            fn()
+            sm.synchronize()
+        return (time.perf_counter() - w0) / k
+
+    plain_s = timed(lambda: body(g.stream), g.stream)
+    res["api_calls_ms_per_step"] = round(plain_s * 1e3, 4)
+    res["api_calls_value"] = round(st.kv_bytes / plain_s / 1e9, 2)
+    e2e_s, how = plain_s, "one public API call after the other, every step"
+    if graphs:
+        graph = capture_step_graph(body, dev)
+        if graph is not None:
+            cur = torch.cuda.current_stream(dev)
+            graph.replay()
+            e2e_s = timed(graph.replay, cur)
+            how = ("the step's public API calls (H2D copy, library calls, D2H copy) captured "
+                   "once as a CUDA graph, one graph launch per step")
+    res.update({"value": round(st.kv_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_s * 1e3, 4), "how": how})
+    return res
+
+
+def capture_step_graph(body, dev):
+    """CUDA graph of body(stream), captured on a side stream after two
+    eager runs there; None if capture is refused."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            body(side)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
+            body(side)
+    except RuntimeError as e:
+        sys.stderr.write("graph capture refused (%s); e2e uses the plain calls\n" % e)
+        torch.cuda.synchronize(dev)
+        return None
+    torch.cuda.synchronize(dev)
+    return graph
+
+
+def e2e_with_allocator(pkv, st, dev, k, graphs=True):
+    """End to end with the host side of every step in the timed region, as a
+    serving loop runs it: the library's allocator reserves each sequence's
+    next slot (pkv_step_append_tables: new blocks, copy-on-write decisions)
+    and patches the batch's block tables and lengths in place; they go into
+    one of two pinned input buffers, which is copied to the device with the
+    step's q and new K/V; the step runs (append + attention); the fp32 output
+    is copied back and the host waits for it.  The host plans step i+1 while
+    the device runs step i (the allocator needs only the lengths, not the
+    step's output).  Each step's copies and calls are one CUDA graph launch
+    (one graph per input buffer, captured from the public calls).  Lengths
+    grow one token a step per sequence, as in serving, so the tables get
+    spare columns and the KV bytes are summed over the steps."""
+    w = st.w
+    B = w.block_size
+    S = st.q.shape[0]
+    L0 = st.lens.to(torch.int64) - 1  # tokens held before the first timed step
+    a = pkv.BlockAllocator(st.k_cache.shape[0], B, free_order=st.pool_order)
+    for s_ in range(S):
+        a.add(s_, int(L0[s_]))
+    seqs = torch.arange(S, dtype=torch.int64)
+    maxb = int((L0.max() + k + B - 1) // B) + 1
+    tables, lens = a.dense_tables(range(S), maxb)  # kept current by the allocator
+    pairs = torch.zeros((S, 2), dtype=torch.int64)
+    slots = torch.empty(S, dtype=torch.int64)
+    kc, vc = st.k_cache.to(dev), st.v_cache.to(dev)
+    out = torch.empty((S, w.num_heads, w.head_dim), dtype=torch.float32, device=dev)
+    h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    bufs = []
+    for _ in range(2):
+        h_pack, views = pack_inputs([st.q, tables, torch.zeros_like(lens), pairs, st.new_key,
+                                     st.new_value], dev)
+        b_ = dict(zip(("q", "bt", "cl", "pairs_d", "nk", "nv", "d_pack"), views))
+        b_["h_pack"] = h_pack
+        offs, total = [], 0
+        for t in (st.q, tables, lens, pairs):
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        b_["h_tables"] = h_pack[offs[1]:offs[1] + tables.numel() * 4].view(torch.int32) \
+            .view(S, maxb)
+        b_["h_lens"] = h_pack[offs[2]:offs[2] + S * 4].view(torch.int32)
+        b_["h_pairs"] = h_pack[offs[3]:offs[3] + S * 16].view(torch.int64).view(S, 2)
+        bufs.append(b_)
+
+    def body(b_, sm, n_pairs=0):
+        b_["d_pack"].copy_(b_["h_pack"], non_blocking=True)
+        if n_pairs:
+            pkv.kv_copy_blocks(kc, vc, b_["pairs_d"][:n_pairs], stream=sm)
+        pkv.decode_step(out, b_["q"], b_["nk"], b_["nv"], kc, vc, b_["bt"], b_["cl"], w.scale, B,
+                        w.num_kv_heads, partition_size=0, stream=sm)
+        h_out.copy_(out, non_blocking=True)
+
+    # captured while the lengths are 0: the capture's runs write and read nothing
+    for b_ in bufs:
+        b_["graph"] = capture_step_graph(lambda sm, b_=b_: body(b_, sm), dev) if graphs else None
+    stream = torch.cuda.current_stream(dev)
+    kv_tok = 2 * w.num_kv_heads * w.head_dim * w.torch_dtype.itemsize
+    graphed = all(b_["graph"] is not None for b_ in bufs)
+
+    def plan(b_):
+        """Host side of the next step into input buffer b_ (its count of CoW pairs)."""
+        n = a.step_append_tables(seqs, slots, pairs, tables, lens)
+        b_["h_tables"].copy_(tables)
+        b_["h_lens"].copy_(lens)
+        if n:
+            b_["h_pairs"][:n].copy_(pairs[:n])
+        return n
+
+    kv_total, t_plan = 0, 0.0
+    torch.cuda.synchronize(dev)
+    w0 = time.perf_counter()
+    ta = time.perf_counter()
+    n_pairs = plan(bufs[0])
+    t_plan += time.perf_counter() - ta
+    for i in range(k):
+        b_ = bufs[i % 2]
+        if n_pairs or not graphed:  # copies to make first: this step runs call by call
+            body(b_, stream, n_pairs)
+        else:
+            b_["graph"].replay()
+        kv_total += int(L0.sum() + (i + 1) * S) * kv_tok
+        if i + 1 < k:  # plan the next step while this one runs
+            ta = time.perf_counter()
+            n_pairs = plan(bufs[(i + 1) % 2])
+            t_plan += time.perf_counter() - ta
+        stream.synchronize()
+    dt = time.perf_counter() - w0
+    assert pkv.device_status() == 0
+    assert torch.isfinite(h_out).all()
+    del kc, vc
+    torch.cuda.empty_cache()
+    return {"value": round(kv_total / dt / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(dt / k * 1e3, 4), "steps": k,
+            "h2d_bytes_per_step": int(bufs[0]["h_pack"].numel()),
+            "d2h_bytes_per_step": int(h_out.numel() * 4),
+            "host_plan_us_per_step": round(t_plan / k * 1e6, 2),
+            "graphs": graphed,
+            "what": "pkv_step_append_tables (slots, new blocks, CoW decisions; tables and "
+                    "lengths patched in place) for step i+1 on the host while the device runs "
+                    "step i; per step one H2D copy of the pinned inputs + decode_step + output "
+                    "D2H + synchronise; lengths grow one token a step"}
 
 
 def pack_inputs(tensors, dev):
@@ -410,47 +686,74 @@ def pack_inputs(tensors, dev):
 
 
 def host_allocator_timing(st, pkv, grouped=False, steps=256):
-    """Host side of a decode step (a1/a2): pkv_step_append for every sequence
-    (slot mapping, new blocks, copy-on-write decisions) plus the read-back of
-    the dense block tables the device calls take (and, for beam groups, the
-    shared prefix of each group found from those tables).  Timed over `steps`
+    """Host side of a decode step (a1/a2) through the C ABI:
+    pkv_step_append_tables for every sequence (slot mapping, new blocks,
+    copy-on-write decisions), which keeps the dense block tables and lengths
+    the device calls take current in place (and, for beam groups, the shared
+    prefix of each group found from those tables).  Timed over `steps`
     consecutive steps from the workload's lengths, in a pool with room for
-    them; mean microseconds per step."""
+    them; mean microseconds per step.  The earlier form, pkv_step_append
+    plus a dense read-back of every table, is timed beside it."""
     w = st.w
     lens = st.lens.tolist()
     S, B = len(lens), w.block_size
     need = sum((n + steps + B - 1) // B for n in lens)
-    a = pkv.BlockAllocator(need + S, B)
-    for i, n in enumerate(lens):
-        a.add(i, max(0, n - 1))
-    seqs = list(range(S))
     maxb = max((n + steps + B - 1) // B for n in lens)
     gstart = torch.arange(0, S + 1, max(1, w.beam_width), dtype=torch.int32)
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        a.step_append(seqs)
-        tables, tl = a.dense_tables(seqs, maxb)
-        if grouped:
-            pkv.group_shared_tokens(tables, tl, gstart, B)
-    us = (time.perf_counter() - t0) / steps * 1e6
-    return {"us_per_step": round(us, 2), "steps": steps, "sequences": S,
-            "what": "pkv_step_append for every sequence + dense block-table read-back" +
-            (" + shared prefix per beam group" if grouped else "")}
+    res = {}
+    for form in ("patched", "dense"):
+        a = pkv.BlockAllocator(need + S, B)
+        for i, n in enumerate(lens):
+            a.add(i, max(0, n - 1))
+        seqs = torch.arange(S, dtype=torch.int64)
+        tables, tl = a.dense_tables(range(S), maxb)
+        slots = torch.empty(S, dtype=torch.int64)
+        pairs = torch.empty((S, 2), dtype=torch.int64)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            if form == "patched":
+                a.step_append_tables(seqs, slots, pairs, tables, tl)
+            else:
+                a.step_append(range(S))
+                tables, tl = a.dense_tables(range(S), maxb)
+            if grouped:
+                pkv.group_shared_tokens(tables, tl, gstart, B)
+        res[form] = (time.perf_counter() - t0) / steps * 1e6
+    return {"us_per_step": round(res["patched"], 2), "steps": steps, "sequences": S,
+            "what": "pkv_step_append_tables for every sequence (tables and lengths patched in "
+                    "place)" + (" + shared prefix per beam group" if grouped else ""),
+            "us_per_step_dense_readback": round(res["dense"], 2)}
 
 
-def cpu_baseline(st, budget_s=8.0):
-    """Time the oracle (as it stands) on this host's cores on a bounded sample
-    of the same step: passes over the step's sequences (write + attention)
-    until the budget is used."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def _oracle_rate(st, kc, vc, budget_s, threads):
+    """Passes of the oracle over the step's sequences (copies, write and
+    attention) with `threads` threads until `budget_s` of CPU time is used:
+    (KV GB/s, bytes, seconds, passes, chunk)."""
     import oracle
     w = st.w
-    n = os.cpu_count() or 1
     S = st.q.shape[0]
     done_bytes, t_used, passes = 0, 0.0, 0
-    kc, vc = st.k_cache.clone(), st.v_cache.clone()
-    if st.setup_slots is not None:
-        oracle.kv_write(kc, vc, st.setup_keys, st.setup_vals, st.setup_slots, w.block_size)
-    chunk = max(1, min(S, 4 * n))
+    chunk = max(1, min(S, 4 * threads))
     L = st.lens.to(torch.int64)
     while t_used < budget_s and passes < 100:
         for c0 in range(0, S, chunk):
@@ -462,17 +765,36 @@ def cpu_baseline(st, budget_s=8.0):
                 if st.slots is not None:
                     oracle.kv_write(kc, vc, st.new_key, st.new_value, st.slots, w.block_size)
             oracle.paged_decode_attention(st.q[idx], kc, vc, st.tables[idx], st.lens[idx],
-                                          w.scale, w.block_size, w.num_kv_heads, nthreads=n)
+                                          w.scale, w.block_size, w.num_kv_heads, nthreads=threads)
             t_used += time.perf_counter() - t
             done_bytes += int(L[idx].sum()) * 2 * w.num_kv_heads * w.head_dim * \
                 w.torch_dtype.itemsize
             if t_used >= budget_s:
                 break
         passes += 1
-    return {"value": round(done_bytes / t_used / 1e9, 4), "unit": "GB/s", "cores": n,
-            "kind": "oracle",
+    return done_bytes / t_used / 1e9, done_bytes, t_used, passes, chunk
+
+
+def cpu_baseline(st, budget_s=8.0):
+    """Time the oracle (as it stands) on this host's cores on a bounded sample
+    of the same step: passes over the step's sequences (write + attention)
+    until the budget is used, on every core, then on one core (a third of
+    the budget)."""
+    import oracle
+    w = st.w
+    n = os.cpu_count() or 1
+    kc, vc = st.k_cache.clone(), st.v_cache.clone()
+    if st.setup_slots is not None:
+        oracle.kv_write(kc, vc, st.setup_keys, st.setup_vals, st.setup_slots, w.block_size)
+    v, nb, t, passes, chunk = _oracle_rate(st, kc, vc, budget_s, n)
+    v1, nb1, t1, _, _ = _oracle_rate(st, kc, vc, max(1.0, budget_s / 3), 1)
+    return {"value": round(v, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": "%.2f GB of the step's KV (%d pass(es) over chunks of %d sequences, "
-                      "fp64 C oracle, %.1f s)" % (done_bytes / 1e9, passes, chunk, t_used)}
+                      "fp64 C oracle, %d threads, %.1f s)" % (nb / 1e9, passes, chunk, n, t),
+            "single_core": {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
+                            "sample": "%.2f GB of the step's KV, 1 thread, %.1f s" %
+                                      (nb1 / 1e9, t1)}}
 
 
 SWEEP_BLOCKS = (8, 16, 32)
@@ -766,13 +1088,22 @@ def main():
                     help="partition size in tokens (default: the workload's launch setting)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="e2e: one public API call after the other instead of a captured graph")
     ap.add_argument("--ungrouped", action="store_true",
                     help="beam workload: attend every beam on its own (decode_step) instead of "
                          "one CTA per beam group")
     ap.add_argument("--group-parts", type=int, default=1,
                     help="beam workload: CTAs that share one beam group's stages for a KV head")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=8.0)
+    ap.add_argument("--cpu-budget", type=float, default=8.0,
+                    help="seconds of oracle time for the headline workload's CPU baseline")
+    ap.add_argument("--cpu-budget-extra", type=float, default=3.0,
+                    help="seconds of oracle time for each extra workload's CPU baseline")
+    ap.add_argument("--extra", default=None,
+                    help="comma-separated workloads measured after the headline one, into the "
+                         "line's `workloads` object (default 3,4,5 with workload 2, else none; "
+                         "'none' for none)")
     ap.add_argument("--prefill", action="store_true",
                     help="paged prefill throughput (one JSON line; not the benchmark line)")
     ap.add_argument("--swap", action="store_true",
@@ -790,6 +1121,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.extra is None:
+        args.extra = ",".join(str(k) for k in EXTRA_WORKLOADS) if args.workload == 2 else ""
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -816,10 +1149,8 @@ def main():
 
     if world > 1:
         torch.distributed.init_process_group("gloo")
-    line, st = run_gpu(args, rank, world, local_rank)
+    line = run_gpu(args, rank, world, local_rank)
     if rank == 0:
-        if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(st, args.cpu_budget)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -833,7 +1164,7 @@ def run_reference(args):
     import oracle
     from oracle.blockmgr import BlockManager  # the oracle's own block manager builds the tables
 
-    st = Step(args.workload, args.seed, BlockManager)
+    st = Step(args.workload, args.seed, BlockManager, partition=args.partition)
     w = st.w
     n = os.cpu_count() or 1
     kc, vc = st.k_cache.clone(), st.v_cache.clone()
@@ -875,11 +1206,12 @@ def run_reference(args):
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "num_seqs": S, "num_heads": w.num_heads,
-                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                       "block_size": w.block_size},
+            "config": config_of(st, st.unique_blocks is not None and not args.ungrouped,
+                                args.group_parts if st.unique_blocks is not None and
+                                not args.ungrouped else 1,
+                                int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

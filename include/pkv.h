@@ -134,11 +134,21 @@ int pkv_kv_write(void* k_cache, void* v_cache, const void* key, const void* valu
  *                partitions one CTA holds, one per warp, and writes one
  *                partial per CTA), by a second kernel otherwise.  (The pages
  *                are silent on splitting; the merge is exact in real
- *                arithmetic.)
+ *                arithmetic.)  On the tensor-core kernel, batches of up to
+ *                4096 sequences first get a work plan (a one-CTA kernel in
+ *                place of zeroing the merge counters): the CTAs with work are
+ *                listed longest sequence first, so that long items do not
+ *                start last and empty grid slots do not interleave with
+ *                work.  The order changes no result.
  * workspace    : device scratch of at least pkv_decode_workspace_bytes(...)
- *                bytes, 256-byte aligned, when partition_size > 0 (else may be
- *                NULL).  Contents on entry are ignored; calls that share a
- *                workspace must not overlap on the GPU.
+ *                bytes, 256-byte aligned, when partition_size > 0.  With
+ *                partition_size == 0 it is optional: NULL attends the
+ *                sequences in the caller's order; a workspace of
+ *                pkv_decode_workspace_bytes(..., 0) bytes gets the unsplit
+ *                launch a work plan too (longest sequence first), which
+ *                keeps ragged batches from ending on a long sequence that
+ *                started late.  Contents on entry are ignored; calls that
+ *                share a workspace must not overlap on the GPU.
  * Supported: block_size in {8,16,32}; head_dim in {64,128}; num_heads a
  * multiple of num_kv_heads; out_dtype any of the three.  16-bit KV with
  * G = num_heads/num_kv_heads <= 256 runs on the tensor-core kernel (one CTA
@@ -282,7 +292,13 @@ int pkv_paged_prefill_attention(void* out, const void* q, const void* k_cache, c
                                 int kv_dtype, int out_dtype, void* stream);
 
 /* Workspace bytes pkv_paged_decode_attention needs for these sizes, where
- * max_context_len = max_blocks_per_seq * block_size.  0 if partition_size==0. */
+ * max_context_len = max_blocks_per_seq * block_size.  With H = num_heads and
+ * P = ceil(max_context_len / partition_size), each part 256-byte aligned:
+ * merge counters (S*H u32), per-partition (max, sum) (S*H*P float2) and
+ * unnormalised outputs (S*H*P*head_dim float), the work plan's record count
+ * (256 bytes) and records (S*H*P * 16 bytes).  partition_size == 0: the
+ * optional workspace of an unsplit call, the work plan alone (256 + S*H*16
+ * bytes).  0 for bad sizes. */
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                   int max_context_len, int partition_size);
 
@@ -301,9 +317,13 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
  * (pkv_decode_workspace_bytes) exceeds it are rejected with
  * PKV_ERR_WORKSPACE and a message giving both figures; nothing is launched.
  * The call allocates nothing: no cudaMalloc / cudaFree, no allocating
- * library routine.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls on a device share the one
+ * library routine.  Every call looks up the array's device address
+ * (cudaGetSymbolAddress, which allocates nothing) with the caller's device
+ * current, so a reset or another context never sees a stale address; the
+ * first call on a device is its set-up (it may load the library's device
+ * code there), so make that first call before any stream capture.  The
+ * request is checked like pkv_paged_decode_attention's (same codes) before
+ * the scratch limit is.  All calls on a device share the one
  * array, and it keeps the last call's contents (no clearing is needed: each
  * call writes every scratch slot it reads before reading it), so calls that
  * overlap on the GPU -- on different streams, or different threads -- race
@@ -430,6 +450,21 @@ int pkv_seq_append(pkv_allocator* a, int64_t seq, int64_t* slot, int64_t* cow_sr
  * nothing.  slots: [n]; cow_pairs: [n][2] capacity; *num_pairs = pairs made. */
 int pkv_step_append(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots,
                     int64_t* cow_pairs, int* num_pairs);
+
+/* The same step, keeping a dense batch table current in place: on entry
+ * tables [n][max_blocks] and lens [n] hold sequence seqs[i]'s table and
+ * length from before the step (from pkv_block_tables_dense, or from the
+ * previous step's call with the same seqs); the call writes only what the
+ * step changes -- the entry of each new token's block (a fresh block, or the
+ * copy that replaced a shared one) and lens[i] + 1 -- so a serving loop can
+ * keep the tables in the pinned buffer it copies to the device, with no
+ * dense read-back each step.  Entries past a sequence's table are left as
+ * they are.  All or nothing: PKV_ERR_SHAPE (nothing changed) if a table would
+ * grow past max_blocks, PKV_ERR_STATE if a sequence is listed twice;
+ * otherwise as pkv_step_append. */
+int pkv_step_append_tables(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots,
+                           int64_t* cow_pairs, int* num_pairs, int32_t* tables, int max_blocks,
+                           int32_t* lens);
 
 /* child shares every block of parent (each count + 1).  PKV_ERR_STATE if the
  * parent is unknown or the child exists. */

@@ -58,6 +58,7 @@ _SIGS = {
     "pkv_seq_append": (_I, [_P, _I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                             ctypes.POINTER(_I64)]),
     "pkv_step_append": (_I, [_P, _P, _I, _P, _P, ctypes.POINTER(_I)]),
+    "pkv_step_append_tables": (_I, [_P, _P, _I, _P, _P, ctypes.POINTER(_I), _P, _I, _P]),
     "pkv_seq_fork": (_I, [_P, _I64, _I64]),
     "pkv_seq_free": (_I, [_P, _I64]),
     "pkv_seq_len": (_I, [_P, _I64, ctypes.POINTER(_I)]),
@@ -434,6 +435,31 @@ class BlockAllocator:
                                      ctypes.c_void_p(pairs.data_ptr()), ctypes.byref(npairs)),
                "pkv_step_append")
         return slots, pairs[:npairs.value].clone()
+
+    def step_append_tables(self, seqs, slots, pairs, tables, lens):
+        """One decode step that patches the caller's dense tables in place.
+
+        seqs: int64 [n]; slots: int64 [n] (out); pairs: int64 [>= n, 2] (out,
+        copy-on-write pairs first); tables: int32 [n, max_blocks] and lens:
+        int32 [n], holding the batch's tables and lengths from before the
+        step (in any host memory, e.g. a view of a pinned staging buffer).
+        Returns the number of copy-on-write pairs written."""
+        n = seqs.numel()
+        for t, dt, name in ((seqs, torch.int64, "seqs"), (slots, torch.int64, "slots"),
+                            (pairs, torch.int64, "pairs"), (tables, torch.int32, "tables"),
+                            (lens, torch.int32, "lens")):
+            if t.dtype != dt or t.is_cuda or not t.is_contiguous():
+                raise ValueError("step_append_tables: %s must be contiguous host %s" % (name, dt))
+        if slots.numel() < n or pairs.shape[0] < n or tables.shape[0] != n or \
+                lens.numel() != n or tables.dim() != 2:
+            raise ValueError("step_append_tables: bad output shapes")
+        npairs = ctypes.c_int(0)
+        _check(lib().pkv_step_append_tables(
+            self._h, ctypes.c_void_p(seqs.data_ptr()), n, ctypes.c_void_p(slots.data_ptr()),
+            ctypes.c_void_p(pairs.data_ptr()), ctypes.byref(npairs),
+            ctypes.c_void_p(tables.data_ptr()), tables.shape[1],
+            ctypes.c_void_p(lens.data_ptr())), "pkv_step_append_tables")
+        return npairs.value
 
     def fork(self, parent, child):
         _check(lib().pkv_seq_fork(self._h, int(parent), int(child)), "pkv_seq_fork")

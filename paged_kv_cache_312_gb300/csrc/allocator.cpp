@@ -229,50 +229,86 @@ int pkv_seq_append(pkv_allocator* a, int64_t seq, int64_t* slot, int64_t* cow_sr
     return PKV_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Blocks one decode step over seqs[0..n) must take (a fresh block for a token
+// that starts one, a copy target for a write into a shared partial block),
+// found without changing anything: the walk tracks, per sequence, its length
+// and whether its last block is already private, and per shared block the
+// count drops earlier appends of the same step make, so that a block shared
+// by two sequences of the step is copied once and its last holder writes in
+// place.  Also checks every sequence exists and (tables != 0) that no table
+// grows past max_blocks.
+int plan_step(pkv_allocator* a, const int64_t* seqs, int n, const char* fn,
+              std::vector<pkv_allocator::Seq*>& ptr, int max_blocks, int64_t* need_out)
+{
+    struct Sim {
+        int64_t len;
+        int64_t blocks;
+        int32_t last;  // -1: a block taken in this step (private to the sequence)
+    };
+    ptr.resize(n);
+    std::unordered_map<int64_t, Sim> sim;
+    sim.reserve((size_t)n * 2);
+    std::unordered_map<int32_t, int> dref;
+    int64_t need = 0;
+    for (int i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seqs[i]);
+        if (it == a->seqs.end())
+            return pkv_fail(PKV_ERR_STATE, "%s: unknown sequence %lld", fn, (long long)seqs[i]);
+        ptr[i] = &it->second;
+        auto f = sim.find(seqs[i]);
+        if (f != sim.end() && max_blocks > 0)  // one table row per sequence
+            return pkv_fail(PKV_ERR_STATE, "%s: sequence %lld listed twice", fn,
+                            (long long)seqs[i]);
+        if (f == sim.end()) {
+            const pkv_allocator::Seq& q = it->second;
+            f = sim.emplace(seqs[i], Sim{q.len, (int64_t)q.table.size(),
+                                         q.table.empty() ? -1 : q.table.back()})
+                    .first;
+        }
+        Sim& s = f->second;
+        if (s.len % a->block_size == 0) {
+            s.last = -1;
+            s.blocks += 1;
+            need += 1;
+        } else if (s.last >= 0 && a->ref[s.last] > 1) {
+            int& d = dref[s.last];
+            if (a->ref[s.last] + d > 1) {
+                d -= 1;
+                s.last = -1;
+                need += 1;
+            }
+        }
+        s.len += 1;
+        if (max_blocks > 0 && s.blocks > max_blocks)
+            return pkv_fail(PKV_ERR_SHAPE, "%s: sequence %lld would need %lld table entries, %d "
+                            "fit", fn, (long long)seqs[i], (long long)s.blocks, max_blocks);
+    }
+    if (need > (int64_t)a->available())
+        return pkv_fail(PKV_ERR_OOM, "%s: %lld blocks needed, %zu free", fn, (long long)need,
+                        a->available());
+    *need_out = need;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int pkv_step_append(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots,
                     int64_t* cow_pairs, int* num_pairs)
 {
     if (!a || (n > 0 && (!seqs || !slots || !cow_pairs)) || !num_pairs)
         return pkv_fail(PKV_ERR_NULL, "pkv_step_append: NULL argument");
     if (n < 0) return pkv_fail(PKV_ERR_SHAPE, "pkv_step_append: n < 0");
-    // Plan first (all or nothing): walk the batch tracking the count changes
-    // earlier appends would make, so that a block shared by two sequences of
-    // the same step is copied once and the last holder writes in place.
-    std::vector<pkv_allocator::Seq*> ptr(n);
-    std::unordered_map<int32_t, int> dref;
+    // plan first (all or nothing), then commit
+    std::vector<pkv_allocator::Seq*> ptr;
     int64_t need = 0;
-    for (int i = 0; i < n; ++i) {
-        auto it = a->seqs.find(seqs[i]);
-        if (it == a->seqs.end())
-            return pkv_fail(PKV_ERR_STATE, "pkv_step_append: unknown sequence %lld",
-                            (long long)seqs[i]);
-        ptr[i] = &it->second;
-    }
-    {
-        // Simulate on copies of the touched tables.  A table entry of -1
-        // stands for a block taken in this step (private to its sequence).
-        std::unordered_map<int64_t, pkv_allocator::Seq> sim;
-        for (int i = 0; i < n; ++i) {
-            auto f = sim.find(seqs[i]);
-            if (f == sim.end()) f = sim.emplace(seqs[i], *ptr[i]).first;
-            pkv_allocator::Seq& s = f->second;
-            if (s.len % a->block_size == 0) {
-                s.table.push_back(-1);
-                need += 1;
-            } else {
-                int32_t last = s.table.back();
-                if (last >= 0 && a->ref[last] + dref[last] > 1) {
-                    dref[last] -= 1;
-                    s.table.back() = -1;
-                    need += 1;
-                }
-            }
-            s.len += 1;
-        }
-    }
-    if (need > (int64_t)a->available())
-        return pkv_fail(PKV_ERR_OOM, "pkv_step_append: %lld blocks needed, %zu free",
-                        (long long)need, a->available());
+    const int rc = plan_step(a, seqs, n, "pkv_step_append", ptr, 0, &need);
+    if (rc != PKV_OK) return rc;
     int np = 0;
     for (int i = 0; i < n; ++i) {
         int64_t src, dst;
@@ -282,6 +318,39 @@ int pkv_step_append(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots
             cow_pairs[2 * np + 1] = dst;
             ++np;
         }
+    }
+    *num_pairs = np;
+    return PKV_OK;
+}
+
+int pkv_step_append_tables(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots,
+                           int64_t* cow_pairs, int* num_pairs, int32_t* tables, int max_blocks,
+                           int32_t* lens)
+{
+    static const char* fn = "pkv_step_append_tables";
+    if (!a || (n > 0 && (!seqs || !slots || !cow_pairs || !tables || !lens)) || !num_pairs)
+        return pkv_fail(PKV_ERR_NULL, "%s: NULL argument", fn);
+    if (n < 0 || max_blocks <= 0) return pkv_fail(PKV_ERR_SHAPE, "%s: n %d, max_blocks %d", fn, n,
+                                                  max_blocks);
+    std::vector<pkv_allocator::Seq*> ptr;
+    int64_t need = 0;
+    const int rc = plan_step(a, seqs, n, fn, ptr, max_blocks, &need);
+    if (rc != PKV_OK) return rc;
+    int np = 0;
+    for (int i = 0; i < n; ++i) {
+        pkv_allocator::Seq& s = *ptr[i];
+        int64_t src, dst;
+        a->append_one(s, &slots[i], &src, &dst);
+        if (src >= 0) {
+            cow_pairs[2 * np] = src;
+            cow_pairs[2 * np + 1] = dst;
+            ++np;
+        }
+        // the entries this append can change: the token's block (new, or the
+        // copy that replaced a shared one), and the length
+        const int64_t e = (s.len - 1) / a->block_size;
+        tables[(size_t)i * max_blocks + e] = s.table[e];
+        lens[i] = (int32_t)s.len;
     }
     *num_pairs = np;
     return PKV_OK;

@@ -127,20 +127,29 @@ int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtens
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Split workspace, in order (each part 256-byte aligned):
-//   done : u32 [S][H]           partitions finished per (sequence, KV head)
-//   ml   : float2 [S][H][P]     per-partition (max, sum), base 2
-//   o    : float [S][H][P][D]   per-partition unnormalised output
-// with H the number of query heads (an upper bound for the KV heads).
+//   done  : u32 [S][H]           partitions finished per (sequence, KV head)
+//   ml    : float2 [S][H][P]     per-partition (max, sum), base 2
+//   o     : float [S][H][P][D]   per-partition unnormalised output
+//   count : int                  work records in the plan
+//   items : int4 [S][H][P]       the plan's records, one per CTA with work
+// with H the number of query heads (an upper bound for the KV heads times
+// the head slices, so S*H*P bounds every split launch's grid).
 struct WorkspaceLayout {
-    size_t ml, o, total;
+    size_t ml, o, count, items, total;
 };
+
+// Optional workspace of an unsplit launch: the work plan alone (record
+// count, then one record per (sequence, KV head x head slice)).
+size_t plan_bytes(size_t S, size_t H) { return 256 + S * H * 16; }
 
 WorkspaceLayout workspace_layout(size_t S, size_t H, size_t P, size_t D)
 {
     WorkspaceLayout w;
     w.ml = align256(S * H * sizeof(unsigned));
     w.o = w.ml + align256(S * H * P * sizeof(float2));
-    w.total = w.o + S * H * P * D * sizeof(float);
+    w.count = w.o + align256(S * H * P * D * sizeof(float));
+    w.items = w.count + 256;
+    w.total = w.items + S * H * P * 16;
     return w;
 }
 
@@ -327,28 +336,21 @@ int pkv_paged_prefill_attention(void* out, const void* q, const void* k_cache, c
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
                                   int partition_size)
 {
-    if (partition_size <= 0 || num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 ||
+    if (partition_size < 0 || num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 ||
         max_context_len <= 0)
         return 0;
+    if (partition_size == 0) return plan_bytes(num_seqs, num_heads);
     const size_t P = ((size_t)max_context_len + partition_size - 1) / partition_size;
     return workspace_layout(num_seqs, num_heads, P, head_dim).total;
 }
 
 }  // extern "C"
 
-namespace {
-
-// Decode attention, optionally with the step's append fused in (new_k and
-// new_v non-NULL: each sequence's new token goes to position
-// context_lens[s]-1 first).
-int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
-                const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
-                float scale, int block_size, int num_kv_heads, int num_seqs, int num_heads,
-                int head_dim, int max_blocks_per_seq, int num_blocks, int kv_dtype, int out_dtype,
-                int partition_size, void* workspace, size_t workspace_bytes, void* stream,
-                const void* new_k, const void* new_v, const int32_t* group_start = nullptr,
-                const int32_t* shared_tokens = nullptr, int num_groups = 0, int group_parts = 1,
-                int max_members = 0)
+// Checks of a decode request's dtypes and sizes that need no pointer (shared
+// by every decode entry point, so that they report the same codes).
+int pkv_decode_check(const char* fn, int kv_dtype, int out_dtype, int num_seqs, int num_heads,
+                     int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                     int num_blocks, int partition_size, float scale)
 {
     if (!pkv_dtype_bytes(kv_dtype) || !pkv_dtype_bytes(out_dtype))
         return pkv_fail(PKV_ERR_DTYPE, "%s: dtype kv=%d out=%d", fn, kv_dtype, out_dtype);
@@ -373,6 +375,27 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
         return pkv_fail(PKV_ERR_SHAPE, "%s: partition_size %d must be 0 or a multiple of %d", fn,
                         partition_size, block_size);
     if (!std::isfinite(scale)) return pkv_fail(PKV_ERR_SHAPE, "%s: scale is not finite", fn);
+    return PKV_OK;
+}
+
+namespace {
+
+// Decode attention, optionally with the step's append fused in (new_k and
+// new_v non-NULL: each sequence's new token goes to position
+// context_lens[s]-1 first).
+int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
+                const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                float scale, int block_size, int num_kv_heads, int num_seqs, int num_heads,
+                int head_dim, int max_blocks_per_seq, int num_blocks, int kv_dtype, int out_dtype,
+                int partition_size, void* workspace, size_t workspace_bytes, void* stream,
+                const void* new_k, const void* new_v, const int32_t* group_start = nullptr,
+                const int32_t* shared_tokens = nullptr, int num_groups = 0, int group_parts = 1,
+                int max_members = 0)
+{
+    const int chk = pkv_decode_check(fn, kv_dtype, out_dtype, num_seqs, num_heads, num_kv_heads,
+                                     head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                     partition_size, scale);
+    if (chk != PKV_OK) return chk;
     if (num_seqs == 0) return PKV_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return pkv_fail(PKV_ERR_NULL, "%s: NULL pointer", fn);
@@ -429,12 +452,27 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
     p.group_start = nullptr;
     p.shared_tokens = nullptr;
     p.num_groups = 0;
+    p.items = nullptr;
+    p.item_count = nullptr;
+    int* plan_count = nullptr;
+    int4* plan_items = nullptr;
     const int max_ctx = max_blocks_per_seq * block_size;
     p.cta_parts = 1;
     p.head_slices = 1;
     if (partition_size == 0 && (!grouped || group_parts == 1)) {
         p.partition_tokens = max_ctx;
         p.max_partitions = 1;
+        if (!grouped && workspace != nullptr) {
+            // optional: a work plan orders the launch longest sequence first
+            const size_t need = plan_bytes(num_seqs, num_heads);
+            if (workspace_bytes < need)
+                return pkv_fail(PKV_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given",
+                                fn, need, workspace_bytes);
+            if (!aligned(workspace, 256))
+                return pkv_fail(PKV_ERR_ALIGN, "%s: workspace needs 256-byte alignment", fn);
+            plan_count = static_cast<int*>(workspace);
+            plan_items = reinterpret_cast<int4*>(static_cast<char*>(workspace) + 256);
+        }
     } else {
         // token partitions, or (beam groups) parts of each group's stage list
         p.partition_tokens = grouped ? max_ctx : partition_size;
@@ -456,6 +494,8 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
         p.done = reinterpret_cast<unsigned*>(base);
         p.ws_ml = reinterpret_cast<float2*>(base + L.ml);
         p.ws_o = reinterpret_cast<float*>(base + L.o);
+        plan_count = reinterpret_cast<int*>(base + L.count);
+        plan_items = reinterpret_cast<int4*>(base + L.items);
     }
     p.status = pkv_status_word_ptr();
     if (!p.status) return pkv_fail(PKV_ERR_CUDA, "%s: no device status word", fn);
@@ -510,12 +550,36 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
         const long long grid = (long long)num_seqs * num_kv_heads * p.head_slices * groups;
         if (grid >= (1ll << 31))
             return pkv_fail(PKV_ERR_SHAPE, "%s: more than 2^31 work items", fn);
-        if (p.max_partitions > 1) {
-            // completion counters for the in-kernel merge start at zero
-            e = cudaMemsetAsync(p.done, 0,
-                                sizeof(unsigned) * (size_t)num_seqs * num_kv_heads * p.head_slices,
-                                st);
-            if (e != cudaSuccess) return cuda_fail(e, fn);
+        const int counters = p.max_partitions > 1 ? num_seqs * num_kv_heads * p.head_slices : 0;
+        if (plan_items != nullptr || counters > 0) {
+            if (plan_items != nullptr && num_seqs <= kPlanMaxSeqs) {
+                // the plan kernel zeroes the completion counters of the
+                // in-kernel merge and lists the CTAs with work, longest
+                // sequences first
+                DecodePlanParams pp;
+                pp.context_lens = context_lens;
+                pp.num_seqs = num_seqs;
+                pp.num_kv_heads = num_kv_heads;
+                pp.head_slices = p.head_slices;
+                pp.partition_tokens = p.partition_tokens;
+                pp.cta_parts = p.cta_parts;
+                pp.max_len = max_ctx;
+                int shift = 0;
+                while ((max_ctx >> shift) >= kPlanBuckets) ++shift;
+                pp.bucket_shift = shift;
+                pp.items = plan_items;
+                pp.item_count = plan_count;
+                pp.done = p.done;
+                pp.num_counters = counters;
+                e = launch_decode_plan(pp, st);
+                if (e != cudaSuccess) return cuda_fail(e, fn);
+                p.items = plan_items;
+                p.item_count = plan_count;
+            } else if (counters > 0) {
+                // completion counters for the in-kernel merge start at zero
+                e = cudaMemsetAsync(p.done, 0, sizeof(unsigned) * (size_t)counters, st);
+                if (e != cudaSuccess) return cuda_fail(e, fn);
+            }
         }
         // the tensor-core kernel writes the new tokens itself
         p.new_k = new_k;

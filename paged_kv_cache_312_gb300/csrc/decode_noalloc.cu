@@ -11,11 +11,16 @@
 // The array below is a file-scope __device__ object, so every GPU that loads
 // libpkv holds PKV_NOALLOC_SCRATCH_BYTES of it until the process exits. In
 // host code its name is only a host-side stand-in, not a device address: the
-// device address comes from cudaGetSymbolAddress, looked up once per device
-// (with that device current) on the first call made on it.
+// device address comes from cudaGetSymbolAddress, asked on every call with
+// the caller's device current. The first call on a device is the set-up (it
+// loads the library's device code there, if nothing has yet); later calls
+// only look the address up, which allocates nothing. Asking each time, rather
+// than keeping the first answer per device, means a call never uses an
+// address from a context that has since been destroyed (cudaDeviceReset) or
+// that is not the caller's current one.
 #include <cuda_runtime.h>
 
-#include <mutex>
+#include <cstdint>
 
 #include "pkv.h"
 #include "pkv_internal.h"
@@ -24,34 +29,17 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+const char* const kFn = "pkv_paged_decode_attention_noalloc";
 
-// Device address of the scratch array on the current device (set-up on the
-// first call per device).
+// Device address of the scratch array in the current context.
 int scratch_address(void** out)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return pkv_fail(PKV_ERR_CUDA, "pkv_paged_decode_attention_noalloc: cudaGetDevice: %s",
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr)
+        return pkv_fail(PKV_ERR_CUDA, "%s: cudaGetSymbolAddress: %s", kFn,
                         cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices)
-        return pkv_fail(PKV_ERR_UNSUPPORTED,
-                        "pkv_paged_decode_attention_noalloc: device %d beyond %d", dev,
-                        kMaxDevices);
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_addr[dev]) {
-        void* ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess || !ptr)
-            return pkv_fail(PKV_ERR_CUDA,
-                            "pkv_paged_decode_attention_noalloc: cudaGetSymbolAddress: %s",
-                            cudaGetErrorString(e));
-        g_scratch_addr[dev] = ptr;
-    }
-    *out = g_scratch_addr[dev];
+    *out = ptr;
     return PKV_OK;
 }
 
@@ -65,24 +53,27 @@ extern "C" int pkv_paged_decode_attention_noalloc(
 {
     if (partition_size <= 0)
         return pkv_fail(PKV_ERR_SHAPE,
-                        "pkv_paged_decode_attention_noalloc: partition_size must be > 0 "
-                        "(this entry point is the split-context decode)");
-    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
-        block_size <= 0)
-        return pkv_paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
-                                          scale, block_size, num_kv_heads, num_seqs, num_heads,
-                                          head_dim, max_blocks_per_seq, num_blocks, kv_dtype,
-                                          out_dtype, partition_size, nullptr, 0, stream);
-    const size_t need = pkv_decode_workspace_bytes(
-        num_seqs, num_heads, head_dim, max_blocks_per_seq * block_size, partition_size);
+                        "%s: partition_size must be > 0 (this entry point is the split-context "
+                        "decode)", kFn);
+    // the same checks, in the same order, as the workspace entry point, so
+    // that a malformed request gets the same code there and here
+    const int chk = pkv_decode_check(kFn, kv_dtype, out_dtype, num_seqs, num_heads, num_kv_heads,
+                                     head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                     partition_size, scale);
+    if (chk != PKV_OK) return chk;
+    if (num_seqs == 0) return PKV_OK;
+    // the checks above bound the longest context by 2^30 tokens
+    const int64_t max_ctx = (int64_t)max_blocks_per_seq * block_size;
+    const size_t need = pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, (int)max_ctx,
+                                                   partition_size);
     if (need > (size_t)PKV_NOALLOC_SCRATCH_BYTES)
         return pkv_fail(PKV_ERR_WORKSPACE,
-                        "pkv_paged_decode_attention_noalloc: these sizes need %zu bytes of "
-                        "scratch; the fixed array holds %zu (use pkv_paged_decode_attention "
-                        "with a caller workspace, or a larger partition_size)",
-                        need, (size_t)PKV_NOALLOC_SCRATCH_BYTES);
+                        "%s: these sizes need %zu bytes of scratch; the fixed array holds %zu "
+                        "(use pkv_paged_decode_attention with a caller workspace, or a larger "
+                        "partition_size)",
+                        kFn, need, (size_t)PKV_NOALLOC_SCRATCH_BYTES);
     void* scratch = nullptr;
-    int rc = scratch_address(&scratch);
+    const int rc = scratch_address(&scratch);
     if (rc != PKV_OK) return rc;
     // The scratch needs no clearing here: the call below zeroes the
     // completion counters the tensor-core kernel uses, and every (max, sum,

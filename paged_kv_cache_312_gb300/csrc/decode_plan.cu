@@ -1,0 +1,174 @@
+// Work plan of a split decode launch: the longest sequences first, no empty
+// grid slots.
+//
+// A split launch's rectangular grid gives every (sequence, KV head, head
+// slice) as many CTA slots as the longest context needs; with ragged
+// lengths most of them are empty and exit at once, and the long items start
+// wherever the caller put their sequence, so the launch often ends on a
+// long item that started late.  This one-CTA kernel runs in place of the
+// memset that zeroes the split's completion counters: it zeroes them, orders
+// the sequences by context length, longest first (a counting sort on
+// length buckets), and writes one record per CTA that has work -- (sequence,
+// context length, KV head x head slice, partition group) -- consecutive in
+// that order, plus their count.  The decode kernel's CTA b takes record b,
+// or exits if b is past the count.  The order changes no result: every
+// partition's softmax state and every merge are the same whichever CTA runs
+// first.
+//
+// Both launches are programmatic dependent launches: the plan kernel starts
+// while the previous decode launch's last CTAs still run (decode CTAs let
+// dependents launch as they start), reads the lengths and builds the order
+// in shared memory, then waits for that launch to complete before it writes
+// counters and records; the decode CTAs are resident while the plan kernel
+// finishes and wait for it to complete before they read a record.
+#include <cuda_runtime.h>
+
+#include "pkv_kernels.h"
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+struct PlanSmem {
+    static constexpr int LENS = 0;                               // int [kPlanMaxSeqs]
+    static constexpr int SORTED = LENS + kPlanMaxSeqs;           // int [kPlanMaxSeqs]
+    static constexpr int OFF = SORTED + kPlanMaxSeqs;            // int [kPlanMaxSeqs]
+    static constexpr int HIST = OFF + kPlanMaxSeqs;              // int [kPlanBuckets]
+    static constexpr int WSUM = HIST + kPlanBuckets;             // int [32]
+    static constexpr int INTS = WSUM + 32 + 1;
+    static constexpr int BYTES = INTS * 4;
+};
+
+// Exclusive prefix sum over the block of one value per thread; *total gets
+// the sum.  Every thread of the block calls it.
+__device__ int block_exclusive_scan(int v, int* wsum, int* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < kPlanThreads / 32 ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        wsum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = warp > 0 ? wsum[warp - 1] : 0;
+    *total = wsum[kPlanThreads / 32 - 1];
+    __syncthreads();  // wsum may be reused by the caller's next scan
+    return before + x - v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodePlanParams pp)
+{
+    extern __shared__ int psm[];
+    int* lens = psm + PlanSmem::LENS;
+    int* sorted = psm + PlanSmem::SORTED;
+    int* off = psm + PlanSmem::OFF;
+    int* hist = psm + PlanSmem::HIST;
+    int* wsum = psm + PlanSmem::WSUM;
+    const int tid = threadIdx.x;
+    const int S = pp.num_seqs;
+    // the decode launch that follows may start now: its CTAs wait for this
+    // grid to complete (griddepcontrol.wait) before they read anything it
+    // writes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    for (int k = tid; k < kPlanBuckets; k += kPlanThreads) hist[k] = 0;
+    __syncthreads();
+    // histogram of length buckets, longest bucket first (index 0)
+    for (int s = tid; s < S; s += kPlanThreads) {
+        const int L = pp.context_lens[s];
+        lens[s] = L;
+        const int Lc = (L < 0 || L > pp.max_len) ? 0 : L;  // the decode kernel flags it
+        const int key = min(Lc >> pp.bucket_shift, kPlanBuckets - 1);
+        atomicAdd(&hist[kPlanBuckets - 1 - key], 1);
+    }
+    __syncthreads();
+    // bucket starts: exclusive scan, two buckets per thread
+    {
+        static_assert(kPlanBuckets == 2 * kPlanThreads, "two buckets a thread");
+        const int a = hist[2 * tid], b = hist[2 * tid + 1];
+        int total;
+        const int ex = block_exclusive_scan(a + b, wsum, &total);
+        __syncthreads();
+        hist[2 * tid] = ex;
+        hist[2 * tid + 1] = ex + a;
+    }
+    __syncthreads();
+    // rank of each sequence (any order within a bucket)
+    for (int s = tid; s < S; s += kPlanThreads) {
+        const int L = lens[s];
+        const int Lc = (L < 0 || L > pp.max_len) ? 0 : L;
+        const int key = min(Lc >> pp.bucket_shift, kPlanBuckets - 1);
+        sorted[atomicAdd(&hist[kPlanBuckets - 1 - key], 1)] = s;
+    }
+    __syncthreads();
+    // records per sequence: one per (KV head x head slice, partition group);
+    // a sequence with no tokens (or a bad length) keeps one group, whose CTA
+    // writes its zero rows
+    const int per_seq = pp.num_kv_heads * pp.head_slices;
+    auto groups_of = [&](int L) {
+        const int Lc = (L < 0 || L > pp.max_len) ? 0 : L;
+        const int np = max(1, (Lc + pp.partition_tokens - 1) / pp.partition_tokens);
+        return (np + pp.cta_parts - 1) / pp.cta_parts;
+    };
+    int run = 0;
+    for (int r0 = 0; r0 < S; r0 += kPlanThreads) {
+        const int r = r0 + tid;
+        const int c = r < S ? per_seq * groups_of(lens[sorted[r]]) : 0;
+        int total;
+        const int ex = block_exclusive_scan(c, wsum, &total);
+        if (r < S) off[r] = run + ex;
+        run += total;
+    }
+    __syncthreads();
+    // Everything above read only the lengths.  When this kernel runs as a
+    // programmatic dependent of the previous decode launch (which never
+    // writes lengths), that much overlaps its last CTAs; the counters and
+    // records it still reads are written only once it has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int i = tid; i < pp.num_counters; i += kPlanThreads) pp.done[i] = 0u;
+    for (int r = tid; r < S; r += kPlanThreads) {
+        const int s = sorted[r], L = lens[s];
+        const int ng = groups_of(L);
+        int4* out = pp.items + off[r];
+        for (int gh = 0; gh < per_seq; ++gh)
+            for (int grp = 0; grp < ng; ++grp) out[gh * ng + grp] = make_int4(s, L, gh, grp);
+    }
+    if (tid == 0) *pp.item_count = run;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_plan(const DecodePlanParams& pp, cudaStream_t stream)
+{
+    cudaError_t e = cudaFuncSetAttribute(decode_plan_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PlanSmem::BYTES);
+    if (e != cudaSuccess) return e;
+    // a programmatic dependent launch: it starts when the previous kernel on
+    // the stream lets its dependents launch (the decode kernel does so as
+    // its CTAs start; other kernels only at their end) and waits for that
+    // kernel to complete before it writes anything
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.dynamicSmemBytes = PlanSmem::BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_plan_kernel, pp);
+}

@@ -135,6 +135,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.num_heads / p.num_kv_heads;
+    // a work plan for the next call (a programmatic dependent of this launch)
+    // may start once every CTA has started: it reads only lengths until this
+    // launch completes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int s, g, sg, L, nparts, p0, np_cta, wpp, wsub, part, begin, end, nst;
     // this CTA's query heads: g*G + hb .. + ncol - 1 (all of the KV group,
     // or one slice of at most NC of them when the group is wider)
@@ -198,13 +202,31 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         begin = 0;
         end = 0;
     } else {
-        // ---- which item: slot b = (((s * Hkv) + g) * HS + hs) * max_groups +
-        // grp; group grp holds partitions grp * cta_parts .. + cta_parts - 1
-        // of (s, g), for head slice hs of the KV group's query heads
-        const int max_groups = (p.max_partitions + p.cta_parts - 1) / p.cta_parts;
-        const int grp = blockIdx.x % max_groups;
-        sg = blockIdx.x / max_groups;
+        // ---- which item: with a work plan, record b = (s, L, g * HS + hs,
+        // grp); else slot b = (((s * Hkv) + g) * HS + hs) * max_groups + grp.
+        // Group grp holds partitions grp * cta_parts .. + cta_parts - 1 of
+        // (s, g), for head slice hs of the KV group's query heads.
         const int HS = p.head_slices;
+        int grp, plan_len = 0;
+        if (p.items != nullptr) {
+            // launched as a dependent of the plan kernel: wait until it has
+            // completed and its writes (records, zeroed counters) are visible
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            const int4 it = p.items[blockIdx.x];  // read with the count: past it, stale
+            const int count = *p.item_count;
+            if ((int)blockIdx.x >= count) return;
+            if (it.x < 0 || it.x >= p.num_seqs || it.z < 0 || it.z >= p.num_kv_heads * HS) {
+                if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
+                return;
+            }
+            sg = it.x * (p.num_kv_heads * HS) + it.z;
+            plan_len = it.y;
+            grp = it.w;
+        } else {
+            const int max_groups = (p.max_partitions + p.cta_parts - 1) / p.cta_parts;
+            grp = blockIdx.x % max_groups;
+            sg = blockIdx.x / max_groups;
+        }
         const int sgk = sg / HS, hs = sg - sgk * HS;
         s = sgk / p.num_kv_heads;
         g = sgk - s * p.num_kv_heads;
@@ -228,7 +250,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                 spec_ids[u] = tok < (int64_t)p.max_blocks * B ? row[tok / B] : -1;
             }
         }
-        L = p.context_lens[s];
+        L = p.items != nullptr ? plan_len : p.context_lens[s];
         if (L < 0 || (int64_t)L > (int64_t)p.max_blocks * B) {
             if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
             L = 0;
@@ -804,9 +826,25 @@ cudaError_t launch_tc(const DecodeParams& p, const void* kmap, const void* vmap,
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, NW * 32, Gm::SMEM_BYTES, stream>>>(
-        p, *static_cast<const CUtensorMap*>(kmap), *static_cast<const CUtensorMap*>(vmap));
-    return cudaGetLastError();
+    if (p.items == nullptr) {
+        kern<<<(unsigned)grid, NW * 32, Gm::SMEM_BYTES, stream>>>(
+            p, *static_cast<const CUtensorMap*>(kmap), *static_cast<const CUtensorMap*>(vmap));
+        return cudaGetLastError();
+    }
+    // after a work plan: a programmatic dependent launch, so that the CTAs are
+    // resident while the plan kernel runs and start the moment it completes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NW * 32);
+    cfg.dynamicSmemBytes = Gm::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, *static_cast<const CUtensorMap*>(kmap),
+                              *static_cast<const CUtensorMap*>(vmap));
 }
 
 // NT: n8 column tiles of query heads per CTA (1: up to 8 columns, 2: up to 16)

@@ -166,10 +166,20 @@ swap_blocks_kernel(uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
 }
 
 // ---------------------------------------------------------------------------
-// CUDA-core paged decode.  One CTA = one (partition, query head, sequence);
-// its 4 warps take tokens round-robin, each lane holding D/32 elements of q,
-// of the running output and of each K/V row it reads.  Scores are kept in
-// base 2 (scale * log2 e folded into q), so exp2 replaces exp.
+// CUDA-core paged decode (any KV dtype, any group size).  One CTA = one
+// partition of one (sequence, KV head, head slice): the query heads of the
+// KV group -- all of them, or a slice of at most kCoreCols -- attend
+// together, so each K/V tile leaves memory once per group (auturnal guide
+// section 1: GQA/MQA shrink the number of KV heads a token's K/V serve).
+// Tiles of kCoreTile tokens of K and V are staged in shared memory by
+// 16-byte cp.async copies, two tiles in flight.  Per tile:
+//   scores   lane = token, warp w = heads w, w + 4, ...: s = q . k in fp32,
+//            with scale * log2(e) folded into q (scores in base 2);
+//   softmax  per head, against the running max (warp max over the tile);
+//   P V      each thread owns a float4 of head_dim for a few heads.
+// Masked tokens (past the partition's end or in a block whose id is out of
+// range) are staged as zeros and get score -inf, so NaN or stale data in
+// unused slots never reaches the output.
 // ---------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ float to_f32(T x);
@@ -181,6 +191,41 @@ template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x)
 {
     return __bfloat162float(x);
+}
+
+// The two elements of a 32-bit word of 16-bit T (low half first), widened.
+template <typename T>
+__device__ __forceinline__ float2 widen2(uint32_t w);
+template <>
+__device__ __forceinline__ float2 widen2<__nv_bfloat16>(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float2 widen2<__half>(uint32_t w)
+{
+    return make_float2(__half2float(__ushort_as_half((unsigned short)(w & 0xffffu))),
+                       __half2float(__ushort_as_half((unsigned short)(w >> 16))));
+}
+
+// The elements of a 16-byte vector of T (4 fp32 or 8 16-bit), widened.
+template <typename T>
+__device__ __forceinline__ void widen_vec(const uint4 raw, float* f)
+{
+    if constexpr (sizeof(T) == 4) {
+        f[0] = __uint_as_float(raw.x);
+        f[1] = __uint_as_float(raw.y);
+        f[2] = __uint_as_float(raw.z);
+        f[3] = __uint_as_float(raw.w);
+    } else {
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 v = widen2<T>(w[i]);
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
+    }
 }
 
 __device__ __forceinline__ void store_out(void* out, size_t idx, float v, int out_dtype)
@@ -200,6 +245,13 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
+__device__ __forceinline__ float warp_max(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
 // Context length of sequence s, or -1 (flagged) if it is out of range.
 __device__ __forceinline__ int checked_len(const DecodeParams& p, int s)
 {
@@ -211,15 +263,48 @@ __device__ __forceinline__ int checked_len(const DecodeParams& p, int s)
     return L;
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 constexpr int kCoreWarps = 4;
+constexpr int kCoreThreads = kCoreWarps * 32;
+constexpr int kCoreTile = 32;  // tokens per tile: one per lane in the score step
+constexpr int kCoreCols = 16;  // query heads per CTA (wider groups: head slices)
+
+// Shared-memory plan of the CUDA-core kernel for element type T, head_dim D.
+template <typename T, int D>
+struct CoreSmem {
+    static constexpr int EPV = 16 / (int)sizeof(T);       // elements per 16-byte vector
+    static constexpr int VPR = D / EPV;                    // vectors per K/V row
+    static constexpr int ROW = D * (int)sizeof(T) + 16;    // padded row: conflict-free reads
+    static constexpr int TILE = kCoreTile * ROW;           // K (or V) of one tile
+    static constexpr int STAGE = 2 * TILE;                 // K then V
+    static constexpr int Q_OFF = 2 * STAGE;                // float q [kCoreCols][D]
+    static constexpr int P_OFF = Q_OFF + kCoreCols * D * 4;          // float p [cols][tile]
+    static constexpr int A_OFF = P_OFF + kCoreCols * kCoreTile * 4;  // float alpha [cols]
+    static constexpr int M_OFF = A_OFF + kCoreCols * 4;              // float m, l [cols]
+    static constexpr int BYTES = M_OFF + 2 * kCoreCols * 4;
+};
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kCoreWarps * 32)
+__global__ void __launch_bounds__(kCoreThreads)
 decode_cuda_core_kernel(const DecodeParams p)
 {
-    constexpr int E = D / 32;  // elements per lane
-    const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    using Sm = CoreSmem<T, D>;
+    constexpr int ND4 = D / 4;                          // float4 columns of an output row
+    constexpr int PAIRS = kCoreCols * ND4 / kCoreThreads;  // (head, float4) outputs a thread
+    extern __shared__ __align__(16) uint8_t csm[];
+    float* qs = reinterpret_cast<float*>(csm + Sm::Q_OFF);
+    float* ps = reinterpret_cast<float*>(csm + Sm::P_OFF);
+    float* al = reinterpret_cast<float*>(csm + Sm::A_OFF);
+    float* ml = reinterpret_cast<float*>(csm + Sm::M_OFF);
+
+    const int part = blockIdx.x, s = blockIdx.z;
+    const int HS = p.head_slices;
+    const int g = blockIdx.y / HS, hs = blockIdx.y - g * HS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int L = checked_len(p, s);
     if (L < 0) L = 0;  // bad length: zero output, flagged above
     const int nparts = (L + p.partition_tokens - 1) / p.partition_tokens;
@@ -227,73 +312,186 @@ decode_cuda_core_kernel(const DecodeParams p)
     const int begin = part * p.partition_tokens;
     const int end = min(L, begin + p.partition_tokens);
     const int G = p.num_heads / p.num_kv_heads;
-    const int g = h / G;
+    const int GC = (G + HS - 1) / HS;  // columns of a slice
+    const int hb = hs * GC;
+    const int ncol = min(GC, G - hb);
+    const size_t hrow0 = (size_t)s * p.num_heads + (size_t)g * G + hb;  // first output row
 
-    const T* qrow = static_cast<const T*>(p.q) + ((size_t)s * p.num_heads + h) * D + lane * E;
-    float qv[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) qv[e] = to_f32(qrow[e]) * p.scale_log2;
+    // q of this slice's heads, widened and scaled (scores in base 2)
+    for (int i = threadIdx.x; i < kCoreCols * D; i += kCoreThreads) {
+        const int c = i / D, d = i - c * D;
+        qs[i] = c < ncol ? to_f32(static_cast<const T*>(p.q)[(hrow0 + c) * D + d]) * p.scale_log2
+                         : 0.f;
+    }
 
-    const T* kc = static_cast<const T*>(p.k_cache);
-    const T* vc = static_cast<const T*>(p.v_cache);
     const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
-    float m = -INFINITY, l = 0.f, acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
+    const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
+    const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(csm);
+    const int ntiles = (end - begin + kCoreTile - 1) / kCoreTile;
 
-    for (int t = begin + warp; t < end; t += kCoreWarps) {
-        const int32_t blk = table[t / p.block_size];
-        if (blk < 0 || blk >= p.num_blocks) {
-            if (lane == 0) flag(p.status, PKV_STATUS_BAD_BLOCK);
-            continue;
+    // Stage tile i (tokens begin + i*tile ...) into buffer i & 1: a 16-byte
+    // cp.async per vector of a valid token's K and V row, zeros otherwise.
+    auto stage = [&](int i) {
+        const int t0 = begin + i * kCoreTile;
+        uint8_t* buf = csm + (i & 1) * Sm::STAGE;
+        for (int v = threadIdx.x; v < kCoreTile * Sm::VPR; v += kCoreThreads) {
+            const int r = v / Sm::VPR, c = v - r * Sm::VPR;
+            const int t = t0 + r;
+            const int off = r * Sm::ROW + c * 16;
+            int32_t blk = -1;
+            if (t < end) {
+                blk = table[t / p.block_size];
+                if (blk < 0 || blk >= p.num_blocks) {
+                    if (c == 0) flag(p.status, PKV_STATUS_BAD_BLOCK);
+                    blk = -1;
+                }
+            }
+            if (blk >= 0) {
+                const size_t row =
+                    ((size_t)blk * p.num_kv_heads + g) * p.block_size + t % p.block_size;
+                const size_t src = row * (D * sizeof(T)) + (size_t)c * 16;
+                const uint32_t dst = sbase + (uint32_t)((i & 1) * Sm::STAGE + off);
+                cp_async16(dst, kc + src);
+                cp_async16(dst + Sm::TILE, vc + src);
+            } else {
+                *reinterpret_cast<uint4*>(buf + off) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(buf + Sm::TILE + off) = make_uint4(0, 0, 0, 0);
+            }
         }
-        const size_t row = ((size_t)blk * p.num_kv_heads + g) * p.block_size + t % p.block_size;
-        const T* kr = kc + row * D + lane * E;
-        const T* vr = vc + row * D + lane * E;
-        float dot = 0.f;
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    // softmax state of the heads c = warp + 4k this warp scores (all lanes
+    // hold the same copy), and this thread's output accumulators:
+    // pair j = (head c_j, float4 column d4)
+    constexpr int HPW = kCoreCols / kCoreWarps;
+    float m_run[HPW], l_run[HPW];
 #pragma unroll
-        for (int e = 0; e < E; ++e) dot += qv[e] * to_f32(kr[e]);
-        const float z = warp_sum(dot);
-        const float m_new = fmaxf(m, z);
-        const float alpha = exp2f(m - m_new);  // 0 when m is -inf
-        const float pz = exp2f(z - m_new);
-        l = l * alpha + pz;
+    for (int k = 0; k < HPW; ++k) {
+        m_run[k] = -INFINITY;
+        l_run[k] = 0.f;
+    }
+    float4 acc[PAIRS];
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = acc[e] * alpha + pz * to_f32(vr[e]);
-        m = m_new;
+    for (int j = 0; j < PAIRS; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int d4 = threadIdx.x % ND4;
+
+    if (ntiles > 0) stage(0);
+    for (int i = 0; i < ntiles; ++i) {
+        if (i + 1 < ntiles) {
+            stage(i + 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        const uint8_t* kt = csm + (i & 1) * Sm::STAGE;
+        const uint8_t* vt = kt + Sm::TILE;
+        // ---- scores: lane = token, this warp's heads
+        const int t = begin + i * kCoreTile + lane;
+        bool ok = t < end;
+        if (ok) {
+            const int32_t blk = table[t / p.block_size];
+            ok = blk >= 0 && blk < p.num_blocks;
+        }
+        float sc[HPW];
+#pragma unroll
+        for (int k = 0; k < HPW; ++k) sc[k] = 0.f;
+        const uint8_t* krow = kt + lane * Sm::ROW;
+#pragma unroll 4
+        for (int c = 0; c < Sm::VPR; ++c) {
+            float kf[Sm::EPV];
+            widen_vec<T>(*reinterpret_cast<const uint4*>(krow + c * 16), kf);
+#pragma unroll
+            for (int k = 0; k < HPW; ++k) {
+                const float* qq = qs + (warp + kCoreWarps * k) * D + c * Sm::EPV;
+#pragma unroll
+                for (int u = 0; u < Sm::EPV; ++u) sc[k] += qq[u] * kf[u];
+            }
+        }
+        // ---- online softmax per head (base 2)
+#pragma unroll
+        for (int k = 0; k < HPW; ++k) {
+            const int col = warp + kCoreWarps * k;
+            const float x = ok ? sc[k] : -INFINITY;
+            const float m_new = fmaxf(m_run[k], warp_max(x));
+            // nothing seen yet (m_new = -inf): alpha 1, p 0
+            const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run[k] - m_new);
+            const float pz = m_new == -INFINITY ? 0.f : exp2f(x - m_new);
+            l_run[k] = l_run[k] * alpha + warp_sum(pz);
+            m_run[k] = m_new;
+            ps[col * kCoreTile + lane] = pz;
+            if (lane == 0) al[col] = alpha;
+        }
+        __syncthreads();
+        // ---- O += P V for this thread's (head, float4) outputs
+#pragma unroll
+        for (int j = 0; j < PAIRS; ++j) {
+            const int col = (threadIdx.x + j * kCoreThreads) / ND4;
+            const float a = al[col];
+            acc[j].x *= a;
+            acc[j].y *= a;
+            acc[j].z *= a;
+            acc[j].w *= a;
+        }
+#pragma unroll 4
+        for (int r = 0; r < kCoreTile; ++r) {
+            const T* vr = reinterpret_cast<const T*>(vt + r * Sm::ROW) + d4 * 4;
+            float vf[4];
+            if constexpr (sizeof(T) == 4) {
+                const float4 v4 = *reinterpret_cast<const float4*>(vr);
+                vf[0] = v4.x;
+                vf[1] = v4.y;
+                vf[2] = v4.z;
+                vf[3] = v4.w;
+            } else {
+                const uint2 raw = *reinterpret_cast<const uint2*>(vr);
+                const float2 lo = widen2<T>(raw.x), hi = widen2<T>(raw.y);
+                vf[0] = lo.x;
+                vf[1] = lo.y;
+                vf[2] = hi.x;
+                vf[3] = hi.y;
+            }
+#pragma unroll
+            for (int j = 0; j < PAIRS; ++j) {
+                const int col = (threadIdx.x + j * kCoreThreads) / ND4;
+                const float pz = ps[col * kCoreTile + r];
+                acc[j].x += pz * vf[0];
+                acc[j].y += pz * vf[1];
+                acc[j].z += pz * vf[2];
+                acc[j].w += pz * vf[3];
+            }
+        }
+        __syncthreads();  // buffer i & 1 and ps are reused by the next tile
     }
 
-    // Merge the warps' running states.
-    __shared__ float sm_m[kCoreWarps], sm_l[kCoreWarps];
-    __shared__ float sm_o[kCoreWarps][D];
     if (lane == 0) {
-        sm_m[warp] = m;
-        sm_l[warp] = l;
-    }
 #pragma unroll
-    for (int e = 0; e < E; ++e) sm_o[warp][lane * E + e] = acc[e];
+        for (int k = 0; k < HPW; ++k) {
+            const int col = warp + kCoreWarps * k;
+            ml[col] = m_run[k];
+            ml[kCoreCols + col] = l_run[k];
+        }
+    }
     __syncthreads();
-    float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kCoreWarps; ++w) M = fmaxf(M, sm_m[w]);
-    float den = 0.f;
-    float wgt[kCoreWarps];
-#pragma unroll
-    for (int w = 0; w < kCoreWarps; ++w) {
-        wgt[w] = (M == -INFINITY) ? 0.f : exp2f(sm_m[w] - M);
-        den += sm_l[w] * wgt[w];
-    }
-    const size_t orow = ((size_t)s * p.num_heads + h) * D;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCoreWarps; ++w) o += sm_o[w][d] * wgt[w];
+    for (int j = 0; j < PAIRS; ++j) {
+        const int col = (threadIdx.x + j * kCoreThreads) / ND4;
+        if (col >= ncol) continue;
+        const size_t hrow = hrow0 + col;
+        const float den = ml[kCoreCols + col];
         if (nparts <= 1) {
-            store_out(p.out, orow + d, den > 0.f ? o / den : 0.f, p.out_dtype);
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            const size_t o = hrow * D + d4 * 4;
+            store_out(p.out, o + 0, acc[j].x * inv, p.out_dtype);
+            store_out(p.out, o + 1, acc[j].y * inv, p.out_dtype);
+            store_out(p.out, o + 2, acc[j].z * inv, p.out_dtype);
+            store_out(p.out, o + 3, acc[j].w * inv, p.out_dtype);
         } else {
-            const size_t slot = ((size_t)s * p.num_heads + h) * p.max_partitions + part;
-            p.ws_o[slot * D + d] = o;
-            if (d == 0) p.ws_ml[slot] = make_float2(M, den);
+            const size_t slot = hrow * p.max_partitions + part;
+            *reinterpret_cast<float4*>(p.ws_o + slot * D + d4 * 4) = acc[j];
+            if (d4 == 0) p.ws_ml[slot] = make_float2(ml[col], den);
         }
     }
 }
@@ -329,18 +527,14 @@ __global__ void lse_reduce_kernel(const DecodeParams p)
 
 }  // namespace
 
+// Looked up on every call, in the caller's current context: an address kept
+// from an earlier call could belong to a context since destroyed (a device
+// reset) or to another one.  The lookup allocates nothing.
 unsigned int* pkv_status_word_ptr()
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    static unsigned int* cache[64] = {};
-    if (dev < 0 || dev >= 64) return nullptr;
-    if (!cache[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<unsigned int*>(ptr);
-    }
-    return cache[dev];
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+    return static_cast<unsigned int*>(ptr);
 }
 
 cudaError_t launch_kv_write(void* k_cache, void* v_cache, const void* key, const void* value,
@@ -408,25 +602,42 @@ cudaError_t launch_kv_swap_blocks(void* dst_k, void* dst_v, const void* src_k, c
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode_cuda_core(const DecodeParams& p, int kv_dtype, cudaStream_t stream)
+namespace {
+
+template <typename T, int D>
+cudaError_t launch_core(const DecodeParams& p, dim3 grid, cudaStream_t stream)
 {
-    dim3 grid(p.max_partitions, p.num_heads, p.num_seqs);
-    dim3 block(kCoreWarps * 32);
-#define PKV_LAUNCH_CORE(T)                                                        \
-    do {                                                                          \
-        if (p.head_dim == 64)                                                     \
-            decode_cuda_core_kernel<T, 64><<<grid, block, 0, stream>>>(p);        \
-        else                                                                      \
-            decode_cuda_core_kernel<T, 128><<<grid, block, 0, stream>>>(p);       \
-    } while (0)
-    if (kv_dtype == PKV_F32)
-        PKV_LAUNCH_CORE(float);
-    else if (kv_dtype == PKV_F16)
-        PKV_LAUNCH_CORE(__half);
-    else
-        PKV_LAUNCH_CORE(__nv_bfloat16);
-#undef PKV_LAUNCH_CORE
+    constexpr int bytes = CoreSmem<T, D>::BYTES;
+    auto kern = decode_cuda_core_kernel<T, D>;
+    // set on every launch: the attribute belongs to the current device's copy
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kCoreThreads, bytes, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_core_dim(const DecodeParams& p, dim3 grid, cudaStream_t stream)
+{
+    return p.head_dim == 64 ? launch_core<T, 64>(p, grid, stream)
+                            : launch_core<T, 128>(p, grid, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_cuda_core(const DecodeParams& p_in, int kv_dtype, cudaStream_t stream)
+{
+    // one CTA per (partition, KV head x head slice, sequence); a slice holds
+    // at most kCoreCols query heads of the group
+    DecodeParams p = p_in;
+    const int G = p.num_heads / p.num_kv_heads;
+    p.head_slices = (G + kCoreCols - 1) / kCoreCols;
+    const long long gy = (long long)p.num_kv_heads * p.head_slices;
+    if (gy > 65535 || p.num_seqs > 65535) return cudaErrorInvalidConfiguration;
+    dim3 grid(p.max_partitions, (unsigned)gy, p.num_seqs);
+    if (kv_dtype == PKV_F32) return launch_core_dim<float>(p, grid, stream);
+    if (kv_dtype == PKV_F16) return launch_core_dim<__half>(p, grid, stream);
+    return launch_core_dim<__nv_bfloat16>(p, grid, stream);
 }
 
 cudaError_t launch_lse_reduce(const DecodeParams& p, cudaStream_t stream)

@@ -40,7 +40,31 @@ struct DecodeParams {
     const int32_t* group_start;
     const int32_t* shared_tokens;
     int num_groups;
+    // Split launches with a work plan (tensor-core kernel only; NULL
+    // otherwise): CTA b takes record items[b] = (sequence, context length,
+    // KV head * head_slices + head slice, partition group) if b < *item_count,
+    // and exits otherwise.  Written by the plan kernel just before.
+    const int4* items;
+    const int* item_count;
 };
+
+// Work plan of a split tensor-core launch (decode_plan.cu): zeroes the
+// completion counters, orders the sequences longest first and writes one
+// record per CTA with work, in that order.  One CTA; num_seqs <= kPlanMaxSeqs.
+constexpr int kPlanMaxSeqs = 4096;
+constexpr int kPlanBuckets = 2048;  // length buckets of the counting sort
+struct DecodePlanParams {
+    const int32_t* context_lens;  // [num_seqs]
+    int num_seqs, num_kv_heads, head_slices;
+    int partition_tokens, cta_parts;
+    int max_len;                  // max_blocks * block_size: longer lengths are bad
+    int bucket_shift;             // bucket of a length L: min(L >> shift, kPlanBuckets - 1)
+    int4* items;                  // capacity: the launch's grid
+    int* item_count;
+    unsigned int* done;           // completion counters to zero
+    int num_counters;
+};
+cudaError_t launch_decode_plan(const DecodePlanParams& pp, cudaStream_t stream);
 
 // Everything one prefill launch needs (passed by value).
 struct PrefillParams {

@@ -30,6 +30,11 @@ def test_reference_arm_prints_one_contract_line():
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+    # the same workload description as the GPU arm's line (whose Step builds
+    # its tables with the library's allocator: host code, no GPU needed)
+    import paged_kv_cache_312_gb300 as pkv
+    assert d["config"] == bench.config_of(bench.Step(2, 0, pkv.BlockAllocator), False, 1, 1)
+    assert cb["cpu_model"]
 
 
 def test_warmup_below_three_is_refused():
@@ -51,6 +56,25 @@ def test_launch_partition_rule(key):
             assert P == 0
         else:
             assert P == 1024
+
+
+def test_ragged_batches_run_unsplit_with_the_work_plan():
+    # workload 3's lognormal lengths are ragged (the longest far above the
+    # mean): one pass per (sequence, KV head), longest first; workload 2's
+    # uniform lengths are not; a split launch always has the plan
+    import numpy as np
+    from workloads import draw_lengths
+    for key, expect_ragged in ((2, False), (3, True), (4, False)):
+        w = WORKLOADS[key]
+        # the lengths make_decode_case draws first from the same seed
+        lens = draw_lengths(w, np.random.default_rng(0)).tolist()
+        assert bench.ragged(lens) == expect_ragged
+        maxb = -(-max(lens) // w.block_size)
+        P = bench.launch_partition(w, maxb, lens)
+        assert bench.work_plan(w, lens, P) == (expect_ragged or P > 0)
+        if expect_ragged:
+            assert P == 0
+    assert bench.ragged([1, 1, 1, 10]) and not bench.ragged([5, 5, 5, 5])
 
 
 def test_sweep_workloads_cover_the_sweep_grid():

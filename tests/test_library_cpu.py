@@ -123,10 +123,15 @@ def test_decode_with_no_sequences_is_a_no_op():
 
 def test_workspace_size_formula():
     L = pkv.lib()
-    assert L.pkv_decode_workspace_bytes(8, 32, 128, 32768, 0) == 0
+    # unsplit: the optional work plan alone (record count, one record per
+    # (sequence, query head) at most)
+    assert L.pkv_decode_workspace_bytes(8, 32, 128, 32768, 0) == 256 + 8 * 32 * 16
+    assert L.pkv_decode_workspace_bytes(8, 32, 128, 32768, -1) == 0
     S, H, P, D = 8, 32, 64, 128
     a = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    expect = a(S * H * 4) + a(S * H * P * 8) + S * H * P * D * 4
+    # counters, (max, sum) and output per partition, the plan's record count
+    # and its records (one per possible CTA)
+    expect = a(S * H * 4) + a(S * H * P * 8) + a(S * H * P * D * 4) + 256 + S * H * P * 16
     assert L.pkv_decode_workspace_bytes(S, H, D, 32768, 512) == expect
 
 
@@ -359,6 +364,95 @@ def test_allocator_dense_tables():
     assert t.tolist() == [[9, 8, -1], [-1, -1, -1]] and l.tolist() == [5, 0]
     with pytest.raises(pkv.PkvError):
         a.dense_tables([1], 1)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_step_append_tables_keeps_dense_tables_equal_to_the_reference(seed):
+    # A batch stepped 60 times with the in-place table patching (half of it
+    # forked from the other half first, so that shared partial blocks are
+    # copied): after every step the patched tables and lengths equal the
+    # reference block manager's dense tables, and slots / copy pairs its
+    # decisions.
+    from workloads import dense_tables
+    rnd = random.Random(seed)
+    NB, B, W = 400, 4, 6
+    order = list(np.random.default_rng(seed).permutation(NB))
+    cpp, ref = pkv.BlockAllocator(NB, B, free_order=order), BlockManager(NB, B, free_order=order)
+    for s in range(W // 2):
+        n = rnd.randint(0, 9)
+        cpp.add(s, n)
+        ref.add(s, n)
+    for s in range(W // 2, W):
+        cpp.fork(s - W // 2, s)
+        ref.fork(s - W // 2, s)
+    batch, maxb = list(range(W)), 40
+    seqs = torch.tensor(batch, dtype=torch.int64)
+    tables, lens = cpp.dense_tables(batch, maxb)
+    slots = torch.empty(W, dtype=torch.int64)
+    pairs = torch.empty((W, 2), dtype=torch.int64)
+    copies = 0
+    for _ in range(60):
+        ns = cpp.step_append_tables(seqs, slots, pairs, tables, lens)
+        r_slots, r_pairs = ref.step_append(batch)
+        copies += ns
+        assert slots.tolist() == r_slots
+        assert [tuple(p) for p in pairs[:ns].tolist()] == r_pairs
+        t_ref, l_ref = dense_tables(ref, batch, maxb)
+        assert torch.equal(tables, t_ref) and torch.equal(lens, l_ref)
+    assert cpp.stats() == ref.stats()
+
+
+def test_step_append_tables_with_forks_and_errors():
+    from workloads import dense_tables
+    rnd = random.Random(7)
+    NB, B, W = 300, 4, 5
+    order = list(np.random.default_rng(7).permutation(NB))
+    cpp, ref = pkv.BlockAllocator(NB, B, free_order=order), BlockManager(NB, B, free_order=order)
+    for s in range(W):
+        cpp.add(s, 6)
+        ref.add(s, 6)
+    batch, nid, maxb = list(range(W)), W, 30
+    for rnd_sel in range(5):
+        # beam re-selection: new beam b forks old beam parent[b]; old beams freed
+        parent = [rnd.randrange(W) for _ in range(W)]
+        new = list(range(nid, nid + W))
+        for b in range(W):
+            cpp.fork(batch[parent[b]], new[b])
+            ref.fork(batch[parent[b]], new[b])
+        for s in batch:
+            cpp.free(s)
+            ref.free_seq(s)
+        batch, nid = new, nid + W
+        seqs = torch.tensor(batch, dtype=torch.int64)
+        tables, lens = cpp.dense_tables(batch, maxb)
+        slots = torch.empty(W, dtype=torch.int64)
+        pairs = torch.empty((W, 2), dtype=torch.int64)
+        for _ in range(rnd.randint(1, 6)):
+            ns = cpp.step_append_tables(seqs, slots, pairs, tables, lens)
+            r_slots, r_pairs = ref.step_append(batch)
+            assert slots.tolist() == r_slots
+            assert [tuple(p) for p in pairs[:ns].tolist()] == r_pairs
+            t_ref, l_ref = dense_tables(ref, batch, maxb)
+            assert torch.equal(tables, t_ref) and torch.equal(lens, l_ref)
+    # a table that would outgrow its row, or a sequence listed twice: refused,
+    # nothing changed
+    a = pkv.BlockAllocator(20, 4)
+    a.add(0, 8)
+    a.add(1, 3)
+    seqs = torch.tensor([0, 1], dtype=torch.int64)
+    tables, lens = a.dense_tables([0, 1], 2)
+    slots = torch.empty(2, dtype=torch.int64)
+    pairs = torch.empty((2, 2), dtype=torch.int64)
+    snap = (a.table(0), a.table(1), a.num_free(), tables.clone(), lens.clone())
+    with pytest.raises(pkv.PkvError) as ei:
+        a.step_append_tables(seqs, slots, pairs, tables, lens)
+    assert ei.value.code == -2
+    with pytest.raises(pkv.PkvError) as ei:
+        a.step_append_tables(torch.tensor([1, 1], dtype=torch.int64), slots, pairs,
+                             tables, lens)
+    assert ei.value.code == -9
+    assert (a.table(0), a.table(1), a.num_free()) == snap[:3]
+    assert torch.equal(tables, snap[3]) and torch.equal(lens, snap[4])
 
 
 def test_beam_fork_cow_pairs():

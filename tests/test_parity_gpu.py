@@ -4,8 +4,8 @@ Cache writes and block copies must match bit for bit; attention outputs must
 be within max-abs 2e-3 of the oracle for 16-bit KV and 1e-5 for fp32 KV (fp32
 output).  Cases span several 16-token tiles, ragged tails, empty sequences,
 bad ids, every block size / head_dim / group size the kernels support, both
-decode kernels, the split-context path, and the full-size workloads (checked
-on sampled sequences)."""
+decode kernels, the split-context path, and the full-size workloads through
+the benchmark's own step (every sequence checked)."""
 import numpy as np
 import pytest
 import torch
@@ -48,14 +48,18 @@ def bits(t):
     return t.view(torch.int32) if t.element_size() == 4 else t.view(torch.int16)
 
 
-def gpu_decode(q, kc, vc, bt, cl, scale, B, Hkv, P=0, out_dtype=torch.float32, kernel=None):
+def gpu_decode(q, kc, vc, bt, cl, scale, B, Hkv, P=0, out_dtype=torch.float32, kernel=None,
+               plan=False):
+    """Decode attention through the C ABI; `plan` gives an unsplit launch the
+    optional workspace (the work plan: longest sequence first).  Split
+    launches always take a workspace (and so a plan)."""
     if kernel is not None:
         pkv.set_decode_kernel(kernel)
     try:
         S, Hq, D = q.shape
         out = torch.full((S, Hq, D), float("nan"), dtype=out_dtype, device=DEV)
         ws = None
-        if P:
+        if P or plan:
             n = pkv.decode_workspace_bytes(S, Hq, D, bt.shape[1] * B, P)
             ws = torch.empty(n, dtype=torch.uint8, device=DEV)
         pkv.paged_decode_attention(out, q.to(DEV), kc, vc, bt.to(DEV), cl.to(DEV), scale, B, Hkv,
@@ -163,6 +167,29 @@ def test_decode_small(dt, Hq, Hkv, D, B, P, kernel):
     assert torch.equal(out[0].cpu(), torch.zeros_like(out[0].cpu()))  # length-0 row
 
 
+@pytest.mark.parametrize("dt,Hq,Hkv,D,B", SMALL)
+def test_unsplit_work_plan_matches_oracle_and_the_unplanned_call(dt, Hq, Hkv, D, B):
+    # An unsplit call with the optional workspace runs its CTAs longest
+    # sequence first (the work plan); the lengths are shuffled so that the
+    # plan reorders them.  Each (sequence, KV head) is still one CTA doing the
+    # same arithmetic, so the output equals the unplanned call's bit for bit.
+    w = Workload(0, "plan", dt, Hq, Hkv, D, B, len(RAGGED), "fixed")
+    lengths = list(np.random.default_rng(Hq + D + B).permutation(RAGGED + [2049, 5, 0]))
+    case = make_decode_case(w, seed=Hq * 3 + B + D, lengths=lengths)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    planned = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, B, Hkv,
+                         plan=True)
+    assert pkv.device_status() == 0
+    plain = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, B, Hkv)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, B, Hkv)
+    assert max_err(planned, ref) <= tol(w.torch_dtype)
+    assert torch.equal(planned, plain)
+    for s_, n in enumerate(lengths):
+        if n == 0:
+            assert not planned[s_].any()
+
+
 @pytest.mark.parametrize("B", [8, 16, 32])
 @pytest.mark.parametrize("G", [1, 4, 8, 16, 64])
 @pytest.mark.parametrize("D", [64, 128])
@@ -248,8 +275,9 @@ def test_bad_block_id_and_length_are_flagged():
     cl = case.context_lens.clone()
     cl[2] = bt.shape[1] * 16 + 1
     kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
-    for kernel in (pkv.KERNEL_AUTO, pkv.KERNEL_CUDA_CORE):
-        out = gpu_decode(case.q, kc, vc, bt, cl, w.scale, 16, 2, kernel=kernel)
+    for kernel, plan, P in ((pkv.KERNEL_AUTO, False, 0), (pkv.KERNEL_CUDA_CORE, False, 0),
+                            (pkv.KERNEL_AUTO, True, 0), (pkv.KERNEL_AUTO, True, 16)):
+        out = gpu_decode(case.q, kc, vc, bt, cl, w.scale, 16, 2, kernel=kernel, plan=plan, P=P)
         st = pkv.device_status()
         assert st & 1 and st & 2
         ref = oracle.paged_decode_attention(case.q[:1], case.k_cache, case.v_cache, bt[:1],
@@ -466,17 +494,21 @@ STEP_CASES = [  # dtype, Hq, Hkv, D, B, partition
 ]
 
 
+@pytest.mark.parametrize("plan", [False, True])
 @pytest.mark.parametrize("dt,Hq,Hkv,D,B,P", STEP_CASES)
-def test_decode_step_matches_oracle(dt, Hq, Hkv, D, B, P):
+def test_decode_step_matches_oracle(dt, Hq, Hkv, D, B, P, plan):
     # the new position's slot holds NaN until the step writes it; lengths put
-    # the new token first in a block, last in a block, mid-block, alone
+    # the new token first in a block, last in a block, mid-block, alone.
+    # `plan` gives an unsplit step the optional workspace (the work plan)
+    if plan and P:
+        pytest.skip("a split step always has the plan")
     w = Workload(0, "step", dt, Hq, Hkv, D, B, 6, "fixed", writes_new_token=True)
     lengths = [1, B, B + 1, 3 * B - 5, 700, 2049]
     case = make_decode_case(w, seed=Hq + B + P, lengths=lengths)
     kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
     out = torch.full(case.q.shape, float("nan"), dtype=torch.float32, device=DEV)
     ws = None
-    if P:
+    if P or plan:
         n = pkv.decode_workspace_bytes(6, Hq, D, case.block_tables.shape[1] * B, P)
         ws = torch.empty(n, dtype=torch.uint8, device=DEV)
     pkv.decode_step(out, case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV), kc, vc,
@@ -694,17 +726,78 @@ def test_nan_poison_and_physical_permutation():
 # full-size workloads, in the launch configuration the benchmark times
 # --------------------------------------------------------------------------
 
-def sampled_oracle(case_q, kc_host, vc_host, bt, cl, w, idx):
-    idx = torch.as_tensor(idx)
-    return oracle.paged_decode_attention(case_q[idx], kc_host, vc_host, bt[idx], cl[idx], w.scale,
-                                         w.block_size, w.num_kv_heads,
-                                         nthreads=oracle.default_threads())
+def full_oracle(q, kc_host, vc_host, bt, cl, w):
+    """The oracle's output for every sequence and query head of the batch."""
+    return oracle.paged_decode_attention(q, kc_host, vc_host, bt, cl, w.scale, w.block_size,
+                                         w.num_kv_heads, nthreads=oracle.default_threads())
 
 
-def pick(lens, k=6):
-    order = np.argsort(np.asarray(lens))
-    return sorted(set([int(order[0]), int(order[-1]), int(order[len(order) // 2])] +
-                      list(np.random.default_rng(0).choice(len(lens), k, replace=False))))
+_STEPS = {}
+
+
+def bench_steps(key):
+    """The benchmark's host inputs of workload `key` (seed 0), built twice:
+    tables from the library's allocator (what the GPU gets) and from the
+    oracle's own block manager (what the oracle gets).  One workload is kept
+    at a time."""
+    import bench
+    if key not in _STEPS:
+        _STEPS.clear()
+        _STEPS[key] = (bench.Step(key, 0, pkv.BlockAllocator), bench.Step(key, 0, BlockManager))
+    return _STEPS[key]
+
+
+@pytest.mark.parametrize("key,grouped,parts", [
+    pytest.param(2, False, 1, id="w2-decode_step"),
+    pytest.param(3, False, 1, id="w3-gqa"),
+    pytest.param(4, False, 1, id="w4-long-context-split"),
+    pytest.param(5, True, 1, id="w5-beam-groups"),
+    pytest.param(5, True, 2, id="w5-beam-groups-2-parts"),
+    pytest.param(5, False, 1, id="w5-ungrouped-decode_step"),
+])
+def test_full_size_step_as_benchmarked(key, grouped, parts):
+    # The very calls bench.py times (its GpuStep: copy-on-write copies, then
+    # one decode call that appends each sequence's new token and attends, in
+    # the benchmark's launch configuration), at full size, on the benchmark's
+    # inputs.  Every output element of every sequence is checked against the
+    # oracle, and both caches bit for bit.
+    import bench
+    st, st_ref = bench_steps(key)
+    w = st.w
+    assert torch.equal(st.tables, st_ref.tables) and torch.equal(st.lens, st_ref.lens)
+    assert torch.equal(st.pairs, st_ref.pairs)
+    if st.slots is not None:
+        assert torch.equal(st.slots, st_ref.slots)
+    g = bench.GpuStep(pkv, st, DEV, grouped, parts)
+    g.out.fill_(float("nan"))
+    g.run()
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    # the oracle's step on its own copy of the cache
+    kh, vh = st_ref.k_cache.clone(), st_ref.v_cache.clone()
+    B = w.block_size
+    if st_ref.setup_slots is not None:
+        oracle.kv_write(kh, vh, st_ref.setup_keys, st_ref.setup_vals, st_ref.setup_slots, B)
+    if st_ref.pairs.shape[0]:
+        oracle.kv_copy_blocks(kh, vh, st_ref.pairs)
+    if st_ref.slots is not None:
+        oracle.kv_write(kh, vh, st_ref.new_key, st_ref.new_value, st_ref.slots, B)
+    assert torch.equal(bits(g.kc), bits(kh)) and torch.equal(bits(g.vc), bits(vh))
+    ref = full_oracle(st_ref.q, kh, vh, st_ref.tables, st_ref.lens, w)
+    out = g.out.cpu().double().numpy()
+    assert np.isfinite(out).all()
+    err = np.abs(out - ref)
+    worst = np.unravel_index(int(err.argmax()), err.shape)
+    assert float(err.max()) <= TOL16, ("max abs error %g at (seq, head, d) = %s" %
+                                       (float(err.max()), worst))
+    # running the step again (its copies and writes are idempotent) gives the
+    # same output bits: no state leaks from one launch to the next
+    first = g.out.clone()
+    g.run()
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    assert torch.equal(first, g.out)
+    del g
 
 
 def test_workload2_write_then_attend_full_size():
@@ -725,26 +818,8 @@ def test_workload2_write_then_attend_full_size():
     oracle.kv_write(case.k_cache, case.v_cache, case.new_key, case.new_value, slots_r,
                     w.block_size)
     assert torch.equal(bits(kc), bits(case.k_cache)) and torch.equal(bits(vc), bits(case.v_cache))
-    idx = pick(cl.tolist())
-    ref = sampled_oracle(case.q, case.k_cache, case.v_cache, bt_r, cl_r, w, idx)
-    assert max_err(out[idx], ref) <= TOL16
-
-
-@pytest.mark.parametrize("key", [3, 4])
-def test_gqa_and_long_context_full_size(key):
-    import bench
-    w = WORKLOADS[key]
-    case = make_decode_case(w, seed=0)
-    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
-    P = bench.launch_partition(w, case.block_tables.shape[1])
-    out = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, w.block_size,
-                     w.num_kv_heads, P=P)
-    assert pkv.device_status() == 0
-    idx = pick(case.context_lens.tolist(), k=4 if key == 3 else 1)
-    ref = sampled_oracle(case.q, case.k_cache, case.v_cache, case.block_tables,
-                         case.context_lens, w, idx)
-    assert max_err(out[idx], ref) <= TOL16
-    assert torch.isfinite(out).all()
+    ref = full_oracle(case.q, case.k_cache, case.v_cache, bt_r, cl_r, w)
+    assert max_err(out, ref) <= TOL16
 
 
 def test_workload5_beam_step_full_size():
@@ -782,9 +857,8 @@ def test_workload5_beam_step_full_size():
     oracle.kv_copy_blocks(kh, vh, pairs_r)
     oracle.kv_write(kh, vh, case.new_key, case.new_value, slots_r, B)
     assert torch.equal(bits(kc), bits(kh)) and torch.equal(bits(vc), bits(vh))
-    idx = pick(cl.tolist())
-    ref = sampled_oracle(case.q, kh, vh, bt_r, cl_r, w, idx)
-    assert max_err(out[idx], ref) <= TOL16
+    ref = full_oracle(case.q, kh, vh, bt_r, cl_r, w)
+    assert max_err(out, ref) <= TOL16
     # isolation: each beam sees its parent's history plus its own new token
     g0 = 0
     for b in range(W):
@@ -981,9 +1055,8 @@ def test_workload5_grouped_step_full_size(parts, hint):
     assert pkv.device_status() == 0
     oracle.kv_write(kh, vh, case.new_key, case.new_value, slots, B)
     assert torch.equal(bits(kc), bits(kh)) and torch.equal(bits(vc), bits(vh))
-    idx = pick(cl.tolist())
-    ref = sampled_oracle(case.q, kh, vh, bt, cl, w, idx)
-    assert max_err(out[idx], ref) <= TOL16
+    ref = full_oracle(case.q, kh, vh, bt, cl, w)
+    assert max_err(out, ref) <= TOL16
     assert bool(torch.isfinite(out).all())
 
 
