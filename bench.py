@@ -1026,13 +1026,21 @@ def run_sampling(args):
         del kc, vc
 
 
+# NVIDIA's published NVLink-C2C bandwidth of the Grace-Blackwell superchip:
+# 900 GB/s bidirectional, 450 GB/s each way (context: the box's measured
+# copy-engine rate is the achievable reference)
+C2C_NOMINAL_GBS_PER_DIRECTION = 450.0
+
+
 def run_swap(args):
     """Preemption by swapping: move every block of 64 sequences x 2048 tokens
     (bf16, 8 KV heads x 128) from the device cache to a pinned host pool and
     back with kv_swap_blocks, block pairs shuffled on both sides, for block
-    sizes 8 / 16 / 32.  Reference: a plain copy of the same bytes between one
-    contiguous device buffer and one pinned host buffer (torch copy_, the copy
-    engines over NVLink-C2C)."""
+    sizes 8 / 16 / 32; then both directions at once (half the blocks out
+    while the other half comes in, two streams).  Reference: a plain copy of
+    the same bytes between one contiguous device buffer and one pinned host
+    buffer (torch copy_, the copy engines over NVLink-C2C), one way and both
+    ways at once.  Fractions are also given of the nominal C2C rate."""
     import paged_kv_cache_312_gb300 as pkv
     import __graft_entry__
 
@@ -1041,6 +1049,7 @@ def run_swap(args):
     stream = torch.cuda.current_stream(dev)
     S, L, Hkv, D = 64, 2048, 8, 128
     total = S * L * Hkv * D * 2 * 2  # K and V, bf16
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def timed(fn, reps):
         for _ in range(3):
@@ -1055,12 +1064,34 @@ def run_swap(args):
         torch.cuda.synchronize(dev)
         return a.elapsed_time(b) / reps
 
+    def both(fn_out, fn_in):
+        """fn_out on stream s1 and fn_in on stream s2, started together; the
+        main stream waits for both."""
+        def run():
+            s1.wait_stream(stream)
+            s2.wait_stream(stream)
+            fn_out(s1)
+            fn_in(s2)
+            stream.wait_stream(s1)
+            stream.wait_stream(s2)
+        return run
+
     flat_d = torch.empty(total, dtype=torch.uint8, device=dev)
     flat_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    half = total // 2
     ref = {"out": total / (timed(lambda: flat_h.copy_(flat_d, non_blocking=True), 10) * 1e-3)
            / 1e9,
            "in": total / (timed(lambda: flat_d.copy_(flat_h, non_blocking=True), 10) * 1e-3)
            / 1e9}
+
+    def ce_out(sm):
+        with torch.cuda.stream(sm):
+            flat_h[:half].copy_(flat_d[:half], non_blocking=True)
+
+    def ce_in(sm):
+        with torch.cuda.stream(sm):
+            flat_d[half:].copy_(flat_h[half:], non_blocking=True)
+    ref["both"] = total / (timed(both(ce_out, ce_in), 10) * 1e-3) / 1e9
     del flat_d, flat_h
     rng = np.random.default_rng(args.seed)
     for B in (8, 16, 32):
@@ -1074,16 +1105,25 @@ def run_swap(args):
         in_pairs = pairs[:, [1, 0]].contiguous().to(dev)
         ms_out = timed(lambda: pkv.kv_swap_blocks(kh, vh, kd, vd, out_pairs, stream=stream), 10)
         ms_in = timed(lambda: pkv.kv_swap_blocks(kd, vd, kh, vh, in_pairs, stream=stream), 10)
+        # both ways at once: the first half of the pairs out, the second half in
+        h_out_pairs = out_pairs[:nb // 2].contiguous()
+        h_in_pairs = in_pairs[nb // 2:].contiguous()
+        ms_both = timed(both(
+            lambda sm: pkv.kv_swap_blocks(kh, vh, kd, vd, h_out_pairs, stream=sm),
+            lambda sm: pkv.kv_swap_blocks(kd, vd, kh, vh, h_in_pairs, stream=sm)), 10)
         assert pkv.device_status() == 0
-        for direction, ms in (("out (device -> pinned host)", ms_out),
-                              ("in (pinned host -> device)", ms_in)):
+        for key, direction, ms in (("out", "out (device -> pinned host)", ms_out),
+                                   ("in", "in (pinned host -> device)", ms_in),
+                                   ("both", "both at once (half the blocks each way)", ms_both)):
             gbs = total / (ms * 1e-3) / 1e9
-            key = "out" if direction.startswith("out") else "in"
+            nominal = C2C_NOMINAL_GBS_PER_DIRECTION * (2 if key == "both" else 1)
             print(json.dumps({"swap": {"block_size": B, "direction": direction,
                                        "blocks": nb, "block_bytes": Hkv * B * D * 2 * 2},
                               "bytes": total, "ms": round(ms, 4), "gbs": round(gbs, 1),
                               "reference_copy_gbs": round(ref[key], 1),
-                              "frac_of_reference": round(gbs / ref[key], 3)}), flush=True)
+                              "frac_of_reference": round(gbs / ref[key], 3),
+                              "c2c_nominal_gbs": nominal,
+                              "frac_of_c2c_nominal": round(gbs / nominal, 3)}), flush=True)
         del kd, vd, kh, vh
 
 

@@ -5,6 +5,8 @@
 // sequence sits in its logical block i / B at offset i % B (aiplusplus
 // PagedAttention page, "core idea" 1-3).
 #include <cuda_bf16.h>
+#include <algorithm>
+#include <climits>
 #include <cuda_fp16.h>
 
 #include "pkv.h"
@@ -121,45 +123,51 @@ __global__ void copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restric
 // kv_swap_blocks: whole blocks from one pool to another, e.g. the device cache
 // and a pinned host swap pool that the GPU reaches directly over NVLink-C2C
 // (aiplusplus page, section 4, and the cayang0802 walkthrough: a preempted
-// sequence's KV blocks are swapped out to CPU memory and back).  Each thread
-// keeps four 16-byte loads of K and four of V in flight before storing.
+// sequence's KV blocks are swapped out to CPU memory and back).  The work is
+// cut into units of (pair, chunk of kSwapThreads * kSwapUnroll vectors); a
+// grid of at most two CTAs per SM strides over them, so that a swap out and a
+// swap in launched on two streams run side by side and use both directions
+// of the link.  Each thread keeps four 16-byte loads of K and four of V in
+// flight before storing.
 // ---------------------------------------------------------------------------
 constexpr int kSwapThreads = 256;
 constexpr int kSwapUnroll = 4;
+constexpr int kSwapCtasPerSm = 2;
 
 __global__ void __launch_bounds__(kSwapThreads)
 swap_blocks_kernel(uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
                    const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
-                   const int64_t* __restrict__ pairs, int num_src_blocks, int num_dst_blocks,
-                   size_t vec_per_block, unsigned int* status)
+                   const int64_t* __restrict__ pairs, int num_pairs, int num_src_blocks,
+                   int num_dst_blocks, size_t vec_per_block, int chunks, unsigned int* status)
 {
-    const int64_t src = pairs[2 * blockIdx.x], dst = pairs[2 * blockIdx.x + 1];
-    if (src < 0 || src >= num_src_blocks || dst < 0 || dst >= num_dst_blocks) {
-        if (blockIdx.y == 0 && threadIdx.x == 0) flag(status, PKV_STATUS_BAD_PAIR);
-        return;
-    }
-    const uint4* ks = src_k + (size_t)src * vec_per_block;
-    const uint4* vs = src_v + (size_t)src * vec_per_block;
-    uint4* kd = dst_k + (size_t)dst * vec_per_block;
-    uint4* vd = dst_v + (size_t)dst * vec_per_block;
-    const size_t step = (size_t)gridDim.y * kSwapThreads * kSwapUnroll;
-    for (size_t i0 = ((size_t)blockIdx.y * kSwapUnroll) * kSwapThreads + threadIdx.x;
-         i0 < vec_per_block; i0 += step) {
+    const long long units = (long long)num_pairs * chunks;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+        const int pi = (int)(u / chunks), chunk = (int)(u - (long long)pi * chunks);
+        const int64_t src = pairs[2 * pi], dst = pairs[2 * pi + 1];
+        if (src < 0 || src >= num_src_blocks || dst < 0 || dst >= num_dst_blocks) {
+            if (chunk == 0 && threadIdx.x == 0) flag(status, PKV_STATUS_BAD_PAIR);
+            continue;
+        }
+        const uint4* ks = src_k + (size_t)src * vec_per_block;
+        const uint4* vs = src_v + (size_t)src * vec_per_block;
+        uint4* kd = dst_k + (size_t)dst * vec_per_block;
+        uint4* vd = dst_v + (size_t)dst * vec_per_block;
+        const size_t i0 = (size_t)chunk * kSwapUnroll * kSwapThreads + threadIdx.x;
         uint4 a[kSwapUnroll], b[kSwapUnroll];
 #pragma unroll
-        for (int u = 0; u < kSwapUnroll; ++u) {
-            const size_t i = i0 + (size_t)u * kSwapThreads;
+        for (int k = 0; k < kSwapUnroll; ++k) {
+            const size_t i = i0 + (size_t)k * kSwapThreads;
             if (i < vec_per_block) {
-                a[u] = ks[i];
-                b[u] = vs[i];
+                a[k] = ks[i];
+                b[k] = vs[i];
             }
         }
 #pragma unroll
-        for (int u = 0; u < kSwapUnroll; ++u) {
-            const size_t i = i0 + (size_t)u * kSwapThreads;
+        for (int k = 0; k < kSwapUnroll; ++k) {
+            const size_t i = i0 + (size_t)k * kSwapThreads;
             if (i < vec_per_block) {
-                kd[i] = a[u];
-                vd[i] = b[u];
+                kd[i] = a[k];
+                vd[i] = b[k];
             }
         }
     }
@@ -592,13 +600,19 @@ cudaError_t launch_kv_swap_blocks(void* dst_k, void* dst_v, const void* src_k, c
                                   cudaStream_t stream)
 {
     const size_t vec = block_bytes / 16;
-    size_t chunks = (vec + kSwapThreads * kSwapUnroll - 1) / (kSwapThreads * kSwapUnroll);
-    if (chunks < 1) chunks = 1;
-    if (chunks > 65535) chunks = 65535;
-    dim3 grid(num_pairs, (unsigned)chunks);
-    swap_blocks_kernel<<<grid, kSwapThreads, 0, stream>>>(
+    const size_t per_unit = (size_t)kSwapThreads * kSwapUnroll;
+    const size_t chunks = (vec + per_unit - 1) / per_unit;
+    if (chunks > (size_t)INT_MAX) return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long units = (long long)num_pairs * (long long)chunks;
+    const long long grid = std::min<long long>(units, (long long)kSwapCtasPerSm * sms);
+    swap_blocks_kernel<<<(unsigned)grid, kSwapThreads, 0, stream>>>(
         static_cast<uint4*>(dst_k), static_cast<uint4*>(dst_v), static_cast<const uint4*>(src_k),
-        static_cast<const uint4*>(src_v), pairs, num_src_blocks, num_dst_blocks, vec, status);
+        static_cast<const uint4*>(src_v), pairs, num_pairs, num_src_blocks, num_dst_blocks, vec,
+        (int)chunks, status);
     return cudaGetLastError();
 }
 
