@@ -57,7 +57,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 struct MapEntry {
     const void* ptr = nullptr;
     uint64_t rows = 0;
-    int D = 0, B = 0, dtype = -1, halves = 0;
+    int D = 0, box_rows = 0, dtype = -1, halves = 0;
     CUtensorMap map;
 };
 
@@ -80,17 +80,17 @@ int get_encoder()
 }
 
 // A cache viewed as [rows][D] bf16/fp16, loaded in boxes of 64 columns x
-// min(B, 16) rows with the 128-byte swizzle.  halves = 0: a 2-D map, one box
+// box_rows rows with the 128-byte swizzle.  halves = 0: a 2-D map, one box
 // per 64-column half.  halves = 1: a 3-D map whose outermost dimension steps
 // over the 64-column halves (stride 128 bytes), so that one box brings every
-// half of min(B, 16) rows, laid out half after half in shared memory.
-int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtensorMap* out,
+// half of box_rows rows, laid out half after half in shared memory.
+int tensor_map(const void* cache, uint64_t rows, int D, int box_rows, int dtype, CUtensorMap* out,
                int halves = 0)
 {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (const MapEntry& m : g_maps) {
-        if (m.ptr == cache && m.rows == rows && m.D == D && m.B == B && m.dtype == dtype &&
-            m.halves == halves) {
+        if (m.ptr == cache && m.rows == rows && m.D == D && m.box_rows == box_rows &&
+            m.dtype == dtype && m.halves == halves) {
             *out = m.map;
             return PKV_OK;
         }
@@ -99,10 +99,9 @@ int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtens
     if (rc != PKV_OK) return rc;
     MapEntry& m = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % 16;
-    const cuuint32_t box_rows = (cuuint32_t)(B < 16 ? B : 16);
     cuuint64_t dims[3] = {(cuuint64_t)(halves ? 64 : D), (cuuint64_t)rows, (cuuint64_t)(D / 64)};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
-    cuuint32_t box[3] = {64, box_rows, (cuuint32_t)(D / 64)};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)(D / 64)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(&m.map,
                           dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -117,7 +116,7 @@ int tensor_map(const void* cache, uint64_t rows, int D, int B, int dtype, CUtens
     m.ptr = cache;
     m.rows = rows;
     m.D = D;
-    m.B = B;
+    m.box_rows = box_rows;
     m.dtype = dtype;
     m.halves = halves;
     *out = m.map;
@@ -322,8 +321,10 @@ int pkv_paged_prefill_attention(void* out, const void* q, const void* k_cache, c
     if (!p.status) return pkv_fail(PKV_ERR_CUDA, "%s: no device status word", fn);
     CUtensorMap kmap, vmap;
     const uint64_t rows = (uint64_t)num_blocks * num_kv_heads * block_size;
-    int rc = tensor_map(k_cache, rows, head_dim, block_size, kv_dtype, &kmap);
-    if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap);
+    // the prefill kernel's boxes are 16-token groups (or one block of 8)
+    const int box_rows = block_size < 16 ? block_size : 16;
+    int rc = tensor_map(k_cache, rows, head_dim, box_rows, kv_dtype, &kmap);
+    if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, box_rows, kv_dtype, &vmap);
     if (rc != PKV_OK) return rc;
     cudaError_t e =
         g_prefill_kernel == PKV_PREFILL_WARP_MMA
@@ -510,8 +511,9 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
     if (tensor_core) {
         CUtensorMap kmap, vmap;
         const uint64_t rows = (uint64_t)num_blocks * num_kv_heads * block_size;
-        int rc = tensor_map(k_cache, rows, head_dim, block_size, kv_dtype, &kmap, 1);
-        if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, block_size, kv_dtype, &vmap, 1);
+        const int box_rows = decode_box_rows(head_dim, block_size, grouped);
+        int rc = tensor_map(k_cache, rows, head_dim, box_rows, kv_dtype, &kmap, 1);
+        if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, box_rows, kv_dtype, &vmap, 1);
         if (rc != PKV_OK) return rc;
         if (grouped) {
             // one CTA per (beam group, KV head, part); each writes the new
@@ -537,9 +539,10 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
             if (e != cudaSuccess) return cuda_fail(e, fn);
             return PKV_OK;
         }
-        // grid: every (sequence, KV head, partition group) slot, the groups of
-        // one (sequence, KV head) adjacent; slots past a sequence's end exit at
-        // once.  Short partitions of long contexts go one per warp, four to a
+        // grid: every (sequence, KV head, partition group, head slice) slot, the
+        // groups of one (sequence, KV head) adjacent and the slices of one
+        // group next to each other; slots past a sequence's end exit at once
+        // (with a work plan, the CTAs with work take its records instead).  Short partitions of long contexts go one per warp, four to a
         // CTA (with few partitions per sequence, a CTA would leave warps idle).
         if (p.partition_tokens <= kWarpPartitionMaxTokens &&
             p.max_partitions >= kWarpPartitionMinCount)

@@ -138,12 +138,17 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
     // records it still reads are written only once it has completed.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = tid; i < pp.num_counters; i += kPlanThreads) pp.done[i] = 0u;
+    // a sequence's records: KV head, then partition group, then head slice
+    // (the slices of one group adjacent: their reads of a K/V tile meet in L2)
+    const int HS = pp.head_slices;
     for (int r = tid; r < S; r += kPlanThreads) {
         const int s = sorted[r], L = lens[s];
         const int ng = groups_of(L);
         int4* out = pp.items + off[r];
-        for (int gh = 0; gh < per_seq; ++gh)
-            for (int grp = 0; grp < ng; ++grp) out[gh * ng + grp] = make_int4(s, L, gh, grp);
+        for (int g = 0; g < pp.num_kv_heads; ++g)
+            for (int grp = 0; grp < ng; ++grp)
+                for (int hs = 0; hs < HS; ++hs)
+                    out[(g * ng + grp) * HS + hs] = make_int4(s, L, g * HS + hs, grp);
     }
     if (tid == 0) *pp.item_count = run;
 }

@@ -69,14 +69,15 @@ using namespace pkv_tc;
 
 // ---- compile-time geometry -----------------------------------------------------
 
-template <int D, int B, int NW, int NS, int NT = 1>
+template <int D, int B, int NW, int NS, int NT = 1, int TPS = 1>
 struct Geometry {
     static constexpr int NC = 8 * NT;                // query-head columns (n8 tiles x 8)
-    static constexpr int ROWS = B < 16 ? B : 16;     // rows per TMA box
-    static constexpr int IDS = 16 / ROWS;            // physical blocks per 16-token stage
+    static constexpr int ST = 16 * TPS;              // tokens per stage: TPS m16 token tiles
+    static constexpr int ROWS = B < ST ? B : ST;     // rows per TMA box
+    static constexpr int IDS = ST / ROWS;            // physical blocks per stage
     static constexpr int NH = D / 64;                // 128-byte column halves
     static constexpr int SUB_BYTES = ROWS * 128;     // one box
-    static constexpr int KV_BYTES = 16 * D * 2;      // K (or V) of a 16-token stage
+    static constexpr int KV_BYTES = ST * D * 2;      // K (or V) of a stage
     static constexpr int STAGE_BYTES = 2 * KV_BYTES;
     static constexpr int RING_BYTES = NS * STAGE_BYTES;
     static constexpr int MERGE_BYTES = NW * NC * (D + 2) * 4;
@@ -84,21 +85,23 @@ struct Geometry {
         NW * RING_BYTES > MERGE_BYTES ? NW * RING_BYTES : MERGE_BYTES;  // merge reuses rings
     static constexpr int BAR_OFF = DATA_BYTES;
     static constexpr int SID_OFF = BAR_OFF + NW * NS * 8;
-    // per ring slot: block ids of the stage (2), and for beam groups its first
-    // token, region end and member (3)
+    // per ring slot: block ids of the stage (IDS <= 4), and for beam groups its
+    // first token, region end and member
     static constexpr int SID_INTS = 8;
+    static constexpr int SID_TOK = 4, SID_END = 5, SID_MEM = 6;
+    static_assert(IDS <= SID_TOK, "block ids of a stage fit the slot record");
     static constexpr int GM_OFF = SID_OFF + NW * NS * SID_INTS * 4;  // beam groups: [NC] lengths
     static constexpr int SMEM_BYTES = 1024 /*align slack*/ + GM_OFF + NC * 4;
     // partition weights cached for the in-kernel merge (after the warp merge)
     static constexpr int WCACHE = ((DATA_BYTES - MERGE_BYTES) / 4 - 2 * NC - NW * 32 * 4 - 4) & ~3;
     static_assert(WCACHE > 0, "room for merge weights");
     // CTAs per SM the register allocation is held to: as many as the shared
-    // memory admits (D = 128: 3 of ~66 KB, up to 168 registers a thread;
-    // D = 64: 6 of ~34 KB, 80 registers), or 5 for two column tiles at D = 64
-    // (96).  Left to itself the compiler took 96 registers at D = 128, and the
-    // freedom to use more is worth 1-4 % of HBM bandwidth there; at D = 64 it
-    // spilled.
-    static constexpr int MIN_CTAS = D == 128 ? 3 : (NT == 1 ? 6 : 5);
+    // memory admits (8 KB stages -- D = 128, or D = 64 with 32-token stages --
+    // 3 of ~66 KB, up to 168 registers a thread; 4 KB stages: 6 of ~34 KB, 80
+    // registers), or 5 for two column tiles with 4 KB stages (96).  Left to
+    // itself the compiler took 96 registers at D = 128, and the freedom to use
+    // more is worth 1-4 % of HBM bandwidth there; with 4 KB stages it spilled.
+    static constexpr int MIN_CTAS = KV_BYTES >= 4096 ? 3 : (NT == 1 ? 6 : 5);
     static_assert(SUB_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
     static_assert(STAGE_BYTES % 1024 == 0 && RING_BYTES % 1024 == 0, "stage alignment");
 };
@@ -106,28 +109,31 @@ struct Geometry {
 // Shared-memory offset of (token row r of the stage, 16-byte chunk c of the
 // head_dim row) in a K or V stage buffer laid out [block][half][row][128 B],
 // honouring the 128-byte swizzle (chunk XOR row % 8).
-template <int D, int B, int NW, int NS>
+template <class Gm>
 __device__ __forceinline__ uint32_t stage_offset(int r, int c)
 {
-    using Gm = Geometry<D, B, NW, NS>;
     const int u = r / Gm::ROWS, row = r % Gm::ROWS;
     const int half = c >> 3, cc = c & 7;
     return (u * Gm::NH + half) * Gm::SUB_BYTES + row * 128 + ((cc ^ (row & 7)) << 4);
 }
 
 // One CTA = one work item: one partition of one (sequence, KV head, head
-// slice), or one run of a beam group's stage list, whose 16-token stages the
-// NW warps stream in turn (warp w takes stages w, w + NW, ...) through rings
-// of NS stages each, merging their softmax states at the end; or, for short
-// split partitions, up to NW consecutive partitions, one per warp, each
-// warp's state being its partition's result.  NT n8 tiles carry up to 8 * NT
-// query-head columns.
-template <typename T, int D, int B, int NW, int NS, bool GR, int NT>
-__global__ void __launch_bounds__(NW * 32, (Geometry<D, B, NW, NS, NT>::MIN_CTAS))
+// slice), or one run of a beam group's stage list, whose stages of 16 * TPS
+// tokens the NW warps stream in turn (warp w takes stages w, w + NW, ...)
+// through rings of NS stages each, merging their softmax states at the end;
+// or, for short split partitions, up to NW consecutive partitions, one per
+// warp, each warp's state being its partition's result.  NT n8 tiles carry up
+// to 8 * NT query-head columns.  A stage of TPS = 2 (head_dim 64: 8 KB, as a
+// 16-token stage at head_dim 128) is two m16 token tiles, taken one after the
+// other against the same running softmax state.
+template <typename T, int D, int B, int NW, int NS, bool GR, int NT, int TPS>
+__global__ void __launch_bounds__(NW * 32, (Geometry<D, B, NW, NS, NT, TPS>::MIN_CTAS))
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap)
 {
-    using Gm = Geometry<D, B, NW, NS, NT>;
+    using Gm = Geometry<D, B, NW, NS, NT, TPS>;
+    static_assert(!GR || TPS == 1, "beam groups stream 16-token stages");
+    constexpr int ST = Gm::ST;      // tokens per stage
     constexpr int NC = Gm::NC;      // query-head columns of the mma's N (8 per tile)
     constexpr int KSTEPS = D / 16;  // Q K^T k-steps
     constexpr int MTILES = D / 16;  // P V m-tiles (head_dim rows)
@@ -203,9 +209,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         end = 0;
     } else {
         // ---- which item: with a work plan, record b = (s, L, g * HS + hs,
-        // grp); else slot b = (((s * Hkv) + g) * HS + hs) * max_groups + grp.
+        // grp); else slot b = (((s * Hkv) + g) * max_groups + grp) * HS + hs.
         // Group grp holds partitions grp * cta_parts .. + cta_parts - 1 of
-        // (s, g), for head slice hs of the KV group's query heads.
+        // (s, g), for head slice hs of the KV group's query heads; the head
+        // slices of one group are adjacent, so that their reads of the same
+        // K/V tiles meet in L2.
         const int HS = p.head_slices;
         int grp, plan_len = 0;
         if (p.items != nullptr) {
@@ -224,8 +232,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             grp = it.w;
         } else {
             const int max_groups = (p.max_partitions + p.cta_parts - 1) / p.cta_parts;
-            grp = blockIdx.x % max_groups;
-            sg = blockIdx.x / max_groups;
+            const int hs_b = blockIdx.x % HS, t = blockIdx.x / HS;
+            grp = t % max_groups;
+            sg = (t / max_groups) * HS + hs_b;
         }
         const int sgk = sg / HS, hs = sg - sgk * HS;
         s = sgk / p.num_kv_heads;
@@ -242,7 +251,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             spec_solo = p.cta_parts == 1;
             const int gpart = grp * p.cta_parts + (spec_solo ? 0 : warp);
             const int64_t gtok = (int64_t)gpart * p.partition_tokens +
-                                 (spec_solo ? warp + lane * NW : lane) * 16;
+                                 (spec_solo ? warp + lane * NW : lane) * ST;
             const int32_t* row = p.block_tables + (size_t)s * p.max_blocks;
 #pragma unroll
             for (int u = 0; u < IDS; ++u) {
@@ -268,7 +277,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         part = solo ? p0 : p0 + warp;
         begin = part * p.partition_tokens;
         end = min(L, begin + p.partition_tokens);
-        nst = end > begin ? (end - begin + 15) / 16 : 0;
+        nst = end > begin ? (end - begin + ST - 1) / ST : 0;
     }
     // GR: CTA stage q -> first token, end of its region, member (-1: shared)
     auto stage_at = [&](int q, int& tok0, int& endr, int& mem) {
@@ -320,7 +329,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     auto load_window = [&](int jbase) {
         win_base = jbase;
         const int j = jbase + lane;
-        int tk0 = begin + (wsub + j * wpp) * 16, endr = end, mem = -1;
+        int tk0 = begin + (wsub + j * wpp) * ST, endr = end, mem = -1;
         if constexpr (GR) {
             if (j < cnt) stage_at(qbase + warp + j * NW, tk0, endr, mem);
             win_tok = tk0;
@@ -347,7 +356,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         int ids[IDS];
 #pragma unroll
         for (int u = 0; u < IDS; ++u) ids[u] = __shfl_sync(0xffffffffu, win_ids[u], j - win_base);
-        int tok0 = begin + (wsub + j * wpp) * 16;
+        int tok0 = begin + (wsub + j * wpp) * ST;
         int endr = end, mem = -1;
         if constexpr (GR) {
             tok0 = __shfl_sync(0xffffffffu, win_tok, j - win_base);
@@ -357,12 +366,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         if (lane == 0) {
             const int slot = j % NS;
             int* sd = sid + (warp * NS + slot) * Gm::SID_INTS;
-            sd[0] = ids[0];
-            sd[1] = ids[IDS - 1];
+#pragma unroll
+            for (int u = 0; u < IDS; ++u) sd[u] = ids[u];
             if constexpr (GR) {
-                sd[2] = tok0;
-                sd[3] = endr;
-                sd[4] = mem;
+                sd[Gm::SID_TOK] = tok0;
+                sd[Gm::SID_END] = endr;
+                sd[Gm::SID_MEM] = mem;
             }
             const uint32_t bar = smem_u32(&bars[warp * NS + slot]);
             const uint32_t kdst = smem_u32(ring + slot * Gm::STAGE_BYTES);
@@ -425,7 +434,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                     append(s0 + m, lm, table_of(m));
                 qb0 += (lm - shared + 15) / 16;
             }
-        } else if (L > 0 && begin <= L - 1 && L - 1 < end && ((L - 1 - begin) / 16) % wpp == wsub) {
+        } else if (L > 0 && begin <= L - 1 && L - 1 < end && ((L - 1 - begin) / ST) % wpp == wsub) {
             append(s, L, table);
         }
     }
@@ -484,129 +493,136 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             break;
         }
         const int* sinfo = sid + (warp * NS + slot) * Gm::SID_INTS;
-        const int id0 = sinfo[0];
-        const int id1 = sinfo[1];
         const uint32_t kbase = smem_u32(ring + slot * Gm::STAGE_BYTES);
         const uint32_t vbase = kbase + Gm::KV_BYTES;
-        const int tok0 = GR ? sinfo[2] : begin + (wsub + j * wpp) * 16;
-        const int endr = GR ? sinfo[3] : end;
+        const int tok0 = GR ? sinfo[Gm::SID_TOK] : begin + (wsub + j * wpp) * ST;
+        const int endr = GR ? sinfo[Gm::SID_END] : end;
+        // row r of the stage: token tok0 + r of block sinfo[r / B] (one block
+        // when a box holds the whole stage)
         auto valid = [&](int r) {
-            return tok0 + r < endr && ((IDS > 1 && r >= B) ? id1 : id0) >= 0;
+            return tok0 + r < endr && sinfo[IDS > 1 ? r / B : 0] >= 0;
         };
-        const bool all_valid = tok0 + 16 <= endr && id0 >= 0 && id1 >= 0;
+        bool all_valid = tok0 + ST <= endr;
+#pragma unroll
+        for (int u = 0; u < IDS; ++u) all_valid = all_valid && sinfo[u] >= 0;
 
-        // ---- S^T = K Q^T  (16 tokens x 8 heads per tile); with one tile, as
-        // two independent accumulation chains (even and odd k-steps)
-        float sc[NT][4], sd[NT][4];
+        // the stage's m16 token tiles, one after the other
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
-            sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = sd[t][0] = sd[t][1] = sd[t][2] =
-                sd[t][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-            uint32_t a[4];
-            ldsm_x4(kbase + stage_offset<D, B, NW, NS>(k_row, 2 * kk + k_chunk_add), a);
-#pragma unroll
+        for (int hf = 0; hf < TPS; ++hf) {
+            const int r0 = 16 * hf;
+            // ---- S^T = K Q^T  (16 tokens x 8 heads per tile); with one tile, as
+            // two independent accumulation chains (even and odd k-steps)
+            float sc[NT][4], sd[NT][4];
+    #pragma unroll
+            for (int t = 0; t < NT; ++t)
+                sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = sd[t][0] = sd[t][1] = sd[t][2] =
+                    sd[t][3] = 0.f;
+    #pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                uint32_t a[4];
+                ldsm_x4(kbase + stage_offset<Gm>(r0 + k_row, 2 * kk + k_chunk_add), a);
+    #pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if (NT == 1 && (kk & 1))
+                        Mma<T>::run(sd[t], a, qb[t][kk][0], qb[t][kk][1]);
+                    else
+                        Mma<T>::run(sc[t], a, qb[t][kk][0], qb[t][kk][1]);
+                }
+            }
+            // x[t][0..3]: (token gq, column 8t+2tq), (gq, +1), (gq+8, 8t+2tq), (gq+8, +1)
+            float x[NT][4];
+            const bool vg = all_valid || valid(r0 + gq), vg8 = all_valid || valid(r0 + gq + 8);
+    #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                if (NT == 1 && (kk & 1))
-                    Mma<T>::run(sd[t], a, qb[t][kk][0], qb[t][kk][1]);
-                else
-                    Mma<T>::run(sc[t], a, qb[t][kk][0], qb[t][kk][1]);
-            }
-        }
-        // x[t][0..3]: (token gq, column 8t+2tq), (gq, +1), (gq+8, 8t+2tq), (gq+8, +1)
-        float x[NT][4];
-        const bool vg = all_valid || valid(gq), vg8 = all_valid || valid(gq + 8);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[t][e] = (sc[t][e] + sd[t][e]) * sl;
-            if (!vg) x[t][0] = x[t][1] = -INFINITY;
-            if (!vg8) x[t][2] = x[t][3] = -INFINITY;
-            if constexpr (GR) {
-                // a member's own tail: the other members' columns see nothing
-                const int mem = sinfo[4];
-                if (mem >= 0) {
-                    if ((8 * t + 2 * tq) / G != mem) x[t][0] = x[t][2] = -INFINITY;
-                    if ((8 * t + 2 * tq + 1) / G != mem) x[t][1] = x[t][3] = -INFINITY;
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) x[t][e] = (sc[t][e] + sd[t][e]) * sl;
+                if (!vg) x[t][0] = x[t][1] = -INFINITY;
+                if (!vg8) x[t][2] = x[t][3] = -INFINITY;
+                if constexpr (GR) {
+                    // a member's own tail: the other members' columns see nothing
+                    const int mem = sinfo[Gm::SID_MEM];
+                    if (mem >= 0) {
+                        if ((8 * t + 2 * tq) / G != mem) x[t][0] = x[t][2] = -INFINITY;
+                        if ((8 * t + 2 * tq + 1) / G != mem) x[t][1] = x[t][3] = -INFINITY;
+                    }
                 }
             }
-        }
-        // ---- online softmax in base 2 against a reference max per head that
-        // moves only when a score passes it by more than 8 (so p <= 2^8): most
-        // stages need neither the max over the 8 row groups nor a rescale of O
-        bool up = false;
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-            up = up || fmaxf(x[t][0], x[t][2]) > mr[t][0] + 8.f ||
-                 fmaxf(x[t][1], x[t][3]) > mr[t][1] + 8.f;
-        if (__any_sync(0xffffffffu, up)) {
-#pragma unroll
+            // ---- online softmax in base 2 against a reference max per head that
+            // moves only when a score passes it by more than 8 (so p <= 2^8): most
+            // stages need neither the max over the 8 row groups nor a rescale of O
+            bool up = false;
+    #pragma unroll
+            for (int t = 0; t < NT; ++t)
+                up = up || fmaxf(x[t][0], x[t][2]) > mr[t][0] + 8.f ||
+                     fmaxf(x[t][1], x[t][3]) > mr[t][1] + 8.f;
+            if (__any_sync(0xffffffffu, up)) {
+    #pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    float mx0 = fmaxf(x[t][0], x[t][2]), mx1 = fmaxf(x[t][1], x[t][3]);
+    #pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                    }
+                    const float mn0 = fmaxf(mr[t][0], mx0), mn1 = fmaxf(mr[t][1], mx1);
+                    // 0 while m is -inf (nothing accumulated yet), 1 if m stays
+                    const float al0 = mn0 == -INFINITY ? 1.f : ex2(mr[t][0] - mn0);
+                    const float al1 = mn1 == -INFINITY ? 1.f : ex2(mr[t][1] - mn1);
+                    mr[t][0] = mn0;
+                    mr[t][1] = mn1;
+                    lr_[t][0] *= al0;
+                    lr_[t][1] *= al1;
+    #pragma unroll
+                    for (int i = 0; i < MTILES; ++i) {
+                        acc[t][i][0] *= al0;
+                        acc[t][i][1] *= al1;
+                        acc[t][i][2] *= al0;
+                        acc[t][i][3] *= al1;
+                    }
+                }
+            }
+            // ---- P^T operand (tokens 2tq.. x head gq) via an in-register transpose
+            uint32_t bh0[NT], bh1[NT], bl0[NT], bl1[NT];
+    #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                float mx0 = fmaxf(x[t][0], x[t][2]), mx1 = fmaxf(x[t][1], x[t][3]);
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-                }
-                const float mn0 = fmaxf(mr[t][0], mx0), mn1 = fmaxf(mr[t][1], mx1);
-                // 0 while m is -inf (nothing accumulated yet), 1 if m stays
-                const float al0 = mn0 == -INFINITY ? 1.f : ex2(mr[t][0] - mn0);
-                const float al1 = mn1 == -INFINITY ? 1.f : ex2(mr[t][1] - mn1);
-                mr[t][0] = mn0;
-                mr[t][1] = mn1;
-                lr_[t][0] *= al0;
-                lr_[t][1] *= al1;
-#pragma unroll
-                for (int i = 0; i < MTILES; ++i) {
-                    acc[t][i][0] *= al0;
-                    acc[t][i][1] *= al1;
-                    acc[t][i][2] *= al0;
-                    acc[t][i][3] *= al1;
-                }
+                const float ms0 = mr[t][0] == -INFINITY ? 0.f : mr[t][0];
+                const float ms1 = mr[t][1] == -INFINITY ? 0.f : mr[t][1];
+                const float p0 = ex2(x[t][0] - ms0), p1 = ex2(x[t][1] - ms1);
+                const float p2 = ex2(x[t][2] - ms0), p3 = ex2(x[t][3] - ms1);
+                lr_[t][0] += p0 + p2;
+                lr_[t][1] += p1 + p3;
+                uint32_t h01, l01, h23, l23;
+                Mma<T>::split(p0, p1, h01, l01);
+                Mma<T>::split(p2, p3, h23, l23);
+                bh0[t] = movmatrix_trans(h01);
+                bh1[t] = movmatrix_trans(h23);
+                bl0[t] = movmatrix_trans(l01);
+                bl1[t] = movmatrix_trans(l23);
             }
-        }
-        // ---- P^T operand (tokens 2tq.. x head gq) via an in-register transpose
-        uint32_t bh0[NT], bh1[NT], bl0[NT], bl1[NT];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const float ms0 = mr[t][0] == -INFINITY ? 0.f : mr[t][0];
-            const float ms1 = mr[t][1] == -INFINITY ? 0.f : mr[t][1];
-            const float p0 = ex2(x[t][0] - ms0), p1 = ex2(x[t][1] - ms1);
-            const float p2 = ex2(x[t][2] - ms0), p3 = ex2(x[t][3] - ms1);
-            lr_[t][0] += p0 + p2;
-            lr_[t][1] += p1 + p3;
-            uint32_t h01, l01, h23, l23;
-            Mma<T>::split(p0, p1, h01, l01);
-            Mma<T>::split(p2, p3, h23, l23);
-            bh0[t] = movmatrix_trans(h01);
-            bh1[t] = movmatrix_trans(h23);
-            bl0[t] = movmatrix_trans(l01);
-            bl1[t] = movmatrix_trans(l23);
-        }
 
-        bool v0 = true, v1 = true, v8 = true, v9 = true;
-        if (!all_valid) {
-            v0 = valid(2 * tq);
-            v1 = valid(2 * tq + 1);
-            v8 = valid(2 * tq + 8);
-            v9 = valid(2 * tq + 9);
-        }
-        // ---- O^T += V^T P^T
-#pragma unroll
-        for (int i = 0; i < MTILES; ++i) {
-            uint32_t a[4];
-            ldsm_x4_trans(vbase + stage_offset<D, B, NW, NS>(v_row, 2 * i + v_chunk_add), a);
+            bool v0 = true, v1 = true, v8 = true, v9 = true;
             if (!all_valid) {
-                a[0] = mask_pair(a[0], v0, v1);
-                a[1] = mask_pair(a[1], v0, v1);
-                a[2] = mask_pair(a[2], v8, v9);
-                a[3] = mask_pair(a[3], v8, v9);
+                v0 = valid(r0 + 2 * tq);
+                v1 = valid(r0 + 2 * tq + 1);
+                v8 = valid(r0 + 2 * tq + 8);
+                v9 = valid(r0 + 2 * tq + 9);
             }
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                Mma<T>::run(acc[t][i], a, bh0[t], bh1[t]);
-                Mma<T>::run(acc[t][i], a, bl0[t], bl1[t]);
+            // ---- O^T += V^T P^T
+    #pragma unroll
+            for (int i = 0; i < MTILES; ++i) {
+                uint32_t a[4];
+                ldsm_x4_trans(vbase + stage_offset<Gm>(r0 + v_row, 2 * i + v_chunk_add), a);
+                if (!all_valid) {
+                    a[0] = mask_pair(a[0], v0, v1);
+                    a[1] = mask_pair(a[1], v0, v1);
+                    a[2] = mask_pair(a[2], v8, v9);
+                    a[3] = mask_pair(a[3], v8, v9);
+                }
+    #pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    Mma<T>::run(acc[t][i], a, bh0[t], bh1[t]);
+                    Mma<T>::run(acc[t][i], a, bl0[t], bl1[t]);
+                }
             }
         }
         __syncwarp();
@@ -817,11 +833,14 @@ template <typename T, int D, int B, bool GR, int NT>
 cudaError_t launch_tc(const DecodeParams& p, const void* kmap, const void* vmap, long long grid,
                       cudaStream_t stream)
 {
-    // 4 warps x 2-stage rings: 64 KB (D = 128) per CTA, three CTAs per SM,
-    // up to 192 KB of tile loads in flight per SM
+    // 4 warps x 2-stage rings of 8 KB stages (16 tokens at D = 128, 32 at
+    // D = 64; beam groups at D = 64 keep 16): 64 KB per CTA, three CTAs per
+    // SM, up to 192 KB of tile loads in flight per SM
     constexpr int NW = kDecodeTcWarps, NS = 2;
-    using Gm = Geometry<D, B, NW, NS, NT>;
-    auto kern = decode_tc_kernel<T, D, B, NW, NS, GR, NT>;
+    constexpr int TPS = decode_stage_tokens(D, GR) / 16;
+    using Gm = Geometry<D, B, NW, NS, NT, TPS>;
+    static_assert(Gm::ROWS == decode_box_rows(D, B, GR), "tensor map box = stage box");
+    auto kern = decode_tc_kernel<T, D, B, NW, NS, GR, NT, TPS>;
     // set on every launch: the attribute belongs to the current device's copy
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES);

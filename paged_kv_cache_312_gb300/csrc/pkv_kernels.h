@@ -122,9 +122,9 @@ cudaError_t launch_kv_swap_blocks(void* dst_k, void* dst_v, const void* src_k, c
 // CUDA-core decode (any dtype, any group size).  Grid: partitions x heads x seqs.
 cudaError_t launch_decode_cuda_core(const DecodeParams& p, int kv_dtype, cudaStream_t stream);
 
-// Tensor-core decode (16-bit KV), one CTA per (sequence, KV head, head
-// slice, group of p.cta_parts consecutive partitions), the groups of one
-// (sequence, KV head, head slice) adjacent in the grid; the grid is
+// Tensor-core decode (16-bit KV), one CTA per (sequence, KV head, group of
+// p.cta_parts consecutive partitions, head slice), in that order (the head
+// slices of one partition group adjacent in the grid); the grid is
 // S * Hkv * HS * ceil(max_partitions / cta_parts).  A CTA takes ceil(G / HS)
 // query heads as the mma's N columns: launch_decode_tensor_core up to 8
 // (one n8 tile), launch_decode_tensor_core_wide up to 16 (two tiles).  A CTA
@@ -141,6 +141,20 @@ constexpr int kDecodeTcWarps = 4;
 constexpr int kWarpPartitionMaxTokens = 512;
 constexpr int kWarpPartitionMinCount = 16;
 constexpr int kDecodeTcMaxColumns = 16;
+// Tokens per stage of the tensor-core decode kernel: 16 (one m16 token tile),
+// or 32 at head_dim 64 outside beam groups, so that a stage is 8 KB of K and V
+// at either head_dim.  The TMA boxes of its tensor maps hold
+// min(block_size, stage tokens) rows.
+constexpr int decode_stage_tokens(int head_dim, bool grouped)
+{
+    return head_dim == 64 && !grouped ? 32 : 16;
+}
+constexpr int decode_box_rows(int head_dim, int block_size, bool grouped)
+{
+    return block_size < decode_stage_tokens(head_dim, grouped)
+               ? block_size
+               : decode_stage_tokens(head_dim, grouped);
+}
 cudaError_t launch_decode_tensor_core(const DecodeParams& p, int kv_dtype, const void* k_map,
                                       const void* v_map, long long grid, cudaStream_t stream);
 cudaError_t launch_decode_tensor_core_wide(const DecodeParams& p, int kv_dtype, const void* k_map,

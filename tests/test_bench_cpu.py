@@ -46,7 +46,7 @@ def test_warmup_below_three_is_refused():
 @pytest.mark.parametrize("key", [2, 3, 4, 5])
 def test_launch_partition_rule(key):
     # a workload's own split if it names one; else one pass while every
-    # context fits in 2048 tokens, 1024-token partitions beyond
+    # context fits in 2048 tokens, 2048-token partitions beyond
     w = WORKLOADS[key]
     for max_blocks in (1, 2048 // w.block_size, 2048 // w.block_size + 1, 32768 // w.block_size):
         P = bench.launch_partition(w, max_blocks)
@@ -55,7 +55,7 @@ def test_launch_partition_rule(key):
         elif max_blocks * w.block_size <= 2048:
             assert P == 0
         else:
-            assert P == 1024
+            assert P == 2048
 
 
 def test_ragged_batches_run_unsplit_with_the_work_plan():

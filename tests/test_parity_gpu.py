@@ -195,17 +195,19 @@ def test_unsplit_work_plan_matches_oracle_and_the_unplanned_call(dt, Hq, Hkv, D,
 @pytest.mark.parametrize("D", [64, 128])
 def test_sweep_points(B, G, D):
     # every point of the block-size / GQA / head-dim sweep, at a small size
-    # and in its bench launch configuration (1024-token partitions)
+    # and in both launch configurations the sweep times: one pass per
+    # (sequence, KV head) and 2048-token partitions, each with the work plan
     import bench
     w = bench.sweep_workload(B, G, D)
-    case = make_decode_case(w, seed=B * 100 + G * 10 + D, lengths=[1, 700, 1500, 2100])
+    case = make_decode_case(w, seed=B * 100 + G * 10 + D, lengths=[1, 700, 2100, 1500, 4100])
     kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
-    P = bench.launch_partition(w, case.block_tables.shape[1])
-    out = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, B, 8, P=P)
     ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
                                         case.context_lens, w.scale, B, 8)
-    assert pkv.device_status() == 0
-    assert max_err(out, ref) <= TOL16
+    for P in (0, 2048):
+        out = gpu_decode(case.q, kc, vc, case.block_tables, case.context_lens, w.scale, B, 8,
+                         P=P, plan=True)
+        assert pkv.device_status() == 0
+        assert max_err(out, ref) <= TOL16, P
 
 
 def test_workload1_fp32():
