@@ -1104,3 +1104,118 @@ def test_beam_groups_empty_members_and_uncovered_sequences(parts):
     assert max_err(out[:covered], ref[:covered]) <= TOL16
     assert bool((out[0] == 0).all())
     assert bool((out[covered:] == 5.0).all())
+
+
+# --------------------------------------------------------------------------
+# The work plan itself, and the calls replayed from a CUDA graph
+# --------------------------------------------------------------------------
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("P", [0, 64, 512])
+def test_work_plan_records_cover_every_cta_once_longest_first(P):
+    # The plan's records (in the workspace, as include/pkv.h lays it out):
+    # one per CTA with work, each (sequence, KV head x head slice, partition
+    # group) exactly once, sequences in non-increasing order of length
+    # (counting-sort buckets are exact below 2048 tokens), the head slices of
+    # one group adjacent.
+    rng = np.random.default_rng(P + 5)
+    lengths = [int(x) for x in rng.permutation([0, 1, 17, 300, 700, 1500, 2000, 64, 65, 999])]
+    Hq, Hkv, D, B = 48, 2, 128, 16  # G = 24: two head slices of 12
+    w = Workload(0, "plan", "bf16", Hq, Hkv, D, B, len(lengths), "fixed")
+    case = make_decode_case(w, seed=3, lengths=lengths)
+    S = len(lengths)
+    maxb = case.block_tables.shape[1]
+    n = pkv.decode_workspace_bytes(S, Hq, D, maxb * B, P)
+    ws = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    out = torch.empty((S, Hq, D), dtype=torch.float32, device=DEV)
+    pkv.paged_decode_attention(out, case.q.to(DEV), case.k_cache.to(DEV), case.v_cache.to(DEV),
+                               case.block_tables.to(DEV), case.context_lens.to(DEV), w.scale, B,
+                               Hkv, partition_size=P, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    if P == 0:
+        count_off, items_off = 0, 256
+        groups = [1] * S
+    else:
+        nP = -(-maxb * B // P)
+        ml = _align256(S * Hq * 4)
+        o = ml + _align256(S * Hq * nP * 8)
+        count_off = o + _align256(S * Hq * nP * D * 4)
+        items_off = count_off + 256
+        cta_parts = 4 if (P <= 512 and nP >= 16) else 1
+        groups = [-(-max(1, -(-L // P)) // cta_parts) for L in lengths]
+    host = ws.cpu()
+    count = int(host[count_off:count_off + 4].view(torch.int32)[0])
+    HS = 2
+    assert count == sum(Hkv * HS * g for g in groups)
+    rec = host[items_off:items_off + count * 16].view(torch.int32).view(count, 4).tolist()
+    seen = set()
+    for s_, L, gh, grp in rec:
+        assert L == lengths[s_] and 0 <= gh < Hkv * HS and 0 <= grp < groups[s_]
+        seen.add((s_, gh, grp))
+    assert len(seen) == count
+    order = [r[0] for r in rec]
+    firsts = list(dict.fromkeys(order))  # sequences in plan order
+    assert sorted(firsts) == list(range(S))
+    assert [lengths[s_] for s_ in firsts] == sorted(lengths, reverse=True)
+    for i in range(0, count, HS):  # slices of one (sequence, KV head, group) adjacent
+        a, b = rec[i], rec[i + 1]
+        assert a[0] == b[0] and a[3] == b[3] and a[2] // HS == b[2] // HS
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, B, Hkv)
+    assert max_err(out, ref) <= TOL16
+
+
+def test_decode_calls_replayed_from_a_cuda_graph():
+    # The decode calls (split with the plan, unsplit with the plan, the decode
+    # step) captured once in a CUDA graph and replayed: each replay matches the
+    # oracle, also after the inputs are rewritten in place between replays.
+    w = Workload(0, "graph", "bf16", 32, 8, 128, 16, 6, "fixed", writes_new_token=True)
+    lengths = [1, 16, 17, 700, 2049, 300]
+    case = make_decode_case(w, seed=11, lengths=lengths)
+    S, Hq, D = case.q.shape
+    maxb = case.block_tables.shape[1]
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    q, bt, cl = case.q.to(DEV), case.block_tables.to(DEV), case.context_lens.to(DEV)
+    nk, nv = case.new_key.to(DEV), case.new_value.to(DEV)
+    outs = [torch.empty((S, Hq, D), dtype=torch.float32, device=DEV) for _ in range(3)]
+    wss = [torch.empty(pkv.decode_workspace_bytes(S, Hq, D, maxb * 16, P), dtype=torch.uint8,
+                       device=DEV) for P in (128, 0, 0)]
+
+    def body(sm):
+        pkv.decode_step(outs[2], q, nk, nv, kc, vc, bt, cl, w.scale, 16, 8, partition_size=0,
+                        workspace=wss[2], stream=sm)
+        pkv.paged_decode_attention(outs[0], q, kc, vc, bt, cl, w.scale, 16, 8,
+                                   partition_size=128, workspace=wss[0], stream=sm)
+        pkv.paged_decode_attention(outs[1], q, kc, vc, bt, cl, w.scale, 16, 8,
+                                   partition_size=0, workspace=wss[1], stream=sm)
+
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(side):
+        body(side)
+    torch.cuda.current_stream(DEV).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
+        body(side)
+    k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+    q_host = case.q.clone()
+    for rep in range(2):
+        for o in outs:
+            o.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pkv.device_status() == 0
+        ref = oracle.decode_step(q_host, case.new_key, case.new_value, k_ref.clone(),
+                                 v_ref.clone(), case.block_tables, case.context_lens, w.scale,
+                                 16, 8)
+        for o in outs:
+            assert max_err(o, ref) <= TOL16, rep
+        # new queries, written in place: the next replay reads them
+        q_host = torch.randn(q_host.shape, generator=torch.Generator().manual_seed(rep)) \
+            .to(torch.bfloat16)
+        q.copy_(q_host)
