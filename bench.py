@@ -206,8 +206,11 @@ class GpuStep:
                                   dtype=torch.uint8, device=dev)
         self.stream = torch.cuda.current_stream(dev)
         # one decode kernel per call, the append fused in (split mode also
-        # merges inside it, after a driver memset of its completion counters)
-        self.launches_per_step = (1 if self.pairs.shape[0] else 0) + 1
+        # merges inside it); a call with a workspace on the ungrouped path
+        # first runs the one-CTA work-plan kernel (beam groups split over
+        # several CTAs zero their counters with a memset, not a kernel)
+        plan_kernel = (st.P > 0 or st.plan) and not grouped
+        self.launches_per_step = (1 if self.pairs.shape[0] else 0) + 1 + (1 if plan_kernel else 0)
 
     def run(self, ev=None, stream=None):
         """One step on `stream` (default self.stream); `ev`, if given, is
