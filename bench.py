@@ -44,9 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch, valid only while the kernel
 # source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "5d8fed2c8241377c",
-           "bytes_per_launch": {"2": 1109449728, "3": 800089344, "4": 1079619328,
-                                "5": 486439168}}
+TRAFFIC = {"source_sha": "97942a2210e9173b",
+           "bytes_per_launch": {"2": 1109526016, "3": 800011776, "4": 1079577856,
+                                "5": 486561280}}
 
 
 def launch_partition(w, max_blocks: int, lens=None) -> int:
@@ -404,6 +404,7 @@ def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gpar
     if not args.no_e2e:
         e2e = end_to_end(g, st, dev, max(1, min(steps, 50)), graphs=not args.no_graph)
     launches = g.launches_per_step
+    g_pairs = int(g.pairs.shape[0])  # copy-on-write copies in the step
     del g
     torch.cuda.empty_cache()
 
@@ -413,7 +414,8 @@ def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gpar
     # call's work plan from reading its lengths while the previous call's
     # last CTAs run.  Otherwise the per-call events of the roofline pass.
     isolated_avg = statistics.mean(attn_ms)
-    attn_avg = ms_per_step if launches == 1 else isolated_avg
+    one_call = g_pairs == 0
+    attn_avg = ms_per_step if one_call else isolated_avg
     # beam groups: the bytes the launch must read are the physical blocks in
     # use, each once (shared prompt blocks included once), not the logical
     # KV of every beam
@@ -438,8 +440,11 @@ def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gpar
         "roofline": {"bound": "hbm", "kernel": ("paged_decode_grouped" if grouped else
                                                 "decode_step" if st.slots is not None else
                                                 "paged_decode_attention") +
-                     (" call: tensor-core decode kernel with in-kernel log-sum-exp merge "
-                      "(+ counter memset)" if st.P or gparts > 1 else " (tensor-core kernel)"),
+                     (" call: tensor-core decode kernel with in-kernel log-sum-exp merge" +
+                      (" (+ work-plan kernel)" if not grouped else " (+ counter memset)")
+                      if st.P or gparts > 1 else
+                      " (tensor-core kernel + work-plan kernel)" if st.plan and not grouped else
+                      " (tensor-core kernel)"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
@@ -452,7 +457,7 @@ def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gpar
                      (" + new K/V" if st.slots is not None else ""),
                      "avg_launch_ms": round(attn_avg, 5),
                      "avg_launch_timing": "the timed region (K back-to-back decode calls "
-                                          "between two events)" if launches == 1 else
+                                          "between two events)" if one_call else
                                           "events around each decode call",
                      "avg_launch_ms_events_around_each_call": round(isolated_avg, 5),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs); nominal %.0f GB/s" %
