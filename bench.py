@@ -387,14 +387,17 @@ def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gpar
 
     # ---- roofline pass: the same K steps with events around each decode
     # call, for that kernel's own average duration
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     torch.cuda.synchronize(dev)
     for i in range(steps):
+        starts[i].record(stream)
         step(mids[i])
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     attn_ms = [mids[i].elapsed_time(ends[i]) for i in range(steps)]
+    copy_ms = [starts[i].elapsed_time(mids[i]) for i in range(steps)]
     assert pkv.device_status() == 0
 
     # ---- end to end through the public API with pinned host buffers: every
@@ -464,6 +467,16 @@ def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gpar
                      (peak_src, NOMINAL_HBM_GBS)
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
     }
+    # each kernel of the step on its own (events around it): the copy-on-write
+    # copies, and the decode call (the append of the new K/V runs inside it)
+    line["step_kernels_ms"] = {
+        "kv_copy_blocks": round(statistics.mean(copy_ms), 5) if g_pairs else None,
+        "copy_pairs": g_pairs,
+        "decode_call": round(isolated_avg, 5),
+        "decode_call_kernels": ("work plan + " if launches - (1 if g_pairs else 0) == 2 else "") +
+                               "tensor-core decode" +
+                               (" (new K/V appended inside)" if st.slots is not None else ""),
+        "timing": "events around each kernel (adds the gaps the back-to-back region avoids)"}
     if st.unique_blocks is not None:
         line["pct_hbm_peak_unique_bytes"] = round(
             100 * st.unique_bytes / (attn_avg * 1e-3) / 1e9 / peak, 2)

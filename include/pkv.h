@@ -243,6 +243,13 @@ int pkv_decode_step(void* out, const void* q, const void* new_k, const void* new
  * PKV_ERR_UNSUPPORTED).  A group is read by at most `parts` CTAs a KV head,
  * so with few groups and long contexts the split, ungrouped pkv_decode_step
  * can keep more of the GPU busy.
+ * The launch is a programmatic dependent of the kernel before it on the
+ * stream: when that kernel lets dependents start early (this library's
+ * pkv_kv_copy_blocks and decode kernels do), the CTAs read group_start,
+ * context_lens, shared_tokens and block_tables while it runs, and the caches,
+ * q and new_k/new_v only after it has completed.  Those four arrays must
+ * therefore not be written by the preceding kernel of this library (none
+ * writes them); any other kernel is waited for as usual.
  */
 int pkv_paged_decode_grouped(void* out, const void* q, const void* new_k, const void* new_v,
                              void* k_cache, void* v_cache, const int32_t* block_tables,
@@ -351,7 +358,9 @@ int pkv_paged_decode_attention_noalloc(void* out, const void* q, const void* k_c
  *         Destinations must be distinct and must not appear as a source in
  *         the same call (the copies run in parallel); an id outside
  *         [0, num_blocks) skips that pair and sets PKV_STATUS_BAD_PAIR.
- * Bit-exact copy.
+ * Bit-exact copy.  The kernel lets a programmatic dependent launch that
+ * follows it start at once (pkv_paged_decode_grouped is launched that way and
+ * waits for the copy to complete before it reads or writes the caches).
  */
 int pkv_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
                        int num_blocks, int num_kv_heads, int head_dim, int block_size,

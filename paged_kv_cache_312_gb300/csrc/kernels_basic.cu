@@ -96,12 +96,22 @@ __global__ void kv_append_kernel(uint4* __restrict__ k_cache, uint4* __restrict_
 // kv_copy_blocks: physical block src -> dst for K and V; a block of all heads
 // is one contiguous run of block_bytes in this layout.
 // (auturnal guide, section 3: copy-on-write of a shared block that is not
-// full keeps branches from overwriting each other.)
+// full keeps branches from overwriting each other.)  A step copies a few
+// blocks at most, so the copy is one round trip if every load is in flight at
+// once: CTA (pair, chunk) moves kCopyThreads * kCopyUnroll vectors of K and of
+// V, each thread issuing its kCopyUnroll loads of both before it stores.
 // ---------------------------------------------------------------------------
-__global__ void copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                                   const int64_t* __restrict__ pairs, int num_blocks,
-                                   size_t vec_per_block, unsigned int* status)
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(kCopyThreads)
+copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                   const int64_t* __restrict__ pairs, int num_blocks, size_t vec_per_block,
+                   unsigned int* status)
 {
+    // a beam-group decode launched after this copy may start now: it waits
+    // for this grid to complete before it touches the caches
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t src = pairs[2 * blockIdx.x], dst = pairs[2 * blockIdx.x + 1];
     if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
         if (blockIdx.y == 0 && threadIdx.x == 0) flag(status, PKV_STATUS_BAD_PAIR);
@@ -111,11 +121,26 @@ __global__ void copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restric
     const uint4* vs = v_cache + (size_t)src * vec_per_block;
     uint4* kd = k_cache + (size_t)dst * vec_per_block;
     uint4* vd = v_cache + (size_t)dst * vec_per_block;
-    for (size_t i = (size_t)blockIdx.y * blockDim.x + threadIdx.x; i < vec_per_block;
-         i += (size_t)gridDim.y * blockDim.x) {
-        uint4 a = ks[i], b = vs[i];
-        kd[i] = a;
-        vd[i] = b;
+    constexpr size_t per_cta = (size_t)kCopyThreads * kCopyUnroll;
+    for (size_t i0 = (size_t)blockIdx.y * per_cta + threadIdx.x; i0 < vec_per_block;
+         i0 += (size_t)gridDim.y * per_cta) {
+        uint4 a[kCopyUnroll], b[kCopyUnroll];
+#pragma unroll
+        for (int k = 0; k < kCopyUnroll; ++k) {
+            const size_t i = i0 + (size_t)k * kCopyThreads;
+            if (i < vec_per_block) {
+                a[k] = ks[i];
+                b[k] = vs[i];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kCopyUnroll; ++k) {
+            const size_t i = i0 + (size_t)k * kCopyThreads;
+            if (i < vec_per_block) {
+                kd[i] = a[k];
+                vd[i] = b[k];
+            }
+        }
     }
 }
 
@@ -583,12 +608,12 @@ cudaError_t launch_kv_copy_blocks(void* k_cache, void* v_cache, const int64_t* p
                                   unsigned int* status, cudaStream_t stream)
 {
     const size_t vec = block_bytes / 16;
-    const int threads = 256;
-    size_t chunks = (vec + threads * 4 - 1) / (threads * 4);
+    const size_t per_cta = (size_t)kCopyThreads * kCopyUnroll;
+    size_t chunks = (vec + per_cta - 1) / per_cta;
     if (chunks < 1) chunks = 1;
-    if (chunks > 65535) chunks = 65535;
+    if (chunks > 65535) chunks = 65535;  // the CTAs then stride over the rest
     dim3 grid(num_pairs, (unsigned)chunks);
-    copy_blocks_kernel<<<grid, threads, 0, stream>>>(static_cast<uint4*>(k_cache),
+    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint4*>(k_cache),
                                                      static_cast<uint4*>(v_cache), pairs,
                                                      num_blocks, vec, status);
     return cudaGetLastError();

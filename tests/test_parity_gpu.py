@@ -1106,6 +1106,52 @@ def test_beam_groups_empty_members_and_uncovered_sequences(parts):
     assert bool((out[covered:] == 5.0).all())
 
 
+# dtype, Hq, Hkv, B, members per group, decode step, parts (all head_dim 128)
+WAVE_CASES = [
+    ("f16", 32, 32, 16, 4, True, 1),    # one n8 tile (4 columns)
+    ("bf16", 64, 32, 32, 3, False, 2),  # G = 2, 6 columns; two CTAs a group and KV head
+    ("bf16", 32, 16, 8, 6, True, 1),    # G = 2, 12 columns: two tiles
+    ("f16", 16, 16, 16, 16, False, 3),  # 16 members: two tiles, three CTAs
+]
+
+
+@pytest.mark.parametrize("dt,Hq,Hkv,B,members,step,parts", WAVE_CASES)
+def test_beam_groups_over_more_than_one_wave(dt, Hq, Hkv, B, members, step, parts):
+    # groups x KV heads x parts is about 4.5 CTAs a SM (a wave holds three),
+    # with ragged shared prefixes and tails: CTAs of the second wave reuse the
+    # shared memory and counters' neighbours of the first
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = -(-(9 * sms // 2) // (Hkv * parts))
+    assert 3 * sms < n * Hkv * parts <= 6 * sms
+    g = torch.Generator().manual_seed(Hq + members)
+    groups = []
+    for _ in range(n):
+        nsh = int(torch.randint(0, 7, (1,), generator=g))
+        tails = torch.randint(1 if step else 0, 41, (members,), generator=g).tolist()
+        groups.append((nsh, tails))
+    q, kc, vc, bt, cl, gs, nk, nv = make_group_case(dt, Hq, Hkv, 128, B, groups, seed=members,
+                                                    step=step)
+    scale = 128 ** -0.5
+    sh = pkv.group_shared_tokens(bt, cl, gs, B)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=DEV)
+    pkv.paged_decode_grouped(out, q.to(DEV), kd, vd, bt.to(DEV), cl.to(DEV), gs.to(DEV),
+                             sh.to(DEV), scale, B, Hkv,
+                             new_k=nk.to(DEV) if step else None,
+                             new_v=nv.to(DEV) if step else None,
+                             parts=parts, workspace=group_ws(q, parts), max_members=members)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    if step:
+        k_ref, v_ref = kc.clone(), vc.clone()
+        ref = oracle.decode_step(q, nk, nv, k_ref, v_ref, bt, cl, scale, B, Hkv)
+        assert torch.equal(bits(kd), bits(k_ref)) and torch.equal(bits(vd), bits(v_ref))
+    else:
+        ref = oracle.paged_decode_attention(q, kc, vc, bt, cl, scale, B, Hkv)
+    assert max_err(out, ref) <= TOL16
+    assert bool(torch.isfinite(out).all())
+
+
 # --------------------------------------------------------------------------
 # The work plan itself, and the calls replayed from a CUDA graph
 # --------------------------------------------------------------------------
