@@ -26,6 +26,16 @@
  *   the sizes passed in.  A bad value is skipped (never dereferenced) and sets
  *   a bit in the device status word; pkv_device_status() reads it.
  * - dtype codes: PKV_F32, PKV_F16, PKV_BF16.  q, K and V share one dtype.
+ * - The tensor-core decode kernels (pkv_paged_decode_attention, its
+ *   allocation-free form, pkv_decode_step, pkv_paged_decode_grouped) are
+ *   launched as programmatic dependents of the kernel before them on the
+ *   stream.  When that kernel lets its dependents start early (this
+ *   library's decode, work-plan and copy-on-write kernels do, as their CTAs
+ *   start), the decode CTAs read context_lens, block_tables, group_start and
+ *   shared_tokens while it still runs, and everything else only after it
+ *   has completed.  No kernel of this library writes those four arrays; a
+ *   kernel of the caller's that writes them must not let dependents start
+ *   early (kernels that do not use programmatic launches never do).
  *
  * KV cache layout (the pages fix only that a block stores the K and V of B
  * consecutive tokens [AIPP core idea 1]; this layout is this library's
@@ -243,13 +253,9 @@ int pkv_decode_step(void* out, const void* q, const void* new_k, const void* new
  * PKV_ERR_UNSUPPORTED).  A group is read by at most `parts` CTAs a KV head,
  * so with few groups and long contexts the split, ungrouped pkv_decode_step
  * can keep more of the GPU busy.
- * The launch is a programmatic dependent of the kernel before it on the
- * stream: when that kernel lets dependents start early (this library's
- * pkv_kv_copy_blocks and decode kernels do), the CTAs read group_start,
- * context_lens, shared_tokens and block_tables while it runs, and the caches,
- * q and new_k/new_v only after it has completed.  Those four arrays must
- * therefore not be written by the preceding kernel of this library (none
- * writes them); any other kernel is waited for as usual.
+ * Like the other decode calls it is a programmatic dependent launch (see the
+ * conventions above): after pkv_kv_copy_blocks its CTAs read the group
+ * bounds, lengths and tables while the copies run.
  */
 int pkv_paged_decode_grouped(void* out, const void* q, const void* new_k, const void* new_v,
                              void* k_cache, void* v_cache, const int32_t* block_tables,

@@ -422,15 +422,16 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         }
         __syncwarp();
     };
+    // Every launch is a programmatic dependent of the kernel before it (the
+    // previous decode call, the step's copy-on-write copies, or the work
+    // plan, which this CTA has already waited for).  Lengths, group bounds
+    // and the first block ids are read while that kernel runs; the new
+    // tokens, K/V and q only once it has completed and its writes are
+    // visible.  Kernels of this library never write lengths or tables.
     if constexpr (GR) {
-        // A beam-group launch is a programmatic dependent of the kernel before
-        // it (the step's copy-on-write copies, which write blocks this launch
-        // appends to and reads).  Group bounds, lengths and this warp's first
-        // block ids are read while that kernel runs; the new tokens, K/V and
-        // q only once it has completed and its writes are visible.
         if (cnt > 0) load_window(0);
-        asm volatile("griddepcontrol.wait;" ::: "memory");
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (p.new_k != nullptr) {
         if constexpr (GR) {
             // member m's new token (always past the shared prefix) lies in
@@ -854,15 +855,10 @@ cudaError_t launch_tc(const DecodeParams& p, const void* kmap, const void* vmap,
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (p.items == nullptr && !GR) {
-        kern<<<(unsigned)grid, NW * 32, Gm::SMEM_BYTES, stream>>>(
-            p, *static_cast<const CUtensorMap*>(kmap), *static_cast<const CUtensorMap*>(vmap));
-        return cudaGetLastError();
-    }
-    // after a work plan, or (beam groups) after whatever kernel precedes: a
-    // programmatic dependent launch, so that the CTAs are resident and have
-    // read what no earlier kernel of this library writes while that kernel
-    // runs, and go on the moment it completes
+    // a programmatic dependent launch (after a work plan, a copy-on-write
+    // copy, the previous decode call or any kernel): the CTAs are resident
+    // and have read what no kernel of this library writes while the kernel
+    // before them runs, and go on the moment it completes
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(NW * 32);
