@@ -149,7 +149,13 @@ int pkv_kv_write(void* k_cache, void* v_cache, const void* key, const void* valu
  *                place of zeroing the merge counters): the CTAs with work are
  *                listed longest sequence first, so that long items do not
  *                start last and empty grid slots do not interleave with
- *                work.  The order changes no result.
+ *                work.  When every non-empty context has within 10 % the
+ *                same number of stages, the plan instead cuts each context
+ *                into the same number of equal runs of stages (at most its
+ *                partitions, at most 64), the fewest whose CTAs fill their
+ *                last wave of the GPU to 95 %: partition_size then bounds
+ *                the split and sizes the workspace.  Neither the order nor
+ *                the cut changes the result in real arithmetic.
  * workspace    : device scratch of at least pkv_decode_workspace_bytes(...)
  *                bytes, 256-byte aligned, when partition_size > 0.  With
  *                partition_size == 0 it is optional: NULL attends the

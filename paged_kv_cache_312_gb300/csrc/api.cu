@@ -566,6 +566,16 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
                 pp.head_slices = p.head_slices;
                 pp.partition_tokens = p.partition_tokens;
                 pp.cta_parts = p.cta_parts;
+                pp.stage_tokens = decode_stage_tokens(head_dim, false);
+                // pieces of near-equal contexts are sized to the CTAs the GPU
+                // holds at once (split launches only: they merge partials)
+                int dev = 0, sms = 0;
+                pp.slots = 0;
+                if (p.max_partitions > 1 && cudaGetDevice(&dev) == cudaSuccess &&
+                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ==
+                        cudaSuccess)
+                    pp.slots = kDecodeTcCtasPerSm * sms;
+                pp.max_groups = (int)groups;
                 pp.max_len = max_ctx;
                 int shift = 0;
                 while ((max_ctx >> shift) >= kPlanBuckets) ++shift;

@@ -23,6 +23,8 @@
 // finishes and wait for it to complete before they read a record.
 #include <cuda_runtime.h>
 
+#include <climits>
+
 #include "pkv_kernels.h"
 
 namespace {
@@ -35,9 +37,33 @@ struct PlanSmem {
     static constexpr int OFF = SORTED + kPlanMaxSeqs;            // int [kPlanMaxSeqs]
     static constexpr int HIST = OFF + kPlanMaxSeqs;              // int [kPlanBuckets]
     static constexpr int WSUM = HIST + kPlanBuckets;             // int [32]
-    static constexpr int INTS = WSUM + 32 + 1;
+    static constexpr int INFO = WSUM + 32;                       // int [8], below
+    static constexpr int INTS = INFO + 8;
     static constexpr int BYTES = INTS * 4;
+    // INFO: over the non-empty sequences, the fewest and most stages, the
+    // fewest partitions, their count; then the pieces per sequence (0: groups)
+    static constexpr int MIN_NST = 0, MAX_NST = 1, MIN_PARTS = 2, NONEMPTY = 3, PIECES = 4;
 };
+
+// Pieces per sequence for near-equal contexts: the fewest c <= cmax whose
+// items * c CTAs fill their last wave of `slots` to kPlanWaveFillPct; else
+// the c with the fullest last wave.
+__device__ int choose_pieces(long long items, int slots, int cmax)
+{
+    int best = 1;
+    long long best_ctas = 0, best_room = 1;
+    for (int c = 1; c <= cmax; ++c) {
+        const long long ctas = items * c;
+        const long long room = (ctas + slots - 1) / slots * slots;
+        if (100 * ctas >= (long long)kPlanWaveFillPct * room) return c;
+        if (ctas * best_room > best_ctas * room) {
+            best = c;
+            best_ctas = ctas;
+            best_room = room;
+        }
+    }
+    return best;
+}
 
 // Exclusive prefix sum over the block of one value per thread; *total gets
 // the sum.  Every thread of the block calls it.
@@ -83,17 +109,50 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
     // writes
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    int* info = psm + PlanSmem::INFO;
     for (int k = tid; k < kPlanBuckets; k += kPlanThreads) hist[k] = 0;
+    if (tid == 0) {
+        info[PlanSmem::MIN_NST] = INT_MAX;
+        info[PlanSmem::MAX_NST] = 0;
+        info[PlanSmem::MIN_PARTS] = INT_MAX;
+        info[PlanSmem::NONEMPTY] = 0;
+    }
     __syncthreads();
-    // histogram of length buckets, longest bucket first (index 0)
+    // histogram of length buckets, longest bucket first (index 0); the
+    // spread of the non-empty sequences' stage counts
+    const int P = pp.partition_tokens;
     for (int s = tid; s < S; s += kPlanThreads) {
         const int L = pp.context_lens[s];
         lens[s] = L;
         const int Lc = (L < 0 || L > pp.max_len) ? 0 : L;  // the decode kernel flags it
         const int key = min(Lc >> pp.bucket_shift, kPlanBuckets - 1);
         atomicAdd(&hist[kPlanBuckets - 1 - key], 1);
+        if (Lc > 0 && P > 0) {
+            const int nst = (Lc + pp.stage_tokens - 1) / pp.stage_tokens;
+            atomicMin(&info[PlanSmem::MIN_NST], nst);
+            atomicMax(&info[PlanSmem::MAX_NST], nst);
+            atomicMin(&info[PlanSmem::MIN_PARTS], (Lc + P - 1) / P);
+            atomicAdd(&info[PlanSmem::NONEMPTY], 1);
+        }
     }
     __syncthreads();
+    // records per sequence: one per (KV head x head slice, partition group),
+    // or, when the split contexts hold within 10 % the same number of stages,
+    // one per (KV head x head slice, piece): `pieces` equal runs of stages
+    // each, as many as fill the GPU's waves (at most the partitions, and the
+    // groups, a sequence has room for)
+    const int per_seq = pp.num_kv_heads * pp.head_slices;
+    if (tid == 0) {
+        int pieces = 0;
+        const int ne = info[PlanSmem::NONEMPTY];
+        if (pp.slots > 0 && ne > 0 &&
+            10LL * info[PlanSmem::MAX_NST] <= 11LL * info[PlanSmem::MIN_NST]) {
+            const int cmax = min(min(info[PlanSmem::MIN_PARTS], pp.max_groups),
+                                 min(kPlanMaxPieces, kPlanPieceMask));
+            pieces = choose_pieces((long long)ne * per_seq, pp.slots, max(cmax, 1));
+        }
+        info[PlanSmem::PIECES] = pieces;
+    }
     // bucket starts: exclusive scan, two buckets per thread
     {
         static_assert(kPlanBuckets == 2 * kPlanThreads, "two buckets a thread");
@@ -113,12 +172,12 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
         sorted[atomicAdd(&hist[kPlanBuckets - 1 - key], 1)] = s;
     }
     __syncthreads();
-    // records per sequence: one per (KV head x head slice, partition group);
-    // a sequence with no tokens (or a bad length) keeps one group, whose CTA
-    // writes its zero rows
-    const int per_seq = pp.num_kv_heads * pp.head_slices;
+    // a sequence with no tokens (or a bad length) keeps one record, whose
+    // CTA writes its zero rows
+    const int pieces = info[PlanSmem::PIECES];  // written before the barrier above
     auto groups_of = [&](int L) {
         const int Lc = (L < 0 || L > pp.max_len) ? 0 : L;
+        if (pieces > 0) return Lc > 0 ? pieces : 1;
         const int np = max(1, (Lc + pp.partition_tokens - 1) / pp.partition_tokens);
         return (np + pp.cta_parts - 1) / pp.cta_parts;
     };
@@ -138,17 +197,20 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
     // records it still reads are written only once it has completed.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = tid; i < pp.num_counters; i += kPlanThreads) pp.done[i] = 0u;
-    // a sequence's records: KV head, then partition group, then head slice
-    // (the slices of one group adjacent: their reads of a K/V tile meet in L2)
+    // a sequence's records: KV head, then partition group (or piece), then
+    // head slice (the slices of one group adjacent: their reads of a K/V tile
+    // meet in L2)
     const int HS = pp.head_slices;
     for (int r = tid; r < S; r += kPlanThreads) {
         const int s = sorted[r], L = lens[s];
         const int ng = groups_of(L);
         int4* out = pp.items + off[r];
         for (int g = 0; g < pp.num_kv_heads; ++g)
-            for (int grp = 0; grp < ng; ++grp)
+            for (int grp = 0; grp < ng; ++grp) {
+                const int w = pieces > 0 ? kPlanPieceFlag | grp | (ng << kPlanPieceBits) : grp;
                 for (int hs = 0; hs < HS; ++hs)
-                    out[(g * ng + grp) * HS + hs] = make_int4(s, L, g * HS + hs, grp);
+                    out[(g * ng + grp) * HS + hs] = make_int4(s, L, g * HS + hs, w);
+            }
     }
     if (tid == 0) *pp.item_count = run;
 }

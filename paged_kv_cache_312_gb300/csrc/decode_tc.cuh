@@ -146,6 +146,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     // launch completes
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int s, g, sg, L, nparts, p0, np_cta, wpp, wsub, part, begin, end, nst;
+    // this CTA's partial: index pidx_v of ncp_v per (sequence, KV head, head
+    // slice), or (GR) of (group, KV head); ncp_v <= 1: the output itself
+    int ncp_v = 1, pidx_v = 0;
     // this CTA's query heads: g*G + hb .. + ncol - 1 (all of the KV group,
     // or one slice of at most NC of them when the group is wider)
     int hb = 0, ncol;
@@ -200,6 +203,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         ncol = nm * G;
         L = glen[0];
         nparts = gparts;
+        ncp_v = gparts;
+        pidx_v = part;
         p0 = 0;
         np_cta = 1;
         solo = true;
@@ -209,13 +214,14 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         end = 0;
     } else {
         // ---- which item: with a work plan, record b = (s, L, g * HS + hs,
-        // grp); else slot b = (((s * Hkv) + g) * max_groups + grp) * HS + hs.
-        // Group grp holds partitions grp * cta_parts .. + cta_parts - 1 of
-        // (s, g), for head slice hs of the KV group's query heads; the head
-        // slices of one group are adjacent, so that their reads of the same
-        // K/V tiles meet in L2.
+        // grp or piece); else slot b = (((s * Hkv) + g) * max_groups + grp) *
+        // HS + hs.  Group grp holds partitions grp * cta_parts .. + cta_parts
+        // - 1 of (s, g), for head slice hs of the KV group's query heads;
+        // piece i of n holds stages [i * nst / n, (i + 1) * nst / n) of the
+        // sequence's nst = ceil(L / ST).  The head slices of one group are
+        // adjacent, so that their reads of the same K/V tiles meet in L2.
         const int HS = p.head_slices;
-        int grp, plan_len = 0;
+        int grp, plan_len = 0, piece = -1, npieces = 0;
         if (p.items != nullptr) {
             // launched as a dependent of the plan kernel: wait until it has
             // completed and its writes (records, zeroed counters) are visible
@@ -230,6 +236,15 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             sg = it.x * (p.num_kv_heads * HS) + it.z;
             plan_len = it.y;
             grp = it.w;
+            if (it.w & kPlanPieceFlag) {
+                piece = it.w & kPlanPieceMask;
+                npieces = (it.w >> kPlanPieceBits) & kPlanPieceMask;
+                grp = 0;
+                if (npieces < 1 || piece >= npieces || npieces > p.max_partitions) {
+                    if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
+                    return;
+                }
+            }
         } else {
             const int max_groups = (p.max_partitions + p.cta_parts - 1) / p.cta_parts;
             const int hs_b = blockIdx.x % HS, t = blockIdx.x / HS;
@@ -242,16 +257,25 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
         const int GC = (G + HS - 1) / HS;
         hb = hs * GC;
         ncol = min(GC, G - hb);
+        // a piece's stages [sb, se), from the length in its record
+        int sb = 0, se = 0;
+        if (piece >= 0) {
+            const bool ok = plan_len >= 0 && (int64_t)plan_len <= (int64_t)p.max_blocks * B;
+            const int nsq = ok ? (plan_len + ST - 1) / ST : 0;
+            sb = (int)((int64_t)piece * nsq / npieces);
+            se = (int)((int64_t)(piece + 1) * nsq / npieces);
+        }
         // The first window of block ids depends on the context length only
         // through the partition-to-warp mapping, which is known in advance
         // unless a CTA of several partitions ends up with one: so it is read
         // now, overlapping the length's round trip, and used below when the
         // guess holds (entries past the context are then ignored).
         {
-            spec_solo = p.cta_parts == 1;
+            spec_solo = piece >= 0 || p.cta_parts == 1;
             const int gpart = grp * p.cta_parts + (spec_solo ? 0 : warp);
-            const int64_t gtok = (int64_t)gpart * p.partition_tokens +
-                                 (spec_solo ? warp + lane * NW : lane) * ST;
+            const int64_t gtok = (piece >= 0 ? (int64_t)sb * ST
+                                             : (int64_t)gpart * p.partition_tokens) +
+                                 (int64_t)(spec_solo ? warp + lane * NW : lane) * ST;
             const int32_t* row = p.block_tables + (size_t)s * p.max_blocks;
 #pragma unroll
             for (int u = 0; u < IDS; ++u) {
@@ -264,20 +288,38 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
             if (threadIdx.x == 0) atomicOr(p.status, PKV_STATUS_BAD_LEN);
             L = 0;
         }
-        nparts = (L + p.partition_tokens - 1) / p.partition_tokens;
-        p0 = grp * p.cta_parts;
-        if (p0 >= (nparts > 0 ? nparts : 1)) return;
-        // np_cta partitions here: a single one is spread over all NW warps
-        // (warp w streams its stages w, w + NW, ...); several get a warp each,
-        // and warps past np_cta have nothing to stream.
-        np_cta = min(p.cta_parts, (nparts > 0 ? nparts : 1) - p0);
-        solo = np_cta == 1;
-        wpp = solo ? NW : 1;       // warps per partition
-        wsub = solo ? warp : 0;    // this warp's rank within it
-        part = solo ? p0 : p0 + warp;
-        begin = part * p.partition_tokens;
-        end = min(L, begin + p.partition_tokens);
-        nst = end > begin ? (end - begin + ST - 1) / ST : 0;
+        if (piece >= 0) {
+            // one run of stages, spread over all NW warps like one partition
+            nparts = npieces;
+            p0 = piece;
+            np_cta = 1;
+            solo = true;
+            wpp = NW;
+            wsub = warp;
+            part = piece;
+            begin = sb * ST;
+            end = min(L, se * ST);
+            nst = end > begin ? se - sb : 0;
+            ncp_v = npieces;
+            pidx_v = piece;
+        } else {
+            nparts = (L + p.partition_tokens - 1) / p.partition_tokens;
+            p0 = grp * p.cta_parts;
+            if (p0 >= (nparts > 0 ? nparts : 1)) return;
+            // np_cta partitions here: a single one is spread over all NW
+            // warps (warp w streams its stages w, w + NW, ...); several get a
+            // warp each, and warps past np_cta have nothing to stream.
+            np_cta = min(p.cta_parts, (nparts > 0 ? nparts : 1) - p0);
+            solo = np_cta == 1;
+            wpp = solo ? NW : 1;       // warps per partition
+            wsub = solo ? warp : 0;    // this warp's rank within it
+            part = solo ? p0 : p0 + warp;
+            begin = part * p.partition_tokens;
+            end = min(L, begin + p.partition_tokens);
+            nst = end > begin ? (end - begin + ST - 1) / ST : 0;
+            ncp_v = (nparts + p.cta_parts - 1) / p.cta_parts;
+            pidx_v = p0 / p.cta_parts;
+        }
     }
     // GR: CTA stage q -> first token, end of its region, member (-1: shared)
     auto stage_at = [&](int q, int& tok0, int& endr, int& mem) {
@@ -660,9 +702,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     };
     // this CTA's partial: index pidx of ncp per (sequence, KV head, head
     // slice) -- one per CTA, its warps' partitions (or its share of one
-    // partition) merged first -- or (GR) of the group's runs
-    const int ncp = GR ? nparts : (nparts + p.cta_parts - 1) / p.cta_parts;
-    const int pidx = GR ? part : p0 / p.cta_parts;
+    // partition or piece) merged first -- or (GR) of the group's runs
+    const int ncp = ncp_v, pidx = pidx_v;
     // ---- merge the warps (shared memory reused once every ring is drained):
     // their states cover one partition (each a share of its stages) or, with
     // one partition per warp, consecutive partitions of the same sequence

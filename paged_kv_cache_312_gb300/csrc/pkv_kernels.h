@@ -42,8 +42,10 @@ struct DecodeParams {
     int num_groups;
     // Split launches with a work plan (tensor-core kernel only; NULL
     // otherwise): CTA b takes record items[b] = (sequence, context length,
-    // KV head * head_slices + head slice, partition group) if b < *item_count,
-    // and exits otherwise.  Written by the plan kernel just before.
+    // KV head * head_slices + head slice, w) if b < *item_count, and exits
+    // otherwise.  w is a partition group, or (with kPlanPieceFlag set) piece
+    // w & kPlanPieceMask of (w >> kPlanPieceBits) & kPlanPieceMask equal
+    // runs of the sequence's stages.  Written by the plan kernel just before.
     const int4* items;
     const int* item_count;
 };
@@ -51,12 +53,23 @@ struct DecodeParams {
 // Work plan of a split tensor-core launch (decode_plan.cu): zeroes the
 // completion counters, orders the sequences longest first and writes one
 // record per CTA with work, in that order.  One CTA; num_seqs <= kPlanMaxSeqs.
+// When every non-empty context of a split launch has about the same number
+// of stages, the plan cuts each into the same number of equal runs (pieces)
+// instead of partition groups, so that the CTAs fill whole waves.
 constexpr int kPlanMaxSeqs = 4096;
 constexpr int kPlanBuckets = 2048;  // length buckets of the counting sort
+constexpr int kPlanPieceFlag = 1 << 30;
+constexpr int kPlanPieceBits = 15;
+constexpr int kPlanPieceMask = (1 << kPlanPieceBits) - 1;
+constexpr int kPlanMaxPieces = 64;       // pieces per sequence the plan considers
+constexpr int kPlanWaveFillPct = 95;     // the fewest pieces whose last wave is this full
 struct DecodePlanParams {
     const int32_t* context_lens;  // [num_seqs]
     int num_seqs, num_kv_heads, head_slices;
     int partition_tokens, cta_parts;
+    int stage_tokens;             // tokens per stage of the decode kernel
+    int slots;                    // decode CTAs the GPU holds at once (0: no pieces)
+    int max_groups;               // record slots a (sequence, KV head, slice) has in the grid
     int max_len;                  // max_blocks * block_size: longer lengths are bad
     int bucket_shift;             // bucket of a length L: min(L >> shift, kPlanBuckets - 1)
     int4* items;                  // capacity: the launch's grid
@@ -135,6 +148,9 @@ cudaError_t launch_decode_cuda_core(const DecodeParams& p, int kv_dtype, cudaStr
 // zero; the CTA that finishes the last partition of a (sequence, KV head,
 // head slice) merges its partitions.
 constexpr int kDecodeTcWarps = 4;
+// CTAs of the (ungrouped) tensor-core decode kernel one SM holds: its 8 KB
+// stages (16 tokens at head_dim 128, 32 at 64) take ~67 KB of shared memory
+constexpr int kDecodeTcCtasPerSm = 3;
 // Split partitions of at most this many tokens get one warp each (four per
 // CTA), so that a CTA's start-up and end are spread over more KV bytes, when
 // the longest context spans at least kWarpPartitionMinCount of them.

@@ -1215,6 +1215,96 @@ def test_work_plan_records_cover_every_cta_once_longest_first(P):
     assert max_err(out, ref) <= TOL16
 
 
+def _plan_pieces(items, slots, cmax):
+    # the plan's choice of pieces per sequence for near-equal contexts: the
+    # fewest whose CTAs fill their last wave to 95 %, else the fullest
+    best, best_ctas, best_room = 1, 0, 1
+    for c in range(1, cmax + 1):
+        ctas = items * c
+        room = -(-ctas // slots) * slots
+        if 100 * ctas >= 95 * room:
+            return c
+        if ctas * best_room > best_ctas * room:
+            best, best_ctas, best_room = c, ctas, room
+    return best
+
+
+# dtype, Hq, Hkv, D, B, context lengths, partition tokens, decode step
+PIECE_CASES = [
+    ("bf16", 32, 8, 128, 32, [8000, 8600, 8301, 8450], 512, False),  # partitions a warp
+    ("bf16", 8, 8, 64, 16, [3000, 3100, 3071], 256, True),           # 32-token stages, append
+    ("f16", 48, 2, 128, 16, [1950, 2048, 2000, 1999, 2040], 1024, False),  # head slices
+    ("bf16", 32, 8, 128, 16, [4096] * 39 + [0], 512, True),          # many, and an empty one
+]
+
+
+@pytest.mark.parametrize("dt,Hq,Hkv,D,B,lengths,P,step", PIECE_CASES)
+def test_split_near_equal_contexts_in_equal_pieces(dt, Hq, Hkv, D, B, lengths, P, step):
+    # Contexts within 10 % of the same stage count: the plan cuts each into
+    # the same number of equal runs of stages (pieces), as many as fill the
+    # GPU's waves, instead of partition groups; the records say so and the
+    # result is unchanged.
+    S = len(lengths)
+    w = Workload(0, "pieces", dt, Hq, Hkv, D, B, S, "fixed", writes_new_token=step)
+    case = make_decode_case(w, seed=S + D, lengths=lengths)
+    maxb = case.block_tables.shape[1]
+    nP = -(-maxb * B // P)
+    n = pkv.decode_workspace_bytes(S, Hq, D, maxb * B, P)
+    ws = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    out = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    if step:
+        pkv.decode_step(out, case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV), kc,
+                        vc, case.block_tables.to(DEV), case.context_lens.to(DEV), w.scale, B,
+                        Hkv, partition_size=P, workspace=ws)
+    else:
+        pkv.paged_decode_attention(out, case.q.to(DEV), kc, vc, case.block_tables.to(DEV),
+                                   case.context_lens.to(DEV), w.scale, B, Hkv, partition_size=P,
+                                   workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    # the records
+    G = Hq // Hkv
+    HS = -(-G // 16)
+    cta_parts = 4 if (P <= 512 and nP >= 16) else 1
+    max_groups = -(-nP // cta_parts)
+    ST = 32 if D == 64 else 16
+    nst = [-(-L // ST) for L in lengths if L > 0]
+    assert 10 * max(nst) <= 11 * min(nst)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cmax = min(min(-(-L // P) for L in lengths if L > 0), max_groups, 64)
+    pieces = _plan_pieces(len(nst) * Hkv * HS, 3 * sms, cmax)
+    ml = _align256(S * Hq * 4)
+    o = ml + _align256(S * Hq * nP * 8)
+    count_off = o + _align256(S * Hq * nP * D * 4)
+    host = ws.cpu()
+    count = int(host[count_off:count_off + 4].view(torch.int32)[0])
+    per = [pieces if L > 0 else 1 for L in lengths]
+    assert count == sum(Hkv * HS * c for c in per)
+    rec = host[count_off + 256:count_off + 256 + count * 16].view(torch.int32).view(count, 4)
+    seen = set()
+    for s_, L, gh, wv in rec.tolist():
+        assert L == lengths[s_] and 0 <= gh < Hkv * HS
+        assert wv & (1 << 30)  # a piece
+        i, c = wv & 0x7FFF, (wv >> 15) & 0x7FFF
+        assert c == per[s_] and 0 <= i < c
+        seen.add((s_, gh, i))
+    assert len(seen) == count
+    # the result
+    if step:
+        k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+        ref = oracle.decode_step(case.q, case.new_key, case.new_value, k_ref, v_ref,
+                                 case.block_tables, case.context_lens, w.scale, B, Hkv,
+                                 nthreads=oracle.default_threads())
+        assert torch.equal(bits(kc), bits(k_ref)) and torch.equal(bits(vc), bits(v_ref))
+    else:
+        ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache,
+                                            case.block_tables, case.context_lens, w.scale, B,
+                                            Hkv, nthreads=oracle.default_threads())
+    assert max_err(out, ref) <= TOL16
+    assert bool(torch.isfinite(out).all())
+
+
 def test_decode_calls_replayed_from_a_cuda_graph():
     # The decode calls (split with the plan, unsplit with the plan, the decode
     # step) captured once in a CUDA graph and replayed: each replay matches the
