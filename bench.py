@@ -44,9 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch, valid only while the kernel
 # source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "97942a2210e9173b",
-           "bytes_per_launch": {"2": 1109526016, "3": 800011776, "4": 1079577856,
-                                "5": 486561280}}
+TRAFFIC = {"source_sha": "dec9c5b1cca07019",
+           "bytes_per_launch": {"2": 1109798144, "3": 800291840, "4": 1077387776,
+                                "5": 486409728}}
 
 
 def launch_partition(w, max_blocks: int, lens=None) -> int:

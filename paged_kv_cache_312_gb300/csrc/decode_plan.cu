@@ -47,19 +47,44 @@ struct PlanSmem {
 
 // Pieces per sequence for near-equal contexts: the fewest c <= cmax whose
 // items * c CTAs fill their last wave of `slots` to kPlanWaveFillPct; else
-// the c with the fullest last wave.
+// the c with the fullest last wave (the fewest of equals).  One warp calls
+// it, lane l trying c = l + 1, l + 33.  No c qualifies only when items is
+// below ~20 waves of CTAs, so the products below stay far inside 64 bits.
 __device__ int choose_pieces(long long items, int slots, int cmax)
 {
+    const int lane = threadIdx.x & 31;
+    for (int c0 = 1; c0 <= cmax; c0 += 32) {
+        const int c = c0 + lane;
+        bool ok = false;
+        if (c <= cmax) {
+            const long long ctas = items * c;
+            const long long room = (ctas + slots - 1) / slots * slots;
+            ok = 100 * ctas >= (long long)kPlanWaveFillPct * room;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, ok);
+        if (m != 0u) return c0 + __ffs(m) - 1;
+    }
     int best = 1;
-    long long best_ctas = 0, best_room = 1;
-    for (int c = 1; c <= cmax; ++c) {
+    long long bc = 0, br = 1;  // fill of `best`: bc / br
+    for (int c = 1 + lane; c <= cmax; c += 32) {
         const long long ctas = items * c;
         const long long room = (ctas + slots - 1) / slots * slots;
-        if (100 * ctas >= (long long)kPlanWaveFillPct * room) return c;
-        if (ctas * best_room > best_ctas * room) {
+        if (ctas * br > bc * room) {
             best = c;
-            best_ctas = ctas;
-            best_room = room;
+            bc = ctas;
+            br = room;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const int b2 = __shfl_xor_sync(0xffffffffu, best, o);
+        const long long c2 = __shfl_xor_sync(0xffffffffu, bc, o);
+        const long long r2 = __shfl_xor_sync(0xffffffffu, br, o);
+        const long long lhs = c2 * br, rhs = bc * r2;
+        if (lhs > rhs || (lhs == rhs && b2 < best)) {
+            best = b2;
+            bc = c2;
+            br = r2;
         }
     }
     return best;
@@ -142,7 +167,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
     // each, as many as fill the GPU's waves (at most the partitions, and the
     // groups, a sequence has room for)
     const int per_seq = pp.num_kv_heads * pp.head_slices;
-    if (tid == 0) {
+    if (tid < 32) {  // warp 0; the condition is the same for all its lanes
         int pieces = 0;
         const int ne = info[PlanSmem::NONEMPTY];
         if (pp.slots > 0 && ne > 0 &&
@@ -151,7 +176,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
                                  min(kPlanMaxPieces, kPlanPieceMask));
             pieces = choose_pieces((long long)ne * per_seq, pp.slots, max(cmax, 1));
         }
-        info[PlanSmem::PIECES] = pieces;
+        if (tid == 0) info[PlanSmem::PIECES] = pieces;
     }
     // bucket starts: exclusive scan, two buckets per thread
     {
