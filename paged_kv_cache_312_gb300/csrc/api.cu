@@ -554,6 +554,15 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
         if (grid >= (1ll << 31))
             return pkv_fail(PKV_ERR_SHAPE, "%s: more than 2^31 work items", fn);
         const int counters = p.max_partitions > 1 ? num_seqs * num_kv_heads * p.head_slices : 0;
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sms = 0;
+        // An unsplit launch of few items (at most two waves of three CTAs a
+        // SM) runs deep rings: its last, longest CTAs then stream faster.
+        const long long items = (long long)num_seqs * num_kv_heads * p.head_slices;
+        const bool deep = p.max_partitions <= 1 && sms > 0 &&
+                          items <= (long long)kDecodeTcDeepMaxWaves * kDecodeTcCtasPerSm * sms;
         if (plan_items != nullptr || counters > 0) {
             if (plan_items != nullptr && num_seqs <= kPlanMaxSeqs) {
                 // the plan kernel zeroes the completion counters of the
@@ -569,12 +578,7 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
                 pp.stage_tokens = decode_stage_tokens(head_dim, false);
                 // pieces of near-equal contexts are sized to the CTAs the GPU
                 // holds at once (split launches only: they merge partials)
-                int dev = 0, sms = 0;
-                pp.slots = 0;
-                if (p.max_partitions > 1 && cudaGetDevice(&dev) == cudaSuccess &&
-                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ==
-                        cudaSuccess)
-                    pp.slots = kDecodeTcCtasPerSm * sms;
+                pp.slots = p.max_partitions > 1 ? kDecodeTcCtasPerSm * sms : 0;
                 pp.max_groups = (int)groups;
                 pp.max_len = max_ctx;
                 int shift = 0;
@@ -597,8 +601,11 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
         // the tensor-core kernel writes the new tokens itself
         p.new_k = new_k;
         p.new_v = new_v;
-        e = columns > 8 ? launch_decode_tensor_core_wide(p, kv_dtype, &kmap, &vmap, grid, st)
-                        : launch_decode_tensor_core(p, kv_dtype, &kmap, &vmap, grid, st);
+        if (deep)
+            e = launch_decode_tensor_core_deep(p, kv_dtype, &kmap, &vmap, grid, columns > 8, st);
+        else
+            e = columns > 8 ? launch_decode_tensor_core_wide(p, kv_dtype, &kmap, &vmap, grid, st)
+                            : launch_decode_tensor_core(p, kv_dtype, &kmap, &vmap, grid, st);
         if (e != cudaSuccess) return cuda_fail(e, fn);
         return PKV_OK;
     }

@@ -101,7 +101,7 @@ struct Geometry {
     // registers), or 5 for two column tiles with 4 KB stages (96).  Left to
     // itself the compiler took 96 registers at D = 128, and the freedom to use
     // more is worth 1-4 % of HBM bandwidth there; with 4 KB stages it spilled.
-    static constexpr int MIN_CTAS = KV_BYTES >= 4096 ? 3 : (NT == 1 ? 6 : 5);
+    static constexpr int MIN_CTAS = KV_BYTES >= 4096 ? (NS >= 3 ? 2 : 3) : (NT == 1 ? 6 : 5);
     static_assert(SUB_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
     static_assert(STAGE_BYTES % 1024 == 0 && RING_BYTES % 1024 == 0, "stage alignment");
 };
@@ -880,14 +880,16 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
     }
 }
 
-template <typename T, int D, int B, bool GR, int NT>
+template <typename T, int D, int B, bool GR, int NT, int NS = 2>
 cudaError_t launch_tc(const DecodeParams& p, const void* kmap, const void* vmap, long long grid,
                       cudaStream_t stream)
 {
     // 4 warps x 2-stage rings of 8 KB stages (16 tokens at D = 128, 32 at
     // D = 64; beam groups at D = 64 keep 16): 64 KB per CTA, three CTAs per
-    // SM, up to 192 KB of tile loads in flight per SM
-    constexpr int NW = kDecodeTcWarps, NS = 2;
+    // SM, up to 192 KB of tile loads in flight per SM; or (NS = 3) 3-stage
+    // rings, 96 KB per CTA, two CTAs per SM: the same loads per SM, but each
+    // warp keeps two stages in flight while it works on a third
+    constexpr int NW = kDecodeTcWarps;
     constexpr int TPS = decode_stage_tokens(D, GR) / 16;
     using Gm = Geometry<D, B, NW, NS, NT, TPS>;
     static_assert(Gm::ROWS == decode_box_rows(D, B, GR), "tensor map box = stage box");
@@ -914,19 +916,20 @@ cudaError_t launch_tc(const DecodeParams& p, const void* kmap, const void* vmap,
                               *static_cast<const CUtensorMap*>(vmap));
 }
 
-// NT: n8 column tiles of query heads per CTA (1: up to 8 columns, 2: up to 16)
-template <typename T, bool GR, int NT>
+// NT: n8 column tiles of query heads per CTA (1: up to 8 columns, 2: up to 16);
+// NS: stages per warp ring
+template <typename T, bool GR, int NT, int NS = 2>
 cudaError_t launch_tc_dtype(const DecodeParams& p, const void* kmap, const void* vmap,
                             long long grid, cudaStream_t stream)
 {
     if (p.head_dim == 128) {
-        if (p.block_size == 16) return launch_tc<T, 128, 16, GR, NT>(p, kmap, vmap, grid, stream);
-        if (p.block_size == 32) return launch_tc<T, 128, 32, GR, NT>(p, kmap, vmap, grid, stream);
-        return launch_tc<T, 128, 8, GR, NT>(p, kmap, vmap, grid, stream);
+        if (p.block_size == 16) return launch_tc<T, 128, 16, GR, NT, NS>(p, kmap, vmap, grid, stream);
+        if (p.block_size == 32) return launch_tc<T, 128, 32, GR, NT, NS>(p, kmap, vmap, grid, stream);
+        return launch_tc<T, 128, 8, GR, NT, NS>(p, kmap, vmap, grid, stream);
     }
-    if (p.block_size == 16) return launch_tc<T, 64, 16, GR, NT>(p, kmap, vmap, grid, stream);
-    if (p.block_size == 32) return launch_tc<T, 64, 32, GR, NT>(p, kmap, vmap, grid, stream);
-    return launch_tc<T, 64, 8, GR, NT>(p, kmap, vmap, grid, stream);
+    if (p.block_size == 16) return launch_tc<T, 64, 16, GR, NT, NS>(p, kmap, vmap, grid, stream);
+    if (p.block_size == 32) return launch_tc<T, 64, 32, GR, NT, NS>(p, kmap, vmap, grid, stream);
+    return launch_tc<T, 64, 8, GR, NT, NS>(p, kmap, vmap, grid, stream);
 }
 
 }  // namespace

@@ -9,6 +9,7 @@
 cudaError_t launch_decode_tensor_core_wide(const DecodeParams& p, int kv_dtype, const void* k_map,
                                            const void* v_map, long long grid, cudaStream_t stream)
 {
-    if (kv_dtype == PKV_BF16) return launch_tc_dtype<__nv_bfloat16, false, 2>(p, k_map, v_map, grid, stream);
+    if (kv_dtype == PKV_BF16)
+        return launch_tc_dtype<__nv_bfloat16, false, 2>(p, k_map, v_map, grid, stream);
     return launch_tc_dtype<__half, false, 2>(p, k_map, v_map, grid, stream);
 }

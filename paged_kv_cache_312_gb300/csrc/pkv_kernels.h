@@ -175,6 +175,13 @@ cudaError_t launch_decode_tensor_core(const DecodeParams& p, int kv_dtype, const
                                       const void* v_map, long long grid, cudaStream_t stream);
 cudaError_t launch_decode_tensor_core_wide(const DecodeParams& p, int kv_dtype, const void* k_map,
                                            const void* v_map, long long grid, cudaStream_t stream);
+// The same kernel with 3-stage rings, two CTAs a SM (wide: two column tiles),
+// for unsplit launches of at most kDecodeTcDeepMaxWaves waves of
+// kDecodeTcCtasPerSm CTAs a SM: few items, each streaming much.
+constexpr int kDecodeTcDeepMaxWaves = 2;
+cudaError_t launch_decode_tensor_core_deep(const DecodeParams& p, int kv_dtype, const void* k_map,
+                                           const void* v_map, long long grid, bool wide,
+                                           cudaStream_t stream);
 
 // Tensor-core decode over beam groups: one CTA per (group, KV head, part),
 // grid num_groups * num_kv_heads * p.max_partitions, the parts of one (group,

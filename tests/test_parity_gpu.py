@@ -1305,6 +1305,48 @@ def test_split_near_equal_contexts_in_equal_pieces(dt, Hq, Hkv, D, B, lengths, P
     assert bool(torch.isfinite(out).all())
 
 
+# dtype, Hq, Hkv, D, B (the items per sequence: Hkv x head slices)
+SHALLOW_CASES = [
+    ("bf16", 16, 16, 128, 16),
+    ("f16", 64, 8, 64, 32),
+    ("bf16", 96, 8, 128, 8),   # G = 12: two column tiles
+    ("f16", 32, 32, 64, 8),
+    ("bf16", 48, 2, 128, 32),  # G = 24: two head slices
+]
+
+
+@pytest.mark.parametrize("plan", [False, True])
+@pytest.mark.parametrize("dt,Hq,Hkv,D,B", SHALLOW_CASES)
+def test_unsplit_launch_of_many_items(dt, Hq, Hkv, D, B, plan):
+    # An unsplit launch of more items (sequence x KV head x head slice) than
+    # two waves of three CTAs a SM keeps 2-stage rings, three CTAs a SM; fewer
+    # items (every other small test) get 3-stage rings, two a SM.  Short
+    # ragged contexts, some empty, with and without the work plan.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    HS = -(-(Hq // Hkv) // 16)
+    S = -(-(13 * sms) // (2 * Hkv * HS))
+    assert S * Hkv * HS > 6 * sms
+    rng = np.random.default_rng(S + D + B)
+    lengths = [int(x) for x in rng.integers(0, 300, size=S)]
+    w = Workload(0, "shallow", dt, Hq, Hkv, D, B, S, "fixed")
+    case = make_decode_case(w, seed=D + B, lengths=lengths)
+    ws = None
+    if plan:
+        n = pkv.decode_workspace_bytes(S, Hq, D, case.block_tables.shape[1] * B, 0)
+        ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    out = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    pkv.paged_decode_attention(out, case.q.to(DEV), case.k_cache.to(DEV), case.v_cache.to(DEV),
+                               case.block_tables.to(DEV), case.context_lens.to(DEV), w.scale, B,
+                               Hkv, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, B, Hkv,
+                                        nthreads=oracle.default_threads())
+    assert max_err(out, ref) <= TOL16
+    assert bool(torch.isfinite(out).all())
+
+
 def test_decode_calls_replayed_from_a_cuda_graph():
     # The decode calls (split with the plan, unsplit with the plan, the decode
     # step) captured once in a CUDA graph and replayed: each replay matches the
