@@ -84,8 +84,8 @@ def kernel_sha() -> str:
     (the traffic figures above hold only for the code they were captured
     from)."""
     h = hashlib.sha256()
-    for name in ("decode_tc.cu", "decode_wide.cu", "decode_group.cu", "decode_plan.cu",
-                 "decode_tc.cuh", "tc_common.cuh"):
+    for name in ("decode_tc.cu", "decode_wide.cu", "decode_deep.cu", "decode_group.cu",
+                 "decode_plan.cu", "decode_tc.cuh", "tc_common.cuh"):
         text = open(os.path.join(ROOT, "paged_kv_cache_312_gb300", "csrc", name)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
