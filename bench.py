@@ -44,9 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch of the tensor-core decode kernel from
 # one ncu capture of each workload's launch, valid only while the kernel
 # source hashes to `source_sha`.
-TRAFFIC = {"source_sha": "dec9c5b1cca07019",
-           "bytes_per_launch": {"2": 1109798144, "3": 800291840, "4": 1077387776,
-                                "5": 486409728}}
+TRAFFIC = {"source_sha": "be889194e7ba1bac",
+           "bytes_per_launch": {"2": 1109357056, "3": 800045312, "4": 1077338624,
+                                "5": 486553088}}
 
 
 def launch_partition(w, max_blocks: int, lens=None) -> int:
