@@ -212,26 +212,28 @@ class GpuStep:
         plan_kernel = (st.P > 0 or st.plan) and not grouped
         self.launches_per_step = (1 if self.pairs.shape[0] else 0) + 1 + (1 if plan_kernel else 0)
 
-    def run(self, ev=None, stream=None):
+    def run(self, ev=None, stream=None, out=None):
         """One step on `stream` (default self.stream); `ev`, if given, is
-        recorded between the copy-on-write copies and the decode call."""
+        recorded between the copy-on-write copies and the decode call; `out`
+        (default self.out) may be pinned host memory."""
         pkv, w, st = self.pkv, self.w, self.st
         sm = self.stream if stream is None else stream
+        out = self.out if out is None else out
         if self.pairs.shape[0]:
             pkv.kv_copy_blocks(self.kc, self.vc, self.pairs, stream=sm)
         if ev is not None:
             ev.record(sm)
         if self.grouped:  # append the new tokens and attend, one CTA per (group, KV head)
-            pkv.paged_decode_grouped(self.out, self.q, self.kc, self.vc, self.bt, self.cl,
+            pkv.paged_decode_grouped(out, self.q, self.kc, self.vc, self.bt, self.cl,
                                      self.gs, self.sh, w.scale, w.block_size, w.num_kv_heads,
                                      new_k=self.nk, new_v=self.nv, parts=self.gparts,
                                      workspace=self.ws, max_members=w.beam_width, stream=sm)
         elif self.has_write:  # append the new tokens and attend, one call
-            pkv.decode_step(self.out, self.q, self.nk, self.nv, self.kc, self.vc, self.bt,
+            pkv.decode_step(out, self.q, self.nk, self.nv, self.kc, self.vc, self.bt,
                             self.cl, w.scale, w.block_size, w.num_kv_heads, partition_size=st.P,
                             workspace=self.ws, stream=sm)
         else:
-            pkv.paged_decode_attention(self.out, self.q, self.kc, self.vc, self.bt, self.cl,
+            pkv.paged_decode_attention(out, self.q, self.kc, self.vc, self.bt, self.cl,
                                        w.scale, w.block_size, w.num_kv_heads,
                                        partition_size=st.P, workspace=self.ws, stream=sm)
 
@@ -554,10 +556,21 @@ def end_to_end(g, st, dev, k, graphs=True):
             sm.synchronize()
         return (time.perf_counter() - w0) / k
 
+    def body_direct(sm):
+        # the output rows go straight to pinned host memory from the kernel
+        # (NVLink-C2C stores as each CTA finishes): no copy after the launch
+        g.d_pack.copy_(g.h_pack, non_blocking=True)
+        g.run(stream=sm, out=h_out)
+
     plain_s = timed(lambda: body(g.stream), g.stream)
     res["api_calls_ms_per_step"] = round(plain_s * 1e3, 4)
     res["api_calls_value"] = round(st.kv_bytes / plain_s / 1e9, 2)
     e2e_s, how = plain_s, "one public API call after the other, every step"
+    copied = h_out.clone()  # the step's output as the D2H copy brought it back
+    h_out.fill_(float("nan"))
+    direct_s = timed(lambda: body_direct(g.stream), g.stream)
+    assert torch.equal(h_out, copied), "direct output differs from the copied-back output"
+    direct_how = "one public API call after the other, every step"
     if graphs:
         graph = capture_step_graph(body, dev)
         if graph is not None:
@@ -566,8 +579,25 @@ def end_to_end(g, st, dev, k, graphs=True):
             e2e_s = timed(graph.replay, cur)
             how = ("the step's public API calls (H2D copy, library calls, D2H copy) captured "
                    "once as a CUDA graph, one graph launch per step")
+        graph_d = capture_step_graph(body_direct, dev)
+        if graph_d is not None:
+            cur = torch.cuda.current_stream(dev)
+            graph_d.replay()
+            direct_s = min(direct_s, timed(graph_d.replay, cur))
+            direct_how = "the better of the plain calls and their CUDA graph"
     res.update({"value": round(st.kv_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_s * 1e3, 4), "how": how})
+    # the same step with the output written to pinned host memory by the
+    # decode kernel itself: the same bytes cross NVLink-C2C, during the
+    # launch instead of after it
+    res["direct_output"] = {
+        "value": round(st.kv_bytes / direct_s / 1e9, 2), "unit": "GB/s",
+        "ms_per_step": round(direct_s * 1e3, 4),
+        "h2d_bytes_per_step": res["h2d_bytes_per_step"],
+        "d2h_bytes_per_step": res["d2h_bytes_per_step"],
+        "how": "inputs copied as above; the decode call writes its fp32 output to pinned "
+               "host memory directly (NVLink-C2C stores from the kernel), then the host "
+               "synchronises; " + direct_how}
     return res
 
 

@@ -128,6 +128,12 @@ int pkv_kv_write(void* k_cache, void* v_cache, const void* key, const void* valu
  * (grouped-query attention, [AUT section 1]: GQA/MQA change the KV head count).
  *
  * out          : [num_seqs][num_heads][head_dim], dtype out_dtype (written).
+ *                Device memory, or pinned host memory that the GPU addresses
+ *                directly (the same pointer): the launch then stores each
+ *                output row over NVLink-C2C as its CTA finishes, and the
+ *                stream's completion is the read-back, with no copy after it.
+ *                The same holds for the output of pkv_decode_step, its
+ *                allocation-free split form and pkv_paged_decode_grouped.
  * q            : [num_seqs][num_heads][head_dim], dtype kv_dtype.
  * block_tables : int32 [num_seqs][max_blocks_per_seq]; only the first
  *                ceil(context_lens[s]/block_size) entries of row s are read.

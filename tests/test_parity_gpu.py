@@ -1347,6 +1347,50 @@ def test_unsplit_launch_of_many_items(dt, Hq, Hkv, D, B, plan):
     assert bool(torch.isfinite(out).all())
 
 
+@pytest.mark.parametrize("call", ["unsplit", "split", "step", "grouped"])
+def test_output_written_to_pinned_host_memory(call):
+    # out may be pinned host memory: the kernel stores the rows over the
+    # host link; the result is the same bits as with a device output
+    lengths = [1, 700, 33, 2049, 0, 1500]
+    w = Workload(0, "hostout", "bf16", 32, 8, 128, 16, len(lengths), "fixed",
+                 writes_new_token=(call == "step"))
+    case = make_decode_case(w, seed=77, lengths=lengths)
+    S, Hq, D = case.q.shape
+    maxb = case.block_tables.shape[1]
+    outs = []
+    for host in (False, True):
+        kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+        q, bt, cl = case.q.to(DEV), case.block_tables.to(DEV), case.context_lens.to(DEV)
+        out = torch.full((S, Hq, D), float("nan"), dtype=torch.float32)
+        out = out.pin_memory() if host else out.to(DEV)
+        if call == "grouped":
+            gs = torch.tensor([0, 2, 3, 6], dtype=torch.int32)
+            sh = pkv.group_shared_tokens(case.block_tables, case.context_lens, gs, 16)
+            pkv.paged_decode_grouped(out, q, kc, vc, bt, cl, gs.to(DEV), sh.to(DEV), w.scale, 16,
+                                     8)
+        elif call == "step":
+            pkv.decode_step(out, q, case.new_key.to(DEV), case.new_value.to(DEV), kc, vc, bt, cl,
+                            w.scale, 16, 8)
+        else:
+            P = 512 if call == "split" else 0
+            ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, maxb * 16, P),
+                             dtype=torch.uint8, device=DEV)
+            pkv.paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, 16, 8, partition_size=P,
+                                       workspace=ws)
+        torch.cuda.synchronize()
+        assert pkv.device_status() == 0
+        outs.append(out.cpu())
+    assert torch.equal(outs[0], outs[1])
+    if call == "step":
+        k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+        ref = oracle.decode_step(case.q, case.new_key, case.new_value, k_ref, v_ref,
+                                 case.block_tables, case.context_lens, w.scale, 16, 8)
+    else:
+        ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                            case.context_lens, w.scale, 16, 8)
+    assert max_err(outs[1], ref) <= TOL16
+
+
 def test_decode_calls_replayed_from_a_cuda_graph():
     # The decode calls (split with the plan, unsplit with the plan, the decode
     # step) captured once in a CUDA graph and replayed: each replay matches the
