@@ -186,6 +186,10 @@ class GpuStep:
             inputs += [gstart, shared]
         self.h_pack, views = pack_inputs(inputs, dev)
         self.q, self.bt, self.cl, self.pairs = views[:4]
+        # q in the pinned pack (the pack's first tensor), and where the rest starts
+        qn = st.q.numel() * st.q.element_size()
+        self.h_q = self.h_pack[:qn].view(st.q.dtype).view(st.q.shape)
+        self.rest_off = (qn + 255) // 256 * 256
         self.nk = self.nv = None
         if self.has_write:
             self.nk, self.nv = views[4:6]
@@ -212,28 +216,29 @@ class GpuStep:
         plan_kernel = (st.P > 0 or st.plan) and not grouped
         self.launches_per_step = (1 if self.pairs.shape[0] else 0) + 1 + (1 if plan_kernel else 0)
 
-    def run(self, ev=None, stream=None, out=None):
+    def run(self, ev=None, stream=None, out=None, q=None):
         """One step on `stream` (default self.stream); `ev`, if given, is
         recorded between the copy-on-write copies and the decode call; `out`
-        (default self.out) may be pinned host memory."""
+        and `q` (default self.out, self.q) may be pinned host memory."""
         pkv, w, st = self.pkv, self.w, self.st
         sm = self.stream if stream is None else stream
         out = self.out if out is None else out
+        q = self.q if q is None else q
         if self.pairs.shape[0]:
             pkv.kv_copy_blocks(self.kc, self.vc, self.pairs, stream=sm)
         if ev is not None:
             ev.record(sm)
         if self.grouped:  # append the new tokens and attend, one CTA per (group, KV head)
-            pkv.paged_decode_grouped(out, self.q, self.kc, self.vc, self.bt, self.cl,
+            pkv.paged_decode_grouped(out, q, self.kc, self.vc, self.bt, self.cl,
                                      self.gs, self.sh, w.scale, w.block_size, w.num_kv_heads,
                                      new_k=self.nk, new_v=self.nv, parts=self.gparts,
                                      workspace=self.ws, max_members=w.beam_width, stream=sm)
         elif self.has_write:  # append the new tokens and attend, one call
-            pkv.decode_step(out, self.q, self.nk, self.nv, self.kc, self.vc, self.bt,
+            pkv.decode_step(out, q, self.nk, self.nv, self.kc, self.vc, self.bt,
                             self.cl, w.scale, w.block_size, w.num_kv_heads, partition_size=st.P,
                             workspace=self.ws, stream=sm)
         else:
-            pkv.paged_decode_attention(out, self.q, self.kc, self.vc, self.bt, self.cl,
+            pkv.paged_decode_attention(out, q, self.kc, self.vc, self.bt, self.cl,
                                        w.scale, w.block_size, w.num_kv_heads,
                                        partition_size=st.P, workspace=self.ws, stream=sm)
 
@@ -562,6 +567,12 @@ def end_to_end(g, st, dev, k, graphs=True):
         g.d_pack.copy_(g.h_pack, non_blocking=True)
         g.run(stream=sm, out=h_out)
 
+    def body_direct_io(sm):
+        # q read in place from the pinned pack by the kernel as well: only the
+        # rest of the pack (tables, lengths, pairs, new K/V) is copied
+        g.d_pack[g.rest_off:].copy_(g.h_pack[g.rest_off:], non_blocking=True)
+        g.run(stream=sm, out=h_out, q=g.h_q)
+
     plain_s = timed(lambda: body(g.stream), g.stream)
     res["api_calls_ms_per_step"] = round(plain_s * 1e3, 4)
     res["api_calls_value"] = round(st.kv_bytes / plain_s / 1e9, 2)
@@ -585,8 +596,26 @@ def end_to_end(g, st, dev, k, graphs=True):
             graph_d.replay()
             direct_s = min(direct_s, timed(graph_d.replay, cur))
             direct_how = "the better of the plain calls and their CUDA graph"
+    h_out.fill_(float("nan"))
+    io_s = timed(lambda: body_direct_io(g.stream), g.stream)
+    assert torch.equal(h_out, copied), "direct-io output differs from the copied-back output"
+    io_how = "one public API call after the other, every step"
+    if graphs:
+        graph_io = capture_step_graph(body_direct_io, dev)
+        if graph_io is not None:
+            cur = torch.cuda.current_stream(dev)
+            graph_io.replay()
+            io_s = min(io_s, timed(graph_io.replay, cur))
+            io_how = "the better of the plain calls and their CUDA graph"
     res.update({"value": round(st.kv_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_s * 1e3, 4), "how": how})
+    res["direct_io"] = {
+        "value": round(st.kv_bytes / io_s / 1e9, 2), "unit": "GB/s",
+        "ms_per_step": round(io_s * 1e3, 4),
+        "h2d_bytes_per_step": res["h2d_bytes_per_step"],
+        "d2h_bytes_per_step": res["d2h_bytes_per_step"],
+        "how": "q read by the decode kernel from pinned host memory and the fp32 output "
+               "written there (NVLink-C2C); the other inputs copied; " + io_how}
     # the same step with the output written to pinned host memory by the
     # decode kernel itself: the same bytes cross NVLink-C2C, during the
     # launch instead of after it

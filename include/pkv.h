@@ -132,9 +132,11 @@ int pkv_kv_write(void* k_cache, void* v_cache, const void* key, const void* valu
  *                directly (the same pointer): the launch then stores each
  *                output row over NVLink-C2C as its CTA finishes, and the
  *                stream's completion is the read-back, with no copy after it.
- *                The same holds for the output of pkv_decode_step, its
- *                allocation-free split form and pkv_paged_decode_grouped.
- * q            : [num_seqs][num_heads][head_dim], dtype kv_dtype.
+ *                The same holds for out and q of pkv_decode_step, of the
+ *                allocation-free split form and of pkv_paged_decode_grouped.
+ * q            : [num_seqs][num_heads][head_dim], dtype kv_dtype; device
+ *                memory or pinned host memory, like out (each CTA loads its
+ *                rows once, after it has started its first K/V loads).
  * block_tables : int32 [num_seqs][max_blocks_per_seq]; only the first
  *                ceil(context_lens[s]/block_size) entries of row s are read.
  * context_lens : int32 [num_seqs], tokens attended (the token written this

@@ -166,7 +166,8 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
     if workspace is not None:
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
     rc = lib().pkv_paged_decode_attention(
-        _reachable(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _reachable(out, "out"), _reachable(q, "q"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables"), _dev(context_lens, "context_lens"), float(scale),
         int(block_size), int(num_kv_heads), S, Hq, D, block_tables.shape[1], NB,
         DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], int(partition_size), ws_ptr, ws_bytes,
@@ -195,7 +196,7 @@ def decode_step(out, q, new_k, new_v, k_cache, v_cache, block_tables, context_le
     if workspace is not None:
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
     rc = lib().pkv_decode_step(
-        _reachable(out, "out"), _dev(q, "q"), _dev(new_k, "new_k"), _dev(new_v, "new_v"),
+        _reachable(out, "out"), _reachable(q, "q"), _dev(new_k, "new_k"), _dev(new_v, "new_v"),
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"),
         _dev(context_lens, "context_lens"), float(scale), int(block_size), int(num_kv_heads), S,
         Hq, D, block_tables.shape[1], NB, DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype],
@@ -245,7 +246,7 @@ def paged_decode_grouped(out, q, k_cache, v_cache, block_tables, context_lens, g
     if workspace is not None:
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
     rc = lib().pkv_paged_decode_grouped(
-        _reachable(out, "out"), _dev(q, "q"), nk, nv, _dev(k_cache, "k_cache"),
+        _reachable(out, "out"), _reachable(q, "q"), nk, nv, _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables"), _dev(context_lens, "context_lens"),
         _dev(group_start, "group_start"), _dev(shared_tokens, "shared_tokens"), G,
@@ -314,7 +315,8 @@ def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, conte
             context_lens.dtype != torch.int32 or block_tables.shape[0] != S:
         raise ValueError("paged_decode_attention_noalloc: bad out/table/length tensors")
     rc = lib().pkv_paged_decode_attention_noalloc(
-        _reachable(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _reachable(out, "out"), _reachable(q, "q"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables"), _dev(context_lens, "context_lens"), float(scale),
         int(block_size), int(num_kv_heads), S, Hq, D, block_tables.shape[1], NB,
         DTYPE_CODE[q.dtype], DTYPE_CODE[out.dtype], int(partition_size), _stream(stream))

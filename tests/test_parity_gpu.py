@@ -1348,9 +1348,10 @@ def test_unsplit_launch_of_many_items(dt, Hq, Hkv, D, B, plan):
 
 
 @pytest.mark.parametrize("call", ["unsplit", "split", "step", "grouped"])
-def test_output_written_to_pinned_host_memory(call):
-    # out may be pinned host memory: the kernel stores the rows over the
-    # host link; the result is the same bits as with a device output
+def test_query_and_output_in_pinned_host_memory(call):
+    # q and out may be pinned host memory: the kernel loads q and stores the
+    # output rows over the host link; the result is the same bits as with
+    # device tensors
     lengths = [1, 700, 33, 2049, 0, 1500]
     w = Workload(0, "hostout", "bf16", 32, 8, 128, 16, len(lengths), "fixed",
                  writes_new_token=(call == "step"))
@@ -1360,7 +1361,8 @@ def test_output_written_to_pinned_host_memory(call):
     outs = []
     for host in (False, True):
         kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
-        q, bt, cl = case.q.to(DEV), case.block_tables.to(DEV), case.context_lens.to(DEV)
+        q = case.q.pin_memory() if host else case.q.to(DEV)
+        bt, cl = case.block_tables.to(DEV), case.context_lens.to(DEV)
         out = torch.full((S, Hq, D), float("nan"), dtype=torch.float32)
         out = out.pin_memory() if host else out.to(DEV)
         if call == "grouped":
