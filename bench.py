@@ -490,8 +490,12 @@ def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gpar
     if st.slots is not None and rank == 0:
         line["host_allocator"] = host_allocator_timing(st, pkv, grouped)
         if e2e_alloc and not args.no_e2e and not grouped:
-            line["e2e_with_allocator"] = e2e_with_allocator(pkv, st, dev, max(1, min(steps, 50)),
-                                                            graphs=not args.no_graph)
+            ka = max(1, min(steps, 50))
+            ea = e2e_with_allocator(pkv, st, dev, ka, graphs=not args.no_graph)
+            ed = e2e_with_allocator(pkv, st, dev, ka, graphs=not args.no_graph, direct=True)
+            ea["direct_io"] = {k_: ed[k_] for k_ in ("value", "unit", "ms_per_step",
+                                                       "host_plan_us_per_step", "what")}
+            line["e2e_with_allocator"] = ea
     return line
 
 
@@ -652,7 +656,7 @@ def capture_step_graph(body, dev):
     return graph
 
 
-def e2e_with_allocator(pkv, st, dev, k, graphs=True):
+def e2e_with_allocator(pkv, st, dev, k, graphs=True, direct=False):
     """End to end with the host side of every step in the timed region, as a
     serving loop runs it: the library's allocator reserves each sequence's
     next slot (pkv_step_append_tables: new blocks, copy-on-write decisions)
@@ -664,7 +668,10 @@ def e2e_with_allocator(pkv, st, dev, k, graphs=True):
     step's output).  Each step's copies and calls are one CUDA graph launch
     (one graph per input buffer, captured from the public calls).  Lengths
     grow one token a step per sequence, as in serving, so the tables get
-    spare columns and the KV bytes are summed over the steps."""
+    spare columns and the KV bytes are summed over the steps.  With `direct`,
+    the decode call reads q from the pinned input buffer and writes its output
+    to pinned host memory itself (NVLink-C2C), and only the rest of the
+    buffer is copied."""
     w = st.w
     B = w.block_size
     S = st.q.shape[0]
@@ -694,15 +701,22 @@ def e2e_with_allocator(pkv, st, dev, k, graphs=True):
             .view(S, maxb)
         b_["h_lens"] = h_pack[offs[2]:offs[2] + S * 4].view(torch.int32)
         b_["h_pairs"] = h_pack[offs[3]:offs[3] + S * 16].view(torch.int64).view(S, 2)
+        b_["h_q"] = h_pack[:st.q.numel() * st.q.element_size()].view(st.q.dtype).view(st.q.shape)
+        b_["rest"] = offs[1]
         bufs.append(b_)
 
     def body(b_, sm, n_pairs=0):
-        b_["d_pack"].copy_(b_["h_pack"], non_blocking=True)
+        if direct:
+            b_["d_pack"][b_["rest"]:].copy_(b_["h_pack"][b_["rest"]:], non_blocking=True)
+        else:
+            b_["d_pack"].copy_(b_["h_pack"], non_blocking=True)
         if n_pairs:
             pkv.kv_copy_blocks(kc, vc, b_["pairs_d"][:n_pairs], stream=sm)
-        pkv.decode_step(out, b_["q"], b_["nk"], b_["nv"], kc, vc, b_["bt"], b_["cl"], w.scale, B,
-                        w.num_kv_heads, partition_size=0, stream=sm)
-        h_out.copy_(out, non_blocking=True)
+        pkv.decode_step(h_out if direct else out, b_["h_q"] if direct else b_["q"], b_["nk"],
+                        b_["nv"], kc, vc, b_["bt"], b_["cl"], w.scale, B, w.num_kv_heads,
+                        partition_size=0, stream=sm)
+        if not direct:
+            h_out.copy_(out, non_blocking=True)
 
     # captured while the lengths are 0: the capture's runs write and read nothing
     for b_ in bufs:
@@ -751,8 +765,11 @@ def e2e_with_allocator(pkv, st, dev, k, graphs=True):
             "graphs": graphed,
             "what": "pkv_step_append_tables (slots, new blocks, CoW decisions; tables and "
                     "lengths patched in place) for step i+1 on the host while the device runs "
-                    "step i; per step one H2D copy of the pinned inputs + decode_step + output "
-                    "D2H + synchronise; lengths grow one token a step"}
+                    "step i; per step " +
+                    ("one H2D copy of the pinned inputs but q, decode_step reading q from and "
+                     "writing its output to pinned host memory" if direct else
+                     "one H2D copy of the pinned inputs + decode_step + output D2H") +
+                    " + synchronise; lengths grow one token a step"}
 
 
 def pack_inputs(tensors, dev):
