@@ -1393,6 +1393,67 @@ def test_query_and_output_in_pinned_host_memory(call):
     assert max_err(outs[1], ref) <= TOL16
 
 
+def _relayout(case, B_new, seed):
+    """The same logical K/V of every sequence in a fresh pool of block size
+    B_new, in a random physical order, unused slots NaN."""
+    S = len(case.lengths)
+    _, Hkv, B, D = case.k_cache.shape
+    g = torch.Generator().manual_seed(seed)
+    need = [-(-int(L) // B_new) for L in case.lengths]
+    NB = sum(need) + 5
+    perm = torch.randperm(NB, generator=g)
+    maxb = max(max(need), 1)
+    tables = torch.full((S, maxb), -1, dtype=torch.int32)
+    kc = torch.full((NB, Hkv, B_new, D), float("nan"), dtype=case.k_cache.dtype)
+    vc = torch.full_like(kc, float("nan"))
+    nxt = 0
+    for s_, L in enumerate(case.lengths):
+        L = int(L)
+        pos = torch.arange(L)
+        old = case.block_tables[s_, (pos // B).long()].long()
+        ks = case.k_cache[old, :, (pos % B).long()]  # [L, Hkv, D]
+        vs = case.v_cache[old, :, (pos % B).long()]
+        ids = perm[nxt:nxt + need[s_]]
+        nxt += need[s_]
+        tables[s_, :need[s_]] = ids.to(torch.int32)
+        new = ids[(pos // B_new).long()]
+        kc[new, :, (pos % B_new).long()] = ks
+        vc[new, :, (pos % B_new).long()] = vs
+    return kc, vc, tables
+
+
+@pytest.mark.parametrize("D,P", [(128, 0), (128, 512), (64, 0), (64, 256)])
+def test_paging_changes_storage_not_output_bits(D, P):
+    # Paging changes where K/V live, not what attention reads: the same
+    # logical K/V in pools of block size 8, 16 and 32, each in its own random
+    # physical order, give the decode kernel's output bit for bit (a stage
+    # holds the same tokens at every block size), within the tolerance of
+    # the oracle.
+    lengths = [1, 15, 16, 17, 300, 1000, 2049, 513]
+    w = Workload(0, "paging", "bf16", 32, 8, D, 16, len(lengths), "fixed")
+    case = make_decode_case(w, seed=D + P, lengths=lengths)
+    S, Hq, _ = case.q.shape
+    outs = []
+    for i, Bn in enumerate((16, 8, 32, 16)):
+        kc, vc, bt = _relayout(case, Bn, seed=i + 1)
+        out = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+        ws = None
+        if P:
+            ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, bt.shape[1] * Bn, P),
+                             dtype=torch.uint8, device=DEV)
+        pkv.paged_decode_attention(out, case.q.to(DEV), kc.to(DEV), vc.to(DEV), bt.to(DEV),
+                                   case.context_lens.to(DEV), w.scale, Bn, 8, partition_size=P,
+                                   workspace=ws)
+        torch.cuda.synchronize()
+        assert pkv.device_status() == 0
+        outs.append(out.cpu())
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, 16, 8)
+    assert max_err(outs[0], ref) <= TOL16
+
+
 def test_decode_calls_replayed_from_a_cuda_graph():
     # The decode calls (split with the plan, unsplit with the plan, the decode
     # step) captured once in a CUDA graph and replayed: each replay matches the
