@@ -415,6 +415,7 @@ def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gpar
         e2e = end_to_end(g, st, dev, max(1, min(steps, 50)), graphs=not args.no_graph)
     launches = g.launches_per_step
     g_pairs = int(g.pairs.shape[0])  # copy-on-write copies in the step
+    gpu_out = g.out.cpu()  # the step's output, for the oracle comparison of the CPU baseline
     del g
     torch.cuda.empty_cache()
 
@@ -484,6 +485,7 @@ def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gpar
                                "tensor-core decode" +
                                (" (new K/V appended inside)" if st.slots is not None else ""),
         "timing": "events around each kernel (adds the gaps the back-to-back region avoids)"}
+    line["_gpu_out"] = gpu_out
     if st.unique_blocks is not None:
         line["pct_hbm_peak_unique_bytes"] = round(
             100 * st.unique_bytes / (attn_avg * 1e-3) / 1e9 / peak, 2)
@@ -515,9 +517,10 @@ def run_gpu(args, rank, world, local_rank):
     gparts = args.group_parts if grouped else 1
     line = measure(pkv, st, args, rank, world, local_rank, args.steps, args.warmup, grouped,
                    gparts, e2e_alloc=True)
+    gout = line.pop("_gpu_out")
     if cpu:
-        line["cpu_baseline"] = cpu_baseline(st, args.cpu_budget)
-    del st
+        line["cpu_baseline"] = cpu_baseline(st, args.cpu_budget, gout)
+    del st, gout
     extra = [] if args.extra in ("", "none") else [int(x) for x in args.extra.split(",")]
     if extra:
         line["workloads"] = {}
@@ -531,8 +534,9 @@ def run_gpu(args, rank, world, local_rank):
         lx = measure(pkv, sx, args, rank, world, local_rank, args.steps, args.warmup, gx, 1)
         for k_ in ("metric", "higher_is_better", "scaling", "vs_baseline", "n_gpus", "data"):
             lx.pop(k_, None)
+        gx_out = lx.pop("_gpu_out")
         if cpu:
-            lx["cpu_baseline"] = cpu_baseline(sx, args.cpu_budget_extra)
+            lx["cpu_baseline"] = cpu_baseline(sx, args.cpu_budget_extra, gx_out)
         line["workloads"][str(key)] = lx
         del sx
     return line
@@ -853,10 +857,13 @@ def cpu_model() -> str:
     return platform.machine()
 
 
-def _oracle_rate(st, kc, vc, budget_s, threads):
+def _oracle_rate(st, kc, vc, budget_s, threads, gpu_out=None, err=None):
     """Passes of the oracle over the step's sequences (copies, write and
     attention) with `threads` threads until `budget_s` of CPU time is used:
-    (KV GB/s, bytes, seconds, passes, chunk)."""
+    (KV GB/s, bytes, seconds, passes, chunk).  With `gpu_out` (the GPU step's
+    output), each sequence the first pass computes is compared with it,
+    outside the timed region: err gets the largest absolute difference and
+    the number of sequences compared."""
     import oracle
     w = st.w
     S = st.q.shape[0]
@@ -872,9 +879,14 @@ def _oracle_rate(st, kc, vc, budget_s, threads):
                     oracle.kv_copy_blocks(kc, vc, st.pairs)
                 if st.slots is not None:
                     oracle.kv_write(kc, vc, st.new_key, st.new_value, st.slots, w.block_size)
-            oracle.paged_decode_attention(st.q[idx], kc, vc, st.tables[idx], st.lens[idx],
-                                          w.scale, w.block_size, w.num_kv_heads, nthreads=threads)
+            ref = oracle.paged_decode_attention(st.q[idx], kc, vc, st.tables[idx], st.lens[idx],
+                                                w.scale, w.block_size, w.num_kv_heads,
+                                                nthreads=threads)
             t_used += time.perf_counter() - t
+            if gpu_out is not None and passes == 0:
+                d = np.abs(gpu_out[idx].double().numpy() - np.asarray(ref)).max()
+                err["max_abs_err"] = max(err.get("max_abs_err", 0.0), float(d))
+                err["sequences"] = err.get("sequences", 0) + len(idx)
             done_bytes += int(L[idx].sum()) * 2 * w.num_kv_heads * w.head_dim * \
                 w.torch_dtype.itemsize
             if t_used >= budget_s:
@@ -883,26 +895,33 @@ def _oracle_rate(st, kc, vc, budget_s, threads):
     return done_bytes / t_used / 1e9, done_bytes, t_used, passes, chunk
 
 
-def cpu_baseline(st, budget_s=8.0):
+def cpu_baseline(st, budget_s=8.0, gpu_out=None):
     """Time the oracle (as it stands) on this host's cores on a bounded sample
     of the same step: passes over the step's sequences (write + attention)
     until the budget is used, on every core, then on one core (a third of
-    the budget)."""
+    the budget).  With the GPU step's output, the sequences the oracle
+    computed are compared with it (max abs error beside the timing)."""
     import oracle
     w = st.w
     n = os.cpu_count() or 1
     kc, vc = st.k_cache.clone(), st.v_cache.clone()
     if st.setup_slots is not None:
         oracle.kv_write(kc, vc, st.setup_keys, st.setup_vals, st.setup_slots, w.block_size)
-    v, nb, t, passes, chunk = _oracle_rate(st, kc, vc, budget_s, n)
+    err = {}
+    v, nb, t, passes, chunk = _oracle_rate(st, kc, vc, budget_s, n, gpu_out, err)
     v1, nb1, t1, _, _ = _oracle_rate(st, kc, vc, max(1.0, budget_s / 3), 1)
-    return {"value": round(v, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+    out = {"value": round(v, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
             "cpu_model": cpu_model(),
             "sample": "%.2f GB of the step's KV (%d pass(es) over chunks of %d sequences, "
                       "fp64 C oracle, %d threads, %.1f s)" % (nb / 1e9, passes, chunk, n, t),
             "single_core": {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
                             "sample": "%.2f GB of the step's KV, 1 thread, %.1f s" %
                                       (nb1 / 1e9, t1)}}
+    if err:
+        out["gpu_output_vs_oracle"] = {
+            "max_abs_err": err["max_abs_err"], "sequences": err["sequences"],
+            "of": int(st.q.shape[0]), "bound": 1e-5 if w.dtype == "f32" else 2e-3}
+    return out
 
 
 SWEEP_BLOCKS = (8, 16, 32)

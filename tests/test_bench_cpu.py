@@ -6,6 +6,7 @@ import subprocess
 import sys
 
 import pytest
+import torch
 
 import bench
 from workloads import WORKLOADS
@@ -87,3 +88,26 @@ def test_sweep_workloads_cover_the_sweep_grid():
                 assert w.num_kv_heads == 8 and w.dtype == "bf16"
                 seen.add(w.name)
     assert len(seen) == len(bench.SWEEP_BLOCKS) * len(bench.SWEEP_GROUPS) * len(bench.SWEEP_DIMS)
+
+
+def test_cpu_baseline_compares_the_gpu_output_with_the_oracle():
+    # The CPU-baseline leg computes the oracle's output for the sequences it
+    # times; given the GPU step's output it reports the largest difference.
+    # Here the "GPU output" is the oracle's own (difference 0) and then that
+    # output with one element moved by 0.25.
+    import numpy as np
+    import oracle
+    import paged_kv_cache_312_gb300 as pkv
+    st = bench.Step(1, 0, pkv.BlockAllocator)
+    w = st.w
+    ref = torch.from_numpy(np.asarray(oracle.paged_decode_attention(
+        st.q, st.k_cache, st.v_cache, st.tables, st.lens, w.scale, w.block_size,
+        w.num_kv_heads))).float()
+    cb = bench.cpu_baseline(st, 0.2, ref)
+    g = cb["gpu_output_vs_oracle"]
+    assert g["sequences"] == g["of"] == st.q.shape[0]
+    assert g["max_abs_err"] < 1e-6 and g["bound"] == 1e-5
+    bad = ref.clone()
+    bad[2, 1, 5] += 0.25
+    g = bench.cpu_baseline(st, 0.2, bad)["gpu_output_vs_oracle"]
+    assert abs(g["max_abs_err"] - 0.25) < 1e-6
