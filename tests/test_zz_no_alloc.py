@@ -14,7 +14,8 @@ attention tolerance of the other GPU tests) and against the regular entry
 point with a caller workspace.  The cases reach every layout the scratch
 takes: partitions spread over a CTA's four warps, one partition per warp
 (short partitions of long contexts), head slices of a wide query-head group,
-and the CUDA-core kernel with its separate log-sum-exp merge (fp32 KV).  It
+the CUDA-core kernel with its separate log-sum-exp merge (fp32 KV), and the
+equal pieces the work plan cuts near-equal contexts into.  It
 also checks that a request larger than the array is refused, and that a
 malformed request gets the same code as from the workspace entry point.  It
 must pass in a fresh process and after the other tests (the file name makes
@@ -49,6 +50,7 @@ CASES = [
     ("bf16", 16, 4, 128, 16, [2048, 3000, 17, 1200, 2100], 32, "one partition per warp"),
     ("bf16", 48, 2, 128, 16, [1500, 700, 2100, 16], 256, "head slices of a 24-head group"),
     ("f32", 8, 2, 64, 16, [1000, 33, 600, 0, 257], 128, "CUDA-core kernel + separate merge"),
+    ("bf16", 32, 8, 128, 32, [4096, 4000, 4050, 3990], 512, "pieces of near-equal contexts"),
 ]
 
 
