@@ -262,9 +262,11 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self, t_begin=None, t_end=None):
+    def stop(self, t_begin=None, t_end=None, t_load_end=None):
         """Stops sampling; summarises the samples taken between host wall
-        times t_begin and t_end (all samples if no window holds any)."""
+        times t_begin and t_load_end (the timed region and the same steps
+        kept running after it), or t_end without a load window, or else all
+        samples."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -286,8 +288,16 @@ class ClockSampler:
                              {n for n, v in zip(names, f[5:9]) if v.lower() == "active"}))
             except (ValueError, IndexError):
                 continue
-        inside = [r for r in rows if t_begin is None or t_begin - 0.05 <= r[0] <= t_end + 0.05]
-        window = "timed region" if inside else "around the timed region"
+        if t_load_end is not None:
+            inside = [r for r in rows if t_begin - 0.05 <= r[0] <= t_load_end + 0.05]
+            window = "timed region and the same steps run on, untimed, for %.1f s after it" % (
+                t_load_end - t_end)
+        else:
+            inside = [r for r in rows
+                      if t_begin is None or t_begin - 0.05 <= r[0] <= t_end + 0.05]
+            window = "timed region"
+        if not inside:
+            window = "around the timed region"
         use = inside or rows
         if not use:
             return None
@@ -384,7 +394,17 @@ def measure(pkv, st, args, rank, world, local_rank, steps, warmup, grouped, gpar
     t1.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
-    clk = clocks.stop(wall0, wall1) if clocks else None
+    # clocks under this load: a short timed region (K steps of 0.1-0.2 ms)
+    # holds no nvidia-smi sample (one every 100 ms), so the same step keeps
+    # running, untimed, for 0.4 s after it while the sampler runs on
+    wall2 = None
+    if clocks:
+        while time.time() - wall1 < 0.4:
+            for _ in range(50):
+                step()
+            torch.cuda.synchronize(dev)
+        wall2 = time.time()
+    clk = clocks.stop(wall0, wall1, wall2) if clocks else None
     total_ms = t0.elapsed_time(t1)
     if world > 1:
         torch.distributed.barrier()
