@@ -149,7 +149,9 @@ def decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, parti
 def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                            block_size, num_kv_heads, partition_size=0, workspace=None,
                            stream=None):
-    """out [S, Hq, D] = paged decode attention of q [S, Hq, D] over the caches."""
+    """out [S, Hq, D] = paged decode attention of q [S, Hq, D] over the caches.
+    q and out may be CUDA tensors or pinned host tensors (the kernel reads q
+    and writes out over the host link); the other tensors are CUDA tensors."""
     S, Hq, D = q.shape
     NB, Hkv, B, Dk = k_cache.shape
     if (Hkv, B, Dk) != (num_kv_heads, block_size, D) or v_cache.shape != k_cache.shape:
@@ -179,7 +181,8 @@ def decode_step(out, q, new_k, new_v, k_cache, v_cache, block_tables, context_le
                 block_size, num_kv_heads, partition_size=0, workspace=None, stream=None):
     """One decode step: new_k/new_v [S, Hkv, D] are written at position
     context_lens[s]-1 of each sequence, then out [S, Hq, D] = paged decode
-    attention of q over the updated caches."""
+    attention of q over the updated caches (q and out may be pinned host
+    tensors, as in paged_decode_attention)."""
     S, Hq, D = q.shape
     NB, Hkv, B, Dk = k_cache.shape
     if (Hkv, B, Dk) != (num_kv_heads, block_size, D) or v_cache.shape != k_cache.shape:
@@ -211,7 +214,8 @@ def paged_decode_grouped(out, q, k_cache, v_cache, block_tables, context_lens, g
     given) for groups of consecutive sequences sharing a prefix of physical
     blocks: group i is sequences group_start[i]..group_start[i+1]-1, whose
     first shared_tokens[i] positions use the same table entries.  Same
-    result as decode_step / paged_decode_attention for every sequence.
+    result as decode_step / paged_decode_attention for every sequence; q and
+    out may likewise be pinned host tensors.
     parts > 1 cuts each group's stage list over that many CTAs (merged in
     the launch); it needs a workspace of
     decode_workspace_bytes(S, Hq, D, parts, 1) bytes.  max_members bounds the
@@ -306,7 +310,8 @@ NOALLOC_SCRATCH_BYTES = 16 << 20
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                                    block_size, num_kv_heads, partition_size, stream=None):
     """Split-context decode whose scratch is the library's fixed device array
-    (for callers that cannot allocate device memory); see include/pkv.h."""
+    (for callers that cannot allocate device memory); q and out may be pinned
+    host tensors.  The C declaration in include/pkv.h gives the limits."""
     S, Hq, D = q.shape
     NB, Hkv, B, Dk = k_cache.shape
     if (Hkv, B, Dk) != (num_kv_heads, block_size, D) or v_cache.shape != k_cache.shape:
