@@ -526,6 +526,47 @@ def test_decode_step_matches_oracle(dt, Hq, Hkv, D, B, P, plan):
     assert max_err(out, ref) <= tol(w.torch_dtype)
 
 
+@pytest.mark.parametrize("P", [0, 512])
+def test_back_to_back_steps_see_each_others_writes(P):
+    # Two decode steps back to back on one stream, one workspace, no
+    # synchronisation between them: the second appends its token at the next
+    # position, attends over the cache the first one appended to, and takes
+    # the first one's bf16 output as its queries.  Each decode launch starts
+    # while the kernel before it runs, so it must read the cache and q only
+    # after waiting for that kernel.
+    B = 16
+    lengths = [5, 17, 700, 2049, 1001, 35]  # the next position stays in the last block
+    w = Workload(0, "chain", "bf16", 32, 8, 128, B, len(lengths), "fixed",
+                 writes_new_token=True)
+    case = make_decode_case(w, seed=31, lengths=lengths)
+    S, Hq, D = case.q.shape
+    g = torch.Generator().manual_seed(7)
+    nk2 = torch.randn(S, 8, D, generator=g).to(torch.bfloat16)
+    nv2 = torch.randn(S, 8, D, generator=g).to(torch.bfloat16)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    bt = case.block_tables.to(DEV)
+    cl1, cl2 = case.context_lens.to(DEV), (case.context_lens + 1).to(DEV)
+    out1 = torch.full((S, Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out2 = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, case.block_tables.shape[1] * B, P),
+                     dtype=torch.uint8, device=DEV)
+    pkv.decode_step(out1, case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV), kc, vc,
+                    bt, cl1, w.scale, B, 8, partition_size=P, workspace=ws)
+    pkv.decode_step(out2, out1, nk2.to(DEV), nv2.to(DEV), kc, vc, bt, cl2, w.scale, B, 8,
+                    partition_size=P, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+    ref1 = oracle.decode_step(case.q, case.new_key, case.new_value, k_ref, v_ref,
+                              case.block_tables, case.context_lens, w.scale, B, 8)
+    q2 = out1.cpu()  # the first step's output, as the second step took it
+    assert max_err(q2.float(), ref1) <= TOL16 + 2 ** -8 * float(np.abs(ref1).max())
+    ref2 = oracle.decode_step(q2, nk2, nv2, k_ref, v_ref, case.block_tables,
+                              case.context_lens + 1, w.scale, B, 8)
+    assert torch.equal(bits(kc), bits(k_ref)) and torch.equal(bits(vc), bits(v_ref))
+    assert max_err(out2, ref2) <= TOL16
+
+
 def test_decode_step_equals_write_then_attend_and_flags_bad_block():
     w = Workload(0, "step2", "bf16", 16, 4, 128, 16, 3, "fixed", writes_new_token=True)
     case = make_decode_case(w, seed=5, lengths=[33, 64, 200])
