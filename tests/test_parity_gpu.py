@@ -1496,6 +1496,66 @@ def test_paging_changes_storage_not_output_bits(D, P):
     assert max_err(outs[0], ref) <= TOL16
 
 
+def _random_decode_config(i):
+    """Configuration i of the seeded random sweep: dtype, heads, head_dim, block size,
+    lengths (ragged, or near-equal so that a split call gets pieces), split, plan, step."""
+    r = np.random.default_rng(1000 + i)
+    dt = ["bf16", "f16"][int(r.integers(2))]
+    Hkv = int(r.choice([1, 2, 4, 8]))
+    G = int(r.choice([1, 2, 4, 6, 8, 12, 16, 24, 32]))
+    D = int(r.choice([64, 128]))
+    B = int(r.choice([8, 16, 32]))
+    S = int(r.integers(1, 24))
+    if r.random() < 0.4:  # near-equal contexts
+        base = int(r.integers(40, 900))
+        lengths = [base + int(x) for x in r.integers(0, max(1, base // 12), size=S)]
+    else:
+        lengths = [int(x) for x in r.integers(0, 1200, size=S)]
+    P = int(r.choice([0, 0, 0, B, 2 * B, 8 * B, 16 * B]))
+    plan = bool(r.integers(2)) if P == 0 else True
+    step = bool(r.integers(2))
+    if step:
+        lengths = [max(1, L) for L in lengths]
+    return dt, Hkv * G, Hkv, D, B, lengths, P, plan, step
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_random_decode_configurations(i):
+    # Seeded random configurations crossing the launch choices (work plan or
+    # not, partition groups or pieces, deep or 2-stage rings, one or two
+    # column tiles or head slices, decode step or attention) against the oracle.
+    dt, Hq, Hkv, D, B, lengths, P, plan, step = _random_decode_config(i)
+    w = Workload(0, "random", dt, Hq, Hkv, D, B, len(lengths), "fixed", writes_new_token=step)
+    case = make_decode_case(w, seed=i, lengths=lengths)
+    S = len(lengths)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    out = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    ws = None
+    if P or plan:
+        ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, case.block_tables.shape[1] * B, P),
+                         dtype=torch.uint8, device=DEV)
+    args = (case.block_tables.to(DEV), case.context_lens.to(DEV), w.scale, B, Hkv)
+    if step:
+        pkv.decode_step(out, case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV), kc, vc,
+                        *args, partition_size=P, workspace=ws)
+    else:
+        pkv.paged_decode_attention(out, case.q.to(DEV), kc, vc, *args, partition_size=P,
+                                   workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    if step:
+        k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+        ref = oracle.decode_step(case.q, case.new_key, case.new_value, k_ref, v_ref,
+                                 case.block_tables, case.context_lens, w.scale, B, Hkv)
+        assert torch.equal(bits(kc), bits(k_ref)) and torch.equal(bits(vc), bits(v_ref))
+    else:
+        ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache,
+                                            case.block_tables, case.context_lens, w.scale, B,
+                                            Hkv)
+    assert max_err(out, ref) <= TOL16, (dt, Hq, Hkv, D, B, P, plan, step)
+    assert bool(torch.isfinite(out).all())
+
+
 def test_decode_calls_replayed_from_a_cuda_graph():
     # The decode calls (split with the plan, unsplit with the plan, the decode
     # step) captured once in a CUDA graph and replayed: each replay matches the
