@@ -627,7 +627,32 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         const float sl = p.scale_log2;
         const bool vec = (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
         uint8_t* qx = smem + x * Gm::Q_BYTES;
+        // This thread's row of item it2's Q into shared memory by asynchronous
+        // 16-byte copies (zeros past qn), and the wait that makes them visible
+        // to the tensor cores before the hand-over to the MMA warp.
+        auto issue_q = [&](const Item& it2) {
+            const int row2 = it2.q0 + x * kTileRows + r;
+            const bool have = row2 < it2.qn;
+            const T* src = static_cast<const T*>(p.q) +
+                           ((size_t)(it2.r0 + (have ? row2 : 0)) * p.num_heads + it2.h) * D;
+            const uint32_t bytes = have ? 16u : 0u;
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                                 smem_u32(qx + (c >> 3) * Gm::HALF_Q + swz(r, c & 7))),
+                             "l"(src + c * 8), "r"(bytes)
+                             : "memory");
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        auto hand_over_q = [&]() {
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            fence_proxy_async();
+            tmem_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&q_full[x]));
+        };
         int n = 0, kt0 = 0;
+        int preloaded = -1;  // the item whose Q the previous epilogue already brought in
         for (int v = blockIdx.x; v < total_items && ok; v += gridDim.x) {
             Item it;
             if (!decode_item<B>(p, items_x, v, it)) continue;
@@ -635,20 +660,13 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             const int row = it.q0 + x * kTileRows + r;
             const int pos = row < it.qn ? it.base_pos + row : -1;  // -1: padding row
             if (my_nkt > 0) {
-                // this row of Q into shared memory (zero past qn); the S MMAs of
-                // this tile's previous item finished before its last softmax
-                const T* src = static_cast<const T*>(p.q) +
-                               ((size_t)(it.r0 + row) * p.num_heads + it.h) * D;
-#pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
-                    uint4 q4 = make_uint4(0u, 0u, 0u, 0u);
-                    if (row < it.qn) q4 = *reinterpret_cast<const uint4*>(src + c * 8);
-                    *reinterpret_cast<uint4*>(qx + (c >> 3) * Gm::HALF_Q + swz(r, c & 7)) = q4;
+                // this row of Q into shared memory (zero past qn), unless this
+                // tile's previous item's epilogue did it; the S MMAs of that item
+                // finished before its last softmax
+                if (preloaded != v) {
+                    issue_q(it);
+                    hand_over_q();
                 }
-                fence_proxy_async();
-                tmem_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&q_full[x]));
                 // the next item's Q row of this thread into L2 meanwhile
                 {
                     Item nx;
@@ -771,6 +789,14 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
             if (my_nkt > 0) {
                 wait(&o_full[x], (n - 1) & 1);
                 tmem_fence_after();
+                // the next item in which this tile has rows: its Q comes in while
+                // O is read out (this item's last S on this tile has completed)
+                Item nx;
+                int vn = v + gridDim.x;
+                for (; vn < total_items; vn += gridDim.x)
+                    if (decode_item<B>(p, items_x, vn, nx) && (x ? nx.nkt_b : nx.nkt_a) > 0) break;
+                const bool early = ok && vn < total_items;
+                if (early) issue_q(nx);
                 const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -784,6 +810,10 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                                     o, p.out_dtype, vec);
                 }
                 tmem_fence_before();
+                if (early) {
+                    hand_over_q();
+                    preloaded = vn;
+                }
             }
             kt0 += it.nkt;
         }
