@@ -971,6 +971,8 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     peak, _ = measured_peaks()
     stream = torch.cuda.current_stream(dev)
+    wide = {"tcgen05": pkv.WIDE_TCGEN05, "head_slices": pkv.WIDE_HEAD_SLICES}[args.wide_kernel]
+    pkv.set_wide_group_kernel(wide)
     blocks, groups, dims = SWEEP_BLOCKS, SWEEP_GROUPS, SWEEP_DIMS
     if args.sweep_point:
         pb, pg, pd = (int(x) for x in args.sweep_point.split(","))
@@ -1017,7 +1019,8 @@ def run_sweep(args):
                 ms = timed[best]
                 line = {"sweep": {"block_size": B, "group": G, "head_dim": D,
                                   "num_heads": w.num_heads, "num_kv_heads": 8,
-                                  "partition_size": best, "work_plan": True},
+                                  "partition_size": best, "work_plan": True,
+                                  "wide_group_kernel": args.wide_kernel},
                         "attn_ms": round(ms, 5), "kv_bytes": kv,
                         "attn_gbs": round(kv / (ms * 1e-3) / 1e9, 1),
                         "frac_of_measured_peak": round(kv / (ms * 1e-3) / 1e9 / peak, 4),
@@ -1314,6 +1317,9 @@ def main():
                          "(one JSON line per point; not the benchmark line)")
     ap.add_argument("--sweep-point", default=None, metavar="B,G,D",
                     help="with --sweep: time only this block size, group and head_dim")
+    ap.add_argument("--wide-kernel", default="tcgen05", choices=("tcgen05", "head_slices"),
+                    help="with --sweep: kernel of unsplit launches with G a multiple of 32 at "
+                         "head_dim 128 (the tcgen05 kernel, or head slices on mma.sync)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

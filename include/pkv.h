@@ -432,6 +432,26 @@ int pkv_selftest_bounded_wait(int num_ctas, unsigned int* drained, void* stream)
 int pkv_set_decode_kernel(int which);
 
 /*
+ * Kernel for unsplit decode of wide query-head groups (process-wide): with
+ * G = num_heads / num_kv_heads a multiple of 32, head_dim 128, 16-bit KV,
+ * block size 8, 16 or 32, q 16-byte aligned and partition_size 0 (outside
+ * beam groups),
+ * PKV_WIDE_TCGEN05 (default) runs the 5th-generation tensor-core kernel: a
+ * K/V tile's 128 tokens are the MMA's M and 32 query heads its N, one
+ * persistent CTA a SM, the work plan's longest-first order when a workspace
+ * is given (pkv_decode_workspace_bytes with partition_size 0; its bytes 0-4
+ * and 64-68 are the plan's count and the kernel's record counter).
+ * PKV_WIDE_HEAD_SLICES runs the mma.sync kernel on head slices of 16 query
+ * heads (also used for every other shape).  Both compute the same result up
+ * to fp32 accumulation order.  With new_k / new_v (pkv_decode_step) the
+ * tcgen05 path writes the new tokens in a kernel of its own first.  Returns
+ * PKV_ERR_SHAPE for an unknown value.
+ */
+#define PKV_WIDE_TCGEN05 0
+#define PKV_WIDE_HEAD_SLICES 1
+int pkv_set_wide_group_kernel(int which);
+
+/*
  * Kernel selection for pkv_paged_prefill_attention (process-wide):
  * PKV_PREFILL_TCGEN05 (default) runs the 5th-generation tensor-core kernel
  * (tcgen05 MMAs with S, P and O in tensor memory, 256 query rows per CTA,

@@ -20,6 +20,7 @@ PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
 DTYPE_CODE = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
 KERNEL_AUTO, KERNEL_CUDA_CORE = 0, 1
 PREFILL_TCGEN05, PREFILL_WARP_MMA = 0, 1
+WIDE_TCGEN05, WIDE_HEAD_SLICES = 0, 1
 STATUS_BITS = {1: "bad block id", 2: "bad context length", 4: "bad slot", 8: "bad copy pair",
                16: "wait timeout"}
 
@@ -52,6 +53,7 @@ _SIGS = {
     "pkv_set_decode_kernel": (_I, [_I]),
     "pkv_selftest_bounded_wait": (_I, [_I, _P, _P]),
     "pkv_set_prefill_kernel": (_I, [_I]),
+    "pkv_set_wide_group_kernel": (_I, [_I]),
     "pkv_alloc_create": (_I, [_I, _I, _P, ctypes.POINTER(_P)]),
     "pkv_alloc_destroy": (_I, [_P]),
     "pkv_seq_add": (_I, [_P, _I64, _I]),
@@ -389,6 +391,12 @@ def selftest_bounded_wait(num_ctas, drained, stream=None):
 
 def set_decode_kernel(which):
     _check(lib().pkv_set_decode_kernel(int(which)), "pkv_set_decode_kernel")
+
+
+def set_wide_group_kernel(which):
+    """Kernel for unsplit decode of groups of 32 k query heads: 0 the tcgen05
+    kernel (default), 1 head slices on the mma.sync kernel."""
+    _check(lib().pkv_set_wide_group_kernel(int(which)), "pkv_set_wide_group_kernel")
 
 
 def set_prefill_kernel(which):

@@ -23,6 +23,7 @@ namespace {
 thread_local char g_err[512] = "";
 int g_decode_kernel = PKV_KERNEL_AUTO;
 int g_prefill_kernel = PKV_PREFILL_TCGEN05;
+int g_wide_kernel = PKV_WIDE_TCGEN05;
 }  // namespace
 
 int pkv_fail(int code, const char* fmt, ...)
@@ -139,7 +140,10 @@ struct WorkspaceLayout {
 
 // Optional workspace of an unsplit launch: the work plan alone (record
 // count, then one record per (sequence, KV head x head slice)).
+// Optional workspace of an unsplit launch: the plan's record count at byte 0,
+// the wide-group kernel's record counter at byte 64, records from byte 256.
 size_t plan_bytes(size_t S, size_t H) { return 256 + S * H * 16; }
+constexpr size_t kPlanNextOffset = 64;
 
 WorkspaceLayout workspace_layout(size_t S, size_t H, size_t P, size_t D)
 {
@@ -165,6 +169,14 @@ int pkv_set_decode_kernel(int which)
     if (which != PKV_KERNEL_AUTO && which != PKV_KERNEL_CUDA_CORE)
         return pkv_fail(PKV_ERR_SHAPE, "pkv_set_decode_kernel: unknown value %d", which);
     g_decode_kernel = which;
+    return PKV_OK;
+}
+
+int pkv_set_wide_group_kernel(int which)
+{
+    if (which != PKV_WIDE_TCGEN05 && which != PKV_WIDE_HEAD_SLICES)
+        return pkv_fail(PKV_ERR_SHAPE, "pkv_set_wide_group_kernel: unknown value %d", which);
+    g_wide_kernel = which;
     return PKV_OK;
 }
 
@@ -381,6 +393,74 @@ int pkv_decode_check(const char* fn, int kv_dtype, int out_dtype, int num_seqs, 
 
 namespace {
 
+int sm_count_of_device()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 0;
+    return sms;
+}
+
+// Unsplit decode of groups of 32 k query heads on the tcgen05 kernel: the
+// step's append first (its own kernel), then the plan when a workspace came
+// with the call (records longest first, the kernel's counter zeroed), then
+// the persistent kernel.
+int decode_wide(const char* fn, DecodeParams& p, int kv_dtype, const void* k_cache,
+                const void* v_cache, const void* new_k, const void* new_v, int* plan_count,
+                int4* plan_items, cudaStream_t st)
+{
+    const int G = p.num_heads / p.num_kv_heads;
+    p.head_slices = G / kDecodeWideHeads;
+    CUtensorMap kmap, vmap;
+    const uint64_t rows = (uint64_t)p.num_blocks * p.num_kv_heads * p.block_size;
+    const int box_rows = p.block_size < 16 ? p.block_size : 16;
+    int rc = tensor_map(k_cache, rows, p.head_dim, box_rows, kv_dtype, &kmap);
+    if (rc == PKV_OK) rc = tensor_map(v_cache, rows, p.head_dim, box_rows, kv_dtype, &vmap);
+    if (rc != PKV_OK) return rc;
+    const long long items = (long long)p.num_seqs * p.num_kv_heads * p.head_slices;
+    if (items >= (1ll << 31)) return pkv_fail(PKV_ERR_SHAPE, "%s: more than 2^31 work items", fn);
+    cudaError_t e;
+    if (new_k != nullptr) {
+        e = launch_kv_append(const_cast<void*>(k_cache), const_cast<void*>(v_cache), new_k, new_v,
+                             p.block_tables, p.context_lens, p.num_seqs, p.max_blocks,
+                             p.num_blocks, p.num_kv_heads, p.head_dim, p.block_size,
+                             pkv_dtype_bytes(kv_dtype), p.status, st);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+    }
+    const int sms = sm_count_of_device();
+    if (plan_items != nullptr && p.num_seqs <= kPlanMaxSeqs) {
+        int* next = reinterpret_cast<int*>(reinterpret_cast<char*>(plan_count) + kPlanNextOffset);
+        DecodePlanParams pp;
+        pp.context_lens = p.context_lens;
+        pp.num_seqs = p.num_seqs;
+        pp.num_kv_heads = p.num_kv_heads;
+        pp.head_slices = p.head_slices;
+        pp.partition_tokens = p.partition_tokens;
+        pp.cta_parts = 1;
+        pp.stage_tokens = 128;
+        pp.slots = 0;
+        pp.max_groups = 1;
+        pp.max_len = p.max_blocks * p.block_size;
+        int shift = 0;
+        while ((pp.max_len >> shift) >= kPlanBuckets) ++shift;
+        pp.bucket_shift = shift;
+        pp.items = plan_items;
+        pp.item_count = plan_count;
+        pp.done = reinterpret_cast<unsigned*>(next);
+        pp.num_counters = 1;
+        e = launch_decode_plan(pp, st);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+        p.items = plan_items;
+        p.item_count = plan_count;
+        p.item_next = next;
+    }
+    e = launch_decode_wide_tcgen05(p, kv_dtype, &kmap, &vmap, (int)items, sms > 0 ? sms : 148,
+                                   st);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return PKV_OK;
+}
+
 // Decode attention, optionally with the step's append fused in (new_k and
 // new_v non-NULL: each sequence's new token goes to position
 // context_lens[s]-1 first).
@@ -455,6 +535,7 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
     p.num_groups = 0;
     p.items = nullptr;
     p.item_count = nullptr;
+    p.item_next = nullptr;
     int* plan_count = nullptr;
     int4* plan_items = nullptr;
     const int max_ctx = max_blocks_per_seq * block_size;
@@ -515,6 +596,10 @@ int decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
         int rc = tensor_map(k_cache, rows, head_dim, box_rows, kv_dtype, &kmap, 1);
         if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, box_rows, kv_dtype, &vmap, 1);
         if (rc != PKV_OK) return rc;
+        if (!grouped && p.max_partitions <= 1 && g_wide_kernel == PKV_WIDE_TCGEN05 &&
+            decode_wide_tcgen05_supported(kv_dtype, head_dim, block_size, G, q))
+            return decode_wide(fn, p, kv_dtype, k_cache, v_cache, new_k, new_v, plan_count,
+                               plan_items, st);
         if (grouped) {
             // one CTA per (beam group, KV head, part); each writes the new
             // tokens of its run

@@ -48,6 +48,9 @@ struct DecodeParams {
     // runs of the sequence's stages.  Written by the plan kernel just before.
     const int4* items;
     const int* item_count;
+    // Wide-group tcgen05 kernel with a work plan: CTAs take the records in
+    // order through this counter (zeroed by the plan kernel); NULL otherwise.
+    int* item_next;
 };
 
 // Work plan of a split tensor-core launch (decode_plan.cu): zeroes the
@@ -182,6 +185,20 @@ constexpr int kDecodeTcDeepMaxWaves = 2;
 cudaError_t launch_decode_tensor_core_deep(const DecodeParams& p, int kv_dtype, const void* k_map,
                                            const void* v_map, long long grid, bool wide,
                                            cudaStream_t stream);
+
+// Unsplit decode for groups of G = 32 k query heads per KV head on the
+// tcgen05 tensor cores (decode_tc05.cu): items (sequence, KV head, slice of
+// kDecodeWideHeads query heads), p.head_slices = G / kDecodeWideHeads, taken
+// by persistent CTAs (one a SM, at most `sms`) from p.items through
+// p.item_next when p.items is set, else in grid-stride order.  16-bit KV,
+// head_dim 128, block size 8, 16 or 32, q 16-byte aligned; a programmatic
+// dependent launch.
+constexpr int kDecodeWideHeads = 32;
+bool decode_wide_tcgen05_supported(int kv_dtype, int head_dim, int block_size, int group,
+                                   const void* q);
+cudaError_t launch_decode_wide_tcgen05(const DecodeParams& p, int kv_dtype, const void* k_map,
+                                       const void* v_map, int items, int sms,
+                                       cudaStream_t stream);
 
 // Tensor-core decode over beam groups: one CTA per (group, KV head, part),
 // grid num_groups * num_kv_heads * p.max_partitions, the parts of one (group,

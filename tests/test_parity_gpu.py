@@ -1606,3 +1606,180 @@ def test_decode_calls_replayed_from_a_cuda_graph():
         q_host = torch.randn(q_host.shape, generator=torch.Generator().manual_seed(rep)) \
             .to(torch.bfloat16)
         q.copy_(q_host)
+
+
+# --------------------------------------------------------------------------
+# Wide query-head groups (G a multiple of 32, head_dim 128, unsplit): the
+# tcgen05 kernel, against the oracle and against the head-slice kernel
+# --------------------------------------------------------------------------
+
+WIDE_LENGTHS = [1, 127, 128, 129, 0, 700, 2049, 4100, 255, 33]
+
+
+def wide_decode(case, w, kc, vc, which, plan, out_dtype=torch.float32, q=None, out=None):
+    pkv.set_wide_group_kernel(which)
+    try:
+        return gpu_decode(case.q if q is None else q, kc, vc, case.block_tables,
+                          case.context_lens, w.scale, w.block_size, w.num_kv_heads,
+                          out_dtype=out_dtype, plan=plan)
+    finally:
+        pkv.set_wide_group_kernel(pkv.WIDE_TCGEN05)
+
+
+@pytest.mark.parametrize("dt,G,Hkv,B", [("bf16", 32, 2, 16), ("f16", 32, 1, 8),
+                                         ("bf16", 64, 2, 32), ("f16", 96, 1, 16),
+                                         ("bf16", 32, 8, 8)])
+@pytest.mark.parametrize("plan", [False, True])
+def test_wide_groups_tcgen05_match_oracle_and_head_slices(dt, G, Hkv, B, plan):
+    # ragged lengths around the 128-token tile (1, 127, 128, 129, ...), an
+    # empty sequence, NaN in every unused cache slot; with and without the
+    # work plan (records taken through the kernel's counter)
+    w = Workload(0, "wide", dt, G * Hkv, Hkv, 128, B, len(WIDE_LENGTHS), "fixed")
+    case = make_decode_case(w, seed=G + B + Hkv, lengths=WIDE_LENGTHS)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, B, Hkv)
+    for which in (pkv.WIDE_TCGEN05, pkv.WIDE_HEAD_SLICES):
+        out = wide_decode(case, w, kc, vc, which, plan)
+        assert pkv.device_status() == 0, which
+        assert max_err(out, ref) <= TOL16, which
+        assert torch.equal(out[4].cpu(), torch.zeros_like(out[4].cpu()))  # length 0
+
+
+@pytest.mark.parametrize("plan", [False, True])
+def test_wide_groups_many_items_per_cta(plan):
+    # 600 items (300 sequences x 2 KV heads) over at most one CTA a SM: each
+    # CTA runs several items back to back through both Q buffers, among them
+    # one-token and empty ones
+    lengths = [int(x) for x in np.random.default_rng(4).integers(0, 600, size=300)]
+    lengths[:5] = [1, 0, 0, 1, 128]
+    w = Workload(0, "wide_many", "bf16", 64, 2, 128, 16, len(lengths), "fixed")
+    case = make_decode_case(w, seed=8, lengths=lengths)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, 16, 2)
+    out = wide_decode(case, w, kc, vc, pkv.WIDE_TCGEN05, plan)
+    assert pkv.device_status() == 0
+    assert max_err(out, ref) <= TOL16
+
+
+@pytest.mark.parametrize("rising", [True, False])
+def test_wide_groups_running_max_moves(rising):
+    # keys scaled up (or down) along each context, so that the per-head max
+    # rises by more than the 2^8 margin several times mid-sequence (O^T and
+    # the partial sums are then rescaled) -- or is set by the first tile
+    lengths = [2049, 900, 3000]
+    w = Workload(0, "wide_max", "bf16", 32, 1, 128, 16, len(lengths), "fixed")
+    case = make_decode_case(w, seed=31, lengths=lengths)
+    kc = case.k_cache.float()
+    for s, L in enumerate(lengths):
+        for pos in range(L):
+            f = 1.0 + 7.0 * pos / L
+            kc[case.block_tables[s, pos // 16], :, pos % 16] *= f if rising else 8.0 / f
+    case.k_cache.copy_(kc.to(case.k_cache.dtype))
+    dk, dv = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, 16, 1)
+    out = wide_decode(case, w, dk, dv, pkv.WIDE_TCGEN05, True)
+    assert pkv.device_status() == 0
+    assert max_err(out, ref) <= TOL16
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
+def test_wide_groups_16bit_outputs(out_dtype):
+    # rounded once to the output dtype, as in test_16bit_outputs
+    w = Workload(0, "wide_o", "bf16", 64, 2, 128, 16, 4, "fixed")
+    case = make_decode_case(w, seed=6, lengths=[5, 300, 129, 1000])
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, 16, 2)
+    out = wide_decode(case, w, kc, vc, pkv.WIDE_TCGEN05, False, out_dtype=out_dtype)
+    rel = 2.0 ** -8 if out_dtype == torch.bfloat16 else 2.0 ** -11
+    diff = np.abs(out.cpu().double().numpy() - ref)
+    assert (diff <= TOL16 + rel * np.abs(ref)).all()
+
+
+def test_wide_groups_bad_block_and_length_are_flagged():
+    w = Workload(0, "wide_bad", "bf16", 32, 1, 128, 16, 3, "fixed")
+    case = make_decode_case(w, seed=19, lengths=[300, 300, 300])
+    bt = case.block_tables.clone()
+    bt[1, 3] = case.num_blocks + 5
+    cl = case.context_lens.clone()
+    cl[2] = bt.shape[1] * 16 + 1
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_decode_attention(case.q[:1], case.k_cache, case.v_cache, bt[:1], cl[:1],
+                                        w.scale, 16, 1)
+    for plan in (False, True):
+        pkv.set_wide_group_kernel(pkv.WIDE_TCGEN05)
+        out = gpu_decode(case.q, kc, vc, bt, cl, w.scale, 16, 1, plan=plan)
+        st = pkv.device_status(reset=True)
+        assert st & 1 and st & 2
+        assert max_err(out[:1], ref) <= TOL16  # the healthy sequence is unaffected
+        assert torch.isfinite(out[1]).all()
+        assert torch.equal(out[2].cpu(), torch.zeros_like(out[2].cpu()))
+
+
+@pytest.mark.parametrize("plan", [False, True])
+def test_wide_groups_decode_step(plan):
+    # the step's append runs first (a kernel of its own), then the tcgen05
+    # kernel attends over the new token too; the cache is bit-exact
+    lengths = [1, 16, 17, 129, 700, 2049]
+    w = Workload(0, "wide_step", "bf16", 64, 2, 128, 16, len(lengths), "fixed",
+                 writes_new_token=True)
+    case = make_decode_case(w, seed=23, lengths=lengths)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    out = torch.full(case.q.shape, float("nan"), dtype=torch.float32, device=DEV)
+    ws = None
+    if plan:
+        n = pkv.decode_workspace_bytes(len(lengths), 64, 128, case.block_tables.shape[1] * 16, 0)
+        ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    pkv.decode_step(out, case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV), kc, vc,
+                    case.block_tables.to(DEV), case.context_lens.to(DEV), w.scale, 16, 2,
+                    workspace=ws)
+    torch.cuda.synchronize()
+    k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+    ref = oracle.decode_step(case.q, case.new_key, case.new_value, k_ref, v_ref,
+                             case.block_tables, case.context_lens, w.scale, 16, 2)
+    assert pkv.device_status() == 0
+    assert torch.equal(bits(kc), bits(k_ref)) and torch.equal(bits(vc), bits(v_ref))
+    assert max_err(out, ref) <= TOL16
+
+
+def test_wide_groups_query_and_output_in_pinned_host_memory():
+    # q read and the output written over the host link: the same bits as
+    # with device tensors
+    lengths = [1, 700, 33, 2049, 0]
+    w = Workload(0, "wide_host", "bf16", 32, 2, 128, 16, len(lengths), "fixed")
+    case = make_decode_case(w, seed=41, lengths=lengths)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    S, Hq, D = case.q.shape
+    outs = []
+    for host in (False, True):
+        q = case.q.pin_memory() if host else case.q.to(DEV)
+        out = torch.full((S, Hq, D), float("nan"), dtype=torch.float32)
+        out = out.pin_memory() if host else out.to(DEV)
+        pkv.paged_decode_attention(out, q, kc, vc, case.block_tables.to(DEV),
+                                   case.context_lens.to(DEV), w.scale, 16, 2)
+        torch.cuda.synchronize()
+        outs.append(out.cpu())
+    assert pkv.device_status() == 0
+    assert torch.equal(bits(outs[0]), bits(outs[1]))
+
+
+def test_wide_groups_unaligned_query_takes_head_slices():
+    # q 4-byte but not 16-byte aligned: the call runs the head-slice kernel
+    # (the tcgen05 kernel reads q in 16-byte pieces) with the same result
+    lengths = [40, 300, 129]
+    w = Workload(0, "wide_ua", "bf16", 32, 1, 128, 16, len(lengths), "fixed")
+    case = make_decode_case(w, seed=43, lengths=lengths)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_decode_attention(case.q, case.k_cache, case.v_cache, case.block_tables,
+                                        case.context_lens, w.scale, 16, 1)
+    n = case.q.numel()
+    big = torch.empty(n + 2, dtype=case.q.dtype, device=DEV)
+    q = big[2:].view(case.q.shape)
+    q.copy_(case.q.to(DEV))
+    assert q.data_ptr() % 16 != 0 and q.data_ptr() % 4 == 0
+    out = gpu_decode(q, kc, vc, case.block_tables, case.context_lens, w.scale, 16, 1)
+    assert pkv.device_status() == 0
+    assert max_err(out, ref) <= TOL16
