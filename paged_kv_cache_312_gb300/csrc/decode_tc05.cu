@@ -750,19 +750,24 @@ decode_tc05_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kma
             }
             // ---- epilogue: out[head][t] = O^T[t][head] / sum(head)
             const int kl = kt0 + nkt - 1;
+            // the partial sums through a scratch in the P buffer of tile
+            // kl - 1, free once its P V has finished, while the last P V runs
+            {
+                uint8_t* scr = smem + W::P_OFF + ((kl - 1) & 1) * W::P_BYTES;
+                if (kl >= 1) warp_wait(&o_done[(kl - 1) & 1], ((kl - 1) >> 1) & 1);
+                put_rows(scr, l);
+                softmax_sync();
+                red[t] = column_op<false>(scr);
+                softmax_sync();
+                if (warp == 0) {
+                    const float sum =
+                        (red[lane] + red[32 + lane]) + (red[64 + lane] + red[96 + lane]);
+                    inv_s[lane] = sum > 0.f ? 1.f / sum : 0.f;
+                }
+                softmax_sync();
+            }
             warp_wait(&o_done[kl & 1], (kl >> 1) & 1);
             tmem_fence_after();
-            // the partial sums through a scratch in the P buffers (both free:
-            // every P V of the item has finished)
-            put_rows(smem + W::P_OFF, l);
-            softmax_sync();
-            red[t] = column_op<false>(smem + W::P_OFF);
-            softmax_sync();
-            if (warp == 0) {
-                const float sum = (red[lane] + red[32 + lane]) + (red[64 + lane] + red[96 + lane]);
-                inv_s[lane] = sum > 0.f ? 1.f / sum : 0.f;
-            }
-            softmax_sync();
             float o[kN], o2[kN];
             tmem_ld32(tl + kColO, o);
             tmem_ld32(tl + kColO + kN, o2);

@@ -484,11 +484,14 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                         }
                     }
                 };
-                // pass 1: row max (eight independent partial maxima)
+                // pass 1: row max (eight independent partial maxima).  The
+                // 32-key chunks of both passes are rolled loops: the unrolled
+                // code (with the masked variant of the diagonal tiles) did not
+                // stay in the instruction cache
                 float mp[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
-#pragma unroll
+#pragma unroll 1
                 for (int c = 0; c < kKeys / 32; ++c) {
                     float vv[32];
                     load_chunk(c, vv);
@@ -510,9 +513,11 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                     m = mx;
                 }
                 const float ms = m == -INFINITY ? 0.f : m;
-                // O is rescaled before P V_x(j) is issued (it waits for p_half)
+                // O is rescaled before P V_x(j) is issued (it waits for p_half).
+                // A rolled loop: this path runs on an item's first tile and
+                // rarely after, so its code is cold in the instruction cache
                 if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         float o[32];
                         tmem_ld32(tl + kColO + c * 32, o);
@@ -525,7 +530,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                 // as [16-key step][high parts 8 columns][remainders 8 columns]
                 float2 sum2 = make_float2(0.f, 0.f);
                 const float2 mul2 = make_float2(mul, mul), nms2 = make_float2(-ms, -ms);
-#pragma unroll
+#pragma unroll 1
                 for (int c = 0; c < kKeys / 32; ++c) {
                     float vv[32];
                     load_chunk(c, vv);
@@ -570,7 +575,8 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                 const bool early = ok && vn < total_items;
                 if (early) issue_q(nx);
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
+                // rolled, like the rescale: once an item
+#pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     float o[32];
                     tmem_ld32(tl + kColO + c * 32, o);
