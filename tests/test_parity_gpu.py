@@ -1783,3 +1783,42 @@ def test_wide_groups_unaligned_query_takes_head_slices():
     out = gpu_decode(q, kc, vc, case.block_tables, case.context_lens, w.scale, 16, 1)
     assert pkv.device_status() == 0
     assert max_err(out, ref) <= TOL16
+
+
+@pytest.mark.parametrize("Hq", [64, 128])
+def test_wide_groups_back_to_back_steps_see_each_others_writes(Hq):
+    # As test_back_to_back_steps_see_each_others_writes, for G = 32 and 64 on
+    # the tcgen05 kernel: append kernel, work plan and persistent kernel, all
+    # dependent launches, twice on one stream and one workspace (the plan
+    # zeroes the kernel's record counter again before the second launch)
+    B, Hkv = 16, 2
+    lengths = [5, 17, 700, 2049, 1001, 35]
+    w = Workload(0, "wide_chain", "bf16", Hq, Hkv, 128, B, len(lengths), "fixed",
+                 writes_new_token=True)
+    case = make_decode_case(w, seed=37, lengths=lengths)
+    S, _, D = case.q.shape
+    g = torch.Generator().manual_seed(9)
+    nk2 = torch.randn(S, Hkv, D, generator=g).to(torch.bfloat16)
+    nv2 = torch.randn(S, Hkv, D, generator=g).to(torch.bfloat16)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    bt = case.block_tables.to(DEV)
+    cl1, cl2 = case.context_lens.to(DEV), (case.context_lens + 1).to(DEV)
+    out1 = torch.full((S, Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out2 = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, case.block_tables.shape[1] * B, 0),
+                     dtype=torch.uint8, device=DEV)
+    pkv.decode_step(out1, case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV), kc, vc,
+                    bt, cl1, w.scale, B, Hkv, workspace=ws)
+    pkv.decode_step(out2, out1, nk2.to(DEV), nv2.to(DEV), kc, vc, bt, cl2, w.scale, B, Hkv,
+                    workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+    ref1 = oracle.decode_step(case.q, case.new_key, case.new_value, k_ref, v_ref,
+                              case.block_tables, case.context_lens, w.scale, B, Hkv)
+    q2 = out1.cpu()
+    assert max_err(q2.float(), ref1) <= TOL16 + 2 ** -8 * float(np.abs(ref1).max())
+    ref2 = oracle.decode_step(q2, nk2, nv2, k_ref, v_ref, case.block_tables,
+                              case.context_lens + 1, w.scale, B, Hkv)
+    assert torch.equal(bits(kc), bits(k_ref)) and torch.equal(bits(vc), bits(v_ref))
+    assert max_err(out2, ref2) <= TOL16
