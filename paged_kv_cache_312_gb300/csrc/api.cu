@@ -411,7 +411,7 @@ int decode_wide(const char* fn, DecodeParams& p, int kv_dtype, const void* k_cac
                 int4* plan_items, cudaStream_t st)
 {
     const int G = p.num_heads / p.num_kv_heads;
-    p.head_slices = G / kDecodeWideHeads;
+    p.head_slices = G / decode_wide_tcgen05_heads(G);
     CUtensorMap kmap, vmap;
     const uint64_t rows = (uint64_t)p.num_blocks * p.num_kv_heads * p.block_size;
     const int box_rows = p.block_size < 16 ? p.block_size : 16;

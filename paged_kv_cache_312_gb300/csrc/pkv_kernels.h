@@ -188,14 +188,15 @@ cudaError_t launch_decode_tensor_core_deep(const DecodeParams& p, int kv_dtype, 
 
 // Unsplit decode for groups of G = 32 k query heads per KV head on the
 // tcgen05 tensor cores (decode_tc05.cu): items (sequence, KV head, slice of
-// kDecodeWideHeads query heads), p.head_slices = G / kDecodeWideHeads, taken
-// by persistent CTAs (one a SM, at most `sms`) from p.items through
-// p.item_next when p.items is set, else in grid-stride order.  16-bit KV,
-// head_dim 128, block size 8, 16 or 32, q 16-byte aligned; a programmatic
-// dependent launch.
+// decode_wide_tcgen05_heads(G) query heads: 64 when G is a multiple of 64,
+// else 32), p.head_slices = G / that, taken by persistent CTAs (one a SM, at
+// most `sms`) from p.items through p.item_next when p.items is set, else in
+// grid-stride order.  16-bit KV, head_dim 128, block size 8, 16 or 32, q
+// 16-byte aligned; a programmatic dependent launch.
 constexpr int kDecodeWideHeads = 32;
 bool decode_wide_tcgen05_supported(int kv_dtype, int head_dim, int block_size, int group,
                                    const void* q);
+int decode_wide_tcgen05_heads(int group);
 cudaError_t launch_decode_wide_tcgen05(const DecodeParams& p, int kv_dtype, const void* k_map,
                                        const void* v_map, int items, int sms,
                                        cudaStream_t stream);
