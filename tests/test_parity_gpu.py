@@ -1628,7 +1628,8 @@ def wide_decode(case, w, kc, vc, which, plan, out_dtype=torch.float32, q=None, o
 
 @pytest.mark.parametrize("dt,G,Hkv,B", [("bf16", 32, 2, 16), ("f16", 32, 1, 8),
                                          ("bf16", 64, 2, 32), ("f16", 96, 1, 16),
-                                         ("bf16", 32, 8, 8)])
+                                         ("bf16", 32, 8, 8), ("f16", 64, 1, 8),
+                                         ("bf16", 128, 1, 16)])
 @pytest.mark.parametrize("plan", [False, True])
 def test_wide_groups_tcgen05_match_oracle_and_head_slices(dt, G, Hkv, B, plan):
     # ragged lengths around the 128-token tile (1, 127, 128, 129, ...), an
@@ -1663,13 +1664,15 @@ def test_wide_groups_many_items_per_cta(plan):
     assert max_err(out, ref) <= TOL16
 
 
+@pytest.mark.parametrize("G", [32, 64])
 @pytest.mark.parametrize("rising", [True, False])
-def test_wide_groups_running_max_moves(rising):
+def test_wide_groups_running_max_moves(rising, G):
     # keys scaled up (or down) along each context, so that the per-head max
     # rises by more than the 2^8 margin several times mid-sequence (O^T and
-    # the partial sums are then rescaled) -- or is set by the first tile
+    # the partial sums are then rescaled) -- or is set by the first tile;
+    # G = 64 runs one 64-head item, two halves with a running max each
     lengths = [2049, 900, 3000]
-    w = Workload(0, "wide_max", "bf16", 32, 1, 128, 16, len(lengths), "fixed")
+    w = Workload(0, "wide_max", "bf16", G, 1, 128, 16, len(lengths), "fixed")
     case = make_decode_case(w, seed=31, lengths=lengths)
     kc = case.k_cache.float()
     for s, L in enumerate(lengths):
