@@ -32,16 +32,16 @@
 //    buffers; then all three load the item's K and V tiles of 128 tokens by
 //    TMA (16-row boxes of the paged cache, 128-byte swizzle, [column half]
 //    [token][128 B]), each warp about a third of a tile's boxes, into a ring
-//    of five 32 KB slots, in the order the MMAs use them: K(0) K(1) K(2)
-//    V(0) K(3) V(1) ... V(n-2) V(n-1) (S^T runs two tiles ahead of P V).  A slot's
+//    of five 32 KB slots, in the order the MMAs use them: K(0) K(1) K(2) V(0)
+//    K(3) V(1) ... V(n-2) V(n-1) (S^T runs two tiles ahead of P V).  A slot's
 //    barrier takes one arrival (with its bytes) from each load warp: a single
 //    warp issuing every copy of a tile holds the SM well below the HBM rate.
 //    Lanes read their boxes' block-table entries two tiles ahead and record
 //    bad ones.  While an item's tiles are issued, warp 5 already claims the
-//    next record, loads its Q into registers and reads the entries of its
-//    first two tiles, one stage a step, so that nothing waits on a global
-//    round trip between items.  Eight warps, two a scheduler, leave the
-//    softmax its registers.
+//    next record and reads the entries of its first two tiles, one stage a
+//    step, so that the item boundary waits on no global round trip but the
+//    Q rows'.  Eight warps, two a scheduler, leave the softmax its registers
+//    (twelve, three a scheduler, with NH = 64: 168 registers a thread).
 //  * warp 4 (MMA issue): S^T(j + 2) into S buffer j & 1 as soon as the
 //    softmax has read S^T(j) out of it (early in its tile), then, once the
 //    softmax has posted P(j) in shared memory, O^T += V(j)^T P(j)^T.
@@ -49,8 +49,8 @@
 //    tokens): thread t owns token t of each tile (row t of S^T) and row
 //    d = t of O^T, for its 32 heads.  Every head's running max is shared by
 //    the CTA (in shared memory) and moves only when a score passes it by
-//    more than 8 (a factor 2^8):
-//    a barrier-reduction vote finds out, then the tile's scores, put through
+//    more than 8 (a factor 2^8): a barrier-reduction vote (per half of the
+//    heads, a named barrier each) finds out, then the tile's scores, put through
 //    a scratch in the tile's P buffer, give its maxima per head, and O^T and
 //    the partial sums are rescaled.  Each thread sums P over its own tokens
 //    per head; those sums are reduced across the 128 threads through the
