@@ -1825,3 +1825,54 @@ def test_wide_groups_back_to_back_steps_see_each_others_writes(Hq):
                               case.context_lens + 1, w.scale, B, Hkv)
     assert torch.equal(bits(kc), bits(k_ref)) and torch.equal(bits(vc), bits(v_ref))
     assert max_err(out2, ref2) <= TOL16
+
+
+def test_wide_groups_split_decode_step_and_back_to_back():
+    # G = 32: two split decode steps back to back on one workspace (split
+    # launches of wide groups run head slices with the in-launch merge); the
+    # plan zeroes the merge counters again before the second
+    B, Hkv, Hq, P = 16, 2, 64, 256
+    lengths = [5, 17, 700, 2049, 1001, 35]
+    w = Workload(0, "wide_split_step", "bf16", Hq, Hkv, 128, B, len(lengths), "fixed",
+                 writes_new_token=True)
+    case = make_decode_case(w, seed=53, lengths=lengths)
+    S, _, D = case.q.shape
+    g = torch.Generator().manual_seed(11)
+    nk2 = torch.randn(S, Hkv, D, generator=g).to(torch.bfloat16)
+    nv2 = torch.randn(S, Hkv, D, generator=g).to(torch.bfloat16)
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    bt = case.block_tables.to(DEV)
+    cl1, cl2 = case.context_lens.to(DEV), (case.context_lens + 1).to(DEV)
+    out1 = torch.full((S, Hq, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out2 = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, case.block_tables.shape[1] * B, P),
+                     dtype=torch.uint8, device=DEV)
+    pkv.decode_step(out1, case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV), kc, vc,
+                    bt, cl1, w.scale, B, Hkv, partition_size=P, workspace=ws)
+    pkv.decode_step(out2, out1, nk2.to(DEV), nv2.to(DEV), kc, vc, bt, cl2, w.scale, B, Hkv,
+                    partition_size=P, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.device_status() == 0
+    k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+    ref1 = oracle.decode_step(case.q, case.new_key, case.new_value, k_ref, v_ref,
+                              case.block_tables, case.context_lens, w.scale, B, Hkv)
+    q2 = out1.cpu()
+    assert max_err(q2.float(), ref1) <= TOL16 + 2 ** -8 * float(np.abs(ref1).max())
+    ref2 = oracle.decode_step(q2, nk2, nv2, k_ref, v_ref, case.block_tables,
+                              case.context_lens + 1, w.scale, B, Hkv)
+    assert torch.equal(bits(kc), bits(k_ref)) and torch.equal(bits(vc), bits(v_ref))
+    assert max_err(out2, ref2) <= TOL16
+
+
+def test_wide_groups_split_bad_block_is_flagged():
+    w = Workload(0, "wide_split_bad", "bf16", 64, 1, 128, 16, 3, "fixed")
+    case = make_decode_case(w, seed=59, lengths=[1500, 1500, 1500])
+    bt = case.block_tables.clone()
+    bt[1, 40] = case.num_blocks + 5  # in the second 512-token partition
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    ref = oracle.paged_decode_attention(case.q[:1], case.k_cache, case.v_cache, bt[:1],
+                                        case.context_lens[:1], w.scale, 16, 1)
+    out = gpu_decode(case.q, kc, vc, bt, case.context_lens, w.scale, 16, 1, P=512)
+    assert pkv.device_status(reset=True) & 1
+    assert max_err(out[:1], ref) <= TOL16
+    assert torch.isfinite(out[1]).all()
