@@ -1876,3 +1876,43 @@ def test_wide_groups_split_bad_block_is_flagged():
     assert pkv.device_status(reset=True) & 1
     assert max_err(out[:1], ref) <= TOL16
     assert torch.isfinite(out[1]).all()
+
+
+def test_wide_groups_in_a_cuda_graph():
+    # a wide-group decode step (append kernel, work plan, persistent tcgen05
+    # kernel) captured once as a CUDA graph and replayed: each replay zeroes
+    # the record counter again and gives the same result as a direct call
+    lengths = [1, 700, 129, 2049]
+    w = Workload(0, "wide_graph", "bf16", 64, 2, 128, 16, len(lengths), "fixed",
+                 writes_new_token=True)
+    case = make_decode_case(w, seed=61, lengths=lengths)
+    S, Hq, D = case.q.shape
+    kc, vc = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    q, nk, nv = case.q.to(DEV), case.new_key.to(DEV), case.new_value.to(DEV)
+    bt, cl = case.block_tables.to(DEV), case.context_lens.to(DEV)
+    ws = torch.empty(pkv.decode_workspace_bytes(S, Hq, D, case.block_tables.shape[1] * 16, 0),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    stream = torch.cuda.Stream(DEV)
+    stream.wait_stream(torch.cuda.current_stream(DEV))
+    # a separate cache for the warm-up call outside the capture (it appends
+    # the new tokens too)
+    kw, vw = case.k_cache.to(DEV), case.v_cache.to(DEV)
+    with torch.cuda.stream(stream):
+        pkv.decode_step(out, q, nk, nv, kw, vw, bt, cl, w.scale, 16, 2, workspace=ws,
+                        stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+        pkv.decode_step(out, q, nk, nv, kc, vc, bt, cl, w.scale, 16, 2, workspace=ws,
+                        stream=stream)
+    k_ref, v_ref = case.k_cache.clone(), case.v_cache.clone()
+    ref = oracle.decode_step(case.q, case.new_key, case.new_value, k_ref, v_ref,
+                             case.block_tables, case.context_lens, w.scale, 16, 2)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pkv.device_status() == 0
+        assert max_err(out, ref) <= TOL16
+    assert torch.equal(bits(kc), bits(k_ref)) and torch.equal(bits(vc), bits(v_ref))
