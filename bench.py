@@ -559,6 +559,10 @@ def run_gpu(args, rank, world, local_rank):
             lx["cpu_baseline"] = cpu_baseline(sx, args.cpu_budget_extra, gx_out)
         line["workloads"][str(key)] = lx
         del sx
+    if rank == 0 and world == 1 and args.workload == 2 and not args.no_wide:
+        # wide query-head groups on their tcgen05 kernel (the sweep workload's
+        # G = 32 and 64 points), attention call only
+        line["wide_groups"] = wide_group_points(pkv, args.steps, args.warmup, args.seed)
     return line
 
 
@@ -956,6 +960,59 @@ def sweep_workload(B: int, G: int, D: int) -> Workload:
                     "uniform:1024:4096")
 
 
+def time_decode_call(pkv, call, steps, warmup, stream, dev):
+    """Mean ms of `call` over `steps` back-to-back launches on `stream` (CUDA
+    events around them), after `warmup` untimed ones."""
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert pkv.device_status() == 0
+    return t0.elapsed_time(t1) / steps
+
+
+def wide_group_points(pkv, steps, warmup, seed=0):
+    """The sweep workload at G = 32 and 64 (block 16, head_dim 128, unsplit with
+    the work plan): the decode kernel for wide query-head groups, as a
+    fraction of the measured copy peak (KV bytes once per (token, KV head))."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+    peak, _ = measured_peaks()
+    B, D = 16, 128
+    base = sweep_workload(B, 64, D)
+    case = make_decode_case(base, seed=seed)
+    kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
+    bt, cl = case.block_tables.to(dev), case.context_lens.to(dev)
+    kv = int(case.context_lens.to(torch.int64).sum()) * 2 * 8 * D * 2
+    res = {}
+    for G in (32, 64):
+        w = sweep_workload(B, G, D)
+        q = case.q[:, :w.num_heads].contiguous().to(dev)
+        S = q.shape[0]
+        out = torch.empty((S, w.num_heads, D), dtype=torch.float32, device=dev)
+        ws = torch.empty(pkv.decode_workspace_bytes(S, w.num_heads, D, bt.shape[1] * B, 0),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            pkv.paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, B, 8, partition_size=0,
+                                       workspace=ws, stream=stream)
+        ms = time_decode_call(pkv, call, steps, warmup, stream, dev)
+        res[str(G)] = {"kernel": "decode_tc05 (tcgen05, %d heads an item)" % (64 if G % 64 == 0
+                                                                               else 32),
+                       "query_heads": w.num_heads, "kv_heads": 8, "head_dim": D,
+                       "block_size": B, "sequences": S, "kv_bytes": kv,
+                       "attn_ms": round(ms, 5), "attn_gbs": round(kv / (ms * 1e-3) / 1e9, 1),
+                       "frac_of_measured_peak": round(kv / (ms * 1e-3) / 1e9 / peak, 4)}
+    del kc, vc
+    return res
+
+
 def run_sweep(args):
     """Attention GB/s over B x G x D, one JSON line per point, plus the
     allocation side of the same trade-off for the drawn lengths: table entries
@@ -1003,18 +1060,7 @@ def run_sweep(args):
                     def call():
                         pkv.paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, B, 8,
                                                    partition_size=P, workspace=ws, stream=stream)
-                    for _ in range(args.warmup):
-                        call()
-                    torch.cuda.synchronize(dev)
-                    t0 = torch.cuda.Event(enable_timing=True)
-                    t1 = torch.cuda.Event(enable_timing=True)
-                    t0.record(stream)
-                    for _ in range(args.steps):
-                        call()
-                    t1.record(stream)
-                    torch.cuda.synchronize(dev)
-                    assert pkv.device_status() == 0
-                    timed[P] = t0.elapsed_time(t1) / args.steps
+                    timed[P] = time_decode_call(pkv, call, args.steps, args.warmup, stream, dev)
                 best = min(timed, key=timed.get)
                 ms = timed[best]
                 line = {"sweep": {"block_size": B, "group": G, "head_dim": D,
@@ -1295,6 +1341,9 @@ def main():
     ap.add_argument("--group-parts", type=int, default=1,
                     help="beam workload: CTAs that share one beam group's stages for a KV head")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-wide", action="store_true",
+                    help="leave out the wide query-head group points (G = 32, 64 on the sweep "
+                         "workload) that the default line carries in `wide_groups`")
     ap.add_argument("--cpu-budget", type=float, default=8.0,
                     help="seconds of oracle time for the headline workload's CPU baseline")
     ap.add_argument("--cpu-budget-extra", type=float, default=3.0,
