@@ -437,10 +437,12 @@ int pkv_set_decode_kernel(int which);
  * block size 8, 16 or 32, q 16-byte aligned and partition_size 0 (outside
  * beam groups),
  * PKV_WIDE_TCGEN05 (default) runs the 5th-generation tensor-core kernel: a
- * K/V tile's 128 tokens are the MMA's M and 32 query heads its N, one
- * persistent CTA a SM, the work plan's longest-first order when a workspace
- * is given (pkv_decode_workspace_bytes with partition_size 0; its bytes 0-4
- * and 64-68 are the plan's count and the kernel's record counter).
+ * K/V tile's 128 tokens are the MMA's M and 64 query heads (when G is a
+ * multiple of 64, else 32) its N, one persistent CTA a SM, the work plan's
+ * longest-first order when a workspace is given (pkv_decode_workspace_bytes
+ * with partition_size 0; its bytes 0-4 and 64-68 are the plan's count and
+ * the kernel's record counter).  Split launches (partition_size > 0) of such
+ * groups run head slices.
  * PKV_WIDE_HEAD_SLICES runs the mma.sync kernel on head slices of 16 query
  * heads (also used for every other shape).  Both compute the same result up
  * to fp32 accumulation order.  With new_k / new_v (pkv_decode_step) the
