@@ -30,8 +30,10 @@
 //  * warps 5-7 (loads): warp 5 takes an item's record and loads its 32 rows
 //    of Q (plain loads, so q may be pinned host memory) into one of two Q
 //    buffers; then all three load the item's K and V tiles of 128 tokens by
-//    TMA (16-row boxes of the paged cache, 128-byte swizzle, [column half]
-//    [token][128 B]), each warp about a third of a tile's boxes, into a ring
+//    TMA (16-row boxes of the paged cache, 128-byte swizzle; K as [column
+//    half][token][128 B], two copies a box; V as [16-token group][column
+//    half][16 rows][128 B], one copy a box, the layout P V reads a 16-token
+//    step from), each warp about a third of a tile's boxes, into a ring
 //    of five 32 KB slots, in the order the MMAs use them: K(0) K(1) K(2) V(0)
 //    K(3) V(1) ... V(n-2) V(n-1) (S^T runs two tiles ahead of P V).  A slot's
 //    barrier takes one arrival (with its bytes) from each load warp: a single
@@ -102,8 +104,13 @@ struct W5 {
     static constexpr int Q_BYTES = 2 * HALF_Q;
     static constexpr int P_ATOM = kTok * 128;        // a head half's P^T: [token][high | low]
     static constexpr int P_BYTES = HALVES * P_ATOM;
-    static constexpr int HALF_KV = kTok * 128;       // K or V: [half][token][128 B]
+    static constexpr int HALF_KV = kTok * 128;       // K: [half][token][128 B]
     static constexpr int SLOT_BYTES = 2 * HALF_KV;
+    // V: per 16-token group (4 KB), both halves of each box from one copy:
+    // [half][16 rows][128 B], or at block size 8 [8-row box][half][8 rows][128 B]
+    static constexpr int V_GROUP = 4096;
+    static constexpr int V_LBO = ROWS == 16 ? 2048 : 1024;  // between the halves
+    static constexpr int V_SBO = ROWS == 16 ? 1024 : 2048;  // between 8-row groups
     static constexpr int P_OFF = QB * Q_BYTES;
     static constexpr int SLOT_OFF = P_OFF + 2 * P_BYTES;
     // full, empty per slot; q_full, q_empty per Q buffer; s_full, s_free,
@@ -495,11 +502,16 @@ decode_tc05_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kma
                 if (id >= 0 || zero_box) {
                     const int row = zero_box ? -W::ROWS
                                              : (id * p.num_kv_heads + g) * B + (IDS > 1 ? 0 : tok % B);
-                    const uint32_t dst = smem_u32(smem + W::SLOT_OFF + sl * W::SLOT_BYTES) +
-                                         bx * W::ROWS * 128;
-                    const CUtensorMap* map = kv ? &vmap : &kmap;
-                    tma_load_2d(dst, map, 0, row, bar);
-                    tma_load_2d(dst + W::HALF_KV, map, 64, row, bar);
+                    const uint32_t slot = smem_u32(smem + W::SLOT_OFF + sl * W::SLOT_BYTES);
+                    if (kv == 0) {
+                        const uint32_t dst = slot + bx * W::ROWS * 128;
+                        tma_load_2d(dst, &kmap, 0, row, bar);
+                        tma_load_2d(dst + W::HALF_KV, &kmap, 64, row, bar);
+                    } else {
+                        // box bx = 16-token group bx / IDS, 8-row box bx % IDS
+                        const uint32_t dst = slot + (bx / IDS) * W::V_GROUP + (bx % IDS) * 2048;
+                        tma_load_3d(dst, &vmap, 0, row, 0, bar);
+                    }
                 }
                 if (lead && stage < 3) advance();
             }
@@ -520,7 +532,7 @@ decode_tc05_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kma
         // operand is one of these moved by a constant or per-buffer offset
         const uint64_t q_desc = smem_desc(smem_u32(smem), 16, 1024);
         const uint64_t k_desc = smem_desc(slot_base, 16, 1024);
-        const uint64_t v_desc = smem_desc(slot_base, W::HALF_KV, 1024);
+        const uint64_t v_desc = smem_desc(slot_base, W::V_LBO, W::V_SBO);
         // P^T: MN-major, one 128-byte atom (64 columns) per head half
         const uint64_t p_desc = smem_desc(smem_u32(smem + W::P_OFF), W::P_ATOM, 1024);
         auto commit = [&](uint64_t* bar) {
@@ -545,8 +557,11 @@ decode_tc05_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kma
                 uint8_t* vt = smem + W::SLOT_OFF + sl * W::SLOT_BYTES;
                 for (int i = lane; i < (k1 - k0) * 16; i += 32) {
                     const int k = k0 + (i >> 4), hf = (i >> 3) & 1, c = i & 7;
-                    *reinterpret_cast<uint4*>(vt + hf * W::HALF_KV + k * 128 + c * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
+                    const int r = k & 15;
+                    const int at = (k >> 4) * W::V_GROUP +
+                                   (W::ROWS == 16 ? hf * 2048 + r * 128
+                                                  : (r >> 3) * 2048 + hf * 1024 + (r & 7) * 128);
+                    *reinterpret_cast<uint4*>(vt + at + c * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async();
             }
@@ -574,7 +589,7 @@ decode_tc05_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kma
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kTok / 16; ++kk)
-                    umma(tm + COL_O, desc_add(vd, kk * 2048), desc_add(pd, kk * 2048), id_o,
+                    umma(tm + COL_O, desc_add(vd, kk * W::V_GROUP), desc_add(pd, kk * 2048), id_o,
                          !first || kk > 0);
                 umma_commit(smem_u32(&o_done[kt & 1]));
             }
