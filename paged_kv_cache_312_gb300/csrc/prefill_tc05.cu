@@ -86,21 +86,37 @@ struct G5 {
 };
 
 // One work item: 256 query rows (tiles A and B) of one query head of one
-// sequence.  Items are numbered with the latest (heaviest) rows first and the
-// head fastest, so consecutive items (taken by neighbouring CTAs) have equal
-// cost and share their sequence's K/V in L2.
+// sequence.  Items are numbered (item_coords) so that consecutive items,
+// taken by neighbouring CTAs, have about equal cost and share K/V in L2.
 struct Item {
     int h, s, r0, qn, L, q0, g, base_pos, nkt_a, nkt_b, nkt;
 };
 
+// Item v's row tile (counted from the first), sequence and head.  Items come
+// in groups of kSeqGroup sequences (the last group may hold fewer); within a
+// group, the latest (heaviest) row tiles first, then the sequence, the head
+// fastest.  A group's K/V (a few tens of MB for long prompts) stays in L2
+// while its row tiles pass over it; all sequences at once would not.
+constexpr int kSeqGroup = 4;
+__device__ __forceinline__ void item_coords(const PrefillParams& p, int items_x, int v, int& ct,
+                                            int& s, int& h)
+{
+    const int per_group = items_x * kSeqGroup * p.num_heads;
+    const int gi = v / per_group;
+    const int s0 = gi * kSeqGroup;
+    const int per_level = min(kSeqGroup, p.num_seqs - s0) * p.num_heads;
+    const int rem = v - gi * per_group;
+    ct = items_x - 1 - rem / per_level;
+    const int r2 = rem - (rem / per_level) * per_level;
+    s = s0 + r2 / p.num_heads;
+    h = r2 - (r2 / p.num_heads) * p.num_heads;
+}
+
 template <int B>
 __device__ __forceinline__ bool decode_item(const PrefillParams& p, int items_x, int v, Item& it)
 {
-    const int hs = p.num_heads * p.num_seqs;
-    const int ct = items_x - 1 - v / hs;
-    const int rem = v % hs;
-    it.h = rem % p.num_heads;
-    it.s = rem / p.num_heads;
+    int ct;
+    item_coords(p, items_x, v, ct, it.s, it.h);
     it.r0 = p.query_start[it.s];
     it.qn = p.query_start[it.s + 1] - it.r0;
     it.L = p.context_lens[it.s];
@@ -124,11 +140,9 @@ __device__ __forceinline__ bool decode_item(const PrefillParams& p, int items_x,
 template <int B>
 __device__ __forceinline__ bool item_bad_lengths(const PrefillParams& p, int items_x, int v)
 {
-    const int hs = p.num_heads * p.num_seqs;
-    const int ct = items_x - 1 - v / hs;
-    const int rem = v % hs;
-    if (ct != items_x - 1 || rem % p.num_heads != 0) return false;  // once per sequence
-    const int s = rem / p.num_heads;
+    int ct, s, h;
+    item_coords(p, items_x, v, ct, s, h);
+    if (ct != items_x - 1 || h != 0) return false;  // once per sequence
     const int qn = p.query_start[s + 1] - p.query_start[s];
     const int L = p.context_lens[s];
     return L < 0 || (int64_t)L > (int64_t)p.max_blocks * B || qn < 0 || qn > L ||
