@@ -85,9 +85,16 @@ int get_encoder()
 // per 64-column half.  halves = 1: a 3-D map whose outermost dimension steps
 // over the 64-column halves (stride 128 bytes), so that one box brings every
 // half of box_rows rows, laid out half after half in shared memory.
+// halves = 2: a 4-D map over [row group of 8][half][row in group][64 columns]
+// (strides 8 rows, 128 bytes, one row), so that one box brings box_rows rows
+// (a multiple of 8) of every half as 1024-byte swizzle atoms, row group by
+// row group, each group's halves side by side.
 int tensor_map(const void* cache, uint64_t rows, int D, int box_rows, int dtype, CUtensorMap* out,
                int halves = 0)
 {
+    if (halves == 2 && (rows % 8 != 0 || box_rows % 8 != 0))
+        return pkv_fail(PKV_ERR_SHAPE, "row-group tensor map: rows %llu, box %d not multiples of 8",
+                        (unsigned long long)rows, box_rows);
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (const MapEntry& m : g_maps) {
         if (m.ptr == cache && m.rows == rows && m.D == D && m.box_rows == box_rows &&
@@ -100,14 +107,23 @@ int tensor_map(const void* cache, uint64_t rows, int D, int box_rows, int dtype,
     if (rc != PKV_OK) return rc;
     MapEntry& m = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % 16;
-    cuuint64_t dims[3] = {(cuuint64_t)(halves ? 64 : D), (cuuint64_t)rows, (cuuint64_t)(D / 64)};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)(D / 64)};
-    cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint64_t pitch = (cuuint64_t)D * 2;
+    cuuint64_t dims[4] = {(cuuint64_t)(halves ? 64 : D), (cuuint64_t)rows, (cuuint64_t)(D / 64), 1};
+    cuuint64_t strides[3] = {pitch, 128, 0};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_rows, (cuuint32_t)(D / 64), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (halves == 2) {
+        dims[1] = 8;
+        dims[3] = rows / 8;
+        strides[2] = 8 * pitch;
+        box[1] = 8;
+        box[3] = (cuuint32_t)(box_rows / 8);
+    }
+    const cuuint32_t rank = halves == 2 ? 4 : halves ? 3 : 2;
     CUresult r = g_encode(&m.map,
                           dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                          halves ? 3 : 2, const_cast<void*>(cache), dims, strides, box, estr,
+                          rank, const_cast<void*>(cache), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -333,10 +349,12 @@ int pkv_paged_prefill_attention(void* out, const void* q, const void* k_cache, c
     if (!p.status) return pkv_fail(PKV_ERR_CUDA, "%s: no device status word", fn);
     CUtensorMap kmap, vmap;
     const uint64_t rows = (uint64_t)num_blocks * num_kv_heads * block_size;
-    // the prefill kernel's boxes are 16-token groups (or one block of 8)
+    // the tcgen05 kernel's boxes are 16-token groups (or one block of 8) of
+    // both column halves in 8-row groups; the warp-MMA kernel's are per half
     const int box_rows = block_size < 16 ? block_size : 16;
-    int rc = tensor_map(k_cache, rows, head_dim, box_rows, kv_dtype, &kmap);
-    if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, box_rows, kv_dtype, &vmap);
+    const int halves = g_prefill_kernel == PKV_PREFILL_WARP_MMA ? 0 : 2;
+    int rc = tensor_map(k_cache, rows, head_dim, box_rows, kv_dtype, &kmap, halves);
+    if (rc == PKV_OK) rc = tensor_map(v_cache, rows, head_dim, box_rows, kv_dtype, &vmap, halves);
     if (rc != PKV_OK) return rc;
     cudaError_t e =
         g_prefill_kernel == PKV_PREFILL_WARP_MMA

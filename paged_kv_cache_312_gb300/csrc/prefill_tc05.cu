@@ -10,10 +10,11 @@
 // How (GB300 design): one CTA of 10 warps per (256 query rows, query head,
 // sequence), latest (heaviest) rows first; the rows form two 128-row tiles
 // A and B whose softmax work alternates with each other's tensor-core work.
-//  * warp 9 (loads): K and V tiles of 128 tokens by TMA (16-row boxes of the
-//    paged cache, 128-byte swizzle, [column half][key][128 B]) into a ring of
-//    slots, K(0) V(0) K(1) V(1) ...; its lanes read the tile's block-table
-//    entries in parallel (one tile ahead) and record bad entries.
+//  * warp 9 (loads): K and V tiles of 128 tokens by TMA (one copy per
+//    16-row box of the paged cache brings both column halves, 128-byte
+//    swizzle, [8-key group][column half][key][128 B]) into a ring of slots,
+//    K(0) V(0) K(1) V(1) ...; its lanes read the tile's block-table entries
+//    in parallel (one tile ahead) and record bad entries.
 //  * warp 8 (MMA issue): S_X(j) = Q_X K(j)^T into tensor memory (M=128,
 //    N=128, K=head_dim; Q and K K-major in shared memory), then
 //    O_X += P_X(j) V(j) with P read from tensor memory (M=128, N=head_dim,
@@ -66,9 +67,13 @@ struct G5 {
     static constexpr int NH = D / 64;
     static constexpr int ROWS = B < 16 ? B : 16;  // rows per TMA box
     static constexpr int IDS = 16 / ROWS;         // boxes per 16-token group
-    static constexpr int SUBS = (kKeys / 16) * IDS;  // boxes per key tile and half
+    static constexpr int SUBS = (kKeys / 16) * IDS;  // boxes (copies) per key tile
     static constexpr int HALF_Q = kTileRows * 128;
     static constexpr int HALF_KV = kKeys * 128;
+    // K/V tiles hold 8-key groups of RG_BYTES, each group's column halves
+    // side by side (1024-byte swizzle atoms): key k, half hf at
+    // (k / 8) RG_BYTES + hf 1024 + (k % 8) 128
+    static constexpr int RG_BYTES = NH * 1024;
     static constexpr int Q_BYTES = NH * HALF_Q;
     static constexpr int SLOT_BYTES = NH * HALF_KV;
     static constexpr int SLOTS = D == 128 ? 4 : 8;  // K/V ring (one K or V tile each)
@@ -253,11 +258,9 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                             (id * p.num_kv_heads + it.g) * B + (IDS > 1 ? 0 : tok % B);
                         const uint32_t dst =
                             smem_u32(smem + Gm::SLOT_OFF + sl * Gm::SLOT_BYTES) +
-                            (grp * 16 + u * Gm::ROWS) * 128;
-#pragma unroll
-                        for (int hf = 0; hf < Gm::NH; ++hf)
-                            tma_load_2d(dst + hf * Gm::HALF_KV, kv ? &vmap : &kmap, hf * 64, row,
-                                        bar);
+                            (grp * 16 + u * Gm::ROWS) / 8 * Gm::RG_BYTES;
+                        // one copy brings the box's rows of every column half
+                        tma_load_4d(dst, kv ? &vmap : &kmap, 0, 0, 0, row / 8, bar);
                     }
                 }
                 if (!ok) break;
@@ -279,8 +282,8 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         // descriptors of Q and of ring slot 0; every operand is one of these
         // moved by a constant or per-slot offset
         const uint64_t q_desc = smem_desc(q_base, 16, 1024);
-        const uint64_t k_desc = smem_desc(slot_base, 16, 1024);          // K-major
-        const uint64_t v_desc = smem_desc(slot_base, Gm::HALF_KV, 1024);  // MN-major
+        const uint64_t k_desc = smem_desc(slot_base, 16, Gm::RG_BYTES);  // K-major
+        const uint64_t v_desc = smem_desc(slot_base, 1024, Gm::RG_BYTES);  // MN-major
         // S_x = Q_x K(kt)^T into tile x's S/P columns
         auto issue_s = [&](int x, int kt) {
             const uint64_t qd = desc_add(q_desc, x * Gm::Q_BYTES);
@@ -290,7 +293,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     umma(d, desc_add(qd, (kk >> 2) * Gm::HALF_Q + (kk & 3) * 32),
-                         desc_add(kd, (kk >> 2) * Gm::HALF_KV + (kk & 3) * 32), id_s, kk > 0);
+                         desc_add(kd, (kk >> 2) * 1024 + (kk & 3) * 32), id_s, kk > 0);
                 umma_commit(smem_u32(&s_full[x]));
             }
             __syncwarp();
@@ -305,7 +308,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
 #pragma unroll
                 for (int k4 = 0; k4 < kKeys / 32; ++k4) {
                     const int kk = hh * (kKeys / 32) + k4;
-                    const uint64_t b = desc_add(vd, kk * 2048);
+                    const uint64_t b = desc_add(vd, kk * 2 * Gm::RG_BYTES);
                     umma_ts(oc, pc + kk * 16, b, id_o, !first || kk > 0);
                     umma_ts(oc, pc + kk * 16 + 8, b, id_o, 1);
                 }
@@ -336,7 +339,8 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                     const int hf = i / (kKeys * 8), k = (i >> 3) % kKeys, c = i & 7;
                     const int box = (k >> 4) * IDS + (k & 15) / Gm::ROWS;
                     if (key0 + k >= L || ((bm >> box) & 1u))
-                        *reinterpret_cast<uint4*>(vt + hf * Gm::HALF_KV + k * 128 + c * 16) =
+                        *reinterpret_cast<uint4*>(vt + (k >> 3) * Gm::RG_BYTES + hf * 1024 +
+                                                  (k & 7) * 128 + c * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async();
@@ -482,37 +486,60 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                 tmem_fence_after();
                 const int key0 = j * kKeys;
                 const uint32_t bm = kbad[(kt0 + j) % kRing];
-                // unmasked tile (every key visible and loaded, positive scale):
-                // scores stay raw and the scale is folded into the exponent's FMA
+                // unmasked tile for the whole warp (every key visible and loaded,
+                // positive scale): scores stay raw and the scale is folded into
+                // the exponent's FMA.  Otherwise pass 1 writes the scaled scores
+                // back over S, -inf where a key is masked, for pass 2 to read
                 const bool plain = key0 + kKeys - 1 <= pos && bm == 0 && sl > 0.f;
-                const float mul = plain ? sl : 1.f;
-                auto load_chunk = [&](int c, float (&vv)[32]) {
-                    tmem_ld32(tl + c * 32, vv);
-                    if (!plain) {
+                const bool wplain = __all_sync(0xffffffffu, plain);
+                const float mul = wplain ? sl : 1.f;
+                // keys of chunk c this row may see: causally visible (k <= pos -
+                // key0) and not in a bad block (one bit of bm per box of ROWS keys)
+                auto chunk_valid = [&](int c) {
+                    const int r = pos - key0 - c * 32;
+                    uint32_t v = r >= 31 ? 0xffffffffu : r < 0 ? 0u : (2u << r) - 1u;
+                    const uint32_t bb = bm >> (c * 2 * IDS);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int k = c * 32 + i;
-                            const int box = (k >> 4) * IDS + (k & 15) / Gm::ROWS;
-                            const bool valid = key0 + k <= pos && !((bm >> box) & 1u);
-                            vv[i] = valid ? vv[i] * sl : -INFINITY;
-                        }
-                    }
+                    for (int q = 0; q < 2 * IDS; ++q)
+                        if ((bb >> q) & 1u) v &= ~(((1u << Gm::ROWS) - 1u) << (q * Gm::ROWS));
+                    return v;
                 };
                 // pass 1: row max (eight independent partial maxima).  The
-                // 32-key chunks of both passes are rolled loops: the unrolled
-                // code (with the masked variant of the diagonal tiles) did not
-                // stay in the instruction cache
+                // 32-key chunks of both passes are rolled loops: unrolled code
+                // (with the masked variant of the diagonal tiles) did not stay in
+                // the instruction cache
                 float mp[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+                if (wplain) {
 #pragma unroll 1
-                for (int c = 0; c < kKeys / 32; ++c) {
-                    float vv[32];
-                    load_chunk(c, vv);
+                    for (int c = 0; c < kKeys / 32; ++c) {
+                        float vv[32];
+                        tmem_ld32(tl + c * 32, vv);
 #pragma unroll
-                    for (int i = 0; i < 32; i += 16)
+                        for (int i = 0; i < 32; i += 16)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) mp[e] = fmax3(mp[e], vv[i + e], vv[i + 8 + e]);
+                            for (int e = 0; e < 8; ++e)
+                                mp[e] = fmax3(mp[e], vv[i + e], vv[i + 8 + e]);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < kKeys / 32; ++c) {
+                        float vv[32];
+                        tmem_ld32(tl + c * 32, vv);
+                        const uint32_t valid = chunk_valid(c);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            vv[i] = (valid >> i) & 1u ? vv[i] * sl : -INFINITY;
+                        tmem_st32(tl + c * 32, vv);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 16)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                mp[e] = fmax3(mp[e], vv[i + e], vv[i + 8 + e]);
+                    }
+                    // the masked scores are in place before pass 2 reads them
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
 #pragma unroll
                 for (int w = 4; w >= 1; w >>= 1)
@@ -547,7 +574,7 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
 #pragma unroll 1
                 for (int c = 0; c < kKeys / 32; ++c) {
                     float vv[32];
-                    load_chunk(c, vv);
+                    tmem_ld32(tl + c * 32, vv);
                     float pw[32];
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
