@@ -420,18 +420,25 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
         // This thread's row of item it2's Q into shared memory by asynchronous
         // 16-byte copies (zeros past qn), and the wait that makes them visible
         // to the tensor cores before the hand-over to the MMA warp.
+        // The warp copies its 32 rows together, D / 8 16-byte pieces a row, so
+        // that each instruction reads whole rows (rows are H D elements apart).
         auto issue_q = [&](const Item& it2) {
-            const int row2 = it2.q0 + x * kTileRows + r;
-            const bool have = row2 < it2.qn;
-            const T* src = static_cast<const T*>(p.q) +
-                           ((size_t)(it2.r0 + (have ? row2 : 0)) * p.num_heads + it2.h) * D;
-            const uint32_t bytes = have ? 16u : 0u;
+            constexpr int PIECES = D / 8;
+            const int wrow0 = (warp & 3) * 32;
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c)
+            for (int u = 0; u < PIECES; ++u) {
+                const int idx = u * 32 + lane;
+                const int t = wrow0 + idx / PIECES, c = idx % PIECES;
+                const int row2 = it2.q0 + x * kTileRows + t;
+                const bool have = row2 < it2.qn;
+                const T* src = static_cast<const T*>(p.q) +
+                               ((size_t)(it2.r0 + (have ? row2 : 0)) * p.num_heads + it2.h) * D +
+                               c * 8;
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                                 smem_u32(qx + (c >> 3) * Gm::HALF_Q + swz(r, c & 7))),
-                             "l"(src + c * 8), "r"(bytes)
+                                 smem_u32(qx + (c >> 3) * Gm::HALF_Q + swz(t, c & 7))),
+                             "l"(src), "r"(have ? 16u : 0u)
                              : "memory");
+            }
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
         auto hand_over_q = [&]() {
