@@ -383,11 +383,19 @@ prefill_tc05_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap k
                 for (int x = 0; x < kQTiles && ok; ++x) {
                     if (j >= nkt_of(x)) continue;
                     // the first half of P_x(j) goes to the tensor cores while the
-                    // softmax computes the second
+                    // softmax computes the second.  Usually the softmax has posted
+                    // both halves before this warp gets here; a completed second
+                    // half implies the first (each softmax warp arrives on the
+                    // first half before the second), so one test covers both
+                    bool both = false;
+                    if (lane == 0) both = mbar_test_wait(smem_u32(&p_half[x * 2 + 1]), n[x] & 1);
+                    both = __shfl_sync(0xffffffffu, both, 0);
                     for (int hh = 0; hh < 2 && ok; ++hh) {
-                        if (lane == 0) wait(&p_half[x * 2 + hh], n[x] & 1);
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (!ok) break;
+                        if (!both) {
+                            if (lane == 0) wait(&p_half[x * 2 + hh], n[x] & 1);
+                            ok = __shfl_sync(0xffffffffu, ok, 0);
+                            if (!ok) break;
+                        }
                         tmem_fence_after();
                         issue_pv_half(x, kt, hh, j == 0);
                     }
