@@ -433,8 +433,9 @@ int decode_wide(const char* fn, DecodeParams& p, int kv_dtype, const void* k_cac
     CUtensorMap kmap, vmap;
     const uint64_t rows = (uint64_t)p.num_blocks * p.num_kv_heads * p.block_size;
     const int box_rows = p.block_size < 16 ? p.block_size : 16;
-    // K in 64-column boxes, V in boxes of both halves (its P V layout)
-    int rc = tensor_map(k_cache, rows, p.head_dim, box_rows, kv_dtype, &kmap);
+    // K in boxes of both halves by 8-row groups (its S MMA layout), V in boxes
+    // of both halves (its P V layout)
+    int rc = tensor_map(k_cache, rows, p.head_dim, box_rows, kv_dtype, &kmap, 2);
     if (rc == PKV_OK) rc = tensor_map(v_cache, rows, p.head_dim, box_rows, kv_dtype, &vmap, 1);
     if (rc != PKV_OK) return rc;
     const long long items = (long long)p.num_seqs * p.num_kv_heads * p.head_slices;

@@ -104,7 +104,9 @@ struct W5 {
     static constexpr int Q_BYTES = 2 * HALF_Q;
     static constexpr int P_ATOM = kTok * 128;        // a head half's P^T: [token][high | low]
     static constexpr int P_BYTES = HALVES * P_ATOM;
-    static constexpr int HALF_KV = kTok * 128;       // K: [half][token][128 B]
+    // K: [8-token group][half][token][128 B], a group's halves side by side
+    // (2048 bytes a group); V: see V_GROUP
+    static constexpr int HALF_KV = kTok * 128;
     static constexpr int SLOT_BYTES = 2 * HALF_KV;
     // V: per 16-token group (4 KB), both halves of each box from one copy:
     // [half][16 rows][128 B], or at block size 8 [8-row box][half][8 rows][128 B]
@@ -504,9 +506,9 @@ decode_tc05_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kma
                                              : (id * p.num_kv_heads + g) * B + (IDS > 1 ? 0 : tok % B);
                     const uint32_t slot = smem_u32(smem + W::SLOT_OFF + sl * W::SLOT_BYTES);
                     if (kv == 0) {
-                        const uint32_t dst = slot + bx * W::ROWS * 128;
-                        tma_load_2d(dst, &kmap, 0, row, bar);
-                        tma_load_2d(dst + W::HALF_KV, &kmap, 64, row, bar);
+                        // one copy brings the box's rows of both column halves
+                        const uint32_t dst = slot + bx * W::ROWS * 256;
+                        tma_load_4d(dst, &kmap, 0, 0, 0, row / 8, bar);
                     } else {
                         // box bx = 16-token group bx / IDS, 8-row box bx % IDS
                         const uint32_t dst = slot + (bx / IDS) * W::V_GROUP + (bx % IDS) * 2048;
@@ -531,7 +533,7 @@ decode_tc05_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kma
         // descriptors of Q buffer 0, P buffer 0 and ring slot 0; every
         // operand is one of these moved by a constant or per-buffer offset
         const uint64_t q_desc = smem_desc(smem_u32(smem), 16, 1024);
-        const uint64_t k_desc = smem_desc(slot_base, 16, 1024);
+        const uint64_t k_desc = smem_desc(slot_base, 16, 2048);
         const uint64_t v_desc = smem_desc(slot_base, W::V_LBO, W::V_SBO);
         // P^T: MN-major, one 128-byte atom (64 columns) per head half
         const uint64_t p_desc = smem_desc(smem_u32(smem + W::P_OFF), W::P_ATOM, 1024);
@@ -575,7 +577,7 @@ decode_tc05_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kma
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
-                    umma(d, desc_add(kd, (kk >> 2) * W::HALF_KV + (kk & 3) * 32),
+                    umma(d, desc_add(kd, (kk >> 2) * 1024 + (kk & 3) * 32),
                          desc_add(qd, (kk >> 2) * W::HALF_Q + (kk & 3) * 32), id_s, kk > 0);
                 umma_commit(smem_u32(&s_full[kt & 1]));
             }
