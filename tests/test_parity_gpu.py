@@ -747,6 +747,45 @@ def test_prefill_nan_poison_and_bad_block(kernel):
     assert max_err(out_bad[:70], ref[:70]) <= TOL16  # the healthy sequence is unaffected
 
 
+@pytest.mark.parametrize("kernel", PREFILL_KERNELS)
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_prefill_bad_block_keys_are_masked_exactly(B, kernel):
+    # A table entry out of range: the kernel flags it, masks that block's keys
+    # and attends to the rest.  Each expected row comes from the oracle's
+    # partition form: the runs of visible keys before and after the bad block,
+    # merged by their log-sum-exp.
+    Hq, Hkv, D, L, qn = 8, 2, 128, 200, 150
+    w = Workload(0, "pb", "bf16", Hq, Hkv, D, B, 1, "fixed")
+    case = make_decode_case(w, seed=41 + B, lengths=[L])
+    qs = torch.tensor([0, qn], dtype=torch.int32)
+    q = torch.randn(qn, Hq, D, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    bad = 2  # logical block 2: keys [2B, 3B)
+    bt = case.block_tables.clone()
+    bt[0, bad] = case.num_blocks + 7
+    pkv.device_status(reset=True)
+    out = gpu_prefill(q, case.k_cache.to(DEV), case.v_cache.to(DEV), bt, case.context_lens, qs,
+                      w.scale, B, Hkv, kernel=kernel)
+    assert pkv.device_status() & 1
+    pkv.device_status(reset=True)
+    K = oracle.gather_sequence(case.k_cache, case.block_tables[0], L)
+    V = oracle.gather_sequence(case.v_cache, case.block_tables[0], L)
+    Q = oracle.widen(q)
+    got = out.double().cpu().numpy()
+    lo, hi = bad * B, (bad + 1) * B
+    worst = 0.0
+    for t in range(qn):
+        pos = L - qn + t
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            parts = []
+            for a, b in ((0, min(lo, pos + 1)), (hi, pos + 1)):
+                if b > a:
+                    parts += oracle.decode_partitions(Q[t, h], K[a:b, g], V[a:b, g], w.scale,
+                                                      b - a)
+            worst = max(worst, float(np.abs(got[t, h] - oracle.lse_combine(parts)).max()))
+    assert worst <= TOL16
+
+
 def test_nan_poison_and_physical_permutation():
     # Same logical data paged twice with different physical ids: same output.
     w = Workload(0, "perm", "f16", 16, 4, 128, 16, 4, "fixed")
