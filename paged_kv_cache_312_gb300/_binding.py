@@ -460,6 +460,16 @@ class BlockAllocator:
         int32 [n], holding the batch's tables and lengths from before the
         step (in any host memory, e.g. a view of a pinned staging buffer).
         Returns the number of copy-on-write pairs written."""
+        return self.prepare_step_append_tables(seqs, slots, pairs, tables, lens)()
+
+    def prepare_step_append_tables(self, seqs, slots, pairs, tables, lens):
+        """Checks the buffers of step_append_tables once and returns step(),
+        which runs pkv_step_append_tables on them and returns the number of
+        copy-on-write pairs.  Between calls the buffers' contents may change
+        (the batch's sequence ids, tables the caller patched); their storage,
+        shapes and dtypes must not.  Made for a serving loop that reuses its
+        staging buffers every step: a call is then the C function and one
+        ctypes call.  step keeps the allocator and the buffers alive."""
         n = seqs.numel()
         for t, dt, name in ((seqs, torch.int64, "seqs"), (slots, torch.int64, "slots"),
                             (pairs, torch.int64, "pairs"), (tables, torch.int32, "tables"),
@@ -470,12 +480,19 @@ class BlockAllocator:
                 lens.numel() != n or tables.dim() != 2:
             raise ValueError("step_append_tables: bad output shapes")
         npairs = ctypes.c_int(0)
-        _check(lib().pkv_step_append_tables(
-            self._h, ctypes.c_void_p(seqs.data_ptr()), n, ctypes.c_void_p(slots.data_ptr()),
-            ctypes.c_void_p(pairs.data_ptr()), ctypes.byref(npairs),
-            ctypes.c_void_p(tables.data_ptr()), tables.shape[1],
-            ctypes.c_void_p(lens.data_ptr())), "pkv_step_append_tables")
-        return npairs.value
+        fn = lib().pkv_step_append_tables
+        args = (self._h, ctypes.c_void_p(seqs.data_ptr()), n, ctypes.c_void_p(slots.data_ptr()),
+                ctypes.c_void_p(pairs.data_ptr()), ctypes.byref(npairs),
+                ctypes.c_void_p(tables.data_ptr()), tables.shape[1],
+                ctypes.c_void_p(lens.data_ptr()))
+
+        def step():
+            rc = fn(*args)
+            if rc:
+                _check(rc, "pkv_step_append_tables")
+            return npairs.value
+        step.buffers = (self, seqs, slots, pairs, tables, lens)
+        return step
 
     def fork(self, parent, child):
         _check(lib().pkv_seq_fork(self._h, int(parent), int(child)), "pkv_seq_fork")

@@ -74,8 +74,21 @@ struct pkv_allocator {
     struct Seq {
         std::vector<int32_t> table;
         int64_t len = 0;
+        // a decode step's plan (plan_step): valid while mark == the step's stamp
+        uint64_t mark = 0;
+        int64_t sim_len = 0, sim_blocks = 0;
+        int32_t sim_last = -1;  // -1: a block taken in this step (private)
     };
     std::unordered_map<int64_t, Seq> seqs;
+
+    // ---- scratch of a decode step, kept across steps so a step allocates
+    // nothing: the stamp of the current plan, the sequences of the step, and
+    // per block the count drops earlier appends of the step make (valid
+    // where dref_mark == stamp)
+    uint64_t stamp = 0;
+    std::vector<Seq*> step_seqs;
+    std::vector<int32_t> dref;
+    std::vector<uint64_t> dref_mark;
 
     // ---- prefix cache: registered full blocks
     std::unordered_map<uint64_t, int32_t> index;  // key -> block
@@ -176,6 +189,8 @@ int pkv_alloc_create(int num_blocks, int block_size, const int32_t* free_order,
     a->parent_key.assign(num_blocks, 0);
     a->tokens.assign((size_t)num_blocks * block_size, 0);
     a->cached_pos.resize(num_blocks);
+    a->dref.assign(num_blocks, 0);
+    a->dref_mark.assign(num_blocks, 0);
     a->free_stack.resize(num_blocks);
     std::vector<char> seen(num_blocks, 0);
     for (int i = 0; i < num_blocks; ++i) {
@@ -235,57 +250,54 @@ namespace {
 
 // Blocks one decode step over seqs[0..n) must take (a fresh block for a token
 // that starts one, a copy target for a write into a shared partial block),
-// found without changing anything: the walk tracks, per sequence, its length
-// and whether its last block is already private, and per shared block the
-// count drops earlier appends of the same step make, so that a block shared
-// by two sequences of the step is copied once and its last holder writes in
-// place.  Also checks every sequence exists and (tables != 0) that no table
-// grows past max_blocks.
-int plan_step(pkv_allocator* a, const int64_t* seqs, int n, const char* fn,
-              std::vector<pkv_allocator::Seq*>& ptr, int max_blocks, int64_t* need_out)
+// found without changing the allocator's state (only its step scratch): the
+// walk tracks, per sequence, its length and whether its last block is
+// already private, and per shared block the count drops earlier appends of
+// the same step make, so that a block shared by two sequences of the step is
+// copied once and its last holder writes in place.  Also checks every
+// sequence exists and (max_blocks > 0) that no table grows past max_blocks.
+// Leaves the step's sequences in a->step_seqs.
+int plan_step(pkv_allocator* a, const int64_t* seqs, int n, const char* fn, int max_blocks,
+              int64_t* need_out)
 {
-    struct Sim {
-        int64_t len;
-        int64_t blocks;
-        int32_t last;  // -1: a block taken in this step (private to the sequence)
-    };
-    ptr.resize(n);
-    std::unordered_map<int64_t, Sim> sim;
-    sim.reserve((size_t)n * 2);
-    std::unordered_map<int32_t, int> dref;
+    const uint64_t stamp = ++a->stamp;
+    a->step_seqs.resize(n);
     int64_t need = 0;
     for (int i = 0; i < n; ++i) {
         auto it = a->seqs.find(seqs[i]);
         if (it == a->seqs.end())
             return pkv_fail(PKV_ERR_STATE, "%s: unknown sequence %lld", fn, (long long)seqs[i]);
-        ptr[i] = &it->second;
-        auto f = sim.find(seqs[i]);
-        if (f != sim.end() && max_blocks > 0)  // one table row per sequence
+        pkv_allocator::Seq& s = it->second;
+        a->step_seqs[i] = &s;
+        if (s.mark == stamp && max_blocks > 0)  // one table row per sequence
             return pkv_fail(PKV_ERR_STATE, "%s: sequence %lld listed twice", fn,
                             (long long)seqs[i]);
-        if (f == sim.end()) {
-            const pkv_allocator::Seq& q = it->second;
-            f = sim.emplace(seqs[i], Sim{q.len, (int64_t)q.table.size(),
-                                         q.table.empty() ? -1 : q.table.back()})
-                    .first;
+        if (s.mark != stamp) {
+            s.mark = stamp;
+            s.sim_len = s.len;
+            s.sim_blocks = (int64_t)s.table.size();
+            s.sim_last = s.table.empty() ? -1 : s.table.back();
         }
-        Sim& s = f->second;
-        if (s.len % a->block_size == 0) {
-            s.last = -1;
-            s.blocks += 1;
+        if (s.sim_len % a->block_size == 0) {
+            s.sim_last = -1;
+            s.sim_blocks += 1;
             need += 1;
-        } else if (s.last >= 0 && a->ref[s.last] > 1) {
-            int& d = dref[s.last];
-            if (a->ref[s.last] + d > 1) {
-                d -= 1;
-                s.last = -1;
+        } else if (s.sim_last >= 0 && a->ref[s.sim_last] > 1) {
+            const int32_t b = s.sim_last;
+            if (a->dref_mark[b] != stamp) {
+                a->dref_mark[b] = stamp;
+                a->dref[b] = 0;
+            }
+            if (a->ref[b] + a->dref[b] > 1) {
+                a->dref[b] -= 1;
+                s.sim_last = -1;
                 need += 1;
             }
         }
-        s.len += 1;
-        if (max_blocks > 0 && s.blocks > max_blocks)
+        s.sim_len += 1;
+        if (max_blocks > 0 && s.sim_blocks > max_blocks)
             return pkv_fail(PKV_ERR_SHAPE, "%s: sequence %lld would need %lld table entries, %d "
-                            "fit", fn, (long long)seqs[i], (long long)s.blocks, max_blocks);
+                            "fit", fn, (long long)seqs[i], (long long)s.sim_blocks, max_blocks);
     }
     if (need > (int64_t)a->available())
         return pkv_fail(PKV_ERR_OOM, "%s: %lld blocks needed, %zu free", fn, (long long)need,
@@ -305,14 +317,13 @@ int pkv_step_append(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots
         return pkv_fail(PKV_ERR_NULL, "pkv_step_append: NULL argument");
     if (n < 0) return pkv_fail(PKV_ERR_SHAPE, "pkv_step_append: n < 0");
     // plan first (all or nothing), then commit
-    std::vector<pkv_allocator::Seq*> ptr;
     int64_t need = 0;
-    const int rc = plan_step(a, seqs, n, "pkv_step_append", ptr, 0, &need);
+    const int rc = plan_step(a, seqs, n, "pkv_step_append", 0, &need);
     if (rc != PKV_OK) return rc;
     int np = 0;
     for (int i = 0; i < n; ++i) {
         int64_t src, dst;
-        a->append_one(*ptr[i], &slots[i], &src, &dst);
+        a->append_one(*a->step_seqs[i], &slots[i], &src, &dst);
         if (src >= 0) {
             cow_pairs[2 * np] = src;
             cow_pairs[2 * np + 1] = dst;
@@ -332,13 +343,12 @@ int pkv_step_append_tables(pkv_allocator* a, const int64_t* seqs, int n, int64_t
         return pkv_fail(PKV_ERR_NULL, "%s: NULL argument", fn);
     if (n < 0 || max_blocks <= 0) return pkv_fail(PKV_ERR_SHAPE, "%s: n %d, max_blocks %d", fn, n,
                                                   max_blocks);
-    std::vector<pkv_allocator::Seq*> ptr;
     int64_t need = 0;
-    const int rc = plan_step(a, seqs, n, fn, ptr, max_blocks, &need);
+    const int rc = plan_step(a, seqs, n, fn, max_blocks, &need);
     if (rc != PKV_OK) return rc;
     int np = 0;
     for (int i = 0; i < n; ++i) {
-        pkv_allocator::Seq& s = *ptr[i];
+        pkv_allocator::Seq& s = *a->step_seqs[i];
         int64_t src, dst;
         a->append_one(s, &slots[i], &src, &dst);
         if (src >= 0) {

@@ -455,6 +455,51 @@ def test_step_append_tables_with_forks_and_errors():
     assert torch.equal(tables, snap[3]) and torch.equal(lens, snap[4])
 
 
+def test_prepared_step_append_tables_matches_the_reference_across_steps():
+    # One prepared step, reused over many steps while the batch's contents
+    # change in place (beams forked, sequence ids rewritten), gives the
+    # reference's slots, copy-on-write pairs, tables and lengths; it keeps
+    # its allocator alive.
+    from workloads import dense_tables
+    rnd = random.Random(11)
+    NB, B, W, maxb = 400, 4, 6, 40
+    order = list(np.random.default_rng(11).permutation(NB))
+    cpp, ref = pkv.BlockAllocator(NB, B, free_order=order), BlockManager(NB, B, free_order=order)
+    for s in range(W):
+        cpp.add(s, 5 + s)
+        ref.add(s, 5 + s)
+    batch, nid = list(range(W)), W
+    seqs = torch.tensor(batch, dtype=torch.int64)
+    tables, lens = cpp.dense_tables(batch, maxb)
+    slots = torch.empty(W, dtype=torch.int64)
+    pairs = torch.empty((W, 2), dtype=torch.int64)
+    step = cpp.prepare_step_append_tables(seqs, slots, pairs, tables, lens)
+    del cpp  # the prepared step holds the allocator
+    a = step.buffers[0]
+    for _ in range(4):
+        for _ in range(rnd.randint(1, 5)):
+            ns = step()
+            r_slots, r_pairs = ref.step_append(batch)
+            assert slots.tolist() == r_slots
+            assert [tuple(p) for p in pairs[:ns].tolist()] == r_pairs
+            t_ref, l_ref = dense_tables(ref, batch, maxb)
+            assert torch.equal(tables, t_ref) and torch.equal(lens, l_ref)
+        # re-select beams: new ids into the same buffers, tables rewritten in place
+        parent = [rnd.randrange(W) for _ in range(W)]
+        new = list(range(nid, nid + W))
+        for b in range(W):
+            a.fork(batch[parent[b]], new[b])
+            ref.fork(batch[parent[b]], new[b])
+        for s in batch:
+            a.free(s)
+            ref.free_seq(s)
+        batch, nid = new, nid + W
+        seqs.copy_(torch.tensor(batch, dtype=torch.int64))
+        t_new, l_new = a.dense_tables(batch, maxb)
+        tables.copy_(t_new)
+        lens.copy_(l_new)
+
+
 def test_beam_fork_cow_pairs():
     # A width-4 beam over one partial block: three children copy, the last
     # holder writes in place.
