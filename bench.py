@@ -851,11 +851,16 @@ def host_allocator_timing(st, pkv, grouped=False, steps=256):
         slots = torch.empty(S, dtype=torch.int64)
         pairs = torch.empty((S, 2), dtype=torch.int64)
         step = a.prepare_step_append_tables(seqs, slots, pairs, tables, tl)
+        shared = torch.zeros(gstart.numel() - 1, dtype=torch.int32)
+        group_step = pkv.prepare_group_shared_tokens(tables, tl, gstart, B, shared)
         t0 = time.perf_counter()
         for _ in range(steps):
             if form == "prepared":
                 step()
-            elif form == "patched":
+                if grouped:
+                    group_step()
+                continue
+            if form == "patched":
                 a.step_append_tables(seqs, slots, pairs, tables, tl)
             else:
                 a.step_append(range(S))

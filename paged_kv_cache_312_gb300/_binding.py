@@ -270,16 +270,37 @@ def group_shared_tokens(block_tables, context_lens, group_start, block_size):
     bt = block_tables.to(torch.int32).contiguous()
     cl = context_lens.to(torch.int32).contiguous()
     gs = group_start.to(torch.int32).contiguous()
-    if bt.is_cuda or cl.is_cuda or gs.is_cuda:
-        raise ValueError("group_shared_tokens takes host tensors")
-    G = gs.shape[0] - 1
-    out = torch.zeros(max(G, 0), dtype=torch.int32)
-    rc = lib().pkv_group_shared_tokens(
-        ctypes.c_void_p(bt.data_ptr()), ctypes.c_void_p(cl.data_ptr()),
-        ctypes.c_void_p(gs.data_ptr()), G, bt.shape[0], bt.shape[1], int(block_size),
-        ctypes.c_void_p(out.data_ptr()))
-    _check(rc, "pkv_group_shared_tokens")
+    out = torch.zeros(max(gs.shape[0] - 1, 0), dtype=torch.int32)
+    prepare_group_shared_tokens(bt, cl, gs, block_size, out)()
     return out
+
+
+def prepare_group_shared_tokens(block_tables, context_lens, group_start, block_size, out):
+    """group_shared_tokens on fixed buffers: checks them once (contiguous host
+    int32: tables [S, max_blocks], lengths [S], group starts [G + 1], out [G])
+    and returns step(), which writes each group's shared positions into out
+    and returns it.  The buffers' contents may change between calls, not
+    their storage or shapes; step keeps them alive."""
+    bufs = (block_tables, context_lens, group_start, out)
+    for t, name in zip(bufs, ("block_tables", "context_lens", "group_start", "out")):
+        if t.dtype != torch.int32 or t.is_cuda or not t.is_contiguous():
+            raise ValueError("group_shared_tokens: %s must be a contiguous host int32 tensor"
+                             % name)
+    G = group_start.shape[0] - 1
+    if block_tables.dim() != 2 or out.numel() < max(G, 0):
+        raise ValueError("group_shared_tokens: bad shapes")
+    fn = lib().pkv_group_shared_tokens
+    args = (ctypes.c_void_p(block_tables.data_ptr()), ctypes.c_void_p(context_lens.data_ptr()),
+            ctypes.c_void_p(group_start.data_ptr()), G, block_tables.shape[0],
+            block_tables.shape[1], int(block_size), ctypes.c_void_p(out.data_ptr()))
+
+    def step():
+        rc = fn(*args)
+        if rc:
+            _check(rc, "pkv_group_shared_tokens")
+        return out
+    step.buffers = bufs
+    return step
 
 
 def paged_prefill_attention(out, q, k_cache, v_cache, block_tables, context_lens, query_start,

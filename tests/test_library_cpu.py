@@ -573,6 +573,28 @@ def test_group_shared_tokens_against_a_reference():
         got = pkv.group_shared_tokens(torch.from_numpy(bt), torch.from_numpy(cl),
                                       torch.tensor(gs, dtype=torch.int32), B)
         assert got.tolist() == _shared_reference(bt, cl, gs, B), (bt, cl, gs, B)
+    # the prepared form, reused while the tables change in place, agrees
+    rng = np.random.default_rng(6)
+    S, mb, B = 8, 6, 16
+    bt_t = torch.zeros((S, mb), dtype=torch.int32)
+    cl_t = torch.zeros(S, dtype=torch.int32)
+    gs_t = torch.tensor([0, 3, 5, 8], dtype=torch.int32)
+    out_t = torch.full((3,), -1, dtype=torch.int32)
+    step = pkv.prepare_group_shared_tokens(bt_t, cl_t, gs_t, B, out_t)
+    for trial in range(50):
+        bt = rng.integers(-1, 6, size=(S, mb)).astype(np.int32)
+        gs = gs_t.tolist()
+        for i in range(len(gs) - 1):
+            k = int(rng.integers(0, mb + 1))
+            for s in range(gs[i] + 1, gs[i + 1]):
+                bt[s, :k] = bt[gs[i], :k]
+        cl = rng.integers(0, mb * B + 1, size=S).astype(np.int32)
+        bt_t.copy_(torch.from_numpy(bt))
+        cl_t.copy_(torch.from_numpy(cl))
+        assert step() is out_t
+        assert out_t.tolist() == _shared_reference(bt, cl, gs, B)
+    with pytest.raises(ValueError):  # buffers must be int32
+        pkv.prepare_group_shared_tokens(bt_t.to(torch.int64), cl_t, gs_t, B, out_t)
     with pytest.raises(pkv.PkvError):  # a group past the last sequence
         pkv.group_shared_tokens(torch.zeros(2, 3, dtype=torch.int32),
                                 torch.ones(2, dtype=torch.int32),
