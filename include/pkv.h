@@ -512,10 +512,11 @@ int pkv_step_append(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots
  * dense read-back each step.  Entries past a sequence's table are left as
  * they are.  All or nothing: PKV_ERR_SHAPE (nothing changed) if a table would
  * grow past max_blocks, PKV_ERR_STATE if a sequence is listed twice;
- * otherwise as pkv_step_append.  Neither step call allocates host memory
- * unless the step takes more sequences than any step before it (the plan
- * lives in the allocator's per-sequence and per-block scratch); the time is
- * a hash lookup and a few comparisons per sequence. */
+ * otherwise as pkv_step_append.  The step's plan lives in the allocator's
+ * per-sequence and per-block scratch: a step call allocates host memory only
+ * when it takes more sequences than any step before it, or when a sequence's
+ * block list outgrows its capacity (amortised, once per doubling).  The time
+ * is a hash lookup and a few comparisons per sequence. */
 int pkv_step_append_tables(pkv_allocator* a, const int64_t* seqs, int n, int64_t* slots,
                            int64_t* cow_pairs, int* num_pairs, int32_t* tables, int max_blocks,
                            int32_t* lens);
