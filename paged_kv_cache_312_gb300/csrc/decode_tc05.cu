@@ -310,7 +310,7 @@ decode_tc05_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kma
             atomicOr(p.status, PKV_STATUS_TIMEOUT);
         }
     };
-    // lane 0 waits, the warp follows with its verdict
+    // lane 0 waits, the warp follows with its result
     auto warp_wait = [&](uint64_t* bar, int parity) {
         if (lane == 0) wait(bar, parity);
         ok = __shfl_sync(kFull, ok, 0);
